@@ -1,0 +1,85 @@
+"""Build libfa.so (the CUDA library behind include/fa.h) in-tree for sm_103a.
+
+Each translation unit is compiled by nvcc in parallel, then linked into
+``exact_attention_26_gb300/_lib/libfa.so`` against the shared CUDA runtime.
+"""
+from __future__ import annotations
+
+import concurrent.futures as cf
+import os
+import shutil
+import subprocess
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(PKG)
+CSRC = os.path.join(PKG, "csrc")
+INCLUDE = os.path.join(ROOT, "include")
+OUT_DIR = os.path.join(PKG, "_lib")
+LIB = os.path.join(OUT_DIR, "libfa.so")
+SOURCES = ["fa_api.cu", "fa_fwd.cu", "fa_bwd.cu"]
+ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
+
+
+def _nvcc() -> str:
+    cand = shutil.which("nvcc") or "/usr/local/cuda/bin/nvcc"
+    if not os.path.exists(cand):
+        raise RuntimeError("nvcc not found")
+    return cand
+
+
+def _cuda_lib_dir(nvcc: str) -> str:
+    return os.path.join(os.path.dirname(os.path.dirname(nvcc)), "lib64")
+
+
+def compile_flags(extra=()):
+    return [*ARCH, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
+            "-I", INCLUDE, "-I", CSRC, *extra]
+
+
+def build(verbose: bool = False, extra_flags=(), ptxas_info: bool = False) -> str:
+    nvcc = _nvcc()
+    obj_dir = os.path.join(OUT_DIR, "obj")
+    os.makedirs(obj_dir, exist_ok=True)
+    flags = compile_flags(extra_flags)
+    if ptxas_info:
+        flags += ["-Xptxas", "-v"]
+
+    def one(src):
+        obj = os.path.join(obj_dir, src.replace(".cu", ".o"))
+        cmd = [nvcc, *flags, "-c", os.path.join(CSRC, src), "-o", obj]
+        res = subprocess.run(cmd, capture_output=True, text=True)
+        if res.returncode != 0:
+            raise RuntimeError(f"nvcc failed for {src}:\n{' '.join(cmd)}\n{res.stderr}")
+        return obj, res.stderr
+
+    with cf.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
+        results = list(ex.map(one, SOURCES))
+    if verbose or ptxas_info:
+        for (_, log), src in zip(results, SOURCES):
+            if log.strip():
+                print(f"--- {src}\n{log}")
+    tmp = LIB + f".tmp{os.getpid()}"
+    libdir = _cuda_lib_dir(nvcc)
+    cmd = [nvcc, *ARCH, "-shared", "-cudart", "shared", "-o", tmp, *[o for o, _ in results],
+           "-Xlinker", f"-rpath,{libdir}"]
+    res = subprocess.run(cmd, capture_output=True, text=True)
+    if res.returncode != 0:
+        raise RuntimeError(f"link failed:\n{' '.join(cmd)}\n{res.stderr}")
+    os.replace(tmp, LIB)
+    return LIB
+
+
+def needs_build() -> bool:
+    if not os.path.exists(LIB):
+        return True
+    t = os.path.getmtime(LIB)
+    for d in (CSRC, INCLUDE):
+        for f in os.listdir(d):
+            if os.path.getmtime(os.path.join(d, f)) > t:
+                return True
+    return False
+
+
+if __name__ == "__main__":
+    import sys
+    print(build(verbose=True, ptxas_info="-v" in sys.argv))

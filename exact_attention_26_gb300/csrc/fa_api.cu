@@ -1,0 +1,217 @@
+// Host side of the C ABI declared in include/fa.h: argument validation, the
+// per-device cache, TMA tensor-map encoding, and dispatch to the kernels.
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "fa_internal.h"
+
+namespace fa {
+namespace {
+
+// Device status record written by the kernels' bounded waits: [0] error code,
+// [1] wait site of the first error.  One copy per device (module global).
+__device__ int g_status[2];
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceCache {
+    bool ready = false;
+    int num_sms = 0;
+    int *status = nullptr;
+};
+
+std::mutex g_mutex;
+DeviceCache g_devices[kMaxDevices];
+
+int current_device(DeviceCache **out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FA_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    DeviceCache &dc = g_devices[dev];
+    if (!dc.ready) {
+        int sms = 0;
+        void *status = nullptr;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return FA_ERR_CUDA;
+        if (cudaGetSymbolAddress(&status, g_status) != cudaSuccess) return FA_ERR_CUDA;
+        dc.num_sms = sms;
+        dc.status = static_cast<int *>(status);
+        dc.ready = true;
+    }
+    *out = &dc;
+    return FA_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_tiled() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// 3-D map over a contiguous bf16 [BH][N][d] tensor: x = column within the head
+// dimension, y = row, z = (batch, head).  Boxes are 64 columns (128 bytes, one
+// swizzle span) by `box_rows` rows; rows past N read as zeros.
+int make_bhnd_map(CUtensorMap *map, const void *ptr, int BH, int N, int d, int box_rows) {
+    auto enc = encode_tiled();
+    if (!enc) return FA_ERR_CUDA;
+    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
+    cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)N * (cuuint64_t)d * 2};
+    cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
+    cuuint32_t elem_strides[3] = {1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims,
+                     strides, box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_sizes(int B, int H, int N, int d, bool fwd) {
+    if (B < 1 || H < 1 || N < 1) return FA_ERR_INVALID_ARG;
+    if ((long long)B * H * N >= (1LL << 31)) return FA_ERR_INVALID_ARG;
+    if (fwd) {
+        if (d != 64 && d != 128 && d != 256) return FA_ERR_UNSUPPORTED;
+    } else {
+        if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+    }
+    return FA_OK;
+}
+
+int check_scale(float scale) {
+    return (std::isfinite(scale) && scale > 0.f) ? FA_OK : FA_ERR_INVALID_ARG;
+}
+
+constexpr float kLog2e = 1.4426950408889634074f;
+
+size_t round_up(size_t x, size_t m) { return (x + m - 1) / m * m; }
+
+}  // namespace
+
+// Keys per K/V tile of the forward kernel for head dimension d.
+int fwd_block_n(int d) { return d == 256 ? 64 : 128; }
+
+}  // namespace fa
+
+using namespace fa;
+
+extern "C" int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B,
+                      int H, int N, int d, int causal, float scale, void *stream) {
+    if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
+    int rc = check_sizes(B, H, N, d, true);
+    if (rc != FA_OK) return rc;
+    if ((rc = check_scale(scale)) != FA_OK) return rc;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+        return FA_ERR_MISALIGNED;
+
+    DeviceCache *dc = nullptr;
+    if ((rc = current_device(&dc)) != FA_OK) return rc;
+    FwdParams p{};
+    const int BH = B * H;
+    if ((rc = make_bhnd_map(&p.tm_q, q, BH, N, d, 128)) != FA_OK) return rc;
+    if ((rc = make_bhnd_map(&p.tm_k, k, BH, N, d, fwd_block_n(d))) != FA_OK) return rc;
+    if ((rc = make_bhnd_map(&p.tm_v, v, BH, N, d, fwd_block_n(d))) != FA_OK) return rc;
+    p.o = o;
+    p.lse = lse;
+    p.N = N;
+    p.BH = BH;
+    p.d = d;
+    p.causal = causal ? 1 : 0;
+    p.scale_log2 = scale * kLog2e;
+    p.status = dc->status;
+    p.limit_ns = kWaitLimitNs;
+    p.num_sms = dc->num_sms;
+    return launch_fwd(p, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" size_t fa_bwd_workspace_bytes(int B, int H, int N, int d) {
+    if (check_sizes(B, H, N, d, false) != FA_OK) return 0;
+    const size_t npad = round_up((size_t)N, kBwdPad);
+    // delta[BH][Npad] and lse2[BH][Npad], fp32 each
+    return 2 * (size_t)B * (size_t)H * npad * sizeof(float);
+}
+
+extern "C" int fa_bwd(const void *q, const void *k, const void *v, const void *o,
+                      const float *lse, const void *dout, float *dq, float *dk, float *dv, int B,
+                      int H, int N, int d, int causal, float scale, void *workspace,
+                      size_t workspace_bytes, void *stream) {
+    if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
+    int rc = check_sizes(B, H, N, d, false);
+    if (rc != FA_OK) return rc;
+    if ((rc = check_scale(scale)) != FA_OK) return rc;
+    const size_t need = fa_bwd_workspace_bytes(B, H, N, d);
+    if (!workspace || workspace_bytes < need) return FA_ERR_WORKSPACE;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
+        !aligned16(dout) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv) ||
+        !aligned16(workspace))
+        return FA_ERR_MISALIGNED;
+
+    DeviceCache *dc = nullptr;
+    if ((rc = current_device(&dc)) != FA_OK) return rc;
+    BwdParams p{};
+    const int BH = B * H;
+    const int npad = (int)round_up((size_t)N, kBwdPad);
+    const int q_rows = (d == 128) ? 64 : 128;  // query rows per backward q-block
+    if ((rc = make_bhnd_map(&p.tm_q, q, BH, N, d, q_rows)) != FA_OK) return rc;
+    if ((rc = make_bhnd_map(&p.tm_do, dout, BH, N, d, q_rows)) != FA_OK) return rc;
+    if ((rc = make_bhnd_map(&p.tm_k, k, BH, N, d, 128)) != FA_OK) return rc;
+    if ((rc = make_bhnd_map(&p.tm_v, v, BH, N, d, 128)) != FA_OK) return rc;
+    p.o = o;
+    p.dout = dout;
+    p.lse = lse;
+    p.dq = dq;
+    p.dk = dk;
+    p.dv = dv;
+    p.ws_delta = static_cast<float *>(workspace);
+    p.ws_lse2 = p.ws_delta + (size_t)BH * (size_t)npad;
+    p.N = N;
+    p.Npad = npad;
+    p.BH = BH;
+    p.d = d;
+    p.causal = causal ? 1 : 0;
+    p.scale = scale;
+    p.scale_log2 = scale * kLog2e;
+    p.status = dc->status;
+    p.limit_ns = kWaitLimitNs;
+    p.num_sms = dc->num_sms;
+    return launch_bwd(p, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" const char *fa_status_string(int status) {
+    switch (status) {
+        case FA_OK: return "FA_OK";
+        case FA_ERR_INVALID_ARG: return "FA_ERR_INVALID_ARG: invalid argument";
+        case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED: head dimension not supported";
+        case FA_ERR_MISALIGNED: return "FA_ERR_MISALIGNED: pointer not 16-byte aligned";
+        case FA_ERR_CUDA: return "FA_ERR_CUDA: CUDA runtime or driver call failed";
+        case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT: a bounded in-kernel wait ran out";
+        case FA_ERR_WORKSPACE: return "FA_ERR_WORKSPACE: workspace missing or too small";
+        default: return "unknown fa_status";
+    }
+}
+
+extern "C" int fa_device_status(void *stream) {
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return FA_ERR_CUDA;
+    DeviceCache *dc = nullptr;
+    if (current_device(&dc) != FA_OK) return FA_ERR_CUDA;
+    int rec[2] = {0, 0};
+    if (cudaMemcpy(rec, dc->status, sizeof(rec), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return FA_ERR_CUDA;
+    if (rec[0] != 0) {
+        const int zero[2] = {0, 0};
+        if (cudaMemcpy(dc->status, zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
+            return FA_ERR_CUDA;
+    }
+    return rec[0];
+}

@@ -1,0 +1,68 @@
+// Declarations shared by the host API and the kernel translation units.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "fa.h"
+
+namespace fa {
+
+// Where a bounded wait gave up (second word of the device status record).
+enum WaitSite : int {
+    SITE_NONE = 0,
+    SITE_FWD_LOAD_KV_EMPTY = 1,
+    SITE_FWD_MMA_Q = 2,
+    SITE_FWD_MMA_KV_FULL = 3,
+    SITE_FWD_MMA_P_FULL = 4,
+    SITE_FWD_SOFTMAX_S_FULL = 5,
+    SITE_FWD_EPILOGUE_O_FULL = 6,
+    SITE_FWD_DRAIN = 7,
+    SITE_BWD_LOAD_EMPTY = 11,
+    SITE_BWD_MMA_KV = 12,
+    SITE_BWD_MMA_Q_FULL = 13,
+    SITE_BWD_MMA_DS_FULL = 14,
+    SITE_BWD_MMA_DQ_FREE = 15,
+    SITE_BWD_SOFTMAX_S_FULL = 16,
+    SITE_BWD_DQ_FULL = 17,
+    SITE_BWD_EPILOGUE = 18,
+    SITE_BWD_DRAIN = 19,
+    SITE_SELFTEST = 30,
+};
+
+// Default limit of one in-kernel wait.
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;
+
+struct FwdParams {
+    CUtensorMap tm_q, tm_k, tm_v;  // 3-D maps over [BH][N][d] bf16
+    void *o;                       // bf16 [BH][N][d]
+    float *lse;                    // fp32 [BH][N]
+    int N, BH, d, causal;
+    float scale_log2;              // scale * log2(e)
+    int *status;                   // device status record (2 ints)
+    unsigned long long limit_ns;
+    int num_sms;
+};
+
+struct BwdParams {
+    CUtensorMap tm_q, tm_k, tm_v, tm_do;  // 3-D maps over [BH][N][d] bf16
+    const void *o, *dout;                 // bf16 [BH][N][d]
+    const float *lse;                     // fp32 [BH][N]
+    float *dq, *dk, *dv;                  // fp32 [BH][N][d]
+    float *ws_delta, *ws_lse2;            // workspace, [BH][Npad] each
+    int N, Npad, BH, d, causal;
+    float scale, scale_log2;
+    int *status;
+    unsigned long long limit_ns;
+    int num_sms;
+};
+
+// Query rows per backward q-block and the padding unit of the workspace vectors.
+constexpr int kBwdPad = 128;
+
+int launch_fwd(const FwdParams &p, cudaStream_t stream);
+int launch_bwd(const BwdParams &p, cudaStream_t stream);
+
+}  // namespace fa

@@ -1,0 +1,160 @@
+"""Thin ctypes binding over libfa.so, with the C ABI's names.
+
+Argument marshalling only: every step of the attention computation runs in the
+library's CUDA kernels.  torch supplies device memory and the current stream.
+There is no CPU path; a missing library or a non-CUDA tensor raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+import torch
+
+from . import build as _build
+
+FA_OK = 0
+FA_ERR_INVALID_ARG = 1
+FA_ERR_UNSUPPORTED = 2
+FA_ERR_MISALIGNED = 3
+FA_ERR_CUDA = 4
+FA_ERR_TIMEOUT = 5
+FA_ERR_WORKSPACE = 6
+
+EXPORTED = ("fa_fwd", "fa_bwd", "fa_bwd_workspace_bytes", "fa_status_string", "fa_device_status")
+
+_vp = ctypes.c_void_p
+_int = ctypes.c_int
+_LIB = None
+
+
+class FaError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {fa_status_string(status)} (status {status})")
+
+
+def lib_path() -> str:
+    return _build.LIB
+
+
+def load() -> ctypes.CDLL:
+    """Load libfa.so (raises if it has not been built)."""
+    global _LIB
+    if _LIB is None:
+        path = lib_path()
+        if not os.path.exists(path):
+            raise RuntimeError(f"{path} is missing: build it first (__graft_entry__.build())")
+        lib = ctypes.CDLL(path)
+        lib.fa_fwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _int, _int, _int, _int, _int,
+                               ctypes.c_float, _vp]
+        lib.fa_fwd.restype = _int
+        lib.fa_bwd_workspace_bytes.argtypes = [_int, _int, _int, _int]
+        lib.fa_bwd_workspace_bytes.restype = ctypes.c_size_t
+        lib.fa_bwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _int, _int, _int,
+                               _int, _int, ctypes.c_float, _vp, ctypes.c_size_t, _vp]
+        lib.fa_bwd.restype = _int
+        lib.fa_status_string.argtypes = [_int]
+        lib.fa_status_string.restype = ctypes.c_char_p
+        lib.fa_device_status.argtypes = [_vp]
+        lib.fa_device_status.restype = _int
+        _LIB = lib
+    return _LIB
+
+
+# ------------------------------------------------------------ raw C-ABI calls
+
+def fa_fwd(q, k, v, o, lse, B, H, N, d, causal, scale, stream) -> int:
+    return load().fa_fwd(q, k, v, o, lse, B, H, N, d, int(bool(causal)), scale, stream)
+
+
+def fa_bwd_workspace_bytes(B, H, N, d) -> int:
+    return load().fa_bwd_workspace_bytes(B, H, N, d)
+
+
+def fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, H, N, d, causal, scale, workspace,
+           workspace_bytes, stream) -> int:
+    return load().fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, H, N, d, int(bool(causal)),
+                         scale, workspace, workspace_bytes, stream)
+
+
+def fa_status_string(status: int) -> str:
+    return load().fa_status_string(status).decode()
+
+
+def fa_device_status(stream=None) -> int:
+    return load().fa_device_status(stream)
+
+
+# ------------------------------------------------------------ tensor wrappers
+
+def _check(name, t, dtype, shape=None):
+    if not isinstance(t, torch.Tensor) or t.device.type != "cuda":
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+
+
+def _stream(t, stream):
+    if stream is None:
+        return torch.cuda.current_stream(t.device).cuda_stream
+    return stream.cuda_stream if isinstance(stream, torch.cuda.Stream) else int(stream)
+
+
+def forward(q, k, v, causal=False, scale=None, out=None, lse=None, stream=None):
+    """O, L = attention(q, k, v); q/k/v bf16 CUDA [B,H,N,d].  Returns (o, lse)."""
+    _check("q", q, torch.bfloat16)
+    if q.dim() != 4:
+        raise ValueError("q must be [B, H, N, d]")
+    B, H, N, d = q.shape
+    _check("k", k, torch.bfloat16, q.shape)
+    _check("v", v, torch.bfloat16, q.shape)
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    if out is None:
+        out = torch.empty_like(q)
+    _check("out", out, torch.bfloat16, q.shape)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    _check("lse", lse, torch.float32, (B, H, N))
+    with torch.cuda.device(q.device):
+        rc = fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                    B, H, N, d, causal, scale, _stream(q, stream))
+    if rc != FA_OK:
+        raise FaError(rc, "fa_fwd")
+    return out, lse
+
+
+def backward(q, k, v, o, lse, do, causal=False, scale=None, dq=None, dk=None, dv=None,
+             workspace=None, stream=None):
+    """dQ, dK, dV (fp32) of attention(q, k, v) given dO; o and lse from forward()."""
+    _check("q", q, torch.bfloat16)
+    if q.dim() != 4:
+        raise ValueError("q must be [B, H, N, d]")
+    B, H, N, d = q.shape
+    for name, t in (("k", k), ("v", v), ("o", o), ("do", do)):
+        _check(name, t, torch.bfloat16, q.shape)
+    _check("lse", lse, torch.float32, (B, H, N))
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    grads = []
+    for name, t in (("dq", dq), ("dk", dk), ("dv", dv)):
+        if t is None:
+            t = torch.empty(q.shape, dtype=torch.float32, device=q.device)
+        _check(name, t, torch.float32, q.shape)
+        grads.append(t)
+    need = fa_bwd_workspace_bytes(B, H, N, d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    _check("workspace", workspace, torch.uint8)
+    with torch.cuda.device(q.device):
+        rc = fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                    do.data_ptr(), grads[0].data_ptr(), grads[1].data_ptr(), grads[2].data_ptr(),
+                    B, H, N, d, causal, scale, workspace.data_ptr(), workspace.numel(),
+                    _stream(q, stream))
+    if rc != FA_OK:
+        raise FaError(rc, "fa_bwd")
+    return tuple(grads)

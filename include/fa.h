@@ -1,0 +1,110 @@
+/*
+ * fa.h - C ABI of libfa.so: exact scaled-dot-product attention on GB300 (sm_103a).
+ *
+ * The operation ("FlashAttention: Move Less, Not Compute Less", section "The
+ * Multiplication May Not Be the Slow Part"; the 1/sqrt(d) scale and causal rule
+ * from the course page "10 FlashAttention", sections 1 and 4):
+ *
+ *     O = softmax(Q K^T * scale + mask) V,   per (batch b, head h),
+ *     mask[i][j] = -inf where causal and j > i (query i sees keys 0..i), else 0,
+ *     L[i] = m_i + ln(l_i) with m_i the row max of the scaled, masked scores and
+ *            l_i = sum_j exp(s_ij - m_i)   ("FlashAttention-2: Why the Attention
+ *            Bottleneck Wasn't Where Everyone Was Looking", section "FA2 change #1").
+ *
+ * The N x N score and probability matrices are never written to global memory:
+ * the forward pass streams K/V tiles through on-chip memory with the online
+ * softmax update and divides by l once at the end; the backward pass rebuilds S
+ * and P tile by tile from L ("Why More Arithmetic Can Finish Sooner").
+ *
+ * Conventions shared by every entry point:
+ *  - Tensors are DEVICE pointers in the caller's CUDA context, contiguous,
+ *    row-major [B][H][N][d] for q, k, v, o, dout, dq, dk, dv and [B][H][N] for lse.
+ *    q, k, v, o, dout hold bfloat16 values (raw 16-bit __nv_bfloat16 bits);
+ *    lse, dq, dk, dv hold float32.
+ *  - Every pointer must be 16-byte aligned (FA_ERR_MISALIGNED otherwise).
+ *  - The caller owns every buffer.  The library allocates no device memory per
+ *    call; it keeps a small per-device cache (SM count, an 8-byte device status
+ *    word that lives in the library's own device data).
+ *  - Calls are asynchronous on `stream` (a cudaStream_t passed as void*; NULL is
+ *    the legacy default stream) and never synchronise, except fa_device_status.
+ *  - Argument errors are reported by the return value BEFORE anything is
+ *    launched.  A launch failure returns FA_ERR_CUDA (from cudaGetLastError).
+ *  - Every wait inside the kernels is bounded (about two seconds).  A wait that
+ *    runs out records FA_ERR_TIMEOUT in the device status word and the kernel
+ *    returns without hanging; fa_device_status reports it.
+ */
+#ifndef FA_H
+#define FA_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    FA_OK = 0,
+    FA_ERR_INVALID_ARG = 1, /* null pointer, non-positive size, bad scale, ... */
+    FA_ERR_UNSUPPORTED = 2, /* head dimension not built */
+    FA_ERR_MISALIGNED = 3,  /* a pointer is not 16-byte aligned */
+    FA_ERR_CUDA = 4,        /* a CUDA runtime/driver call failed */
+    FA_ERR_TIMEOUT = 5,     /* a bounded in-kernel wait ran out (device status) */
+    FA_ERR_WORKSPACE = 6    /* workspace missing or smaller than required */
+} fa_status;
+
+/*
+ * Forward pass.
+ *   q, k, v : bf16 [B][H][N][d] inputs.
+ *   o       : bf16 [B][H][N][d] output, O = (sum_j P_ij V_j), rounded to nearest even.
+ *   lse     : fp32 [B][H][N] output, the natural-log L of each query row.
+ *   B, H, N : batch, heads, sequence length (queries = keys = N); each >= 1,
+ *             B*H*N < 2^31.  N need not be a multiple of any tile size.
+ *   d       : head dimension, one of 64, 128, 256.
+ *   causal  : nonzero for the causal mask (top-left aligned, j <= i).
+ *   scale   : multiplies Q K^T before the softmax; finite and > 0 (1/sqrt(d) is
+ *             the usual value).
+ * Returns FA_OK or an fa_status code; nothing is launched on an error.
+ */
+int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H,
+           int N, int d, int causal, float scale, void *stream);
+
+/*
+ * Bytes of caller-provided device workspace fa_bwd needs for these sizes (the
+ * per-row D_i = dO_i . O_i and the base-2 copy of L, padded per head).
+ * Returns 0 for invalid sizes.
+ */
+size_t fa_bwd_workspace_bytes(int B, int H, int N, int d);
+
+/*
+ * Backward pass: the gradients of the forward above with respect to q, k and v,
+ * given dout = dL/dO, rebuilding S and P from q, k and the saved lse.
+ *   q, k, v, o, dout : bf16 [B][H][N][d] (o and lse exactly as fa_fwd wrote them).
+ *   lse              : fp32 [B][H][N].
+ *   dq, dk, dv       : fp32 [B][H][N][d] outputs, overwritten (fa_bwd zeroes dq
+ *                      itself before accumulating into it).
+ *   d                : 64 or 128 (256 returns FA_ERR_UNSUPPORTED).
+ *   workspace        : device buffer of at least fa_bwd_workspace_bytes(B,H,N,d)
+ *                      bytes, 16-byte aligned, owned by the caller; its contents
+ *                      on entry do not matter and are overwritten.
+ * Other arguments as in fa_fwd.  Calls that share a workspace must not overlap.
+ */
+int fa_bwd(const void *q, const void *k, const void *v, const void *o, const float *lse,
+           const void *dout, float *dq, float *dk, float *dv, int B, int H, int N, int d,
+           int causal, float scale, void *workspace, size_t workspace_bytes, void *stream);
+
+/* Static, human-readable name of a status code (never NULL). */
+const char *fa_status_string(int status);
+
+/*
+ * Synchronises `stream`, then returns FA_OK if no kernel of this library has
+ * recorded an error on the current device since the last call, or the recorded
+ * code (FA_ERR_TIMEOUT) otherwise, and clears the record.  A CUDA error during
+ * the synchronisation or the read returns FA_ERR_CUDA.
+ */
+int fa_device_status(void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_H */

@@ -1,0 +1,106 @@
+"""The C ABI without a GPU: symbols, status strings and argument validation.
+
+Every call here returns before anything touches CUDA, so it runs on the CPU.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def fa():
+    from exact_attention_26_gb300 import build as fb
+    if fb.needs_build():
+        fb.build()
+    import exact_attention_26_gb300 as fa
+    fa.load()
+    return fa
+
+
+def _declared_functions():
+    names = []
+    for fn in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names += re.findall(r"^[A-Za-z_][\w\s\*]*?\b(fa_\w+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_boundary():
+    names = _declared_functions()
+    for n in ("fa_fwd", "fa_bwd", "fa_bwd_workspace_bytes", "fa_status_string", "fa_device_status"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(fa):
+    lib = ctypes.CDLL(fa.fa.lib_path())
+    for name in _declared_functions():
+        assert hasattr(lib, name), f"{name} declared in include/ but not exported"
+
+
+def test_status_strings(fa):
+    for code in range(7):
+        s = fa.fa_status_string(code)
+        assert s and s != "unknown fa_status"
+    assert fa.fa_status_string(99) == "unknown fa_status"
+
+
+DUMMY = 0x10000  # 16-byte aligned, never dereferenced: validation fails first
+
+
+def _fwd(fa, **kw):
+    a = dict(q=DUMMY, k=DUMMY, v=DUMMY, o=DUMMY, lse=DUMMY, B=1, H=1, N=128, d=64, causal=0,
+             scale=0.125, stream=None)
+    a.update(kw)
+    return fa.fa_fwd(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"], a["N"], a["d"],
+                     a["causal"], a["scale"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=None), 1), (dict(k=None), 1), (dict(v=None), 1), (dict(o=None), 1), (dict(lse=None), 1),
+    (dict(B=0), 1), (dict(H=-1), 1), (dict(N=0), 1), (dict(B=65536, H=256, N=256), 1),
+    (dict(d=96), 2), (dict(d=32), 2), (dict(d=0), 2),
+    (dict(scale=0.0), 1), (dict(scale=-1.0), 1), (dict(scale=float("inf")), 1), (dict(scale=float("nan")), 1),
+    (dict(q=DUMMY + 8), 3), (dict(lse=DUMMY + 4), 3), (dict(o=DUMMY + 2), 3),
+])
+def test_fwd_rejects_bad_arguments(fa, kw, code):
+    assert _fwd(fa, **kw) == code
+
+
+def _bwd(fa, **kw):
+    a = dict(q=DUMMY, k=DUMMY, v=DUMMY, o=DUMMY, lse=DUMMY, do=DUMMY, dq=DUMMY, dk=DUMMY, dv=DUMMY,
+             B=1, H=1, N=128, d=128, causal=1, scale=0.125, ws=DUMMY, ws_bytes=1 << 20, stream=None)
+    a.update(kw)
+    return fa.fa_bwd(a["q"], a["k"], a["v"], a["o"], a["lse"], a["do"], a["dq"], a["dk"], a["dv"],
+                     a["B"], a["H"], a["N"], a["d"], a["causal"], a["scale"], a["ws"], a["ws_bytes"],
+                     a["stream"])
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=None), 1), (dict(do=None), 1), (dict(dq=None), 1), (dict(dv=None), 1),
+    (dict(N=0), 1), (dict(d=256), 2), (dict(d=96), 2), (dict(scale=0.0), 1),
+    (dict(ws=None), 6), (dict(ws_bytes=16), 6),
+    (dict(dk=DUMMY + 4), 3), (dict(ws=DUMMY + 8), 3),
+])
+def test_bwd_rejects_bad_arguments(fa, kw, code):
+    assert _bwd(fa, **kw) == code
+
+
+def test_workspace_size(fa):
+    # delta and base-2 lse, fp32, rows padded to 128 per head
+    assert fa.fa_bwd_workspace_bytes(2, 16, 4096, 128) == 2 * 32 * 4096 * 4
+    assert fa.fa_bwd_workspace_bytes(1, 1, 129, 64) == 2 * 256 * 4
+    assert fa.fa_bwd_workspace_bytes(1, 1, 0, 64) == 0
+    assert fa.fa_bwd_workspace_bytes(1, 1, 128, 256) == 0
+
+
+def test_python_wrapper_rejects_cpu_tensors(fa):
+    import torch
+    q = torch.zeros(1, 1, 8, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        fa.forward(q, q, q)
