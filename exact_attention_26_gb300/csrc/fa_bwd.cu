@@ -1,8 +1,553 @@
-// Backward pass of exact attention for sm_103a (kernels follow).
+// Backward pass of exact attention for sm_103a.
+//
+// The pages fix the structure ("FlashAttention-2: Why the Attention Bottleneck
+// Wasn't Where Everyone Was Looking", section "FA2 change #2", backward: one
+// worker per K/V column block owns dK_j and dV_j, dQ takes additive updates;
+// "FlashAttention: Move Less, Not Compute Less", section "Why More Arithmetic Can
+// Finish Sooner": S and P are rebuilt on chip from the saved row statistics).
+// The formulas are the chain rule of O = softmax(scale QK^T + mask) V:
+//
+//   P   = exp(scale S - L)                  (S = Q K^T, L the forward's log-sum-exp)
+//   dV  = P^T dO
+//   dP  = dO V^T
+//   dS  = P o (dP - D),   D_i = dO_i . O_i
+//   dQ  = scale dS K,     dK = scale dS^T Q
+//
+// Kernel 1 (fa_bwd_pre): D_i, L_i log2(e) (padded rows get D = 0, L = +inf so
+// their P is exactly 0), and dQ := 0.
+//
+// Kernel 2 (fa_bwd_kernel): one CTA per (batch*head, block of 128 keys), looping
+// over query blocks of BQ rows (BQ = 64 for d = 128, 128 for d = 64).  All
+// products are tcgen05 MMAs with fp32 accumulators in tensor memory, computed in
+// the transposed orientation so that a TMEM lane is a key:
+//
+//   S^T  = K_j Q_i^T        (A = K  smem K-major,  B = Q  smem K-major)
+//   dP^T = V_j dO_i^T       (A = V,  B = dO)
+//   dV  += P^T dO_i         (A = P^T from TMEM,  B = dO smem MN-major)
+//   dK  += dS^T Q_i         (A = dS^T from TMEM, B = Q  smem MN-major)
+//   d=128: dQ_i^T = K_j^T dS^T (A = K smem MN-major, B = dS^T smem MN-major)
+//   d=64:  dQ_i   = dS K_j     (A = dS^T smem MN-major, B = K smem MN-major)
+//
+// dQ_i leaves tensor memory through a shared-memory staging tile and one bulk
+// asynchronous fp32 add (cp.reduce.async.bulk) into the global dQ rows, which
+// are contiguous.  At the end dK (times scale) and dV are stored once.
+//
+// Warp roles (320 threads):
+//   warps 0-3  P^T = exp2(S^T scale log2e - L log2e), dS^T = P^T o (dP^T - D)
+//              (one key per thread), written as bf16 to TMEM and dS^T to smem;
+//              final dK/dV epilogue
+//   warps 4-7  dQ readout: TMEM -> staging smem -> bulk add into global dQ
+//   warp 8     TMA producer: K_j, V_j once; Q_i, dO_i, L_i, D_i per 2-stage slot
+//   warp 9     TMEM allocator; lane 0 issues every MMA and commit
 #include "fa_ptx.cuh"
 
 namespace fa {
+namespace {
 
-int launch_bwd(const BwdParams &, cudaStream_t) { return FA_ERR_UNSUPPORTED; }
+template <int D>
+struct BwdTile {
+    static constexpr int BN = 128;                      // keys per CTA
+    static constexpr int BQ = (D == 128) ? 64 : 128;    // query rows per block
+    static constexpr bool DQ_T = (D == 128);            // dQ computed transposed
+    static constexpr int NCH = D / 64;
+    static constexpr uint32_t K_CHUNK = BN * 128;       // 64 columns x 128 keys
+    static constexpr uint32_t Q_CHUNK = BQ * 128;       // 64 columns x BQ rows
+    static constexpr uint32_t KV_BYTES = BN * D * 2;
+    static constexpr uint32_t Q_BYTES = BQ * D * 2;
+    static constexpr uint32_t DS_CHUNK = BN * 128;      // 64 queries x 128 keys, bf16
+    static constexpr uint32_t DS_BYTES = BQ * BN * 2;
+    static constexpr uint32_t STAGE_BYTES = BQ * D * 4; // dQ tile, fp32
+    static constexpr uint32_t VEC_BYTES = BQ * 4;       // L or D of one q-block
+    // tensor memory columns
+    static constexpr uint32_t TM_DV = 0;
+    static constexpr uint32_t TM_DK = D;
+    static constexpr uint32_t TM_ST = 2 * D;            // S^T fp32 (BQ cols); P^T bf16 over it
+    static constexpr uint32_t TM_DPT = 2 * D + BQ;      // dP^T fp32 (BQ cols); dS^T bf16 over it
+    static constexpr uint32_t TM_DQ0 = 384;             // dQ buffers, 64 cols each
+    static constexpr uint32_t TM_DQ1 = 448;
+    static constexpr uint32_t TM_COLS = 512;
+    // shared memory layout
+    static constexpr uint32_t OFF_K = 0;
+    static constexpr uint32_t OFF_V = OFF_K + KV_BYTES;
+    static constexpr uint32_t OFF_Q = OFF_V + KV_BYTES;           // 2 stages
+    static constexpr uint32_t OFF_DO = OFF_Q + 2 * Q_BYTES;       // 2 stages
+    static constexpr uint32_t OFF_DS = OFF_DO + 2 * Q_BYTES;      // 2 buffers
+    static constexpr uint32_t OFF_STAGE = OFF_DS + 2 * DS_BYTES;  // dQ staging
+    static constexpr uint32_t OFF_L2 = OFF_STAGE + STAGE_BYTES;   // 2 stages
+    static constexpr uint32_t OFF_DELTA = OFF_L2 + 2 * VEC_BYTES; // 2 stages
+    static constexpr uint32_t OFF_BAR = OFF_DELTA + 2 * VEC_BYTES;
+    // kv_full, q_full[2], q_empty[2], s_full, ds_full, dq_full[2], dq_empty[2], done,
+    // stg_free, stg_full
+    static constexpr int NBAR = 14;
+    static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
+    static constexpr uint32_t SMEM_BYTES = OFF_MISC + 16 + 1024;
+    static constexpr int THREADS = 320;
+
+    static_assert(D == 64 || D == 128, "backward head dim");
+    static_assert(TM_DPT + BQ <= TM_DQ0, "tensor memory budget");
+    static_assert(Q_CHUNK % 1024 == 0 && DS_CHUNK % 1024 == 0, "swizzle atoms must stay aligned");
+    static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+};
+
+// ---------------------------------------------------------------- preprocess
+
+template <int D>
+__global__ void __launch_bounds__(256)
+    fa_bwd_pre_kernel(const __nv_bfloat16 *__restrict__ o, const __nv_bfloat16 *__restrict__ dout,
+                      const float *__restrict__ lse, float *__restrict__ delta,
+                      float *__restrict__ lse2, float *__restrict__ dq, int N, int Npad, int BH) {
+    constexpr int PER = D / 32;  // elements per lane
+    const int lane = threadIdx.x & 31;
+    const long long warp0 = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
+    const long long rows = (long long)BH * Npad;
+    constexpr float kLog2e = 1.4426950408889634074f;
+    for (long long r = warp0; r < rows; r += nwarps) {
+        const int bh = (int)(r / Npad);
+        const int i = (int)(r % Npad);
+        if (i < N) {
+            const size_t row = ((size_t)bh * N + i) * D + (size_t)lane * PER;
+            float acc = 0.f;
+            if constexpr (PER == 4) {
+                const uint2 a = *reinterpret_cast<const uint2 *>(o + row);
+                const uint2 b = *reinterpret_cast<const uint2 *>(dout + row);
+                const __nv_bfloat162 *pa = reinterpret_cast<const __nv_bfloat162 *>(&a);
+                const __nv_bfloat162 *pb = reinterpret_cast<const __nv_bfloat162 *>(&b);
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const float2 fa = __bfloat1622float2(pa[e]);
+                    const float2 fb = __bfloat1622float2(pb[e]);
+                    acc = fmaf(fa.x, fb.x, acc);
+                    acc = fmaf(fa.y, fb.y, acc);
+                }
+                *reinterpret_cast<float4 *>(dq + row) = make_float4(0.f, 0.f, 0.f, 0.f);
+            } else {
+                const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162 *>(o + row);
+                const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162 *>(dout + row);
+                const float2 fa = __bfloat1622float2(a);
+                const float2 fb = __bfloat1622float2(b);
+                acc = fmaf(fa.x, fb.x, fmaf(fa.y, fb.y, 0.f));
+                *reinterpret_cast<float2 *>(dq + row) = make_float2(0.f, 0.f);
+            }
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+            if (lane == 0) {
+                delta[r] = acc;
+                lse2[r] = lse[(size_t)bh * N + i] * kLog2e;
+            }
+        } else if (lane == 0) {
+            delta[r] = 0.f;
+            lse2[r] = INFINITY;
+        }
+    }
+}
+
+// ---------------------------------------------------------------- main kernel
+
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(320, 1)
+    fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                  const float *__restrict__ ws_lse2, const float *__restrict__ ws_delta,
+                  float *__restrict__ dq, float *__restrict__ dk, float *__restrict__ dv, int N,
+                  int Npad, int BH, float scale, float scale_log2, int *status,
+                  unsigned long long limit_ns) {
+    using T = BwdTile<D>;
+    constexpr int BQ = T::BQ;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *gbase = smem_raw + (base - raw);
+
+    const uint32_t sK = base + T::OFF_K, sV = base + T::OFF_V;
+    const uint32_t sQ = base + T::OFF_Q, sDO = base + T::OFF_DO;
+    const uint32_t sDS = base + T::OFF_DS, sStage = base + T::OFF_STAGE;
+    const uint32_t sL2 = base + T::OFF_L2, sDelta = base + T::OFF_DELTA;
+    const uint32_t bar = base + T::OFF_BAR;
+    const uint32_t bar_kv_full = bar;
+    const uint32_t bar_q_full = bar + 8;        // [2]
+    const uint32_t bar_q_empty = bar + 24;      // [2]
+    const uint32_t bar_s_full = bar + 40;
+    const uint32_t bar_ds_full = bar + 48;
+    const uint32_t bar_dq_full = bar + 56;      // [2]
+    const uint32_t bar_dq_empty = bar + 72;     // [2]
+    const uint32_t bar_done = bar + 88;
+    const uint32_t bar_stg_free = bar + 96;     // staging tile may be overwritten
+    const uint32_t bar_stg_full = bar + 104;    // staging tile written by all 128 threads
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + T::OFF_MISC);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(gbase + T::OFF_MISC + 4);
+    float *stage_f = reinterpret_cast<float *>(gbase + T::OFF_STAGE);
+    const float *l2_f = reinterpret_cast<const float *>(gbase + T::OFF_L2);
+    const float *delta_f = reinterpret_cast<const float *>(gbase + T::OFF_DELTA);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    // Causal: key block 0 has the most query blocks, so low blockIdx = key block first.
+    const int bh = blockIdx.x % BH;
+    const int jb = blockIdx.x / BH;
+    const int kv0 = jb * T::BN;
+    const int n_qb = (N + BQ - 1) / BQ;
+    const int i_start = CAUSAL ? kv0 / BQ : 0;
+    const int n_it = n_qb - i_start;
+
+    if (threadIdx.x == 0) {
+        mbar_init(bar_kv_full, 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(bar_q_full + 8 * s, 1);
+            mbar_init(bar_q_empty + 8 * s, 1);
+            mbar_init(bar_dq_full + 8 * s, 1);
+            mbar_init(bar_dq_empty + 8 * s, 128);
+        }
+        mbar_init(bar_s_full, 1);
+        mbar_init(bar_ds_full, 128);
+        mbar_init(bar_done, 1);
+        mbar_init(bar_stg_free, 1);
+        mbar_init(bar_stg_full, 128);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 9) {
+        tmem_alloc(smem_u32(tmem_slot), T::TM_COLS);
+        tmem_relinquish();
+    }
+    if (warp == 8 && lane == 0) {
+        tma_prefetch_desc(&tm_q);
+        tma_prefetch_desc(&tm_k);
+        tma_prefetch_desc(&tm_v);
+        tma_prefetch_desc(&tm_do);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const Guard g{status, abort_flag, limit_ns};
+
+    if (warp == 8) {
+        // ------------------------------------------------------- TMA producer
+        if (lane == 0) {
+            mbar_arrive_expect_tx(bar_kv_full, 2 * T::KV_BYTES);
+            for (int c = 0; c < T::NCH; ++c) {
+                tma_load_3d(sK + c * T::K_CHUNK, &tm_k, bar_kv_full, c * 64, kv0, bh);
+                tma_load_3d(sV + c * T::K_CHUNK, &tm_v, bar_kv_full, c * 64, kv0, bh);
+            }
+            int issued = 0;
+            for (int it = 0; it < n_it; ++it) {
+                const int s = it & 1;
+                const int q0 = (i_start + it) * BQ;
+                if (it >= 2 && !mbar_wait(bar_q_empty + 8 * s, ((it >> 1) - 1) & 1, g,
+                                          SITE_BWD_LOAD_EMPTY))
+                    break;
+                const uint32_t fb = bar_q_full + 8 * s;
+                mbar_arrive_expect_tx(fb, 2 * T::Q_BYTES + 2 * T::VEC_BYTES);
+                for (int c = 0; c < T::NCH; ++c) {
+                    tma_load_3d(sQ + s * T::Q_BYTES + c * T::Q_CHUNK, &tm_q, fb, c * 64, q0, bh);
+                    tma_load_3d(sDO + s * T::Q_BYTES + c * T::Q_CHUNK, &tm_do, fb, c * 64, q0, bh);
+                }
+                const size_t voff = (size_t)bh * Npad + q0;
+                bulk_load(sL2 + s * T::VEC_BYTES, ws_lse2 + voff, T::VEC_BYTES, fb);
+                bulk_load(sDelta + s * T::VEC_BYTES, ws_delta + voff, T::VEC_BYTES, fb);
+                ++issued;
+            }
+            if (*abort_flag) {
+                volatile int never = 0;
+                const Guard g2{status, &never, limit_ns / 4};
+                mbar_wait(bar_kv_full, 0, g2, SITE_BWD_DRAIN);
+                for (int it = (issued > 2 ? issued - 2 : 0); it < issued; ++it)
+                    mbar_wait(bar_q_full + 8 * (it & 1), (it >> 1) & 1, g2, SITE_BWD_DRAIN);
+            }
+        }
+    } else if (warp == 9) {
+        // ------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t kIdescT = idesc_bf16_f32(128, BQ, false, false);   // S^T, dP^T
+            constexpr uint32_t kIdescAcc = idesc_bf16_f32(128, D, false, true);   // dV, dK
+            constexpr uint32_t kIdescDQ = T::DQ_T ? idesc_bf16_f32(128, BQ, true, true)  // dQ^T
+                                                  : idesc_bf16_f32(128, D, true, true);  // dQ
+            bool ok = mbar_wait(bar_kv_full, 0, g, SITE_BWD_MMA_KV);
+            auto issue_st_dpt = [&](int it) {
+                const int s = it & 1;
+                const uint32_t q_t = sQ + s * T::Q_BYTES, do_t = sDO + s * T::Q_BYTES;
+#pragma unroll
+                for (int ks = 0; ks < D / 16; ++ks) {
+                    const uint32_t koff = (ks & 3) * 32;
+                    const uint32_t kc = (ks >> 2);
+                    mma_ss(tmem + T::TM_ST, sdesc_sw128(sK + kc * T::K_CHUNK + koff, 16, 1024),
+                           sdesc_sw128(q_t + kc * T::Q_CHUNK + koff, 16, 1024), kIdescT,
+                           ks > 0 ? 1u : 0u);
+                }
+#pragma unroll
+                for (int ks = 0; ks < D / 16; ++ks) {
+                    const uint32_t koff = (ks & 3) * 32;
+                    const uint32_t kc = (ks >> 2);
+                    mma_ss(tmem + T::TM_DPT, sdesc_sw128(sV + kc * T::K_CHUNK + koff, 16, 1024),
+                           sdesc_sw128(do_t + kc * T::Q_CHUNK + koff, 16, 1024), kIdescT,
+                           ks > 0 ? 1u : 0u);
+                }
+                tc_commit(bar_s_full);
+            };
+            if (ok && mbar_wait(bar_q_full, 0, g, SITE_BWD_MMA_Q_FULL)) {
+                tc_fence_after();
+                issue_st_dpt(0);
+            } else {
+                ok = false;
+            }
+            for (int it = 0; ok && it < n_it; ++it) {
+                const int s = it & 1;
+                const uint32_t q_t = sQ + s * T::Q_BYTES, do_t = sDO + s * T::Q_BYTES;
+                if (!mbar_wait(bar_ds_full, it & 1, g, SITE_BWD_MMA_DS_FULL)) { ok = false; break; }
+                tc_fence_after();
+                // dV += P^T dO_i ; dK += dS^T Q_i   (K = BQ queries, 16 per step)
+#pragma unroll
+                for (int ks = 0; ks < BQ / 16; ++ks)
+                    mma_ts(tmem + T::TM_DV, tmem + T::TM_ST + ks * 8,
+                           sdesc_sw128(do_t + ks * 2048, T::Q_CHUNK, 1024), kIdescAcc,
+                           (it > 0 || ks > 0) ? 1u : 0u);
+#pragma unroll
+                for (int ks = 0; ks < BQ / 16; ++ks)
+                    mma_ts(tmem + T::TM_DK, tmem + T::TM_DPT + ks * 8,
+                           sdesc_sw128(q_t + ks * 2048, T::Q_CHUNK, 1024), kIdescAcc,
+                           (it > 0 || ks > 0) ? 1u : 0u);
+                tc_commit(bar_q_empty + 8 * s);
+                // Next block's S^T and dP^T overlap this block's dQ and the softmax of the next.
+                if (it + 1 < n_it) {
+                    if (!mbar_wait(bar_q_full + 8 * ((it + 1) & 1), ((it + 1) >> 1) & 1, g,
+                                   SITE_BWD_MMA_Q_FULL)) { ok = false; break; }
+                    tc_fence_after();
+                    issue_st_dpt(it + 1);
+                }
+                // dQ of this block into TMEM buffer it&1 (K = 128 keys, 16 per step).
+                const int b = it & 1;
+                if (it >= 2 && !mbar_wait(bar_dq_empty + 8 * b, ((it >> 1) - 1) & 1, g,
+                                          SITE_BWD_MMA_DQ_FREE)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t ds_t = sDS + b * T::DS_BYTES;
+                const uint32_t dq_tm = tmem + (b ? T::TM_DQ1 : T::TM_DQ0);
+#pragma unroll
+                for (int ks = 0; ks < T::BN / 16; ++ks) {
+                    if constexpr (T::DQ_T) {
+                        // dQ^T[d][q] = sum_k K[k][d] dS^T[k][q]: A = K (M = d), B = dS^T (N = q)
+                        mma_ss(dq_tm, sdesc_sw128(sK + ks * 2048, T::K_CHUNK, 1024),
+                               sdesc_sw128(ds_t + ks * 2048, T::DS_CHUNK, 1024), kIdescDQ,
+                               ks > 0 ? 1u : 0u);
+                    } else {
+                        // dQ[q][d] = sum_k dS^T[k][q] K[k][d]: A = dS^T (M = q), B = K (N = d)
+                        mma_ss(dq_tm, sdesc_sw128(ds_t + ks * 2048, T::DS_CHUNK, 1024),
+                               sdesc_sw128(sK + ks * 2048, T::K_CHUNK, 1024), kIdescDQ,
+                               ks > 0 ? 1u : 0u);
+                    }
+                }
+                tc_commit(bar_dq_full + 8 * b);
+            }
+            tc_commit(bar_done);
+            volatile int never = 0;
+            const Guard g2{status, &never, limit_ns};
+            mbar_wait(bar_done, 0, g2, SITE_BWD_DRAIN);
+        }
+    } else if (warp < 4) {
+        // ------------------------------------------------------- P^T and dS^T
+        const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+        const uint32_t t_st = tmem + lane_base + T::TM_ST;
+        const uint32_t t_dpt = tmem + lane_base + T::TM_DPT;
+        const int r = threadIdx.x;       // key row within the block (TMEM lane)
+        const int key = kv0 + r;
+        bool ok = true;
+        for (int it = 0; it < n_it; ++it) {
+            const int s = it & 1;
+            const int q0 = (i_start + it) * BQ;
+            ok = mbar_wait_warp(bar_s_full, it & 1, g, SITE_BWD_SOFTMAX_S_FULL);
+            if (!ok) break;
+            tc_fence_after();
+            const bool need_mask = (kv0 + T::BN > N) || (CAUSAL && q0 < kv0 + T::BN - 1);
+            const float *l2v = l2_f + s * BQ;
+            const float *dlv = delta_f + s * BQ;
+            uint8_t *ds_row = gbase + T::OFF_DS + (it & 1) * T::DS_BYTES + r * 128;
+#pragma unroll 1
+            for (int c = 0; c < BQ / 32; ++c) {
+                uint32_t sv[32], dpv[32];
+                tmem_ld32(t_st + c * 32, sv);
+                tmem_ld32(t_dpt + c * 32, dpv);
+                tmem_wait_ld(sv);
+                tmem_wait_ld(dpv);
+                uint32_t pk[16], dk_[16];
+#pragma unroll
+                for (int e = 0; e < 32; e += 4) {
+                    const float4 l4 = *reinterpret_cast<const float4 *>(l2v + c * 32 + e);
+                    const float4 d4 = *reinterpret_cast<const float4 *>(dlv + c * 32 + e);
+                    const float lq[4] = {l4.x, l4.y, l4.z, l4.w};
+                    const float dq_[4] = {d4.x, d4.y, d4.z, d4.w};
+                    float p[4], ds[4];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        p[u] = ex2(fmaf(__uint_as_float(sv[e + u]), scale_log2, -lq[u]));
+                        if (need_mask) {
+                            const int q = q0 + c * 32 + e + u;
+                            if (key >= N || (CAUSAL && q < key)) p[u] = 0.f;
+                        }
+                        ds[u] = p[u] * (__uint_as_float(dpv[e + u]) - dq_[u]);
+                    }
+                    pk[e / 2] = pack_bf16(p[0], p[1]);
+                    pk[e / 2 + 1] = pack_bf16(p[2], p[3]);
+                    dk_[e / 2] = pack_bf16(ds[0], ds[1]);
+                    dk_[e / 2 + 1] = pack_bf16(ds[2], ds[3]);
+                }
+                tmem_st16(t_st + c * 16, pk);
+                tmem_st16(t_dpt + c * 16, dk_);
+                // dS^T row r, queries [32c, 32c + 32): 4 swizzled 16-byte units.
+                const int h = (c * 32) / 64;
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int unit = ((c * 32) % 64) / 8 + u;
+                    uint4 *dst = reinterpret_cast<uint4 *>(ds_row + h * T::DS_CHUNK +
+                                                           ((unit ^ (r & 7)) * 16));
+                    *dst = make_uint4(dk_[4 * u], dk_[4 * u + 1], dk_[4 * u + 2], dk_[4 * u + 3]);
+                }
+            }
+            tmem_wait_st();
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(bar_ds_full);
+        }
+        // ------------------------------------------------------- dK, dV epilogue
+        ok = ok && mbar_wait_warp(bar_done, 0, g, SITE_BWD_EPILOGUE);
+        if (ok) {
+            tc_fence_after();
+            float *dv_row = dv + ((size_t)bh * N + key) * D;
+            float *dk_row = dk + ((size_t)bh * N + key) * D;
+#pragma unroll 1
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t a[32], b2[32];
+                tmem_ld32(tmem + lane_base + T::TM_DV + c * 32, a);
+                tmem_ld32(tmem + lane_base + T::TM_DK + c * 32, b2);
+                tmem_wait_ld(a);
+                tmem_wait_ld(b2);
+                if (key < N) {
+#pragma unroll
+                    for (int e = 0; e < 32; e += 4) {
+                        *reinterpret_cast<float4 *>(dv_row + c * 32 + e) =
+                            make_float4(__uint_as_float(a[e]), __uint_as_float(a[e + 1]),
+                                        __uint_as_float(a[e + 2]), __uint_as_float(a[e + 3]));
+                        *reinterpret_cast<float4 *>(dk_row + c * 32 + e) = make_float4(
+                            __uint_as_float(b2[e]) * scale, __uint_as_float(b2[e + 1]) * scale,
+                            __uint_as_float(b2[e + 2]) * scale, __uint_as_float(b2[e + 3]) * scale);
+                    }
+                }
+            }
+        }
+    } else {
+        // ------------------------------------------------------- dQ readout (warps 4-7)
+        const int t = threadIdx.x - 128;  // TMEM lane: d index (d = 128) or query row (d = 64)
+        const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+        bool ok = true;
+        for (int it = 0; it < n_it; ++it) {
+            const int b = it & 1;
+            const int q0 = (i_start + it) * BQ;
+            ok = mbar_wait_warp(bar_dq_full + 8 * b, (it >> 1) & 1, g, SITE_BWD_DQ_FULL);
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t src = tmem + lane_base + (b ? T::TM_DQ1 : T::TM_DQ0);
+            uint32_t x0[32], x1[32];
+            tmem_ld32(src, x0);
+            tmem_ld32(src + 32, x1);
+            tmem_wait_ld(x0);
+            tmem_wait_ld(x1);
+            tc_fence_before();
+            mbar_arrive(bar_dq_empty + 8 * b);
+            // The staging tile is free once the previous bulk add has read it.  All
+            // syncs here are bounded mbarrier waits, so an abort cannot strand a warp.
+            if (t == 0) {
+                bulk_wait_group_read<0>();
+                mbar_arrive(bar_stg_free);
+            }
+            ok = mbar_wait_warp(bar_stg_free, it & 1, g, SITE_BWD_DQ_FULL);
+            if (!ok) break;
+            if constexpr (T::DQ_T) {
+                // lane t = column d of dQ; the 64 columns of TMEM are the block's queries
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                    stage_f[e * D + t] = __uint_as_float(x0[e]) * scale;
+                    stage_f[(e + 32) * D + t] = __uint_as_float(x1[e]) * scale;
+                }
+            } else {
+                // lane t = query row; the 64 columns are d
+                float *row = stage_f + t * D;
+#pragma unroll
+                for (int e = 0; e < 32; e += 4) {
+                    *reinterpret_cast<float4 *>(row + e) =
+                        make_float4(__uint_as_float(x0[e]) * scale, __uint_as_float(x0[e + 1]) * scale,
+                                    __uint_as_float(x0[e + 2]) * scale, __uint_as_float(x0[e + 3]) * scale);
+                    *reinterpret_cast<float4 *>(row + 32 + e) =
+                        make_float4(__uint_as_float(x1[e]) * scale, __uint_as_float(x1[e + 1]) * scale,
+                                    __uint_as_float(x1[e + 2]) * scale, __uint_as_float(x1[e + 3]) * scale);
+                }
+            }
+            fence_proxy_async_smem();
+            mbar_arrive(bar_stg_full);
+            if (warp == 4) {
+                bool ok0 = true;
+                if (lane == 0) {
+                    ok0 = mbar_wait(bar_stg_full, it & 1, g, SITE_BWD_DQ_FULL);
+                    if (ok0) {
+                        const int rows = min(BQ, N - q0);
+                        bulk_reduce_add_f32(dq + ((size_t)bh * N + q0) * D, sStage,
+                                            (uint32_t)(rows * D * 4));
+                        bulk_commit_group();
+                    }
+                }
+                ok0 = __shfl_sync(0xffffffffu, ok0 ? 1 : 0, 0) != 0;
+                if (!ok0) {
+                    ok = false;
+                    break;
+                }
+            }
+        }
+        if (t == 0) bulk_wait_group<0>();
+    }
+
+    __syncwarp();
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 9) {
+        tc_fence_after();
+        tmem_dealloc(tmem, T::TM_COLS);
+    }
+}
+
+template <int D, bool CAUSAL>
+int launch_bwd_t(const BwdParams &p, cudaStream_t stream) {
+    using T = BwdTile<D>;
+    {
+        const long long rows = (long long)p.BH * p.Npad;
+        long long blocks = (rows * 32 + 255) / 256;
+        const long long cap = (long long)p.num_sms * 16;
+        if (blocks > cap) blocks = cap;
+        if (blocks < 1) blocks = 1;
+        fa_bwd_pre_kernel<D><<<(unsigned)blocks, 256, 0, stream>>>(
+            reinterpret_cast<const __nv_bfloat16 *>(p.o),
+            reinterpret_cast<const __nv_bfloat16 *>(p.dout), p.lse, p.ws_delta, p.ws_lse2, p.dq,
+            p.N, p.Npad, p.BH);
+        if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
+    }
+    auto kern = fa_bwd_kernel<D, CAUSAL>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)T::SMEM_BYTES) != cudaSuccess)
+        return FA_ERR_CUDA;
+    const long long grid = (long long)((p.N + T::BN - 1) / T::BN) * p.BH;
+    if (grid > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
+    kern<<<(unsigned)grid, T::THREADS, T::SMEM_BYTES, stream>>>(
+        p.tm_q, p.tm_k, p.tm_v, p.tm_do, p.ws_lse2, p.ws_delta, p.dq, p.dk, p.dv, p.N, p.Npad,
+        p.BH, p.scale, p.scale_log2, p.status, p.limit_ns);
+    return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+}  // namespace
+
+int launch_bwd(const BwdParams &p, cudaStream_t stream) {
+    switch (p.d) {
+        case 64: return p.causal ? launch_bwd_t<64, true>(p, stream) : launch_bwd_t<64, false>(p, stream);
+        case 128: return p.causal ? launch_bwd_t<128, true>(p, stream) : launch_bwd_t<128, false>(p, stream);
+        default: return FA_ERR_UNSUPPORTED;
+    }
+}
 
 }  // namespace fa

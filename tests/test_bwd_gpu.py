@@ -1,0 +1,107 @@
+"""Backward parity on the GPU: fa_bwd (through the C ABI) against the float64 oracle."""
+import numpy as np
+import pytest
+import torch
+
+from exact_attention_26_gb300.inputs import normal_qkv, to_f64
+from gpu_common import GRAD_ABS, assert_abs_close, load_fa
+from oracle import Oracle
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module")
+def fa():
+    return load_fa()
+
+
+@pytest.fixture(scope="module")
+def orc():
+    return Oracle()
+
+
+def _grads(fa, q, k, v, do, causal, scale=None, workspace=None):
+    q, k, v, do = (t.to(DEV) for t in (q, k, v, do))
+    o, lse = fa.forward(q, k, v, causal=causal, scale=scale)
+    dq, dk, dv = fa.backward(q, k, v, o, lse, do, causal=causal, scale=scale, workspace=workspace)
+    torch.cuda.synchronize()
+    assert fa.fa_device_status(None) == 0
+    return [t.cpu().numpy() for t in (dq, dk, dv)]
+
+
+def _check(got, ref, what):
+    for name, g, r in zip(("dQ", "dK", "dV"), got, ref):
+        assert_abs_close(g, r, GRAD_ABS, f"{what} {name}")
+
+
+SMALL = [
+    (1, 1, 1, 64), (1, 1, 2, 128), (1, 2, 100, 64), (1, 1, 128, 128), (2, 1, 129, 128),
+    (1, 2, 300, 64), (1, 1, 513, 128), (2, 2, 640, 128), (1, 1, 1000, 64),
+]
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("shape", SMALL, ids=lambda s: "x".join(map(str, s)))
+def test_bwd_small(fa, orc, shape, causal):
+    B, H, N, d = shape
+    q, k, v, do = normal_qkv(B, H, N, d, seed=3 * N + d, with_do=True)
+    got = _grads(fa, q, k, v, do, causal)
+    ref = orc.bwd(to_f64(q), to_f64(k), to_f64(v), to_f64(do), causal=causal)
+    _check(got, ref, f"{shape} causal={causal}")
+
+
+def test_bwd_b2_h16_n4096_d128_causal(fa, orc):
+    """The full fwd+bwd workload in the benchmark's launch configuration; the
+    oracle recomputes three whole heads (heads are independent)."""
+    B, H, N, d = 2, 16, 4096, 128
+    q, k, v, do = normal_qkv(B, H, N, d, seed=0, with_do=True)
+    got = _grads(fa, q, k, v, do, True)
+    for (b, h) in [(0, 0), (1, 7), (1, 15)]:
+        sl = (slice(b, b + 1), slice(h, h + 1))
+        ref = orc.bwd(to_f64(q[sl]), to_f64(k[sl]), to_f64(v[sl]), to_f64(do[sl]), causal=True)
+        _check([g[sl] for g in got], ref, f"head ({b},{h})")
+    # properties that hold for every head at any size: sum_j dK_j = 0, sum_j dV_j = sum_i dO_i
+    dk_sum = got[1].sum(axis=2)
+    dv_sum = got[2].sum(axis=2)
+    do_sum = do.double().sum(dim=2).numpy()
+    assert np.max(np.abs(dk_sum)) < 0.5, np.max(np.abs(dk_sum))
+    assert np.max(np.abs(dv_sum - do_sum)) < 0.5, np.max(np.abs(dv_sum - do_sum))
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_bwd_b2_h4_n2048_d64(fa, orc, causal):
+    q, k, v, do = normal_qkv(2, 4, 2048, 64, seed=4, with_do=True)
+    got = _grads(fa, q, k, v, do, causal)
+    sl = (slice(1, 2), slice(2, 4))
+    ref = orc.bwd(to_f64(q[sl]), to_f64(k[sl]), to_f64(v[sl]), to_f64(do[sl]), causal=causal)
+    _check([g[sl] for g in got], ref, "2048x64")
+
+
+@pytest.mark.parametrize("scale", [1.5, 0.02])
+def test_bwd_extreme_scales(fa, orc, scale):
+    q, k, v, do = normal_qkv(1, 2, 400, 128, seed=11, with_do=True)
+    for causal in (False, True):
+        got = _grads(fa, q, k, v, do, causal, scale=scale)
+        ref = orc.bwd(to_f64(q), to_f64(k), to_f64(v), to_f64(do), causal=causal, scale=scale)
+        _check(got, ref, f"scale={scale} causal={causal}")
+
+
+def test_bwd_workspace_contents_do_not_matter(fa):
+    q, k, v, do = normal_qkv(1, 2, 333, 128, seed=12, with_do=True)
+    need = fa.fa_bwd_workspace_bytes(1, 2, 333, 128)
+    ws = torch.full((need,), 0xFF, dtype=torch.uint8, device=DEV)  # NaN bit patterns
+    a = _grads(fa, q, k, v, do, True, workspace=ws)
+    b = _grads(fa, q, k, v, do, True)
+    for x, y in zip(a, b):
+        assert np.allclose(x, y, atol=1e-6, rtol=0)
+
+
+def test_bwd_dk_dv_deterministic(fa):
+    """dK and dV are owned by one CTA each, so they are bit-reproducible."""
+    q, k, v, do = normal_qkv(2, 2, 777, 128, seed=13, with_do=True)
+    a = _grads(fa, q, k, v, do, True)
+    b = _grads(fa, q, k, v, do, True)
+    assert np.array_equal(a[1], b[1]) and np.array_equal(a[2], b[2])
+    assert np.allclose(a[0], b[0], atol=1e-5, rtol=0)
