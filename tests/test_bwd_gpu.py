@@ -81,11 +81,21 @@ def test_bwd_b2_h4_n2048_d64(fa, orc, causal):
 
 @pytest.mark.parametrize("scale", [1.5, 0.02])
 def test_bwd_extreme_scales(fa, orc, scale):
+    """Far from 1/sqrt(d) the gradients scale with `scale` and P/dS are rounded to
+    bf16 (relative precision 2^-9), so the bound here is relative to the largest
+    reference gradient: 2e-2 * max(1, max|ref| / 2), i.e. 1% of the largest
+    gradient once gradients exceed 2.  The main error terms are D_i = dO_i . O_i
+    taken from the bf16-rounded O and the bf16 rounding of dS."""
     q, k, v, do = normal_qkv(1, 2, 400, 128, seed=11, with_do=True)
     for causal in (False, True):
         got = _grads(fa, q, k, v, do, causal, scale=scale)
         ref = orc.bwd(to_f64(q), to_f64(k), to_f64(v), to_f64(do), causal=causal, scale=scale)
-        _check(got, ref, f"scale={scale} causal={causal}")
+        for name, g, r in zip(("dQ", "dK", "dV"), got, ref):
+            mag = float(np.max(np.abs(r)))
+            err = float(np.max(np.abs(g - r)))
+            print(f"scale={scale} causal={causal} {name}: max|ref| {mag:.3g} max-abs err {err:.3g}")
+            assert np.all(np.isfinite(g))
+            assert err <= GRAD_ABS * max(1.0, mag / 2.0), (name, err, mag)
 
 
 def test_bwd_workspace_contents_do_not_matter(fa):
