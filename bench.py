@@ -1,0 +1,506 @@
+#!/usr/bin/env python3
+"""Benchmark of the exact-attention hot path on GB300.
+
+One step = one forward (fa_fwd) and one backward (fa_bwd) over the workload
+B=2, H=16, N=4096, d=128, causal, scale 1/sqrt(d), bf16 N(0,1) inputs (seed 0):
+the one workload that runs every step of the path.  Throughput is algorithmic
+TFLOPS: 4*B*H*N^2*d per forward and 10*B*H*N^2*d per backward (the five GEMMs
+S, dP, dV, dK, dQ), both halved for the causal mask.
+
+Prints ONE JSON line (rank 0).  Under torchrun each rank runs its own copy of the
+workload on its own GPU (weak scaling, no data-path collective); the timed region
+is bracketed by a barrier and a synchronize, and the slowest rank's time counts.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the float64 CPU oracle on the host cores instead (a
+bounded row sample of the same workload per step).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "attention fwd/bwd TFLOPS (causal & non-causal) and % of GB300 dense BF16 peak"
+UNIT = "TFLOPS"
+WORKLOAD = dict(B=2, H=16, N=4096, d=128, causal=True)
+WORKLOAD_NAME = "exact SDPA fwd+bwd, B=2 H=16 N=4096 d=128, causal, bf16 in, fp32 dQ/dK/dV"
+L2_FLUSH_BYTES = 256 << 20
+FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "hbm_gbs": 6800.0}
+
+# Forward/backward workloads reported beside the step (context, outside the timed region).
+FWD_WORKLOADS = [
+    ("B8_H16_N2048_d64_noncausal", 8, 16, 2048, 64, False, "normal"),
+    ("B8_H16_N2048_d64_causal", 8, 16, 2048, 64, True, "normal"),
+    ("B1_H16_N16384_d128_causal", 1, 16, 16384, 128, True, "normal"),
+    ("B4_H8_N8192_d256_noncausal_boosted", 4, 8, 8192, 256, False, "boosted"),
+    ("B2_H16_N4096_d128_causal", 2, 16, 4096, 128, True, "normal"),
+]
+BWD_WORKLOADS = [
+    ("B2_H16_N4096_d128_causal", 2, 16, 4096, 128, True),
+    ("B2_H16_N4096_d128_noncausal", 2, 16, 4096, 128, False),
+    ("B8_H16_N2048_d64_causal", 8, 16, 2048, 64, True),
+]
+
+
+def fwd_flops(B, H, N, d, causal):
+    return 4.0 * B * H * N * N * d * (0.5 if causal else 1.0)
+
+
+def bwd_flops(B, H, N, d, causal):
+    return 10.0 * B * H * N * N * d * (0.5 if causal else 1.0)
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {"bf16_tflops": float(p["bf16_tflops"]), "hbm_gbs": float(p["hbm_gbs"]),
+                "source": "measured (MEASURED_PEAKS.json, burst bf16 GEMM)"}
+    except Exception:
+        return dict(FALLBACK_PEAKS, source="fallback (no MEASURED_PEAKS.json)")
+
+
+def source_digest(files):
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel_key):
+    """DRAM bytes per launch from the committed ncu summary, if the kernel sources
+    have not changed since it was captured; else None."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)[kernel_key]
+        if rec["source_digest"] != source_digest(rec["sources"]):
+            return None
+        return float(rec["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, gpu_id):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+               "-lms", "50"]
+        if self.gpu_id is not None:
+            cmd += ["-i", self.gpu_id]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"],
+                    "samples": 0}
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, power, reasons = [], [], [], set()
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for name, val in zip(self.REASONS, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(power) if power else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ our arm
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+
+    import exact_attention_26_gb300 as fa
+    from exact_attention_26_gb300.inputs import boosted_qkv, normal_qkv
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    fa.load()
+    B, H, N, d, causal = (WORKLOAD[k] for k in ("B", "H", "N", "d", "causal"))
+    q_h, k_h, v_h, do_h = normal_qkv(B, H, N, d, seed=0, with_do=True)
+    q, k, v, do = (t.to(dev) for t in (q_h, k_h, v_h, do_h))
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    dq, dk, dv = (torch.empty(q.shape, dtype=torch.float32, device=dev) for _ in range(3))
+    ws = torch.empty(fa.fa_bwd_workspace_bytes(B, H, N, d), dtype=torch.uint8, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def fwd():
+        fa.forward(q, k, v, causal=causal, out=o, lse=lse)
+
+    def bwd():
+        fa.backward(q, k, v, o, lse, do, causal=causal, dq=dq, dk=dk, dv=dv, workspace=ws)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        fwd()
+        bwd()
+    torch.cuda.synchronize(dev)
+    status = fa.fa_device_status(None)
+    if status != 0:
+        raise RuntimeError(f"device status {fa.fa_status_string(status)} after warm-up")
+
+    gpu_id = None
+    try:
+        gpu_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        pass
+    sampler = ClockSampler(gpu_id)
+    sampler.start()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    wall0 = time.perf_counter()
+    for it in range(args.steps):
+        flush.zero_()  # L2 flush, outside the per-step events
+        evs[it][0].record(stream)
+        fwd()
+        evs[it][1].record(stream)
+        bwd()
+        evs[it][2].record(stream)
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    wall1 = time.perf_counter()
+    clocks = sampler.stop()
+    status = fa.fa_device_status(None)
+    if status != 0:
+        raise RuntimeError(f"device status {fa.fa_status_string(status)} in the timed region")
+
+    fwd_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    bwd_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    step_ms_local = sum(fwd_ms) / len(fwd_ms) + sum(bwd_ms) / len(bwd_ms)
+    step_ms = step_ms_local
+    if world > 1:
+        t = torch.tensor([step_ms_local], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        step_ms = float(t.item())
+    flops_step = fwd_flops(B, H, N, d, causal) + bwd_flops(B, H, N, d, causal)
+    value = flops_step * world / (step_ms * 1e-3) / 1e12
+
+    result = None
+    if rank == 0:
+        peaks = load_peaks()
+        f_ms = statistics.mean(fwd_ms)
+        b_ms = statistics.mean(bwd_ms)
+        if b_ms >= f_ms:
+            kern, kflops, kms = "fa_bwd (fa_bwd_pre_kernel + fa_bwd_kernel<128,causal>)", \
+                bwd_flops(B, H, N, d, causal), b_ms
+            traffic = recorded_traffic("fa_bwd_d128_causal_b2h16n4096")
+        else:
+            kern, kflops, kms = "fa_fwd_kernel<128,causal>", fwd_flops(B, H, N, d, causal), f_ms
+            traffic = recorded_traffic("fa_fwd_d128_causal_b2h16n4096")
+        achieved = kflops / (kms * 1e-3) / 1e12
+        result = {
+            "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_ms, 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": WORKLOAD_NAME, "B": B, "H": H, "N": N, "d": d,
+                       "causal": causal, "scale": 1.0 / math.sqrt(d),
+                       "inputs": "bf16(N(0,1)) q,k,v,dO from one torch CPU generator, seed 0",
+                       "l2": f"flushed between steps ({L2_FLUSH_BYTES >> 20} MiB write, outside "
+                             "the per-step CUDA events)",
+                       "per_rank": "each rank runs its own copy (independent batches)"},
+            "fwd_ms": round(f_ms, 5), "bwd_ms": round(b_ms, 5),
+            "fwd_tflops": round(fwd_flops(B, H, N, d, causal) / (f_ms * 1e-3) / 1e12, 2),
+            "bwd_tflops": round(bwd_flops(B, H, N, d, causal) / (b_ms * 1e-3) / 1e12, 2),
+            "wall_ms_per_step_incl_flush": round((wall1 - wall0) * 1e3 / args.steps, 5),
+            "roofline": {"bound": "tensor", "kernel": kern, "achieved": round(achieved, 2),
+                         "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                         "frac": round(achieved / peaks["bf16_tflops"], 4),
+                         "traffic": traffic, "peak_source": peaks["source"]},
+            "gpu_launches": 3 * args.steps,
+            "clocks": clocks,
+        }
+    # End-to-end through the public API with host buffers: H2D of q, k, v, dO from
+    # pinned memory, forward, backward, D2H of o, lse, dq, dk, dv, every step.
+    e2e = run_e2e(args, fa, torch, dev, (q_h, k_h, v_h, do_h), causal, flops_step, world)
+    if world > 1:
+        t = torch.tensor([e2e["ms"]], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e["ms"] = float(t.item())
+    if rank == 0:
+        result["e2e"] = {"value": round(flops_step * world / (e2e["ms"] * 1e-3) / 1e12, 2),
+                         "unit": UNIT, "h2d_bytes_per_step": e2e["h2d"],
+                         "d2h_bytes_per_step": e2e["d2h"], "ms_per_step": round(e2e["ms"], 5)}
+        if world == 1 and not args.no_extra:
+            result["forward_workloads"] = sweep_forward(fa, torch, dev, flush, normal_qkv,
+                                                        boosted_qkv, load_peaks())
+            result["backward_workloads"] = sweep_backward(fa, torch, dev, flush, normal_qkv,
+                                                          load_peaks())
+        if world == 1 and not args.no_cpu_baseline:
+            result["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
+        else:
+            result["cpu_baseline"] = None
+    return result
+
+
+def run_e2e(args, fa, torch, dev, host_inputs, causal, flops_step, world):
+    pin = [t.pin_memory() for t in host_inputs]
+    dq_, dk_, dv_ = (torch.empty(pin[0].shape, dtype=torch.float32, device=dev) for _ in range(3))
+    outs_h = [torch.empty(pin[0].shape, dtype=torch.bfloat16).pin_memory(),
+              torch.empty(pin[0].shape[:3], dtype=torch.float32).pin_memory()] + \
+             [torch.empty(pin[0].shape, dtype=torch.float32).pin_memory() for _ in range(3)]
+    dev_in = [torch.empty_like(t, device=dev) for t in pin]
+    B, H, N, d = pin[0].shape
+    ws = torch.empty(fa.fa_bwd_workspace_bytes(B, H, N, d), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        for dst, src in zip(dev_in, pin):
+            dst.copy_(src, non_blocking=True)
+        q, k, v, do = dev_in
+        o, lse = fa.forward(q, k, v, causal=causal)
+        g = fa.backward(q, k, v, o, lse, do, causal=causal, dq=dq_, dk=dk_, dv=dv_, workspace=ws)
+        for dst, src in zip(outs_h, (o, lse) + tuple(g)):
+            dst.copy_(src, non_blocking=True)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize(dev)
+    n = max(3, min(args.steps, 30))
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(n):
+        step()
+    b.record(stream)
+    b.synchronize()
+    h2d = sum(t.numel() * t.element_size() for t in pin)
+    d2h = sum(t.numel() * t.element_size() for t in outs_h)
+    return {"ms": a.elapsed_time(b) / n, "h2d": h2d, "d2h": d2h}
+
+
+def _time_call(torch, dev, fn, flush, iters=20, warm=3):
+    for _ in range(warm):
+        fn()
+    torch.cuda.synchronize(dev)
+    ts = []
+    for _ in range(iters):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        fn()
+        b.record()
+        b.synchronize()
+        ts.append(a.elapsed_time(b))
+    return statistics.median(ts)
+
+
+def sweep_forward(fa, torch, dev, flush, normal_qkv, boosted_qkv, peaks):
+    out = {}
+    for name, B, H, N, d, causal, kind in FWD_WORKLOADS:
+        gen = boosted_qkv if kind == "boosted" else normal_qkv
+        q, k, v = (t.to(dev) for t in gen(B, H, N, d, seed=0))
+        o = torch.empty_like(q)
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+        ms = _time_call(torch, dev, lambda: fa.forward(q, k, v, causal=causal, out=o, lse=lse),
+                        flush)
+        tf = fwd_flops(B, H, N, d, causal) / (ms * 1e-3) / 1e12
+        out[name] = {"ms": round(ms, 5), "tflops": round(tf, 2),
+                     "frac_of_peak": round(tf / peaks["bf16_tflops"], 4)}
+        del q, k, v, o, lse
+    return out
+
+
+def sweep_backward(fa, torch, dev, flush, normal_qkv, peaks):
+    out = {}
+    for name, B, H, N, d, causal in BWD_WORKLOADS:
+        q, k, v, do = (t.to(dev) for t in normal_qkv(B, H, N, d, seed=0, with_do=True))
+        o, lse = fa.forward(q, k, v, causal=causal)
+        g = [torch.empty(q.shape, dtype=torch.float32, device=dev) for _ in range(3)]
+        ws = torch.empty(fa.fa_bwd_workspace_bytes(B, H, N, d), dtype=torch.uint8, device=dev)
+        ms = _time_call(torch, dev, lambda: fa.backward(q, k, v, o, lse, do, causal=causal,
+                                                        dq=g[0], dk=g[1], dv=g[2], workspace=ws),
+                        flush)
+        tf = bwd_flops(B, H, N, d, causal) / (ms * 1e-3) / 1e12
+        out[name] = {"ms": round(ms, 5), "tflops": round(tf, 2),
+                     "frac_of_peak": round(tf / peaks["bf16_tflops"], 4)}
+        del q, k, v, do, o, lse, g, ws
+    return out
+
+
+# ------------------------------------------------------------------ oracle timing
+
+_HEAD0 = None
+
+
+def _head0_inputs():
+    """Head (0, 0) of the workload's seeded inputs, upcast to float64 (cached)."""
+    global _HEAD0
+    if _HEAD0 is None:
+        from exact_attention_26_gb300.inputs import normal_qkv, to_f64
+        B, H, N, d = (WORKLOAD[k] for k in ("B", "H", "N", "d"))
+        q, k, v, do = normal_qkv(B, H, N, d, seed=0, with_do=True)
+        sl = (slice(0, 1), slice(0, 1))
+        _HEAD0 = tuple(to_f64(t[sl]) for t in (q, k, v, do))
+    return _HEAD0
+
+
+def _oracle_sample(nrows):
+    """A bounded sample of the step on the CPU: forward and backward of `nrows`
+    seeded query rows of head (0, 0) of the workload.  Returns (seconds, flops, rows)."""
+    from exact_attention_26_gb300.inputs import sample_rows
+    from oracle import default as oracle_default
+
+    orc = oracle_default()
+    N, d, causal = WORKLOAD["N"], WORKLOAD["d"], WORKLOAD["causal"]
+    q, k, v, do = _head0_inputs()
+    rows = sample_rows(N, nrows, seed=2).numpy()
+    keys = (rows + 1) if causal else (N * (rows * 0 + 1))
+    flops = float(((4.0 + 10.0) * d * keys).sum())
+    t0 = time.perf_counter()
+    orc.fwd_rows(q, k, v, rows, causal=causal)
+    orc.bwd_rows(q, k, v, do, rows, causal=causal)
+    return time.perf_counter() - t0, flops, rows.size
+
+
+def _cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def _rows_for(seconds):
+    """Rows per sample so that one sample takes about `seconds` (two calibration passes)."""
+    n = 32
+    for _ in range(2):
+        t, _, n_done = _oracle_sample(n)
+        n = int(max(8, min(WORKLOAD["N"], n_done * seconds / max(t, 1e-3))))
+        if t > 0.25 * seconds:
+            break
+    return n
+
+
+def cpu_baseline(target_seconds):
+    _head0_inputs()
+    nrows = _rows_for(target_seconds)
+    secs, flops, n = _oracle_sample(nrows)
+    return {"value": round(flops / secs / 1e12, 6), "unit": UNIT, "cores": _cores(),
+            "kind": "oracle",
+            "sample": f"float64 oracle forward + backward of {n} seeded query rows of head (0,0) "
+                      f"of the workload ({secs:.1f} s on the host cores; same FLOP convention)"}
+
+
+def run_reference(args):
+    """The oracle as it stands, timed on the host cores: each step a bounded row
+    sample of the workload sized so the whole run stays within a few minutes."""
+    total_budget = 150.0
+    _head0_inputs()
+    nrows = _rows_for(total_budget / max(1, args.steps + args.warmup))
+    for _ in range(args.warmup):
+        _oracle_sample(nrows)
+    secs, flops = 0.0, 0.0
+    n = nrows
+    for _ in range(args.steps):
+        s, f, n = _oracle_sample(nrows)
+        secs += s
+        flops += f
+    value = flops / secs / 1e12
+    sample = (f"float64 oracle forward + backward of {n} seeded query rows of head (0,0) per "
+              f"step, {_cores()} host threads")
+    return {
+        "metric": METRIC, "value": round(value, 6), "unit": UNIT, "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(secs * 1e3 / args.steps, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD_NAME, **WORKLOAD,
+                   "inputs": "bf16(N(0,1)) q,k,v,dO from one torch CPU generator, seed 0"},
+        "impl": "reference",
+        "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": _cores(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="skip the per-workload forward/backward sweep")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    try:
+        result = run_ours(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+
+
+if __name__ == "__main__":
+    main()

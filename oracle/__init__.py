@@ -3,4 +3,4 @@
 Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline leg
 may import this package.  The CUDA library neither imports nor links it.
 """
-from .oracle import Oracle, bwd, default, default_threads, fwd, fwd_rows  # noqa: F401
+from .oracle import Oracle, bwd, bwd_rows, default, default_threads, fwd, fwd_rows  # noqa: F401

@@ -166,20 +166,24 @@ int oracle_fwd_rows(const double *q, const double *k, const double *v, const lon
     return rc;
 }
 
-/* Backward of query rows [row_begin, row_end) of head bh; dK, dV go to this
- * thread's partial buffers, dQ rows are owned by the thread and written directly. */
+/* Backward of query rows [row_begin, row_end) of head bh (or of rows[row_begin ..
+ * row_end) when a row list is given); dK, dV go to this thread's partial buffers,
+ * dQ rows are owned by the thread and written directly (row t of the list goes to
+ * dq row t in row-list mode). */
 static void *bwd_worker(void *arg) {
     job_t *jb = (job_t *)arg;
     long N = jb->N, d = jb->d;
     size_t head = (size_t)jb->bh * (size_t)N * (size_t)d;
     const double *Q = jb->q + head, *K = jb->k + head, *V = jb->v + head;
     const double *dO = jb->dout + head;
-    double *dQ = jb->dq + head;
+    double *dQ = jb->rows ? jb->dq + (size_t)jb->bh * (size_t)jb->nrows * (size_t)d
+                          : jb->dq + head;
     double *s = (double *)malloc(sizeof(double) * (size_t)(N > 0 ? N : 1));
     double *dp = (double *)malloc(sizeof(double) * (size_t)(N > 0 ? N : 1));
     memset(jb->dk_part, 0, sizeof(double) * (size_t)N * (size_t)d);
     memset(jb->dv_part, 0, sizeof(double) * (size_t)N * (size_t)d);
-    for (long i = jb->row_begin; i < jb->row_end; ++i) {
+    for (long t = jb->row_begin; t < jb->row_end; ++t) {
+        long i = jb->rows ? jb->rows[t] : t;
         long n = n_allowed(i, N, jb->causal);
         double l;
         score_row(Q + i * d, K, n, d, jb->scale, s, &l);
@@ -193,7 +197,7 @@ static void *bwd_worker(void *arg) {
             dp[j] = acc;     /* dP_ij */
             Di += s[j] * dp[j];
         }
-        double *dqi = dQ + i * d;
+        double *dqi = dQ + t * d;
         for (long c = 0; c < d; ++c) dqi[c] = 0.0;
         const double *qi = Q + i * d;
         for (long j = 0; j < n; ++j) {
@@ -213,13 +217,18 @@ static void *bwd_worker(void *arg) {
     return NULL;
 }
 
-/* Backward over every row.  dq, dk, dv: [BH][N][d]. */
-int oracle_bwd(const double *q, const double *k, const double *v, const double *dout,
-               double *dq, double *dk, double *dv, long BH, long N, long d, int causal,
-               double scale, int nthreads) {
-    if (BH < 0 || N < 0 || d < 1) return -2;
+/* Backward over the query rows `rows` (NULL: every row) of every head.
+ * dq: [BH][nrows][d] (or [BH][N][d]); dk, dv: [BH][N][d], the contributions of
+ * the selected rows only. */
+static int bwd_impl(const double *q, const double *k, const double *v, const double *dout,
+                    const long *rows, long nrows, double *dq, double *dk, double *dv, long BH,
+                    long N, long d, int causal, double scale, int nthreads) {
+    if (BH < 0 || N < 0 || d < 1 || nrows < 0) return -2;
+    for (long r = 0; rows && r < nrows; ++r)
+        if (rows[r] < 0 || rows[r] >= N) return -2;
+    long nwork = rows ? nrows : N;
     if (nthreads < 1) nthreads = 1;
-    if (nthreads > N) nthreads = (int)(N > 0 ? N : 1);
+    if (nthreads > nwork) nthreads = (int)(nwork > 0 ? nwork : 1);
     size_t hsz = (size_t)N * (size_t)d;
     double *parts = (double *)malloc(sizeof(double) * hsz * 2 * (size_t)nthreads + 1);
     job_t *jobs = (job_t *)malloc(sizeof(job_t) * (size_t)nthreads);
@@ -231,13 +240,14 @@ int oracle_bwd(const double *q, const double *k, const double *v, const double *
         base.q = q; base.k = k; base.v = v; base.dout = dout; base.dq = dq;
         base.BH = BH; base.N = N; base.d = d; base.causal = causal; base.scale = scale;
         base.bh = bh;
+        base.rows = rows; base.nrows = nrows;
         pthread_t *th = (pthread_t *)malloc(sizeof(pthread_t) * (size_t)nthreads);
         if (!th) { rc = -1; break; }
         int started = 0;
         for (int t = 0; t < nthreads; ++t) {
             jobs[t] = base;
-            jobs[t].row_begin = N * t / nthreads;
-            jobs[t].row_end = N * (t + 1) / nthreads;
+            jobs[t].row_begin = nwork * t / nthreads;
+            jobs[t].row_end = nwork * (t + 1) / nthreads;
             jobs[t].dk_part = parts + hsz * (size_t)(2 * t);
             jobs[t].dv_part = parts + hsz * (size_t)(2 * t + 1);
             if (pthread_create(&th[t], NULL, bwd_worker, &jobs[t]) != 0) { rc = -1; break; }
@@ -260,4 +270,19 @@ int oracle_bwd(const double *q, const double *k, const double *v, const double *
     free(parts);
     free(jobs);
     return rc;
+}
+
+/* Backward over every row.  dq, dk, dv: [BH][N][d]. */
+int oracle_bwd(const double *q, const double *k, const double *v, const double *dout,
+               double *dq, double *dk, double *dv, long BH, long N, long d, int causal,
+               double scale, int nthreads) {
+    return bwd_impl(q, k, v, dout, NULL, 0, dq, dk, dv, BH, N, d, causal, scale, nthreads);
+}
+
+/* Backward restricted to the query rows `rows` (the same rows in every head):
+ * dq: [BH][nrows][d]; dk, dv: [BH][N][d] hold those rows' contributions. */
+int oracle_bwd_rows(const double *q, const double *k, const double *v, const double *dout,
+                    const long *rows, long nrows, double *dq, double *dk, double *dv, long BH,
+                    long N, long d, int causal, double scale, int nthreads) {
+    return bwd_impl(q, k, v, dout, rows, nrows, dq, dk, dv, BH, N, d, causal, scale, nthreads);
 }

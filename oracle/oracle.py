@@ -46,6 +46,10 @@ class Oracle:
                                    ctypes.c_long, ctypes.c_long, ctypes.c_int, ctypes.c_double,
                                    ctypes.c_int]
         lib.oracle_bwd.restype = ctypes.c_int
+        lib.oracle_bwd_rows.argtypes = [_dp, _dp, _dp, _dp, _lp, ctypes.c_long, _dp, _dp, _dp,
+                                        ctypes.c_long, ctypes.c_long, ctypes.c_long, ctypes.c_int,
+                                        ctypes.c_double, ctypes.c_int]
+        lib.oracle_bwd_rows.restype = ctypes.c_int
         self.lib = lib
 
     @staticmethod
@@ -105,6 +109,24 @@ class Oracle:
             raise RuntimeError(f"oracle_bwd failed ({rc})")
         return dq, dk, dv
 
+    def bwd_rows(self, q, k, v, do, rows, causal=False, scale=None, nthreads=None):
+        """Backward restricted to query rows `rows`: dQ of those rows [B,H,R,d] and
+        their contributions to dK, dV [B,H,N,d]."""
+        q, k, v, do = self._f64(q), self._f64(k), self._f64(v), self._f64(do)
+        B, H, N, d = q.shape
+        rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64)).astype(np.dtype("l"))
+        scale = 1.0 / np.sqrt(d) if scale is None else float(scale)
+        R = rows.shape[0]
+        dq = np.empty((B, H, R, d), dtype=np.float64)
+        dk, dv = np.empty_like(q), np.empty_like(q)
+        rc = self.lib.oracle_bwd_rows(self._ptr(q), self._ptr(k), self._ptr(v), self._ptr(do),
+                                      rows.ctypes.data_as(_lp), R, self._ptr(dq), self._ptr(dk),
+                                      self._ptr(dv), B * H, N, d, int(bool(causal)), scale,
+                                      nthreads or default_threads())
+        if rc != 0:
+            raise RuntimeError(f"oracle_bwd_rows failed ({rc})")
+        return dq, dk, dv
+
 
 _default = None
 
@@ -126,3 +148,7 @@ def fwd_rows(*a, **kw):
 
 def bwd(*a, **kw):
     return default().bwd(*a, **kw)
+
+
+def bwd_rows(*a, **kw):
+    return default().bwd_rows(*a, **kw)

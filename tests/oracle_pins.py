@@ -333,6 +333,23 @@ def check_bwd_invariants(orc):
         _close(dv.sum(axis=2), do.sum(axis=2), 1e-11, f"sum dV (causal={causal})")
 
 
+def check_bwd_rows_partition(orc):
+    """Backward over a partition of the query rows: the dQ rows are those of the
+    full backward and the dK, dV contributions add up to the full dK, dV."""
+    r = _rng(16)
+    q, k, v, do = (r.standard_normal((1, 2, 41, 8)) for _ in range(4))
+    rows_a = np.array([0, 3, 7, 8, 20, 40])
+    rows_b = np.setdiff1d(np.arange(41), rows_a)
+    for causal in (False, True):
+        dq, dk, dv = orc.bwd(q, k, v, do, causal=causal, scale=0.5, nthreads=3)
+        qa, ka, va = orc.bwd_rows(q, k, v, do, rows_a, causal=causal, scale=0.5, nthreads=2)
+        qb, kb, vb = orc.bwd_rows(q, k, v, do, rows_b, causal=causal, scale=0.5, nthreads=4)
+        _close(qa, dq[:, :, rows_a], 1e-14, "bwd_rows dQ (a)")
+        _close(qb, dq[:, :, rows_b], 1e-14, "bwd_rows dQ (b)")
+        _close(ka + kb, dk, 1e-13, "bwd_rows dK partition")
+        _close(va + vb, dv, 1e-13, "bwd_rows dV partition")
+
+
 FORWARD_CHECKS = [
     check_rows_of_p_sum_to_one,
     check_identity_v_is_softmax,
@@ -351,5 +368,6 @@ BACKWARD_CHECKS = [
     check_bwd_finite_differences,
     check_bwd_torch_autograd,
     check_bwd_invariants,
+    check_bwd_rows_partition,
 ]
 ALL_CHECKS = FORWARD_CHECKS + BACKWARD_CHECKS
