@@ -79,6 +79,17 @@ def fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, H, N, d, causal, scale, workspa
                          scale, workspace, workspace_bytes, stream)
 
 
+def fa_bwd_noalloc(q, k, v, o, lse, dout, dq, dk, dv, B, H, N, d, causal, scale,
+                   stream) -> int:
+    """fa_bwd without a workspace: the library's fixed scratch array is used instead."""
+    fn = load().fa_bwd_noalloc
+    if fn.restype is not _int:
+        fn.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _int, _int, _int, _int, _int,
+                       ctypes.c_float, _vp]
+        fn.restype = _int
+    return fn(q, k, v, o, lse, dout, dq, dk, dv, B, H, N, d, int(bool(causal)), scale, stream)
+
+
 def fa_status_string(status: int) -> str:
     return load().fa_status_string(status).decode()
 

@@ -92,6 +92,32 @@ int fa_bwd(const void *q, const void *k, const void *v, const void *o, const flo
            const void *dout, float *dq, float *dk, float *dv, int B, int H, int N, int d,
            int causal, float scale, void *workspace, size_t workspace_bytes, void *stream);
 
+/*
+ * Backward pass that allocates nothing, for callers that cannot allocate device
+ * memory or pass a workspace: a host that reserves all device memory up front in
+ * its own pool and forbids side allocations, or a latency-critical loop where a
+ * cudaMalloc, which may synchronise the device, is not acceptable.  (The pages
+ * have no counterpart to this entry point; it is a deployment convenience.)
+ *
+ * Same arguments, results and errors as fa_bwd, minus the workspace.  Instead of
+ * a workspace it uses a scratch array of FA_NOALLOC_SCRATCH_BYTES compiled into
+ * the library; every GPU that loads the library holds that array until exit.
+ *   - Sizes whose fa_bwd_workspace_bytes(B, H, N, d) exceeds
+ *     FA_NOALLOC_SCRATCH_BYTES, i.e. B*H*roundup(N, 128) > 1,048,576 rows, return
+ *     FA_ERR_WORKSPACE before anything is launched.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress) while that device is current; make that first call
+ *     before any stream capture.
+ *   - Every call shares the one array; its contents on entry do not matter (each
+ *     call rewrites what it reads).  Calls that overlap on the GPU (different
+ *     streams, no ordering between them) race on it and give wrong results.
+ * Calls no cudaMalloc, cudaFree or other allocating routine.
+ */
+#define FA_NOALLOC_SCRATCH_BYTES ((size_t)8 << 20)
+int fa_bwd_noalloc(const void *q, const void *k, const void *v, const void *o,
+                   const float *lse, const void *dout, float *dq, float *dk, float *dv, int B,
+                   int H, int N, int d, int causal, float scale, void *stream);
+
 /* Static, human-readable name of a status code (never NULL). */
 const char *fa_status_string(int status);
 
