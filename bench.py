@@ -28,6 +28,8 @@ import subprocess
 import sys
 import time
 
+import numpy as np
+
 ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
@@ -371,37 +373,38 @@ def sweep_backward(fa, torch, dev, flush, normal_qkv, peaks):
 
 # ------------------------------------------------------------------ oracle timing
 
-_HEAD0 = None
+_INPUTS = None
 
 
-def _head0_inputs():
-    """Head (0, 0) of the workload's seeded inputs, upcast to float64 (cached)."""
-    global _HEAD0
-    if _HEAD0 is None:
-        from exact_attention_26_gb300.inputs import normal_qkv, to_f64
+def _workload_heads(nheads):
+    """The first `nheads` (batch, head) pairs of the workload's seeded inputs,
+    upcast to float64 as [1, nheads, N, d] arrays (the bf16 tensors are cached)."""
+    global _INPUTS
+    from exact_attention_26_gb300.inputs import normal_qkv, to_f64
+    if _INPUTS is None:
         B, H, N, d = (WORKLOAD[k] for k in ("B", "H", "N", "d"))
-        q, k, v, do = normal_qkv(B, H, N, d, seed=0, with_do=True)
-        sl = (slice(0, 1), slice(0, 1))
-        _HEAD0 = tuple(to_f64(t[sl]) for t in (q, k, v, do))
-    return _HEAD0
+        _INPUTS = tuple(t.reshape(1, B * H, N, d)
+                        for t in normal_qkv(B, H, N, d, seed=0, with_do=True))
+    return tuple(to_f64(t[:, :nheads]) for t in _INPUTS)
 
 
-def _oracle_sample(nrows):
+def _oracle_sample(nrows, nheads=1):
     """A bounded sample of the step on the CPU: forward and backward of `nrows`
-    seeded query rows of head (0, 0) of the workload.  Returns (seconds, flops, rows)."""
+    seeded query rows in each of the first `nheads` heads of the workload.
+    Returns (seconds, flops, rows, heads)."""
     from exact_attention_26_gb300.inputs import sample_rows
     from oracle import default as oracle_default
 
     orc = oracle_default()
     N, d, causal = WORKLOAD["N"], WORKLOAD["d"], WORKLOAD["causal"]
-    q, k, v, do = _head0_inputs()
+    q, k, v, do = _workload_heads(nheads)
     rows = sample_rows(N, nrows, seed=2).numpy()
-    keys = (rows + 1) if causal else (N * (rows * 0 + 1))
-    flops = float(((4.0 + 10.0) * d * keys).sum())
+    keys = (rows + 1) if causal else np.full(rows.shape, N)
+    flops = float(nheads * ((4.0 + 10.0) * d * keys).sum())
     t0 = time.perf_counter()
     orc.fwd_rows(q, k, v, rows, causal=causal)
     orc.bwd_rows(q, k, v, do, rows, causal=causal)
-    return time.perf_counter() - t0, flops, rows.size
+    return time.perf_counter() - t0, flops, rows.size, nheads
 
 
 def _cores():
@@ -411,44 +414,44 @@ def _cores():
         return os.cpu_count() or 1
 
 
-def _rows_for(seconds):
-    """Rows per sample so that one sample takes about `seconds` (two calibration passes)."""
-    n = 32
-    for _ in range(2):
-        t, _, n_done = _oracle_sample(n)
-        n = int(max(8, min(WORKLOAD["N"], n_done * seconds / max(t, 1e-3))))
-        if t > 0.25 * seconds:
-            break
-    return n
+def _sample_size(seconds):
+    """(rows, heads) so that one sample takes about `seconds`: rows first, then heads."""
+    max_heads = WORKLOAD["B"] * WORKLOAD["H"]
+    N = WORKLOAD["N"]
+    t, _, n, _ = _oracle_sample(min(512, N), 1)
+    rows = int(max(8, min(N, seconds * n / max(t, 1e-9))))
+    if rows < N:
+        return rows, 1
+    t_head, _, _, _ = _oracle_sample(N, 1)
+    return N, int(max(1, min(max_heads, round(seconds / max(t_head, 1e-9)))))
 
 
 def cpu_baseline(target_seconds):
-    _head0_inputs()
-    nrows = _rows_for(target_seconds)
-    secs, flops, n = _oracle_sample(nrows)
+    rows, heads = _sample_size(target_seconds)
+    secs, flops, n, h = _oracle_sample(rows, heads)
     return {"value": round(flops / secs / 1e12, 6), "unit": UNIT, "cores": _cores(),
             "kind": "oracle",
-            "sample": f"float64 oracle forward + backward of {n} seeded query rows of head (0,0) "
-                      f"of the workload ({secs:.1f} s on the host cores; same FLOP convention)"}
+            "sample": f"float64 oracle forward + backward of {n} seeded query rows in each of "
+                      f"{h} heads of the workload ({secs:.1f} s on {_cores()} host threads; "
+                      "same FLOP convention)"}
 
 
 def run_reference(args):
     """The oracle as it stands, timed on the host cores: each step a bounded row
     sample of the workload sized so the whole run stays within a few minutes."""
     total_budget = 150.0
-    _head0_inputs()
-    nrows = _rows_for(total_budget / max(1, args.steps + args.warmup))
+    rows, heads = _sample_size(total_budget / max(1, args.steps + args.warmup))
     for _ in range(args.warmup):
-        _oracle_sample(nrows)
+        _oracle_sample(rows, heads)
     secs, flops = 0.0, 0.0
-    n = nrows
+    n, h = rows, heads
     for _ in range(args.steps):
-        s, f, n = _oracle_sample(nrows)
+        s, f, n, h = _oracle_sample(rows, heads)
         secs += s
         flops += f
     value = flops / secs / 1e12
-    sample = (f"float64 oracle forward + backward of {n} seeded query rows of head (0,0) per "
-              f"step, {_cores()} host threads")
+    sample = (f"float64 oracle forward + backward of {n} seeded query rows in each of {h} "
+              f"heads per step, {_cores()} host threads")
     return {
         "metric": METRIC, "value": round(value, 6), "unit": UNIT, "n_gpus": 1,
         "steps": args.steps, "warmup": args.warmup,
