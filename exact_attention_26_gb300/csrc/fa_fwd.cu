@@ -1,34 +1,41 @@
 // Forward pass of exact attention for sm_103a.
 //
-// One CTA owns one tile of 128 query rows of one (batch, head) and streams the
-// K/V tiles of that head through shared memory ("FlashAttention-2: Why the
-// Attention Bottleneck Wasn't Where Everyone Was Looking", section "FA2 change
-// #2": outer loop over query blocks, inner loop over key/value blocks, the
-// softmax state kept on chip).  Per K/V tile j:
+// One CTA owns NT tiles of 128 query rows of one (batch, head) (NT = 2 for
+// d <= 128, 1 for d = 256) and streams the K/V tiles of that head through shared
+// memory once for all of them ("FlashAttention-2: Why the Attention Bottleneck
+// Wasn't Where Everyone Was Looking", section "FA2 change #2": outer loop over
+// query blocks, inner loop over key/value blocks, the softmax state kept on chip).
+// Per K/V tile j and query tile t:
 //
-//   S   = Q K_j^T                     tcgen05.mma, fp32 accumulator in TMEM
-//   m'  = max(m, rowmax(S) * scale)   one thread per row, the whole row in registers
-//   P   = exp(S * scale - m')         written back to TMEM as bf16 over S
-//   l'  = exp(m - m') l + rowsum(P)
-//   O~  = exp(m - m') O~ + P V_j      rescale in TMEM, then tcgen05.mma (A = P from TMEM)
+//   S_t = Q_t K_j^T                   tcgen05.mma, fp32 accumulator in TMEM
+//   m'  = max(m, rowmax(S_t) * scale) one thread per row, the whole row in registers
+//   P_t = exp(S_t * scale - m')       written back to TMEM as bf16 over S_t
+//   l'  = exp(m - m') l + rowsum(P_t)
+//   O_t = exp(m - m') O_t + P_t V_j   rescale in TMEM, then tcgen05.mma (A = P_t from TMEM)
 //
 // which is the online-softmax update of "FlashAttention: Move Less, Not Compute
 // Less", section "Tiling Is Easy; Softmax Couples the Entire Row", with the
 // division by l deferred to the end ("FA2 change #1").  Exponentials run in base
 // 2 with scale*log2(e) folded into one FMA.  The reference maximum m only moves
 // when the new row maximum exceeds it by more than 2^8 (kRescaleLog2); a stale
-// reference cancels exactly in O~/l and in L, and keeps every P <= 256.
+// reference cancels exactly in O/l and in L, and keeps every P <= 256.
 //
-// Warp roles (192 threads):
-//   warps 0-3  softmax: thread t owns query row t (TMEM lane t); rescale of O~;
-//              epilogue O = O~/l -> bf16, L = (m + log2 l) ln 2
-//   warp 4     TMA producer (lane 0): Q once, then K_j/V_j into a 2-stage ring
-//   warp 5     TMEM allocator; lane 0 issues every MMA and commit
+// With two tiles the MMA issue order per K/V tile is PV_0(j), S_0(j+1), PV_1(j),
+// S_1(j+1): while the softmax warps of one tile work, the tensor core runs the
+// other tile's products (the ping-pong of the course page "10 FlashAttention",
+// section 6, mapped onto one MMA-issuing thread and two softmax warpgroups).
 //
-// Causal tiles above the diagonal are never loaded; the diagonal and the ragged
-// tail (keys >= N) are masked to -inf element by element, other tiles take no
-// mask work ("The causal masking freebie").  Rows past N compute on zero-filled
-// Q rows and are not stored.
+// Warp roles (128 NT + 64 threads):
+//   warpgroup t (t < NT)  softmax of tile t: thread r owns query row r (TMEM lane
+//                         r); rescale of O_t; epilogue O = O_t/l -> bf16, L
+//   warp 4 NT             TMEM allocator; lane 0 issues every MMA and commit
+//   warp 4 NT + 1         TMA producer (lane 0): Q tiles, then K_j/V_j into a ring
+//
+// Causal tiles above the diagonal are never loaded or multiplied; the diagonal
+// and the ragged tail (keys >= N) are masked to -inf element by element, other
+// tiles take no mask work ("The causal masking freebie").  A tile whose first row
+// is past N is skipped; rows past N inside a tile compute on zero-filled Q rows
+// and are not stored.
 #include "fa_ptx.cuh"
 
 namespace fa {
@@ -39,43 +46,54 @@ constexpr float kLn2 = 0.69314718055994530942f;
 
 template <int D>
 struct FwdTile {
-    static constexpr int BM = 128;                  // query rows per tile
+    static constexpr int NT = (D <= 128) ? 2 : 1;     // 128-row query tiles per CTA
+    static constexpr int SB = (NT == 1) ? 2 : 1;      // S slots per tile (double buffer)
+    static constexpr int NS = NT * SB;                // S slots in TMEM
+    static constexpr int BM = 128;
+    static constexpr int ROWS = NT * BM;              // query rows per CTA
     static constexpr int BN = (D == 256) ? 64 : 128;  // keys per K/V tile
-    static constexpr int STAGES = 2;
-    static constexpr int NCH = D / 64;              // 128-byte swizzle chunks per row
+    static constexpr int KS = (D == 64) ? 4 : 3;      // K ring stages
+    static constexpr int VS = (D == 64) ? 4 : 2;      // V ring stages
+    static constexpr int NCH = D / 64;                // 128-byte swizzle chunks per row
     static constexpr uint32_t Q_CHUNK = BM * 128;
     static constexpr uint32_t KV_CHUNK = BN * 128;
-    static constexpr uint32_t Q_BYTES = BM * D * 2;
-    static constexpr uint32_t KV_BYTES = BN * D * 2;
-    // tensor memory columns
-    static constexpr uint32_t TM_S = 0;             // S (fp32, BN cols), P (bf16) over it
-    static constexpr uint32_t TM_O = 128;           // O~ (fp32, D cols)
-    static constexpr uint32_t TM_COLS = (128 + D <= 256) ? 256 : 512;
+    static constexpr uint32_t Q_BYTES = BM * D * 2;   // one query tile
+    static constexpr uint32_t KV_BYTES = BN * D * 2;  // one of K_j, V_j
+    // tensor memory columns: S slot u at BN u (fp32; P as bf16 over its first BN/2
+    // columns), then O_t (fp32, D columns) at BN NS + D t
+    static constexpr uint32_t TM_O0 = BN * NS;
+    static constexpr uint32_t TM_COLS = 512;
     // shared memory layout (offsets from a 1024-byte aligned base)
     static constexpr uint32_t OFF_Q = 0;
-    static constexpr uint32_t OFF_K = OFF_Q + Q_BYTES;
-    static constexpr uint32_t OFF_V = OFF_K + STAGES * KV_BYTES;
-    static constexpr uint32_t OFF_BAR = OFF_V + STAGES * KV_BYTES;
-    // barriers: q_full, kv_full[STAGES], kv_empty[STAGES], s_full, p_full, o_full
-    static constexpr int NBAR = 1 + 2 * STAGES + 3;
+    static constexpr uint32_t OFF_K = OFF_Q + NT * Q_BYTES;
+    static constexpr uint32_t OFF_V = OFF_K + KS * KV_BYTES;
+    static constexpr uint32_t OFF_BAR = OFF_V + VS * KV_BYTES;
+    // q_full[NT], k_full[KS], k_empty[KS], v_full[VS], v_empty[VS], s_full[NS],
+    // p_full[NT], o_full[NT], pv_done, mma_done
+    static constexpr int NBAR = NT + 2 * KS + 2 * VS + NS + 2 * NT + 2;
     static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr uint32_t SMEM_BYTES = OFF_MISC + 16 + 1024;
-    static constexpr int THREADS = 192;
+    static constexpr int WARP_MMA = 4 * NT;
+    static constexpr int WARP_LOAD = 4 * NT + 1;
+    static constexpr int THREADS = 128 * NT + 64;
 
     static_assert(D == 64 || D == 128 || D == 256, "head dim");
     static_assert(Q_CHUNK % 1024 == 0 && KV_CHUNK % 1024 == 0, "swizzle atoms must stay aligned");
-    static_assert(TM_O + D <= TM_COLS, "tensor memory budget");
+    static_assert(TM_O0 + NT * D <= TM_COLS, "tensor memory budget");
     static_assert(BN % 64 == 0, "P is packed 64 keys per tcgen05.st");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 };
 
 template <int D, bool CAUSAL>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(FwdTile<D>::THREADS, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, __nv_bfloat16 *__restrict__ out,
-                  float *__restrict__ lse, int N, int BH, int n_qblocks, float scale_log2,
+                  float *__restrict__ lse, int N, int BH, int n_cblocks, float scale_log2,
                   int *status, unsigned long long limit_ns) {
     using T = FwdTile<D>;
+    constexpr int NT = T::NT;
+    constexpr int KS = T::KS;
+    constexpr int VS = T::VS;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -84,41 +102,65 @@ __global__ void __launch_bounds__(192, 1)
     const uint32_t sQ = base + T::OFF_Q;
     const uint32_t sK = base + T::OFF_K;
     const uint32_t sV = base + T::OFF_V;
-    const uint32_t bar_q = base + T::OFF_BAR;
-    const uint32_t bar_kv_full = bar_q + 8;
-    const uint32_t bar_kv_empty = bar_kv_full + 8 * T::STAGES;
-    const uint32_t bar_s_full = bar_kv_empty + 8 * T::STAGES;
-    const uint32_t bar_p_full = bar_s_full + 8;
-    const uint32_t bar_o_full = bar_p_full + 8;
+    const uint32_t bar_q_full = base + T::OFF_BAR;      // [NT]
+    const uint32_t bar_k_full = bar_q_full + 8 * NT;     // [KS]
+    const uint32_t bar_k_empty = bar_k_full + 8 * KS;    // [KS]
+    const uint32_t bar_v_full = bar_k_empty + 8 * KS;    // [VS]
+    const uint32_t bar_v_empty = bar_v_full + 8 * VS;    // [VS]
+    const uint32_t bar_s_full = bar_v_empty + 8 * VS;    // [NS]
+    const uint32_t bar_p_full = bar_s_full + 8 * T::NS;  // [NT]
+    const uint32_t bar_o_full = bar_p_full + 8 * NT;     // [NT]
+    const uint32_t bar_pv_done = bar_o_full + 8 * NT;    // one tile, two S slots only
+    const uint32_t bar_mma_done = bar_pv_done + 8;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + T::OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(gbase + T::OFF_MISC + 4);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
-    // Tile of this CTA.  Causal: the longest rows (largest q-block) go first.
+    // Work of this CTA: ROWS query rows of one head.  Causal: the longest rows
+    // (largest block index) are issued first.
     const int bh = blockIdx.x % BH;
-    const int qb = CAUSAL ? (n_qblocks - 1 - (int)(blockIdx.x / BH)) : (int)(blockIdx.x / BH);
+    const int cb = CAUSAL ? (n_cblocks - 1 - (int)(blockIdx.x / BH)) : (int)(blockIdx.x / BH);
     const int n_kv_all = (N + T::BN - 1) / T::BN;
-    const int n_kv = CAUSAL ? min(n_kv_all, ((qb + 1) * T::BM + T::BN - 1) / T::BN) : n_kv_all;
+    int n_kv[NT];  // K/V tiles each query tile visits (0: tile entirely past N)
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+        const int row0 = cb * T::ROWS + t * T::BM;
+        if (row0 >= N)
+            n_kv[t] = 0;
+        else
+            n_kv[t] = CAUSAL ? min(n_kv_all, (row0 + T::BM + T::BN - 1) / T::BN) : n_kv_all;
+    }
+    int n_max = 0;
+#pragma unroll
+    for (int t = 0; t < NT; ++t) n_max = max(n_max, n_kv[t]);
 
     if (threadIdx.x == 0) {
-        mbar_init(bar_q, 1);
-        for (int s = 0; s < T::STAGES; ++s) {
-            mbar_init(bar_kv_full + 8 * s, 1);
-            mbar_init(bar_kv_empty + 8 * s, 1);
+        for (int t = 0; t < NT; ++t) {
+            mbar_init(bar_q_full + 8 * t, 1);
+            mbar_init(bar_p_full + 8 * t, 128);
+            mbar_init(bar_o_full + 8 * t, 1);
         }
-        mbar_init(bar_s_full, 1);
-        mbar_init(bar_p_full, 128);
-        mbar_init(bar_o_full, 1);
+        for (int u = 0; u < T::NS; ++u) mbar_init(bar_s_full + 8 * u, 1);
+        for (int s = 0; s < KS; ++s) {
+            mbar_init(bar_k_full + 8 * s, 1);
+            mbar_init(bar_k_empty + 8 * s, 1);
+        }
+        for (int s = 0; s < VS; ++s) {
+            mbar_init(bar_v_full + 8 * s, 1);
+            mbar_init(bar_v_empty + 8 * s, 1);
+        }
+        mbar_init(bar_pv_done, 1);
+        mbar_init(bar_mma_done, 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
-    if (warp == 5) {
+    if (warp == T::WARP_MMA) {
         tmem_alloc(smem_u32(tmem_slot), T::TM_COLS);
         tmem_relinquish();
     }
-    if (warp == 4 && lane == 0) {
+    if (warp == T::WARP_LOAD && lane == 0) {
         tma_prefetch_desc(&tm_q);
         tma_prefetch_desc(&tm_k);
         tma_prefetch_desc(&tm_v);
@@ -129,94 +171,196 @@ __global__ void __launch_bounds__(192, 1)
     const uint32_t tmem = *tmem_slot;
     const Guard g{status, abort_flag, limit_ns};
 
-    if (warp == 4) {
+    if (warp == T::WARP_LOAD) {
         // ------------------------------------------------------- TMA producer
+        // Order: Q_0, K_0, (other Q tiles), then K_{i} ahead of V_{i-1}, since S
+        // needs K one step before PV needs V.
         if (lane == 0) {
-            mbar_arrive_expect_tx(bar_q, T::Q_BYTES);
-            for (int c = 0; c < T::NCH; ++c)
-                tma_load_3d(sQ + c * T::Q_CHUNK, &tm_q, bar_q, c * 64, qb * T::BM, bh);
-            int issued = 0;
-            for (int j = 0; j < n_kv; ++j) {
-                const int s = j % T::STAGES;
-                if (j >= T::STAGES &&
-                    !mbar_wait(bar_kv_empty + 8 * s, ((j / T::STAGES) - 1) & 1, g,
-                               SITE_FWD_LOAD_KV_EMPTY))
-                    break;
-                mbar_arrive_expect_tx(bar_kv_full + 8 * s, 2 * T::KV_BYTES);
-                for (int c = 0; c < T::NCH; ++c) {
-                    tma_load_3d(sK + s * T::KV_BYTES + c * T::KV_CHUNK, &tm_k, bar_kv_full + 8 * s,
+            auto load_q = [&](int t) {
+                mbar_arrive_expect_tx(bar_q_full + 8 * t, T::Q_BYTES);
+                for (int c = 0; c < T::NCH; ++c)
+                    tma_load_3d(sQ + t * T::Q_BYTES + c * T::Q_CHUNK, &tm_q, bar_q_full + 8 * t,
+                                c * 64, cb * T::ROWS + t * T::BM, bh);
+            };
+            auto load_kv = [&](const CUtensorMap *map, uint32_t ring, uint32_t full, int stage,
+                               int j) {
+                mbar_arrive_expect_tx(full + 8 * stage, T::KV_BYTES);
+                for (int c = 0; c < T::NCH; ++c)
+                    tma_load_3d(ring + stage * T::KV_BYTES + c * T::KV_CHUNK, map, full + 8 * stage,
                                 c * 64, j * T::BN, bh);
-                    tma_load_3d(sV + s * T::KV_BYTES + c * T::KV_CHUNK, &tm_v, bar_kv_full + 8 * s,
-                                c * 64, j * T::BN, bh);
+            };
+            load_q(0);
+            int k_issued = 0, v_issued = 0;
+            bool ok = true;
+            for (int i = 0; ok && i <= n_max; ++i) {
+                if (i < n_max) {
+                    const int ks = i % KS;
+                    if (i >= KS && !mbar_wait(bar_k_empty + 8 * ks, ((i / KS) - 1) & 1, g,
+                                              SITE_FWD_LOAD_KV_EMPTY)) {
+                        ok = false;
+                        break;
+                    }
+                    load_kv(&tm_k, sK, bar_k_full, ks, i);
+                    ++k_issued;
+                    if (i == 0)
+                        for (int t = 1; t < NT; ++t)
+                            if (n_kv[t] > 0) load_q(t);
                 }
-                ++issued;
+                if (i >= 1) {
+                    const int j = i - 1;
+                    const int vs = j % VS;
+                    if (j >= VS && !mbar_wait(bar_v_empty + 8 * vs, ((j / VS) - 1) & 1, g,
+                                              SITE_FWD_LOAD_KV_EMPTY)) {
+                        ok = false;
+                        break;
+                    }
+                    load_kv(&tm_v, sV, bar_v_full, vs, j);
+                    ++v_issued;
+                }
             }
             if (*abort_flag) {
                 // Let the copies already in flight land before the CTA exits.
                 volatile int never = 0;
                 const Guard g2{status, &never, limit_ns / 4};
-                mbar_wait(bar_q, 0, g2, SITE_FWD_DRAIN);
-                for (int j = (issued > T::STAGES ? issued - T::STAGES : 0); j < issued; ++j)
-                    mbar_wait(bar_kv_full + 8 * (j % T::STAGES), (j / T::STAGES) & 1, g2,
-                              SITE_FWD_DRAIN);
+                for (int t = 0; t < NT; ++t)
+                    if (n_kv[t] > 0 && (t == 0 || k_issued > 0))
+                        mbar_wait(bar_q_full + 8 * t, 0, g2, SITE_FWD_DRAIN);
+                for (int j = (k_issued > KS ? k_issued - KS : 0); j < k_issued; ++j)
+                    mbar_wait(bar_k_full + 8 * (j % KS), (j / KS) & 1, g2, SITE_FWD_DRAIN);
+                for (int j = (v_issued > VS ? v_issued - VS : 0); j < v_issued; ++j)
+                    mbar_wait(bar_v_full + 8 * (j % VS), (j / VS) & 1, g2, SITE_FWD_DRAIN);
             }
         }
-    } else if (warp == 5) {
+    } else if (warp == T::WARP_MMA) {
         // ------------------------------------------------------- MMA issuer
         if (lane == 0) {
             constexpr uint32_t kIdescS = idesc_bf16_f32(128, T::BN, false, false);
             constexpr uint32_t kIdescO = idesc_bf16_f32(128, D, false, true);
-            bool ok = mbar_wait(bar_q, 0, g, SITE_FWD_MMA_Q);
-            for (int j = 0; ok && j < n_kv; ++j) {
-                const int s = j % T::STAGES;
-                if (!mbar_wait(bar_kv_full + 8 * s, (j / T::STAGES) & 1, g, SITE_FWD_MMA_KV_FULL)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                const uint32_t k_tile = sK + s * T::KV_BYTES;
-                // S = Q K_j^T: M = 128, N = BN, K = D in steps of 16 (32 bytes).
+            // S slot u = Q_t K_j^T from K stage ks: M = 128, N = BN, K = D.
+            auto issue_s = [&](int t, int u, int ks_stage) {
+                const uint32_t q_tile = sQ + t * T::Q_BYTES;
+                const uint32_t k_tile = sK + ks_stage * T::KV_BYTES;
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks) {
                     const uint32_t koff = (ks & 3) * 32;  // 16 bf16 = 32 bytes per K step
-                    const uint64_t a = sdesc_sw128(sQ + (ks >> 2) * T::Q_CHUNK + koff, 16, 1024);
+                    const uint64_t a = sdesc_sw128(q_tile + (ks >> 2) * T::Q_CHUNK + koff, 16, 1024);
                     const uint64_t b = sdesc_sw128(k_tile + (ks >> 2) * T::KV_CHUNK + koff, 16, 1024);
-                    mma_ss(tmem + T::TM_S, a, b, kIdescS, ks > 0 ? 1u : 0u);
+                    mma_ss(tmem + T::BN * u, a, b, kIdescS, ks > 0 ? 1u : 0u);
                 }
-                tc_commit(bar_s_full);
-                if (!mbar_wait(bar_p_full, j & 1, g, SITE_FWD_MMA_P_FULL)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                // O~ += P V_j: M = 128, N = D, K = BN; P from TMEM, V MN-major in smem.
-                const uint32_t v_tile = sV + s * T::KV_BYTES;
+                tc_commit(bar_s_full + 8 * u);
+            };
+            // O_t += P V from S slot u and V stage vs: M = 128, N = D, K = BN.
+            auto issue_pv = [&](int t, int u, int vs, bool first) {
+                const uint32_t v_tile = sV + vs * T::KV_BYTES;
 #pragma unroll
                 for (int ks = 0; ks < T::BN / 16; ++ks) {
                     const uint64_t b = sdesc_sw128(v_tile + ks * 2048, T::KV_CHUNK, 1024);
-                    mma_ts(tmem + T::TM_O, tmem + T::TM_S + ks * 8, b, kIdescO,
-                           (j > 0 || ks > 0) ? 1u : 0u);
+                    mma_ts(tmem + T::TM_O0 + D * t, tmem + T::BN * u + ks * 8, b, kIdescO,
+                           (!first || ks > 0) ? 1u : 0u);
                 }
-                tc_commit(bar_kv_empty + 8 * s);
+            };
+            auto wait_k = [&](int j) {
+                const bool r = mbar_wait(bar_k_full + 8 * (j % KS), (j / KS) & 1, g,
+                                         SITE_FWD_MMA_KV_FULL);
+                tc_fence_after();
+                return r;
+            };
+            auto wait_v = [&](int j) {
+                const bool r = mbar_wait(bar_v_full + 8 * (j % VS), (j / VS) & 1, g,
+                                         SITE_FWD_MMA_KV_FULL);
+                tc_fence_after();
+                return r;
+            };
+            bool ok = wait_k(0);
+            if constexpr (T::SB == 1) {
+                // NT tiles, one S slot each: PV_0(j), S_0(j+1), PV_1(j), S_1(j+1), ...
+                for (int t = 0; ok && t < NT; ++t) {
+                    if (n_kv[t] == 0) continue;
+                    ok = mbar_wait(bar_q_full + 8 * t, 0, g, SITE_FWD_MMA_Q);
+                    tc_fence_after();
+                    if (ok) issue_s(t, t, 0);
+                }
+                if (ok) tc_commit(bar_k_empty);
+                for (int j = 0; ok && j < n_max; ++j) {
+                    int last_pv = 0, last_s = -1;
+#pragma unroll
+                    for (int t = 0; t < NT; ++t) {
+                        if (j < n_kv[t]) last_pv = t;
+                        if (j + 1 < n_kv[t]) last_s = t;
+                    }
+                    bool v_ready = false, k_ready = false;
+#pragma unroll
+                    for (int t = 0; t < NT; ++t) {
+                        if (!ok || j >= n_kv[t]) continue;
+                        ok = mbar_wait(bar_p_full + 8 * t, j & 1, g, SITE_FWD_MMA_P_FULL);
+                        tc_fence_after();
+                        if (ok && !v_ready) ok = v_ready = wait_v(j);
+                        if (!ok) break;
+                        issue_pv(t, t, j % VS, j == 0);
+                        if (t == last_pv) tc_commit(bar_v_empty + 8 * (j % VS));
+                        if (j + 1 < n_kv[t]) {
+                            if (!k_ready) ok = k_ready = wait_k(j + 1);
+                            if (!ok) break;
+                            issue_s(t, t, (j + 1) % KS);
+                            if (t == last_s) tc_commit(bar_k_empty + 8 * ((j + 1) % KS));
+                        } else {
+                            tc_commit(bar_o_full + 8 * t);  // O_t is final once this fires
+                        }
+                    }
+                }
+            } else {
+                // One tile, two S slots: S(j+2) is issued right after PV(j) frees slot j&1,
+                // so the tensor core computes it while the softmax works on S(j+1).
+                const int n = n_kv[0];
+                ok = ok && mbar_wait(bar_q_full, 0, g, SITE_FWD_MMA_Q);
+                tc_fence_after();
+                if (ok) {
+                    issue_s(0, 0, 0);
+                    tc_commit(bar_k_empty);
+                }
+                if (ok && n > 1 && (ok = wait_k(1))) {
+                    issue_s(0, 1, 1 % KS);
+                    tc_commit(bar_k_empty + 8 * (1 % KS));
+                }
+                for (int j = 0; ok && j < n; ++j) {
+                    ok = mbar_wait(bar_p_full, j & 1, g, SITE_FWD_MMA_P_FULL);
+                    tc_fence_after();
+                    if (ok) ok = wait_v(j);
+                    if (!ok) break;
+                    issue_pv(0, j & 1, j % VS, j == 0);
+                    tc_commit(bar_v_empty + 8 * (j % VS));
+                    tc_commit(bar_pv_done);
+                    if (j + 2 < n) {
+                        if (!(ok = wait_k(j + 2))) break;
+                        issue_s(0, j & 1, (j + 2) % KS);
+                        tc_commit(bar_k_empty + 8 * ((j + 2) % KS));
+                    }
+                }
+                if (ok) tc_commit(bar_o_full);
             }
             // Fires once every MMA issued above has completed (normal or aborted run).
-            tc_commit(bar_o_full);
+            tc_commit(bar_mma_done);
             volatile int never = 0;
             const Guard g2{status, &never, limit_ns};
-            mbar_wait(bar_o_full, 0, g2, SITE_FWD_DRAIN);
+            mbar_wait(bar_mma_done, 0, g2, SITE_FWD_DRAIN);
         }
     } else {
-        // ------------------------------------------------------- softmax warps
-        const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-        const uint32_t t_s = tmem + lane_base + T::TM_S;
-        const uint32_t t_o = tmem + lane_base + T::TM_O;
-        const int row = threadIdx.x;
-        const int q_idx = qb * T::BM + row;
+        // ------------------------------------------------------- softmax warpgroups
+        const int t = warp >> 2;  // query tile of this warpgroup
+        const int r = threadIdx.x & 127;
+        const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+        const uint32_t t_o = tmem + lane_base + T::TM_O0 + D * t;
+        const int row0 = cb * T::ROWS + t * T::BM;
+        const int q_idx = row0 + r;
+        const int n_it = n_kv[t];
         float m_ref = -INFINITY;  // reference max, base-2 scaled units
         float l = 0.f;
         bool ok = true;
-        for (int j = 0; j < n_kv; ++j) {
-            ok = mbar_wait_warp(bar_s_full, j & 1, g, SITE_FWD_SOFTMAX_S_FULL);
+        for (int j = 0; j < n_it; ++j) {
+            const int u = (T::SB == 1) ? t : (j & 1);                 // S slot
+            const uint32_t par = (T::SB == 1) ? (j & 1) : ((j >> 1) & 1);
+            const uint32_t t_s = tmem + lane_base + T::BN * u;
+            ok = mbar_wait_warp(bar_s_full + 8 * u, par, g, SITE_FWD_SOFTMAX_S_FULL);
             if (!ok) break;
             tc_fence_after();
             uint32_t sr[T::BN / 32][32];
@@ -231,7 +375,7 @@ __global__ void __launch_bounds__(192, 1)
                 for (int e = 0; e < 32; ++e) s[c * 32 + e] = __uint_as_float(sr[c][e]);
 
             const int kv0 = j * T::BN;
-            const bool need_mask = (kv0 + T::BN > N) || (CAUSAL && kv0 + T::BN - 1 > qb * T::BM);
+            const bool need_mask = (kv0 + T::BN > N) || (CAUSAL && kv0 + T::BN - 1 > row0);
             if (need_mask) {
                 const int lim = CAUSAL ? min(N, q_idx + 1) : N;  // keys [0, lim) are visible
 #pragma unroll
@@ -248,8 +392,33 @@ __global__ void __launch_bounds__(192, 1)
                 alpha = ex2(m_ref - m_tile);
                 m_ref = m_tile;
             }
+            const float neg_m = -m_ref;
+            float sum = 0.f;
+#pragma unroll
+            for (int c = 0; c < T::BN; ++c) {
+                s[c] = ex2(fmaf(s[c], scale_log2, neg_m));
+                sum += s[c];
+            }
+            l = l * alpha + sum;
+            // P as bf16 pairs into the first BN/2 columns of the S slot.
+#pragma unroll
+            for (int c = 0; c < T::BN / 64; ++c) {
+                uint32_t pk[32];
+#pragma unroll
+                for (int e = 0; e < 32; ++e) pk[e] = pack_bf16(s[c * 64 + 2 * e], s[c * 64 + 2 * e + 1]);
+                tmem_st32(t_s + c * 32, pk);
+            }
             if (j > 0 && __any_sync(0xffffffffu, move)) {
-                // O~ <- alpha O~ for this warp's 32 rows (alpha = 1 on rows that kept m).
+                // O_t <- alpha O_t for this warp's 32 rows (alpha = 1 on rows that kept m),
+                // after P is stored so the S registers are free.  PV(j-1) must be
+                // complete: with one slot per tile S(j) was issued after it; with two
+                // slots it is awaited here.  PV(j) waits for the arrive below.
+                if (T::SB == 2 && !mbar_wait_warp(bar_pv_done, (j - 1) & 1, g,
+                                                  SITE_FWD_SOFTMAX_S_FULL)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
 #pragma unroll 1
                 for (int c = 0; c < D / 32; ++c) {
                     uint32_t o[32];
@@ -260,28 +429,12 @@ __global__ void __launch_bounds__(192, 1)
                     tmem_st32(t_o + c * 32, o);
                 }
             }
-            const float neg_m = -m_ref;
-            float sum = 0.f;
-#pragma unroll
-            for (int c = 0; c < T::BN; ++c) {
-                s[c] = ex2(fmaf(s[c], scale_log2, neg_m));
-                sum += s[c];
-            }
-            l = l * alpha + sum;
-            // P as bf16 pairs into the first BN/2 columns of S.
-#pragma unroll
-            for (int c = 0; c < T::BN / 64; ++c) {
-                uint32_t pk[32];
-#pragma unroll
-                for (int e = 0; e < 32; ++e) pk[e] = pack_bf16(s[c * 64 + 2 * e], s[c * 64 + 2 * e + 1]);
-                tmem_st32(t_s + c * 32, pk);
-            }
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(bar_p_full);
+            mbar_arrive(bar_p_full + 8 * t);
         }
         // ------------------------------------------------------- epilogue
-        ok = ok && mbar_wait_warp(bar_o_full, 0, g, SITE_FWD_EPILOGUE_O_FULL);
+        ok = ok && n_it > 0 && mbar_wait_warp(bar_o_full + 8 * t, 0, g, SITE_FWD_EPILOGUE_O_FULL);
         if (ok) {
             tc_fence_after();
             const float inv_l = 1.f / l;
@@ -305,12 +458,13 @@ __global__ void __launch_bounds__(192, 1)
             }
             if (q_idx < N) lse[(size_t)bh * (size_t)N + q_idx] = (m_ref + lg2(l)) * kLn2;
         }
+        tmem_wait_st();  // an aborted iteration may leave a store in flight
     }
 
     __syncwarp();
     tc_fence_before();
     __syncthreads();
-    if (warp == 5) {
+    if (warp == T::WARP_MMA) {
         tc_fence_after();
         tmem_dealloc(tmem, T::TM_COLS);
     }
@@ -323,12 +477,12 @@ int launch_fwd_t(const FwdParams &p, cudaStream_t stream) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)T::SMEM_BYTES);
     if (e != cudaSuccess) return FA_ERR_CUDA;
-    const int n_qblocks = (p.N + T::BM - 1) / T::BM;
-    const long long grid = (long long)n_qblocks * p.BH;
+    const int n_cblocks = (p.N + T::ROWS - 1) / T::ROWS;
+    const long long grid = (long long)n_cblocks * p.BH;
     if (grid > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
     kern<<<(unsigned)grid, T::THREADS, T::SMEM_BYTES, stream>>>(
         p.tm_q, p.tm_k, p.tm_v, reinterpret_cast<__nv_bfloat16 *>(p.o), p.lse, p.N, p.BH,
-        n_qblocks, p.scale_log2, p.status, p.limit_ns);
+        n_cblocks, p.scale_log2, p.status, p.limit_ns);
     return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
