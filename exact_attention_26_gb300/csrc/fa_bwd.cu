@@ -513,6 +513,372 @@ __global__ void __launch_bounds__(320, 1)
     }
 }
 
+// ---------------------------------------------------------------- d = 128 kernel
+//
+// Same products as fa_bwd_kernel, scheduled so the tensor core never waits for
+// the P^T/dS^T warps.  Tensor memory (512 columns): dV [0,128), dK [128,256),
+// S^T [256,320), dP^T [320,384), PD [384,448) holding bf16 P^T (first 32
+// columns) and dS^T (last 32), dQ^T [448,512).  Because P^T and dS^T go to their
+// own region, the next block's S^T and dP^T can be issued as soon as the compute
+// warps have READ the current ones (st_free), and they run on the tensor core
+// while the compute warps work; the dV/dK products of block i release PD for
+// block i+1 (pd_free).  Per block the MMA thread issues
+//   S^T(i+1), dP^T(i+1)  |  dV(i), dK(i)  |  dQ^T(i)
+// Two compute warpgroups split the 64 query columns of a block.
+struct Bwd128 {
+    static constexpr int D = 128;
+    static constexpr int BN = 128;
+    static constexpr int BQ = 64;
+    static constexpr int NCH = 2;
+    static constexpr int QS = 4;                        // Q/dO/L/D ring stages
+    static constexpr uint32_t K_CHUNK = BN * 128;
+    static constexpr uint32_t Q_CHUNK = BQ * 128;
+    static constexpr uint32_t KV_BYTES = BN * D * 2;
+    static constexpr uint32_t Q_BYTES = BQ * D * 2;
+    static constexpr uint32_t DS_BYTES = BQ * BN * 2;   // dS^T, [128 keys][64 queries] bf16
+    static constexpr uint32_t VEC_BYTES = BQ * 4;
+    static constexpr uint32_t TM_DV = 0, TM_DK = 128, TM_ST = 256, TM_DPT = 320, TM_PD = 384,
+                              TM_DQ = 448, TM_COLS = 512;
+    static constexpr uint32_t OFF_K = 0;
+    static constexpr uint32_t OFF_V = OFF_K + KV_BYTES;
+    static constexpr uint32_t OFF_Q = OFF_V + KV_BYTES;
+    static constexpr uint32_t OFF_DO = OFF_Q + QS * Q_BYTES;
+    static constexpr uint32_t OFF_DS = OFF_DO + QS * Q_BYTES;
+    static constexpr uint32_t OFF_L2 = OFF_DS + DS_BYTES;  // one dS^T buffer
+    static constexpr uint32_t OFF_DELTA = OFF_L2 + QS * VEC_BYTES;
+    static constexpr uint32_t OFF_BAR = OFF_DELTA + QS * VEC_BYTES;
+    // kv_full, q_full[QS], q_empty[QS], s_full, st_free, ds_full, pd_free, dq_full,
+    // dq_empty, done (dq_full also tells the compute warps that dS^T smem is free)
+    static constexpr int NBAR = 1 + 2 * QS + 7;
+    static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
+    static constexpr uint32_t SMEM_BYTES = OFF_MISC + 16 + 1024;
+    static constexpr int THREADS = 448;  // compute 0-7, dQ readout 8-11, TMA 12, MMA 13
+    static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+    static_assert(Q_CHUNK % 1024 == 0 && DS_BYTES % 1024 == 0, "swizzle atoms must stay aligned");
+};
+
+template <bool CAUSAL>
+__global__ void __launch_bounds__(448, 1)
+    fa_bwd_kernel_d128(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                       const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                       const float *__restrict__ ws_lse2, const float *__restrict__ ws_delta,
+                       float *__restrict__ dq, float *__restrict__ dk, float *__restrict__ dv, int N,
+                       int Npad, int BH, float scale, float scale_log2, int *status,
+                       unsigned long long limit_ns) {
+    using T = Bwd128;
+    constexpr int BQ = T::BQ, QS = T::QS, D = T::D;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *gbase = smem_raw + (base - raw);
+
+    const uint32_t sK = base + T::OFF_K, sV = base + T::OFF_V;
+    const uint32_t sQ = base + T::OFF_Q, sDO = base + T::OFF_DO;
+    const uint32_t sDS = base + T::OFF_DS;
+    const uint32_t sL2 = base + T::OFF_L2, sDelta = base + T::OFF_DELTA;
+    const uint32_t bar = base + T::OFF_BAR;
+    const uint32_t bar_kv_full = bar;
+    const uint32_t bar_q_full = bar + 8;                 // [QS]
+    const uint32_t bar_q_empty = bar_q_full + 8 * QS;     // [QS]
+    const uint32_t bar_s_full = bar_q_empty + 8 * QS;
+    const uint32_t bar_st_free = bar_s_full + 8;
+    const uint32_t bar_ds_full = bar_s_full + 16;
+    const uint32_t bar_pd_free = bar_s_full + 24;
+    const uint32_t bar_dq_full = bar_s_full + 32;
+    const uint32_t bar_dq_empty = bar_s_full + 40;
+    const uint32_t bar_done = bar_s_full + 48;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + T::OFF_MISC);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(gbase + T::OFF_MISC + 4);
+    const float *l2_f = reinterpret_cast<const float *>(gbase + T::OFF_L2);
+    const float *delta_f = reinterpret_cast<const float *>(gbase + T::OFF_DELTA);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    // Causal: key block 0 has the most query blocks, so low blockIdx = key block first.
+    const int bh = blockIdx.x % BH;
+    const int kv0 = (blockIdx.x / BH) * T::BN;
+    const int n_qb = (N + BQ - 1) / BQ;
+    const int i_start = CAUSAL ? kv0 / BQ : 0;
+    const int n_it = n_qb - i_start;
+
+    if (threadIdx.x == 0) {
+        mbar_init(bar_kv_full, 1);
+        for (int s = 0; s < QS; ++s) {
+            mbar_init(bar_q_full + 8 * s, 1);
+            mbar_init(bar_q_empty + 8 * s, 1);
+        }
+        mbar_init(bar_s_full, 1);
+        mbar_init(bar_st_free, 256);
+        mbar_init(bar_ds_full, 256);
+        mbar_init(bar_pd_free, 1);
+        mbar_init(bar_dq_full, 1);
+        mbar_init(bar_dq_empty, 128);
+        mbar_init(bar_done, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 13) {
+        tmem_alloc(smem_u32(tmem_slot), T::TM_COLS);
+        tmem_relinquish();
+    }
+    if (warp == 12 && lane == 0) {
+        tma_prefetch_desc(&tm_q);
+        tma_prefetch_desc(&tm_k);
+        tma_prefetch_desc(&tm_v);
+        tma_prefetch_desc(&tm_do);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const Guard g{status, abort_flag, limit_ns};
+
+    if (warp == 12) {
+        // ------------------------------------------------------- TMA producer
+        if (lane == 0) {
+            mbar_arrive_expect_tx(bar_kv_full, 2 * T::KV_BYTES);
+            for (int c = 0; c < T::NCH; ++c) {
+                tma_load_3d(sK + c * T::K_CHUNK, &tm_k, bar_kv_full, c * 64, kv0, bh);
+                tma_load_3d(sV + c * T::K_CHUNK, &tm_v, bar_kv_full, c * 64, kv0, bh);
+            }
+            int issued = 0;
+            for (int it = 0; it < n_it; ++it) {
+                const int s = it % QS;
+                const int q0 = (i_start + it) * BQ;
+                if (it >= QS && !mbar_wait(bar_q_empty + 8 * s, ((it / QS) - 1) & 1, g,
+                                           SITE_BWD_LOAD_EMPTY))
+                    break;
+                const uint32_t fb = bar_q_full + 8 * s;
+                mbar_arrive_expect_tx(fb, 2 * T::Q_BYTES + 2 * T::VEC_BYTES);
+                for (int c = 0; c < T::NCH; ++c) {
+                    tma_load_3d(sQ + s * T::Q_BYTES + c * T::Q_CHUNK, &tm_q, fb, c * 64, q0, bh);
+                    tma_load_3d(sDO + s * T::Q_BYTES + c * T::Q_CHUNK, &tm_do, fb, c * 64, q0, bh);
+                }
+                const size_t voff = (size_t)bh * Npad + q0;
+                bulk_load(sL2 + s * T::VEC_BYTES, ws_lse2 + voff, T::VEC_BYTES, fb);
+                bulk_load(sDelta + s * T::VEC_BYTES, ws_delta + voff, T::VEC_BYTES, fb);
+                ++issued;
+            }
+            if (*abort_flag) {
+                volatile int never = 0;
+                const Guard g2{status, &never, limit_ns / 4};
+                mbar_wait(bar_kv_full, 0, g2, SITE_BWD_DRAIN);
+                for (int it = (issued > QS ? issued - QS : 0); it < issued; ++it)
+                    mbar_wait(bar_q_full + 8 * (it % QS), (it / QS) & 1, g2, SITE_BWD_DRAIN);
+            }
+        }
+    } else if (warp == 13) {
+        // ------------------------------------------------------- MMA issuer
+        // The whole warp runs this loop (warp-uniform); one elected lane issues.
+        {
+            constexpr uint32_t kIdescT = idesc_bf16_f32(128, BQ, false, false);   // S^T, dP^T
+            constexpr uint32_t kIdescAcc = idesc_bf16_f32(128, D, false, true);   // dV, dK
+            constexpr uint32_t kIdescDQ = idesc_bf16_f32(128, BQ, true, true);    // dQ^T
+            const uint64_t dK_k = sdesc_sw128(sK, 16, 1024);           // K, K-major (A of S^T)
+            const uint64_t dV_k = sdesc_sw128(sV, 16, 1024);           // V, K-major (A of dP^T)
+            const uint64_t dK_mn = sdesc_sw128(sK, T::K_CHUNK, 1024);  // K, MN-major (A of dQ^T)
+            const uint64_t dDS = sdesc_sw128(sDS, T::DS_BYTES, 1024);  // dS^T, MN-major
+            auto issue_st_dpt = [&](int it) {
+                const int s = it % QS;
+                const uint64_t dQ_k = sdesc_sw128(sQ + s * T::Q_BYTES, 16, 1024);
+                const uint64_t dDO_k = sdesc_sw128(sDO + s * T::Q_BYTES, 16, 1024);
+#pragma unroll
+                for (int ks = 0; ks < D / 16; ++ks) {
+                    const uint32_t koff = (ks & 3) * 32, kc = ks >> 2;
+                    mma_ss_elect(tmem + T::TM_ST, desc_add(dK_k, kc * T::K_CHUNK + koff),
+                                 desc_add(dQ_k, kc * T::Q_CHUNK + koff), kIdescT, ks > 0 ? 1u : 0u);
+                }
+#pragma unroll
+                for (int ks = 0; ks < D / 16; ++ks) {
+                    const uint32_t koff = (ks & 3) * 32, kc = ks >> 2;
+                    mma_ss_elect(tmem + T::TM_DPT, desc_add(dV_k, kc * T::K_CHUNK + koff),
+                                 desc_add(dDO_k, kc * T::Q_CHUNK + koff), kIdescT, ks > 0 ? 1u : 0u);
+                }
+                tc_commit_elect(bar_s_full);
+            };
+            bool ok = mbar_wait_warp(bar_kv_full, 0, g, SITE_BWD_MMA_KV) &&
+                      mbar_wait_warp(bar_q_full, 0, g, SITE_BWD_MMA_Q_FULL);
+            tc_fence_after();
+            if (ok) issue_st_dpt(0);
+            for (int it = 0; ok && it < n_it; ++it) {
+                const int s = it % QS;
+                // 1. S^T, dP^T of the next block, once the compute warps have read this one.
+                if (it + 1 < n_it) {
+                    ok = mbar_wait_warp(bar_st_free, it & 1, g, SITE_BWD_MMA_DS_FULL) &&
+                         mbar_wait_warp(bar_q_full + 8 * ((it + 1) % QS), ((it + 1) / QS) & 1, g,
+                                        SITE_BWD_MMA_Q_FULL);
+                    if (!ok) break;
+                    tc_fence_after();
+                    issue_st_dpt(it + 1);
+                }
+                // 2. dV += P^T dO_i, dK += dS^T Q_i (K = 64 queries, 16 per step).
+                if (!(ok = mbar_wait_warp(bar_ds_full, it & 1, g, SITE_BWD_MMA_DS_FULL))) break;
+                tc_fence_after();
+                const uint64_t dQ_mn = sdesc_sw128(sQ + s * T::Q_BYTES, T::Q_CHUNK, 1024);
+                const uint64_t dDO_mn = sdesc_sw128(sDO + s * T::Q_BYTES, T::Q_CHUNK, 1024);
+#pragma unroll
+                for (int ks = 0; ks < BQ / 16; ++ks)
+                    mma_ts_elect(tmem + T::TM_DV, tmem + T::TM_PD + ks * 8, desc_add(dDO_mn, ks * 2048),
+                                 kIdescAcc, (it > 0 || ks > 0) ? 1u : 0u);
+#pragma unroll
+                for (int ks = 0; ks < BQ / 16; ++ks)
+                    mma_ts_elect(tmem + T::TM_DK, tmem + T::TM_PD + 32 + ks * 8,
+                                 desc_add(dQ_mn, ks * 2048), kIdescAcc, (it > 0 || ks > 0) ? 1u : 0u);
+                tc_commit_elect(bar_pd_free);
+                tc_commit_elect(bar_q_empty + 8 * s);
+                // 3. dQ^T[d][q] = sum_k K[k][d] dS^T[k][q] (K = 128 keys, 16 per step).
+                if (it >= 1 &&
+                    !(ok = mbar_wait_warp(bar_dq_empty, (it - 1) & 1, g, SITE_BWD_MMA_DQ_FREE)))
+                    break;
+                tc_fence_after();
+#pragma unroll
+                for (int ks = 0; ks < T::BN / 16; ++ks)
+                    mma_ss_elect(tmem + T::TM_DQ, desc_add(dK_mn, ks * 2048), desc_add(dDS, ks * 2048),
+                                 kIdescDQ, ks > 0 ? 1u : 0u);
+                tc_commit_elect(bar_dq_full);
+            }
+            tc_commit_elect(bar_done);
+            volatile int never = 0;
+            const Guard g2{status, &never, limit_ns};
+            mbar_wait_warp(bar_done, 0, g2, SITE_BWD_DRAIN);
+        }
+    } else if (warp < 8) {
+        // ------------------------------------------------------- P^T and dS^T
+        const int h = warp >> 2;          // query columns [32h, 32h + 32) of each block
+        const int r = threadIdx.x & 127;  // key row within the block (TMEM lane)
+        const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+        const int key = kv0 + r;
+        bool ok = true;
+        for (int it = 0; it < n_it; ++it) {
+            const int s = it % QS;
+            const int q0 = (i_start + it) * BQ;
+            ok = mbar_wait_warp(bar_s_full, it & 1, g, SITE_BWD_SOFTMAX_S_FULL);
+            if (!ok) break;
+            tc_fence_after();
+            uint32_t sv[32], dpv[32];
+            tmem_ld32(tmem + lane_base + T::TM_ST + 32 * h, sv);
+            tmem_ld32(tmem + lane_base + T::TM_DPT + 32 * h, dpv);
+            tmem_wait_ld(sv);
+            tmem_wait_ld(dpv);
+            tc_fence_before();
+            mbar_arrive(bar_st_free);  // S^T / dP^T may now be overwritten
+            const bool need_mask = (kv0 + T::BN > N) || (CAUSAL && q0 < kv0 + T::BN - 1);
+            const float *l2v = l2_f + s * BQ + 32 * h;
+            const float *dlv = delta_f + s * BQ + 32 * h;
+            uint32_t pk[16], dk_[16];
+#pragma unroll
+            for (int e = 0; e < 32; e += 4) {
+                const float4 l4 = *reinterpret_cast<const float4 *>(l2v + e);
+                const float4 d4 = *reinterpret_cast<const float4 *>(dlv + e);
+                const float lq[4] = {l4.x, l4.y, l4.z, l4.w};
+                const float dq_[4] = {d4.x, d4.y, d4.z, d4.w};
+                float p[4], ds[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    p[u] = ex2(fmaf(__uint_as_float(sv[e + u]), scale_log2, -lq[u]));
+                    if (need_mask) {
+                        const int q = q0 + 32 * h + e + u;
+                        if (key >= N || (CAUSAL && q < key)) p[u] = 0.f;
+                    }
+                    ds[u] = p[u] * (__uint_as_float(dpv[e + u]) - dq_[u]);
+                }
+                pk[e / 2] = pack_bf16(p[0], p[1]);
+                pk[e / 2 + 1] = pack_bf16(p[2], p[3]);
+                dk_[e / 2] = pack_bf16(ds[0], ds[1]);
+                dk_[e / 2 + 1] = pack_bf16(ds[2], ds[3]);
+            }
+            // dS^T row r, queries [32h, 32h + 32): 4 swizzled 16-byte units (MN-major).
+            // The single dS^T buffer is free once dQ^T of the previous block is done.
+            if (it > 0 && !(ok = mbar_wait_warp(bar_dq_full, (it - 1) & 1, g,
+                                                SITE_BWD_SOFTMAX_S_FULL)))
+                break;
+            uint8_t *ds_row = gbase + T::OFF_DS + r * 128;
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int unit = 4 * h + u;
+                *reinterpret_cast<uint4 *>(ds_row + ((unit ^ (r & 7)) * 16)) =
+                    make_uint4(dk_[4 * u], dk_[4 * u + 1], dk_[4 * u + 2], dk_[4 * u + 3]);
+            }
+            // PD is free once dV/dK of the previous block have read it.
+            if (it > 0 && !(ok = mbar_wait_warp(bar_pd_free, (it - 1) & 1, g,
+                                                SITE_BWD_SOFTMAX_S_FULL)))
+                break;
+            tc_fence_after();
+            tmem_st16(tmem + lane_base + T::TM_PD + 16 * h, pk);
+            tmem_st16(tmem + lane_base + T::TM_PD + 32 + 16 * h, dk_);
+            tmem_wait_st();
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(bar_ds_full);
+        }
+        // ------------------------------------------------------- dK, dV epilogue
+        ok = ok && mbar_wait_warp(bar_done, 0, g, SITE_BWD_EPILOGUE);
+        if (ok) {
+            tc_fence_after();
+            float *dv_row = dv + ((size_t)bh * N + key) * D;
+            float *dk_row = dk + ((size_t)bh * N + key) * D;
+#pragma unroll 1
+            for (int c = 2 * h; c < 2 * h + 2; ++c) {
+                uint32_t a[32], b2[32];
+                tmem_ld32(tmem + lane_base + T::TM_DV + c * 32, a);
+                tmem_ld32(tmem + lane_base + T::TM_DK + c * 32, b2);
+                tmem_wait_ld(a);
+                tmem_wait_ld(b2);
+                if (key < N) {
+#pragma unroll
+                    for (int e = 0; e < 32; e += 4) {
+                        *reinterpret_cast<float4 *>(dv_row + c * 32 + e) =
+                            make_float4(__uint_as_float(a[e]), __uint_as_float(a[e + 1]),
+                                        __uint_as_float(a[e + 2]), __uint_as_float(a[e + 3]));
+                        *reinterpret_cast<float4 *>(dk_row + c * 32 + e) = make_float4(
+                            __uint_as_float(b2[e]) * scale, __uint_as_float(b2[e + 1]) * scale,
+                            __uint_as_float(b2[e + 2]) * scale, __uint_as_float(b2[e + 3]) * scale);
+                    }
+                }
+            }
+        }
+        tmem_wait_st();
+    } else {
+        // ------------------------------------------------------- dQ readout (warps 8-11)
+        const int t = threadIdx.x - 256;  // TMEM lane = column d of dQ
+        const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+        bool ok = true;
+        for (int it = 0; it < n_it; ++it) {
+            const int q0 = (i_start + it) * BQ;
+            ok = mbar_wait_warp(bar_dq_full, it & 1, g, SITE_BWD_DQ_FULL);
+            if (!ok) break;
+            tc_fence_after();
+            uint32_t x0[32], x1[32];
+            tmem_ld32(tmem + lane_base + T::TM_DQ, x0);
+            tmem_ld32(tmem + lane_base + T::TM_DQ + 32, x1);
+            tmem_wait_ld(x0);
+            tmem_wait_ld(x1);
+            tc_fence_before();
+            mbar_arrive(bar_dq_empty);
+            // Lane t holds column d = t of 64 dQ rows: for each row, one warp-wide
+            // instruction adds 32 consecutive floats (coalesced), straight from
+            // registers, so neither shared memory nor the TMA unit is involved.
+            float *col = dq + ((size_t)bh * N + q0) * D + t;
+            const int rows = min(BQ, N - q0);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+                if (e < rows) red_add_f32(col + (size_t)e * D, __uint_as_float(x0[e]) * scale);
+                if (e + 32 < rows)
+                    red_add_f32(col + (size_t)(e + 32) * D, __uint_as_float(x1[e]) * scale);
+            }
+        }
+    }
+
+    __syncwarp();
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 13) {
+        tc_fence_after();
+        tmem_dealloc(tmem, T::TM_COLS);
+    }
+}
+
 template <int D, bool CAUSAL>
 int launch_bwd_t(const BwdParams &p, cudaStream_t stream) {
     using T = BwdTile<D>;
@@ -528,15 +894,25 @@ int launch_bwd_t(const BwdParams &p, cudaStream_t stream) {
             p.N, p.Npad, p.BH);
         if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
     }
-    auto kern = fa_bwd_kernel<D, CAUSAL>;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)T::SMEM_BYTES) != cudaSuccess)
-        return FA_ERR_CUDA;
     const long long grid = (long long)((p.N + T::BN - 1) / T::BN) * p.BH;
     if (grid > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
-    kern<<<(unsigned)grid, T::THREADS, T::SMEM_BYTES, stream>>>(
-        p.tm_q, p.tm_k, p.tm_v, p.tm_do, p.ws_lse2, p.ws_delta, p.dq, p.dk, p.dv, p.N, p.Npad,
-        p.BH, p.scale, p.scale_log2, p.status, p.limit_ns);
+    if constexpr (D == 128) {
+        auto kern = fa_bwd_kernel_d128<CAUSAL>;
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)Bwd128::SMEM_BYTES) != cudaSuccess)
+            return FA_ERR_CUDA;
+        kern<<<(unsigned)grid, Bwd128::THREADS, Bwd128::SMEM_BYTES, stream>>>(
+            p.tm_q, p.tm_k, p.tm_v, p.tm_do, p.ws_lse2, p.ws_delta, p.dq, p.dk, p.dv, p.N, p.Npad,
+            p.BH, p.scale, p.scale_log2, p.status, p.limit_ns);
+    } else {
+        auto kern = fa_bwd_kernel<D, CAUSAL>;
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)T::SMEM_BYTES) != cudaSuccess)
+            return FA_ERR_CUDA;
+        kern<<<(unsigned)grid, T::THREADS, T::SMEM_BYTES, stream>>>(
+            p.tm_q, p.tm_k, p.tm_v, p.tm_do, p.ws_lse2, p.ws_delta, p.dq, p.dk, p.dv, p.N, p.Npad,
+            p.BH, p.scale, p.scale_log2, p.status, p.limit_ns);
+    }
     return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 

@@ -233,40 +233,41 @@ __global__ void __launch_bounds__(FwdTile<D>::THREADS, 1)
         }
     } else if (warp == T::WARP_MMA) {
         // ------------------------------------------------------- MMA issuer
-        if (lane == 0) {
+        // The whole warp runs this loop (warp-uniform); one elected lane issues.
+        {
             constexpr uint32_t kIdescS = idesc_bf16_f32(128, T::BN, false, false);
             constexpr uint32_t kIdescO = idesc_bf16_f32(128, D, false, true);
             // S slot u = Q_t K_j^T from K stage ks: M = 128, N = BN, K = D.
             auto issue_s = [&](int t, int u, int ks_stage) {
-                const uint32_t q_tile = sQ + t * T::Q_BYTES;
-                const uint32_t k_tile = sK + ks_stage * T::KV_BYTES;
+                const uint64_t dq = sdesc_sw128(sQ + t * T::Q_BYTES, 16, 1024);
+                const uint64_t dk = sdesc_sw128(sK + ks_stage * T::KV_BYTES, 16, 1024);
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks) {
                     const uint32_t koff = (ks & 3) * 32;  // 16 bf16 = 32 bytes per K step
-                    const uint64_t a = sdesc_sw128(q_tile + (ks >> 2) * T::Q_CHUNK + koff, 16, 1024);
-                    const uint64_t b = sdesc_sw128(k_tile + (ks >> 2) * T::KV_CHUNK + koff, 16, 1024);
-                    mma_ss(tmem + T::BN * u, a, b, kIdescS, ks > 0 ? 1u : 0u);
+                    const uint64_t a = desc_add(dq, (ks >> 2) * T::Q_CHUNK + koff);
+                    const uint64_t b = desc_add(dk, (ks >> 2) * T::KV_CHUNK + koff);
+                    mma_ss_elect(tmem + T::BN * u, a, b, kIdescS, ks > 0 ? 1u : 0u);
                 }
-                tc_commit(bar_s_full + 8 * u);
+                tc_commit_elect(bar_s_full + 8 * u);
             };
             // O_t += P V from S slot u and V stage vs: M = 128, N = D, K = BN.
             auto issue_pv = [&](int t, int u, int vs, bool first) {
-                const uint32_t v_tile = sV + vs * T::KV_BYTES;
+                const uint64_t dv = sdesc_sw128(sV + vs * T::KV_BYTES, T::KV_CHUNK, 1024);
 #pragma unroll
                 for (int ks = 0; ks < T::BN / 16; ++ks) {
-                    const uint64_t b = sdesc_sw128(v_tile + ks * 2048, T::KV_CHUNK, 1024);
-                    mma_ts(tmem + T::TM_O0 + D * t, tmem + T::BN * u + ks * 8, b, kIdescO,
+                    const uint64_t b = desc_add(dv, ks * 2048);
+                    mma_ts_elect(tmem + T::TM_O0 + D * t, tmem + T::BN * u + ks * 8, b, kIdescO,
                            (!first || ks > 0) ? 1u : 0u);
                 }
             };
             auto wait_k = [&](int j) {
-                const bool r = mbar_wait(bar_k_full + 8 * (j % KS), (j / KS) & 1, g,
+                const bool r = mbar_wait_warp(bar_k_full + 8 * (j % KS), (j / KS) & 1, g,
                                          SITE_FWD_MMA_KV_FULL);
                 tc_fence_after();
                 return r;
             };
             auto wait_v = [&](int j) {
-                const bool r = mbar_wait(bar_v_full + 8 * (j % VS), (j / VS) & 1, g,
+                const bool r = mbar_wait_warp(bar_v_full + 8 * (j % VS), (j / VS) & 1, g,
                                          SITE_FWD_MMA_KV_FULL);
                 tc_fence_after();
                 return r;
@@ -276,11 +277,11 @@ __global__ void __launch_bounds__(FwdTile<D>::THREADS, 1)
                 // NT tiles, one S slot each: PV_0(j), S_0(j+1), PV_1(j), S_1(j+1), ...
                 for (int t = 0; ok && t < NT; ++t) {
                     if (n_kv[t] == 0) continue;
-                    ok = mbar_wait(bar_q_full + 8 * t, 0, g, SITE_FWD_MMA_Q);
+                    ok = mbar_wait_warp(bar_q_full + 8 * t, 0, g, SITE_FWD_MMA_Q);
                     tc_fence_after();
                     if (ok) issue_s(t, t, 0);
                 }
-                if (ok) tc_commit(bar_k_empty);
+                if (ok) tc_commit_elect(bar_k_empty);
                 for (int j = 0; ok && j < n_max; ++j) {
                     int last_pv = 0, last_s = -1;
 #pragma unroll
@@ -292,19 +293,19 @@ __global__ void __launch_bounds__(FwdTile<D>::THREADS, 1)
 #pragma unroll
                     for (int t = 0; t < NT; ++t) {
                         if (!ok || j >= n_kv[t]) continue;
-                        ok = mbar_wait(bar_p_full + 8 * t, j & 1, g, SITE_FWD_MMA_P_FULL);
+                        ok = mbar_wait_warp(bar_p_full + 8 * t, j & 1, g, SITE_FWD_MMA_P_FULL);
                         tc_fence_after();
                         if (ok && !v_ready) ok = v_ready = wait_v(j);
                         if (!ok) break;
                         issue_pv(t, t, j % VS, j == 0);
-                        if (t == last_pv) tc_commit(bar_v_empty + 8 * (j % VS));
+                        if (t == last_pv) tc_commit_elect(bar_v_empty + 8 * (j % VS));
                         if (j + 1 < n_kv[t]) {
                             if (!k_ready) ok = k_ready = wait_k(j + 1);
                             if (!ok) break;
                             issue_s(t, t, (j + 1) % KS);
-                            if (t == last_s) tc_commit(bar_k_empty + 8 * ((j + 1) % KS));
+                            if (t == last_s) tc_commit_elect(bar_k_empty + 8 * ((j + 1) % KS));
                         } else {
-                            tc_commit(bar_o_full + 8 * t);  // O_t is final once this fires
+                            tc_commit_elect(bar_o_full + 8 * t);  // O_t is final once this fires
                         }
                     }
                 }
@@ -312,37 +313,37 @@ __global__ void __launch_bounds__(FwdTile<D>::THREADS, 1)
                 // One tile, two S slots: S(j+2) is issued right after PV(j) frees slot j&1,
                 // so the tensor core computes it while the softmax works on S(j+1).
                 const int n = n_kv[0];
-                ok = ok && mbar_wait(bar_q_full, 0, g, SITE_FWD_MMA_Q);
+                ok = ok && mbar_wait_warp(bar_q_full, 0, g, SITE_FWD_MMA_Q);
                 tc_fence_after();
                 if (ok) {
                     issue_s(0, 0, 0);
-                    tc_commit(bar_k_empty);
+                    tc_commit_elect(bar_k_empty);
                 }
                 if (ok && n > 1 && (ok = wait_k(1))) {
                     issue_s(0, 1, 1 % KS);
-                    tc_commit(bar_k_empty + 8 * (1 % KS));
+                    tc_commit_elect(bar_k_empty + 8 * (1 % KS));
                 }
                 for (int j = 0; ok && j < n; ++j) {
-                    ok = mbar_wait(bar_p_full, j & 1, g, SITE_FWD_MMA_P_FULL);
+                    ok = mbar_wait_warp(bar_p_full, j & 1, g, SITE_FWD_MMA_P_FULL);
                     tc_fence_after();
                     if (ok) ok = wait_v(j);
                     if (!ok) break;
                     issue_pv(0, j & 1, j % VS, j == 0);
-                    tc_commit(bar_v_empty + 8 * (j % VS));
-                    tc_commit(bar_pv_done);
+                    tc_commit_elect(bar_v_empty + 8 * (j % VS));
+                    tc_commit_elect(bar_pv_done);
                     if (j + 2 < n) {
                         if (!(ok = wait_k(j + 2))) break;
                         issue_s(0, j & 1, (j + 2) % KS);
-                        tc_commit(bar_k_empty + 8 * ((j + 2) % KS));
+                        tc_commit_elect(bar_k_empty + 8 * ((j + 2) % KS));
                     }
                 }
-                if (ok) tc_commit(bar_o_full);
+                if (ok) tc_commit_elect(bar_o_full);
             }
             // Fires once every MMA issued above has completed (normal or aborted run).
-            tc_commit(bar_mma_done);
+            tc_commit_elect(bar_mma_done);
             volatile int never = 0;
             const Guard g2{status, &never, limit_ns};
-            mbar_wait(bar_mma_done, 0, g2, SITE_FWD_DRAIN);
+            mbar_wait_warp(bar_mma_done, 0, g2, SITE_FWD_DRAIN);
         }
     } else {
         // ------------------------------------------------------- softmax warpgroups

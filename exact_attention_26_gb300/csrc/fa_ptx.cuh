@@ -53,6 +53,23 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return done != 0;
 }
 
+// The same test, but a thread whose phase is not complete yet is suspended (it
+// issues nothing) until the phase completes or about `hint_ns` nanoseconds pass.
+// Waiting warps share issue slots with the warp that feeds the tensor core, so
+// they must sleep rather than spin.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity,
+                                                    uint32_t hint_ns) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return done != 0;
+}
+
 // Everything a bounded wait needs: where to record a failure, the CTA's shared
 // abort flag (set by the first wait that gives up, so the other roles stop
 // waiting early), and the time limit.
@@ -66,8 +83,7 @@ __device__ __noinline__ inline bool mbar_wait_slow(uint32_t bar, uint32_t parity
                                                    int site) {
     const uint64_t t0 = global_timer_ns();
     for (;;) {
-        for (int i = 0; i < 64; ++i)
-            if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait_sleep(bar, parity, 100000u)) return true;
         if (*g.abort) return false;
         if (global_timer_ns() - t0 > g.limit_ns) {
             *g.abort = 1;
@@ -144,6 +160,11 @@ __device__ __forceinline__ void bulk_wait_group() {
     asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
 }
 
+// Fire-and-forget fp32 add to global memory (no return value).
+__device__ __forceinline__ void red_add_f32(float *addr, float v) {
+    asm volatile("red.global.add.f32 [%0], %1;" ::"l"(addr), "f"(v) : "memory");
+}
+
 // Make generic-proxy writes to shared memory visible to the async proxy (TMA, MMA).
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -202,6 +223,39 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
         : "memory");
 }
 
+// Warp-uniform forms: every lane of the warp executes the call with the same
+// operands and exactly one elected lane issues the instruction.  Keeping the
+// issuing code warp-uniform lets the compiler do the descriptor arithmetic on
+// the uniform datapath instead of per-lane registers, which matters because the
+// issuing warp shares its scheduler with busy softmax/compute warps.
+__device__ __forceinline__ void mma_ss_elect(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                             uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred e, p;\n\telect.sync _|e, 0xffffffff;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_ts_elect(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                             uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred e, p;\n\telect.sync _|e, 0xffffffff;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_commit_elect(uint32_t bar) {
+    asm volatile(
+        "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(
+            bar)
+        : "memory");
+}
+
 // Instruction descriptor, kind::f16 with bf16 A/B and fp32 D, dense.
 //   bits 4-5 D format (1 = f32), 7-9 A format (1 = bf16), 10-12 B format (1 = bf16),
 //   bit 15 A major (0 = K-major, 1 = MN-major), bit 16 B major, 17-22 N>>3, 24-28 M>>4.
@@ -228,6 +282,12 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_byt
     d |= (uint64_t)1 << 46;
     d |= (uint64_t)2 << 61;
     return d;
+}
+
+// A descriptor for an address `byte_off` bytes past the one `d` describes (the
+// start-address field is the low word's address >> 4 and never overflows here).
+__device__ __forceinline__ uint64_t desc_add(uint64_t d, uint32_t byte_off) {
+    return d + (uint64_t)(byte_off >> 4);
 }
 
 // 32 lanes x 32 consecutive 32-bit columns: lane t of the warp gets row
