@@ -530,12 +530,13 @@ struct Bwd128 {
     static constexpr int BN = 128;
     static constexpr int BQ = 64;
     static constexpr int NCH = 2;
-    static constexpr int QS = 4;                        // Q/dO/L/D ring stages
+    static constexpr int QS = 3;                        // Q/dO/L/D ring stages
     static constexpr uint32_t K_CHUNK = BN * 128;
     static constexpr uint32_t Q_CHUNK = BQ * 128;
     static constexpr uint32_t KV_BYTES = BN * D * 2;
     static constexpr uint32_t Q_BYTES = BQ * D * 2;
     static constexpr uint32_t DS_BYTES = BQ * BN * 2;   // dS^T, [128 keys][64 queries] bf16
+    static constexpr uint32_t STAGE_BYTES = BQ * D * 4; // dQ tile, fp32
     static constexpr uint32_t VEC_BYTES = BQ * 4;
     static constexpr uint32_t TM_DV = 0, TM_DK = 128, TM_ST = 256, TM_DPT = 320, TM_PD = 384,
                               TM_DQ = 448, TM_COLS = 512;
@@ -544,12 +545,14 @@ struct Bwd128 {
     static constexpr uint32_t OFF_Q = OFF_V + KV_BYTES;
     static constexpr uint32_t OFF_DO = OFF_Q + QS * Q_BYTES;
     static constexpr uint32_t OFF_DS = OFF_DO + QS * Q_BYTES;
-    static constexpr uint32_t OFF_L2 = OFF_DS + DS_BYTES;  // one dS^T buffer
+    static constexpr uint32_t OFF_STAGE = OFF_DS + DS_BYTES;  // one dS^T buffer
+    static constexpr uint32_t OFF_L2 = OFF_STAGE + STAGE_BYTES;
     static constexpr uint32_t OFF_DELTA = OFF_L2 + QS * VEC_BYTES;
     static constexpr uint32_t OFF_BAR = OFF_DELTA + QS * VEC_BYTES;
     // kv_full, q_full[QS], q_empty[QS], s_full, st_free, ds_full, pd_free, dq_full,
-    // dq_empty, done (dq_full also tells the compute warps that dS^T smem is free)
-    static constexpr int NBAR = 1 + 2 * QS + 7;
+    // dq_empty, stg_free, stg_full, done (dq_full also tells the compute warps that
+    // the dS^T buffer is free)
+    static constexpr int NBAR = 1 + 2 * QS + 9;
     static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr uint32_t SMEM_BYTES = OFF_MISC + 16 + 1024;
     static constexpr int THREADS = 448;  // compute 0-7, dQ readout 8-11, TMA 12, MMA 13
@@ -574,7 +577,7 @@ __global__ void __launch_bounds__(448, 1)
 
     const uint32_t sK = base + T::OFF_K, sV = base + T::OFF_V;
     const uint32_t sQ = base + T::OFF_Q, sDO = base + T::OFF_DO;
-    const uint32_t sDS = base + T::OFF_DS;
+    const uint32_t sDS = base + T::OFF_DS, sStage = base + T::OFF_STAGE;
     const uint32_t sL2 = base + T::OFF_L2, sDelta = base + T::OFF_DELTA;
     const uint32_t bar = base + T::OFF_BAR;
     const uint32_t bar_kv_full = bar;
@@ -586,9 +589,12 @@ __global__ void __launch_bounds__(448, 1)
     const uint32_t bar_pd_free = bar_s_full + 24;
     const uint32_t bar_dq_full = bar_s_full + 32;
     const uint32_t bar_dq_empty = bar_s_full + 40;
-    const uint32_t bar_done = bar_s_full + 48;
+    const uint32_t bar_stg_free = bar_s_full + 48;  // staging tile may be overwritten
+    const uint32_t bar_stg_full = bar_s_full + 56;  // staging tile written by all 128 threads
+    const uint32_t bar_done = bar_s_full + 64;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + T::OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(gbase + T::OFF_MISC + 4);
+    float *stage_f = reinterpret_cast<float *>(gbase + T::OFF_STAGE);
     const float *l2_f = reinterpret_cast<const float *>(gbase + T::OFF_L2);
     const float *delta_f = reinterpret_cast<const float *>(gbase + T::OFF_DELTA);
 
@@ -614,6 +620,8 @@ __global__ void __launch_bounds__(448, 1)
         mbar_init(bar_pd_free, 1);
         mbar_init(bar_dq_full, 1);
         mbar_init(bar_dq_empty, 128);
+        mbar_init(bar_stg_free, 1);
+        mbar_init(bar_stg_full, 128);
         mbar_init(bar_done, 1);
         *abort_flag = 0;
         fence_mbar_init();
@@ -856,18 +864,42 @@ __global__ void __launch_bounds__(448, 1)
             tmem_wait_ld(x1);
             tc_fence_before();
             mbar_arrive(bar_dq_empty);
-            // Lane t holds column d = t of 64 dQ rows: for each row, one warp-wide
-            // instruction adds 32 consecutive floats (coalesced), straight from
-            // registers, so neither shared memory nor the TMA unit is involved.
-            float *col = dq + ((size_t)bh * N + q0) * D + t;
-            const int rows = min(BQ, N - q0);
+            // dQ^T column t of the block's 64 rows -> row-major fp32 staging tile ->
+            // one bulk asynchronous add into the block's contiguous global dQ rows.
+            // The tile is free once the previous bulk add has read it; every sync here
+            // is a bounded mbarrier wait, so an abort cannot strand a warp.
+            if (t == 0) {
+                bulk_wait_group_read<0>();
+                mbar_arrive(bar_stg_free);
+            }
+            ok = mbar_wait_warp(bar_stg_free, it & 1, g, SITE_BWD_DQ_FULL);
+            if (!ok) break;
 #pragma unroll
             for (int e = 0; e < 32; ++e) {
-                if (e < rows) red_add_f32(col + (size_t)e * D, __uint_as_float(x0[e]) * scale);
-                if (e + 32 < rows)
-                    red_add_f32(col + (size_t)(e + 32) * D, __uint_as_float(x1[e]) * scale);
+                stage_f[e * D + t] = __uint_as_float(x0[e]) * scale;
+                stage_f[(e + 32) * D + t] = __uint_as_float(x1[e]) * scale;
+            }
+            fence_proxy_async_smem();
+            mbar_arrive(bar_stg_full);
+            if (warp == 8) {
+                bool ok0 = true;
+                if (lane == 0) {
+                    ok0 = mbar_wait(bar_stg_full, it & 1, g, SITE_BWD_DQ_FULL);
+                    if (ok0) {
+                        const int rows = min(BQ, N - q0);
+                        bulk_reduce_add_f32(dq + ((size_t)bh * N + q0) * D, sStage,
+                                            (uint32_t)(rows * D * 4));
+                        bulk_commit_group();
+                    }
+                }
+                ok0 = __shfl_sync(0xffffffffu, ok0 ? 1 : 0, 0) != 0;
+                if (!ok0) {
+                    ok = false;
+                    break;
+                }
             }
         }
+        if (t == 0) bulk_wait_group<0>();
     }
 
     __syncwarp();
