@@ -259,12 +259,13 @@ __global__ void __launch_bounds__(320, 1)
         }
     } else if (warp == 9) {
         // ------------------------------------------------------- MMA issuer
-        if (lane == 0) {
+        // The whole warp runs this loop (warp-uniform); one elected lane issues.
+        {
             constexpr uint32_t kIdescT = idesc_bf16_f32(128, BQ, false, false);   // S^T, dP^T
             constexpr uint32_t kIdescAcc = idesc_bf16_f32(128, D, false, true);   // dV, dK
             constexpr uint32_t kIdescDQ = T::DQ_T ? idesc_bf16_f32(128, BQ, true, true)  // dQ^T
                                                   : idesc_bf16_f32(128, D, true, true);  // dQ
-            bool ok = mbar_wait(bar_kv_full, 0, g, SITE_BWD_MMA_KV);
+            bool ok = mbar_wait_warp(bar_kv_full, 0, g, SITE_BWD_MMA_KV);
             auto issue_st_dpt = [&](int it) {
                 const int s = it & 1;
                 const uint32_t q_t = sQ + s * T::Q_BYTES, do_t = sDO + s * T::Q_BYTES;
@@ -272,7 +273,7 @@ __global__ void __launch_bounds__(320, 1)
                 for (int ks = 0; ks < D / 16; ++ks) {
                     const uint32_t koff = (ks & 3) * 32;
                     const uint32_t kc = (ks >> 2);
-                    mma_ss(tmem + T::TM_ST, sdesc_sw128(sK + kc * T::K_CHUNK + koff, 16, 1024),
+                    mma_ss_elect(tmem + T::TM_ST, sdesc_sw128(sK + kc * T::K_CHUNK + koff, 16, 1024),
                            sdesc_sw128(q_t + kc * T::Q_CHUNK + koff, 16, 1024), kIdescT,
                            ks > 0 ? 1u : 0u);
                 }
@@ -280,13 +281,13 @@ __global__ void __launch_bounds__(320, 1)
                 for (int ks = 0; ks < D / 16; ++ks) {
                     const uint32_t koff = (ks & 3) * 32;
                     const uint32_t kc = (ks >> 2);
-                    mma_ss(tmem + T::TM_DPT, sdesc_sw128(sV + kc * T::K_CHUNK + koff, 16, 1024),
+                    mma_ss_elect(tmem + T::TM_DPT, sdesc_sw128(sV + kc * T::K_CHUNK + koff, 16, 1024),
                            sdesc_sw128(do_t + kc * T::Q_CHUNK + koff, 16, 1024), kIdescT,
                            ks > 0 ? 1u : 0u);
                 }
-                tc_commit(bar_s_full);
+                tc_commit_elect(bar_s_full);
             };
-            if (ok && mbar_wait(bar_q_full, 0, g, SITE_BWD_MMA_Q_FULL)) {
+            if (ok && mbar_wait_warp(bar_q_full, 0, g, SITE_BWD_MMA_Q_FULL)) {
                 tc_fence_after();
                 issue_st_dpt(0);
             } else {
@@ -295,30 +296,30 @@ __global__ void __launch_bounds__(320, 1)
             for (int it = 0; ok && it < n_it; ++it) {
                 const int s = it & 1;
                 const uint32_t q_t = sQ + s * T::Q_BYTES, do_t = sDO + s * T::Q_BYTES;
-                if (!mbar_wait(bar_ds_full, it & 1, g, SITE_BWD_MMA_DS_FULL)) { ok = false; break; }
+                if (!mbar_wait_warp(bar_ds_full, it & 1, g, SITE_BWD_MMA_DS_FULL)) { ok = false; break; }
                 tc_fence_after();
                 // dV += P^T dO_i ; dK += dS^T Q_i   (K = BQ queries, 16 per step)
 #pragma unroll
                 for (int ks = 0; ks < BQ / 16; ++ks)
-                    mma_ts(tmem + T::TM_DV, tmem + T::TM_ST + ks * 8,
+                    mma_ts_elect(tmem + T::TM_DV, tmem + T::TM_ST + ks * 8,
                            sdesc_sw128(do_t + ks * 2048, T::Q_CHUNK, 1024), kIdescAcc,
                            (it > 0 || ks > 0) ? 1u : 0u);
 #pragma unroll
                 for (int ks = 0; ks < BQ / 16; ++ks)
-                    mma_ts(tmem + T::TM_DK, tmem + T::TM_DPT + ks * 8,
+                    mma_ts_elect(tmem + T::TM_DK, tmem + T::TM_DPT + ks * 8,
                            sdesc_sw128(q_t + ks * 2048, T::Q_CHUNK, 1024), kIdescAcc,
                            (it > 0 || ks > 0) ? 1u : 0u);
-                tc_commit(bar_q_empty + 8 * s);
+                tc_commit_elect(bar_q_empty + 8 * s);
                 // Next block's S^T and dP^T overlap this block's dQ and the softmax of the next.
                 if (it + 1 < n_it) {
-                    if (!mbar_wait(bar_q_full + 8 * ((it + 1) & 1), ((it + 1) >> 1) & 1, g,
+                    if (!mbar_wait_warp(bar_q_full + 8 * ((it + 1) & 1), ((it + 1) >> 1) & 1, g,
                                    SITE_BWD_MMA_Q_FULL)) { ok = false; break; }
                     tc_fence_after();
                     issue_st_dpt(it + 1);
                 }
                 // dQ of this block into TMEM buffer it&1 (K = 128 keys, 16 per step).
                 const int b = it & 1;
-                if (it >= 2 && !mbar_wait(bar_dq_empty + 8 * b, ((it >> 1) - 1) & 1, g,
+                if (it >= 2 && !mbar_wait_warp(bar_dq_empty + 8 * b, ((it >> 1) - 1) & 1, g,
                                           SITE_BWD_MMA_DQ_FREE)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t ds_t = sDS + b * T::DS_BYTES;
@@ -327,22 +328,22 @@ __global__ void __launch_bounds__(320, 1)
                 for (int ks = 0; ks < T::BN / 16; ++ks) {
                     if constexpr (T::DQ_T) {
                         // dQ^T[d][q] = sum_k K[k][d] dS^T[k][q]: A = K (M = d), B = dS^T (N = q)
-                        mma_ss(dq_tm, sdesc_sw128(sK + ks * 2048, T::K_CHUNK, 1024),
+                        mma_ss_elect(dq_tm, sdesc_sw128(sK + ks * 2048, T::K_CHUNK, 1024),
                                sdesc_sw128(ds_t + ks * 2048, T::DS_CHUNK, 1024), kIdescDQ,
                                ks > 0 ? 1u : 0u);
                     } else {
                         // dQ[q][d] = sum_k dS^T[k][q] K[k][d]: A = dS^T (M = q), B = K (N = d)
-                        mma_ss(dq_tm, sdesc_sw128(ds_t + ks * 2048, T::DS_CHUNK, 1024),
+                        mma_ss_elect(dq_tm, sdesc_sw128(ds_t + ks * 2048, T::DS_CHUNK, 1024),
                                sdesc_sw128(sK + ks * 2048, T::K_CHUNK, 1024), kIdescDQ,
                                ks > 0 ? 1u : 0u);
                     }
                 }
-                tc_commit(bar_dq_full + 8 * b);
+                tc_commit_elect(bar_dq_full + 8 * b);
             }
-            tc_commit(bar_done);
+            tc_commit_elect(bar_done);
             volatile int never = 0;
             const Guard g2{status, &never, limit_ns};
-            mbar_wait(bar_done, 0, g2, SITE_BWD_DRAIN);
+            mbar_wait_warp(bar_done, 0, g2, SITE_BWD_DRAIN);
         }
     } else if (warp < 4) {
         // ------------------------------------------------------- P^T and dS^T
