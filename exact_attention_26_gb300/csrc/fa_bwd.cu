@@ -825,27 +825,38 @@ __global__ void __launch_bounds__(448, 1)
         ok = ok && mbar_wait_warp(bar_done, 0, g, SITE_BWD_EPILOGUE);
         if (ok) {
             tc_fence_after();
-            float *dv_row = dv + ((size_t)bh * N + key) * D;
-            float *dk_row = dk + ((size_t)bh * N + key) * D;
+            // Each thread owns half a key row (d columns [64h, 64h + 64)).  Rows are
+            // staged in shared memory at a 528-byte pitch (16-byte writes without bank
+            // conflicts; the Q/dO area is free once every MMA is done) and leave with
+            // one bulk copy per half-row, so global writes are 256 contiguous bytes.
+            constexpr uint32_t kPitch = 528;
+            static_assert(128 * kPitch <= T::OFF_DS - T::OFF_Q, "epilogue staging fits Q/dO area");
+            uint8_t *stg = gbase + T::OFF_Q + r * kPitch + 256 * h;
+            const uint32_t stg_s = sQ + r * kPitch + 256 * h;
 #pragma unroll 1
-            for (int c = 2 * h; c < 2 * h + 2; ++c) {
-                uint32_t a[32], b2[32];
-                tmem_ld32(tmem + lane_base + T::TM_DV + c * 32, a);
-                tmem_ld32(tmem + lane_base + T::TM_DK + c * 32, b2);
-                tmem_wait_ld(a);
-                tmem_wait_ld(b2);
-                if (key < N) {
+            for (int pass = 0; pass < 2; ++pass) {  // 0: dV, 1: dK (times scale)
+                const uint32_t tcol = (pass == 0 ? T::TM_DV : T::TM_DK) + 64 * h;
+                const float mul = pass == 0 ? 1.f : scale;
+                if (pass == 1) bulk_wait_group_read<0>();  // own staging row is reused
 #pragma unroll
-                    for (int e = 0; e < 32; e += 4) {
-                        *reinterpret_cast<float4 *>(dv_row + c * 32 + e) =
-                            make_float4(__uint_as_float(a[e]), __uint_as_float(a[e + 1]),
-                                        __uint_as_float(a[e + 2]), __uint_as_float(a[e + 3]));
-                        *reinterpret_cast<float4 *>(dk_row + c * 32 + e) = make_float4(
-                            __uint_as_float(b2[e]) * scale, __uint_as_float(b2[e + 1]) * scale,
-                            __uint_as_float(b2[e + 2]) * scale, __uint_as_float(b2[e + 3]) * scale);
-                    }
+                for (int c = 0; c < 2; ++c) {
+                    uint32_t a[32];
+                    tmem_ld32(tmem + lane_base + tcol + 32 * c, a);
+                    tmem_wait_ld(a);
+#pragma unroll
+                    for (int e = 0; e < 32; e += 4)
+                        *reinterpret_cast<float4 *>(stg + (32 * c + e) * 4) = make_float4(
+                            __uint_as_float(a[e]) * mul, __uint_as_float(a[e + 1]) * mul,
+                            __uint_as_float(a[e + 2]) * mul, __uint_as_float(a[e + 3]) * mul);
                 }
+                fence_proxy_async_smem();
+                if (key < N) {
+                    float *dst = (pass == 0 ? dv : dk) + ((size_t)bh * N + key) * D + 64 * h;
+                    bulk_store(dst, stg_s, 256);
+                }
+                bulk_commit_group();
             }
+            bulk_wait_group_read<0>();
         }
         tmem_wait_st();
     } else {

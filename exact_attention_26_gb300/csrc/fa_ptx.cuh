@@ -144,6 +144,13 @@ __device__ __forceinline__ void bulk_reduce_add_f32(void *dst, uint32_t src, uin
         : "memory");
 }
 
+// Plain bulk copy shared -> global (async proxy); size and addresses 16-byte aligned.
+__device__ __forceinline__ void bulk_store(void *dst, uint32_t src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst),
+                 "r"(src), "r"(bytes)
+                 : "memory");
+}
+
 __device__ __forceinline__ void bulk_commit_group() {
     asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
