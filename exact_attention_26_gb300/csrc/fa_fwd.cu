@@ -68,9 +68,9 @@ struct FwdTile {
     static constexpr uint32_t OFF_K = OFF_Q + NT * Q_BYTES;
     static constexpr uint32_t OFF_V = OFF_K + KS * KV_BYTES;
     static constexpr uint32_t OFF_BAR = OFF_V + VS * KV_BYTES;
-    // q_full[NT], k_full[KS], k_empty[KS], v_full[VS], v_empty[VS], s_full[NS],
-    // p_full[NT], o_full[NT], pv_done, mma_done
-    static constexpr int NBAR = NT + 2 * KS + 2 * VS + NS + 2 * NT + 2;
+    // q_full[NT], q_empty[NT], k_full[KS], k_empty[KS], v_full[VS], v_empty[VS],
+    // s_full[NS], p_full[NT], o_full[NT], o_free[NT], pv_done, mma_done
+    static constexpr int NBAR = 2 * NT + 2 * KS + 2 * VS + NS + 3 * NT + 2;
     static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr uint32_t SMEM_BYTES = OFF_MISC + 16 + 1024;
     static constexpr int WARP_MMA = 4 * NT;
@@ -103,14 +103,16 @@ __global__ void __launch_bounds__(FwdTile<D>::THREADS, 1)
     const uint32_t sK = base + T::OFF_K;
     const uint32_t sV = base + T::OFF_V;
     const uint32_t bar_q_full = base + T::OFF_BAR;      // [NT]
-    const uint32_t bar_k_full = bar_q_full + 8 * NT;     // [KS]
+    const uint32_t bar_q_empty = bar_q_full + 8 * NT;    // [NT]
+    const uint32_t bar_k_full = bar_q_empty + 8 * NT;    // [KS]
     const uint32_t bar_k_empty = bar_k_full + 8 * KS;    // [KS]
     const uint32_t bar_v_full = bar_k_empty + 8 * KS;    // [VS]
     const uint32_t bar_v_empty = bar_v_full + 8 * VS;    // [VS]
     const uint32_t bar_s_full = bar_v_empty + 8 * VS;    // [NS]
     const uint32_t bar_p_full = bar_s_full + 8 * T::NS;  // [NT]
     const uint32_t bar_o_full = bar_p_full + 8 * NT;     // [NT]
-    const uint32_t bar_pv_done = bar_o_full + 8 * NT;    // one tile, two S slots only
+    const uint32_t bar_o_free = bar_o_full + 8 * NT;     // [NT]
+    const uint32_t bar_pv_done = bar_o_free + 8 * NT;    // one tile, two S slots only
     const uint32_t bar_mma_done = bar_pv_done + 8;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + T::OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(gbase + T::OFF_MISC + 4);
@@ -118,29 +120,47 @@ __global__ void __launch_bounds__(FwdTile<D>::THREADS, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
-    // Work of this CTA: ROWS query rows of one head.  Causal: the longest rows
-    // (largest block index) are issued first.
-    const int bh = blockIdx.x % BH;
-    const int cb = CAUSAL ? (n_cblocks - 1 - (int)(blockIdx.x / BH)) : (int)(blockIdx.x / BH);
+    // Persistent schedule.  Work item w = ROWS query rows of one head; w runs over
+    // (batch*head) fastest and, when causal, over row blocks from the last (longest)
+    // to the first.  CTA c takes item r*G + c in even rounds r and r*G + G-1-c in
+    // odd ones (G = gridDim.x), which visits every item once and evens out the
+    // longest-first sizes.  Every role walks the same sequence; barrier phases are
+    // running counts carried from one item to the next.
+    const int n_items = n_cblocks * BH;
+    const int G = (int)gridDim.x;
+    const int n_rounds = (n_items + G - 1) / G;
     const int n_kv_all = (N + T::BN - 1) / T::BN;
-    int n_kv[NT];  // K/V tiles each query tile visits (0: tile entirely past N)
+    auto item_of = [&](int rnd) -> int {
+        const int idx = rnd * G + ((rnd & 1) ? (G - 1 - (int)blockIdx.x) : (int)blockIdx.x);
+        return idx < n_items ? idx : -1;
+    };
+    struct Item {
+        int bh, cb, n_kv[NT], n_max;
+    };
+    auto decode = [&](int w) {
+        Item it;
+        it.bh = w % BH;
+        it.cb = CAUSAL ? (n_cblocks - 1 - w / BH) : (w / BH);
+        it.n_max = 0;
 #pragma unroll
-    for (int t = 0; t < NT; ++t) {
-        const int row0 = cb * T::ROWS + t * T::BM;
-        if (row0 >= N)
-            n_kv[t] = 0;
-        else
-            n_kv[t] = CAUSAL ? min(n_kv_all, (row0 + T::BM + T::BN - 1) / T::BN) : n_kv_all;
-    }
-    int n_max = 0;
-#pragma unroll
-    for (int t = 0; t < NT; ++t) n_max = max(n_max, n_kv[t]);
+        for (int t = 0; t < NT; ++t) {  // K/V tiles query tile t visits (0: past N)
+            const int row0 = it.cb * T::ROWS + t * T::BM;
+            if (row0 >= N)
+                it.n_kv[t] = 0;
+            else
+                it.n_kv[t] = CAUSAL ? min(n_kv_all, (row0 + T::BM + T::BN - 1) / T::BN) : n_kv_all;
+            it.n_max = max(it.n_max, it.n_kv[t]);
+        }
+        return it;
+    };
 
     if (threadIdx.x == 0) {
         for (int t = 0; t < NT; ++t) {
             mbar_init(bar_q_full + 8 * t, 1);
+            mbar_init(bar_q_empty + 8 * t, 1);
             mbar_init(bar_p_full + 8 * t, 128);
             mbar_init(bar_o_full + 8 * t, 1);
+            mbar_init(bar_o_free + 8 * t, 128);
         }
         for (int u = 0; u < T::NS; ++u) mbar_init(bar_s_full + 8 * u, 1);
         for (int s = 0; s < KS; ++s) {
@@ -173,49 +193,54 @@ __global__ void __launch_bounds__(FwdTile<D>::THREADS, 1)
 
     if (warp == T::WARP_LOAD) {
         // ------------------------------------------------------- TMA producer
-        // Order: Q_0, K_0, (other Q tiles), then K_{i} ahead of V_{i-1}, since S
-        // needs K one step before PV needs V.
+        // Per item: Q tiles (each once the previous item's last S MMA on that tile
+        // has read it), then K_i ahead of V_{i-1}, since S needs K one step before
+        // PV needs V.  The K/V rings run on across items.
         if (lane == 0) {
-            auto load_q = [&](int t) {
-                mbar_arrive_expect_tx(bar_q_full + 8 * t, T::Q_BYTES);
-                for (int c = 0; c < T::NCH; ++c)
-                    tma_load_3d(sQ + t * T::Q_BYTES + c * T::Q_CHUNK, &tm_q, bar_q_full + 8 * t,
-                                c * 64, cb * T::ROWS + t * T::BM, bh);
-            };
-            auto load_kv = [&](const CUtensorMap *map, uint32_t ring, uint32_t full, int stage,
-                               int j) {
-                mbar_arrive_expect_tx(full + 8 * stage, T::KV_BYTES);
-                for (int c = 0; c < T::NCH; ++c)
-                    tma_load_3d(ring + stage * T::KV_BYTES + c * T::KV_CHUNK, map, full + 8 * stage,
-                                c * 64, j * T::BN, bh);
-            };
-            load_q(0);
-            int k_issued = 0, v_issued = 0;
+            int k_issued = 0, v_issued = 0;  // running counts over all items
+            int q_issued[NT];
+#pragma unroll
+            for (int t = 0; t < NT; ++t) q_issued[t] = 0;
             bool ok = true;
-            for (int i = 0; ok && i <= n_max; ++i) {
-                if (i < n_max) {
-                    const int ks = i % KS;
-                    if (i >= KS && !mbar_wait(bar_k_empty + 8 * ks, ((i / KS) - 1) & 1, g,
-                                              SITE_FWD_LOAD_KV_EMPTY)) {
-                        ok = false;
+            for (int rnd = 0; ok && rnd < n_rounds; ++rnd) {
+                const int w = item_of(rnd);
+                if (w < 0) continue;
+                const Item itm = decode(w);
+                auto load_kv = [&](const CUtensorMap *map, uint32_t ring, uint32_t full, int stage,
+                                   int j) {
+                    mbar_arrive_expect_tx(full + 8 * stage, T::KV_BYTES);
+                    for (int c = 0; c < T::NCH; ++c)
+                        tma_load_3d(ring + stage * T::KV_BYTES + c * T::KV_CHUNK, map,
+                                    full + 8 * stage, c * 64, j * T::BN, itm.bh);
+                };
+                for (int t = 0; ok && t < NT; ++t) {
+                    if (itm.n_kv[t] == 0) continue;
+                    if (q_issued[t] > 0 && !(ok = mbar_wait(bar_q_empty + 8 * t, (q_issued[t] - 1) & 1,
+                                                            g, SITE_FWD_LOAD_KV_EMPTY)))
                         break;
-                    }
-                    load_kv(&tm_k, sK, bar_k_full, ks, i);
-                    ++k_issued;
-                    if (i == 0)
-                        for (int t = 1; t < NT; ++t)
-                            if (n_kv[t] > 0) load_q(t);
+                    mbar_arrive_expect_tx(bar_q_full + 8 * t, T::Q_BYTES);
+                    for (int c = 0; c < T::NCH; ++c)
+                        tma_load_3d(sQ + t * T::Q_BYTES + c * T::Q_CHUNK, &tm_q, bar_q_full + 8 * t,
+                                    c * 64, itm.cb * T::ROWS + t * T::BM, itm.bh);
+                    ++q_issued[t];
                 }
-                if (i >= 1) {
-                    const int j = i - 1;
-                    const int vs = j % VS;
-                    if (j >= VS && !mbar_wait(bar_v_empty + 8 * vs, ((j / VS) - 1) & 1, g,
-                                              SITE_FWD_LOAD_KV_EMPTY)) {
-                        ok = false;
-                        break;
+                for (int i = 0; ok && i <= itm.n_max; ++i) {
+                    if (i < itm.n_max) {
+                        const int gk = k_issued, ks = gk % KS;
+                        if (gk >= KS && !(ok = mbar_wait(bar_k_empty + 8 * ks, ((gk / KS) - 1) & 1, g,
+                                                         SITE_FWD_LOAD_KV_EMPTY)))
+                            break;
+                        load_kv(&tm_k, sK, bar_k_full, ks, i);
+                        ++k_issued;
                     }
-                    load_kv(&tm_v, sV, bar_v_full, vs, j);
-                    ++v_issued;
+                    if (i >= 1) {
+                        const int gv = v_issued, vs = gv % VS;
+                        if (gv >= VS && !(ok = mbar_wait(bar_v_empty + 8 * vs, ((gv / VS) - 1) & 1, g,
+                                                         SITE_FWD_LOAD_KV_EMPTY)))
+                            break;
+                        load_kv(&tm_v, sV, bar_v_full, vs, i - 1);
+                        ++v_issued;
+                    }
                 }
             }
             if (*abort_flag) {
@@ -223,8 +248,8 @@ __global__ void __launch_bounds__(FwdTile<D>::THREADS, 1)
                 volatile int never = 0;
                 const Guard g2{status, &never, limit_ns / 4};
                 for (int t = 0; t < NT; ++t)
-                    if (n_kv[t] > 0 && (t == 0 || k_issued > 0))
-                        mbar_wait(bar_q_full + 8 * t, 0, g2, SITE_FWD_DRAIN);
+                    if (q_issued[t] > 0)
+                        mbar_wait(bar_q_full + 8 * t, (q_issued[t] - 1) & 1, g2, SITE_FWD_DRAIN);
                 for (int j = (k_issued > KS ? k_issued - KS : 0); j < k_issued; ++j)
                     mbar_wait(bar_k_full + 8 * (j % KS), (j / KS) & 1, g2, SITE_FWD_DRAIN);
                 for (int j = (v_issued > VS ? v_issued - VS : 0); j < v_issued; ++j)
@@ -272,72 +297,107 @@ __global__ void __launch_bounds__(FwdTile<D>::THREADS, 1)
                 tc_fence_after();
                 return r;
             };
-            bool ok = wait_k(0);
-            if constexpr (T::SB == 1) {
-                // NT tiles, one S slot each: PV_0(j), S_0(j+1), PV_1(j), S_1(j+1), ...
-                for (int t = 0; ok && t < NT; ++t) {
-                    if (n_kv[t] == 0) continue;
-                    ok = mbar_wait_warp(bar_q_full + 8 * t, 0, g, SITE_FWD_MMA_Q);
-                    tc_fence_after();
-                    if (ok) issue_s(t, t, 0);
-                }
-                if (ok) tc_commit_elect(bar_k_empty);
-                for (int j = 0; ok && j < n_max; ++j) {
-                    int last_pv = 0, last_s = -1;
+            bool ok = true;
+            int kc = 0, vc = 0;  // K/V tiles consumed before the current item (running)
+            int qc[NT], pc[NT], oc[NT];  // per tile: Q loads, P arrivals, items finished
 #pragma unroll
-                    for (int t = 0; t < NT; ++t) {
-                        if (j < n_kv[t]) last_pv = t;
-                        if (j + 1 < n_kv[t]) last_s = t;
-                    }
-                    bool v_ready = false, k_ready = false;
-#pragma unroll
-                    for (int t = 0; t < NT; ++t) {
-                        if (!ok || j >= n_kv[t]) continue;
-                        ok = mbar_wait_warp(bar_p_full + 8 * t, j & 1, g, SITE_FWD_MMA_P_FULL);
+            for (int t = 0; t < NT; ++t) qc[t] = pc[t] = oc[t] = 0;
+            int gs = 0;          // S products issued before the current item (two-slot case)
+            for (int rnd = 0; ok && rnd < n_rounds; ++rnd) {
+                const int w = item_of(rnd);
+                if (w < 0) continue;
+                const Item itm = decode(w);
+                if constexpr (T::SB == 1) {
+                    // NT tiles, one S slot each: PV_0(j), S_0(j+1), PV_1(j), S_1(j+1), ...
+                    ok = wait_k(kc);
+                    for (int t = 0; ok && t < NT; ++t) {
+                        if (itm.n_kv[t] == 0) continue;
+                        ok = mbar_wait_warp(bar_q_full + 8 * t, qc[t] & 1, g, SITE_FWD_MMA_Q);
+                        ++qc[t];
                         tc_fence_after();
-                        if (ok && !v_ready) ok = v_ready = wait_v(j);
                         if (!ok) break;
-                        issue_pv(t, t, j % VS, j == 0);
-                        if (t == last_pv) tc_commit_elect(bar_v_empty + 8 * (j % VS));
-                        if (j + 1 < n_kv[t]) {
-                            if (!k_ready) ok = k_ready = wait_k(j + 1);
+                        issue_s(t, t, kc % KS);
+                        if (itm.n_kv[t] == 1) tc_commit_elect(bar_q_empty + 8 * t);
+                    }
+                    if (ok) tc_commit_elect(bar_k_empty + 8 * (kc % KS));
+                    for (int j = 0; ok && j < itm.n_max; ++j) {
+                        int last_pv = 0, last_s = -1;
+#pragma unroll
+                        for (int t = 0; t < NT; ++t) {
+                            if (j < itm.n_kv[t]) last_pv = t;
+                            if (j + 1 < itm.n_kv[t]) last_s = t;
+                        }
+                        bool v_ready = false, k_ready = false;
+#pragma unroll
+                        for (int t = 0; t < NT; ++t) {
+                            if (!ok || j >= itm.n_kv[t]) continue;
+                            ok = mbar_wait_warp(bar_p_full + 8 * t, pc[t] & 1, g, SITE_FWD_MMA_P_FULL);
+                            ++pc[t];
+                            // The first PV of an item overwrites O_t: the previous item's
+                            // epilogue must have read it.
+                            if (ok && j == 0 && oc[t] > 0)
+                                ok = mbar_wait_warp(bar_o_free + 8 * t, (oc[t] - 1) & 1, g,
+                                                    SITE_FWD_MMA_P_FULL);
+                            tc_fence_after();
+                            if (ok && !v_ready) ok = v_ready = wait_v(vc + j);
                             if (!ok) break;
-                            issue_s(t, t, (j + 1) % KS);
-                            if (t == last_s) tc_commit_elect(bar_k_empty + 8 * ((j + 1) % KS));
-                        } else {
-                            tc_commit_elect(bar_o_full + 8 * t);  // O_t is final once this fires
+                            issue_pv(t, t, (vc + j) % VS, j == 0);
+                            if (t == last_pv) tc_commit_elect(bar_v_empty + 8 * ((vc + j) % VS));
+                            if (j + 1 < itm.n_kv[t]) {
+                                if (!k_ready) ok = k_ready = wait_k(kc + j + 1);
+                                if (!ok) break;
+                                issue_s(t, t, (kc + j + 1) % KS);
+                                if (j + 2 == itm.n_kv[t]) tc_commit_elect(bar_q_empty + 8 * t);
+                                if (t == last_s) tc_commit_elect(bar_k_empty + 8 * ((kc + j + 1) % KS));
+                            } else {
+                                tc_commit_elect(bar_o_full + 8 * t);  // O_t is final once this fires
+                                ++oc[t];
+                            }
                         }
                     }
-                }
-            } else {
-                // One tile, two S slots: S(j+2) is issued right after PV(j) frees slot j&1,
-                // so the tensor core computes it while the softmax works on S(j+1).
-                const int n = n_kv[0];
-                ok = ok && mbar_wait_warp(bar_q_full, 0, g, SITE_FWD_MMA_Q);
-                tc_fence_after();
-                if (ok) {
-                    issue_s(0, 0, 0);
-                    tc_commit_elect(bar_k_empty);
-                }
-                if (ok && n > 1 && (ok = wait_k(1))) {
-                    issue_s(0, 1, 1 % KS);
-                    tc_commit_elect(bar_k_empty + 8 * (1 % KS));
-                }
-                for (int j = 0; ok && j < n; ++j) {
-                    ok = mbar_wait_warp(bar_p_full, j & 1, g, SITE_FWD_MMA_P_FULL);
-                    tc_fence_after();
-                    if (ok) ok = wait_v(j);
-                    if (!ok) break;
-                    issue_pv(0, j & 1, j % VS, j == 0);
-                    tc_commit_elect(bar_v_empty + 8 * (j % VS));
-                    tc_commit_elect(bar_pv_done);
-                    if (j + 2 < n) {
-                        if (!(ok = wait_k(j + 2))) break;
-                        issue_s(0, j & 1, (j + 2) % KS);
-                        tc_commit_elect(bar_k_empty + 8 * ((j + 2) % KS));
+                } else {
+                    // One tile, two S slots: S(j+2) is issued right after PV(j) frees its
+                    // slot, so the tensor core computes it while the softmax works on S(j+1).
+                    const int n = itm.n_kv[0];
+                    ok = mbar_wait_warp(bar_q_full, qc[0] & 1, g, SITE_FWD_MMA_Q);
+                    ++qc[0];
+                    ok = ok && wait_k(kc);
+                    if (ok) {
+                        issue_s(0, gs & 1, kc % KS);
+                        tc_commit_elect(bar_k_empty + 8 * (kc % KS));
+                        if (n == 1) tc_commit_elect(bar_q_empty);
                     }
+                    if (ok && n > 1 && (ok = wait_k(kc + 1))) {
+                        issue_s(0, (gs + 1) & 1, (kc + 1) % KS);
+                        tc_commit_elect(bar_k_empty + 8 * ((kc + 1) % KS));
+                        if (n == 2) tc_commit_elect(bar_q_empty);
+                    }
+                    for (int j = 0; ok && j < n; ++j) {
+                        ok = mbar_wait_warp(bar_p_full, pc[0] & 1, g, SITE_FWD_MMA_P_FULL);
+                        ++pc[0];
+                        if (ok && j == 0 && oc[0] > 0)
+                            ok = mbar_wait_warp(bar_o_free, (oc[0] - 1) & 1, g, SITE_FWD_MMA_P_FULL);
+                        tc_fence_after();
+                        if (ok) ok = wait_v(vc + j);
+                        if (!ok) break;
+                        issue_pv(0, (gs + j) & 1, (vc + j) % VS, j == 0);
+                        tc_commit_elect(bar_v_empty + 8 * ((vc + j) % VS));
+                        tc_commit_elect(bar_pv_done);
+                        if (j + 2 < n) {
+                            if (!(ok = wait_k(kc + j + 2))) break;
+                            issue_s(0, (gs + j) & 1, (kc + j + 2) % KS);
+                            tc_commit_elect(bar_k_empty + 8 * ((kc + j + 2) % KS));
+                            if (j + 3 == n) tc_commit_elect(bar_q_empty);
+                        }
+                    }
+                    if (ok) {
+                        tc_commit_elect(bar_o_full);
+                        ++oc[0];
+                    }
+                    gs += n;
                 }
-                if (ok) tc_commit_elect(bar_o_full);
+                kc += itm.n_max;
+                vc += itm.n_max;
             }
             // Fires once every MMA issued above has completed (normal or aborted run).
             tc_commit_elect(bar_mma_done);
@@ -351,100 +411,114 @@ __global__ void __launch_bounds__(FwdTile<D>::THREADS, 1)
         const int r = threadIdx.x & 127;
         const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
         const uint32_t t_o = tmem + lane_base + T::TM_O0 + D * t;
-        const int row0 = cb * T::ROWS + t * T::BM;
-        const int q_idx = row0 + r;
-        const int n_it = n_kv[t];
-        float m_ref = -INFINITY;  // reference max, base-2 scaled units
-        float l = 0.f;
+        int sc = 0;  // S products of this tile consumed before the current item
+        int oc = 0;  // items of this tile finished
         bool ok = true;
-        for (int j = 0; j < n_it; ++j) {
-            const int u = (T::SB == 1) ? t : (j & 1);                 // S slot
-            const uint32_t par = (T::SB == 1) ? (j & 1) : ((j >> 1) & 1);
-            const uint32_t t_s = tmem + lane_base + T::BN * u;
-            ok = mbar_wait_warp(bar_s_full + 8 * u, par, g, SITE_FWD_SOFTMAX_S_FULL);
+        for (int rnd = 0; ok && rnd < n_rounds; ++rnd) {
+            const int w = item_of(rnd);
+            if (w < 0) continue;
+            const Item itm = decode(w);
+            const int n_it = itm.n_kv[t];
+            if (n_it == 0) continue;
+            const int row0 = itm.cb * T::ROWS + t * T::BM;
+            const int q_idx = row0 + r;
+            float m_ref = -INFINITY;  // reference max, base-2 scaled units
+            float l = 0.f;
+            for (int j = 0; j < n_it; ++j) {
+                const int gsj = sc + j;                                     // running S index
+                const int u = (T::SB == 1) ? t : (gsj & 1);                 // S slot
+                const uint32_t par = (T::SB == 1) ? (gsj & 1) : ((gsj >> 1) & 1);
+                const uint32_t t_s = tmem + lane_base + T::BN * u;
+                ok = mbar_wait_warp(bar_s_full + 8 * u, par, g, SITE_FWD_SOFTMAX_S_FULL);
+                if (!ok) break;
+                tc_fence_after();
+                uint32_t sr[T::BN / 32][32];
+#pragma unroll
+                for (int c = 0; c < T::BN / 32; ++c) tmem_ld32(t_s + c * 32, sr[c]);
+#pragma unroll
+                for (int c = 0; c < T::BN / 32; ++c) tmem_wait_ld(sr[c]);
+                float s[T::BN];
+#pragma unroll
+                for (int c = 0; c < T::BN / 32; ++c)
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) s[c * 32 + e] = __uint_as_float(sr[c][e]);
+
+                const int kv0 = j * T::BN;
+                const bool need_mask = (kv0 + T::BN > N) || (CAUSAL && kv0 + T::BN - 1 > row0);
+                if (need_mask) {
+                    const int lim = CAUSAL ? min(N, q_idx + 1) : N;  // keys [0, lim) are visible
+#pragma unroll
+                    for (int c = 0; c < T::BN; ++c)
+                        if (kv0 + c >= lim) s[c] = -INFINITY;
+                }
+                float mx = s[0];
+#pragma unroll
+                for (int c = 1; c < T::BN; ++c) mx = fmaxf(mx, s[c]);
+                const float m_tile = mx * scale_log2;
+                float alpha = 1.f;
+                const bool move = m_tile > m_ref + kRescaleLog2;
+                if (move) {
+                    alpha = ex2(m_ref - m_tile);
+                    m_ref = m_tile;
+                }
+                const float neg_m = -m_ref;
+                float sum = 0.f;
+#pragma unroll
+                for (int c = 0; c < T::BN; ++c) {
+                    s[c] = ex2(fmaf(s[c], scale_log2, neg_m));
+                    sum += s[c];
+                }
+                l = l * alpha + sum;
+                // P as bf16 pairs into the first BN/2 columns of the S slot.
+#pragma unroll
+                for (int c = 0; c < T::BN / 64; ++c) {
+                    uint32_t pk[32];
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) pk[e] = pack_bf16(s[c * 64 + 2 * e], s[c * 64 + 2 * e + 1]);
+                    tmem_st32(t_s + c * 32, pk);
+                }
+                if (j > 0 && __any_sync(0xffffffffu, move)) {
+                    // O_t <- alpha O_t for this warp's 32 rows (alpha = 1 on rows that kept
+                    // m), after P is stored so the S registers are free.  PV(j-1) must be
+                    // complete: with one slot per tile S(j) was issued after it; with two
+                    // slots it is awaited here.  PV(j) waits for the arrive below.
+                    if (T::SB == 2 && !mbar_wait_warp(bar_pv_done, (gsj - 1) & 1, g,
+                                                      SITE_FWD_SOFTMAX_S_FULL)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+#pragma unroll 1
+                    for (int c = 0; c < D / 32; ++c) {
+                        uint32_t o[32];
+                        tmem_ld32(t_o + c * 32, o);
+                        tmem_wait_ld(o);
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                        tmem_st32(t_o + c * 32, o);
+                    }
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(bar_p_full + 8 * t);
+            }
+            sc += n_it;
+            // --------------------------------------------------- epilogue of this item
+            ok = ok && mbar_wait_warp(bar_o_full + 8 * t, oc & 1, g, SITE_FWD_EPILOGUE_O_FULL);
             if (!ok) break;
             tc_fence_after();
-            uint32_t sr[T::BN / 32][32];
-#pragma unroll
-            for (int c = 0; c < T::BN / 32; ++c) tmem_ld32(t_s + c * 32, sr[c]);
-#pragma unroll
-            for (int c = 0; c < T::BN / 32; ++c) tmem_wait_ld(sr[c]);
-            float s[T::BN];
-#pragma unroll
-            for (int c = 0; c < T::BN / 32; ++c)
-#pragma unroll
-                for (int e = 0; e < 32; ++e) s[c * 32 + e] = __uint_as_float(sr[c][e]);
-
-            const int kv0 = j * T::BN;
-            const bool need_mask = (kv0 + T::BN > N) || (CAUSAL && kv0 + T::BN - 1 > row0);
-            if (need_mask) {
-                const int lim = CAUSAL ? min(N, q_idx + 1) : N;  // keys [0, lim) are visible
-#pragma unroll
-                for (int c = 0; c < T::BN; ++c)
-                    if (kv0 + c >= lim) s[c] = -INFINITY;
-            }
-            float mx = s[0];
-#pragma unroll
-            for (int c = 1; c < T::BN; ++c) mx = fmaxf(mx, s[c]);
-            const float m_tile = mx * scale_log2;
-            float alpha = 1.f;
-            const bool move = m_tile > m_ref + kRescaleLog2;
-            if (move) {
-                alpha = ex2(m_ref - m_tile);
-                m_ref = m_tile;
-            }
-            const float neg_m = -m_ref;
-            float sum = 0.f;
-#pragma unroll
-            for (int c = 0; c < T::BN; ++c) {
-                s[c] = ex2(fmaf(s[c], scale_log2, neg_m));
-                sum += s[c];
-            }
-            l = l * alpha + sum;
-            // P as bf16 pairs into the first BN/2 columns of the S slot.
-#pragma unroll
-            for (int c = 0; c < T::BN / 64; ++c) {
-                uint32_t pk[32];
-#pragma unroll
-                for (int e = 0; e < 32; ++e) pk[e] = pack_bf16(s[c * 64 + 2 * e], s[c * 64 + 2 * e + 1]);
-                tmem_st32(t_s + c * 32, pk);
-            }
-            if (j > 0 && __any_sync(0xffffffffu, move)) {
-                // O_t <- alpha O_t for this warp's 32 rows (alpha = 1 on rows that kept m),
-                // after P is stored so the S registers are free.  PV(j-1) must be
-                // complete: with one slot per tile S(j) was issued after it; with two
-                // slots it is awaited here.  PV(j) waits for the arrive below.
-                if (T::SB == 2 && !mbar_wait_warp(bar_pv_done, (j - 1) & 1, g,
-                                                  SITE_FWD_SOFTMAX_S_FULL)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-#pragma unroll 1
-                for (int c = 0; c < D / 32; ++c) {
-                    uint32_t o[32];
-                    tmem_ld32(t_o + c * 32, o);
-                    tmem_wait_ld(o);
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-                    tmem_st32(t_o + c * 32, o);
-                }
-            }
-            tmem_wait_st();
-            tc_fence_before();
-            mbar_arrive(bar_p_full + 8 * t);
-        }
-        // ------------------------------------------------------- epilogue
-        ok = ok && n_it > 0 && mbar_wait_warp(bar_o_full + 8 * t, 0, g, SITE_FWD_EPILOGUE_O_FULL);
-        if (ok) {
-            tc_fence_after();
             const float inv_l = 1.f / l;
-            __nv_bfloat16 *orow = out + ((size_t)bh * (size_t)N + (size_t)q_idx) * D;
+            __nv_bfloat16 *orow = out + ((size_t)itm.bh * (size_t)N + (size_t)q_idx) * D;
 #pragma unroll 1
             for (int c = 0; c < D / 32; ++c) {
                 uint32_t o[32];
                 tmem_ld32(t_o + c * 32, o);
                 tmem_wait_ld(o);
+                if (c == D / 32 - 1) {
+                    // O_t has been read: the next item's first PV may overwrite it.
+                    tc_fence_before();
+                    mbar_arrive(bar_o_free + 8 * t);
+                }
                 uint32_t pk[16];
 #pragma unroll
                 for (int e = 0; e < 16; ++e)
@@ -457,7 +531,8 @@ __global__ void __launch_bounds__(FwdTile<D>::THREADS, 1)
                         dst[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
                 }
             }
-            if (q_idx < N) lse[(size_t)bh * (size_t)N + q_idx] = (m_ref + lg2(l)) * kLn2;
+            if (q_idx < N) lse[(size_t)itm.bh * (size_t)N + q_idx] = (m_ref + lg2(l)) * kLn2;
+            ++oc;
         }
         tmem_wait_st();  // an aborted iteration may leave a store in flight
     }
@@ -479,8 +554,10 @@ int launch_fwd_t(const FwdParams &p, cudaStream_t stream) {
                                          (int)T::SMEM_BYTES);
     if (e != cudaSuccess) return FA_ERR_CUDA;
     const int n_cblocks = (p.N + T::ROWS - 1) / T::ROWS;
-    const long long grid = (long long)n_cblocks * p.BH;
-    if (grid > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
+    const long long items = (long long)n_cblocks * p.BH;
+    if (items > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
+    // Persistent: one CTA per SM (the shared-memory footprint allows no more).
+    const long long grid = items < p.num_sms ? items : p.num_sms;
     kern<<<(unsigned)grid, T::THREADS, T::SMEM_BYTES, stream>>>(
         p.tm_q, p.tm_k, p.tm_v, reinterpret_cast<__nv_bfloat16 *>(p.o), p.lse, p.N, p.BH,
         n_cblocks, p.scale_log2, p.status, p.limit_ns);
