@@ -7,6 +7,7 @@
 #include <mutex>
 
 #include "fa_internal.h"
+#include "fa_ptx.cuh"
 
 namespace fa {
 namespace {
@@ -96,6 +97,23 @@ int check_scale(float scale) {
 constexpr float kLog2e = 1.4426950408889634074f;
 
 size_t round_up(size_t x, size_t m) { return (x + m - 1) / m * m; }
+
+// One warp waits, through the same bounded wait the attention kernels use, on an
+// mbarrier that nothing ever arrives on; the wait gives up after `limit_ns`,
+// records FA_ERR_TIMEOUT in the status word and the kernel returns.
+__global__ void __launch_bounds__(32) fa_wait_selftest_kernel(int *status,
+                                                             unsigned long long limit_ns) {
+    __shared__ __align__(8) unsigned long long bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&bar), 1);
+        abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncwarp();
+    const Guard g{status, &abort_flag, limit_ns};
+    mbar_wait_warp(smem_u32(&bar), 0, g, SITE_SELFTEST);
+}
 
 }  // namespace
 
@@ -214,4 +232,13 @@ extern "C" int fa_device_status(void *stream) {
             return FA_ERR_CUDA;
     }
     return rec[0];
+}
+
+extern "C" int fa_selftest_wait_timeout(unsigned long long limit_ns, void *stream) {
+    if (limit_ns < 1000ull || limit_ns > 5000000000ull) return FA_ERR_INVALID_ARG;
+    DeviceCache *dc = nullptr;
+    int rc = current_device(&dc);
+    if (rc != FA_OK) return rc;
+    fa_wait_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(dc->status, limit_ns);
+    return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }

@@ -251,7 +251,7 @@ __global__ void __launch_bounds__(320, 1)
             }
             if (*abort_flag) {
                 volatile int never = 0;
-                const Guard g2{status, &never, limit_ns / 4};
+                const Guard g2{status, &never, kWaitLimitNs};
                 mbar_wait(bar_kv_full, 0, g2, SITE_BWD_DRAIN);
                 for (int it = (issued > 2 ? issued - 2 : 0); it < issued; ++it)
                     mbar_wait(bar_q_full + 8 * (it & 1), (it >> 1) & 1, g2, SITE_BWD_DRAIN);
@@ -342,7 +342,7 @@ __global__ void __launch_bounds__(320, 1)
             }
             tc_commit_elect(bar_done);
             volatile int never = 0;
-            const Guard g2{status, &never, limit_ns};
+            const Guard g2{status, &never, kWaitLimitNs};
             mbar_wait_warp(bar_done, 0, g2, SITE_BWD_DRAIN);
         }
     } else if (warp < 4) {
@@ -671,7 +671,7 @@ __global__ void __launch_bounds__(448, 1)
             }
             if (*abort_flag) {
                 volatile int never = 0;
-                const Guard g2{status, &never, limit_ns / 4};
+                const Guard g2{status, &never, kWaitLimitNs};
                 mbar_wait(bar_kv_full, 0, g2, SITE_BWD_DRAIN);
                 for (int it = (issued > QS ? issued - QS : 0); it < issued; ++it)
                     mbar_wait(bar_q_full + 8 * (it % QS), (it / QS) & 1, g2, SITE_BWD_DRAIN);
@@ -749,7 +749,7 @@ __global__ void __launch_bounds__(448, 1)
             }
             tc_commit_elect(bar_done);
             volatile int never = 0;
-            const Guard g2{status, &never, limit_ns};
+            const Guard g2{status, &never, kWaitLimitNs};
             mbar_wait_warp(bar_done, 0, g2, SITE_BWD_DRAIN);
         }
     } else if (warp < 8) {

@@ -246,7 +246,7 @@ __global__ void __launch_bounds__(FwdTile<D>::THREADS, 1)
             if (*abort_flag) {
                 // Let the copies already in flight land before the CTA exits.
                 volatile int never = 0;
-                const Guard g2{status, &never, limit_ns / 4};
+                const Guard g2{status, &never, kWaitLimitNs};
                 for (int t = 0; t < NT; ++t)
                     if (q_issued[t] > 0)
                         mbar_wait(bar_q_full + 8 * t, (q_issued[t] - 1) & 1, g2, SITE_FWD_DRAIN);
@@ -402,7 +402,7 @@ __global__ void __launch_bounds__(FwdTile<D>::THREADS, 1)
             // Fires once every MMA issued above has completed (normal or aborted run).
             tc_commit_elect(bar_mma_done);
             volatile int never = 0;
-            const Guard g2{status, &never, limit_ns};
+            const Guard g2{status, &never, kWaitLimitNs};
             mbar_wait_warp(bar_mma_done, 0, g2, SITE_FWD_DRAIN);
         }
     } else {

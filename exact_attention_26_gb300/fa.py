@@ -22,7 +22,8 @@ FA_ERR_CUDA = 4
 FA_ERR_TIMEOUT = 5
 FA_ERR_WORKSPACE = 6
 
-EXPORTED = ("fa_fwd", "fa_bwd", "fa_bwd_workspace_bytes", "fa_status_string", "fa_device_status")
+EXPORTED = ("fa_fwd", "fa_bwd", "fa_bwd_workspace_bytes", "fa_status_string", "fa_device_status",
+            "fa_selftest_wait_timeout")
 
 _vp = ctypes.c_void_p
 _int = ctypes.c_int
@@ -83,11 +84,20 @@ def fa_bwd_noalloc(q, k, v, o, lse, dout, dq, dk, dv, B, H, N, d, causal, scale,
                    stream) -> int:
     """fa_bwd without a workspace: the library's fixed scratch array is used instead."""
     fn = load().fa_bwd_noalloc
-    if fn.restype is not _int:
+    if fn.argtypes is None:
         fn.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _int, _int, _int, _int, _int,
                        ctypes.c_float, _vp]
         fn.restype = _int
     return fn(q, k, v, o, lse, dout, dq, dk, dv, B, H, N, d, int(bool(causal)), scale, stream)
+
+
+def fa_selftest_wait_timeout(limit_ns: int, stream=None) -> int:
+    """Run the bounded-wait self test (a wait nothing satisfies, limited to limit_ns)."""
+    fn = load().fa_selftest_wait_timeout
+    if fn.argtypes is None:
+        fn.argtypes = [ctypes.c_ulonglong, _vp]
+        fn.restype = _int
+    return fn(limit_ns, stream)
 
 
 def fa_status_string(status: int) -> str:

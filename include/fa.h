@@ -118,6 +118,16 @@ int fa_bwd_noalloc(const void *q, const void *k, const void *v, const void *o,
                    const float *lse, const void *dout, float *dq, float *dk, float *dv, int B,
                    int H, int N, int d, int causal, float scale, void *stream);
 
+/*
+ * Diagnostic: launches one warp that waits, through the same bounded wait the
+ * attention kernels use, on a barrier that nothing ever arrives on.  The wait
+ * gives up after `limit_ns` nanoseconds (1e3 <= limit_ns <= 5e9, else
+ * FA_ERR_INVALID_ARG), records FA_ERR_TIMEOUT in the device status word and the
+ * kernel returns; fa_device_status then reports FA_ERR_TIMEOUT once.  Shows that
+ * a wait that runs out leaves the context usable.  Asynchronous on `stream`.
+ */
+int fa_selftest_wait_timeout(unsigned long long limit_ns, void *stream);
+
 /* Static, human-readable name of a status code (never NULL). */
 const char *fa_status_string(int status);
 
