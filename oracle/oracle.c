@@ -23,6 +23,12 @@
  *   allowed(i) = {0..N-1}, or {0..i} when causal.  Masked keys are left out of
  *   every sum, which is what adding -inf to their scores means.
  *
+ *   Decode (course page "10 FlashAttention", section "The decode variant:
+ *   FlashDecoding": a few query rows per sequence against a long key/value cache):
+ *   the same per-row definition with Nq query rows and Nk keys per head and no
+ *   mask, allowed(i) = {0..Nk-1}.  How the GPU splits the keys and merges the
+ *   partial results is not the oracle's business; it computes each row whole.
+ *
  *   Backward (the pages only say that S and P are rebuilt from the saved
  *   statistics; the formulas are the chain rule applied to the forward above):
  *     dP_j  = dO[i] . V[j]
@@ -46,6 +52,7 @@ typedef struct {
     const double *q, *k, *v, *dout;
     double *o, *lse, *dq, *dk, *dv;
     long BH, N, d;
+    long Nq;          /* decode: query rows per head (N is then the key count) */
     int causal;
     double scale;
     const long *rows; /* NULL: every row; else the rows to compute in each head */
@@ -108,6 +115,21 @@ static void *fwd_worker(void *arg) {
     return NULL;
 }
 
+/* Decode rows: t = bh * Nq + i; q, o are [BH][Nq][d], k, v are [BH][N][d]. */
+static void *dec_worker(void *arg) {
+    job_t *jb = (job_t *)arg;
+    double *s = (double *)malloc(sizeof(double) * (size_t)(jb->N > 0 ? jb->N : 1));
+    for (long t = jb->row_begin; t < jb->row_end; ++t) {
+        long bh = t / jb->Nq, i = t % jb->Nq;
+        const double *Q = jb->q + (size_t)bh * (size_t)jb->Nq * (size_t)jb->d;
+        size_t kv = (size_t)bh * (size_t)jb->N * (size_t)jb->d;
+        forward_row(Q, jb->k + kv, jb->v + kv, jb->N, jb->d, i, 0, jb->scale, s,
+                    jb->o + (size_t)t * (size_t)jb->d, jb->lse + t);
+    }
+    free(s);
+    return NULL;
+}
+
 static int run_threads(job_t *base, long total, int nthreads, void *(*fn)(void *),
                        job_t *jobs) {
     if (nthreads < 1) nthreads = 1;
@@ -141,6 +163,23 @@ int oracle_fwd(const double *q, const double *k, const double *v, double *o, dou
     job_t *jobs = (job_t *)malloc(sizeof(job_t) * (size_t)(nthreads > 0 ? nthreads : 1));
     if (!jobs) return -1;
     int rc = run_threads(&base, BH * N, nthreads, fwd_worker, jobs);
+    free(jobs);
+    return rc;
+}
+
+/* Decode: Nq query rows per head, each attending to all Nk keys of its head.
+ * q, o: [BH][Nq][d]; k, v: [BH][Nk][d]; lse: [BH][Nq].  Returns 0 on success. */
+int oracle_decode(const double *q, const double *k, const double *v, double *o, double *lse,
+                  long BH, long Nq, long Nk, long d, double scale, int nthreads) {
+    if (BH < 0 || Nq < 0 || Nk < 1 || d < 1) return -2;
+    job_t base;
+    memset(&base, 0, sizeof(base));
+    base.q = q; base.k = k; base.v = v; base.o = o; base.lse = lse;
+    base.BH = BH; base.N = Nk; base.Nq = Nq; base.d = d; base.scale = scale;
+    base.row_begin = 0;
+    job_t *jobs = (job_t *)malloc(sizeof(job_t) * (size_t)(nthreads > 0 ? nthreads : 1));
+    if (!jobs) return -1;
+    int rc = run_threads(&base, BH * Nq, nthreads, dec_worker, jobs);
     free(jobs);
     return rc;
 }

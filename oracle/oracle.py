@@ -42,6 +42,9 @@ class Oracle:
                                         ctypes.c_long, ctypes.c_long, ctypes.c_long,
                                         ctypes.c_int, ctypes.c_double, ctypes.c_int]
         lib.oracle_fwd_rows.restype = ctypes.c_int
+        lib.oracle_decode.argtypes = [_dp, _dp, _dp, _dp, _dp, ctypes.c_long, ctypes.c_long,
+                                      ctypes.c_long, ctypes.c_long, ctypes.c_double, ctypes.c_int]
+        lib.oracle_decode.restype = ctypes.c_int
         lib.oracle_bwd.argtypes = [_dp, _dp, _dp, _dp, _dp, _dp, _dp, ctypes.c_long,
                                    ctypes.c_long, ctypes.c_long, ctypes.c_int, ctypes.c_double,
                                    ctypes.c_int]
@@ -77,6 +80,24 @@ class Oracle:
                                  nthreads or default_threads())
         if rc != 0:
             raise RuntimeError(f"oracle_fwd failed ({rc})")
+        return o, lse
+
+    def decode(self, q, k, v, scale=None, nthreads=None):
+        """Decode shapes: q [B,H,Nq,d] against k, v [B,H,Nk,d], no mask.
+        Return (O [B,H,Nq,d], L [B,H,Nq]) in float64."""
+        q, k, v = self._f64(q), self._f64(k), self._f64(v)
+        B, H, Nq, d = q.shape
+        if k.shape[:2] != (B, H) or k.shape[3] != d or v.shape != k.shape:
+            raise ValueError("k and v must be [B, H, Nk, d] with q's B, H and d")
+        Nk = k.shape[2]
+        scale = 1.0 / np.sqrt(d) if scale is None else float(scale)
+        o = np.empty_like(q)
+        lse = np.empty((B, H, Nq), dtype=np.float64)
+        rc = self.lib.oracle_decode(self._ptr(q), self._ptr(k), self._ptr(v), self._ptr(o),
+                                    self._ptr(lse), B * H, Nq, Nk, d, scale,
+                                    nthreads or default_threads())
+        if rc != 0:
+            raise RuntimeError(f"oracle_decode failed ({rc})")
         return o, lse
 
     def fwd_rows(self, q, k, v, rows, causal=False, scale=None, nthreads=None):

@@ -16,8 +16,9 @@ Sources of the pinned facts:
 * Course page "10 FlashAttention", section 4 "Tiny example — the algorithm":
   causal rule "query i sees keys 0..i", scale 1/sqrt(d), and the worked check
   that a blockwise computation (blocks of 128, S=2048, d=64) agrees with the
-  textbook version to about 1e-15; section 5 "The decode variant": partial
-  results merge with the same rescaling (associativity).
+  textbook version to about 1e-15; section "The decode variant: FlashDecoding":
+  partial results over disjoint key ranges merge with the same rescaling
+  (associativity), which the decode pins use on uneven key splits.
 * Library routines used as independent references on tiny inputs:
   ``scipy.special.softmax``/``logsumexp`` and torch float64 autograd.
 """
@@ -350,6 +351,67 @@ def check_bwd_rows_partition(orc):
         _close(va + vb, dv, 1e-13, "bwd_rows dV partition")
 
 
+# ---------------------------------------------------------------- decode pins
+
+def check_decode_brute_force(orc):
+    """Decode shapes (Nq query rows against Nk keys, no mask): full score matrix with
+    the library softmax and logsumexp on tiny random inputs."""
+    r = _rng(20)
+    for (B, H, Nq, Nk, d) in [(1, 1, 1, 1, 4), (1, 2, 1, 40, 8), (2, 3, 5, 17, 16), (1, 1, 9, 3, 6)]:
+        q = r.standard_normal((B, H, Nq, d))
+        k, v = (r.standard_normal((B, H, Nk, d)) for _ in range(2))
+        scale = float(r.uniform(0.1, 1.5))
+        o, lse = orc.decode(q, k, v, scale=scale, nthreads=2)
+        s = scale * np.einsum("bhic,bhjc->bhij", q, k)
+        p = scipy.special.softmax(s, axis=-1)
+        _close(o, p @ v, 1e-13, f"decode brute force O {B,H,Nq,Nk,d}")
+        _close(lse, scipy.special.logsumexp(s, axis=-1), 1e-13, f"decode brute force L {B,H,Nq,Nk,d}")
+
+
+def check_decode_identical_keys(orc):
+    """All Nk keys equal: every query row averages V, and L = scale*q.k + ln Nk."""
+    r = _rng(21)
+    B, H, Nq, Nk, d = 2, 2, 3, 77, 8
+    q = r.standard_normal((B, H, Nq, d))
+    krow = r.standard_normal((B, H, 1, d))
+    k = np.repeat(krow, Nk, axis=2)
+    v = r.standard_normal((B, H, Nk, d))
+    o, lse = orc.decode(q, k, v, scale=0.4, nthreads=3)
+    _close(o, np.broadcast_to(v.mean(axis=2, keepdims=True), o.shape), 1e-13, "decode identical keys O")
+    s = 0.4 * np.einsum("bhic,bhc->bhi", q, krow[:, :, 0, :])
+    _close(lse, s + np.log(Nk), 1e-12, "decode identical keys L")
+
+
+def check_decode_merge_of_splits(orc):
+    """The decode variant's key split: (O_s, L_s) over disjoint key ranges merge into
+    the result over all keys by L = log sum_s exp(L_s), O = sum_s exp(L_s - L) O_s
+    (the course page's statement that partial results combine with the same
+    rescaling).  Uneven splits, one of a single key."""
+    r = _rng(22)
+    B, H, Nq, Nk, d = 1, 3, 2, 61, 8
+    q = r.standard_normal((B, H, Nq, d))
+    k, v = (r.standard_normal((B, H, Nk, d)) for _ in range(2))
+    full_o, full_l = orc.decode(q, k, v, scale=0.7, nthreads=2)
+    cuts = [0, 1, 20, 44, Nk]
+    parts = [orc.decode(q, k[:, :, a:b], v[:, :, a:b], scale=0.7, nthreads=1)
+             for a, b in zip(cuts[:-1], cuts[1:])]
+    ls = np.stack([p[1] for p in parts])
+    lm = scipy.special.logsumexp(ls, axis=0)
+    om = sum(np.exp(p[1] - lm)[..., None] * p[0] for p in parts)
+    _close(om, full_o, 1e-13, "decode merged O")
+    _close(lm, full_l, 1e-13, "decode merged L")
+
+
+def check_decode_is_noncausal_forward(orc):
+    """With Nq = Nk the decode rows are the non-causal forward's rows."""
+    r = _rng(23)
+    q, k, v = (r.standard_normal((2, 2, 13, 8)) for _ in range(3))
+    o1, l1 = orc.decode(q, k, v, scale=0.3, nthreads=2)
+    o2, l2 = orc.fwd(q, k, v, causal=False, scale=0.3, nthreads=2)
+    _close(o1, o2, 0.0, "decode vs forward O")
+    _close(l1, l2, 0.0, "decode vs forward L")
+
+
 FORWARD_CHECKS = [
     check_rows_of_p_sum_to_one,
     check_identity_v_is_softmax,
@@ -363,6 +425,10 @@ FORWARD_CHECKS = [
     check_blockwise_equivalence,
     check_rows_subset,
     check_thread_count_independent,
+    check_decode_brute_force,
+    check_decode_identical_keys,
+    check_decode_merge_of_splits,
+    check_decode_is_noncausal_forward,
 ]
 BACKWARD_CHECKS = [
     check_bwd_finite_differences,

@@ -32,6 +32,10 @@ MUTANTS = {
     "bwd_dq_uses_q": ("dqi[c] += jb->scale * ds * kj[c];", "dqi[c] += jb->scale * ds * qi[c];"),
     "bwd_dv_uses_dp": ("dvj[c] += s[j] * doi[c];", "dvj[c] += dp[j] * doi[c];"),
     "bwd_p_unnormalised": ("s[j] = s[j] / l; /* P_ij */", "s[j] = s[j]; /* P_ij */"),
+    "decode_kv_head_stride": ("size_t kv = (size_t)bh * (size_t)jb->N * (size_t)jb->d;",
+                              "size_t kv = (size_t)bh * (size_t)jb->Nq * (size_t)jb->d;"),
+    "decode_first_row_only": ("long bh = t / jb->Nq, i = t % jb->Nq;",
+                              "long bh = t / jb->Nq, i = 0;"),
 }
 
 _FAST = {"check_blockwise_equivalence": lambda orc: pins.check_blockwise_equivalence(orc, big=False)}
