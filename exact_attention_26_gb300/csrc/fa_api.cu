@@ -206,6 +206,108 @@ extern "C" int fa_bwd(const void *q, const void *k, const void *v, const void *o
     return launch_bwd(p, static_cast<cudaStream_t>(stream));
 }
 
+namespace fa {
+namespace {
+
+int check_decode_sizes(int B, int H, int Nq, int Nk, int d) {
+    if (B < 1 || H < 1 || Nq < 1 || Nk < 1 || Nq > 65535) return FA_ERR_INVALID_ARG;
+    if ((long long)B * H * Nq >= (1LL << 31) || (long long)B * H * Nk >= (1LL << 31))
+        return FA_ERR_INVALID_ARG;
+    if (d != 64 && d != 128 && d != 256) return FA_ERR_UNSUPPORTED;
+    return FA_OK;
+}
+
+// Key ranges of the decode split: the requested count (0 = automatic) clamped so
+// that every range holds whole pipeline stages and none is empty.  The automatic
+// count aims at about eight CTAs per SM over the launch (two resident per SM, four
+// waves) while keeping at least four stages of keys per range.
+void decode_split(int B, int H, int Nq, int Nk, int d, int requested, int num_sms, int *S,
+                  int *keys_per_split) {
+    const long long bk = decode_block_keys(d);
+    const long long tiles = (Nk + bk - 1) / bk;
+    const long long qb = (Nq == 1) ? 1 : (d == 256 ? 4 : 8);
+    const long long base = (long long)B * H * ((Nq + qb - 1) / qb);
+    long long s;
+    if (requested > 0) {
+        s = requested;
+    } else {
+        const long long target = 8LL * (num_sms > 0 ? num_sms : 1);
+        s = (target + base - 1) / base;
+        const long long cap = (tiles + 3) / 4;
+        if (s > cap) s = cap;
+    }
+    if (s > tiles) s = tiles;
+    if (s > 65535) s = 65535;
+    if (s < 1) s = 1;
+    const long long per = ((tiles + s - 1) / s) * bk;
+    *keys_per_split = (int)per;
+    *S = (int)((Nk + per - 1) / per);
+}
+
+size_t decode_ws_bytes(long long BH, int S, int Nq, int d) {
+    if (S <= 1) return 0;
+    const size_t po = (size_t)BH * S * Nq * d * sizeof(float);
+    return round_up(po, 256) + (size_t)BH * S * Nq * sizeof(float);
+}
+
+}  // namespace
+}  // namespace fa
+
+extern "C" int fa_decode_num_splits(int B, int H, int Nq, int Nk, int d, int num_splits) {
+    int rc = check_decode_sizes(B, H, Nq, Nk, d);
+    if (rc != FA_OK) return -rc;
+    if (num_splits < 0) return -FA_ERR_INVALID_ARG;
+    DeviceCache *dc = nullptr;
+    if ((rc = current_device(&dc)) != FA_OK) return -rc;
+    int S = 1, per = 0;
+    decode_split(B, H, Nq, Nk, d, num_splits, dc->num_sms, &S, &per);
+    return S;
+}
+
+extern "C" size_t fa_decode_workspace_bytes(int B, int H, int Nq, int Nk, int d, int num_splits) {
+    const int S = fa_decode_num_splits(B, H, Nq, Nk, d, num_splits);
+    if (S < 1) return 0;
+    return decode_ws_bytes((long long)B * H, S, Nq, d);
+}
+
+extern "C" int fa_decode(const void *q, const void *k, const void *v, void *o, float *lse, int B,
+                         int H, int Nq, int Nk, int d, float scale, int num_splits,
+                         void *workspace, size_t workspace_bytes, void *stream) {
+    if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
+    int rc = check_decode_sizes(B, H, Nq, Nk, d);
+    if (rc != FA_OK) return rc;
+    if (num_splits < 0) return FA_ERR_INVALID_ARG;
+    if ((rc = check_scale(scale)) != FA_OK) return rc;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+        return FA_ERR_MISALIGNED;
+    DeviceCache *dc = nullptr;
+    if ((rc = current_device(&dc)) != FA_OK) return rc;
+    DecodeParams p{};
+    decode_split(B, H, Nq, Nk, d, num_splits, dc->num_sms, &p.S, &p.keys_per_split);
+    const long long BH = (long long)B * H;
+    const size_t need = decode_ws_bytes(BH, p.S, Nq, d);
+    if (need > 0) {
+        if (!workspace || workspace_bytes < need) return FA_ERR_WORKSPACE;
+        if (!aligned16(workspace)) return FA_ERR_MISALIGNED;
+        p.part_o = static_cast<float *>(workspace);
+        p.part_l = reinterpret_cast<float *>(static_cast<char *>(workspace) +
+                                             round_up((size_t)BH * p.S * Nq * d * sizeof(float), 256));
+    }
+    p.q = q;
+    p.k = k;
+    p.v = v;
+    p.o = o;
+    p.lse = lse;
+    p.BH = (int)BH;
+    p.Nq = Nq;
+    p.Nk = Nk;
+    p.d = d;
+    p.scale_log2 = scale * kLog2e;
+    p.status = dc->status;
+    p.limit_ns = kWaitLimitNs;
+    return launch_decode(p, static_cast<cudaStream_t>(stream));
+}
+
 extern "C" const char *fa_status_string(int status) {
     switch (status) {
         case FA_OK: return "FA_OK";

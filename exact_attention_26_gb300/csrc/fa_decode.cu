@@ -1,0 +1,372 @@
+// Decode attention with the key range split across CTAs and an LSE merge
+// (course page "10 FlashAttention", section "The decode variant: FlashDecoding":
+// a decode step has one or a few query rows per sequence, so parallelising over
+// (batch, head) alone leaves most SMs idle; each CTA instead takes one key range,
+// produces a partial result with its own running max and sum, and a second kernel
+// merges the partials with the same rescaling the online softmax uses).
+//
+// The work is a matrix-vector product that streams the key/value cache once, so
+// it is bound by HBM bandwidth, not by the tensor cores: keys and values reach
+// shared memory through plain bulk copies (a key range of one head is contiguous)
+// in an mbarrier ring, and CUDA cores do the arithmetic.  Per CTA: one producer
+// warp and four compute warps; compute warp w takes keys [w*KW, w*KW + KW) of
+// every stage, its lanes split the head dimension, and each warp keeps its own
+// running (max, sum, output) per query row until the four are merged at the end.
+#include "fa_internal.h"
+#include "fa_ptx.cuh"
+
+namespace fa {
+namespace {
+
+template <int D>
+struct DecTile {
+    static constexpr int BK = (D == 256) ? 32 : 64;   // keys per stage
+    static constexpr int STAGES = (D == 64) ? 4 : 3;
+    static constexpr int NWC = 4;                       // compute warps
+    static constexpr int KW = BK / NWC;                 // keys per compute warp per stage
+    static constexpr int E = D / 32;                    // head-dim elements per lane
+    static constexpr uint32_t TILE_BYTES = BK * D * 2;  // K (or V) rows of one stage, bf16
+    static constexpr uint32_t STAGE_BYTES = 2 * TILE_BYTES;
+    static constexpr uint32_t OFF_BAR = STAGES * STAGE_BYTES;
+    static constexpr uint32_t SMEM_BYTES = OFF_BAR + 2 * STAGES * 8 + 16;
+    static constexpr int THREADS = 32 * (NWC + 1);
+    static_assert(KW % 8 == 0, "keys are reduced in groups of eight");
+};
+
+// Query rows per CTA: one for plain decode, a block of them otherwise.
+template <int D>
+constexpr int dec_qblock() { return D == 256 ? 4 : 8; }
+
+constexpr unsigned kFull = 0xffffffffu;
+constexpr float kLn2 = 0.69314718055994530942f;
+
+// Eight per-lane partial dot products (one per key of a group) -> the full
+// 32-lane sum of key ((lane >> 2) & 7) in every lane, with 9 shuffles instead of
+// 40: each exchange step halves the keys a lane keeps.
+__device__ __forceinline__ float reduce8_transpose(const float (&v)[8], int lane) {
+    const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4;
+    float a[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float send = b4 ? v[i] : v[i + 4];
+        const float keep = b4 ? v[i + 4] : v[i];
+        a[i] = keep + __shfl_xor_sync(kFull, send, 16);
+    }
+    float b[2];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const float send = b3 ? a[i] : a[i + 2];
+        const float keep = b3 ? a[i + 2] : a[i];
+        b[i] = keep + __shfl_xor_sync(kFull, send, 8);
+    }
+    float c = (b2 ? b[1] : b[0]) + __shfl_xor_sync(kFull, b2 ? b[0] : b[1], 4);
+    c += __shfl_xor_sync(kFull, c, 2);
+    c += __shfl_xor_sync(kFull, c, 1);
+    return c;
+}
+
+// E consecutive bf16 values (E = 2, 4 or 8; address aligned to 2E bytes) from
+// shared memory in one load, exactly widened to fp32.
+template <int E>
+__device__ __forceinline__ void lds_bf16(const uint8_t *p, float (&x)[E]) {
+    uint32_t u[E / 2];
+    if constexpr (E == 2) {
+        u[0] = *reinterpret_cast<const uint32_t *>(p);
+    } else if constexpr (E == 4) {
+        const uint2 w = *reinterpret_cast<const uint2 *>(p);
+        u[0] = w.x; u[1] = w.y;
+    } else {
+        const uint4 w = *reinterpret_cast<const uint4 *>(p);
+        u[0] = w.x; u[1] = w.y; u[2] = w.z; u[3] = w.w;
+    }
+#pragma unroll
+    for (int w = 0; w < E / 2; ++w) {
+        x[2 * w] = __uint_as_float(u[w] << 16);
+        x[2 * w + 1] = __uint_as_float(u[w] & 0xffff0000u);
+    }
+}
+
+template <int D, int QB>
+__global__ void __launch_bounds__(DecTile<D>::THREADS, 2)
+    fa_decode_split_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
+                           const __nv_bfloat16 *__restrict__ v, __nv_bfloat16 *__restrict__ o,
+                           float *__restrict__ lse, float *__restrict__ part_o,
+                           float *__restrict__ part_l, int Nq, int Nk, int keys_per_split, int S,
+                           float scale_log2, int *status, unsigned long long limit_ns) {
+    using T = DecTile<D>;
+    constexpr int E = T::E, KW = T::KW, BK = T::BK, STAGES = T::STAGES;
+    extern __shared__ __align__(128) uint8_t smem[];
+    const uint32_t sbase = smem_u32(smem);
+    const uint32_t bar_full = sbase + T::OFF_BAR;            // [STAGES]
+    const uint32_t bar_empty = bar_full + 8 * STAGES;        // [STAGES]
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + T::OFF_BAR + 16 * STAGES);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int bh = blockIdx.x, split = blockIdx.y, i0 = blockIdx.z * QB;
+    const int nq = min(QB, Nq - i0);
+    const int k0 = split * keys_per_split;
+    const int k1 = min(Nk, k0 + keys_per_split);
+    const int n_tiles = (k1 - k0 + BK - 1) / BK;
+    const size_t kv_head = (size_t)bh * (size_t)Nk * D;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(bar_full + 8 * s, 1);
+            mbar_init(bar_empty + 8 * s, T::NWC);
+        }
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    const Guard g{status, abort_flag, limit_ns};
+
+    float m[QB], l[QB], acc[QB][E];
+    if (warp == T::NWC) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            int issued = 0;
+            for (int t = 0; t < n_tiles; ++t) {
+                const int slot = t % STAGES;
+                if (t >= STAGES && !mbar_wait(bar_empty + 8 * slot, ((t / STAGES) - 1) & 1, g,
+                                              SITE_DEC_EMPTY))
+                    break;
+                const int j0 = k0 + t * BK;
+                const uint32_t bytes = (uint32_t)(min(BK, k1 - j0) * D * 2);
+                const uint32_t dst = sbase + slot * T::STAGE_BYTES;
+                mbar_arrive_expect_tx(bar_full + 8 * slot, 2 * bytes);
+                bulk_load(dst, k + kv_head + (size_t)j0 * D, bytes, bar_full + 8 * slot);
+                bulk_load(dst + T::TILE_BYTES, v + kv_head + (size_t)j0 * D, bytes, bar_full + 8 * slot);
+                ++issued;
+            }
+            if (*abort_flag) {
+                // let every copy still in flight land before the CTA exits
+                volatile int never = 0;
+                const Guard g2{status, &never, kWaitLimitNs};
+                for (int t = (issued > STAGES ? issued - STAGES : 0); t < issued; ++t)
+                    mbar_wait(bar_full + 8 * (t % STAGES), (t / STAGES) & 1, g2, SITE_DEC_DRAIN);
+            }
+        }
+    } else {
+        // ------------------------------------------------------------ compute warps
+        float qv[QB][E];
+#pragma unroll
+        for (int qi = 0; qi < QB; ++qi) {
+            m[qi] = -INFINITY;
+            l[qi] = 0.f;
+#pragma unroll
+            for (int e = 0; e < E; ++e) {
+                acc[qi][e] = 0.f;
+                qv[qi][e] = qi < nq ? __bfloat162float(q[((size_t)bh * Nq + i0 + qi) * D + lane * E + e]) : 0.f;
+            }
+        }
+        const int mykey = (lane >> 2) & 7;  // key of a group of eight that this lane scores
+        for (int t = 0; t < n_tiles; ++t) {
+            const int slot = t % STAGES;
+            if (!mbar_wait_warp(bar_full + 8 * slot, (t / STAGES) & 1, g, SITE_DEC_FULL)) break;
+            const int nvalid = min(KW, k1 - (k0 + t * BK + warp * KW));  // warp-uniform
+            if (nvalid > 0) {
+                const uint8_t *Ks = smem + slot * T::STAGE_BYTES + (size_t)warp * KW * D * 2 + lane * E * 2;
+                const uint8_t *Vs = Ks + T::TILE_BYTES;
+                float sc[QB][KW / 8];
+#pragma unroll
+                for (int grp = 0; grp < KW / 8; ++grp) {
+                    float part[QB][8];
+#pragma unroll
+                    for (int r = 0; r < 8; ++r) {
+                        float kx[E];
+                        lds_bf16<E>(Ks + (size_t)(grp * 8 + r) * D * 2, kx);
+#pragma unroll
+                        for (int qi = 0; qi < QB; ++qi) {
+                            float a = 0.f;
+#pragma unroll
+                            for (int e = 0; e < E; ++e) a = fmaf(qv[qi][e], kx[e], a);
+                            part[qi][r] = a;
+                        }
+                    }
+#pragma unroll
+                    for (int qi = 0; qi < QB; ++qi) {
+                        const float s2 = reduce8_transpose(part[qi], lane) * scale_log2;
+                        sc[qi][grp] = (grp * 8 + mykey < nvalid) ? s2 : -INFINITY;
+                    }
+                }
+                float p[QB][KW / 8];
+#pragma unroll
+                for (int qi = 0; qi < QB; ++qi) {
+                    float mx = sc[qi][0];
+#pragma unroll
+                    for (int grp = 1; grp < KW / 8; ++grp) mx = fmaxf(mx, sc[qi][grp]);
+                    mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 16));
+                    mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 8));
+                    mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 4));
+                    const float m_new = fmaxf(m[qi], mx);  // finite: this warp has a valid key
+                    const float alpha = ex2(m[qi] - m_new);
+                    float rs = 0.f;
+#pragma unroll
+                    for (int grp = 0; grp < KW / 8; ++grp) {
+                        p[qi][grp] = ex2(sc[qi][grp] - m_new);  // exp2(-inf) = 0 for masked keys
+                        rs += p[qi][grp];
+                    }
+                    rs += __shfl_xor_sync(kFull, rs, 16);
+                    rs += __shfl_xor_sync(kFull, rs, 8);
+                    rs += __shfl_xor_sync(kFull, rs, 4);
+                    l[qi] = l[qi] * alpha + rs;
+                    m[qi] = m_new;
+#pragma unroll
+                    for (int e = 0; e < E; ++e) acc[qi][e] *= alpha;
+                }
+#pragma unroll
+                for (int r = 0; r < KW; ++r) {
+                    if (r < nvalid) {
+                        float vx[E];
+                        lds_bf16<E>(Vs + (size_t)r * D * 2, vx);
+#pragma unroll
+                        for (int qi = 0; qi < QB; ++qi) {
+                            const float pr = __shfl_sync(kFull, p[qi][r / 8], (r % 8) << 2);
+#pragma unroll
+                            for (int e = 0; e < E; ++e) acc[qi][e] = fmaf(pr, vx[e], acc[qi][e]);
+                        }
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_empty + 8 * slot);
+        }
+    }
+
+    // ---------------------------------------------------------------- merge warps
+    // Every stage has been consumed (or the CTA is aborting); the ring's memory now
+    // holds each compute warp's (max, sum, unnormalised output) per query row.
+    __syncthreads();
+    float *red = reinterpret_cast<float *>(smem);  // [NWC][QB][D + 2]
+    constexpr int RS = D + 2;
+    if (warp < T::NWC) {
+#pragma unroll
+        for (int qi = 0; qi < QB; ++qi) {
+            float *rw = red + (warp * QB + qi) * RS;
+#pragma unroll
+            for (int e = 0; e < E; ++e) rw[lane * E + e] = acc[qi][e];
+            if (lane == 0) {
+                rw[D] = m[qi];
+                rw[D + 1] = l[qi];
+            }
+        }
+    }
+    __syncthreads();
+    if (warp < T::NWC && !*abort_flag) {
+        for (int qi = warp; qi < nq; qi += T::NWC) {
+            float mw[T::NWC], M = -INFINITY;
+#pragma unroll
+            for (int w = 0; w < T::NWC; ++w) {
+                mw[w] = red[(w * QB + qi) * RS + D];
+                M = fmaxf(M, mw[w]);
+            }
+            float L = 0.f, out[E];
+#pragma unroll
+            for (int e = 0; e < E; ++e) out[e] = 0.f;
+#pragma unroll
+            for (int w = 0; w < T::NWC; ++w) {
+                const float f = ex2(mw[w] - M);  // a warp without keys has mw = -inf: f = 0
+                const float *rw = red + (w * QB + qi) * RS;
+                L = fmaf(rw[D + 1], f, L);
+#pragma unroll
+                for (int e = 0; e < E; ++e) out[e] = fmaf(rw[lane * E + e], f, out[e]);
+            }
+            const float inv = 1.f / L;
+            const float l_nat = (M + lg2(L)) * kLn2;  // natural-log LSE of this key range
+            const size_t row = (size_t)bh * Nq + i0 + qi;
+            if (S == 1) {
+#pragma unroll
+                for (int e = 0; e < E; e += 2) {
+                    const uint32_t pk = pack_bf16(out[e] * inv, out[e + 1] * inv);
+                    *reinterpret_cast<uint32_t *>(o + row * D + lane * E + e) = pk;
+                }
+                if (lane == 0) lse[row] = l_nat;
+            } else {
+                const size_t prow = ((size_t)bh * S + split) * Nq + i0 + qi;
+                float *po = part_o + prow * D + lane * E;
+#pragma unroll
+                for (int e = 0; e < E; ++e) po[e] = out[e] * inv;
+                if (lane == 0) part_l[prow] = l_nat;
+            }
+        }
+    }
+}
+
+// Merge of the S partial results of one query row: L = log sum_s exp(L_s),
+// O = sum_s exp(L_s - L) O_s.  One warp per row; lanes split the head dimension.
+template <int D>
+__global__ void __launch_bounds__(128)
+    fa_decode_combine_kernel(const float *__restrict__ part_o, const float *__restrict__ part_l,
+                             __nv_bfloat16 *__restrict__ o, float *__restrict__ lse, long long rows,
+                             int Nq, int S) {
+    constexpr int E = D / 32;
+    const long long row = (long long)blockIdx.x * 4 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (row >= rows) return;
+    const long long bh = row / Nq;
+    const int i = (int)(row % Nq);
+    const float *pl = part_l + (size_t)bh * S * Nq + i;  // stride Nq over splits
+    float M = -INFINITY;
+    for (int s = lane; s < S; s += 32) M = fmaxf(M, pl[(size_t)s * Nq]);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, off));
+    float W = 0.f, out[E];
+#pragma unroll
+    for (int e = 0; e < E; ++e) out[e] = 0.f;
+    for (int s = 0; s < S; ++s) {
+        const float w = __expf(pl[(size_t)s * Nq] - M);
+        W += w;
+        const float *po = part_o + (((size_t)bh * S + s) * Nq + i) * D + lane * E;
+#pragma unroll
+        for (int e = 0; e < E; ++e) out[e] = fmaf(w, po[e], out[e]);
+    }
+    const float inv = 1.f / W;
+#pragma unroll
+    for (int e = 0; e < E; e += 2) {
+        const uint32_t pk = pack_bf16(out[e] * inv, out[e + 1] * inv);
+        *reinterpret_cast<uint32_t *>(o + (size_t)row * D + lane * E + e) = pk;
+    }
+    if (lane == 0) lse[row] = M + __logf(W);
+}
+
+template <int D, int QB>
+int launch_decode_t(const DecodeParams &p, cudaStream_t stream) {
+    using T = DecTile<D>;
+    auto kern = fa_decode_split_kernel<D, QB>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)T::SMEM_BYTES) !=
+        cudaSuccess)
+        return FA_ERR_CUDA;
+    const dim3 grid((unsigned)p.BH, (unsigned)p.S, (unsigned)((p.Nq + QB - 1) / QB));
+    kern<<<grid, T::THREADS, T::SMEM_BYTES, stream>>>(
+        reinterpret_cast<const __nv_bfloat16 *>(p.q), reinterpret_cast<const __nv_bfloat16 *>(p.k),
+        reinterpret_cast<const __nv_bfloat16 *>(p.v), reinterpret_cast<__nv_bfloat16 *>(p.o), p.lse,
+        p.part_o, p.part_l, p.Nq, p.Nk, p.keys_per_split, p.S, p.scale_log2, p.status, p.limit_ns);
+    if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
+    if (p.S > 1) {
+        const long long rows = (long long)p.BH * p.Nq;
+        fa_decode_combine_kernel<D><<<(unsigned)((rows + 3) / 4), 128, 0, stream>>>(
+            p.part_o, p.part_l, reinterpret_cast<__nv_bfloat16 *>(p.o), p.lse, rows, p.Nq, p.S);
+        if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
+    }
+    return FA_OK;
+}
+
+template <int D>
+int launch_decode_d(const DecodeParams &p, cudaStream_t stream) {
+    return p.Nq == 1 ? launch_decode_t<D, 1>(p, stream) : launch_decode_t<D, dec_qblock<D>()>(p, stream);
+}
+
+}  // namespace
+
+int decode_block_keys(int d) { return d == 256 ? DecTile<256>::BK : DecTile<128>::BK; }
+
+int launch_decode(const DecodeParams &p, cudaStream_t stream) {
+    switch (p.d) {
+        case 64: return launch_decode_d<64>(p, stream);
+        case 128: return launch_decode_d<128>(p, stream);
+        case 256: return launch_decode_d<256>(p, stream);
+        default: return FA_ERR_UNSUPPORTED;
+    }
+}
+
+}  // namespace fa

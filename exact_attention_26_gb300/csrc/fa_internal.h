@@ -29,6 +29,9 @@ enum WaitSite : int {
     SITE_BWD_DQ_FULL = 17,
     SITE_BWD_EPILOGUE = 18,
     SITE_BWD_DRAIN = 19,
+    SITE_DEC_FULL = 21,
+    SITE_DEC_EMPTY = 22,
+    SITE_DEC_DRAIN = 23,
     SITE_SELFTEST = 30,
 };
 
@@ -62,7 +65,22 @@ struct BwdParams {
 // Query rows per backward q-block and the padding unit of the workspace vectors.
 constexpr int kBwdPad = 128;
 
+struct DecodeParams {
+    const void *q;            // bf16 [BH][Nq][d]
+    const void *k, *v;        // bf16 [BH][Nk][d]
+    void *o;                  // bf16 [BH][Nq][d]
+    float *lse;               // fp32 [BH][Nq]
+    float *part_o, *part_l;   // workspace when S > 1: [BH][S][Nq][d], [BH][S][Nq]
+    int BH, Nq, Nk, d;
+    int S, keys_per_split;    // key ranges [s*keys_per_split, ...) per CTA
+    float scale_log2;
+    int *status;
+    unsigned long long limit_ns;
+};
+
 int launch_fwd(const FwdParams &p, cudaStream_t stream);
 int launch_bwd(const BwdParams &p, cudaStream_t stream);
+int launch_decode(const DecodeParams &p, cudaStream_t stream);
+int decode_block_keys(int d);  // keys per pipeline stage of the decode kernel
 
 }  // namespace fa

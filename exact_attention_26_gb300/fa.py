@@ -23,7 +23,8 @@ FA_ERR_TIMEOUT = 5
 FA_ERR_WORKSPACE = 6
 
 EXPORTED = ("fa_fwd", "fa_bwd", "fa_bwd_workspace_bytes", "fa_status_string", "fa_device_status",
-            "fa_selftest_wait_timeout")
+            "fa_selftest_wait_timeout", "fa_decode", "fa_decode_num_splits",
+            "fa_decode_workspace_bytes")
 
 _vp = ctypes.c_void_p
 _int = ctypes.c_int
@@ -60,6 +61,13 @@ def load() -> ctypes.CDLL:
         lib.fa_status_string.restype = ctypes.c_char_p
         lib.fa_device_status.argtypes = [_vp]
         lib.fa_device_status.restype = _int
+        lib.fa_decode.argtypes = [_vp, _vp, _vp, _vp, _vp, _int, _int, _int, _int, _int,
+                                  ctypes.c_float, _int, _vp, ctypes.c_size_t, _vp]
+        lib.fa_decode.restype = _int
+        lib.fa_decode_num_splits.argtypes = [_int] * 6
+        lib.fa_decode_num_splits.restype = _int
+        lib.fa_decode_workspace_bytes.argtypes = [_int] * 6
+        lib.fa_decode_workspace_bytes.restype = ctypes.c_size_t
         _LIB = lib
     return _LIB
 
@@ -98,6 +106,20 @@ def fa_selftest_wait_timeout(limit_ns: int, stream=None) -> int:
         fn.argtypes = [ctypes.c_ulonglong, _vp]
         fn.restype = _int
     return fn(limit_ns, stream)
+
+
+def fa_decode(q, k, v, o, lse, B, H, Nq, Nk, d, scale, num_splits, workspace, workspace_bytes,
+              stream) -> int:
+    return load().fa_decode(q, k, v, o, lse, B, H, Nq, Nk, d, scale, num_splits, workspace,
+                            workspace_bytes, stream)
+
+
+def fa_decode_num_splits(B, H, Nq, Nk, d, num_splits=0) -> int:
+    return load().fa_decode_num_splits(B, H, Nq, Nk, d, num_splits)
+
+
+def fa_decode_workspace_bytes(B, H, Nq, Nk, d, num_splits=0) -> int:
+    return load().fa_decode_workspace_bytes(B, H, Nq, Nk, d, num_splits)
 
 
 def fa_status_string(status: int) -> str:
@@ -179,3 +201,37 @@ def backward(q, k, v, o, lse, do, causal=False, scale=None, dq=None, dk=None, dv
     if rc != FA_OK:
         raise FaError(rc, "fa_bwd")
     return tuple(grads)
+
+
+def decode(q, k, v, scale=None, num_splits=0, out=None, lse=None, workspace=None, stream=None):
+    """Decode attention: q bf16 CUDA [B,H,Nq,d] against the cache k, v [B,H,Nk,d] (no
+    mask), the key range split over CTAs and merged by LSE.  Returns (o, lse)."""
+    _check("q", q, torch.bfloat16)
+    if q.dim() != 4:
+        raise ValueError("q must be [B, H, Nq, d]")
+    B, H, Nq, d = q.shape
+    _check("k", k, torch.bfloat16)
+    if k.dim() != 4 or k.shape[0] != B or k.shape[1] != H or k.shape[3] != d:
+        raise ValueError("k must be [B, H, Nk, d] with q's B, H and d")
+    Nk = k.shape[2]
+    _check("v", v, torch.bfloat16, k.shape)
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    if out is None:
+        out = torch.empty_like(q)
+    _check("out", out, torch.bfloat16, q.shape)
+    if lse is None:
+        lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+    _check("lse", lse, torch.float32, (B, H, Nq))
+    with torch.cuda.device(q.device):
+        need = fa_decode_workspace_bytes(B, H, Nq, Nk, d, num_splits)
+        if workspace is None and need > 0:
+            workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+        if workspace is not None:
+            _check("workspace", workspace, torch.uint8)
+        ws_ptr = workspace.data_ptr() if workspace is not None else None
+        ws_len = workspace.numel() if workspace is not None else 0
+        rc = fa_decode(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                       B, H, Nq, Nk, d, scale, num_splits, ws_ptr, ws_len, _stream(q, stream))
+    if rc != FA_OK:
+        raise FaError(rc, "fa_decode")
+    return out, lse

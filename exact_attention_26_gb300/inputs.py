@@ -17,14 +17,22 @@ Recipes (one per workload of the measurement plan):
   rescale path is exercised.
 * ``sample_rows``: rows {0, N-1} plus distinct rows drawn by ``torch.randperm``
   from a generator seeded with ``seed``, sorted, ``count`` in total.
+* ``decode_qkv``: decode shapes, q [B, H, Nq, d] and a key/value cache k, v
+  [B, H, Nk, d], i.i.d. N(0, 1) * ``mult`` drawn in the order q, k, v from one
+  generator seeded with ``seed`` on ``device`` (the cache of the long-context
+  workload is drawn on the GPU; a test copies the heads it checks back to the
+  host for the oracle), rounded to bf16.  With ``boost`` > 0, a second generator
+  (``seed + 1``) picks one key per block of ``boost_block`` keys of every head and
+  adds ``boost`` to that K row, so some key ranges dominate others.
 
-All tensors are contiguous ``[B, H, N, d]`` bf16 on the CPU; callers move them.
+All tensors are contiguous bf16, on the CPU unless a device is given; callers
+move them.
 """
 from __future__ import annotations
 
 import torch
 
-__all__ = ["normal_qkv", "boosted_qkv", "sample_rows", "to_f64"]
+__all__ = ["normal_qkv", "boosted_qkv", "decode_qkv", "sample_rows", "to_f64"]
 
 
 def _draw(gen: torch.Generator, shape, mult: float = 1.0) -> torch.Tensor:
@@ -65,6 +73,36 @@ def boosted_qkv(B: int, H: int, N: int, d: int, seed: int = 0, mult: float = 0.5
                 j = lo + int(torch.randint(0, width, (1,), generator=gen).item())
                 kf[b, h, j, :] += boost
     return q, kf.to(torch.bfloat16).contiguous(), v
+
+
+def decode_qkv(B: int, H: int, Nq: int, Nk: int, d: int, seed: int = 0, mult: float = 1.0,
+               boost: float = 0.0, boost_block: int = 128, device: str = "cpu"):
+    """Return (q [B,H,Nq,d], k [B,H,Nk,d], v [B,H,Nk,d]) bf16 on ``device``."""
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed)
+
+    def draw(shape):
+        x = torch.randn(shape, generator=gen, dtype=torch.float32, device=device)
+        if mult != 1.0:
+            x = x * mult
+        return x.to(torch.bfloat16).contiguous()
+
+    q = draw((B, H, Nq, d))
+    k = draw((B, H, Nk, d))
+    v = draw((B, H, Nk, d))
+    if boost > 0:
+        g2 = torch.Generator(device=device)
+        g2.manual_seed(seed + 1)
+        nblk = (Nk + boost_block - 1) // boost_block
+        lo = torch.arange(nblk, device=device) * boost_block
+        width = torch.clamp(Nk - lo, max=boost_block)
+        r = torch.randint(0, boost_block, (B, H, nblk), generator=g2, device=device)
+        idx = lo + r % width
+        kf = k.to(torch.float32)
+        kf.scatter_add_(2, idx[..., None].expand(B, H, nblk, d),
+                        torch.full((B, H, nblk, d), float(boost), device=device))
+        k = kf.to(torch.bfloat16).contiguous()
+    return q, k, v
 
 
 def sample_rows(N: int, count: int, seed: int = 2) -> torch.Tensor:

@@ -119,6 +119,51 @@ int fa_bwd_noalloc(const void *q, const void *k, const void *v, const void *o,
                    int H, int N, int d, int causal, float scale, void *stream);
 
 /*
+ * Decode attention with a split key range (course page "10 FlashAttention",
+ * section "The decode variant: FlashDecoding"): Nq query rows per (b, h), usually
+ * one, attend to all Nk cached keys of their head, with no mask:
+ *
+ *     O[i] = softmax(q_i K^T * scale) V,   L[i] = m_i + ln(l_i)   (natural log).
+ *
+ * The key range of each head is cut into S contiguous ranges handled by separate
+ * CTAs; each produces a partial (O_s, L_s) of its range, and a second kernel
+ * merges them: L = ln sum_s exp(L_s), O = sum_s exp(L_s - L) O_s.  The result is
+ * the same as with one range up to rounding.
+ *   q      : bf16 [B][H][Nq][d] (the new tokens' queries).
+ *   k, v   : bf16 [B][H][Nk][d] (the key/value cache, contiguous per head).
+ *   o      : bf16 [B][H][Nq][d] output, rounded to nearest even.
+ *   lse    : fp32 [B][H][Nq] output.
+ *   B, H   : >= 1.  Nq in [1, 65535], Nk >= 1, B*H*Nq and B*H*Nk < 2^31.
+ *   d      : 64, 128 or 256.
+ *   scale  : finite and > 0.
+ *   num_splits : 0 chooses S automatically (about eight CTAs per SM in total,
+ *            at least four pipeline stages of keys per range); a positive value
+ *            asks for that many ranges, reduced so that none is empty.
+ *   workspace : device buffer of at least fa_decode_workspace_bytes(...) bytes,
+ *            16-byte aligned, owned by the caller, contents on entry irrelevant;
+ *            may be NULL when that size is 0 (S = 1).  Calls that share a
+ *            workspace must not overlap.
+ * Returns FA_OK or an fa_status code; nothing is launched on an error.
+ */
+int fa_decode(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H,
+              int Nq, int Nk, int d, float scale, int num_splits, void *workspace,
+              size_t workspace_bytes, void *stream);
+
+/*
+ * The number of key ranges S that fa_decode would use for these arguments on the
+ * current device (>= 1), or minus an fa_status code for invalid sizes or a CUDA
+ * error.  Needs the device's SM count when num_splits is 0.
+ */
+int fa_decode_num_splits(int B, int H, int Nq, int Nk, int d, int num_splits);
+
+/*
+ * Workspace bytes fa_decode needs: 0 when S = 1, else room for the S partial
+ * outputs (fp32 [B][H][S][Nq][d]) and their L values (fp32 [B][H][S][Nq]).
+ * Returns 0 for invalid sizes as well.
+ */
+size_t fa_decode_workspace_bytes(int B, int H, int Nq, int Nk, int d, int num_splits);
+
+/*
  * Diagnostic: launches one warp that waits, through the same bounded wait the
  * attention kernels use, on a barrier that nothing ever arrives on.  The wait
  * gives up after `limit_ns` nanoseconds (1e3 <= limit_ns <= 5e9, else

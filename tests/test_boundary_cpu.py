@@ -104,3 +104,30 @@ def test_python_wrapper_rejects_cpu_tensors(fa):
     q = torch.zeros(1, 1, 8, 64, dtype=torch.bfloat16)
     with pytest.raises(ValueError):
         fa.forward(q, q, q)
+
+
+def _dec(fa, **kw):
+    a = dict(q=DUMMY, k=DUMMY, v=DUMMY, o=DUMMY, lse=DUMMY, B=1, H=2, Nq=1, Nk=1000, d=128,
+             scale=0.1, splits=0, ws=None, ws_bytes=0, stream=None)
+    a.update(kw)
+    return fa.fa_decode(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"], a["Nq"], a["Nk"],
+                        a["d"], a["scale"], a["splits"], a["ws"], a["ws_bytes"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=None), 1), (dict(k=None), 1), (dict(v=None), 1), (dict(o=None), 1), (dict(lse=None), 1),
+    (dict(B=0), 1), (dict(H=0), 1), (dict(Nq=0), 1), (dict(Nq=65536), 1), (dict(Nk=0), 1),
+    (dict(B=65536, H=256, Nk=256), 1), (dict(d=96), 2), (dict(d=32), 2),
+    (dict(scale=0.0), 1), (dict(scale=float("nan")), 1), (dict(splits=-1), 1),
+    (dict(q=DUMMY + 8), 3), (dict(k=DUMMY + 2), 3), (dict(lse=DUMMY + 4), 3),
+])
+def test_decode_rejects_bad_arguments(fa, kw, code):
+    assert _dec(fa, **kw) == code
+
+
+def test_decode_split_queries_reject_bad_sizes(fa):
+    assert fa.fa_decode_num_splits(0, 1, 1, 100, 128, 0) == -1
+    assert fa.fa_decode_num_splits(1, 1, 1, 100, 96, 0) == -2
+    assert fa.fa_decode_num_splits(1, 1, 1, 100, 128, -3) == -1
+    assert fa.fa_decode_workspace_bytes(1, 1, 0, 100, 128, 0) == 0
+    assert fa.fa_decode_workspace_bytes(1, 1, 1, 100, 80, 2) == 0
