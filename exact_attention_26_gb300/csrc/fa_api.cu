@@ -219,22 +219,33 @@ int check_decode_sizes(int B, int H, int Nq, int Nk, int d) {
 
 // Key ranges of the decode split: the requested count (0 = automatic) clamped so
 // that every range holds whole pipeline stages and none is empty.  The automatic
-// count aims at about eight CTAs per SM over the launch (two resident per SM, four
-// waves) while keeping at least four stages of keys per range.
+// count minimises a wave model of the launch: with `slots` CTAs resident at once,
+// a launch of C CTAs of T stages each takes about ceil(C / slots) * (T + 4) stage
+// times (four stages of fill and merge per CTA), and each range keeps at least
+// eight stages so the ring has something to overlap.
 void decode_split(int B, int H, int Nq, int Nk, int d, int requested, int num_sms, int *S,
                   int *keys_per_split) {
     const long long bk = decode_block_keys(d);
     const long long tiles = (Nk + bk - 1) / bk;
-    const long long qb = (Nq == 1) ? 1 : (d == 256 ? 4 : 8);
+    const long long qb = decode_query_block(d, Nq);
     const long long base = (long long)B * H * ((Nq + qb - 1) / qb);
-    long long s;
+    long long s = 1;
     if (requested > 0) {
         s = requested;
     } else {
-        const long long target = 8LL * (num_sms > 0 ? num_sms : 1);
-        s = (target + base - 1) / base;
-        const long long cap = (tiles + 3) / 4;
-        if (s > cap) s = cap;
+        const long long slots = (long long)(num_sms > 0 ? num_sms : 1) * decode_ctas_per_sm(d, Nq);
+        long long cap = tiles / 8;
+        if (cap < 1) cap = 1;
+        if (cap > 1024) cap = 1024;
+        long long best = -1;
+        for (long long c = 1; c <= cap; ++c) {
+            const long long waves = (base * c + slots - 1) / slots;
+            const long long cost = waves * ((tiles + c - 1) / c + 4);
+            if (best < 0 || cost < best) {
+                best = cost;
+                s = c;
+            }
+        }
     }
     if (s > tiles) s = tiles;
     if (s > 65535) s = 65535;

@@ -356,9 +356,40 @@ int launch_decode_d(const DecodeParams &p, cudaStream_t stream) {
     return p.Nq == 1 ? launch_decode_t<D, 1>(p, stream) : launch_decode_t<D, dec_qblock<D>()>(p, stream);
 }
 
+template <int D, int QB>
+int ctas_per_sm_t() {
+    auto kern = fa_decode_split_kernel<D, QB>;
+    int n = 0;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)DecTile<D>::SMEM_BYTES) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, DecTile<D>::THREADS,
+                                                      DecTile<D>::SMEM_BYTES) != cudaSuccess)
+        return 1;
+    return n > 0 ? n : 1;
+}
+
+template <int D>
+int ctas_per_sm_d(int Nq) {
+    return Nq == 1 ? ctas_per_sm_t<D, 1>() : ctas_per_sm_t<D, dec_qblock<D>()>();
+}
+
 }  // namespace
 
 int decode_block_keys(int d) { return d == 256 ? DecTile<256>::BK : DecTile<128>::BK; }
+
+int decode_query_block(int d, int Nq) {
+    if (Nq == 1) return 1;
+    return d == 256 ? dec_qblock<256>() : dec_qblock<128>();
+}
+
+int decode_ctas_per_sm(int d, int Nq) {
+    switch (d) {
+        case 64: return ctas_per_sm_d<64>(Nq);
+        case 128: return ctas_per_sm_d<128>(Nq);
+        case 256: return ctas_per_sm_d<256>(Nq);
+        default: return 1;
+    }
+}
 
 int launch_decode(const DecodeParams &p, cudaStream_t stream) {
     switch (p.d) {

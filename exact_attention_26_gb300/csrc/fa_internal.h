@@ -81,6 +81,8 @@ struct DecodeParams {
 int launch_fwd(const FwdParams &p, cudaStream_t stream);
 int launch_bwd(const BwdParams &p, cudaStream_t stream);
 int launch_decode(const DecodeParams &p, cudaStream_t stream);
-int decode_block_keys(int d);  // keys per pipeline stage of the decode kernel
+int decode_block_keys(int d);          // keys per pipeline stage of the decode kernel
+int decode_query_block(int d, int Nq);  // query rows per decode CTA
+int decode_ctas_per_sm(int d, int Nq);  // resident decode CTAs per SM (occupancy query)
 
 }  // namespace fa
