@@ -55,6 +55,20 @@ BWD_WORKLOADS = [
     ("B8_H16_N2048_d64_causal", 8, 16, 2048, 64, True),
 ]
 
+# Split-KV decode (one query row per sequence against a long cache): bound by HBM.
+DEC_WORKLOADS = [
+    ("B8_H32_Nq1_Nk32768_d128", 8, 32, 1, 32768, 128),
+    ("B1_H32_Nq1_Nk32768_d128", 1, 32, 1, 32768, 128),
+    ("B8_H32_Nq1_Nk32768_d64", 8, 32, 1, 32768, 64),
+    ("B4_H16_Nq1_Nk32768_d256", 4, 16, 1, 32768, 256),
+]
+
+
+def decode_bytes(B, H, Nq, Nk, d):
+    """Algorithmic HBM bytes of one decode call: read K, V (bf16) and q, write o
+    (bf16) and L (fp32); the partial results stay in L2."""
+    return 2 * B * H * Nk * d * 2 + 2 * B * H * Nq * d * 2 + B * H * Nq * 4
+
 
 def fwd_flops(B, H, N, d, causal):
     return 4.0 * B * H * N * N * d * (0.5 if causal else 1.0)
@@ -280,6 +294,7 @@ def run_ours(args, rank, world, local_rank):
                                                         boosted_qkv, load_peaks())
             result["backward_workloads"] = sweep_backward(fa, torch, dev, flush, normal_qkv,
                                                           load_peaks())
+            result["decode_workloads"] = sweep_decode(fa, torch, dev, flush, load_peaks())
         if world == 1 and not args.no_cpu_baseline:
             result["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
         else:
@@ -368,6 +383,27 @@ def sweep_backward(fa, torch, dev, flush, normal_qkv, peaks):
         out[name] = {"ms": round(ms, 5), "tflops": round(tf, 2),
                      "frac_of_peak": round(tf / peaks["bf16_tflops"], 4)}
         del q, k, v, do, o, lse, g, ws
+    return out
+
+
+def sweep_decode(fa, torch, dev, flush, peaks):
+    """Decode calls (automatic key-range split) against the measured HBM copy rate."""
+    from exact_attention_26_gb300.inputs import decode_qkv
+    out = {}
+    for name, B, H, Nq, Nk, d in DEC_WORKLOADS:
+        q, k, v = decode_qkv(B, H, Nq, Nk, d, seed=0, device=dev)
+        o = torch.empty_like(q)
+        lse = torch.empty((B, H, Nq), dtype=torch.float32, device=dev)
+        need = fa.fa_decode_workspace_bytes(B, H, Nq, Nk, d, 0)
+        ws = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+        ms = _time_call(torch, dev, lambda: fa.decode(q, k, v, out=o, lse=lse, workspace=ws), flush)
+        gbs = decode_bytes(B, H, Nq, Nk, d) / (ms * 1e-3) / 1e9
+        out[name] = {"ms": round(ms, 5), "GB/s": round(gbs, 1),
+                     "splits": fa.fa_decode_num_splits(B, H, Nq, Nk, d, 0),
+                     "roofline": {"bound": "hbm", "achieved": round(gbs, 1),
+                                  "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                  "frac": round(gbs / peaks["hbm_gbs"], 4)}}
+        del q, k, v, o, lse, ws
     return out
 
 
