@@ -310,9 +310,91 @@ extern "C" int fa_decode(const void *q, const void *k, const void *v, void *o, f
     p.o = o;
     p.lse = lse;
     p.BH = (int)BH;
+    p.H = H;
     p.Nq = Nq;
     p.Nk = Nk;
     p.d = d;
+    p.scale_log2 = scale * kLog2e;
+    p.status = dc->status;
+    p.limit_ns = kWaitLimitNs;
+    return launch_decode(p, static_cast<cudaStream_t>(stream));
+}
+
+namespace fa {
+namespace {
+
+bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+// Sizes of a paged decode; the longest possible sequence page_size * max_pages
+// plays the role of Nk for the split.
+int check_paged_sizes(int B, int H, int Nq, int d, int page_size, int max_pages, int num_pages) {
+    if (page_size < 1 || max_pages < 1 || num_pages < 1) return FA_ERR_INVALID_ARG;
+    const long long nk = (long long)page_size * max_pages;
+    if (nk >= (1LL << 31) || (long long)B * max_pages >= (1LL << 31)) return FA_ERR_INVALID_ARG;
+    return check_decode_sizes(B, H, Nq, 1, d);
+}
+
+}  // namespace
+}  // namespace fa
+
+extern "C" int fa_decode_paged_num_splits(int B, int H, int Nq, int d, int page_size,
+                                          int max_pages_per_seq, int num_splits) {
+    int rc = check_paged_sizes(B, H, Nq, d, page_size, max_pages_per_seq, 1);
+    if (rc != FA_OK) return -rc;
+    return fa_decode_num_splits(B, H, Nq, page_size * max_pages_per_seq, d, num_splits);
+}
+
+extern "C" size_t fa_decode_paged_workspace_bytes(int B, int H, int Nq, int d, int page_size,
+                                                  int max_pages_per_seq, int num_splits) {
+    const int S = fa_decode_paged_num_splits(B, H, Nq, d, page_size, max_pages_per_seq, num_splits);
+    if (S < 1) return 0;
+    return decode_ws_bytes((long long)B * H, S, Nq, d);
+}
+
+extern "C" int fa_decode_paged(const void *q, const void *k_cache, const void *v_cache,
+                               const int *block_table, const int *seq_lens, void *o, float *lse,
+                               int B, int H, int Nq, int d, int page_size, int max_pages_per_seq,
+                               int num_pages, float scale, int num_splits, void *workspace,
+                               size_t workspace_bytes, void *stream) {
+    if (!q || !k_cache || !v_cache || !block_table || !seq_lens || !o || !lse)
+        return FA_ERR_INVALID_ARG;
+    int rc = check_paged_sizes(B, H, Nq, d, page_size, max_pages_per_seq, num_pages);
+    if (rc != FA_OK) return rc;
+    if (num_splits < 0) return FA_ERR_INVALID_ARG;
+    if ((rc = check_scale(scale)) != FA_OK) return rc;
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o) ||
+        !aligned16(lse) || !aligned4(block_table) || !aligned4(seq_lens))
+        return FA_ERR_MISALIGNED;
+    DeviceCache *dc = nullptr;
+    if ((rc = current_device(&dc)) != FA_OK) return rc;
+    const int nk_max = page_size * max_pages_per_seq;
+    DecodeParams p{};
+    decode_split(B, H, Nq, nk_max, d, num_splits, dc->num_sms, &p.S, &p.keys_per_split);
+    const long long BH = (long long)B * H;
+    const size_t need = decode_ws_bytes(BH, p.S, Nq, d);
+    if (need > 0) {
+        if (!workspace || workspace_bytes < need) return FA_ERR_WORKSPACE;
+        if (!aligned16(workspace)) return FA_ERR_MISALIGNED;
+        p.part_o = static_cast<float *>(workspace);
+        p.part_l = reinterpret_cast<float *>(static_cast<char *>(workspace) +
+                                             round_up((size_t)BH * p.S * Nq * d * sizeof(float), 256));
+    }
+    p.q = q;
+    p.k = k_cache;
+    p.v = v_cache;
+    p.o = o;
+    p.lse = lse;
+    p.block_table = block_table;
+    p.seq_lens = seq_lens;
+    p.BH = (int)BH;
+    p.H = H;
+    p.Nq = Nq;
+    p.Nk = nk_max;
+    p.d = d;
+    p.paged = 1;
+    p.page_size = page_size;
+    p.max_pages = max_pages_per_seq;
+    p.num_pages = num_pages;
     p.scale_log2 = scale * kLog2e;
     p.status = dc->status;
     p.limit_ns = kWaitLimitNs;
@@ -328,6 +410,8 @@ extern "C" const char *fa_status_string(int status) {
         case FA_ERR_CUDA: return "FA_ERR_CUDA: CUDA runtime or driver call failed";
         case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT: a bounded in-kernel wait ran out";
         case FA_ERR_WORKSPACE: return "FA_ERR_WORKSPACE: workspace missing or too small";
+        case FA_ERR_BAD_INDEX:
+            return "FA_ERR_BAD_INDEX: a block-table entry or sequence length was out of range";
         default: return "unknown fa_status";
     }
 }

@@ -86,13 +86,16 @@ __device__ __forceinline__ void lds_bf16(const uint8_t *p, float (&x)[E]) {
     }
 }
 
-template <int D, int QB>
+// Record a device-side argument error once (code and site) and stop this CTA.
+__device__ __forceinline__ void flag_bad_index(int *status, volatile int *abort_flag, int site) {
+    *abort_flag = 1;
+    atomicCAS(status + 1, 0, site);
+    atomicExch(status, FA_ERR_BAD_INDEX);
+}
+
+template <int D, int QB, bool PAGED>
 __global__ void __launch_bounds__(DecTile<D>::THREADS, 2)
-    fa_decode_split_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
-                           const __nv_bfloat16 *__restrict__ v, __nv_bfloat16 *__restrict__ o,
-                           float *__restrict__ lse, float *__restrict__ part_o,
-                           float *__restrict__ part_l, int Nq, int Nk, int keys_per_split, int S,
-                           float scale_log2, int *status, unsigned long long limit_ns) {
+    fa_decode_split_kernel(const __grid_constant__ DecodeParams p) {
     using T = DecTile<D>;
     constexpr int E = T::E, KW = T::KW, BK = T::BK, STAGES = T::STAGES;
     extern __shared__ __align__(128) uint8_t smem[];
@@ -100,14 +103,25 @@ __global__ void __launch_bounds__(DecTile<D>::THREADS, 2)
     const uint32_t bar_full = sbase + T::OFF_BAR;            // [STAGES]
     const uint32_t bar_empty = bar_full + 8 * STAGES;        // [STAGES]
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + T::OFF_BAR + 16 * STAGES);
+    const __nv_bfloat16 *q = reinterpret_cast<const __nv_bfloat16 *>(p.q);
+    const __nv_bfloat16 *k = reinterpret_cast<const __nv_bfloat16 *>(p.k);
+    const __nv_bfloat16 *v = reinterpret_cast<const __nv_bfloat16 *>(p.v);
+    __nv_bfloat16 *o = reinterpret_cast<__nv_bfloat16 *>(p.o);
+    float *lse = p.lse, *part_o = p.part_o, *part_l = p.part_l;
+    const int Nq = p.Nq, S = p.S;
+    const float scale_log2 = p.scale_log2;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int bh = blockIdx.x, split = blockIdx.y, i0 = blockIdx.z * QB;
     const int nq = min(QB, Nq - i0);
-    const int k0 = split * keys_per_split;
-    const int k1 = min(Nk, k0 + keys_per_split);
-    const int n_tiles = (k1 - k0 + BK - 1) / BK;
-    const size_t kv_head = (size_t)bh * (size_t)Nk * D;
+    // Keys of this head: the whole cache, or the sequence's own length when paged
+    // (checked on the device: 1 <= len <= page_size * max_pages).
+    int len = p.Nk;
+    if constexpr (PAGED) len = p.seq_lens[bh / p.H];
+    const bool bad_len = PAGED && (len < 1 || len > p.Nk);
+    const int k0 = split * p.keys_per_split;
+    const int k1 = bad_len ? k0 : min(len, k0 + p.keys_per_split);
+    const int n_tiles = k1 > k0 ? (k1 - k0 + BK - 1) / BK : 0;  // 0: this range is empty
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -115,33 +129,68 @@ __global__ void __launch_bounds__(DecTile<D>::THREADS, 2)
             mbar_init(bar_empty + 8 * s, T::NWC);
         }
         *abort_flag = 0;
+        if (bad_len) flag_bad_index(p.status, abort_flag, SITE_DEC_BAD_LEN);
         fence_mbar_init();
     }
     __syncthreads();
-    const Guard g{status, abort_flag, limit_ns};
+    const Guard g{p.status, abort_flag, p.limit_ns};
 
     float m[QB], l[QB], acc[QB][E];
     if (warp == T::NWC) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
             int issued = 0;
+            const int h = bh % p.H;
+            const int *bt = PAGED ? p.block_table + (size_t)(bh / p.H) * p.max_pages : nullptr;
             for (int t = 0; t < n_tiles; ++t) {
                 const int slot = t % STAGES;
                 if (t >= STAGES && !mbar_wait(bar_empty + 8 * slot, ((t / STAGES) - 1) & 1, g,
                                               SITE_DEC_EMPTY))
                     break;
                 const int j0 = k0 + t * BK;
-                const uint32_t bytes = (uint32_t)(min(BK, k1 - j0) * D * 2);
+                const int rows = min(BK, k1 - j0);
                 const uint32_t dst = sbase + slot * T::STAGE_BYTES;
-                mbar_arrive_expect_tx(bar_full + 8 * slot, 2 * bytes);
-                bulk_load(dst, k + kv_head + (size_t)j0 * D, bytes, bar_full + 8 * slot);
-                bulk_load(dst + T::TILE_BYTES, v + kv_head + (size_t)j0 * D, bytes, bar_full + 8 * slot);
+                const uint32_t fb = bar_full + 8 * slot;
+                if constexpr (PAGED) {
+                    // every physical page of this stage is checked before any byte is
+                    // promised or read: an entry outside [0, num_pages) stops the CTA
+                    bool pages_ok = true;
+                    for (int j = j0; j < j0 + rows; j = (j / p.page_size + 1) * p.page_size) {
+                        const int phys = bt[j / p.page_size];
+                        if (phys < 0 || phys >= p.num_pages) {
+                            pages_ok = false;
+                            break;
+                        }
+                    }
+                    if (!pages_ok) {
+                        flag_bad_index(p.status, abort_flag, SITE_DEC_BAD_PAGE);
+                        break;
+                    }
+                    mbar_arrive_expect_tx(fb, (uint32_t)(2 * rows * D * 2));
+                    // one copy of K and one of V per page segment of the stage
+                    for (int j = j0, r = 0; j < j0 + rows;) {
+                        const int pg = j / p.page_size, off = j - pg * p.page_size;
+                        const int n = min(p.page_size - off, j0 + rows - j);
+                        const size_t src = (((size_t)bt[pg] * p.H + h) * p.page_size + off) * D;
+                        const uint32_t bytes = (uint32_t)(n * D * 2);
+                        bulk_load(dst + r * D * 2, k + src, bytes, fb);
+                        bulk_load(dst + T::TILE_BYTES + r * D * 2, v + src, bytes, fb);
+                        j += n;
+                        r += n;
+                    }
+                } else {
+                    const size_t src = ((size_t)bh * p.Nk + j0) * D;
+                    const uint32_t bytes = (uint32_t)(rows * D * 2);
+                    mbar_arrive_expect_tx(fb, 2 * bytes);
+                    bulk_load(dst, k + src, bytes, fb);
+                    bulk_load(dst + T::TILE_BYTES, v + src, bytes, fb);
+                }
                 ++issued;
             }
             if (*abort_flag) {
                 // let every copy still in flight land before the CTA exits
                 volatile int never = 0;
-                const Guard g2{status, &never, kWaitLimitNs};
+                const Guard g2{p.status, &never, kWaitLimitNs};
                 for (int t = (issued > STAGES ? issued - STAGES : 0); t < issued; ++t)
                     mbar_wait(bar_full + 8 * (t % STAGES), (t / STAGES) & 1, g2, SITE_DEC_DRAIN);
             }
@@ -265,14 +314,18 @@ __global__ void __launch_bounds__(DecTile<D>::THREADS, 2)
             for (int e = 0; e < E; ++e) out[e] = 0.f;
 #pragma unroll
             for (int w = 0; w < T::NWC; ++w) {
-                const float f = ex2(mw[w] - M);  // a warp without keys has mw = -inf: f = 0
+                // a warp without keys has mw = -inf: f = 0 (and no keys at all: f unused)
+                const float f = (mw[w] == -INFINITY) ? 0.f : ex2(mw[w] - M);
                 const float *rw = red + (w * QB + qi) * RS;
                 L = fmaf(rw[D + 1], f, L);
 #pragma unroll
                 for (int e = 0; e < E; ++e) out[e] = fmaf(rw[lane * E + e], f, out[e]);
             }
-            const float inv = 1.f / L;
-            const float l_nat = (M + lg2(L)) * kLn2;  // natural-log LSE of this key range
+            // an empty key range (a short sequence's tail ranges) contributes
+            // L = -inf and O = 0 to the merge
+            const bool empty = (M == -INFINITY);
+            const float inv = empty ? 0.f : 1.f / L;
+            const float l_nat = empty ? -INFINITY : (M + lg2(L)) * kLn2;  // natural-log LSE
             const size_t row = (size_t)bh * Nq + i0 + qi;
             if (S == 1) {
 #pragma unroll
@@ -329,18 +382,15 @@ __global__ void __launch_bounds__(128)
     if (lane == 0) lse[row] = M + __logf(W);
 }
 
-template <int D, int QB>
+template <int D, int QB, bool PAGED>
 int launch_decode_t(const DecodeParams &p, cudaStream_t stream) {
     using T = DecTile<D>;
-    auto kern = fa_decode_split_kernel<D, QB>;
+    auto kern = fa_decode_split_kernel<D, QB, PAGED>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)T::SMEM_BYTES) !=
         cudaSuccess)
         return FA_ERR_CUDA;
     const dim3 grid((unsigned)p.BH, (unsigned)p.S, (unsigned)((p.Nq + QB - 1) / QB));
-    kern<<<grid, T::THREADS, T::SMEM_BYTES, stream>>>(
-        reinterpret_cast<const __nv_bfloat16 *>(p.q), reinterpret_cast<const __nv_bfloat16 *>(p.k),
-        reinterpret_cast<const __nv_bfloat16 *>(p.v), reinterpret_cast<__nv_bfloat16 *>(p.o), p.lse,
-        p.part_o, p.part_l, p.Nq, p.Nk, p.keys_per_split, p.S, p.scale_log2, p.status, p.limit_ns);
+    kern<<<grid, T::THREADS, T::SMEM_BYTES, stream>>>(p);
     if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
     if (p.S > 1) {
         const long long rows = (long long)p.BH * p.Nq;
@@ -353,12 +403,15 @@ int launch_decode_t(const DecodeParams &p, cudaStream_t stream) {
 
 template <int D>
 int launch_decode_d(const DecodeParams &p, cudaStream_t stream) {
-    return p.Nq == 1 ? launch_decode_t<D, 1>(p, stream) : launch_decode_t<D, dec_qblock<D>()>(p, stream);
+    constexpr int QB = dec_qblock<D>();
+    if (p.paged)
+        return p.Nq == 1 ? launch_decode_t<D, 1, true>(p, stream) : launch_decode_t<D, QB, true>(p, stream);
+    return p.Nq == 1 ? launch_decode_t<D, 1, false>(p, stream) : launch_decode_t<D, QB, false>(p, stream);
 }
 
 template <int D, int QB>
 int ctas_per_sm_t() {
-    auto kern = fa_decode_split_kernel<D, QB>;
+    auto kern = fa_decode_split_kernel<D, QB, false>;
     int n = 0;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)DecTile<D>::SMEM_BYTES) != cudaSuccess ||

@@ -32,6 +32,8 @@ enum WaitSite : int {
     SITE_DEC_FULL = 21,
     SITE_DEC_EMPTY = 22,
     SITE_DEC_DRAIN = 23,
+    SITE_DEC_BAD_LEN = 24,
+    SITE_DEC_BAD_PAGE = 25,
     SITE_SELFTEST = 30,
 };
 
@@ -67,12 +69,15 @@ constexpr int kBwdPad = 128;
 
 struct DecodeParams {
     const void *q;            // bf16 [BH][Nq][d]
-    const void *k, *v;        // bf16 [BH][Nk][d]
+    const void *k, *v;        // bf16 [BH][Nk][d], or paged [num_pages][H][page_size][d]
     void *o;                  // bf16 [BH][Nq][d]
     float *lse;               // fp32 [BH][Nq]
     float *part_o, *part_l;   // workspace when S > 1: [BH][S][Nq][d], [BH][S][Nq]
-    int BH, Nq, Nk, d;
+    const int *block_table;   // paged: [B][max_pages] physical page of each logical page
+    const int *seq_lens;      // paged: [B] cached tokens of each sequence
+    int BH, H, Nq, Nk, d;     // Nk: keys per head (paged: page_size * max_pages, an upper bound)
     int S, keys_per_split;    // key ranges [s*keys_per_split, ...) per CTA
+    int paged, page_size, max_pages, num_pages;
     float scale_log2;
     int *status;
     unsigned long long limit_ns;

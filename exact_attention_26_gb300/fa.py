@@ -21,10 +21,12 @@ FA_ERR_MISALIGNED = 3
 FA_ERR_CUDA = 4
 FA_ERR_TIMEOUT = 5
 FA_ERR_WORKSPACE = 6
+FA_ERR_BAD_INDEX = 7
 
 EXPORTED = ("fa_fwd", "fa_bwd", "fa_bwd_workspace_bytes", "fa_status_string", "fa_device_status",
             "fa_selftest_wait_timeout", "fa_decode", "fa_decode_num_splits",
-            "fa_decode_workspace_bytes")
+            "fa_decode_workspace_bytes", "fa_decode_paged", "fa_decode_paged_num_splits",
+            "fa_decode_paged_workspace_bytes")
 
 _vp = ctypes.c_void_p
 _int = ctypes.c_int
@@ -68,6 +70,13 @@ def load() -> ctypes.CDLL:
         lib.fa_decode_num_splits.restype = _int
         lib.fa_decode_workspace_bytes.argtypes = [_int] * 6
         lib.fa_decode_workspace_bytes.restype = ctypes.c_size_t
+        lib.fa_decode_paged.argtypes = [_vp] * 7 + [_int] * 7 + [ctypes.c_float, _int, _vp,
+                                                                ctypes.c_size_t, _vp]
+        lib.fa_decode_paged.restype = _int
+        lib.fa_decode_paged_num_splits.argtypes = [_int] * 7
+        lib.fa_decode_paged_num_splits.restype = _int
+        lib.fa_decode_paged_workspace_bytes.argtypes = [_int] * 7
+        lib.fa_decode_paged_workspace_bytes.restype = ctypes.c_size_t
         _LIB = lib
     return _LIB
 
@@ -120,6 +129,22 @@ def fa_decode_num_splits(B, H, Nq, Nk, d, num_splits=0) -> int:
 
 def fa_decode_workspace_bytes(B, H, Nq, Nk, d, num_splits=0) -> int:
     return load().fa_decode_workspace_bytes(B, H, Nq, Nk, d, num_splits)
+
+
+def fa_decode_paged(q, k_cache, v_cache, block_table, seq_lens, o, lse, B, H, Nq, d, page_size,
+                    max_pages, num_pages, scale, num_splits, workspace, workspace_bytes,
+                    stream) -> int:
+    return load().fa_decode_paged(q, k_cache, v_cache, block_table, seq_lens, o, lse, B, H, Nq, d,
+                                  page_size, max_pages, num_pages, scale, num_splits, workspace,
+                                  workspace_bytes, stream)
+
+
+def fa_decode_paged_num_splits(B, H, Nq, d, page_size, max_pages, num_splits=0) -> int:
+    return load().fa_decode_paged_num_splits(B, H, Nq, d, page_size, max_pages, num_splits)
+
+
+def fa_decode_paged_workspace_bytes(B, H, Nq, d, page_size, max_pages, num_splits=0) -> int:
+    return load().fa_decode_paged_workspace_bytes(B, H, Nq, d, page_size, max_pages, num_splits)
 
 
 def fa_status_string(status: int) -> str:
@@ -234,4 +259,47 @@ def decode(q, k, v, scale=None, num_splits=0, out=None, lse=None, workspace=None
                        B, H, Nq, Nk, d, scale, num_splits, ws_ptr, ws_len, _stream(q, stream))
     if rc != FA_OK:
         raise FaError(rc, "fa_decode")
+    return out, lse
+
+
+def decode_paged(q, k_cache, v_cache, block_table, seq_lens, scale=None, num_splits=0, out=None,
+                 lse=None, workspace=None, stream=None):
+    """Decode against a paged cache: q bf16 [B,H,Nq,d]; k_cache, v_cache bf16
+    [num_pages, H, page_size, d]; block_table int32 [B, max_pages]; seq_lens int32 [B]
+    (all CUDA).  Returns (o, lse)."""
+    _check("q", q, torch.bfloat16)
+    if q.dim() != 4:
+        raise ValueError("q must be [B, H, Nq, d]")
+    B, H, Nq, d = q.shape
+    _check("k_cache", k_cache, torch.bfloat16)
+    if k_cache.dim() != 4 or k_cache.shape[1] != H or k_cache.shape[3] != d:
+        raise ValueError("k_cache must be [num_pages, H, page_size, d]")
+    num_pages, _, page_size, _ = k_cache.shape
+    _check("v_cache", v_cache, torch.bfloat16, k_cache.shape)
+    _check("block_table", block_table, torch.int32)
+    if block_table.dim() != 2 or block_table.shape[0] != B:
+        raise ValueError("block_table must be [B, max_pages]")
+    max_pages = block_table.shape[1]
+    _check("seq_lens", seq_lens, torch.int32, (B,))
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    if out is None:
+        out = torch.empty_like(q)
+    _check("out", out, torch.bfloat16, q.shape)
+    if lse is None:
+        lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+    _check("lse", lse, torch.float32, (B, H, Nq))
+    with torch.cuda.device(q.device):
+        need = fa_decode_paged_workspace_bytes(B, H, Nq, d, page_size, max_pages, num_splits)
+        if workspace is None and need > 0:
+            workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+        if workspace is not None:
+            _check("workspace", workspace, torch.uint8)
+        ws_ptr = workspace.data_ptr() if workspace is not None else None
+        ws_len = workspace.numel() if workspace is not None else 0
+        rc = fa_decode_paged(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+                             block_table.data_ptr(), seq_lens.data_ptr(), out.data_ptr(),
+                             lse.data_ptr(), B, H, Nq, d, page_size, max_pages, num_pages, scale,
+                             num_splits, ws_ptr, ws_len, _stream(q, stream))
+    if rc != FA_OK:
+        raise FaError(rc, "fa_decode_paged")
     return out, lse

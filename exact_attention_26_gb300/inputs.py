@@ -25,6 +25,12 @@ Recipes (one per workload of the measurement plan):
   (``seed + 1``) picks one key per block of ``boost_block`` keys of every head and
   adds ``boost`` to that K row, so some key ranges dominate others.
 
+* ``paged_cache``: rearranges a contiguous cache k, v [B, H, Nk, d] (Nk a multiple
+  of ``page_size``) into pages [num_pages, H, page_size, d]: logical page p of
+  sequence b goes to physical page perm[b * Nk / page_size + p], where perm is
+  ``torch.randperm`` of the B * Nk / page_size pages from a generator seeded with
+  ``seed``; returns the paged k, v and the int32 block table [B, Nk / page_size].
+
 All tensors are contiguous bf16, on the CPU unless a device is given; callers
 move them.
 """
@@ -32,7 +38,7 @@ from __future__ import annotations
 
 import torch
 
-__all__ = ["normal_qkv", "boosted_qkv", "decode_qkv", "sample_rows", "to_f64"]
+__all__ = ["normal_qkv", "boosted_qkv", "decode_qkv", "paged_cache", "sample_rows", "to_f64"]
 
 
 def _draw(gen: torch.Generator, shape, mult: float = 1.0) -> torch.Tensor:
@@ -103,6 +109,25 @@ def decode_qkv(B: int, H: int, Nq: int, Nk: int, d: int, seed: int = 0, mult: fl
                         torch.full((B, H, nblk, d), float(boost), device=device))
         k = kf.to(torch.bfloat16).contiguous()
     return q, k, v
+
+
+def paged_cache(k: torch.Tensor, v: torch.Tensor, page_size: int, seed: int = 3):
+    """Return (k_cache, v_cache [num_pages, H, page_size, d], block_table int32 [B, P])."""
+    B, H, Nk, d = k.shape
+    if Nk % page_size:
+        raise ValueError("Nk must be a multiple of page_size")
+    P = Nk // page_size
+    gen = torch.Generator(device="cpu")
+    gen.manual_seed(seed)
+    perm = torch.randperm(B * P, generator=gen).to(k.device)
+
+    def pages(x):
+        xp = x.reshape(B, H, P, page_size, d).permute(0, 2, 1, 3, 4).reshape(B * P, H, page_size, d)
+        out = torch.empty_like(xp)
+        out[perm] = xp
+        return out.contiguous()
+
+    return pages(k), pages(v), perm.reshape(B, P).to(torch.int32).contiguous()
 
 
 def sample_rows(N: int, count: int, seed: int = 2) -> torch.Tensor:

@@ -49,7 +49,9 @@ typedef enum {
     FA_ERR_MISALIGNED = 3,  /* a pointer is not 16-byte aligned */
     FA_ERR_CUDA = 4,        /* a CUDA runtime/driver call failed */
     FA_ERR_TIMEOUT = 5,     /* a bounded in-kernel wait ran out (device status) */
-    FA_ERR_WORKSPACE = 6    /* workspace missing or smaller than required */
+    FA_ERR_WORKSPACE = 6,   /* workspace missing or smaller than required */
+    FA_ERR_BAD_INDEX = 7    /* device status: a block-table entry or sequence length out
+                               of range (paged decode); that CTA wrote nothing */
 } fa_status;
 
 /*
@@ -162,6 +164,44 @@ int fa_decode_num_splits(int B, int H, int Nq, int Nk, int d, int num_splits);
  * Returns 0 for invalid sizes as well.
  */
 size_t fa_decode_workspace_bytes(int B, int H, int Nq, int Nk, int d, int num_splits);
+
+/*
+ * Decode against a paged key/value cache (course page "10 FlashAttention",
+ * section "Paged FlashAttention": the K/V blocks of a sequence are gathered
+ * through a block table instead of being read contiguously).  Same operation,
+ * split and merge as fa_decode, except that sequence b has its own length
+ * seq_lens[b] and its key j lives in physical page block_table[b][j / page_size]
+ * at row j % page_size:
+ *   k_cache, v_cache : bf16 [num_pages][H][page_size][d]; one page holds
+ *                      page_size consecutive tokens of every head, each head's
+ *                      rows contiguous (one bulk copy per page and head).
+ *   block_table      : int32 [B][max_pages_per_seq], device memory; entries in
+ *                      [0, num_pages) for the pages a sequence uses (the rest are
+ *                      never read).
+ *   seq_lens         : int32 [B], device memory; 1 <= seq_lens[b] <=
+ *                      page_size * max_pages_per_seq.
+ *   q, o, lse        : as in fa_decode, [B][H][Nq][d] and [B][H][Nq].
+ *   page_size, max_pages_per_seq, num_pages >= 1; page_size * max_pages_per_seq
+ *   < 2^31.  Pages of any size work; each page costs one copy per stage.
+ * The table and the lengths live on the device, so they are checked there: an
+ * out-of-range entry or length makes the affected CTA write nothing and records
+ * FA_ERR_BAD_INDEX in the device status word (fa_device_status); nothing outside
+ * the cache is read.  The key ranges are cut from the longest possible sequence;
+ * ranges past a shorter sequence's end contribute nothing to its merge.
+ * Workspace as in fa_decode, sized by fa_decode_paged_workspace_bytes.
+ */
+int fa_decode_paged(const void *q, const void *k_cache, const void *v_cache,
+                    const int *block_table, const int *seq_lens, void *o, float *lse, int B, int H,
+                    int Nq, int d, int page_size, int max_pages_per_seq, int num_pages, float scale,
+                    int num_splits, void *workspace, size_t workspace_bytes, void *stream);
+
+/* Key ranges (>= 1) fa_decode_paged would use, or minus an fa_status code. */
+int fa_decode_paged_num_splits(int B, int H, int Nq, int d, int page_size, int max_pages_per_seq,
+                               int num_splits);
+
+/* Workspace bytes fa_decode_paged needs (0 when one range suffices or sizes are invalid). */
+size_t fa_decode_paged_workspace_bytes(int B, int H, int Nq, int d, int page_size,
+                                       int max_pages_per_seq, int num_splits);
 
 /*
  * Diagnostic: launches one warp that waits, through the same bounded wait the

@@ -44,7 +44,7 @@ def test_library_exports_every_declared_symbol(fa):
 
 
 def test_status_strings(fa):
-    for code in range(7):
+    for code in range(8):
         s = fa.fa_status_string(code)
         assert s and s != "unknown fa_status"
     assert fa.fa_status_string(99) == "unknown fa_status"
@@ -131,3 +131,28 @@ def test_decode_split_queries_reject_bad_sizes(fa):
     assert fa.fa_decode_num_splits(1, 1, 1, 100, 128, -3) == -1
     assert fa.fa_decode_workspace_bytes(1, 1, 0, 100, 128, 0) == 0
     assert fa.fa_decode_workspace_bytes(1, 1, 1, 100, 80, 2) == 0
+
+
+def _pdec(fa, **kw):
+    a = dict(q=DUMMY, kc=DUMMY, vc=DUMMY, bt=DUMMY, sl=DUMMY, o=DUMMY, lse=DUMMY, B=2, H=2, Nq=1,
+             d=128, ps=16, mp=8, np_=16, scale=0.1, splits=0, ws=None, ws_bytes=0, stream=None)
+    a.update(kw)
+    return fa.fa_decode_paged(a["q"], a["kc"], a["vc"], a["bt"], a["sl"], a["o"], a["lse"], a["B"],
+                              a["H"], a["Nq"], a["d"], a["ps"], a["mp"], a["np_"], a["scale"],
+                              a["splits"], a["ws"], a["ws_bytes"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=None), 1), (dict(kc=None), 1), (dict(bt=None), 1), (dict(sl=None), 1), (dict(lse=None), 1),
+    (dict(B=0), 1), (dict(Nq=0), 1), (dict(ps=0), 1), (dict(mp=0), 1), (dict(np_=0), 1),
+    (dict(ps=1 << 16, mp=1 << 16), 1), (dict(d=80), 2), (dict(scale=-1.0), 1), (dict(splits=-2), 1),
+    (dict(kc=DUMMY + 8), 3), (dict(bt=DUMMY + 2), 3), (dict(sl=DUMMY + 1), 3),
+])
+def test_decode_paged_rejects_bad_arguments(fa, kw, code):
+    assert _pdec(fa, **kw) == code
+
+
+def test_decode_paged_split_queries_reject_bad_sizes(fa):
+    assert fa.fa_decode_paged_num_splits(1, 1, 1, 128, 0, 4, 0) == -1
+    assert fa.fa_decode_paged_num_splits(1, 1, 1, 96, 16, 4, 0) == -2
+    assert fa.fa_decode_paged_workspace_bytes(1, 1, 1, 128, 16, 0, 2) == 0
