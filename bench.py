@@ -64,6 +64,13 @@ DEC_WORKLOADS = [
 ]
 
 
+# Paged decode: the same B8 H32 Nk32768 d128 cache in 16-token pages scattered at random.
+PAGED_WORKLOADS = [
+    ("B8_H32_Nq1_Nk32768_d128_page16", 8, 32, 1, 32768, 128, 16),
+    ("B8_H32_Nq1_Nk32768_d128_page64", 8, 32, 1, 32768, 128, 64),
+]
+
+
 def decode_bytes(B, H, Nq, Nk, d):
     """Algorithmic HBM bytes of one decode call: read K, V (bf16) and q, write o
     (bf16) and L (fp32); the partial results stay in L2."""
@@ -404,6 +411,24 @@ def sweep_decode(fa, torch, dev, flush, peaks):
                                   "peak": peaks["hbm_gbs"], "unit": "GB/s",
                                   "frac": round(gbs / peaks["hbm_gbs"], 4)}}
         del q, k, v, o, lse, ws
+    from exact_attention_26_gb300.inputs import paged_cache
+    for name, B, H, Nq, Nk, d, ps in PAGED_WORKLOADS:
+        q, k, v = decode_qkv(B, H, Nq, Nk, d, seed=0, device=dev)
+        kc, vc, bt = paged_cache(k, v, ps)
+        del k, v
+        lens = torch.full((B,), Nk, dtype=torch.int32, device=dev)
+        o = torch.empty_like(q)
+        lse = torch.empty((B, H, Nq), dtype=torch.float32, device=dev)
+        need = fa.fa_decode_paged_workspace_bytes(B, H, Nq, d, ps, Nk // ps, 0)
+        ws = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+        ms = _time_call(torch, dev, lambda: fa.decode_paged(q, kc, vc, bt, lens, out=o, lse=lse,
+                                                            workspace=ws), flush)
+        gbs = decode_bytes(B, H, Nq, Nk, d) / (ms * 1e-3) / 1e9
+        out[name] = {"ms": round(ms, 5), "GB/s": round(gbs, 1),
+                     "roofline": {"bound": "hbm", "achieved": round(gbs, 1),
+                                  "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                  "frac": round(gbs / peaks["hbm_gbs"], 4)}}
+        del q, kc, vc, bt, o, lse, ws
     return out
 
 

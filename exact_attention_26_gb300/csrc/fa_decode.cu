@@ -138,63 +138,65 @@ __global__ void __launch_bounds__(DecTile<D>::THREADS, 2)
     float m[QB], l[QB], acc[QB][E];
     if (warp == T::NWC) {
         // ------------------------------------------------------------ producer
-        if (lane == 0) {
-            int issued = 0;
-            const int h = bh % p.H;
-            const int *bt = PAGED ? p.block_table + (size_t)(bh / p.H) * p.max_pages : nullptr;
-            for (int t = 0; t < n_tiles; ++t) {
-                const int slot = t % STAGES;
-                if (t >= STAGES && !mbar_wait(bar_empty + 8 * slot, ((t / STAGES) - 1) & 1, g,
-                                              SITE_DEC_EMPTY))
+        // The whole warp runs the loop.  Contiguous cache: lane 0 issues one copy of K
+        // and one of V per stage.  Paged cache: lane i looks up page i of the stage
+        // (all lookups in flight at once), the warp votes on their validity, and every
+        // lane issues the copies of its own page segment.
+        int issued = 0;
+        const int h = bh % p.H;
+        const int *bt = PAGED ? p.block_table + (size_t)(bh / p.H) * p.max_pages : nullptr;
+        for (int t = 0; t < n_tiles; ++t) {
+            const int slot = t % STAGES;
+            if (t >= STAGES && !mbar_wait_warp(bar_empty + 8 * slot, ((t / STAGES) - 1) & 1, g,
+                                               SITE_DEC_EMPTY))
+                break;
+            const int j0 = k0 + t * BK;
+            const int rows = min(BK, k1 - j0);
+            const uint32_t dst = sbase + slot * T::STAGE_BYTES;
+            const uint32_t fb = bar_full + 8 * slot;
+            if constexpr (PAGED) {
+                // every physical page of this stage is checked before any byte is
+                // promised or read: an entry outside [0, num_pages) stops the CTA
+                const int ps = p.page_size;
+                const int pg0 = j0 / ps, nseg = (j0 + rows - 1) / ps - pg0 + 1;
+                bool ok = true;
+                for (int i = lane; i < nseg; i += 32) {
+                    const int phys = bt[pg0 + i];
+                    ok = ok && phys >= 0 && phys < p.num_pages;
+                }
+                if (!__all_sync(kFull, ok)) {
+                    if (lane == 0) flag_bad_index(p.status, abort_flag, SITE_DEC_BAD_PAGE);
                     break;
-                const int j0 = k0 + t * BK;
-                const int rows = min(BK, k1 - j0);
-                const uint32_t dst = sbase + slot * T::STAGE_BYTES;
-                const uint32_t fb = bar_full + 8 * slot;
-                if constexpr (PAGED) {
-                    // every physical page of this stage is checked before any byte is
-                    // promised or read: an entry outside [0, num_pages) stops the CTA
-                    bool pages_ok = true;
-                    for (int j = j0; j < j0 + rows; j = (j / p.page_size + 1) * p.page_size) {
-                        const int phys = bt[j / p.page_size];
-                        if (phys < 0 || phys >= p.num_pages) {
-                            pages_ok = false;
-                            break;
-                        }
-                    }
-                    if (!pages_ok) {
-                        flag_bad_index(p.status, abort_flag, SITE_DEC_BAD_PAGE);
-                        break;
-                    }
-                    mbar_arrive_expect_tx(fb, (uint32_t)(2 * rows * D * 2));
-                    // one copy of K and one of V per page segment of the stage
-                    for (int j = j0, r = 0; j < j0 + rows;) {
-                        const int pg = j / p.page_size, off = j - pg * p.page_size;
-                        const int n = min(p.page_size - off, j0 + rows - j);
-                        const size_t src = (((size_t)bt[pg] * p.H + h) * p.page_size + off) * D;
-                        const uint32_t bytes = (uint32_t)(n * D * 2);
-                        bulk_load(dst + r * D * 2, k + src, bytes, fb);
-                        bulk_load(dst + T::TILE_BYTES + r * D * 2, v + src, bytes, fb);
-                        j += n;
-                        r += n;
-                    }
-                } else {
+                }
+                if (lane == 0) mbar_arrive_expect_tx(fb, (uint32_t)(2 * rows * D * 2));
+                __syncwarp();
+                for (int i = lane; i < nseg; i += 32) {
+                    const int pg = pg0 + i;
+                    const int js = max(j0, pg * ps), je = min(j0 + rows, (pg + 1) * ps);
+                    const size_t src = (((size_t)bt[pg] * p.H + h) * ps + (js - pg * ps)) * D;
+                    const uint32_t off = (uint32_t)((js - j0) * D * 2), bytes = (uint32_t)((je - js) * D * 2);
+                    bulk_load(dst + off, k + src, bytes, fb);
+                    bulk_load(dst + T::TILE_BYTES + off, v + src, bytes, fb);
+                }
+            } else {
+                if (lane == 0) {
                     const size_t src = ((size_t)bh * p.Nk + j0) * D;
                     const uint32_t bytes = (uint32_t)(rows * D * 2);
                     mbar_arrive_expect_tx(fb, 2 * bytes);
                     bulk_load(dst, k + src, bytes, fb);
                     bulk_load(dst + T::TILE_BYTES, v + src, bytes, fb);
                 }
-                ++issued;
             }
-            if (*abort_flag) {
-                // let every copy still in flight land before the CTA exits
-                volatile int never = 0;
-                const Guard g2{p.status, &never, kWaitLimitNs};
-                for (int t = (issued > STAGES ? issued - STAGES : 0); t < issued; ++t)
-                    mbar_wait(bar_full + 8 * (t % STAGES), (t / STAGES) & 1, g2, SITE_DEC_DRAIN);
-            }
+            ++issued;
         }
+        if (lane == 0 && *abort_flag) {
+            // let every copy still in flight land before the CTA exits
+            volatile int never = 0;
+            const Guard g2{p.status, &never, kWaitLimitNs};
+            for (int t = (issued > STAGES ? issued - STAGES : 0); t < issued; ++t)
+                mbar_wait(bar_full + 8 * (t % STAGES), (t / STAGES) & 1, g2, SITE_DEC_DRAIN);
+        }
+        __syncwarp();
     } else {
         // ------------------------------------------------------------ compute warps
         float qv[QB][E];
