@@ -401,12 +401,12 @@ def sweep_decode(fa, torch, dev, flush, peaks):
         q, k, v = decode_qkv(B, H, Nq, Nk, d, seed=0, device=dev)
         o = torch.empty_like(q)
         lse = torch.empty((B, H, Nq), dtype=torch.float32, device=dev)
-        need = fa.fa_decode_workspace_bytes(B, H, Nq, Nk, d, 0)
+        need = fa.fa_decode_workspace_bytes(B, H, H, Nq, Nk, d, 0)
         ws = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
         ms = _time_call(torch, dev, lambda: fa.decode(q, k, v, out=o, lse=lse, workspace=ws), flush)
         gbs = decode_bytes(B, H, Nq, Nk, d) / (ms * 1e-3) / 1e9
         out[name] = {"ms": round(ms, 5), "GB/s": round(gbs, 1),
-                     "splits": fa.fa_decode_num_splits(B, H, Nq, Nk, d, 0),
+                     "splits": fa.fa_decode_num_splits(B, H, H, Nq, Nk, d, 0),
                      "roofline": {"bound": "hbm", "achieved": round(gbs, 1),
                                   "peak": peaks["hbm_gbs"], "unit": "GB/s",
                                   "frac": round(gbs / peaks["hbm_gbs"], 4)}}
@@ -419,7 +419,7 @@ def sweep_decode(fa, torch, dev, flush, peaks):
         lens = torch.full((B,), Nk, dtype=torch.int32, device=dev)
         o = torch.empty_like(q)
         lse = torch.empty((B, H, Nq), dtype=torch.float32, device=dev)
-        need = fa.fa_decode_paged_workspace_bytes(B, H, Nq, d, ps, Nk // ps, 0)
+        need = fa.fa_decode_paged_workspace_bytes(B, H, H, Nq, d, ps, Nk // ps, 0)
         ws = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
         ms = _time_call(torch, dev, lambda: fa.decode_paged(q, kc, vc, bt, lens, out=o, lse=lse,
                                                             workspace=ws), flush)

@@ -124,11 +124,23 @@ int fwd_block_n(int d) { return d == 256 ? 64 : 128; }
 
 using namespace fa;
 
-extern "C" int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B,
-                      int H, int N, int d, int causal, float scale, void *stream) {
+namespace fa {
+namespace {
+// Query heads per key/value head, or 0 if Hkv does not divide H.
+int gqa_group(int H, int Hkv) {
+    if (Hkv < 1 || Hkv > H || H % Hkv != 0) return 0;
+    return H / Hkv;
+}
+}  // namespace
+}  // namespace fa
+
+extern "C" int fa_fwd_gqa(const void *q, const void *k, const void *v, void *o, float *lse, int B,
+                          int H, int Hkv, int N, int d, int causal, float scale, void *stream) {
     if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
     int rc = check_sizes(B, H, N, d, true);
     if (rc != FA_OK) return rc;
+    const int group = gqa_group(H, Hkv);
+    if (group == 0) return FA_ERR_INVALID_ARG;
     if ((rc = check_scale(scale)) != FA_OK) return rc;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
         return FA_ERR_MISALIGNED;
@@ -138,12 +150,14 @@ extern "C" int fa_fwd(const void *q, const void *k, const void *v, void *o, floa
     FwdParams p{};
     const int BH = B * H;
     if ((rc = make_bhnd_map(&p.tm_q, q, BH, N, d, 128)) != FA_OK) return rc;
-    if ((rc = make_bhnd_map(&p.tm_k, k, BH, N, d, fwd_block_n(d))) != FA_OK) return rc;
-    if ((rc = make_bhnd_map(&p.tm_v, v, BH, N, d, fwd_block_n(d))) != FA_OK) return rc;
+    if ((rc = make_bhnd_map(&p.tm_k, k, B * Hkv, N, d, fwd_block_n(d))) != FA_OK) return rc;
+    if ((rc = make_bhnd_map(&p.tm_v, v, B * Hkv, N, d, fwd_block_n(d))) != FA_OK) return rc;
     p.o = o;
     p.lse = lse;
     p.N = N;
     p.BH = BH;
+    p.H = H;
+    p.group = group;
     p.d = d;
     p.causal = causal ? 1 : 0;
     p.scale_log2 = scale * kLog2e;
@@ -153,6 +167,11 @@ extern "C" int fa_fwd(const void *q, const void *k, const void *v, void *o, floa
     return launch_fwd(p, static_cast<cudaStream_t>(stream));
 }
 
+extern "C" int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B,
+                      int H, int N, int d, int causal, float scale, void *stream) {
+    return fa_fwd_gqa(q, k, v, o, lse, B, H, H, N, d, causal, scale, stream);
+}
+
 extern "C" size_t fa_bwd_workspace_bytes(int B, int H, int N, int d) {
     if (check_sizes(B, H, N, d, false) != FA_OK) return 0;
     const size_t npad = round_up((size_t)N, kBwdPad);
@@ -160,13 +179,15 @@ extern "C" size_t fa_bwd_workspace_bytes(int B, int H, int N, int d) {
     return 2 * (size_t)B * (size_t)H * npad * sizeof(float);
 }
 
-extern "C" int fa_bwd(const void *q, const void *k, const void *v, const void *o,
-                      const float *lse, const void *dout, float *dq, float *dk, float *dv, int B,
-                      int H, int N, int d, int causal, float scale, void *workspace,
-                      size_t workspace_bytes, void *stream) {
+extern "C" int fa_bwd_gqa(const void *q, const void *k, const void *v, const void *o,
+                          const float *lse, const void *dout, float *dq, float *dk, float *dv,
+                          int B, int H, int Hkv, int N, int d, int causal, float scale,
+                          void *workspace, size_t workspace_bytes, void *stream) {
     if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
     int rc = check_sizes(B, H, N, d, false);
     if (rc != FA_OK) return rc;
+    const int group = gqa_group(H, Hkv);
+    if (group == 0) return FA_ERR_INVALID_ARG;
     if ((rc = check_scale(scale)) != FA_OK) return rc;
     const size_t need = fa_bwd_workspace_bytes(B, H, N, d);
     if (!workspace || workspace_bytes < need) return FA_ERR_WORKSPACE;
@@ -183,8 +204,8 @@ extern "C" int fa_bwd(const void *q, const void *k, const void *v, const void *o
     const int q_rows = (d == 128) ? 64 : 128;  // query rows per backward q-block
     if ((rc = make_bhnd_map(&p.tm_q, q, BH, N, d, q_rows)) != FA_OK) return rc;
     if ((rc = make_bhnd_map(&p.tm_do, dout, BH, N, d, q_rows)) != FA_OK) return rc;
-    if ((rc = make_bhnd_map(&p.tm_k, k, BH, N, d, 128)) != FA_OK) return rc;
-    if ((rc = make_bhnd_map(&p.tm_v, v, BH, N, d, 128)) != FA_OK) return rc;
+    if ((rc = make_bhnd_map(&p.tm_k, k, B * Hkv, N, d, 128)) != FA_OK) return rc;
+    if ((rc = make_bhnd_map(&p.tm_v, v, B * Hkv, N, d, 128)) != FA_OK) return rc;
     p.o = o;
     p.dout = dout;
     p.lse = lse;
@@ -196,6 +217,8 @@ extern "C" int fa_bwd(const void *q, const void *k, const void *v, const void *o
     p.N = N;
     p.Npad = npad;
     p.BH = BH;
+    p.H = H;
+    p.group = group;
     p.d = d;
     p.causal = causal ? 1 : 0;
     p.scale = scale;
@@ -206,12 +229,23 @@ extern "C" int fa_bwd(const void *q, const void *k, const void *v, const void *o
     return launch_bwd(p, static_cast<cudaStream_t>(stream));
 }
 
+extern "C" int fa_bwd(const void *q, const void *k, const void *v, const void *o,
+                      const float *lse, const void *dout, float *dq, float *dk, float *dv, int B,
+                      int H, int N, int d, int causal, float scale, void *workspace,
+                      size_t workspace_bytes, void *stream) {
+    return fa_bwd_gqa(q, k, v, o, lse, dout, dq, dk, dv, B, H, H, N, d, causal, scale, workspace,
+                      workspace_bytes, stream);
+}
+
 namespace fa {
 namespace {
 
-int check_decode_sizes(int B, int H, int Nq, int Nk, int d) {
+// Decode sizes.  R = (H / Hkv) * Nq query rows share each key/value head.
+int check_decode_sizes(int B, int H, int Hkv, int Nq, int Nk, int d) {
     if (B < 1 || H < 1 || Nq < 1 || Nk < 1 || Nq > 65535) return FA_ERR_INVALID_ARG;
-    if ((long long)B * H * Nq >= (1LL << 31) || (long long)B * H * Nk >= (1LL << 31))
+    if (gqa_group(H, Hkv) == 0) return FA_ERR_INVALID_ARG;
+    if ((long long)(H / Hkv) * Nq > 65535) return FA_ERR_INVALID_ARG;
+    if ((long long)B * H * Nq >= (1LL << 31) || (long long)B * Hkv * Nk >= (1LL << 31))
         return FA_ERR_INVALID_ARG;
     if (d != 64 && d != 128 && d != 256) return FA_ERR_UNSUPPORTED;
     return FA_OK;
@@ -222,18 +256,19 @@ int check_decode_sizes(int B, int H, int Nq, int Nk, int d) {
 // count minimises a wave model of the launch: with `slots` CTAs resident at once,
 // a launch of C CTAs of T stages each takes about ceil(C / slots) * (T + 4) stage
 // times (four stages of fill and merge per CTA), and each range keeps at least
-// eight stages so the ring has something to overlap.
-void decode_split(int B, int H, int Nq, int Nk, int d, int requested, int num_sms, int *S,
+// eight stages so the ring has something to overlap.  BHkv key/value heads, R
+// query rows per key/value head.
+void decode_split(long long BHkv, int R, int Nk, int d, int requested, int num_sms, int *S,
                   int *keys_per_split) {
     const long long bk = decode_block_keys(d);
     const long long tiles = (Nk + bk - 1) / bk;
-    const long long qb = decode_query_block(d, Nq);
-    const long long base = (long long)B * H * ((Nq + qb - 1) / qb);
+    const long long qb = decode_query_block(d, R);
+    const long long base = BHkv * ((R + qb - 1) / qb);
     long long s = 1;
     if (requested > 0) {
         s = requested;
     } else {
-        const long long slots = (long long)(num_sms > 0 ? num_sms : 1) * decode_ctas_per_sm(d, Nq);
+        const long long slots = (long long)(num_sms > 0 ? num_sms : 1) * decode_ctas_per_sm(d, R);
         long long cap = tiles / 8;
         if (cap < 1) cap = 1;
         if (cap > 1024) cap = 1024;
@@ -255,69 +290,81 @@ void decode_split(int B, int H, int Nq, int Nk, int d, int requested, int num_sm
     *S = (int)((Nk + per - 1) / per);
 }
 
-size_t decode_ws_bytes(long long BH, int S, int Nq, int d) {
+size_t decode_ws_bytes(long long rows, int S, int d) {  // rows = B * H * Nq
     if (S <= 1) return 0;
-    const size_t po = (size_t)BH * S * Nq * d * sizeof(float);
-    return round_up(po, 256) + (size_t)BH * S * Nq * sizeof(float);
+    const size_t po = (size_t)rows * S * d * sizeof(float);
+    return round_up(po, 256) + (size_t)rows * S * sizeof(float);
 }
 
-}  // namespace
-}  // namespace fa
-
-extern "C" int fa_decode_num_splits(int B, int H, int Nq, int Nk, int d, int num_splits) {
-    int rc = check_decode_sizes(B, H, Nq, Nk, d);
-    if (rc != FA_OK) return -rc;
-    if (num_splits < 0) return -FA_ERR_INVALID_ARG;
+// Shared tail of fa_decode and fa_decode_paged: split, workspace, launch.
+int decode_launch(DecodeParams &p, int B, int num_splits, void *workspace, size_t workspace_bytes,
+                  void *stream) {
     DeviceCache *dc = nullptr;
-    if ((rc = current_device(&dc)) != FA_OK) return -rc;
-    int S = 1, per = 0;
-    decode_split(B, H, Nq, Nk, d, num_splits, dc->num_sms, &S, &per);
-    return S;
-}
-
-extern "C" size_t fa_decode_workspace_bytes(int B, int H, int Nq, int Nk, int d, int num_splits) {
-    const int S = fa_decode_num_splits(B, H, Nq, Nk, d, num_splits);
-    if (S < 1) return 0;
-    return decode_ws_bytes((long long)B * H, S, Nq, d);
-}
-
-extern "C" int fa_decode(const void *q, const void *k, const void *v, void *o, float *lse, int B,
-                         int H, int Nq, int Nk, int d, float scale, int num_splits,
-                         void *workspace, size_t workspace_bytes, void *stream) {
-    if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
-    int rc = check_decode_sizes(B, H, Nq, Nk, d);
+    int rc = current_device(&dc);
     if (rc != FA_OK) return rc;
-    if (num_splits < 0) return FA_ERR_INVALID_ARG;
-    if ((rc = check_scale(scale)) != FA_OK) return rc;
-    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
-        return FA_ERR_MISALIGNED;
-    DeviceCache *dc = nullptr;
-    if ((rc = current_device(&dc)) != FA_OK) return rc;
-    DecodeParams p{};
-    decode_split(B, H, Nq, Nk, d, num_splits, dc->num_sms, &p.S, &p.keys_per_split);
-    const long long BH = (long long)B * H;
-    const size_t need = decode_ws_bytes(BH, p.S, Nq, d);
+    const int R = p.group * p.Nq;
+    decode_split((long long)B * p.Hkv, R, p.Nk, p.d, num_splits, dc->num_sms, &p.S,
+                 &p.keys_per_split);
+    const long long rows = (long long)B * p.H * p.Nq;
+    const size_t need = decode_ws_bytes(rows, p.S, p.d);
     if (need > 0) {
         if (!workspace || workspace_bytes < need) return FA_ERR_WORKSPACE;
         if (!aligned16(workspace)) return FA_ERR_MISALIGNED;
         p.part_o = static_cast<float *>(workspace);
         p.part_l = reinterpret_cast<float *>(static_cast<char *>(workspace) +
-                                             round_up((size_t)BH * p.S * Nq * d * sizeof(float), 256));
+                                             round_up((size_t)rows * p.S * p.d * sizeof(float), 256));
     }
+    p.BH = B * p.H;
+    p.status = dc->status;
+    p.limit_ns = kWaitLimitNs;
+    return launch_decode(p, static_cast<cudaStream_t>(stream));
+}
+
+}  // namespace
+}  // namespace fa
+
+extern "C" int fa_decode_num_splits(int B, int H, int Hkv, int Nq, int Nk, int d, int num_splits) {
+    int rc = check_decode_sizes(B, H, Hkv, Nq, Nk, d);
+    if (rc != FA_OK) return -rc;
+    if (num_splits < 0) return -FA_ERR_INVALID_ARG;
+    DeviceCache *dc = nullptr;
+    if ((rc = current_device(&dc)) != FA_OK) return -rc;
+    int S = 1, per = 0;
+    decode_split((long long)B * Hkv, (H / Hkv) * Nq, Nk, d, num_splits, dc->num_sms, &S, &per);
+    return S;
+}
+
+extern "C" size_t fa_decode_workspace_bytes(int B, int H, int Hkv, int Nq, int Nk, int d,
+                                            int num_splits) {
+    const int S = fa_decode_num_splits(B, H, Hkv, Nq, Nk, d, num_splits);
+    if (S < 1) return 0;
+    return decode_ws_bytes((long long)B * H * Nq, S, d);
+}
+
+extern "C" int fa_decode(const void *q, const void *k, const void *v, void *o, float *lse, int B,
+                         int H, int Hkv, int Nq, int Nk, int d, float scale, int num_splits,
+                         void *workspace, size_t workspace_bytes, void *stream) {
+    if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
+    int rc = check_decode_sizes(B, H, Hkv, Nq, Nk, d);
+    if (rc != FA_OK) return rc;
+    if (num_splits < 0) return FA_ERR_INVALID_ARG;
+    if ((rc = check_scale(scale)) != FA_OK) return rc;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+        return FA_ERR_MISALIGNED;
+    DecodeParams p{};
     p.q = q;
     p.k = k;
     p.v = v;
     p.o = o;
     p.lse = lse;
-    p.BH = (int)BH;
     p.H = H;
+    p.Hkv = Hkv;
+    p.group = H / Hkv;
     p.Nq = Nq;
     p.Nk = Nk;
     p.d = d;
     p.scale_log2 = scale * kLog2e;
-    p.status = dc->status;
-    p.limit_ns = kWaitLimitNs;
-    return launch_decode(p, static_cast<cudaStream_t>(stream));
+    return decode_launch(p, B, num_splits, workspace, workspace_bytes, stream);
 }
 
 namespace fa {
@@ -327,58 +374,48 @@ bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0
 
 // Sizes of a paged decode; the longest possible sequence page_size * max_pages
 // plays the role of Nk for the split.
-int check_paged_sizes(int B, int H, int Nq, int d, int page_size, int max_pages, int num_pages) {
+int check_paged_sizes(int B, int H, int Hkv, int Nq, int d, int page_size, int max_pages,
+                      int num_pages) {
     if (page_size < 1 || max_pages < 1 || num_pages < 1) return FA_ERR_INVALID_ARG;
     const long long nk = (long long)page_size * max_pages;
     if (nk >= (1LL << 31) || (long long)B * max_pages >= (1LL << 31)) return FA_ERR_INVALID_ARG;
-    return check_decode_sizes(B, H, Nq, 1, d);
+    return check_decode_sizes(B, H, Hkv, Nq, 1, d);
 }
 
 }  // namespace
 }  // namespace fa
 
-extern "C" int fa_decode_paged_num_splits(int B, int H, int Nq, int d, int page_size,
+extern "C" int fa_decode_paged_num_splits(int B, int H, int Hkv, int Nq, int d, int page_size,
                                           int max_pages_per_seq, int num_splits) {
-    int rc = check_paged_sizes(B, H, Nq, d, page_size, max_pages_per_seq, 1);
+    int rc = check_paged_sizes(B, H, Hkv, Nq, d, page_size, max_pages_per_seq, 1);
     if (rc != FA_OK) return -rc;
-    return fa_decode_num_splits(B, H, Nq, page_size * max_pages_per_seq, d, num_splits);
+    return fa_decode_num_splits(B, H, Hkv, Nq, page_size * max_pages_per_seq, d, num_splits);
 }
 
-extern "C" size_t fa_decode_paged_workspace_bytes(int B, int H, int Nq, int d, int page_size,
-                                                  int max_pages_per_seq, int num_splits) {
-    const int S = fa_decode_paged_num_splits(B, H, Nq, d, page_size, max_pages_per_seq, num_splits);
+extern "C" size_t fa_decode_paged_workspace_bytes(int B, int H, int Hkv, int Nq, int d,
+                                                  int page_size, int max_pages_per_seq,
+                                                  int num_splits) {
+    const int S =
+        fa_decode_paged_num_splits(B, H, Hkv, Nq, d, page_size, max_pages_per_seq, num_splits);
     if (S < 1) return 0;
-    return decode_ws_bytes((long long)B * H, S, Nq, d);
+    return decode_ws_bytes((long long)B * H * Nq, S, d);
 }
 
 extern "C" int fa_decode_paged(const void *q, const void *k_cache, const void *v_cache,
                                const int *block_table, const int *seq_lens, void *o, float *lse,
-                               int B, int H, int Nq, int d, int page_size, int max_pages_per_seq,
-                               int num_pages, float scale, int num_splits, void *workspace,
-                               size_t workspace_bytes, void *stream) {
+                               int B, int H, int Hkv, int Nq, int d, int page_size,
+                               int max_pages_per_seq, int num_pages, float scale, int num_splits,
+                               void *workspace, size_t workspace_bytes, void *stream) {
     if (!q || !k_cache || !v_cache || !block_table || !seq_lens || !o || !lse)
         return FA_ERR_INVALID_ARG;
-    int rc = check_paged_sizes(B, H, Nq, d, page_size, max_pages_per_seq, num_pages);
+    int rc = check_paged_sizes(B, H, Hkv, Nq, d, page_size, max_pages_per_seq, num_pages);
     if (rc != FA_OK) return rc;
     if (num_splits < 0) return FA_ERR_INVALID_ARG;
     if ((rc = check_scale(scale)) != FA_OK) return rc;
     if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o) ||
         !aligned16(lse) || !aligned4(block_table) || !aligned4(seq_lens))
         return FA_ERR_MISALIGNED;
-    DeviceCache *dc = nullptr;
-    if ((rc = current_device(&dc)) != FA_OK) return rc;
-    const int nk_max = page_size * max_pages_per_seq;
     DecodeParams p{};
-    decode_split(B, H, Nq, nk_max, d, num_splits, dc->num_sms, &p.S, &p.keys_per_split);
-    const long long BH = (long long)B * H;
-    const size_t need = decode_ws_bytes(BH, p.S, Nq, d);
-    if (need > 0) {
-        if (!workspace || workspace_bytes < need) return FA_ERR_WORKSPACE;
-        if (!aligned16(workspace)) return FA_ERR_MISALIGNED;
-        p.part_o = static_cast<float *>(workspace);
-        p.part_l = reinterpret_cast<float *>(static_cast<char *>(workspace) +
-                                             round_up((size_t)BH * p.S * Nq * d * sizeof(float), 256));
-    }
     p.q = q;
     p.k = k_cache;
     p.v = v_cache;
@@ -386,19 +423,18 @@ extern "C" int fa_decode_paged(const void *q, const void *k_cache, const void *v
     p.lse = lse;
     p.block_table = block_table;
     p.seq_lens = seq_lens;
-    p.BH = (int)BH;
     p.H = H;
+    p.Hkv = Hkv;
+    p.group = H / Hkv;
     p.Nq = Nq;
-    p.Nk = nk_max;
+    p.Nk = page_size * max_pages_per_seq;
     p.d = d;
     p.paged = 1;
     p.page_size = page_size;
     p.max_pages = max_pages_per_seq;
     p.num_pages = num_pages;
     p.scale_log2 = scale * kLog2e;
-    p.status = dc->status;
-    p.limit_ns = kWaitLimitNs;
-    return launch_decode(p, static_cast<cudaStream_t>(stream));
+    return decode_launch(p, B, num_splits, workspace, workspace_bytes, stream);
 }
 
 extern "C" const char *fa_status_string(int status) {

@@ -150,7 +150,7 @@ __global__ void __launch_bounds__(320, 1)
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                   const float *__restrict__ ws_lse2, const float *__restrict__ ws_delta,
                   float *__restrict__ dq, float *__restrict__ dk, float *__restrict__ dv, int N,
-                  int Npad, int BH, float scale, float scale_log2, int *status,
+                  int Npad, int BHkv, int H, int group, float scale, float scale_log2, int *status,
                   unsigned long long limit_ns) {
     using T = BwdTile<D>;
     constexpr int BQ = T::BQ;
@@ -184,12 +184,19 @@ __global__ void __launch_bounds__(320, 1)
     const int lane = threadIdx.x & 31;
 
     // Causal: key block 0 has the most query blocks, so low blockIdx = key block first.
-    const int bh = blockIdx.x % BH;
-    const int jb = blockIdx.x / BH;
+    // Grouped-query attention: this CTA owns key/value head kvh (= b * Hkv + hk)
+    // and accumulates dK, dV over the `group` query heads that read it, walking
+    // their query blocks one head after the other.
+    const int kvh = blockIdx.x % BHkv;
+    const int jb = blockIdx.x / BHkv;
     const int kv0 = jb * T::BN;
     const int n_qb = (N + BQ - 1) / BQ;
     const int i_start = CAUSAL ? kv0 / BQ : 0;
-    const int n_it = n_qb - i_start;
+    const int n_qit = n_qb - i_start;  // query blocks per query head
+    const int n_it = group * n_qit;
+    const int bhq0 = (kvh / (H / group)) * H + (kvh % (H / group)) * group;
+    auto bh_of = [&](int it) { return bhq0 + it / n_qit; };   // query head of block it
+    auto q0_of = [&](int it) { return (i_start + it % n_qit) * BQ; };
 
     if (threadIdx.x == 0) {
         mbar_init(bar_kv_full, 1);
@@ -228,23 +235,23 @@ __global__ void __launch_bounds__(320, 1)
         if (lane == 0) {
             mbar_arrive_expect_tx(bar_kv_full, 2 * T::KV_BYTES);
             for (int c = 0; c < T::NCH; ++c) {
-                tma_load_3d(sK + c * T::K_CHUNK, &tm_k, bar_kv_full, c * 64, kv0, bh);
-                tma_load_3d(sV + c * T::K_CHUNK, &tm_v, bar_kv_full, c * 64, kv0, bh);
+                tma_load_3d(sK + c * T::K_CHUNK, &tm_k, bar_kv_full, c * 64, kv0, kvh);
+                tma_load_3d(sV + c * T::K_CHUNK, &tm_v, bar_kv_full, c * 64, kv0, kvh);
             }
             int issued = 0;
             for (int it = 0; it < n_it; ++it) {
                 const int s = it & 1;
-                const int q0 = (i_start + it) * BQ;
+                const int q0 = q0_of(it);
                 if (it >= 2 && !mbar_wait(bar_q_empty + 8 * s, ((it >> 1) - 1) & 1, g,
                                           SITE_BWD_LOAD_EMPTY))
                     break;
                 const uint32_t fb = bar_q_full + 8 * s;
                 mbar_arrive_expect_tx(fb, 2 * T::Q_BYTES + 2 * T::VEC_BYTES);
                 for (int c = 0; c < T::NCH; ++c) {
-                    tma_load_3d(sQ + s * T::Q_BYTES + c * T::Q_CHUNK, &tm_q, fb, c * 64, q0, bh);
-                    tma_load_3d(sDO + s * T::Q_BYTES + c * T::Q_CHUNK, &tm_do, fb, c * 64, q0, bh);
+                    tma_load_3d(sQ + s * T::Q_BYTES + c * T::Q_CHUNK, &tm_q, fb, c * 64, q0, bh_of(it));
+                    tma_load_3d(sDO + s * T::Q_BYTES + c * T::Q_CHUNK, &tm_do, fb, c * 64, q0, bh_of(it));
                 }
-                const size_t voff = (size_t)bh * Npad + q0;
+                const size_t voff = (size_t)bh_of(it) * Npad + q0;
                 bulk_load(sL2 + s * T::VEC_BYTES, ws_lse2 + voff, T::VEC_BYTES, fb);
                 bulk_load(sDelta + s * T::VEC_BYTES, ws_delta + voff, T::VEC_BYTES, fb);
                 ++issued;
@@ -355,7 +362,7 @@ __global__ void __launch_bounds__(320, 1)
         bool ok = true;
         for (int it = 0; it < n_it; ++it) {
             const int s = it & 1;
-            const int q0 = (i_start + it) * BQ;
+            const int q0 = q0_of(it);
             ok = mbar_wait_warp(bar_s_full, it & 1, g, SITE_BWD_SOFTMAX_S_FULL);
             if (!ok) break;
             tc_fence_after();
@@ -413,8 +420,8 @@ __global__ void __launch_bounds__(320, 1)
         ok = ok && mbar_wait_warp(bar_done, 0, g, SITE_BWD_EPILOGUE);
         if (ok) {
             tc_fence_after();
-            float *dv_row = dv + ((size_t)bh * N + key) * D;
-            float *dk_row = dk + ((size_t)bh * N + key) * D;
+            float *dv_row = dv + ((size_t)kvh * N + key) * D;
+            float *dk_row = dk + ((size_t)kvh * N + key) * D;
 #pragma unroll 1
             for (int c = 0; c < D / 32; ++c) {
                 uint32_t a[32], b2[32];
@@ -442,7 +449,7 @@ __global__ void __launch_bounds__(320, 1)
         bool ok = true;
         for (int it = 0; it < n_it; ++it) {
             const int b = it & 1;
-            const int q0 = (i_start + it) * BQ;
+            const int q0 = q0_of(it);
             ok = mbar_wait_warp(bar_dq_full + 8 * b, (it >> 1) & 1, g, SITE_BWD_DQ_FULL);
             if (!ok) break;
             tc_fence_after();
@@ -490,7 +497,7 @@ __global__ void __launch_bounds__(320, 1)
                     ok0 = mbar_wait(bar_stg_full, it & 1, g, SITE_BWD_DQ_FULL);
                     if (ok0) {
                         const int rows = min(BQ, N - q0);
-                        bulk_reduce_add_f32(dq + ((size_t)bh * N + q0) * D, sStage,
+                        bulk_reduce_add_f32(dq + ((size_t)bh_of(it) * N + q0) * D, sStage,
                                             (uint32_t)(rows * D * 4));
                         bulk_commit_group();
                     }
@@ -567,7 +574,7 @@ __global__ void __launch_bounds__(448, 1)
                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                        const float *__restrict__ ws_lse2, const float *__restrict__ ws_delta,
                        float *__restrict__ dq, float *__restrict__ dk, float *__restrict__ dv, int N,
-                       int Npad, int BH, float scale, float scale_log2, int *status,
+                       int Npad, int BHkv, int H, int group, float scale, float scale_log2, int *status,
                        unsigned long long limit_ns) {
     using T = Bwd128;
     constexpr int BQ = T::BQ, QS = T::QS, D = T::D;
@@ -603,11 +610,18 @@ __global__ void __launch_bounds__(448, 1)
     const int lane = threadIdx.x & 31;
 
     // Causal: key block 0 has the most query blocks, so low blockIdx = key block first.
-    const int bh = blockIdx.x % BH;
-    const int kv0 = (blockIdx.x / BH) * T::BN;
+    // Grouped-query attention: this CTA owns key/value head kvh (= b * Hkv + hk)
+    // and accumulates dK, dV over the `group` query heads that read it, walking
+    // their query blocks one head after the other.
+    const int kvh = blockIdx.x % BHkv;
+    const int kv0 = (blockIdx.x / BHkv) * T::BN;
     const int n_qb = (N + BQ - 1) / BQ;
     const int i_start = CAUSAL ? kv0 / BQ : 0;
-    const int n_it = n_qb - i_start;
+    const int n_qit = n_qb - i_start;  // query blocks per query head
+    const int n_it = group * n_qit;
+    const int bhq0 = (kvh / (H / group)) * H + (kvh % (H / group)) * group;
+    auto bh_of = [&](int it) { return bhq0 + it / n_qit; };   // query head of block it
+    auto q0_of = [&](int it) { return (i_start + it % n_qit) * BQ; };
 
     if (threadIdx.x == 0) {
         mbar_init(bar_kv_full, 1);
@@ -648,23 +662,23 @@ __global__ void __launch_bounds__(448, 1)
         if (lane == 0) {
             mbar_arrive_expect_tx(bar_kv_full, 2 * T::KV_BYTES);
             for (int c = 0; c < T::NCH; ++c) {
-                tma_load_3d(sK + c * T::K_CHUNK, &tm_k, bar_kv_full, c * 64, kv0, bh);
-                tma_load_3d(sV + c * T::K_CHUNK, &tm_v, bar_kv_full, c * 64, kv0, bh);
+                tma_load_3d(sK + c * T::K_CHUNK, &tm_k, bar_kv_full, c * 64, kv0, kvh);
+                tma_load_3d(sV + c * T::K_CHUNK, &tm_v, bar_kv_full, c * 64, kv0, kvh);
             }
             int issued = 0;
             for (int it = 0; it < n_it; ++it) {
                 const int s = it % QS;
-                const int q0 = (i_start + it) * BQ;
+                const int q0 = q0_of(it);
                 if (it >= QS && !mbar_wait(bar_q_empty + 8 * s, ((it / QS) - 1) & 1, g,
                                            SITE_BWD_LOAD_EMPTY))
                     break;
                 const uint32_t fb = bar_q_full + 8 * s;
                 mbar_arrive_expect_tx(fb, 2 * T::Q_BYTES + 2 * T::VEC_BYTES);
                 for (int c = 0; c < T::NCH; ++c) {
-                    tma_load_3d(sQ + s * T::Q_BYTES + c * T::Q_CHUNK, &tm_q, fb, c * 64, q0, bh);
-                    tma_load_3d(sDO + s * T::Q_BYTES + c * T::Q_CHUNK, &tm_do, fb, c * 64, q0, bh);
+                    tma_load_3d(sQ + s * T::Q_BYTES + c * T::Q_CHUNK, &tm_q, fb, c * 64, q0, bh_of(it));
+                    tma_load_3d(sDO + s * T::Q_BYTES + c * T::Q_CHUNK, &tm_do, fb, c * 64, q0, bh_of(it));
                 }
-                const size_t voff = (size_t)bh * Npad + q0;
+                const size_t voff = (size_t)bh_of(it) * Npad + q0;
                 bulk_load(sL2 + s * T::VEC_BYTES, ws_lse2 + voff, T::VEC_BYTES, fb);
                 bulk_load(sDelta + s * T::VEC_BYTES, ws_delta + voff, T::VEC_BYTES, fb);
                 ++issued;
@@ -761,7 +775,7 @@ __global__ void __launch_bounds__(448, 1)
         bool ok = true;
         for (int it = 0; it < n_it; ++it) {
             const int s = it % QS;
-            const int q0 = (i_start + it) * BQ;
+            const int q0 = q0_of(it);
             ok = mbar_wait_warp(bar_s_full, it & 1, g, SITE_BWD_SOFTMAX_S_FULL);
             if (!ok) break;
             tc_fence_after();
@@ -851,7 +865,7 @@ __global__ void __launch_bounds__(448, 1)
                 }
                 fence_proxy_async_smem();
                 if (key < N) {
-                    float *dst = (pass == 0 ? dv : dk) + ((size_t)bh * N + key) * D + 64 * h;
+                    float *dst = (pass == 0 ? dv : dk) + ((size_t)kvh * N + key) * D + 64 * h;
                     bulk_store(dst, stg_s, 256);
                 }
                 bulk_commit_group();
@@ -865,7 +879,7 @@ __global__ void __launch_bounds__(448, 1)
         const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
         bool ok = true;
         for (int it = 0; it < n_it; ++it) {
-            const int q0 = (i_start + it) * BQ;
+            const int q0 = q0_of(it);
             ok = mbar_wait_warp(bar_dq_full, it & 1, g, SITE_BWD_DQ_FULL);
             if (!ok) break;
             tc_fence_after();
@@ -899,7 +913,7 @@ __global__ void __launch_bounds__(448, 1)
                     ok0 = mbar_wait(bar_stg_full, it & 1, g, SITE_BWD_DQ_FULL);
                     if (ok0) {
                         const int rows = min(BQ, N - q0);
-                        bulk_reduce_add_f32(dq + ((size_t)bh * N + q0) * D, sStage,
+                        bulk_reduce_add_f32(dq + ((size_t)bh_of(it) * N + q0) * D, sStage,
                                             (uint32_t)(rows * D * 4));
                         bulk_commit_group();
                     }
@@ -938,7 +952,7 @@ int launch_bwd_t(const BwdParams &p, cudaStream_t stream) {
             p.N, p.Npad, p.BH);
         if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
     }
-    const long long grid = (long long)((p.N + T::BN - 1) / T::BN) * p.BH;
+    const long long grid = (long long)((p.N + T::BN - 1) / T::BN) * (p.BH / p.group);
     if (grid > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
     if constexpr (D == 128) {
         auto kern = fa_bwd_kernel_d128<CAUSAL>;
@@ -947,7 +961,7 @@ int launch_bwd_t(const BwdParams &p, cudaStream_t stream) {
             return FA_ERR_CUDA;
         kern<<<(unsigned)grid, Bwd128::THREADS, Bwd128::SMEM_BYTES, stream>>>(
             p.tm_q, p.tm_k, p.tm_v, p.tm_do, p.ws_lse2, p.ws_delta, p.dq, p.dk, p.dv, p.N, p.Npad,
-            p.BH, p.scale, p.scale_log2, p.status, p.limit_ns);
+            p.BH / p.group, p.H, p.group, p.scale, p.scale_log2, p.status, p.limit_ns);
     } else {
         auto kern = fa_bwd_kernel<D, CAUSAL>;
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -955,7 +969,7 @@ int launch_bwd_t(const BwdParams &p, cudaStream_t stream) {
             return FA_ERR_CUDA;
         kern<<<(unsigned)grid, T::THREADS, T::SMEM_BYTES, stream>>>(
             p.tm_q, p.tm_k, p.tm_v, p.tm_do, p.ws_lse2, p.ws_delta, p.dq, p.dk, p.dv, p.N, p.Npad,
-            p.BH, p.scale, p.scale_log2, p.status, p.limit_ns);
+            p.BH / p.group, p.H, p.group, p.scale, p.scale_log2, p.status, p.limit_ns);
     }
     return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }

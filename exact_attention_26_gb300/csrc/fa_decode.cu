@@ -112,12 +112,21 @@ __global__ void __launch_bounds__(DecTile<D>::THREADS, 2)
     const float scale_log2 = p.scale_log2;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int bh = blockIdx.x, split = blockIdx.y, i0 = blockIdx.z * QB;
-    const int nq = min(QB, Nq - i0);
+    // One CTA per (key/value head, key range, block of query rows).  With grouped
+    // queries the rows of key/value head kvh are the Nq rows of each of the `group`
+    // query heads that read it (row r: head r / Nq of the group, position r % Nq),
+    // so the cache is read once for all of them.
+    const int kvh = blockIdx.x, split = blockIdx.y, i0 = blockIdx.z * QB;
+    const int R = p.group * Nq;
+    const int nq = min(QB, R - i0);
+    const int b = kvh / p.Hkv;
+    auto qrow = [&](int r) -> size_t {  // flat [B][H][Nq] index of row r of this kv head
+        return (size_t)(b * p.H + (kvh % p.Hkv) * p.group + r / Nq) * Nq + r % Nq;
+    };
     // Keys of this head: the whole cache, or the sequence's own length when paged
     // (checked on the device: 1 <= len <= page_size * max_pages).
     int len = p.Nk;
-    if constexpr (PAGED) len = p.seq_lens[bh / p.H];
+    if constexpr (PAGED) len = p.seq_lens[b];
     const bool bad_len = PAGED && (len < 1 || len > p.Nk);
     const int k0 = split * p.keys_per_split;
     const int k1 = bad_len ? k0 : min(len, k0 + p.keys_per_split);
@@ -143,8 +152,8 @@ __global__ void __launch_bounds__(DecTile<D>::THREADS, 2)
         // (all lookups in flight at once), the warp votes on their validity, and every
         // lane issues the copies of its own page segment.
         int issued = 0;
-        const int h = bh % p.H;
-        const int *bt = PAGED ? p.block_table + (size_t)(bh / p.H) * p.max_pages : nullptr;
+        const int h = kvh % p.Hkv;
+        const int *bt = PAGED ? p.block_table + (size_t)b * p.max_pages : nullptr;
         for (int t = 0; t < n_tiles; ++t) {
             const int slot = t % STAGES;
             if (t >= STAGES && !mbar_wait_warp(bar_empty + 8 * slot, ((t / STAGES) - 1) & 1, g,
@@ -173,14 +182,14 @@ __global__ void __launch_bounds__(DecTile<D>::THREADS, 2)
                 for (int i = lane; i < nseg; i += 32) {
                     const int pg = pg0 + i;
                     const int js = max(j0, pg * ps), je = min(j0 + rows, (pg + 1) * ps);
-                    const size_t src = (((size_t)bt[pg] * p.H + h) * ps + (js - pg * ps)) * D;
+                    const size_t src = (((size_t)bt[pg] * p.Hkv + h) * ps + (js - pg * ps)) * D;
                     const uint32_t off = (uint32_t)((js - j0) * D * 2), bytes = (uint32_t)((je - js) * D * 2);
                     bulk_load(dst + off, k + src, bytes, fb);
                     bulk_load(dst + T::TILE_BYTES + off, v + src, bytes, fb);
                 }
             } else {
                 if (lane == 0) {
-                    const size_t src = ((size_t)bh * p.Nk + j0) * D;
+                    const size_t src = ((size_t)kvh * p.Nk + j0) * D;
                     const uint32_t bytes = (uint32_t)(rows * D * 2);
                     mbar_arrive_expect_tx(fb, 2 * bytes);
                     bulk_load(dst, k + src, bytes, fb);
@@ -207,7 +216,7 @@ __global__ void __launch_bounds__(DecTile<D>::THREADS, 2)
 #pragma unroll
             for (int e = 0; e < E; ++e) {
                 acc[qi][e] = 0.f;
-                qv[qi][e] = qi < nq ? __bfloat162float(q[((size_t)bh * Nq + i0 + qi) * D + lane * E + e]) : 0.f;
+                qv[qi][e] = qi < nq ? __bfloat162float(q[qrow(i0 + qi) * D + lane * E + e]) : 0.f;
             }
         }
         const int mykey = (lane >> 2) & 7;  // key of a group of eight that this lane scores
@@ -328,7 +337,7 @@ __global__ void __launch_bounds__(DecTile<D>::THREADS, 2)
             const bool empty = (M == -INFINITY);
             const float inv = empty ? 0.f : 1.f / L;
             const float l_nat = empty ? -INFINITY : (M + lg2(L)) * kLn2;  // natural-log LSE
-            const size_t row = (size_t)bh * Nq + i0 + qi;
+            const size_t row = qrow(i0 + qi);
             if (S == 1) {
 #pragma unroll
                 for (int e = 0; e < E; e += 2) {
@@ -337,7 +346,7 @@ __global__ void __launch_bounds__(DecTile<D>::THREADS, 2)
                 }
                 if (lane == 0) lse[row] = l_nat;
             } else {
-                const size_t prow = ((size_t)bh * S + split) * Nq + i0 + qi;
+                const size_t prow = ((size_t)kvh * S + split) * R + i0 + qi;
                 float *po = part_o + prow * D + lane * E;
 #pragma unroll
                 for (int e = 0; e < E; ++e) po[e] = out[e] * inv;
@@ -349,29 +358,32 @@ __global__ void __launch_bounds__(DecTile<D>::THREADS, 2)
 
 // Merge of the S partial results of one query row: L = log sum_s exp(L_s),
 // O = sum_s exp(L_s - L) O_s.  One warp per row; lanes split the head dimension.
+// Rows are numbered like the split kernel's: key/value head, then its R rows.
 template <int D>
 __global__ void __launch_bounds__(128)
     fa_decode_combine_kernel(const float *__restrict__ part_o, const float *__restrict__ part_l,
                              __nv_bfloat16 *__restrict__ o, float *__restrict__ lse, long long rows,
-                             int Nq, int S) {
+                             int R, int S, int Nq, int H, int Hkv, int group) {
     constexpr int E = D / 32;
     const long long row = (long long)blockIdx.x * 4 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (row >= rows) return;
-    const long long bh = row / Nq;
-    const int i = (int)(row % Nq);
-    const float *pl = part_l + (size_t)bh * S * Nq + i;  // stride Nq over splits
+    const long long kvh = row / R;
+    const int r = (int)(row % R);
+    const long long b = kvh / Hkv;
+    const size_t orow = (size_t)(b * H + (kvh % Hkv) * group + r / Nq) * Nq + r % Nq;
+    const float *pl = part_l + (size_t)kvh * S * R + r;  // stride R over splits
     float M = -INFINITY;
-    for (int s = lane; s < S; s += 32) M = fmaxf(M, pl[(size_t)s * Nq]);
+    for (int s = lane; s < S; s += 32) M = fmaxf(M, pl[(size_t)s * R]);
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, off));
     float W = 0.f, out[E];
 #pragma unroll
     for (int e = 0; e < E; ++e) out[e] = 0.f;
     for (int s = 0; s < S; ++s) {
-        const float w = __expf(pl[(size_t)s * Nq] - M);
+        const float w = __expf(pl[(size_t)s * R] - M);
         W += w;
-        const float *po = part_o + (((size_t)bh * S + s) * Nq + i) * D + lane * E;
+        const float *po = part_o + (((size_t)kvh * S + s) * R + r) * D + lane * E;
 #pragma unroll
         for (int e = 0; e < E; ++e) out[e] = fmaf(w, po[e], out[e]);
     }
@@ -379,9 +391,9 @@ __global__ void __launch_bounds__(128)
 #pragma unroll
     for (int e = 0; e < E; e += 2) {
         const uint32_t pk = pack_bf16(out[e] * inv, out[e + 1] * inv);
-        *reinterpret_cast<uint32_t *>(o + (size_t)row * D + lane * E + e) = pk;
+        *reinterpret_cast<uint32_t *>(o + orow * D + lane * E + e) = pk;
     }
-    if (lane == 0) lse[row] = M + __logf(W);
+    if (lane == 0) lse[orow] = M + __logf(W);
 }
 
 template <int D, int QB, bool PAGED>
@@ -391,13 +403,15 @@ int launch_decode_t(const DecodeParams &p, cudaStream_t stream) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)T::SMEM_BYTES) !=
         cudaSuccess)
         return FA_ERR_CUDA;
-    const dim3 grid((unsigned)p.BH, (unsigned)p.S, (unsigned)((p.Nq + QB - 1) / QB));
+    const int R = p.group * p.Nq;
+    const dim3 grid((unsigned)(p.BH / p.group), (unsigned)p.S, (unsigned)((R + QB - 1) / QB));
     kern<<<grid, T::THREADS, T::SMEM_BYTES, stream>>>(p);
     if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
     if (p.S > 1) {
-        const long long rows = (long long)p.BH * p.Nq;
+        const long long rows = (long long)(p.BH / p.group) * R;
         fa_decode_combine_kernel<D><<<(unsigned)((rows + 3) / 4), 128, 0, stream>>>(
-            p.part_o, p.part_l, reinterpret_cast<__nv_bfloat16 *>(p.o), p.lse, rows, p.Nq, p.S);
+            p.part_o, p.part_l, reinterpret_cast<__nv_bfloat16 *>(p.o), p.lse, rows, R, p.S, p.Nq,
+            p.H, p.Hkv, p.group);
         if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
     }
     return FA_OK;
@@ -406,9 +420,10 @@ int launch_decode_t(const DecodeParams &p, cudaStream_t stream) {
 template <int D>
 int launch_decode_d(const DecodeParams &p, cudaStream_t stream) {
     constexpr int QB = dec_qblock<D>();
+    const bool one = p.group * p.Nq == 1;  // one query row per key/value head
     if (p.paged)
-        return p.Nq == 1 ? launch_decode_t<D, 1, true>(p, stream) : launch_decode_t<D, QB, true>(p, stream);
-    return p.Nq == 1 ? launch_decode_t<D, 1, false>(p, stream) : launch_decode_t<D, QB, false>(p, stream);
+        return one ? launch_decode_t<D, 1, true>(p, stream) : launch_decode_t<D, QB, true>(p, stream);
+    return one ? launch_decode_t<D, 1, false>(p, stream) : launch_decode_t<D, QB, false>(p, stream);
 }
 
 template <int D, int QB>

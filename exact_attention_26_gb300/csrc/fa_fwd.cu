@@ -88,8 +88,8 @@ template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(FwdTile<D>::THREADS, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, __nv_bfloat16 *__restrict__ out,
-                  float *__restrict__ lse, int N, int BH, int n_cblocks, float scale_log2,
-                  int *status, unsigned long long limit_ns) {
+                  float *__restrict__ lse, int N, int BH, int H, int group, int n_cblocks,
+                  float scale_log2, int *status, unsigned long long limit_ns) {
     using T = FwdTile<D>;
     constexpr int NT = T::NT;
     constexpr int KS = T::KS;
@@ -135,11 +135,13 @@ __global__ void __launch_bounds__(FwdTile<D>::THREADS, 1)
         return idx < n_items ? idx : -1;
     };
     struct Item {
-        int bh, cb, n_kv[NT], n_max;
+        int bh, kvh, cb, n_kv[NT], n_max;
     };
     auto decode = [&](int w) {
         Item it;
         it.bh = w % BH;
+        // grouped-query attention: query head h reads key/value head h / group
+        it.kvh = (it.bh / H) * (H / group) + (it.bh % H) / group;
         it.cb = CAUSAL ? (n_cblocks - 1 - w / BH) : (w / BH);
         it.n_max = 0;
 #pragma unroll
@@ -211,7 +213,7 @@ __global__ void __launch_bounds__(FwdTile<D>::THREADS, 1)
                     mbar_arrive_expect_tx(full + 8 * stage, T::KV_BYTES);
                     for (int c = 0; c < T::NCH; ++c)
                         tma_load_3d(ring + stage * T::KV_BYTES + c * T::KV_CHUNK, map,
-                                    full + 8 * stage, c * 64, j * T::BN, itm.bh);
+                                    full + 8 * stage, c * 64, j * T::BN, itm.kvh);
                 };
                 for (int t = 0; ok && t < NT; ++t) {
                     if (itm.n_kv[t] == 0) continue;
@@ -559,8 +561,8 @@ int launch_fwd_t(const FwdParams &p, cudaStream_t stream) {
     // Persistent: one CTA per SM (the shared-memory footprint allows no more).
     const long long grid = items < p.num_sms ? items : p.num_sms;
     kern<<<(unsigned)grid, T::THREADS, T::SMEM_BYTES, stream>>>(
-        p.tm_q, p.tm_k, p.tm_v, reinterpret_cast<__nv_bfloat16 *>(p.o), p.lse, p.N, p.BH,
-        n_cblocks, p.scale_log2, p.status, p.limit_ns);
+        p.tm_q, p.tm_k, p.tm_v, reinterpret_cast<__nv_bfloat16 *>(p.o), p.lse, p.N, p.BH, p.H,
+        p.group, n_cblocks, p.scale_log2, p.status, p.limit_ns);
     return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 

@@ -41,10 +41,11 @@ enum WaitSite : int {
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 
 struct FwdParams {
-    CUtensorMap tm_q, tm_k, tm_v;  // 3-D maps over [BH][N][d] bf16
+    CUtensorMap tm_q, tm_k, tm_v;  // 3-D maps over [BH][N][d] (q) and [B*Hkv][N][d] (k, v) bf16
     void *o;                       // bf16 [BH][N][d]
     float *lse;                    // fp32 [BH][N]
     int N, BH, d, causal;
+    int H, group;                  // query heads per batch; query heads per key/value head
     float scale_log2;              // scale * log2(e)
     int *status;                   // device status record (2 ints)
     unsigned long long limit_ns;
@@ -52,12 +53,13 @@ struct FwdParams {
 };
 
 struct BwdParams {
-    CUtensorMap tm_q, tm_k, tm_v, tm_do;  // 3-D maps over [BH][N][d] bf16
+    CUtensorMap tm_q, tm_k, tm_v, tm_do;  // 3-D maps over [BH][N][d] (q, do), [B*Hkv][N][d] (k, v)
     const void *o, *dout;                 // bf16 [BH][N][d]
     const float *lse;                     // fp32 [BH][N]
     float *dq, *dk, *dv;                  // fp32 [BH][N][d]
     float *ws_delta, *ws_lse2;            // workspace, [BH][Npad] each
     int N, Npad, BH, d, causal;
+    int H, group;                         // query heads per batch; query heads per k/v head
     float scale, scale_log2;
     int *status;
     unsigned long long limit_ns;
@@ -69,13 +71,14 @@ constexpr int kBwdPad = 128;
 
 struct DecodeParams {
     const void *q;            // bf16 [BH][Nq][d]
-    const void *k, *v;        // bf16 [BH][Nk][d], or paged [num_pages][H][page_size][d]
+    const void *k, *v;        // bf16 [B*Hkv][Nk][d], or paged [num_pages][Hkv][page_size][d]
     void *o;                  // bf16 [BH][Nq][d]
     float *lse;               // fp32 [BH][Nq]
-    float *part_o, *part_l;   // workspace when S > 1: [BH][S][Nq][d], [BH][S][Nq]
+    float *part_o, *part_l;   // workspace when S > 1: [B*Hkv][S][group*Nq][d], [..][S][group*Nq]
     const int *block_table;   // paged: [B][max_pages] physical page of each logical page
     const int *seq_lens;      // paged: [B] cached tokens of each sequence
     int BH, H, Nq, Nk, d;     // Nk: keys per head (paged: page_size * max_pages, an upper bound)
+    int Hkv, group;           // key/value heads; query heads per key/value head (H = Hkv*group)
     int S, keys_per_split;    // key ranges [s*keys_per_split, ...) per CTA
     int paged, page_size, max_pages, num_pages;
     float scale_log2;

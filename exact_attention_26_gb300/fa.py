@@ -26,7 +26,7 @@ FA_ERR_BAD_INDEX = 7
 EXPORTED = ("fa_fwd", "fa_bwd", "fa_bwd_workspace_bytes", "fa_status_string", "fa_device_status",
             "fa_selftest_wait_timeout", "fa_decode", "fa_decode_num_splits",
             "fa_decode_workspace_bytes", "fa_decode_paged", "fa_decode_paged_num_splits",
-            "fa_decode_paged_workspace_bytes")
+            "fa_decode_paged_workspace_bytes", "fa_fwd_gqa", "fa_bwd_gqa")
 
 _vp = ctypes.c_void_p
 _int = ctypes.c_int
@@ -63,19 +63,23 @@ def load() -> ctypes.CDLL:
         lib.fa_status_string.restype = ctypes.c_char_p
         lib.fa_device_status.argtypes = [_vp]
         lib.fa_device_status.restype = _int
-        lib.fa_decode.argtypes = [_vp, _vp, _vp, _vp, _vp, _int, _int, _int, _int, _int,
-                                  ctypes.c_float, _int, _vp, ctypes.c_size_t, _vp]
+        lib.fa_fwd_gqa.argtypes = [_vp] * 5 + [_int] * 6 + [ctypes.c_float, _vp]
+        lib.fa_fwd_gqa.restype = _int
+        lib.fa_bwd_gqa.argtypes = [_vp] * 9 + [_int] * 6 + [ctypes.c_float, _vp, ctypes.c_size_t, _vp]
+        lib.fa_bwd_gqa.restype = _int
+        lib.fa_decode.argtypes = [_vp] * 5 + [_int] * 6 + [ctypes.c_float, _int, _vp,
+                                                          ctypes.c_size_t, _vp]
         lib.fa_decode.restype = _int
-        lib.fa_decode_num_splits.argtypes = [_int] * 6
+        lib.fa_decode_num_splits.argtypes = [_int] * 7
         lib.fa_decode_num_splits.restype = _int
-        lib.fa_decode_workspace_bytes.argtypes = [_int] * 6
+        lib.fa_decode_workspace_bytes.argtypes = [_int] * 7
         lib.fa_decode_workspace_bytes.restype = ctypes.c_size_t
-        lib.fa_decode_paged.argtypes = [_vp] * 7 + [_int] * 7 + [ctypes.c_float, _int, _vp,
+        lib.fa_decode_paged.argtypes = [_vp] * 7 + [_int] * 8 + [ctypes.c_float, _int, _vp,
                                                                 ctypes.c_size_t, _vp]
         lib.fa_decode_paged.restype = _int
-        lib.fa_decode_paged_num_splits.argtypes = [_int] * 7
+        lib.fa_decode_paged_num_splits.argtypes = [_int] * 8
         lib.fa_decode_paged_num_splits.restype = _int
-        lib.fa_decode_paged_workspace_bytes.argtypes = [_int] * 7
+        lib.fa_decode_paged_workspace_bytes.argtypes = [_int] * 8
         lib.fa_decode_paged_workspace_bytes.restype = ctypes.c_size_t
         _LIB = lib
     return _LIB
@@ -117,34 +121,45 @@ def fa_selftest_wait_timeout(limit_ns: int, stream=None) -> int:
     return fn(limit_ns, stream)
 
 
-def fa_decode(q, k, v, o, lse, B, H, Nq, Nk, d, scale, num_splits, workspace, workspace_bytes,
-              stream) -> int:
-    return load().fa_decode(q, k, v, o, lse, B, H, Nq, Nk, d, scale, num_splits, workspace,
+def fa_fwd_gqa(q, k, v, o, lse, B, H, Hkv, N, d, causal, scale, stream) -> int:
+    return load().fa_fwd_gqa(q, k, v, o, lse, B, H, Hkv, N, d, int(bool(causal)), scale, stream)
+
+
+def fa_bwd_gqa(q, k, v, o, lse, dout, dq, dk, dv, B, H, Hkv, N, d, causal, scale, workspace,
+               workspace_bytes, stream) -> int:
+    return load().fa_bwd_gqa(q, k, v, o, lse, dout, dq, dk, dv, B, H, Hkv, N, d, int(bool(causal)),
+                             scale, workspace, workspace_bytes, stream)
+
+
+def fa_decode(q, k, v, o, lse, B, H, Hkv, Nq, Nk, d, scale, num_splits, workspace,
+              workspace_bytes, stream) -> int:
+    return load().fa_decode(q, k, v, o, lse, B, H, Hkv, Nq, Nk, d, scale, num_splits, workspace,
                             workspace_bytes, stream)
 
 
-def fa_decode_num_splits(B, H, Nq, Nk, d, num_splits=0) -> int:
-    return load().fa_decode_num_splits(B, H, Nq, Nk, d, num_splits)
+def fa_decode_num_splits(B, H, Hkv, Nq, Nk, d, num_splits=0) -> int:
+    return load().fa_decode_num_splits(B, H, Hkv, Nq, Nk, d, num_splits)
 
 
-def fa_decode_workspace_bytes(B, H, Nq, Nk, d, num_splits=0) -> int:
-    return load().fa_decode_workspace_bytes(B, H, Nq, Nk, d, num_splits)
+def fa_decode_workspace_bytes(B, H, Hkv, Nq, Nk, d, num_splits=0) -> int:
+    return load().fa_decode_workspace_bytes(B, H, Hkv, Nq, Nk, d, num_splits)
 
 
-def fa_decode_paged(q, k_cache, v_cache, block_table, seq_lens, o, lse, B, H, Nq, d, page_size,
-                    max_pages, num_pages, scale, num_splits, workspace, workspace_bytes,
-                    stream) -> int:
-    return load().fa_decode_paged(q, k_cache, v_cache, block_table, seq_lens, o, lse, B, H, Nq, d,
-                                  page_size, max_pages, num_pages, scale, num_splits, workspace,
-                                  workspace_bytes, stream)
+def fa_decode_paged(q, k_cache, v_cache, block_table, seq_lens, o, lse, B, H, Hkv, Nq, d,
+                    page_size, max_pages, num_pages, scale, num_splits, workspace,
+                    workspace_bytes, stream) -> int:
+    return load().fa_decode_paged(q, k_cache, v_cache, block_table, seq_lens, o, lse, B, H, Hkv,
+                                  Nq, d, page_size, max_pages, num_pages, scale, num_splits,
+                                  workspace, workspace_bytes, stream)
 
 
-def fa_decode_paged_num_splits(B, H, Nq, d, page_size, max_pages, num_splits=0) -> int:
-    return load().fa_decode_paged_num_splits(B, H, Nq, d, page_size, max_pages, num_splits)
+def fa_decode_paged_num_splits(B, H, Hkv, Nq, d, page_size, max_pages, num_splits=0) -> int:
+    return load().fa_decode_paged_num_splits(B, H, Hkv, Nq, d, page_size, max_pages, num_splits)
 
 
-def fa_decode_paged_workspace_bytes(B, H, Nq, d, page_size, max_pages, num_splits=0) -> int:
-    return load().fa_decode_paged_workspace_bytes(B, H, Nq, d, page_size, max_pages, num_splits)
+def fa_decode_paged_workspace_bytes(B, H, Hkv, Nq, d, page_size, max_pages, num_splits=0) -> int:
+    return load().fa_decode_paged_workspace_bytes(B, H, Hkv, Nq, d, page_size, max_pages,
+                                                  num_splits)
 
 
 def fa_status_string(status: int) -> str:
@@ -174,14 +189,24 @@ def _stream(t, stream):
     return stream.cuda_stream if isinstance(stream, torch.cuda.Stream) else int(stream)
 
 
+def _kv_heads(q, k, v):
+    """Key/value head count of k, v [B, Hkv, N, d] next to q [B, H, N, d] (Hkv divides H)."""
+    B, H, N, d = q.shape
+    _check("k", k, torch.bfloat16)
+    if k.dim() != 4 or k.shape[0] != B or k.shape[2] != N or k.shape[3] != d or H % k.shape[1]:
+        raise ValueError("k must be [B, Hkv, N, d] with Hkv dividing q's H")
+    _check("v", v, torch.bfloat16, k.shape)
+    return k.shape[1]
+
+
 def forward(q, k, v, causal=False, scale=None, out=None, lse=None, stream=None):
-    """O, L = attention(q, k, v); q/k/v bf16 CUDA [B,H,N,d].  Returns (o, lse)."""
+    """O, L = attention(q, k, v); q bf16 CUDA [B,H,N,d], k/v [B,Hkv,N,d] (Hkv = H, or
+    fewer heads shared by groups of query heads).  Returns (o, lse)."""
     _check("q", q, torch.bfloat16)
     if q.dim() != 4:
         raise ValueError("q must be [B, H, N, d]")
     B, H, N, d = q.shape
-    _check("k", k, torch.bfloat16, q.shape)
-    _check("v", v, torch.bfloat16, q.shape)
+    Hkv = _kv_heads(q, k, v)
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
     if out is None:
         out = torch.empty_like(q)
@@ -190,55 +215,59 @@ def forward(q, k, v, causal=False, scale=None, out=None, lse=None, stream=None):
         lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
     _check("lse", lse, torch.float32, (B, H, N))
     with torch.cuda.device(q.device):
-        rc = fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
-                    B, H, N, d, causal, scale, _stream(q, stream))
+        rc = fa_fwd_gqa(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                        B, H, Hkv, N, d, causal, scale, _stream(q, stream))
     if rc != FA_OK:
-        raise FaError(rc, "fa_fwd")
+        raise FaError(rc, "fa_fwd_gqa")
     return out, lse
 
 
 def backward(q, k, v, o, lse, do, causal=False, scale=None, dq=None, dk=None, dv=None,
              workspace=None, stream=None):
-    """dQ, dK, dV (fp32) of attention(q, k, v) given dO; o and lse from forward()."""
+    """dQ, dK, dV (fp32) of attention(q, k, v) given dO; o and lse from forward().
+    With fewer key/value heads (k, v [B,Hkv,N,d]) dK, dV are [B,Hkv,N,d] sums over
+    each head's query group."""
     _check("q", q, torch.bfloat16)
     if q.dim() != 4:
         raise ValueError("q must be [B, H, N, d]")
     B, H, N, d = q.shape
-    for name, t in (("k", k), ("v", v), ("o", o), ("do", do)):
+    Hkv = _kv_heads(q, k, v)
+    for name, t in (("o", o), ("do", do)):
         _check(name, t, torch.bfloat16, q.shape)
     _check("lse", lse, torch.float32, (B, H, N))
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
     grads = []
-    for name, t in (("dq", dq), ("dk", dk), ("dv", dv)):
+    for name, t, shape in (("dq", dq, q.shape), ("dk", dk, k.shape), ("dv", dv, k.shape)):
         if t is None:
-            t = torch.empty(q.shape, dtype=torch.float32, device=q.device)
-        _check(name, t, torch.float32, q.shape)
+            t = torch.empty(shape, dtype=torch.float32, device=q.device)
+        _check(name, t, torch.float32, shape)
         grads.append(t)
     need = fa_bwd_workspace_bytes(B, H, N, d)
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
     _check("workspace", workspace, torch.uint8)
     with torch.cuda.device(q.device):
-        rc = fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
-                    do.data_ptr(), grads[0].data_ptr(), grads[1].data_ptr(), grads[2].data_ptr(),
-                    B, H, N, d, causal, scale, workspace.data_ptr(), workspace.numel(),
-                    _stream(q, stream))
+        rc = fa_bwd_gqa(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                        do.data_ptr(), grads[0].data_ptr(), grads[1].data_ptr(),
+                        grads[2].data_ptr(), B, H, Hkv, N, d, causal, scale, workspace.data_ptr(),
+                        workspace.numel(), _stream(q, stream))
     if rc != FA_OK:
-        raise FaError(rc, "fa_bwd")
+        raise FaError(rc, "fa_bwd_gqa")
     return tuple(grads)
 
 
 def decode(q, k, v, scale=None, num_splits=0, out=None, lse=None, workspace=None, stream=None):
-    """Decode attention: q bf16 CUDA [B,H,Nq,d] against the cache k, v [B,H,Nk,d] (no
-    mask), the key range split over CTAs and merged by LSE.  Returns (o, lse)."""
+    """Decode attention: q bf16 CUDA [B,H,Nq,d] against the cache k, v [B,Hkv,Nk,d]
+    (Hkv divides H; no mask), the key range split over CTAs and merged by LSE.
+    Returns (o, lse)."""
     _check("q", q, torch.bfloat16)
     if q.dim() != 4:
         raise ValueError("q must be [B, H, Nq, d]")
     B, H, Nq, d = q.shape
     _check("k", k, torch.bfloat16)
-    if k.dim() != 4 or k.shape[0] != B or k.shape[1] != H or k.shape[3] != d:
-        raise ValueError("k must be [B, H, Nk, d] with q's B, H and d")
-    Nk = k.shape[2]
+    if k.dim() != 4 or k.shape[0] != B or k.shape[3] != d or H % k.shape[1]:
+        raise ValueError("k must be [B, Hkv, Nk, d] with q's B and d, Hkv dividing H")
+    Hkv, Nk = k.shape[1], k.shape[2]
     _check("v", v, torch.bfloat16, k.shape)
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
     if out is None:
@@ -248,7 +277,7 @@ def decode(q, k, v, scale=None, num_splits=0, out=None, lse=None, workspace=None
         lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
     _check("lse", lse, torch.float32, (B, H, Nq))
     with torch.cuda.device(q.device):
-        need = fa_decode_workspace_bytes(B, H, Nq, Nk, d, num_splits)
+        need = fa_decode_workspace_bytes(B, H, Hkv, Nq, Nk, d, num_splits)
         if workspace is None and need > 0:
             workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
         if workspace is not None:
@@ -256,7 +285,7 @@ def decode(q, k, v, scale=None, num_splits=0, out=None, lse=None, workspace=None
         ws_ptr = workspace.data_ptr() if workspace is not None else None
         ws_len = workspace.numel() if workspace is not None else 0
         rc = fa_decode(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
-                       B, H, Nq, Nk, d, scale, num_splits, ws_ptr, ws_len, _stream(q, stream))
+                       B, H, Hkv, Nq, Nk, d, scale, num_splits, ws_ptr, ws_len, _stream(q, stream))
     if rc != FA_OK:
         raise FaError(rc, "fa_decode")
     return out, lse
@@ -265,16 +294,16 @@ def decode(q, k, v, scale=None, num_splits=0, out=None, lse=None, workspace=None
 def decode_paged(q, k_cache, v_cache, block_table, seq_lens, scale=None, num_splits=0, out=None,
                  lse=None, workspace=None, stream=None):
     """Decode against a paged cache: q bf16 [B,H,Nq,d]; k_cache, v_cache bf16
-    [num_pages, H, page_size, d]; block_table int32 [B, max_pages]; seq_lens int32 [B]
-    (all CUDA).  Returns (o, lse)."""
+    [num_pages, Hkv, page_size, d] (Hkv divides H); block_table int32 [B, max_pages];
+    seq_lens int32 [B] (all CUDA).  Returns (o, lse)."""
     _check("q", q, torch.bfloat16)
     if q.dim() != 4:
         raise ValueError("q must be [B, H, Nq, d]")
     B, H, Nq, d = q.shape
     _check("k_cache", k_cache, torch.bfloat16)
-    if k_cache.dim() != 4 or k_cache.shape[1] != H or k_cache.shape[3] != d:
-        raise ValueError("k_cache must be [num_pages, H, page_size, d]")
-    num_pages, _, page_size, _ = k_cache.shape
+    if k_cache.dim() != 4 or H % k_cache.shape[1] or k_cache.shape[3] != d:
+        raise ValueError("k_cache must be [num_pages, Hkv, page_size, d], Hkv dividing H")
+    num_pages, Hkv, page_size, _ = k_cache.shape
     _check("v_cache", v_cache, torch.bfloat16, k_cache.shape)
     _check("block_table", block_table, torch.int32)
     if block_table.dim() != 2 or block_table.shape[0] != B:
@@ -289,7 +318,7 @@ def decode_paged(q, k_cache, v_cache, block_table, seq_lens, scale=None, num_spl
         lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
     _check("lse", lse, torch.float32, (B, H, Nq))
     with torch.cuda.device(q.device):
-        need = fa_decode_paged_workspace_bytes(B, H, Nq, d, page_size, max_pages, num_splits)
+        need = fa_decode_paged_workspace_bytes(B, H, Hkv, Nq, d, page_size, max_pages, num_splits)
         if workspace is None and need > 0:
             workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
         if workspace is not None:
@@ -298,8 +327,8 @@ def decode_paged(q, k_cache, v_cache, block_table, seq_lens, scale=None, num_spl
         ws_len = workspace.numel() if workspace is not None else 0
         rc = fa_decode_paged(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
                              block_table.data_ptr(), seq_lens.data_ptr(), out.data_ptr(),
-                             lse.data_ptr(), B, H, Nq, d, page_size, max_pages, num_pages, scale,
-                             num_splits, ws_ptr, ws_len, _stream(q, stream))
+                             lse.data_ptr(), B, H, Hkv, Nq, d, page_size, max_pages, num_pages,
+                             scale, num_splits, ws_ptr, ws_len, _stream(q, stream))
     if rc != FA_OK:
         raise FaError(rc, "fa_decode_paged")
     return out, lse

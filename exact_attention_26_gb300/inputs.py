@@ -25,6 +25,9 @@ Recipes (one per workload of the measurement plan):
   (``seed + 1``) picks one key per block of ``boost_block`` keys of every head and
   adds ``boost`` to that K row, so some key ranges dominate others.
 
+* ``gqa_qkv``: grouped-query shapes, q (and dO) [B, H, N, d] and k, v [B, Hkv, N, d],
+  i.i.d. N(0, 1) drawn in the order q, k, v, dO from one CPU generator seeded with
+  ``seed``, rounded to bf16.
 * ``paged_cache``: rearranges a contiguous cache k, v [B, H, Nk, d] (Nk a multiple
   of ``page_size``) into pages [num_pages, H, page_size, d]: logical page p of
   sequence b goes to physical page perm[b * Nk / page_size + p], where perm is
@@ -38,7 +41,8 @@ from __future__ import annotations
 
 import torch
 
-__all__ = ["normal_qkv", "boosted_qkv", "decode_qkv", "paged_cache", "sample_rows", "to_f64"]
+__all__ = ["normal_qkv", "boosted_qkv", "decode_qkv", "gqa_qkv", "paged_cache", "sample_rows",
+           "to_f64"]
 
 
 def _draw(gen: torch.Generator, shape, mult: float = 1.0) -> torch.Tensor:
@@ -108,6 +112,18 @@ def decode_qkv(B: int, H: int, Nq: int, Nk: int, d: int, seed: int = 0, mult: fl
         kf.scatter_add_(2, idx[..., None].expand(B, H, nblk, d),
                         torch.full((B, H, nblk, d), float(boost), device=device))
         k = kf.to(torch.bfloat16).contiguous()
+    return q, k, v
+
+
+def gqa_qkv(B: int, H: int, Hkv: int, N: int, d: int, seed: int = 0, with_do: bool = False):
+    """Return (q, k, v) or (q, k, v, do): q, do [B,H,N,d] and k, v [B,Hkv,N,d] bf16."""
+    gen = torch.Generator(device="cpu")
+    gen.manual_seed(seed)
+    q = _draw(gen, (B, H, N, d))
+    k = _draw(gen, (B, Hkv, N, d))
+    v = _draw(gen, (B, Hkv, N, d))
+    if with_do:
+        return q, k, v, _draw(gen, (B, H, N, d))
     return q, k, v
 
 

@@ -95,6 +95,28 @@ int fa_bwd(const void *q, const void *k, const void *v, const void *o, const flo
            int causal, float scale, void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * Grouped-query attention (GQA; multi-query attention when Hkv = 1): the H query
+ * heads of a batch share Hkv key/value heads, query head h reading key/value head
+ * h / (H / Hkv) ("FlashAttention: Move Less, Not Compute Less", section "What It
+ * Changes - and What It Does Not": GQA reduces the number of key/value heads, and
+ * the official implementation has GQA/MQA paths).  The definition is the one above with
+ * K and V of head h taken from that shared head; fa_fwd and fa_bwd are the case
+ * Hkv = H.
+ *   k, v        : bf16 [B][Hkv][N][d]; q, o, dout [B][H][N][d]; lse [B][H][N].
+ *   dk, dv      : fp32 [B][Hkv][N][d], each the sum over the H / Hkv query heads that
+ *                 read that key/value head (accumulated on chip, no atomics).
+ *   Hkv         : >= 1 and divides H (FA_ERR_INVALID_ARG otherwise).
+ * Workspace: fa_bwd_workspace_bytes(B, H, N, d) (per query row).  Other arguments,
+ * results and errors as in fa_fwd / fa_bwd.
+ */
+int fa_fwd_gqa(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H,
+               int Hkv, int N, int d, int causal, float scale, void *stream);
+int fa_bwd_gqa(const void *q, const void *k, const void *v, const void *o, const float *lse,
+               const void *dout, float *dq, float *dk, float *dv, int B, int H, int Hkv, int N,
+               int d, int causal, float scale, void *workspace, size_t workspace_bytes,
+               void *stream);
+
+/*
  * Backward pass that allocates nothing, for callers that cannot allocate device
  * memory or pass a workspace: a host that reserves all device memory up front in
  * its own pool and forbids side allocations, or a latency-critical loop where a
@@ -130,12 +152,15 @@ int fa_bwd_noalloc(const void *q, const void *k, const void *v, const void *o,
  * The key range of each head is cut into S contiguous ranges handled by separate
  * CTAs; each produces a partial (O_s, L_s) of its range, and a second kernel
  * merges them: L = ln sum_s exp(L_s), O = sum_s exp(L_s - L) O_s.  The result is
- * the same as with one range up to rounding.
+ * the same as with one range up to rounding.  With grouped queries (Hkv < H, see
+ * fa_fwd_gqa) the H / Hkv query heads of a key/value head are handled by the same
+ * CTAs, so the cache is read once for all of them.
  *   q      : bf16 [B][H][Nq][d] (the new tokens' queries).
- *   k, v   : bf16 [B][H][Nk][d] (the key/value cache, contiguous per head).
+ *   k, v   : bf16 [B][Hkv][Nk][d] (the key/value cache, contiguous per head).
  *   o      : bf16 [B][H][Nq][d] output, rounded to nearest even.
  *   lse    : fp32 [B][H][Nq] output.
- *   B, H   : >= 1.  Nq in [1, 65535], Nk >= 1, B*H*Nq and B*H*Nk < 2^31.
+ *   B, H   : >= 1; Hkv >= 1 divides H.  Nq in [1, 65535], (H/Hkv)*Nq <= 65535,
+ *            Nk >= 1, B*H*Nq and B*Hkv*Nk < 2^31.
  *   d      : 64, 128 or 256.
  *   scale  : finite and > 0.
  *   num_splits : 0 chooses S automatically (about eight CTAs per SM in total,
@@ -148,7 +173,7 @@ int fa_bwd_noalloc(const void *q, const void *k, const void *v, const void *o,
  * Returns FA_OK or an fa_status code; nothing is launched on an error.
  */
 int fa_decode(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H,
-              int Nq, int Nk, int d, float scale, int num_splits, void *workspace,
+              int Hkv, int Nq, int Nk, int d, float scale, int num_splits, void *workspace,
               size_t workspace_bytes, void *stream);
 
 /*
@@ -156,14 +181,14 @@ int fa_decode(const void *q, const void *k, const void *v, void *o, float *lse, 
  * current device (>= 1), or minus an fa_status code for invalid sizes or a CUDA
  * error.  Needs the device's SM count when num_splits is 0.
  */
-int fa_decode_num_splits(int B, int H, int Nq, int Nk, int d, int num_splits);
+int fa_decode_num_splits(int B, int H, int Hkv, int Nq, int Nk, int d, int num_splits);
 
 /*
  * Workspace bytes fa_decode needs: 0 when S = 1, else room for the S partial
- * outputs (fp32 [B][H][S][Nq][d]) and their L values (fp32 [B][H][S][Nq]).
+ * outputs (fp32, S * B*H*Nq rows of d) and their L values (fp32, S * B*H*Nq).
  * Returns 0 for invalid sizes as well.
  */
-size_t fa_decode_workspace_bytes(int B, int H, int Nq, int Nk, int d, int num_splits);
+size_t fa_decode_workspace_bytes(int B, int H, int Hkv, int Nq, int Nk, int d, int num_splits);
 
 /*
  * Decode against a paged key/value cache (course page "10 FlashAttention",
@@ -172,7 +197,7 @@ size_t fa_decode_workspace_bytes(int B, int H, int Nq, int Nk, int d, int num_sp
  * split and merge as fa_decode, except that sequence b has its own length
  * seq_lens[b] and its key j lives in physical page block_table[b][j / page_size]
  * at row j % page_size:
- *   k_cache, v_cache : bf16 [num_pages][H][page_size][d]; one page holds
+ *   k_cache, v_cache : bf16 [num_pages][Hkv][page_size][d]; one page holds
  *                      page_size consecutive tokens of every head, each head's
  *                      rows contiguous (one bulk copy per page and head).
  *   block_table      : int32 [B][max_pages_per_seq], device memory; entries in
@@ -192,15 +217,16 @@ size_t fa_decode_workspace_bytes(int B, int H, int Nq, int Nk, int d, int num_sp
  */
 int fa_decode_paged(const void *q, const void *k_cache, const void *v_cache,
                     const int *block_table, const int *seq_lens, void *o, float *lse, int B, int H,
-                    int Nq, int d, int page_size, int max_pages_per_seq, int num_pages, float scale,
-                    int num_splits, void *workspace, size_t workspace_bytes, void *stream);
+                    int Hkv, int Nq, int d, int page_size, int max_pages_per_seq, int num_pages,
+                    float scale, int num_splits, void *workspace, size_t workspace_bytes,
+                    void *stream);
 
 /* Key ranges (>= 1) fa_decode_paged would use, or minus an fa_status code. */
-int fa_decode_paged_num_splits(int B, int H, int Nq, int d, int page_size, int max_pages_per_seq,
-                               int num_splits);
+int fa_decode_paged_num_splits(int B, int H, int Hkv, int Nq, int d, int page_size,
+                               int max_pages_per_seq, int num_splits);
 
 /* Workspace bytes fa_decode_paged needs (0 when one range suffices or sizes are invalid). */
-size_t fa_decode_paged_workspace_bytes(int B, int H, int Nq, int d, int page_size,
+size_t fa_decode_paged_workspace_bytes(int B, int H, int Hkv, int Nq, int d, int page_size,
                                        int max_pages_per_seq, int num_splits);
 
 /*

@@ -107,17 +107,18 @@ def test_python_wrapper_rejects_cpu_tensors(fa):
 
 
 def _dec(fa, **kw):
-    a = dict(q=DUMMY, k=DUMMY, v=DUMMY, o=DUMMY, lse=DUMMY, B=1, H=2, Nq=1, Nk=1000, d=128,
+    a = dict(q=DUMMY, k=DUMMY, v=DUMMY, o=DUMMY, lse=DUMMY, B=1, H=2, Hkv=2, Nq=1, Nk=1000, d=128,
              scale=0.1, splits=0, ws=None, ws_bytes=0, stream=None)
     a.update(kw)
-    return fa.fa_decode(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"], a["Nq"], a["Nk"],
-                        a["d"], a["scale"], a["splits"], a["ws"], a["ws_bytes"], a["stream"])
+    return fa.fa_decode(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"], a["Hkv"], a["Nq"],
+                        a["Nk"], a["d"], a["scale"], a["splits"], a["ws"], a["ws_bytes"], a["stream"])
 
 
 @pytest.mark.parametrize("kw,code", [
     (dict(q=None), 1), (dict(k=None), 1), (dict(v=None), 1), (dict(o=None), 1), (dict(lse=None), 1),
     (dict(B=0), 1), (dict(H=0), 1), (dict(Nq=0), 1), (dict(Nq=65536), 1), (dict(Nk=0), 1),
-    (dict(B=65536, H=256, Nk=256), 1), (dict(d=96), 2), (dict(d=32), 2),
+    (dict(B=65536, H=256, Hkv=256, Nk=256), 1), (dict(d=96), 2), (dict(d=32), 2),
+    (dict(Hkv=0), 1), (dict(Hkv=3), 1), (dict(Hkv=4), 1), (dict(H=4096, Hkv=1, Nq=17), 1),
     (dict(scale=0.0), 1), (dict(scale=float("nan")), 1), (dict(splits=-1), 1),
     (dict(q=DUMMY + 8), 3), (dict(k=DUMMY + 2), 3), (dict(lse=DUMMY + 4), 3),
 ])
@@ -126,26 +127,28 @@ def test_decode_rejects_bad_arguments(fa, kw, code):
 
 
 def test_decode_split_queries_reject_bad_sizes(fa):
-    assert fa.fa_decode_num_splits(0, 1, 1, 100, 128, 0) == -1
-    assert fa.fa_decode_num_splits(1, 1, 1, 100, 96, 0) == -2
-    assert fa.fa_decode_num_splits(1, 1, 1, 100, 128, -3) == -1
-    assert fa.fa_decode_workspace_bytes(1, 1, 0, 100, 128, 0) == 0
-    assert fa.fa_decode_workspace_bytes(1, 1, 1, 100, 80, 2) == 0
+    assert fa.fa_decode_num_splits(0, 1, 1, 1, 100, 128, 0) == -1
+    assert fa.fa_decode_num_splits(1, 1, 1, 1, 100, 96, 0) == -2
+    assert fa.fa_decode_num_splits(1, 1, 1, 1, 100, 128, -3) == -1
+    assert fa.fa_decode_num_splits(1, 6, 4, 1, 100, 128, 0) == -1
+    assert fa.fa_decode_workspace_bytes(1, 1, 1, 0, 100, 128, 0) == 0
+    assert fa.fa_decode_workspace_bytes(1, 1, 1, 1, 100, 80, 2) == 0
 
 
 def _pdec(fa, **kw):
-    a = dict(q=DUMMY, kc=DUMMY, vc=DUMMY, bt=DUMMY, sl=DUMMY, o=DUMMY, lse=DUMMY, B=2, H=2, Nq=1,
-             d=128, ps=16, mp=8, np_=16, scale=0.1, splits=0, ws=None, ws_bytes=0, stream=None)
+    a = dict(q=DUMMY, kc=DUMMY, vc=DUMMY, bt=DUMMY, sl=DUMMY, o=DUMMY, lse=DUMMY, B=2, H=2, Hkv=1,
+             Nq=1, d=128, ps=16, mp=8, np_=16, scale=0.1, splits=0, ws=None, ws_bytes=0, stream=None)
     a.update(kw)
     return fa.fa_decode_paged(a["q"], a["kc"], a["vc"], a["bt"], a["sl"], a["o"], a["lse"], a["B"],
-                              a["H"], a["Nq"], a["d"], a["ps"], a["mp"], a["np_"], a["scale"],
-                              a["splits"], a["ws"], a["ws_bytes"], a["stream"])
+                              a["H"], a["Hkv"], a["Nq"], a["d"], a["ps"], a["mp"], a["np_"],
+                              a["scale"], a["splits"], a["ws"], a["ws_bytes"], a["stream"])
 
 
 @pytest.mark.parametrize("kw,code", [
     (dict(q=None), 1), (dict(kc=None), 1), (dict(bt=None), 1), (dict(sl=None), 1), (dict(lse=None), 1),
     (dict(B=0), 1), (dict(Nq=0), 1), (dict(ps=0), 1), (dict(mp=0), 1), (dict(np_=0), 1),
     (dict(ps=1 << 16, mp=1 << 16), 1), (dict(d=80), 2), (dict(scale=-1.0), 1), (dict(splits=-2), 1),
+    (dict(Hkv=3), 1), (dict(Hkv=0), 1),
     (dict(kc=DUMMY + 8), 3), (dict(bt=DUMMY + 2), 3), (dict(sl=DUMMY + 1), 3),
 ])
 def test_decode_paged_rejects_bad_arguments(fa, kw, code):
@@ -153,6 +156,13 @@ def test_decode_paged_rejects_bad_arguments(fa, kw, code):
 
 
 def test_decode_paged_split_queries_reject_bad_sizes(fa):
-    assert fa.fa_decode_paged_num_splits(1, 1, 1, 128, 0, 4, 0) == -1
-    assert fa.fa_decode_paged_num_splits(1, 1, 1, 96, 16, 4, 0) == -2
-    assert fa.fa_decode_paged_workspace_bytes(1, 1, 1, 128, 16, 0, 2) == 0
+    assert fa.fa_decode_paged_num_splits(1, 1, 1, 1, 128, 0, 4, 0) == -1
+    assert fa.fa_decode_paged_num_splits(1, 1, 1, 1, 96, 16, 4, 0) == -2
+    assert fa.fa_decode_paged_workspace_bytes(1, 1, 1, 1, 128, 16, 0, 2) == 0
+
+
+@pytest.mark.parametrize("Hkv,code", [(0, 1), (3, 1), (5, 1), (-1, 1)])
+def test_gqa_rejects_bad_head_counts(fa, Hkv, code):
+    assert fa.fa.fa_fwd_gqa(DUMMY, DUMMY, DUMMY, DUMMY, DUMMY, 1, 4, Hkv, 128, 64, 0, 0.1, None) == code
+    assert fa.fa.fa_bwd_gqa(DUMMY, DUMMY, DUMMY, DUMMY, DUMMY, DUMMY, DUMMY, DUMMY, DUMMY, 1, 4, Hkv, 128,
+                            128, 1, 0.1, DUMMY, 1 << 20, None) == code

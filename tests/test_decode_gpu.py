@@ -59,11 +59,11 @@ def test_decode_small(fa, orc, shape):
 def test_decode_split_count_is_clamped(fa):
     """Requests beyond the number of pipeline stages shrink to one range per stage;
     the automatic count never exceeds a quarter of the stages."""
-    assert fa.fa_decode_num_splits(1, 1, 1, 100, 128, 50) == 2
-    assert fa.fa_decode_num_splits(1, 1, 1, 10, 128, 3) == 1
-    assert fa.fa_decode_num_splits(1, 1, 1, 64 * 40, 128, 0) <= 10
-    assert fa.fa_decode_workspace_bytes(1, 1, 1, 1000, 128, 1) == 0
-    assert fa.fa_decode_workspace_bytes(1, 1, 1, 1000, 128, 4) > 0
+    assert fa.fa_decode_num_splits(1, 1, 1, 1, 100, 128, 50) == 2
+    assert fa.fa_decode_num_splits(1, 1, 1, 1, 10, 128, 3) == 1
+    assert fa.fa_decode_num_splits(1, 1, 1, 1, 64 * 40, 128, 0) <= 10
+    assert fa.fa_decode_workspace_bytes(1, 1, 1, 1, 1000, 128, 1) == 0
+    assert fa.fa_decode_workspace_bytes(1, 1, 1, 1, 1000, 128, 4) > 0
 
 
 @pytest.mark.parametrize("splits", [1, 3, 0])
@@ -98,13 +98,13 @@ def test_decode_rejects_small_workspace(fa):
     q, k, v = (t.to(DEV) for t in decode_qkv(1, 1, 1, 2000, 128, seed=1))
     o = torch.empty_like(q)
     lse = torch.empty((1, 1, 1), dtype=torch.float32, device=DEV)
-    need = fa.fa_decode_workspace_bytes(1, 1, 1, 2000, 128, 4)
+    need = fa.fa_decode_workspace_bytes(1, 1, 1, 1, 2000, 128, 4)
     ws = torch.empty(need - 16, dtype=torch.uint8, device=DEV)
     rc = fa.fa_decode(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), 1, 1, 1,
-                      2000, 128, 0.1, 4, ws.data_ptr(), ws.numel(), None)
+                      1, 2000, 128, 0.1, 4, ws.data_ptr(), ws.numel(), None)
     assert rc == fa.fa.FA_ERR_WORKSPACE
     rc = fa.fa_decode(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), 1, 1, 1,
-                      2000, 128, 0.1, 4, None, 0, None)
+                      1, 2000, 128, 0.1, 4, None, 0, None)
     assert rc == fa.fa.FA_ERR_WORKSPACE
 
 
@@ -117,7 +117,7 @@ def test_decode_long_context_workload(fa, orc, B):
     o, lse = fa.decode(q, k, v)
     torch.cuda.synchronize()
     assert fa.fa_device_status(None) == 0
-    assert fa.fa_decode_num_splits(B, H, 1, Nk, d, 0) > 1
+    assert fa.fa_decode_num_splits(B, H, H, 1, Nk, d, 0) > 1
     heads = [(b, h) for b in range(B) for h in range(H)][:: max(1, (B * H) // 8)][:8]
     for b, h in heads:
         ro, rl = orc.decode(to_f64(q[b:b + 1, h:h + 1].cpu()), to_f64(k[b:b + 1, h:h + 1].cpu()),
