@@ -195,8 +195,8 @@ __global__ void __launch_bounds__(320, 1)
     const int n_qit = n_qb - i_start;  // query blocks per query head
     const int n_it = group * n_qit;
     const int bhq0 = (kvh / (H / group)) * H + (kvh % (H / group)) * group;
-    auto bh_of = [&](int it) { return bhq0 + it / n_qit; };   // query head of block it
-    auto q0_of = [&](int it) { return (i_start + it % n_qit) * BQ; };
+    // Block it is query block qb = it % n_qit of query head bhq0 + it / n_qit; the
+    // loops below carry (qb, gq) as counters instead of dividing every block.
 
     if (threadIdx.x == 0) {
         mbar_init(bar_kv_full, 1);
@@ -239,19 +239,19 @@ __global__ void __launch_bounds__(320, 1)
                 tma_load_3d(sV + c * T::K_CHUNK, &tm_v, bar_kv_full, c * 64, kv0, kvh);
             }
             int issued = 0;
-            for (int it = 0; it < n_it; ++it) {
+            for (int it = 0, qb = 0, gq = 0; it < n_it; ++it, (++qb == n_qit) ? (qb = 0, ++gq) : 0) {
                 const int s = it & 1;
-                const int q0 = q0_of(it);
+                const int q0 = (i_start + qb) * BQ;
                 if (it >= 2 && !mbar_wait(bar_q_empty + 8 * s, ((it >> 1) - 1) & 1, g,
                                           SITE_BWD_LOAD_EMPTY))
                     break;
                 const uint32_t fb = bar_q_full + 8 * s;
                 mbar_arrive_expect_tx(fb, 2 * T::Q_BYTES + 2 * T::VEC_BYTES);
                 for (int c = 0; c < T::NCH; ++c) {
-                    tma_load_3d(sQ + s * T::Q_BYTES + c * T::Q_CHUNK, &tm_q, fb, c * 64, q0, bh_of(it));
-                    tma_load_3d(sDO + s * T::Q_BYTES + c * T::Q_CHUNK, &tm_do, fb, c * 64, q0, bh_of(it));
+                    tma_load_3d(sQ + s * T::Q_BYTES + c * T::Q_CHUNK, &tm_q, fb, c * 64, q0, (bhq0 + gq));
+                    tma_load_3d(sDO + s * T::Q_BYTES + c * T::Q_CHUNK, &tm_do, fb, c * 64, q0, (bhq0 + gq));
                 }
-                const size_t voff = (size_t)bh_of(it) * Npad + q0;
+                const size_t voff = (size_t)(bhq0 + gq) * Npad + q0;
                 bulk_load(sL2 + s * T::VEC_BYTES, ws_lse2 + voff, T::VEC_BYTES, fb);
                 bulk_load(sDelta + s * T::VEC_BYTES, ws_delta + voff, T::VEC_BYTES, fb);
                 ++issued;
@@ -360,9 +360,9 @@ __global__ void __launch_bounds__(320, 1)
         const int r = threadIdx.x;       // key row within the block (TMEM lane)
         const int key = kv0 + r;
         bool ok = true;
-        for (int it = 0; it < n_it; ++it) {
+        for (int it = 0, qb = 0, gq = 0; it < n_it; ++it, (++qb == n_qit) ? (qb = 0, ++gq) : 0) {
             const int s = it & 1;
-            const int q0 = q0_of(it);
+            const int q0 = (i_start + qb) * BQ;
             ok = mbar_wait_warp(bar_s_full, it & 1, g, SITE_BWD_SOFTMAX_S_FULL);
             if (!ok) break;
             tc_fence_after();
@@ -447,9 +447,9 @@ __global__ void __launch_bounds__(320, 1)
         const int t = threadIdx.x - 128;  // TMEM lane: d index (d = 128) or query row (d = 64)
         const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
         bool ok = true;
-        for (int it = 0; it < n_it; ++it) {
+        for (int it = 0, qb = 0, gq = 0; it < n_it; ++it, (++qb == n_qit) ? (qb = 0, ++gq) : 0) {
             const int b = it & 1;
-            const int q0 = q0_of(it);
+            const int q0 = (i_start + qb) * BQ;
             ok = mbar_wait_warp(bar_dq_full + 8 * b, (it >> 1) & 1, g, SITE_BWD_DQ_FULL);
             if (!ok) break;
             tc_fence_after();
@@ -497,7 +497,7 @@ __global__ void __launch_bounds__(320, 1)
                     ok0 = mbar_wait(bar_stg_full, it & 1, g, SITE_BWD_DQ_FULL);
                     if (ok0) {
                         const int rows = min(BQ, N - q0);
-                        bulk_reduce_add_f32(dq + ((size_t)bh_of(it) * N + q0) * D, sStage,
+                        bulk_reduce_add_f32(dq + ((size_t)(bhq0 + gq) * N + q0) * D, sStage,
                                             (uint32_t)(rows * D * 4));
                         bulk_commit_group();
                     }
@@ -620,8 +620,8 @@ __global__ void __launch_bounds__(448, 1)
     const int n_qit = n_qb - i_start;  // query blocks per query head
     const int n_it = group * n_qit;
     const int bhq0 = (kvh / (H / group)) * H + (kvh % (H / group)) * group;
-    auto bh_of = [&](int it) { return bhq0 + it / n_qit; };   // query head of block it
-    auto q0_of = [&](int it) { return (i_start + it % n_qit) * BQ; };
+    // Block it is query block qb = it % n_qit of query head bhq0 + it / n_qit; the
+    // loops below carry (qb, gq) as counters instead of dividing every block.
 
     if (threadIdx.x == 0) {
         mbar_init(bar_kv_full, 1);
@@ -666,19 +666,19 @@ __global__ void __launch_bounds__(448, 1)
                 tma_load_3d(sV + c * T::K_CHUNK, &tm_v, bar_kv_full, c * 64, kv0, kvh);
             }
             int issued = 0;
-            for (int it = 0; it < n_it; ++it) {
+            for (int it = 0, qb = 0, gq = 0; it < n_it; ++it, (++qb == n_qit) ? (qb = 0, ++gq) : 0) {
                 const int s = it % QS;
-                const int q0 = q0_of(it);
+                const int q0 = (i_start + qb) * BQ;
                 if (it >= QS && !mbar_wait(bar_q_empty + 8 * s, ((it / QS) - 1) & 1, g,
                                            SITE_BWD_LOAD_EMPTY))
                     break;
                 const uint32_t fb = bar_q_full + 8 * s;
                 mbar_arrive_expect_tx(fb, 2 * T::Q_BYTES + 2 * T::VEC_BYTES);
                 for (int c = 0; c < T::NCH; ++c) {
-                    tma_load_3d(sQ + s * T::Q_BYTES + c * T::Q_CHUNK, &tm_q, fb, c * 64, q0, bh_of(it));
-                    tma_load_3d(sDO + s * T::Q_BYTES + c * T::Q_CHUNK, &tm_do, fb, c * 64, q0, bh_of(it));
+                    tma_load_3d(sQ + s * T::Q_BYTES + c * T::Q_CHUNK, &tm_q, fb, c * 64, q0, (bhq0 + gq));
+                    tma_load_3d(sDO + s * T::Q_BYTES + c * T::Q_CHUNK, &tm_do, fb, c * 64, q0, (bhq0 + gq));
                 }
-                const size_t voff = (size_t)bh_of(it) * Npad + q0;
+                const size_t voff = (size_t)(bhq0 + gq) * Npad + q0;
                 bulk_load(sL2 + s * T::VEC_BYTES, ws_lse2 + voff, T::VEC_BYTES, fb);
                 bulk_load(sDelta + s * T::VEC_BYTES, ws_delta + voff, T::VEC_BYTES, fb);
                 ++issued;
@@ -773,9 +773,9 @@ __global__ void __launch_bounds__(448, 1)
         const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
         const int key = kv0 + r;
         bool ok = true;
-        for (int it = 0; it < n_it; ++it) {
+        for (int it = 0, qb = 0, gq = 0; it < n_it; ++it, (++qb == n_qit) ? (qb = 0, ++gq) : 0) {
             const int s = it % QS;
-            const int q0 = q0_of(it);
+            const int q0 = (i_start + qb) * BQ;
             ok = mbar_wait_warp(bar_s_full, it & 1, g, SITE_BWD_SOFTMAX_S_FULL);
             if (!ok) break;
             tc_fence_after();
@@ -878,8 +878,8 @@ __global__ void __launch_bounds__(448, 1)
         const int t = threadIdx.x - 256;  // TMEM lane = column d of dQ
         const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
         bool ok = true;
-        for (int it = 0; it < n_it; ++it) {
-            const int q0 = q0_of(it);
+        for (int it = 0, qb = 0, gq = 0; it < n_it; ++it, (++qb == n_qit) ? (qb = 0, ++gq) : 0) {
+            const int q0 = (i_start + qb) * BQ;
             ok = mbar_wait_warp(bar_dq_full, it & 1, g, SITE_BWD_DQ_FULL);
             if (!ok) break;
             tc_fence_after();
@@ -913,7 +913,7 @@ __global__ void __launch_bounds__(448, 1)
                     ok0 = mbar_wait(bar_stg_full, it & 1, g, SITE_BWD_DQ_FULL);
                     if (ok0) {
                         const int rows = min(BQ, N - q0);
-                        bulk_reduce_add_f32(dq + ((size_t)bh_of(it) * N + q0) * D, sStage,
+                        bulk_reduce_add_f32(dq + ((size_t)(bhq0 + gq) * N + q0) * D, sStage,
                                             (uint32_t)(rows * D * 4));
                         bulk_commit_group();
                     }
