@@ -453,9 +453,18 @@ __global__ void __launch_bounds__(FwdTile<D>::THREADS, 1)
                     for (int c = 0; c < T::BN; ++c)
                         if (kv0 + c >= lim) s[c] = -INFINITY;
                 }
-                float mx = s[0];
+                // Row max and row sum as two independent partial chains: one thread
+                // owns the row, and a single chain of BN dependent operations would be
+                // BN latencies long.
+                constexpr int NACC = 2;  // measured best; four spill at 168 registers
+                float mp[NACC];
 #pragma unroll
-                for (int c = 1; c < T::BN; ++c) mx = fmaxf(mx, s[c]);
+                for (int a = 0; a < NACC; ++a) mp[a] = s[a];
+#pragma unroll
+                for (int c = NACC; c < T::BN; ++c) mp[c % NACC] = fmaxf(mp[c % NACC], s[c]);
+#pragma unroll
+                for (int a = 1; a < NACC; ++a) mp[0] = fmaxf(mp[0], mp[a]);
+                const float mx = mp[0];
                 const float m_tile = mx * scale_log2;
                 float alpha = 1.f;
                 const bool move = m_tile > m_ref + kRescaleLog2;
@@ -464,13 +473,17 @@ __global__ void __launch_bounds__(FwdTile<D>::THREADS, 1)
                     m_ref = m_tile;
                 }
                 const float neg_m = -m_ref;
-                float sum = 0.f;
+                float sp[NACC];
+#pragma unroll
+                for (int a = 0; a < NACC; ++a) sp[a] = 0.f;
 #pragma unroll
                 for (int c = 0; c < T::BN; ++c) {
                     s[c] = ex2(fmaf(s[c], scale_log2, neg_m));
-                    sum += s[c];
+                    sp[c % NACC] += s[c];
                 }
-                l = l * alpha + sum;
+#pragma unroll
+                for (int a = 1; a < NACC; ++a) sp[0] += sp[a];
+                l = l * alpha + sp[0];
                 // P as bf16 pairs into the first BN/2 columns of the S slot.
 #pragma unroll
                 for (int c = 0; c < T::BN / 64; ++c) {
