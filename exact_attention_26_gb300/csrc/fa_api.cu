@@ -77,6 +77,23 @@ int make_bhnd_map(CUtensorMap *map, const void *ptr, int BH, int N, int d, int b
     return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
 }
 
+// 3-D map over a packed token-major bf16 [T][heads][d] tensor: x = column, y = head,
+// z = token.  A box of 64 columns x 1 head x `box_rows` tokens lands in shared
+// memory as [box_rows][64], like a box of make_bhnd_map; tokens past T read as zeros.
+int make_thd_map(CUtensorMap *map, const void *ptr, int T, int heads, int d, int box_rows) {
+    auto enc = encode_tiled();
+    if (!enc) return FA_ERR_CUDA;
+    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)heads, (cuuint64_t)T};
+    cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)heads * (cuuint64_t)d * 2};
+    cuuint32_t box[3] = {64, 1, (cuuint32_t)box_rows};
+    cuuint32_t elem_strides[3] = {1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims,
+                     strides, box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
+}
+
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 int check_sizes(int B, int H, int N, int d, bool fwd) {
@@ -170,6 +187,44 @@ extern "C" int fa_fwd_gqa(const void *q, const void *k, const void *v, void *o, 
 extern "C" int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B,
                       int H, int N, int d, int causal, float scale, void *stream) {
     return fa_fwd_gqa(q, k, v, o, lse, B, H, H, N, d, causal, scale, stream);
+}
+
+extern "C" int fa_fwd_varlen(const void *q, const void *k, const void *v, void *o, float *lse,
+                             const int *cu_seqlens, int B, int H, int Hkv, int total_tokens,
+                             int max_seqlen, int d, int causal, float scale, void *stream) {
+    if (!q || !k || !v || !o || !lse || !cu_seqlens) return FA_ERR_INVALID_ARG;
+    if (B < 1 || H < 1 || total_tokens < 1 || max_seqlen < 1) return FA_ERR_INVALID_ARG;
+    if ((long long)total_tokens * H >= (1LL << 31) || (long long)B * H >= (1LL << 31))
+        return FA_ERR_INVALID_ARG;
+    if (d != 64 && d != 128 && d != 256) return FA_ERR_UNSUPPORTED;
+    const int group = gqa_group(H, Hkv);
+    if (group == 0) return FA_ERR_INVALID_ARG;
+    int rc = check_scale(scale);
+    if (rc != FA_OK) return rc;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
+        (reinterpret_cast<uintptr_t>(cu_seqlens) & 3u))
+        return FA_ERR_MISALIGNED;
+    DeviceCache *dc = nullptr;
+    if ((rc = current_device(&dc)) != FA_OK) return rc;
+    FwdParams p{};
+    if ((rc = make_thd_map(&p.tm_q, q, total_tokens, H, d, 128)) != FA_OK) return rc;
+    if ((rc = make_thd_map(&p.tm_k, k, total_tokens, Hkv, d, fwd_block_n(d))) != FA_OK) return rc;
+    if ((rc = make_thd_map(&p.tm_v, v, total_tokens, Hkv, d, fwd_block_n(d))) != FA_OK) return rc;
+    p.o = o;
+    p.lse = lse;
+    p.N = max_seqlen;
+    p.BH = B * H;
+    p.H = H;
+    p.group = group;
+    p.cu_seqlens = cu_seqlens;
+    p.total_tokens = total_tokens;
+    p.d = d;
+    p.causal = causal ? 1 : 0;
+    p.scale_log2 = scale * kLog2e;
+    p.status = dc->status;
+    p.limit_ns = kWaitLimitNs;
+    p.num_sms = dc->num_sms;
+    return launch_fwd(p, static_cast<cudaStream_t>(stream));
 }
 
 extern "C" size_t fa_bwd_workspace_bytes(int B, int H, int N, int d) {

@@ -84,12 +84,17 @@ struct FwdTile {
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 };
 
-template <int D, bool CAUSAL>
+// VARLEN: packed sequences of different lengths, token-major: q, o [T][H][d],
+// k, v [T][Hkv][d], lse [H][T]; sequence b holds tokens [cu_seqlens[b],
+// cu_seqlens[b+1]).  The tensor maps are then (d, heads, T), so a box of 128 tokens
+// of one head lands in shared memory exactly like a box of the fixed layout.
+template <int D, bool CAUSAL, bool VARLEN>
 __global__ void __launch_bounds__(FwdTile<D>::THREADS, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, __nv_bfloat16 *__restrict__ out,
                   float *__restrict__ lse, int N, int BH, int H, int group, int n_cblocks,
-                  float scale_log2, int *status, unsigned long long limit_ns) {
+                  const int *__restrict__ cu_seqlens, int total_tokens, float scale_log2,
+                  int *status, unsigned long long limit_ns) {
     using T = FwdTile<D>;
     constexpr int NT = T::NT;
     constexpr int KS = T::KS;
@@ -129,13 +134,13 @@ __global__ void __launch_bounds__(FwdTile<D>::THREADS, 1)
     const int n_items = n_cblocks * BH;
     const int G = (int)gridDim.x;
     const int n_rounds = (n_items + G - 1) / G;
-    const int n_kv_all = (N + T::BN - 1) / T::BN;
     auto item_of = [&](int rnd) -> int {
         const int idx = rnd * G + ((rnd & 1) ? (G - 1 - (int)blockIdx.x) : (int)blockIdx.x);
         return idx < n_items ? idx : -1;
     };
     struct Item {
         int bh, kvh, cb, n_kv[NT], n_max;
+        int len, tok0;  // rows of this head's sequence; its first token (packed layout)
     };
     auto decode = [&](int w) {
         Item it;
@@ -143,11 +148,31 @@ __global__ void __launch_bounds__(FwdTile<D>::THREADS, 1)
         // grouped-query attention: query head h reads key/value head h / group
         it.kvh = (it.bh / H) * (H / group) + (it.bh % H) / group;
         it.cb = CAUSAL ? (n_cblocks - 1 - w / BH) : (w / BH);
+        it.len = N;
+        it.tok0 = 0;
+        if constexpr (VARLEN) {
+            // cu_seqlens lives on the device, so it is checked here: a sequence that is
+            // not inside [0, total_tokens) or is longer than the launch's maximum is
+            // skipped and reported
+            const int b = it.bh / H;
+            const int a = cu_seqlens[b], e = cu_seqlens[b + 1];
+            if (a < 0 || e < a || e > total_tokens || e - a > N) {  // N: the maximum length
+                if (threadIdx.x == 0 && it.cb == 0 && (it.bh % H) == 0) {
+                    atomicCAS(status + 1, 0, SITE_FWD_BAD_SEQ);
+                    atomicExch(status, FA_ERR_BAD_INDEX);
+                }
+                it.len = 0;
+            } else {
+                it.len = e - a;
+                it.tok0 = a;
+            }
+        }
+        const int n_kv_all = (it.len + T::BN - 1) / T::BN;
         it.n_max = 0;
 #pragma unroll
-        for (int t = 0; t < NT; ++t) {  // K/V tiles query tile t visits (0: past N)
+        for (int t = 0; t < NT; ++t) {  // K/V tiles query tile t visits (0: past the end)
             const int row0 = it.cb * T::ROWS + t * T::BM;
-            if (row0 >= N)
+            if (row0 >= it.len)
                 it.n_kv[t] = 0;
             else
                 it.n_kv[t] = CAUSAL ? min(n_kv_all, (row0 + T::BM + T::BN - 1) / T::BN) : n_kv_all;
@@ -211,9 +236,15 @@ __global__ void __launch_bounds__(FwdTile<D>::THREADS, 1)
                 auto load_kv = [&](const CUtensorMap *map, uint32_t ring, uint32_t full, int stage,
                                    int j) {
                     mbar_arrive_expect_tx(full + 8 * stage, T::KV_BYTES);
-                    for (int c = 0; c < T::NCH; ++c)
-                        tma_load_3d(ring + stage * T::KV_BYTES + c * T::KV_CHUNK, map,
-                                    full + 8 * stage, c * 64, j * T::BN, itm.kvh);
+                    for (int c = 0; c < T::NCH; ++c) {
+                        if constexpr (VARLEN)
+                            tma_load_3d(ring + stage * T::KV_BYTES + c * T::KV_CHUNK, map,
+                                        full + 8 * stage, c * 64, (itm.bh % H) / group,
+                                        itm.tok0 + j * T::BN);
+                        else
+                            tma_load_3d(ring + stage * T::KV_BYTES + c * T::KV_CHUNK, map,
+                                        full + 8 * stage, c * 64, j * T::BN, itm.kvh);
+                    }
                 };
                 for (int t = 0; ok && t < NT; ++t) {
                     if (itm.n_kv[t] == 0) continue;
@@ -221,9 +252,15 @@ __global__ void __launch_bounds__(FwdTile<D>::THREADS, 1)
                                                             g, SITE_FWD_LOAD_KV_EMPTY)))
                         break;
                     mbar_arrive_expect_tx(bar_q_full + 8 * t, T::Q_BYTES);
-                    for (int c = 0; c < T::NCH; ++c)
-                        tma_load_3d(sQ + t * T::Q_BYTES + c * T::Q_CHUNK, &tm_q, bar_q_full + 8 * t,
-                                    c * 64, itm.cb * T::ROWS + t * T::BM, itm.bh);
+                    for (int c = 0; c < T::NCH; ++c) {
+                        const int row = itm.cb * T::ROWS + t * T::BM;
+                        if constexpr (VARLEN)
+                            tma_load_3d(sQ + t * T::Q_BYTES + c * T::Q_CHUNK, &tm_q,
+                                        bar_q_full + 8 * t, c * 64, itm.bh % H, itm.tok0 + row);
+                        else
+                            tma_load_3d(sQ + t * T::Q_BYTES + c * T::Q_CHUNK, &tm_q,
+                                        bar_q_full + 8 * t, c * 64, row, itm.bh);
+                    }
                     ++q_issued[t];
                 }
                 for (int i = 0; ok && i <= itm.n_max; ++i) {
@@ -309,6 +346,7 @@ __global__ void __launch_bounds__(FwdTile<D>::THREADS, 1)
                 const int w = item_of(rnd);
                 if (w < 0) continue;
                 const Item itm = decode(w);
+                if (itm.n_max == 0) continue;  // rows past a short sequence's end: no work
                 if constexpr (T::SB == 1) {
                     // NT tiles, one S slot each: PV_0(j), S_0(j+1), PV_1(j), S_1(j+1), ...
                     ok = wait_k(kc);
@@ -446,9 +484,10 @@ __global__ void __launch_bounds__(FwdTile<D>::THREADS, 1)
                     for (int e = 0; e < 32; ++e) s[c * 32 + e] = __uint_as_float(sr[c][e]);
 
                 const int kv0 = j * T::BN;
-                const bool need_mask = (kv0 + T::BN > N) || (CAUSAL && kv0 + T::BN - 1 > row0);
+                const int len = itm.len;
+                const bool need_mask = (kv0 + T::BN > len) || (CAUSAL && kv0 + T::BN - 1 > row0);
                 if (need_mask) {
-                    const int lim = CAUSAL ? min(N, q_idx + 1) : N;  // keys [0, lim) are visible
+                    const int lim = CAUSAL ? min(len, q_idx + 1) : len;  // keys [0, lim) are visible
 #pragma unroll
                     for (int c = 0; c < T::BN; ++c)
                         if (kv0 + c >= lim) s[c] = -INFINITY;
@@ -523,7 +562,9 @@ __global__ void __launch_bounds__(FwdTile<D>::THREADS, 1)
             if (!ok) break;
             tc_fence_after();
             const float inv_l = 1.f / l;
-            __nv_bfloat16 *orow = out + ((size_t)itm.bh * (size_t)N + (size_t)q_idx) * D;
+            __nv_bfloat16 *orow =
+                VARLEN ? out + ((size_t)(itm.tok0 + q_idx) * H + (itm.bh % H)) * D
+                       : out + ((size_t)itm.bh * (size_t)N + (size_t)q_idx) * D;
 #pragma unroll 1
             for (int c = 0; c < D / 32; ++c) {
                 uint32_t o[32];
@@ -539,14 +580,18 @@ __global__ void __launch_bounds__(FwdTile<D>::THREADS, 1)
                 for (int e = 0; e < 16; ++e)
                     pk[e] = pack_bf16(__uint_as_float(o[2 * e]) * inv_l,
                                       __uint_as_float(o[2 * e + 1]) * inv_l);
-                if (q_idx < N) {
+                if (q_idx < itm.len) {
                     uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
 #pragma unroll
                     for (int e = 0; e < 4; ++e)
                         dst[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
                 }
             }
-            if (q_idx < N) lse[(size_t)itm.bh * (size_t)N + q_idx] = (m_ref + lg2(l)) * kLn2;
+            if (q_idx < itm.len) {
+                const size_t li = VARLEN ? (size_t)(itm.bh % H) * total_tokens + itm.tok0 + q_idx
+                                         : (size_t)itm.bh * (size_t)N + q_idx;
+                lse[li] = (m_ref + lg2(l)) * kLn2;
+            }
             ++oc;
         }
         tmem_wait_st();  // an aborted iteration may leave a store in flight
@@ -561,13 +606,14 @@ __global__ void __launch_bounds__(FwdTile<D>::THREADS, 1)
     }
 }
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool VARLEN>
 int launch_fwd_t(const FwdParams &p, cudaStream_t stream) {
     using T = FwdTile<D>;
-    auto kern = fa_fwd_kernel<D, CAUSAL>;
+    auto kern = fa_fwd_kernel<D, CAUSAL, VARLEN>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)T::SMEM_BYTES);
     if (e != cudaSuccess) return FA_ERR_CUDA;
+    // varlen: N is the longest sequence the caller allows
     const int n_cblocks = (p.N + T::ROWS - 1) / T::ROWS;
     const long long items = (long long)n_cblocks * p.BH;
     if (items > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
@@ -575,17 +621,24 @@ int launch_fwd_t(const FwdParams &p, cudaStream_t stream) {
     const long long grid = items < p.num_sms ? items : p.num_sms;
     kern<<<(unsigned)grid, T::THREADS, T::SMEM_BYTES, stream>>>(
         p.tm_q, p.tm_k, p.tm_v, reinterpret_cast<__nv_bfloat16 *>(p.o), p.lse, p.N, p.BH, p.H,
-        p.group, n_cblocks, p.scale_log2, p.status, p.limit_ns);
+        p.group, n_cblocks, p.cu_seqlens, p.total_tokens, p.scale_log2, p.status, p.limit_ns);
     return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
 }  // namespace
 
+template <int D>
+int launch_fwd_d(const FwdParams &p, cudaStream_t stream) {
+    if (p.cu_seqlens)
+        return p.causal ? launch_fwd_t<D, true, true>(p, stream) : launch_fwd_t<D, false, true>(p, stream);
+    return p.causal ? launch_fwd_t<D, true, false>(p, stream) : launch_fwd_t<D, false, false>(p, stream);
+}
+
 int launch_fwd(const FwdParams &p, cudaStream_t stream) {
     switch (p.d) {
-        case 64: return p.causal ? launch_fwd_t<64, true>(p, stream) : launch_fwd_t<64, false>(p, stream);
-        case 128: return p.causal ? launch_fwd_t<128, true>(p, stream) : launch_fwd_t<128, false>(p, stream);
-        case 256: return p.causal ? launch_fwd_t<256, true>(p, stream) : launch_fwd_t<256, false>(p, stream);
+        case 64: return launch_fwd_d<64>(p, stream);
+        case 128: return launch_fwd_d<128>(p, stream);
+        case 256: return launch_fwd_d<256>(p, stream);
         default: return FA_ERR_UNSUPPORTED;
     }
 }

@@ -20,6 +20,7 @@ enum WaitSite : int {
     SITE_FWD_SOFTMAX_S_FULL = 5,
     SITE_FWD_EPILOGUE_O_FULL = 6,
     SITE_FWD_DRAIN = 7,
+    SITE_FWD_BAD_SEQ = 8,
     SITE_BWD_LOAD_EMPTY = 11,
     SITE_BWD_MMA_KV = 12,
     SITE_BWD_MMA_Q_FULL = 13,
@@ -46,6 +47,8 @@ struct FwdParams {
     float *lse;                    // fp32 [BH][N]
     int N, BH, d, causal;
     int H, group;                  // query heads per batch; query heads per key/value head
+    const int *cu_seqlens;         // varlen: [B+1] sequence starts (token-major layout), else null
+    int total_tokens;              // varlen: T
     float scale_log2;              // scale * log2(e)
     int *status;                   // device status record (2 ints)
     unsigned long long limit_ns;

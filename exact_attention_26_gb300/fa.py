@@ -26,7 +26,7 @@ FA_ERR_BAD_INDEX = 7
 EXPORTED = ("fa_fwd", "fa_bwd", "fa_bwd_workspace_bytes", "fa_status_string", "fa_device_status",
             "fa_selftest_wait_timeout", "fa_decode", "fa_decode_num_splits",
             "fa_decode_workspace_bytes", "fa_decode_paged", "fa_decode_paged_num_splits",
-            "fa_decode_paged_workspace_bytes", "fa_fwd_gqa", "fa_bwd_gqa")
+            "fa_decode_paged_workspace_bytes", "fa_fwd_gqa", "fa_bwd_gqa", "fa_fwd_varlen")
 
 _vp = ctypes.c_void_p
 _int = ctypes.c_int
@@ -67,6 +67,8 @@ def load() -> ctypes.CDLL:
         lib.fa_fwd_gqa.restype = _int
         lib.fa_bwd_gqa.argtypes = [_vp] * 9 + [_int] * 6 + [ctypes.c_float, _vp, ctypes.c_size_t, _vp]
         lib.fa_bwd_gqa.restype = _int
+        lib.fa_fwd_varlen.argtypes = [_vp] * 6 + [_int] * 7 + [ctypes.c_float, _vp]
+        lib.fa_fwd_varlen.restype = _int
         lib.fa_decode.argtypes = [_vp] * 5 + [_int] * 6 + [ctypes.c_float, _int, _vp,
                                                           ctypes.c_size_t, _vp]
         lib.fa_decode.restype = _int
@@ -129,6 +131,12 @@ def fa_bwd_gqa(q, k, v, o, lse, dout, dq, dk, dv, B, H, Hkv, N, d, causal, scale
                workspace_bytes, stream) -> int:
     return load().fa_bwd_gqa(q, k, v, o, lse, dout, dq, dk, dv, B, H, Hkv, N, d, int(bool(causal)),
                              scale, workspace, workspace_bytes, stream)
+
+
+def fa_fwd_varlen(q, k, v, o, lse, cu_seqlens, B, H, Hkv, total_tokens, max_seqlen, d, causal,
+                  scale, stream) -> int:
+    return load().fa_fwd_varlen(q, k, v, o, lse, cu_seqlens, B, H, Hkv, total_tokens, max_seqlen,
+                                d, int(bool(causal)), scale, stream)
 
 
 def fa_decode(q, k, v, o, lse, B, H, Hkv, Nq, Nk, d, scale, num_splits, workspace,
@@ -331,4 +339,38 @@ def decode_paged(q, k_cache, v_cache, block_table, seq_lens, scale=None, num_spl
                              scale, num_splits, ws_ptr, ws_len, _stream(q, stream))
     if rc != FA_OK:
         raise FaError(rc, "fa_decode_paged")
+    return out, lse
+
+
+def forward_varlen(q, k, v, cu_seqlens, max_seqlen, causal=False, scale=None, out=None, lse=None,
+                   stream=None):
+    """Packed variable-length forward: q bf16 CUDA [T,H,d], k/v [T,Hkv,d], cu_seqlens
+    int32 CUDA [B+1] (sequence b = tokens cu[b]..cu[b+1]-1, each <= max_seqlen).
+    Returns (o [T,H,d], lse [H,T])."""
+    _check("q", q, torch.bfloat16)
+    if q.dim() != 3:
+        raise ValueError("q must be [T, H, d]")
+    T, H, d = q.shape
+    _check("k", k, torch.bfloat16)
+    if k.dim() != 3 or k.shape[0] != T or k.shape[2] != d or H % k.shape[1]:
+        raise ValueError("k must be [T, Hkv, d] with Hkv dividing H")
+    Hkv = k.shape[1]
+    _check("v", v, torch.bfloat16, k.shape)
+    _check("cu_seqlens", cu_seqlens, torch.int32)
+    if cu_seqlens.dim() != 1 or cu_seqlens.numel() < 2:
+        raise ValueError("cu_seqlens must be [B + 1]")
+    B = cu_seqlens.numel() - 1
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    if out is None:
+        out = torch.empty_like(q)
+    _check("out", out, torch.bfloat16, q.shape)
+    if lse is None:
+        lse = torch.empty((H, T), dtype=torch.float32, device=q.device)
+    _check("lse", lse, torch.float32, (H, T))
+    with torch.cuda.device(q.device):
+        rc = fa_fwd_varlen(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                           cu_seqlens.data_ptr(), B, H, Hkv, T, int(max_seqlen), d, causal, scale,
+                           _stream(q, stream))
+    if rc != FA_OK:
+        raise FaError(rc, "fa_fwd_varlen")
     return out, lse

@@ -28,6 +28,10 @@ Recipes (one per workload of the measurement plan):
 * ``gqa_qkv``: grouped-query shapes, q (and dO) [B, H, N, d] and k, v [B, Hkv, N, d],
   i.i.d. N(0, 1) drawn in the order q, k, v, dO from one CPU generator seeded with
   ``seed``, rounded to bf16.
+* ``varlen_qkv``: packed sequences of the given lengths, token-major q [T, H, d] and
+  k, v [T, Hkv, d] (T = sum of the lengths), i.i.d. N(0, 1) drawn in the order q,
+  k, v from one CPU generator seeded with ``seed``, rounded to bf16; plus
+  cu_seqlens, the int32 prefix sums [0, l0, l0 + l1, ...].
 * ``paged_cache``: rearranges a contiguous cache k, v [B, H, Nk, d] (Nk a multiple
   of ``page_size``) into pages [num_pages, H, page_size, d]: logical page p of
   sequence b goes to physical page perm[b * Nk / page_size + p], where perm is
@@ -41,8 +45,8 @@ from __future__ import annotations
 
 import torch
 
-__all__ = ["normal_qkv", "boosted_qkv", "decode_qkv", "gqa_qkv", "paged_cache", "sample_rows",
-           "to_f64"]
+__all__ = ["normal_qkv", "boosted_qkv", "decode_qkv", "gqa_qkv", "varlen_qkv", "paged_cache",
+           "sample_rows", "to_f64"]
 
 
 def _draw(gen: torch.Generator, shape, mult: float = 1.0) -> torch.Tensor:
@@ -125,6 +129,19 @@ def gqa_qkv(B: int, H: int, Hkv: int, N: int, d: int, seed: int = 0, with_do: bo
     if with_do:
         return q, k, v, _draw(gen, (B, H, N, d))
     return q, k, v
+
+
+def varlen_qkv(lens, H: int, Hkv: int, d: int, seed: int = 0):
+    """Return (q [T,H,d], k [T,Hkv,d], v [T,Hkv,d], cu_seqlens int32 [len(lens)+1])."""
+    gen = torch.Generator(device="cpu")
+    gen.manual_seed(seed)
+    T = int(sum(lens))
+    q = _draw(gen, (T, H, d))
+    k = _draw(gen, (T, Hkv, d))
+    v = _draw(gen, (T, Hkv, d))
+    cu = torch.zeros(len(lens) + 1, dtype=torch.int32)
+    cu[1:] = torch.cumsum(torch.tensor(lens, dtype=torch.int64), 0).to(torch.int32)
+    return q, k, v, cu
 
 
 def paged_cache(k: torch.Tensor, v: torch.Tensor, page_size: int, seed: int = 3):

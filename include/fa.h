@@ -143,6 +143,27 @@ int fa_bwd_noalloc(const void *q, const void *k, const void *v, const void *o,
                    int H, int N, int d, int causal, float scale, void *stream);
 
 /*
+ * Forward pass over packed sequences of different lengths (variable-length
+ * batches: course page "10 FlashAttention", section "8-9. Production and
+ * mistakes", counts padding sequences instead of packing them among the mistakes).  Sequence
+ * b holds tokens [cu_seqlens[b], cu_seqlens[b+1]) of the packed tensors and
+ * attends only within itself; the causal mask is taken per sequence (its token i
+ * sees its tokens 0..i).  Layout is token-major:
+ *   q, o        : bf16 [total_tokens][H][d];  k, v : bf16 [total_tokens][Hkv][d].
+ *   lse         : fp32 [H][total_tokens].
+ *   cu_seqlens  : int32 [B+1], device memory, 0 <= cu[b] <= cu[b+1] <= total_tokens,
+ *                 each length at most max_seqlen.  Checked on the device: a sequence
+ *                 that breaks these is skipped (its rows are not written) and
+ *                 FA_ERR_BAD_INDEX is recorded for fa_device_status.
+ *   max_seqlen  : >= 1, an upper bound on the lengths (sizes the launch).
+ *   Hkv         : divides H (grouped-query attention as in fa_fwd_gqa).
+ * Other arguments as in fa_fwd.
+ */
+int fa_fwd_varlen(const void *q, const void *k, const void *v, void *o, float *lse,
+                  const int *cu_seqlens, int B, int H, int Hkv, int total_tokens, int max_seqlen,
+                  int d, int causal, float scale, void *stream);
+
+/*
  * Decode attention with a split key range (course page "10 FlashAttention",
  * section "The decode variant: FlashDecoding"): Nq query rows per (b, h), usually
  * one, attend to all Nk cached keys of their head, with no mask:

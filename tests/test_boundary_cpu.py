@@ -166,3 +166,15 @@ def test_gqa_rejects_bad_head_counts(fa, Hkv, code):
     assert fa.fa.fa_fwd_gqa(DUMMY, DUMMY, DUMMY, DUMMY, DUMMY, 1, 4, Hkv, 128, 64, 0, 0.1, None) == code
     assert fa.fa.fa_bwd_gqa(DUMMY, DUMMY, DUMMY, DUMMY, DUMMY, DUMMY, DUMMY, DUMMY, DUMMY, 1, 4, Hkv, 128,
                             128, 1, 0.1, DUMMY, 1 << 20, None) == code
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(cu=None), 1), (dict(q=None), 1), (dict(B=0), 1), (dict(T=0), 1), (dict(maxlen=0), 1),
+    (dict(Hkv=3), 1), (dict(d=96), 2), (dict(scale=0.0), 1), (dict(cu=DUMMY + 2), 3), (dict(q=DUMMY + 8), 3),
+])
+def test_varlen_rejects_bad_arguments(fa, kw, code):
+    a = dict(q=DUMMY, k=DUMMY, v=DUMMY, o=DUMMY, lse=DUMMY, cu=DUMMY, B=2, H=4, Hkv=2, T=100,
+             maxlen=64, d=128, causal=1, scale=0.1)
+    a.update(kw)
+    assert fa.fa_fwd_varlen(a["q"], a["k"], a["v"], a["o"], a["lse"], a["cu"], a["B"], a["H"], a["Hkv"],
+                            a["T"], a["maxlen"], a["d"], a["causal"], a["scale"], None) == code
