@@ -509,7 +509,9 @@ __global__ void __launch_bounds__(320, 1)
                 }
             }
         }
-        if (t == 0) bulk_wait_group<0>();
+        // Only the shared-memory reads of the last bulk add must finish before the
+        // CTA retires; its global writes complete before the kernel does.
+        if (t == 0) bulk_wait_group_read<0>();
     }
 
     __syncwarp();
@@ -925,7 +927,9 @@ __global__ void __launch_bounds__(448, 1)
                 }
             }
         }
-        if (t == 0) bulk_wait_group<0>();
+        // Only the shared-memory reads of the last bulk add must finish before the
+        // CTA retires; its global writes complete before the kernel does.
+        if (t == 0) bulk_wait_group_read<0>();
     }
 
     __syncwarp();
