@@ -3,7 +3,7 @@
 ``forward``/``backward``/``decode`` take torch CUDA tensors; ``fa_*`` are the raw C-ABI
 calls with the names of include/fa.h.  The library is loaded on first use.
 """
-from .fa import (FaError, backward, decode, decode_paged, fa_bwd,  # noqa: F401
+from .fa import (FaError, backward, backward_varlen, decode, decode_paged, fa_bwd,  # noqa: F401
                  fa_bwd_workspace_bytes, fa_decode, fa_decode_num_splits, fa_decode_paged,
                  fa_decode_paged_num_splits, fa_decode_paged_workspace_bytes,
                  fa_decode_workspace_bytes, fa_device_status, fa_fwd, fa_fwd_varlen,

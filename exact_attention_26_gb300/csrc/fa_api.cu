@@ -284,6 +284,63 @@ extern "C" int fa_bwd_gqa(const void *q, const void *k, const void *v, const voi
     return launch_bwd(p, static_cast<cudaStream_t>(stream));
 }
 
+extern "C" int fa_bwd_varlen(const void *q, const void *k, const void *v, const void *o,
+                             const float *lse, const void *dout, float *dq, float *dk, float *dv,
+                             const int *cu_seqlens, int B, int H, int Hkv, int total_tokens,
+                             int max_seqlen, int d, int causal, float scale, void *workspace,
+                             size_t workspace_bytes, void *stream) {
+    if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv || !cu_seqlens)
+        return FA_ERR_INVALID_ARG;
+    if (B < 1 || H < 1 || total_tokens < 1 || max_seqlen < 1) return FA_ERR_INVALID_ARG;
+    if ((long long)total_tokens * H >= (1LL << 31) ||
+        (long long)B * H * (long long)round_up((size_t)max_seqlen, kBwdPad) >= (1LL << 31))
+        return FA_ERR_INVALID_ARG;
+    if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+    const int group = gqa_group(H, Hkv);
+    if (group == 0) return FA_ERR_INVALID_ARG;
+    int rc = check_scale(scale);
+    if (rc != FA_OK) return rc;
+    const size_t need = fa_bwd_workspace_bytes(B, H, max_seqlen, d);
+    if (!workspace || workspace_bytes < need) return FA_ERR_WORKSPACE;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
+        !aligned16(dout) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv) ||
+        !aligned16(workspace) || (reinterpret_cast<uintptr_t>(cu_seqlens) & 3u))
+        return FA_ERR_MISALIGNED;
+    DeviceCache *dc = nullptr;
+    if ((rc = current_device(&dc)) != FA_OK) return rc;
+    BwdParams p{};
+    const int BH = B * H;
+    const int npad = (int)round_up((size_t)max_seqlen, kBwdPad);
+    const int q_rows = (d == 128) ? 64 : 128;
+    if ((rc = make_thd_map(&p.tm_q, q, total_tokens, H, d, q_rows)) != FA_OK) return rc;
+    if ((rc = make_thd_map(&p.tm_do, dout, total_tokens, H, d, q_rows)) != FA_OK) return rc;
+    if ((rc = make_thd_map(&p.tm_k, k, total_tokens, Hkv, d, 128)) != FA_OK) return rc;
+    if ((rc = make_thd_map(&p.tm_v, v, total_tokens, Hkv, d, 128)) != FA_OK) return rc;
+    p.o = o;
+    p.dout = dout;
+    p.lse = lse;
+    p.dq = dq;
+    p.dk = dk;
+    p.dv = dv;
+    p.ws_delta = static_cast<float *>(workspace);
+    p.ws_lse2 = p.ws_delta + (size_t)BH * (size_t)npad;
+    p.N = max_seqlen;
+    p.Npad = npad;
+    p.BH = BH;
+    p.H = H;
+    p.group = group;
+    p.cu_seqlens = cu_seqlens;
+    p.total_tokens = total_tokens;
+    p.d = d;
+    p.causal = causal ? 1 : 0;
+    p.scale = scale;
+    p.scale_log2 = scale * kLog2e;
+    p.status = dc->status;
+    p.limit_ns = kWaitLimitNs;
+    p.num_sms = dc->num_sms;
+    return launch_bwd(p, static_cast<cudaStream_t>(stream));
+}
+
 extern "C" int fa_bwd(const void *q, const void *k, const void *v, const void *o,
                       const float *lse, const void *dout, float *dq, float *dk, float *dv, int B,
                       int H, int N, int d, int causal, float scale, void *workspace,

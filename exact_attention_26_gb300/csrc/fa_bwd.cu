@@ -91,11 +91,16 @@ struct BwdTile {
 
 // ---------------------------------------------------------------- preprocess
 
-template <int D>
+// VARLEN: o, dout, dq token-major [T][H][D], lse [H][T], sequence b = tokens
+// cu_seqlens[b] .. cu_seqlens[b+1]-1 (N is then the maximum length); the workspace
+// rows stay [B*H][Npad].  Rows of a sequence that breaks the bounds are treated
+// as padding (the main kernel reports it).
+template <int D, bool VARLEN>
 __global__ void __launch_bounds__(256)
     fa_bwd_pre_kernel(const __nv_bfloat16 *__restrict__ o, const __nv_bfloat16 *__restrict__ dout,
                       const float *__restrict__ lse, float *__restrict__ delta,
-                      float *__restrict__ lse2, float *__restrict__ dq, int N, int Npad, int BH) {
+                      float *__restrict__ lse2, float *__restrict__ dq, int N, int Npad, int BH,
+                      int H, const int *__restrict__ cu_seqlens, int total_tokens) {
     constexpr int PER = D / 32;  // elements per lane
     const int lane = threadIdx.x & 31;
     const long long warp0 = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -105,8 +110,20 @@ __global__ void __launch_bounds__(256)
     for (long long r = warp0; r < rows; r += nwarps) {
         const int bh = (int)(r / Npad);
         const int i = (int)(r % Npad);
-        if (i < N) {
-            const size_t row = ((size_t)bh * N + i) * D + (size_t)lane * PER;
+        int len = N;
+        size_t row_i, lse_i;  // element offset of row i, index of its L
+        if constexpr (VARLEN) {
+            const int b = bh / H, h = bh % H;
+            const int a = cu_seqlens[b], e = cu_seqlens[b + 1];
+            len = (a >= 0 && e >= a && e <= total_tokens && e - a <= N) ? e - a : 0;
+            row_i = ((size_t)(a + i) * H + h) * D;
+            lse_i = (size_t)h * total_tokens + a + i;
+        } else {
+            row_i = ((size_t)bh * N + i) * D;
+            lse_i = (size_t)bh * N + i;
+        }
+        if (i < len) {
+            const size_t row = row_i + (size_t)lane * PER;
             float acc = 0.f;
             if constexpr (PER == 4) {
                 const uint2 a = *reinterpret_cast<const uint2 *>(o + row);
@@ -133,7 +150,7 @@ __global__ void __launch_bounds__(256)
             for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
             if (lane == 0) {
                 delta[r] = acc;
-                lse2[r] = lse[(size_t)bh * N + i] * kLog2e;
+                lse2[r] = lse[lse_i] * kLog2e;
             }
         } else if (lane == 0) {
             delta[r] = 0.f;
@@ -144,13 +161,14 @@ __global__ void __launch_bounds__(256)
 
 // ---------------------------------------------------------------- main kernel
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool VARLEN>
 __global__ void __launch_bounds__(320, 1)
     fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                   const float *__restrict__ ws_lse2, const float *__restrict__ ws_delta,
                   float *__restrict__ dq, float *__restrict__ dk, float *__restrict__ dv, int N,
-                  int Npad, int BHkv, int H, int group, float scale, float scale_log2, int *status,
+                  int Npad, int BHkv, int H, int group, const int *__restrict__ cu_seqlens,
+                  int total_tokens, float scale, float scale_log2, int *status,
                   unsigned long long limit_ns) {
     using T = BwdTile<D>;
     constexpr int BQ = T::BQ;
@@ -190,7 +208,27 @@ __global__ void __launch_bounds__(320, 1)
     const int kvh = blockIdx.x % BHkv;
     const int jb = blockIdx.x / BHkv;
     const int kv0 = jb * T::BN;
-    const int n_qb = (N + BQ - 1) / BQ;
+    // Keys and queries of this head: N, or with packed sequences (VARLEN: token-major
+    // q, k, v, o, dO, dq, dk, dv, and N is the maximum length) the sequence's own
+    // length, checked on the device.  A key block past the sequence's end has no work.
+    const int hk = kvh % (H / group);
+    int len = N, tok0 = 0;
+    if constexpr (VARLEN) {
+        const int b = kvh / (H / group);
+        const int a = cu_seqlens[b], e = cu_seqlens[b + 1];
+        if (a < 0 || e < a || e > total_tokens || e - a > N) {
+            if (threadIdx.x == 0 && kv0 == 0 && hk == 0) {
+                atomicCAS(status + 1, 0, SITE_BWD_BAD_SEQ);
+                atomicExch(status, FA_ERR_BAD_INDEX);
+            }
+            len = 0;
+        } else {
+            len = e - a;
+            tok0 = a;
+        }
+    }
+    if (kv0 >= len) return;  // uniform across the CTA, before any barrier or TMEM use
+    const int n_qb = (len + BQ - 1) / BQ;
     const int i_start = CAUSAL ? kv0 / BQ : 0;
     const int n_qit = n_qb - i_start;  // query blocks per query head
     const int n_it = group * n_qit;
@@ -235,8 +273,10 @@ __global__ void __launch_bounds__(320, 1)
         if (lane == 0) {
             mbar_arrive_expect_tx(bar_kv_full, 2 * T::KV_BYTES);
             for (int c = 0; c < T::NCH; ++c) {
-                tma_load_3d(sK + c * T::K_CHUNK, &tm_k, bar_kv_full, c * 64, kv0, kvh);
-                tma_load_3d(sV + c * T::K_CHUNK, &tm_v, bar_kv_full, c * 64, kv0, kvh);
+                tma_load_3d(sK + c * T::K_CHUNK, &tm_k, bar_kv_full, c * 64, VARLEN ? hk : kv0,
+                            VARLEN ? tok0 + kv0 : kvh);
+                tma_load_3d(sV + c * T::K_CHUNK, &tm_v, bar_kv_full, c * 64, VARLEN ? hk : kv0,
+                            VARLEN ? tok0 + kv0 : kvh);
             }
             int issued = 0;
             for (int it = 0, qb = 0, gq = 0; it < n_it; ++it, (++qb == n_qit) ? (qb = 0, ++gq) : 0) {
@@ -248,8 +288,10 @@ __global__ void __launch_bounds__(320, 1)
                 const uint32_t fb = bar_q_full + 8 * s;
                 mbar_arrive_expect_tx(fb, 2 * T::Q_BYTES + 2 * T::VEC_BYTES);
                 for (int c = 0; c < T::NCH; ++c) {
-                    tma_load_3d(sQ + s * T::Q_BYTES + c * T::Q_CHUNK, &tm_q, fb, c * 64, q0, (bhq0 + gq));
-                    tma_load_3d(sDO + s * T::Q_BYTES + c * T::Q_CHUNK, &tm_do, fb, c * 64, q0, (bhq0 + gq));
+                    tma_load_3d(sQ + s * T::Q_BYTES + c * T::Q_CHUNK, &tm_q, fb, c * 64, VARLEN ? (bhq0 + gq) % H : q0,
+                                VARLEN ? tok0 + q0 : bhq0 + gq);
+                    tma_load_3d(sDO + s * T::Q_BYTES + c * T::Q_CHUNK, &tm_do, fb, c * 64, VARLEN ? (bhq0 + gq) % H : q0,
+                                VARLEN ? tok0 + q0 : bhq0 + gq);
                 }
                 const size_t voff = (size_t)(bhq0 + gq) * Npad + q0;
                 bulk_load(sL2 + s * T::VEC_BYTES, ws_lse2 + voff, T::VEC_BYTES, fb);
@@ -366,7 +408,7 @@ __global__ void __launch_bounds__(320, 1)
             ok = mbar_wait_warp(bar_s_full, it & 1, g, SITE_BWD_SOFTMAX_S_FULL);
             if (!ok) break;
             tc_fence_after();
-            const bool need_mask = (kv0 + T::BN > N) || (CAUSAL && q0 < kv0 + T::BN - 1);
+            const bool need_mask = (kv0 + T::BN > len) || (CAUSAL && q0 < kv0 + T::BN - 1);
             const float *l2v = l2_f + s * BQ;
             const float *dlv = delta_f + s * BQ;
             uint8_t *ds_row = gbase + T::OFF_DS + (it & 1) * T::DS_BYTES + r * 128;
@@ -390,7 +432,7 @@ __global__ void __launch_bounds__(320, 1)
                         p[u] = ex2(fmaf(__uint_as_float(sv[e + u]), scale_log2, -lq[u]));
                         if (need_mask) {
                             const int q = q0 + c * 32 + e + u;
-                            if (key >= N || (CAUSAL && q < key)) p[u] = 0.f;
+                            if (key >= len || (CAUSAL && q < key)) p[u] = 0.f;
                         }
                         ds[u] = p[u] * (__uint_as_float(dpv[e + u]) - dq_[u]);
                     }
@@ -420,8 +462,9 @@ __global__ void __launch_bounds__(320, 1)
         ok = ok && mbar_wait_warp(bar_done, 0, g, SITE_BWD_EPILOGUE);
         if (ok) {
             tc_fence_after();
-            float *dv_row = dv + ((size_t)kvh * N + key) * D;
-            float *dk_row = dk + ((size_t)kvh * N + key) * D;
+            const size_t krow = VARLEN ? (size_t)(tok0 + key) * (H / group) + hk : (size_t)kvh * N + key;
+            float *dv_row = dv + krow * D;
+            float *dk_row = dk + krow * D;
 #pragma unroll 1
             for (int c = 0; c < D / 32; ++c) {
                 uint32_t a[32], b2[32];
@@ -429,7 +472,7 @@ __global__ void __launch_bounds__(320, 1)
                 tmem_ld32(tmem + lane_base + T::TM_DK + c * 32, b2);
                 tmem_wait_ld(a);
                 tmem_wait_ld(b2);
-                if (key < N) {
+                if (key < len) {
 #pragma unroll
                     for (int e = 0; e < 32; e += 4) {
                         *reinterpret_cast<float4 *>(dv_row + c * 32 + e) =
@@ -463,9 +506,10 @@ __global__ void __launch_bounds__(320, 1)
             mbar_arrive(bar_dq_empty + 8 * b);
             // The staging tile is free once the previous bulk add has read it.  All
             // syncs here are bounded mbarrier waits, so an abort cannot strand a warp.
-            if (t == 0) {
-                bulk_wait_group_read<0>();
-                mbar_arrive(bar_stg_free);
+            if (warp == 4) {
+                bulk_wait_group_read<0>();  // every lane's adds of the previous block
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar_stg_free);
             }
             ok = mbar_wait_warp(bar_stg_free, it & 1, g, SITE_BWD_DQ_FULL);
             if (!ok) break;
@@ -493,13 +537,26 @@ __global__ void __launch_bounds__(320, 1)
             mbar_arrive(bar_stg_full);
             if (warp == 4) {
                 bool ok0 = true;
-                if (lane == 0) {
-                    ok0 = mbar_wait(bar_stg_full, it & 1, g, SITE_BWD_DQ_FULL);
+                const int rows = min(BQ, len - q0);
+                if constexpr (VARLEN) {
+                    // token-major dQ: the block's rows of this head are H * D floats
+                    // apart, so each lane adds its own rows
+                    ok0 = mbar_wait_warp(bar_stg_full, it & 1, g, SITE_BWD_DQ_FULL);
                     if (ok0) {
-                        const int rows = min(BQ, N - q0);
-                        bulk_reduce_add_f32(dq + ((size_t)(bhq0 + gq) * N + q0) * D, sStage,
-                                            (uint32_t)(rows * D * 4));
+                        const int hq = (bhq0 + gq) % H;
+                        for (int i = lane; i < rows; i += 32)
+                            bulk_reduce_add_f32(dq + ((size_t)(tok0 + q0 + i) * H + hq) * D,
+                                                sStage + (uint32_t)(i * D * 4), (uint32_t)(D * 4));
                         bulk_commit_group();
+                    }
+                } else {
+                    if (lane == 0) {
+                        ok0 = mbar_wait(bar_stg_full, it & 1, g, SITE_BWD_DQ_FULL);
+                        if (ok0) {
+                            bulk_reduce_add_f32(dq + ((size_t)(bhq0 + gq) * N + q0) * D, sStage,
+                                                (uint32_t)(rows * D * 4));
+                            bulk_commit_group();
+                        }
                     }
                 }
                 ok0 = __shfl_sync(0xffffffffu, ok0 ? 1 : 0, 0) != 0;
@@ -511,7 +568,7 @@ __global__ void __launch_bounds__(320, 1)
         }
         // Only the shared-memory reads of the last bulk add must finish before the
         // CTA retires; its global writes complete before the kernel does.
-        if (t == 0) bulk_wait_group_read<0>();
+        if (warp == 4) bulk_wait_group_read<0>();
     }
 
     __syncwarp();
@@ -570,13 +627,14 @@ struct Bwd128 {
     static_assert(Q_CHUNK % 1024 == 0 && DS_BYTES % 1024 == 0, "swizzle atoms must stay aligned");
 };
 
-template <bool CAUSAL>
+template <bool CAUSAL, bool VARLEN>
 __global__ void __launch_bounds__(448, 1)
     fa_bwd_kernel_d128(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                        const float *__restrict__ ws_lse2, const float *__restrict__ ws_delta,
                        float *__restrict__ dq, float *__restrict__ dk, float *__restrict__ dv, int N,
-                       int Npad, int BHkv, int H, int group, float scale, float scale_log2, int *status,
+                       int Npad, int BHkv, int H, int group, const int *__restrict__ cu_seqlens,
+                  int total_tokens, float scale, float scale_log2, int *status,
                        unsigned long long limit_ns) {
     using T = Bwd128;
     constexpr int BQ = T::BQ, QS = T::QS, D = T::D;
@@ -617,7 +675,27 @@ __global__ void __launch_bounds__(448, 1)
     // their query blocks one head after the other.
     const int kvh = blockIdx.x % BHkv;
     const int kv0 = (blockIdx.x / BHkv) * T::BN;
-    const int n_qb = (N + BQ - 1) / BQ;
+    // Keys and queries of this head: N, or with packed sequences (VARLEN: token-major
+    // q, k, v, o, dO, dq, dk, dv, and N is the maximum length) the sequence's own
+    // length, checked on the device.  A key block past the sequence's end has no work.
+    const int hk = kvh % (H / group);
+    int len = N, tok0 = 0;
+    if constexpr (VARLEN) {
+        const int b = kvh / (H / group);
+        const int a = cu_seqlens[b], e = cu_seqlens[b + 1];
+        if (a < 0 || e < a || e > total_tokens || e - a > N) {
+            if (threadIdx.x == 0 && kv0 == 0 && hk == 0) {
+                atomicCAS(status + 1, 0, SITE_BWD_BAD_SEQ);
+                atomicExch(status, FA_ERR_BAD_INDEX);
+            }
+            len = 0;
+        } else {
+            len = e - a;
+            tok0 = a;
+        }
+    }
+    if (kv0 >= len) return;  // uniform across the CTA, before any barrier or TMEM use
+    const int n_qb = (len + BQ - 1) / BQ;
     const int i_start = CAUSAL ? kv0 / BQ : 0;
     const int n_qit = n_qb - i_start;  // query blocks per query head
     const int n_it = group * n_qit;
@@ -664,8 +742,10 @@ __global__ void __launch_bounds__(448, 1)
         if (lane == 0) {
             mbar_arrive_expect_tx(bar_kv_full, 2 * T::KV_BYTES);
             for (int c = 0; c < T::NCH; ++c) {
-                tma_load_3d(sK + c * T::K_CHUNK, &tm_k, bar_kv_full, c * 64, kv0, kvh);
-                tma_load_3d(sV + c * T::K_CHUNK, &tm_v, bar_kv_full, c * 64, kv0, kvh);
+                tma_load_3d(sK + c * T::K_CHUNK, &tm_k, bar_kv_full, c * 64, VARLEN ? hk : kv0,
+                            VARLEN ? tok0 + kv0 : kvh);
+                tma_load_3d(sV + c * T::K_CHUNK, &tm_v, bar_kv_full, c * 64, VARLEN ? hk : kv0,
+                            VARLEN ? tok0 + kv0 : kvh);
             }
             int issued = 0;
             for (int it = 0, qb = 0, gq = 0; it < n_it; ++it, (++qb == n_qit) ? (qb = 0, ++gq) : 0) {
@@ -677,8 +757,10 @@ __global__ void __launch_bounds__(448, 1)
                 const uint32_t fb = bar_q_full + 8 * s;
                 mbar_arrive_expect_tx(fb, 2 * T::Q_BYTES + 2 * T::VEC_BYTES);
                 for (int c = 0; c < T::NCH; ++c) {
-                    tma_load_3d(sQ + s * T::Q_BYTES + c * T::Q_CHUNK, &tm_q, fb, c * 64, q0, (bhq0 + gq));
-                    tma_load_3d(sDO + s * T::Q_BYTES + c * T::Q_CHUNK, &tm_do, fb, c * 64, q0, (bhq0 + gq));
+                    tma_load_3d(sQ + s * T::Q_BYTES + c * T::Q_CHUNK, &tm_q, fb, c * 64, VARLEN ? (bhq0 + gq) % H : q0,
+                                VARLEN ? tok0 + q0 : bhq0 + gq);
+                    tma_load_3d(sDO + s * T::Q_BYTES + c * T::Q_CHUNK, &tm_do, fb, c * 64, VARLEN ? (bhq0 + gq) % H : q0,
+                                VARLEN ? tok0 + q0 : bhq0 + gq);
                 }
                 const size_t voff = (size_t)(bhq0 + gq) * Npad + q0;
                 bulk_load(sL2 + s * T::VEC_BYTES, ws_lse2 + voff, T::VEC_BYTES, fb);
@@ -788,7 +870,7 @@ __global__ void __launch_bounds__(448, 1)
             tmem_wait_ld(dpv);
             tc_fence_before();
             mbar_arrive(bar_st_free);  // S^T / dP^T may now be overwritten
-            const bool need_mask = (kv0 + T::BN > N) || (CAUSAL && q0 < kv0 + T::BN - 1);
+            const bool need_mask = (kv0 + T::BN > len) || (CAUSAL && q0 < kv0 + T::BN - 1);
             const float *l2v = l2_f + s * BQ + 32 * h;
             const float *dlv = delta_f + s * BQ + 32 * h;
             uint32_t pk[16], dk_[16];
@@ -804,7 +886,7 @@ __global__ void __launch_bounds__(448, 1)
                     p[u] = ex2(fmaf(__uint_as_float(sv[e + u]), scale_log2, -lq[u]));
                     if (need_mask) {
                         const int q = q0 + 32 * h + e + u;
-                        if (key >= N || (CAUSAL && q < key)) p[u] = 0.f;
+                        if (key >= len || (CAUSAL && q < key)) p[u] = 0.f;
                     }
                     ds[u] = p[u] * (__uint_as_float(dpv[e + u]) - dq_[u]);
                 }
@@ -866,8 +948,10 @@ __global__ void __launch_bounds__(448, 1)
                             __uint_as_float(a[e + 2]) * mul, __uint_as_float(a[e + 3]) * mul);
                 }
                 fence_proxy_async_smem();
-                if (key < N) {
-                    float *dst = (pass == 0 ? dv : dk) + ((size_t)kvh * N + key) * D + 64 * h;
+                if (key < len) {
+                    const size_t krow =
+                        VARLEN ? (size_t)(tok0 + key) * (H / group) + hk : (size_t)kvh * N + key;
+                    float *dst = (pass == 0 ? dv : dk) + krow * D + 64 * h;
                     bulk_store(dst, stg_s, 256);
                 }
                 bulk_commit_group();
@@ -896,9 +980,10 @@ __global__ void __launch_bounds__(448, 1)
             // one bulk asynchronous add into the block's contiguous global dQ rows.
             // The tile is free once the previous bulk add has read it; every sync here
             // is a bounded mbarrier wait, so an abort cannot strand a warp.
-            if (t == 0) {
-                bulk_wait_group_read<0>();
-                mbar_arrive(bar_stg_free);
+            if (warp == 8) {
+                bulk_wait_group_read<0>();  // every lane's adds of the previous block
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar_stg_free);
             }
             ok = mbar_wait_warp(bar_stg_free, it & 1, g, SITE_BWD_DQ_FULL);
             if (!ok) break;
@@ -911,13 +996,26 @@ __global__ void __launch_bounds__(448, 1)
             mbar_arrive(bar_stg_full);
             if (warp == 8) {
                 bool ok0 = true;
-                if (lane == 0) {
-                    ok0 = mbar_wait(bar_stg_full, it & 1, g, SITE_BWD_DQ_FULL);
+                const int rows = min(BQ, len - q0);
+                if constexpr (VARLEN) {
+                    // token-major dQ: the block's rows of this head are H * D floats
+                    // apart, so each lane adds its own rows
+                    ok0 = mbar_wait_warp(bar_stg_full, it & 1, g, SITE_BWD_DQ_FULL);
                     if (ok0) {
-                        const int rows = min(BQ, N - q0);
-                        bulk_reduce_add_f32(dq + ((size_t)(bhq0 + gq) * N + q0) * D, sStage,
-                                            (uint32_t)(rows * D * 4));
+                        const int hq = (bhq0 + gq) % H;
+                        for (int i = lane; i < rows; i += 32)
+                            bulk_reduce_add_f32(dq + ((size_t)(tok0 + q0 + i) * H + hq) * D,
+                                                sStage + (uint32_t)(i * D * 4), (uint32_t)(D * 4));
                         bulk_commit_group();
+                    }
+                } else {
+                    if (lane == 0) {
+                        ok0 = mbar_wait(bar_stg_full, it & 1, g, SITE_BWD_DQ_FULL);
+                        if (ok0) {
+                            bulk_reduce_add_f32(dq + ((size_t)(bhq0 + gq) * N + q0) * D, sStage,
+                                                (uint32_t)(rows * D * 4));
+                            bulk_commit_group();
+                        }
                     }
                 }
                 ok0 = __shfl_sync(0xffffffffu, ok0 ? 1 : 0, 0) != 0;
@@ -929,7 +1027,7 @@ __global__ void __launch_bounds__(448, 1)
         }
         // Only the shared-memory reads of the last bulk add must finish before the
         // CTA retires; its global writes complete before the kernel does.
-        if (t == 0) bulk_wait_group_read<0>();
+        if (warp == 8) bulk_wait_group_read<0>();
     }
 
     __syncwarp();
@@ -941,7 +1039,7 @@ __global__ void __launch_bounds__(448, 1)
     }
 }
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool VARLEN>
 int launch_bwd_t(const BwdParams &p, cudaStream_t stream) {
     using T = BwdTile<D>;
     {
@@ -950,40 +1048,49 @@ int launch_bwd_t(const BwdParams &p, cudaStream_t stream) {
         const long long cap = (long long)p.num_sms * 16;
         if (blocks > cap) blocks = cap;
         if (blocks < 1) blocks = 1;
-        fa_bwd_pre_kernel<D><<<(unsigned)blocks, 256, 0, stream>>>(
+        fa_bwd_pre_kernel<D, VARLEN><<<(unsigned)blocks, 256, 0, stream>>>(
             reinterpret_cast<const __nv_bfloat16 *>(p.o),
             reinterpret_cast<const __nv_bfloat16 *>(p.dout), p.lse, p.ws_delta, p.ws_lse2, p.dq,
-            p.N, p.Npad, p.BH);
+            p.N, p.Npad, p.BH, p.H, p.cu_seqlens, p.total_tokens);
         if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
     }
     const long long grid = (long long)((p.N + T::BN - 1) / T::BN) * (p.BH / p.group);
     if (grid > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
     if constexpr (D == 128) {
-        auto kern = fa_bwd_kernel_d128<CAUSAL>;
+        auto kern = fa_bwd_kernel_d128<CAUSAL, VARLEN>;
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)Bwd128::SMEM_BYTES) != cudaSuccess)
             return FA_ERR_CUDA;
         kern<<<(unsigned)grid, Bwd128::THREADS, Bwd128::SMEM_BYTES, stream>>>(
             p.tm_q, p.tm_k, p.tm_v, p.tm_do, p.ws_lse2, p.ws_delta, p.dq, p.dk, p.dv, p.N, p.Npad,
-            p.BH / p.group, p.H, p.group, p.scale, p.scale_log2, p.status, p.limit_ns);
+            p.BH / p.group, p.H, p.group, p.cu_seqlens, p.total_tokens, p.scale, p.scale_log2,
+            p.status, p.limit_ns);
     } else {
-        auto kern = fa_bwd_kernel<D, CAUSAL>;
+        auto kern = fa_bwd_kernel<D, CAUSAL, VARLEN>;
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)T::SMEM_BYTES) != cudaSuccess)
             return FA_ERR_CUDA;
         kern<<<(unsigned)grid, T::THREADS, T::SMEM_BYTES, stream>>>(
             p.tm_q, p.tm_k, p.tm_v, p.tm_do, p.ws_lse2, p.ws_delta, p.dq, p.dk, p.dv, p.N, p.Npad,
-            p.BH / p.group, p.H, p.group, p.scale, p.scale_log2, p.status, p.limit_ns);
+            p.BH / p.group, p.H, p.group, p.cu_seqlens, p.total_tokens, p.scale, p.scale_log2,
+            p.status, p.limit_ns);
     }
     return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+template <int D>
+int launch_bwd_d(const BwdParams &p, cudaStream_t stream) {
+    if (p.cu_seqlens)
+        return p.causal ? launch_bwd_t<D, true, true>(p, stream) : launch_bwd_t<D, false, true>(p, stream);
+    return p.causal ? launch_bwd_t<D, true, false>(p, stream) : launch_bwd_t<D, false, false>(p, stream);
 }
 
 }  // namespace
 
 int launch_bwd(const BwdParams &p, cudaStream_t stream) {
     switch (p.d) {
-        case 64: return p.causal ? launch_bwd_t<64, true>(p, stream) : launch_bwd_t<64, false>(p, stream);
-        case 128: return p.causal ? launch_bwd_t<128, true>(p, stream) : launch_bwd_t<128, false>(p, stream);
+        case 64: return launch_bwd_d<64>(p, stream);
+        case 128: return launch_bwd_d<128>(p, stream);
         default: return FA_ERR_UNSUPPORTED;
     }
 }

@@ -30,6 +30,7 @@ enum WaitSite : int {
     SITE_BWD_DQ_FULL = 17,
     SITE_BWD_EPILOGUE = 18,
     SITE_BWD_DRAIN = 19,
+    SITE_BWD_BAD_SEQ = 20,
     SITE_DEC_FULL = 21,
     SITE_DEC_EMPTY = 22,
     SITE_DEC_DRAIN = 23,
@@ -63,6 +64,8 @@ struct BwdParams {
     float *ws_delta, *ws_lse2;            // workspace, [BH][Npad] each
     int N, Npad, BH, d, causal;
     int H, group;                         // query heads per batch; query heads per k/v head
+    const int *cu_seqlens;                // varlen: [B+1] sequence starts (token-major), else null
+    int total_tokens;                     // varlen: T
     float scale, scale_log2;
     int *status;
     unsigned long long limit_ns;

@@ -26,7 +26,8 @@ FA_ERR_BAD_INDEX = 7
 EXPORTED = ("fa_fwd", "fa_bwd", "fa_bwd_workspace_bytes", "fa_status_string", "fa_device_status",
             "fa_selftest_wait_timeout", "fa_decode", "fa_decode_num_splits",
             "fa_decode_workspace_bytes", "fa_decode_paged", "fa_decode_paged_num_splits",
-            "fa_decode_paged_workspace_bytes", "fa_fwd_gqa", "fa_bwd_gqa", "fa_fwd_varlen")
+            "fa_decode_paged_workspace_bytes", "fa_fwd_gqa", "fa_bwd_gqa", "fa_fwd_varlen",
+            "fa_bwd_varlen")
 
 _vp = ctypes.c_void_p
 _int = ctypes.c_int
@@ -69,6 +70,9 @@ def load() -> ctypes.CDLL:
         lib.fa_bwd_gqa.restype = _int
         lib.fa_fwd_varlen.argtypes = [_vp] * 6 + [_int] * 7 + [ctypes.c_float, _vp]
         lib.fa_fwd_varlen.restype = _int
+        lib.fa_bwd_varlen.argtypes = [_vp] * 10 + [_int] * 7 + [ctypes.c_float, _vp, ctypes.c_size_t,
+                                                                 _vp]
+        lib.fa_bwd_varlen.restype = _int
         lib.fa_decode.argtypes = [_vp] * 5 + [_int] * 6 + [ctypes.c_float, _int, _vp,
                                                           ctypes.c_size_t, _vp]
         lib.fa_decode.restype = _int
@@ -137,6 +141,13 @@ def fa_fwd_varlen(q, k, v, o, lse, cu_seqlens, B, H, Hkv, total_tokens, max_seql
                   scale, stream) -> int:
     return load().fa_fwd_varlen(q, k, v, o, lse, cu_seqlens, B, H, Hkv, total_tokens, max_seqlen,
                                 d, int(bool(causal)), scale, stream)
+
+
+def fa_bwd_varlen(q, k, v, o, lse, dout, dq, dk, dv, cu_seqlens, B, H, Hkv, total_tokens,
+                  max_seqlen, d, causal, scale, workspace, workspace_bytes, stream) -> int:
+    return load().fa_bwd_varlen(q, k, v, o, lse, dout, dq, dk, dv, cu_seqlens, B, H, Hkv,
+                                total_tokens, max_seqlen, d, int(bool(causal)), scale, workspace,
+                                workspace_bytes, stream)
 
 
 def fa_decode(q, k, v, o, lse, B, H, Hkv, Nq, Nk, d, scale, num_splits, workspace,
@@ -374,3 +385,43 @@ def forward_varlen(q, k, v, cu_seqlens, max_seqlen, causal=False, scale=None, ou
     if rc != FA_OK:
         raise FaError(rc, "fa_fwd_varlen")
     return out, lse
+
+
+def backward_varlen(q, k, v, o, lse, do, cu_seqlens, max_seqlen, causal=False, scale=None,
+                    dq=None, dk=None, dv=None, workspace=None, stream=None):
+    """Gradients of forward_varlen: q/o/do bf16 [T,H,d], k/v [T,Hkv,d], lse [H,T].
+    Returns (dq [T,H,d], dk [T,Hkv,d], dv [T,Hkv,d]) fp32."""
+    _check("q", q, torch.bfloat16)
+    if q.dim() != 3:
+        raise ValueError("q must be [T, H, d]")
+    T, H, d = q.shape
+    _check("k", k, torch.bfloat16)
+    if k.dim() != 3 or k.shape[0] != T or k.shape[2] != d or H % k.shape[1]:
+        raise ValueError("k must be [T, Hkv, d] with Hkv dividing H")
+    Hkv = k.shape[1]
+    _check("v", v, torch.bfloat16, k.shape)
+    for name, t in (("o", o), ("do", do)):
+        _check(name, t, torch.bfloat16, q.shape)
+    _check("lse", lse, torch.float32, (H, T))
+    _check("cu_seqlens", cu_seqlens, torch.int32)
+    B = cu_seqlens.numel() - 1
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    grads = []
+    for name, t, shape in (("dq", dq, q.shape), ("dk", dk, k.shape), ("dv", dv, k.shape)):
+        if t is None:
+            t = torch.zeros(shape, dtype=torch.float32, device=q.device)
+        _check(name, t, torch.float32, shape)
+        grads.append(t)
+    need = fa_bwd_workspace_bytes(B, H, int(max_seqlen), d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    _check("workspace", workspace, torch.uint8)
+    with torch.cuda.device(q.device):
+        rc = fa_bwd_varlen(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                           do.data_ptr(), grads[0].data_ptr(), grads[1].data_ptr(),
+                           grads[2].data_ptr(), cu_seqlens.data_ptr(), B, H, Hkv, T,
+                           int(max_seqlen), d, causal, scale, workspace.data_ptr(),
+                           workspace.numel(), _stream(q, stream))
+    if rc != FA_OK:
+        raise FaError(rc, "fa_bwd_varlen")
+    return tuple(grads)

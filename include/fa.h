@@ -164,6 +164,22 @@ int fa_fwd_varlen(const void *q, const void *k, const void *v, void *o, float *l
                   int d, int causal, float scale, void *stream);
 
 /*
+ * Backward pass of fa_fwd_varlen: gradients for packed sequences.
+ *   q, k, v, o, dout : token-major as in fa_fwd_varlen (o, lse as it wrote them).
+ *   dq               : fp32 [total_tokens][H][d]; dk, dv fp32 [total_tokens][Hkv][d].
+ *                      Rows of the tokens of every sequence are overwritten; rows of
+ *                      tokens that belong to no sequence are left untouched.
+ *   d                : 64 or 128.
+ *   workspace        : fa_bwd_workspace_bytes(B, H, max_seqlen, d) bytes.
+ * cu_seqlens is checked on the device as in fa_fwd_varlen (FA_ERR_BAD_INDEX).  Other
+ * arguments as in fa_bwd / fa_bwd_gqa.
+ */
+int fa_bwd_varlen(const void *q, const void *k, const void *v, const void *o, const float *lse,
+                  const void *dout, float *dq, float *dk, float *dv, const int *cu_seqlens, int B,
+                  int H, int Hkv, int total_tokens, int max_seqlen, int d, int causal, float scale,
+                  void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * Decode attention with a split key range (course page "10 FlashAttention",
  * section "The decode variant: FlashDecoding"): Nq query rows per (b, h), usually
  * one, attend to all Nk cached keys of their head, with no mask:

@@ -178,3 +178,15 @@ def test_varlen_rejects_bad_arguments(fa, kw, code):
     a.update(kw)
     assert fa.fa_fwd_varlen(a["q"], a["k"], a["v"], a["o"], a["lse"], a["cu"], a["B"], a["H"], a["Hkv"],
                             a["T"], a["maxlen"], a["d"], a["causal"], a["scale"], None) == code
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(cu=None), 1), (dict(dq=None), 1), (dict(T=0), 1), (dict(maxlen=0), 1), (dict(Hkv=3), 1),
+    (dict(d=256), 2), (dict(ws=None), 6), (dict(ws_bytes=16), 6), (dict(cu=DUMMY + 1), 3),
+])
+def test_varlen_backward_rejects_bad_arguments(fa, kw, code):
+    a = dict(cu=DUMMY, dq=DUMMY, T=100, maxlen=64, Hkv=2, d=128, ws=DUMMY, ws_bytes=1 << 20)
+    a.update(kw)
+    assert fa.fa.fa_bwd_varlen(DUMMY, DUMMY, DUMMY, DUMMY, DUMMY, DUMMY, a["dq"], DUMMY, DUMMY, a["cu"], 2, 4,
+                               a["Hkv"], a["T"], a["maxlen"], a["d"], 1, 0.1, a["ws"], a["ws_bytes"],
+                               None) == code
