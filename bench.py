@@ -48,11 +48,13 @@ FWD_WORKLOADS = [
     ("B1_H16_N16384_d128_causal", 1, 16, 16384, 128, True, "normal"),
     ("B4_H8_N8192_d256_noncausal_boosted", 4, 8, 8192, 256, False, "boosted"),
     ("B2_H16_N4096_d128_causal", 2, 16, 4096, 128, True, "normal"),
+    ("B4_H16_N4096_d96_causal", 4, 16, 4096, 96, True, "normal"),
 ]
 BWD_WORKLOADS = [
     ("B2_H16_N4096_d128_causal", 2, 16, 4096, 128, True),
     ("B2_H16_N4096_d128_noncausal", 2, 16, 4096, 128, False),
     ("B8_H16_N2048_d64_causal", 8, 16, 2048, 64, True),
+    ("B4_H16_N4096_d96_causal", 4, 16, 4096, 96, True),
 ]
 
 # Split-KV decode (one query row per sequence against a long cache): bound by HBM.
@@ -256,7 +258,7 @@ def run_ours(args, rank, world, local_rank):
         f_ms = statistics.mean(fwd_ms)
         b_ms = statistics.mean(bwd_ms)
         if b_ms >= f_ms:
-            kern, kflops, kms = "fa_bwd (fa_bwd_pre_kernel<128> + fa_bwd_kernel_d128<causal>)", \
+            kern, kflops, kms = "fa_bwd (fa_bwd_pre_kernel<128> + fa_bwd_kernel_wide<128, causal>)", \
                 bwd_flops(B, H, N, d, causal), b_ms
             traffic = recorded_traffic("fa_bwd_d128_causal_b2h16n4096")
         else:

@@ -100,9 +100,9 @@ int check_sizes(int B, int H, int N, int d, bool fwd) {
     if (B < 1 || H < 1 || N < 1) return FA_ERR_INVALID_ARG;
     if ((long long)B * H * N >= (1LL << 31)) return FA_ERR_INVALID_ARG;
     if (fwd) {
-        if (d != 64 && d != 128 && d != 256) return FA_ERR_UNSUPPORTED;
+        if (d != 64 && d != 96 && d != 128 && d != 256) return FA_ERR_UNSUPPORTED;
     } else {
-        if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+        if (d != 64 && d != 96 && d != 128) return FA_ERR_UNSUPPORTED;
     }
     return FA_OK;
 }
@@ -196,7 +196,7 @@ extern "C" int fa_fwd_varlen(const void *q, const void *k, const void *v, void *
     if (B < 1 || H < 1 || total_tokens < 1 || max_seqlen < 1) return FA_ERR_INVALID_ARG;
     if ((long long)total_tokens * H >= (1LL << 31) || (long long)B * H >= (1LL << 31))
         return FA_ERR_INVALID_ARG;
-    if (d != 64 && d != 128 && d != 256) return FA_ERR_UNSUPPORTED;
+    if (d != 64 && d != 96 && d != 128 && d != 256) return FA_ERR_UNSUPPORTED;
     const int group = gqa_group(H, Hkv);
     if (group == 0) return FA_ERR_INVALID_ARG;
     int rc = check_scale(scale);
@@ -256,7 +256,7 @@ extern "C" int fa_bwd_gqa(const void *q, const void *k, const void *v, const voi
     BwdParams p{};
     const int BH = B * H;
     const int npad = (int)round_up((size_t)N, kBwdPad);
-    const int q_rows = (d == 128) ? 64 : 128;  // query rows per backward q-block
+    const int q_rows = (d >= 96) ? 64 : 128;  // query rows per backward q-block
     if ((rc = make_bhnd_map(&p.tm_q, q, BH, N, d, q_rows)) != FA_OK) return rc;
     if ((rc = make_bhnd_map(&p.tm_do, dout, BH, N, d, q_rows)) != FA_OK) return rc;
     if ((rc = make_bhnd_map(&p.tm_k, k, B * Hkv, N, d, 128)) != FA_OK) return rc;
@@ -295,7 +295,7 @@ extern "C" int fa_bwd_varlen(const void *q, const void *k, const void *v, const 
     if ((long long)total_tokens * H >= (1LL << 31) ||
         (long long)B * H * (long long)round_up((size_t)max_seqlen, kBwdPad) >= (1LL << 31))
         return FA_ERR_INVALID_ARG;
-    if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+    if (d != 64 && d != 96 && d != 128) return FA_ERR_UNSUPPORTED;
     const int group = gqa_group(H, Hkv);
     if (group == 0) return FA_ERR_INVALID_ARG;
     int rc = check_scale(scale);
@@ -311,7 +311,7 @@ extern "C" int fa_bwd_varlen(const void *q, const void *k, const void *v, const 
     BwdParams p{};
     const int BH = B * H;
     const int npad = (int)round_up((size_t)max_seqlen, kBwdPad);
-    const int q_rows = (d == 128) ? 64 : 128;
+    const int q_rows = (d >= 96) ? 64 : 128;
     if ((rc = make_thd_map(&p.tm_q, q, total_tokens, H, d, q_rows)) != FA_OK) return rc;
     if ((rc = make_thd_map(&p.tm_do, dout, total_tokens, H, d, q_rows)) != FA_OK) return rc;
     if ((rc = make_thd_map(&p.tm_k, k, total_tokens, Hkv, d, 128)) != FA_OK) return rc;

@@ -123,9 +123,18 @@ __global__ void __launch_bounds__(256)
             lse_i = (size_t)bh * N + i;
         }
         if (i < len) {
-            const size_t row = row_i + (size_t)lane * PER;
             float acc = 0.f;
-            if constexpr (PER == 4) {
+            if constexpr (PER == 3) {
+                // d = 96: lane takes columns lane, lane + 32, lane + 64 (each load of
+                // the warp reads 64 contiguous bytes)
+#pragma unroll
+                for (int e = 0; e < 3; ++e) {
+                    const size_t c = row_i + (size_t)(lane + 32 * e);
+                    acc = fmaf(__bfloat162float(o[c]), __bfloat162float(dout[c]), acc);
+                    dq[c] = 0.f;
+                }
+            } else if constexpr (PER == 4) {
+                const size_t row = row_i + (size_t)lane * PER;
                 const uint2 a = *reinterpret_cast<const uint2 *>(o + row);
                 const uint2 b = *reinterpret_cast<const uint2 *>(dout + row);
                 const __nv_bfloat162 *pa = reinterpret_cast<const __nv_bfloat162 *>(&a);
@@ -139,6 +148,8 @@ __global__ void __launch_bounds__(256)
                 }
                 *reinterpret_cast<float4 *>(dq + row) = make_float4(0.f, 0.f, 0.f, 0.f);
             } else {
+                static_assert(PER == 2, "head dim 64, 96 or 128");
+                const size_t row = row_i + (size_t)lane * PER;
                 const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162 *>(o + row);
                 const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162 *>(dout + row);
                 const float2 fa = __bfloat1622float2(a);
@@ -580,7 +591,7 @@ __global__ void __launch_bounds__(320, 1)
     }
 }
 
-// ---------------------------------------------------------------- d = 128 kernel
+// ---------------------------------------------------------------- d = 96, 128 kernel
 //
 // Same products as fa_bwd_kernel, scheduled so the tensor core never waits for
 // the P^T/dS^T warps.  Tensor memory (512 columns): dV [0,128), dK [128,256),
@@ -592,16 +603,23 @@ __global__ void __launch_bounds__(320, 1)
 // block i+1 (pd_free).  Per block the MMA thread issues
 //   S^T(i+1), dP^T(i+1)  |  dV(i), dK(i)  |  dQ^T(i)
 // Two compute warpgroups split the 64 query columns of a block.
-struct Bwd128 {
-    static constexpr int D = 128;
+//
+// d = 96 keeps the d = 128 layout: rows are two 64-column swizzle chunks whose
+// columns past d the copies zero-fill, S^T and dP^T run D/16 K steps, dV and dK
+// have N = D, and dQ^T keeps M = 128 (its rows past d come out zero and are not
+// read).
+template <int D_>
+struct BwdWide {
+    static constexpr int D = D_;
+    static constexpr int DP = 128;                      // row width in shared memory
     static constexpr int BN = 128;
     static constexpr int BQ = 64;
     static constexpr int NCH = 2;
     static constexpr int QS = 3;                        // Q/dO/L/D ring stages
     static constexpr uint32_t K_CHUNK = BN * 128;
     static constexpr uint32_t Q_CHUNK = BQ * 128;
-    static constexpr uint32_t KV_BYTES = BN * D * 2;
-    static constexpr uint32_t Q_BYTES = BQ * D * 2;
+    static constexpr uint32_t KV_BYTES = BN * DP * 2;
+    static constexpr uint32_t Q_BYTES = BQ * DP * 2;
     static constexpr uint32_t DS_BYTES = BQ * BN * 2;   // dS^T, [128 keys][64 queries] bf16
     static constexpr uint32_t STAGE_BYTES = BQ * D * 4; // dQ tile, fp32
     static constexpr uint32_t VEC_BYTES = BQ * 4;
@@ -625,19 +643,20 @@ struct Bwd128 {
     static constexpr int THREADS = 448;  // compute 0-7, dQ readout 8-11, TMA 12, MMA 13
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
     static_assert(Q_CHUNK % 1024 == 0 && DS_BYTES % 1024 == 0, "swizzle atoms must stay aligned");
+    static_assert(D == 96 || D == 128, "head dim");
 };
 
-template <bool CAUSAL, bool VARLEN>
+template <int D, bool CAUSAL, bool VARLEN>
 __global__ void __launch_bounds__(448, 1)
-    fa_bwd_kernel_d128(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+    fa_bwd_kernel_wide(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                        const float *__restrict__ ws_lse2, const float *__restrict__ ws_delta,
                        float *__restrict__ dq, float *__restrict__ dk, float *__restrict__ dv, int N,
                        int Npad, int BHkv, int H, int group, const int *__restrict__ cu_seqlens,
                   int total_tokens, float scale, float scale_log2, int *status,
                        unsigned long long limit_ns) {
-    using T = Bwd128;
-    constexpr int BQ = T::BQ, QS = T::QS, D = T::D;
+    using T = BwdWide<D>;
+    constexpr int BQ = T::BQ, QS = T::QS;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -923,7 +942,7 @@ __global__ void __launch_bounds__(448, 1)
         ok = ok && mbar_wait_warp(bar_done, 0, g, SITE_BWD_EPILOGUE);
         if (ok) {
             tc_fence_after();
-            // Each thread owns half a key row (d columns [64h, 64h + 64)).  Rows are
+            // Each thread owns half a key row (d columns [64h, min(64h + 64, D))).  Rows are
             // staged in shared memory at a 528-byte pitch (16-byte writes without bank
             // conflicts; the Q/dO area is free once every MMA is done) and leave with
             // one bulk copy per half-row, so global writes are 256 contiguous bytes.
@@ -936,8 +955,10 @@ __global__ void __launch_bounds__(448, 1)
                 const uint32_t tcol = (pass == 0 ? T::TM_DV : T::TM_DK) + 64 * h;
                 const float mul = pass == 0 ? 1.f : scale;
                 if (pass == 1) bulk_wait_group_read<0>();  // own staging row is reused
+                constexpr int kHalf1 = (D - 64) / 32;  // 32-column loads of the second half
 #pragma unroll
                 for (int c = 0; c < 2; ++c) {
+                    if (h == 1 && c >= kHalf1) break;
                     uint32_t a[32];
                     tmem_ld32(tmem + lane_base + tcol + 32 * c, a);
                     tmem_wait_ld(a);
@@ -952,7 +973,7 @@ __global__ void __launch_bounds__(448, 1)
                     const size_t krow =
                         VARLEN ? (size_t)(tok0 + key) * (H / group) + hk : (size_t)kvh * N + key;
                     float *dst = (pass == 0 ? dv : dk) + krow * D + 64 * h;
-                    bulk_store(dst, stg_s, 256);
+                    bulk_store(dst, stg_s, h == 0 ? 256u : (uint32_t)(D - 64) * 4);
                 }
                 bulk_commit_group();
             }
@@ -987,10 +1008,12 @@ __global__ void __launch_bounds__(448, 1)
             }
             ok = mbar_wait_warp(bar_stg_free, it & 1, g, SITE_BWD_DQ_FULL);
             if (!ok) break;
+            if (t < D) {  // rows of dQ^T past d are zero padding
 #pragma unroll
-            for (int e = 0; e < 32; ++e) {
-                stage_f[e * D + t] = __uint_as_float(x0[e]) * scale;
-                stage_f[(e + 32) * D + t] = __uint_as_float(x1[e]) * scale;
+                for (int e = 0; e < 32; ++e) {
+                    stage_f[e * D + t] = __uint_as_float(x0[e]) * scale;
+                    stage_f[(e + 32) * D + t] = __uint_as_float(x1[e]) * scale;
+                }
             }
             fence_proxy_async_smem();
             mbar_arrive(bar_stg_full);
@@ -1041,7 +1064,6 @@ __global__ void __launch_bounds__(448, 1)
 
 template <int D, bool CAUSAL, bool VARLEN>
 int launch_bwd_t(const BwdParams &p, cudaStream_t stream) {
-    using T = BwdTile<D>;
     {
         const long long rows = (long long)p.BH * p.Npad;
         long long blocks = (rows * 32 + 255) / 256;
@@ -1054,18 +1076,22 @@ int launch_bwd_t(const BwdParams &p, cudaStream_t stream) {
             p.N, p.Npad, p.BH, p.H, p.cu_seqlens, p.total_tokens);
         if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
     }
-    const long long grid = (long long)((p.N + T::BN - 1) / T::BN) * (p.BH / p.group);
+    constexpr int kBN = 128;  // keys per CTA in both kernels
+    static_assert(kBN == BwdWide<128>::BN && kBN == BwdTile<64>::BN, "key block");
+    const long long grid = (long long)((p.N + kBN - 1) / kBN) * (p.BH / p.group);
     if (grid > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
-    if constexpr (D == 128) {
-        auto kern = fa_bwd_kernel_d128<CAUSAL, VARLEN>;
+    if constexpr (D >= 96) {
+        using W = BwdWide<D>;
+        auto kern = fa_bwd_kernel_wide<D, CAUSAL, VARLEN>;
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)Bwd128::SMEM_BYTES) != cudaSuccess)
+                                 (int)W::SMEM_BYTES) != cudaSuccess)
             return FA_ERR_CUDA;
-        kern<<<(unsigned)grid, Bwd128::THREADS, Bwd128::SMEM_BYTES, stream>>>(
+        kern<<<(unsigned)grid, W::THREADS, W::SMEM_BYTES, stream>>>(
             p.tm_q, p.tm_k, p.tm_v, p.tm_do, p.ws_lse2, p.ws_delta, p.dq, p.dk, p.dv, p.N, p.Npad,
             p.BH / p.group, p.H, p.group, p.cu_seqlens, p.total_tokens, p.scale, p.scale_log2,
             p.status, p.limit_ns);
     } else {
+        using T = BwdTile<D>;
         auto kern = fa_bwd_kernel<D, CAUSAL, VARLEN>;
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)T::SMEM_BYTES) != cudaSuccess)
@@ -1090,6 +1116,7 @@ int launch_bwd_d(const BwdParams &p, cudaStream_t stream) {
 int launch_bwd(const BwdParams &p, cudaStream_t stream) {
     switch (p.d) {
         case 64: return launch_bwd_d<64>(p, stream);
+        case 96: return launch_bwd_d<96>(p, stream);
         case 128: return launch_bwd_d<128>(p, stream);
         default: return FA_ERR_UNSUPPORTED;
     }

@@ -54,11 +54,15 @@ struct FwdTile {
     static constexpr int BN = (D == 256) ? 64 : 128;  // keys per K/V tile
     static constexpr int KS = (D == 64) ? 4 : 3;      // K ring stages
     static constexpr int VS = (D == 64) ? 4 : 2;      // V ring stages
-    static constexpr int NCH = D / 64;                // 128-byte swizzle chunks per row
+    // Rows sit in shared memory as 128-byte swizzle chunks of 64 columns; d = 96
+    // takes two chunks, the columns past d zero-filled by the copy and never read
+    // by a product (S runs D/16 K steps, PV has N = D).
+    static constexpr int DP = (D + 63) / 64 * 64;     // row width in shared memory
+    static constexpr int NCH = DP / 64;               // 128-byte swizzle chunks per row
     static constexpr uint32_t Q_CHUNK = BM * 128;
     static constexpr uint32_t KV_CHUNK = BN * 128;
-    static constexpr uint32_t Q_BYTES = BM * D * 2;   // one query tile
-    static constexpr uint32_t KV_BYTES = BN * D * 2;  // one of K_j, V_j
+    static constexpr uint32_t Q_BYTES = BM * DP * 2;  // one query tile
+    static constexpr uint32_t KV_BYTES = BN * DP * 2; // one of K_j, V_j
     // tensor memory columns: S slot u at BN u (fp32; P as bf16 over its first BN/2
     // columns), then O_t (fp32, D columns) at BN NS + D t
     static constexpr uint32_t TM_O0 = BN * NS;
@@ -77,7 +81,7 @@ struct FwdTile {
     static constexpr int WARP_LOAD = 4 * NT + 1;
     static constexpr int THREADS = 128 * NT + 64;
 
-    static_assert(D == 64 || D == 128 || D == 256, "head dim");
+    static_assert(D == 64 || D == 96 || D == 128 || D == 256, "head dim");
     static_assert(Q_CHUNK % 1024 == 0 && KV_CHUNK % 1024 == 0, "swizzle atoms must stay aligned");
     static_assert(TM_O0 + NT * D <= TM_COLS, "tensor memory budget");
     static_assert(BN % 64 == 0, "P is packed 64 keys per tcgen05.st");
@@ -637,6 +641,7 @@ int launch_fwd_d(const FwdParams &p, cudaStream_t stream) {
 int launch_fwd(const FwdParams &p, cudaStream_t stream) {
     switch (p.d) {
         case 64: return launch_fwd_d<64>(p, stream);
+        case 96: return launch_fwd_d<96>(p, stream);
         case 128: return launch_fwd_d<128>(p, stream);
         case 256: return launch_fwd_d<256>(p, stream);
         default: return FA_ERR_UNSUPPORTED;

@@ -61,7 +61,8 @@ typedef enum {
  *   lse     : fp32 [B][H][N] output, the natural-log L of each query row.
  *   B, H, N : batch, heads, sequence length (queries = keys = N); each >= 1,
  *             B*H*N < 2^31.  N need not be a multiple of any tile size.
- *   d       : head dimension, one of 64, 128, 256.
+ *   d       : head dimension, one of 64, 96, 128, 256 (96: rows padded to 128 columns
+ *             in shared memory by the copies, products run over the 96 columns).
  *   causal  : nonzero for the causal mask (top-left aligned, j <= i).
  *   scale   : multiplies Q K^T before the softmax; finite and > 0 (1/sqrt(d) is
  *             the usual value).
@@ -84,7 +85,7 @@ size_t fa_bwd_workspace_bytes(int B, int H, int N, int d);
  *   lse              : fp32 [B][H][N].
  *   dq, dk, dv       : fp32 [B][H][N][d] outputs, overwritten (fa_bwd zeroes dq
  *                      itself before accumulating into it).
- *   d                : 64 or 128 (256 returns FA_ERR_UNSUPPORTED).
+ *   d                : 64, 96 or 128 (256 returns FA_ERR_UNSUPPORTED).
  *   workspace        : device buffer of at least fa_bwd_workspace_bytes(B,H,N,d)
  *                      bytes, 16-byte aligned, owned by the caller; its contents
  *                      on entry do not matter and are overwritten.
@@ -169,7 +170,7 @@ int fa_fwd_varlen(const void *q, const void *k, const void *v, void *o, float *l
  *   dq               : fp32 [total_tokens][H][d]; dk, dv fp32 [total_tokens][Hkv][d].
  *                      Rows of the tokens of every sequence are overwritten; rows of
  *                      tokens that belong to no sequence are left untouched.
- *   d                : 64 or 128.
+ *   d                : 64, 96 or 128.
  *   workspace        : fa_bwd_workspace_bytes(B, H, max_seqlen, d) bytes.
  * cu_seqlens is checked on the device as in fa_fwd_varlen (FA_ERR_BAD_INDEX).  Other
  * arguments as in fa_bwd / fa_bwd_gqa.

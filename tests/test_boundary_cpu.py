@@ -64,7 +64,7 @@ def _fwd(fa, **kw):
 @pytest.mark.parametrize("kw,code", [
     (dict(q=None), 1), (dict(k=None), 1), (dict(v=None), 1), (dict(o=None), 1), (dict(lse=None), 1),
     (dict(B=0), 1), (dict(H=-1), 1), (dict(N=0), 1), (dict(B=65536, H=256, N=256), 1),
-    (dict(d=96), 2), (dict(d=32), 2), (dict(d=0), 2),
+    (dict(d=80), 2), (dict(d=32), 2), (dict(d=0), 2),
     (dict(scale=0.0), 1), (dict(scale=-1.0), 1), (dict(scale=float("inf")), 1), (dict(scale=float("nan")), 1),
     (dict(q=DUMMY + 8), 3), (dict(lse=DUMMY + 4), 3), (dict(o=DUMMY + 2), 3),
 ])
@@ -83,7 +83,7 @@ def _bwd(fa, **kw):
 
 @pytest.mark.parametrize("kw,code", [
     (dict(q=None), 1), (dict(do=None), 1), (dict(dq=None), 1), (dict(dv=None), 1),
-    (dict(N=0), 1), (dict(d=256), 2), (dict(d=96), 2), (dict(scale=0.0), 1),
+    (dict(N=0), 1), (dict(d=256), 2), (dict(d=80), 2), (dict(scale=0.0), 1),
     (dict(ws=None), 6), (dict(ws_bytes=16), 6),
     (dict(dk=DUMMY + 4), 3), (dict(ws=DUMMY + 8), 3),
 ])
@@ -97,6 +97,7 @@ def test_workspace_size(fa):
     assert fa.fa_bwd_workspace_bytes(1, 1, 129, 64) == 2 * 256 * 4
     assert fa.fa_bwd_workspace_bytes(1, 1, 0, 64) == 0
     assert fa.fa_bwd_workspace_bytes(1, 1, 128, 256) == 0
+    assert fa.fa_bwd_workspace_bytes(1, 2, 100, 96) == 2 * 2 * 128 * 4
 
 
 def test_python_wrapper_rejects_cpu_tensors(fa):
@@ -170,7 +171,7 @@ def test_gqa_rejects_bad_head_counts(fa, Hkv, code):
 
 @pytest.mark.parametrize("kw,code", [
     (dict(cu=None), 1), (dict(q=None), 1), (dict(B=0), 1), (dict(T=0), 1), (dict(maxlen=0), 1),
-    (dict(Hkv=3), 1), (dict(d=96), 2), (dict(scale=0.0), 1), (dict(cu=DUMMY + 2), 3), (dict(q=DUMMY + 8), 3),
+    (dict(Hkv=3), 1), (dict(d=80), 2), (dict(scale=0.0), 1), (dict(cu=DUMMY + 2), 3), (dict(q=DUMMY + 8), 3),
 ])
 def test_varlen_rejects_bad_arguments(fa, kw, code):
     a = dict(q=DUMMY, k=DUMMY, v=DUMMY, o=DUMMY, lse=DUMMY, cu=DUMMY, B=2, H=4, Hkv=2, T=100,

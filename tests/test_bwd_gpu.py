@@ -38,7 +38,8 @@ def _check(got, ref, what):
 
 SMALL = [
     (1, 1, 1, 64), (1, 1, 2, 128), (1, 2, 100, 64), (1, 1, 128, 128), (2, 1, 129, 128),
-    (1, 2, 300, 64), (1, 1, 513, 128), (2, 2, 640, 128), (1, 1, 1000, 64),
+    (1, 2, 300, 64), (1, 1, 513, 128), (2, 2, 640, 128), (1, 1, 1000, 64), (1, 1, 1, 96),
+    (1, 2, 130, 96), (2, 1, 513, 96),
 ]
 
 
@@ -77,6 +78,19 @@ def test_bwd_b2_h4_n2048_d64(fa, orc, causal):
     sl = (slice(1, 2), slice(2, 4))
     ref = orc.bwd(to_f64(q[sl]), to_f64(k[sl]), to_f64(v[sl]), to_f64(do[sl]), causal=causal)
     _check([g[sl] for g in got], ref, "2048x64")
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_bwd_b2_h8_n2048_d96(fa, orc, causal):
+    """Head dimension 96 at a size that fills the GPU: two whole heads against the
+    oracle, the gradient sums on every head."""
+    q, k, v, do = normal_qkv(2, 8, 2048, 96, seed=5, with_do=True)
+    got = _grads(fa, q, k, v, do, causal)
+    sl = (slice(1, 2), slice(3, 5))
+    ref = orc.bwd(to_f64(q[sl]), to_f64(k[sl]), to_f64(v[sl]), to_f64(do[sl]), causal=causal)
+    _check([g[sl] for g in got], ref, "2048x96")
+    assert np.max(np.abs(got[1].sum(axis=2))) < 0.5
+    assert np.max(np.abs(got[2].sum(axis=2) - do.double().sum(dim=2).numpy())) < 0.5
 
 
 @pytest.mark.parametrize("scale", [1.5, 0.02])

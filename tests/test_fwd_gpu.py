@@ -37,7 +37,7 @@ def _run(fa, q, k, v, causal, scale=None):
 SMALL = [
     (1, 1, 1, 64), (1, 2, 2, 128), (1, 1, 100, 64), (1, 1, 128, 64), (2, 1, 129, 128),
     (1, 2, 256, 128), (1, 1, 300, 256), (1, 2, 383, 64), (1, 1, 513, 128), (1, 1, 200, 256),
-    (2, 3, 640, 64), (1, 1, 1000, 256),
+    (2, 3, 640, 64), (1, 1, 1000, 256), (1, 1, 1, 96), (1, 2, 200, 96), (2, 1, 513, 96),
 ]
 
 
@@ -70,6 +70,12 @@ def _sampled(fa, orc, q, k, v, causal, nrows, seed=2):
     assert_o_close(o[:, :, rows], ro, f"{tuple(q.shape)} causal={causal} sampled")
     assert_abs_close(lse[:, :, rows], rl, L_ABS, f"{tuple(q.shape)} L sampled")
     return o, lse
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_fwd_b4_h16_n4096_d96(fa, orc, causal):
+    q, k, v = normal_qkv(4, 16, 4096, 96, seed=0)
+    _sampled(fa, orc, q, k, v, causal, 48)
 
 
 @pytest.mark.parametrize("causal", [False, True])

@@ -41,7 +41,7 @@ def _fold(g, group):
 
 
 FWD = [(1, 4, 1, 300, 64), (2, 8, 2, 256, 128), (1, 6, 3, 129, 256), (1, 4, 4, 200, 128),
-       (1, 16, 2, 640, 64)]
+       (1, 16, 2, 640, 64), (1, 4, 2, 333, 96)]
 
 
 @pytest.mark.parametrize("causal", [False, True])
@@ -68,7 +68,8 @@ def test_gqa_forward_equals_repeated_heads(fa):
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
 
 
-BWD = [(1, 4, 2, 300, 128), (2, 4, 1, 256, 64), (1, 8, 2, 513, 128), (1, 3, 3, 129, 64)]
+BWD = [(1, 4, 2, 300, 128), (2, 4, 1, 256, 64), (1, 8, 2, 513, 128), (1, 3, 3, 129, 64),
+       (1, 4, 2, 257, 96)]
 
 
 @pytest.mark.parametrize("causal", [False, True])

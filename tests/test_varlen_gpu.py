@@ -32,7 +32,7 @@ def orc():
 
 CASES = [
     ([200, 129, 1, 513], 4, 2, 128), ([300, 0, 77], 2, 2, 64), ([256, 256], 3, 1, 256),
-    ([1, 2, 3], 4, 4, 128), ([1000, 17, 640], 8, 2, 64),
+    ([1, 2, 3], 4, 4, 128), ([1000, 17, 640], 8, 2, 64), ([70, 300, 129], 4, 2, 96),
 ]
 
 
@@ -88,7 +88,7 @@ def test_varlen_bad_offsets_are_reported(fa):
 
 
 BWD_CASES = [([200, 129, 1, 513], 4, 2, 128), ([300, 0, 77], 2, 2, 64), ([1, 2, 3], 4, 4, 128),
-             ([640, 17], 8, 2, 64), ([384, 256], 2, 1, 128)]
+             ([640, 17], 8, 2, 64), ([384, 256], 2, 1, 128), ([200, 1, 65], 4, 2, 96)]
 
 
 @pytest.mark.parametrize("causal", [False, True])
