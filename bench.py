@@ -225,6 +225,11 @@ def run_ours(args, rank, world, local_rank):
         dist.barrier()
     torch.cuda.synchronize(dev)
     wall0 = time.perf_counter()
+    # Two extra flushes give the host a head start, so that it has enqueued the first
+    # step's calls before the GPU reaches that step's first event (the host then
+    # stays ahead: a step is ~0.5 ms of GPU work and far less host work).
+    flush.zero_()
+    flush.zero_()
     for it in range(args.steps):
         flush.zero_()  # L2 flush, outside the per-step events
         evs[it][0].record(stream)
@@ -304,6 +309,7 @@ def run_ours(args, rank, world, local_rank):
             result["backward_workloads"] = sweep_backward(fa, torch, dev, flush, normal_qkv,
                                                           load_peaks())
             result["decode_workloads"] = sweep_decode(fa, torch, dev, flush, load_peaks())
+            result["fp8_workloads"] = sweep_fp8(fa, torch, dev, flush, load_peaks())
         if world == 1 and not args.no_cpu_baseline:
             result["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
         else:
@@ -347,19 +353,24 @@ def run_e2e(args, fa, torch, dev, host_inputs, causal, flops_step, world):
 
 
 def _time_call(torch, dev, fn, flush, iters=20, warm=3):
+    """Median device time of fn() between CUDA events, L2 flushed before each call.
+    Every iteration is enqueued before any is waited for, so the host's per-call
+    work (argument checks, tensor-map encoding) overlaps the previous flush and
+    never leaves the GPU idle inside the events."""
     for _ in range(warm):
         fn()
     torch.cuda.synchronize(dev)
-    ts = []
+    evs = []
+    flush.zero_()
     for _ in range(iters):
         flush.zero_()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record()
         fn()
         b.record()
-        b.synchronize()
-        ts.append(a.elapsed_time(b))
-    return statistics.median(ts)
+        evs.append((a, b))
+    torch.cuda.synchronize(dev)
+    return statistics.median(a.elapsed_time(b) for a, b in evs)
 
 
 def sweep_forward(fa, torch, dev, flush, normal_qkv, boosted_qkv, peaks):
@@ -431,6 +442,48 @@ def sweep_decode(fa, torch, dev, flush, peaks):
                                   "peak": peaks["hbm_gbs"], "unit": "GB/s",
                                   "frac": round(gbs / peaks["hbm_gbs"], 4)}}
         del q, kc, vc, bt, o, lse, ws
+    return out
+
+
+# Low-precision forward: e4m3 inputs (per-128-row scales of Q and K, per-head scale of
+# V), both products on the tensor cores with 8-bit operands.
+FP8_WORKLOADS = [
+    ("B1_H16_N16384_d128_causal", 1, 16, 16384, 128, True),
+    ("B2_H16_N4096_d128_causal", 2, 16, 4096, 128, True),
+    ("B4_H8_N8192_d128_noncausal", 4, 8, 8192, 128, False),
+]
+# nominal dense e4m3 / bf16 tensor rates of the part (4.5 / 2.25 PFLOP/s)
+FP8_OVER_BF16 = 2.0
+
+
+def sweep_fp8(fa, torch, dev, flush, peaks):
+    """fa_fwd_fp8 against the fp8 tensor peak (the measured bf16 GEMM rate times the
+    nominal e4m3/bf16 ratio), and the quantiser against the HBM copy rate."""
+    from exact_attention_26_gb300.inputs import normal_qkv
+    out = {}
+    peak8 = peaks["bf16_tflops"] * FP8_OVER_BF16
+    for name, B, H, N, d, causal in FP8_WORKLOADS:
+        q, k, v = (t.to(dev) for t in normal_qkv(B, H, N, d, seed=0))
+        qc, qd = fa.quantize_fp8(q, 128)
+        kc, kd = fa.quantize_fp8(k, 128)
+        vc, vd = fa.quantize_fp8(v, 0, transpose=True)
+        o = torch.empty_like(q)
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+        ms = _time_call(torch, dev, lambda: fa.forward_fp8(qc, kc, vc, qd, kd, vd, causal=causal,
+                                                           out=o, lse=lse), flush)
+        tf = fwd_flops(B, H, N, d, causal) / (ms * 1e-3) / 1e12
+        # quantiser: algorithmic bytes = read x (bf16) once + write the codes
+        ws = torch.empty(max(fa.fa_quantize_fp8_workspace_bytes(B * H, N, d), 16),
+                         dtype=torch.uint8, device=dev)
+        qms = _time_call(torch, dev, lambda: fa.quantize_fp8(q, 128, workspace=ws), flush)
+        gbs = (q.numel() * 3) / (qms * 1e-3) / 1e9
+        out[name] = {"ms": round(ms, 5), "tflops": round(tf, 2),
+                     "roofline": {"bound": "tensor", "achieved": round(tf, 2), "peak": peak8,
+                                  "unit": "TFLOP/s", "frac": round(tf / peak8, 4),
+                                  "peak_source": "measured bf16 GEMM x nominal e4m3/bf16 ratio 2"},
+                     "quantize_ms": round(qms, 5), "quantize_GB/s": round(gbs, 1),
+                     "quantize_frac_of_hbm": round(gbs / peaks["hbm_gbs"], 4)}
+        del q, k, v, qc, kc, vc, qd, kd, vd, o, lse, ws
     return out
 
 

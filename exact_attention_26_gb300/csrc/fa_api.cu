@@ -94,7 +94,25 @@ int make_thd_map(CUtensorMap *map, const void *ptr, int T, int heads, int d, int
     return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
 }
 
+// 3-D map over bytes (e4m3 codes): dims x (innermost), y, z with the given row and
+// plane pitches (multiples of 16 bytes); boxes of box_x (128: one swizzle span) by
+// box_y by 1; elements past the dims read as zeros.
+int make_u8_map(CUtensorMap *map, const void *ptr, uint64_t nx, uint64_t ny, uint64_t nz,
+                uint64_t pitch_y, uint64_t pitch_z, uint32_t box_x, uint32_t box_y) {
+    auto enc = encode_tiled();
+    if (!enc) return FA_ERR_CUDA;
+    cuuint64_t dims[3] = {(cuuint64_t)nx, (cuuint64_t)ny, (cuuint64_t)nz};
+    cuuint64_t strides[2] = {(cuuint64_t)pitch_y, (cuuint64_t)pitch_z};
+    cuuint32_t box[3] = {box_x, box_y, 1};
+    cuuint32_t elem_strides[3] = {1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(ptr), dims, strides,
+                     box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
+}
+
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
 int check_sizes(int B, int H, int N, int d, bool fwd) {
     if (B < 1 || H < 1 || N < 1) return FA_ERR_INVALID_ARG;
@@ -182,6 +200,87 @@ extern "C" int fa_fwd_gqa(const void *q, const void *k, const void *v, void *o, 
     p.limit_ns = kWaitLimitNs;
     p.num_sms = dc->num_sms;
     return launch_fwd(p, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int fa_fwd_fp8(const void *q8, const void *k8, const void *vt8, const float *q_descale,
+                          const float *k_descale, const float *v_descale, void *o, float *lse,
+                          int B, int H, int Hkv, int N, int d, int causal, float scale,
+                          void *stream) {
+    if (!q8 || !k8 || !vt8 || !q_descale || !k_descale || !v_descale || !o || !lse)
+        return FA_ERR_INVALID_ARG;
+    if (B < 1 || H < 1 || N < 1) return FA_ERR_INVALID_ARG;
+    if ((long long)B * H * N >= (1LL << 31)) return FA_ERR_INVALID_ARG;
+    if (d != 128) return FA_ERR_UNSUPPORTED;
+    const int group = gqa_group(H, Hkv);
+    if (group == 0) return FA_ERR_INVALID_ARG;
+    int rc = check_scale(scale);
+    if (rc != FA_OK) return rc;
+    if (!aligned16(q8) || !aligned16(k8) || !aligned16(vt8) || !aligned16(o) || !aligned16(lse) ||
+        !aligned4(q_descale) || !aligned4(k_descale) || !aligned4(v_descale))
+        return FA_ERR_MISALIGNED;
+    DeviceCache *dc = nullptr;
+    if ((rc = current_device(&dc)) != FA_OK) return rc;
+    FwdParams p{};
+    const int BH = B * H, BHkv = B * Hkv;
+    const uint64_t np = ((uint64_t)N + 15) / 16 * 16;
+    const uint64_t row = (uint64_t)d;  // bytes per row of q8 / k8
+    if ((rc = make_u8_map(&p.tm_q, q8, d, N, BH, row, row * N, 128, 128)) != FA_OK) return rc;
+    if ((rc = make_u8_map(&p.tm_k, k8, d, N, BHkv, row, row * N, 128, 128)) != FA_OK) return rc;
+    if ((rc = make_u8_map(&p.tm_v, vt8, np, d, BHkv, np, np * d, 128, (uint32_t)d)) != FA_OK)
+        return rc;
+    p.o = o;
+    p.lse = lse;
+    p.N = N;
+    p.BH = BH;
+    p.H = H;
+    p.group = group;
+    p.d = d;
+    p.causal = causal ? 1 : 0;
+    p.scale_log2 = scale * kLog2e;
+    p.fp8 = 1;
+    p.q_descale = q_descale;
+    p.k_descale = k_descale;
+    p.v_descale = v_descale;
+    p.status = dc->status;
+    p.limit_ns = kWaitLimitNs;
+    p.num_sms = dc->num_sms;
+    return launch_fwd(p, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" size_t fa_quantize_fp8_workspace_bytes(int BH, int N, int d) {
+    if (BH < 1 || N < 1 || (d != 64 && d != 128 && d != 256)) return 0;
+    const size_t chunks = ((size_t)N + 127) / 128;
+    return ((size_t)BH * chunks * sizeof(float) + 15) / 16 * 16;
+}
+
+extern "C" int fa_quantize_fp8(const void *x, void *codes, float *descale, int BH, int N, int d,
+                               int block_rows, const float *signs, int transpose, void *workspace,
+                               size_t workspace_bytes, void *stream) {
+    if (!x || !codes || !descale) return FA_ERR_INVALID_ARG;
+    if (BH < 1 || N < 1 || (long long)BH * N >= (1LL << 31)) return FA_ERR_INVALID_ARG;
+    if (d != 64 && d != 128 && d != 256) return FA_ERR_UNSUPPORTED;
+    if (block_rows < 0 || block_rows % 128 != 0) return FA_ERR_INVALID_ARG;
+    const size_t need = fa_quantize_fp8_workspace_bytes(BH, N, d);
+    if (!workspace || workspace_bytes < need) return FA_ERR_WORKSPACE;
+    if (!aligned16(x) || !aligned16(codes) || !aligned4(descale) || !aligned16(workspace) ||
+        (signs && !aligned16(signs)))
+        return FA_ERR_MISALIGNED;
+    DeviceCache *dc = nullptr;
+    int rc = current_device(&dc);
+    if (rc != FA_OK) return rc;
+    QuantParams p{};
+    p.x = x;
+    p.codes = codes;
+    p.descale = descale;
+    p.partial = static_cast<float *>(workspace);
+    p.signs = signs;
+    p.BH = BH;
+    p.N = N;
+    p.d = d;
+    p.block_rows = block_rows;
+    p.transpose = transpose ? 1 : 0;
+    p.Np = (N + 15) / 16 * 16;
+    return launch_quant(p, static_cast<cudaStream_t>(stream));
 }
 
 extern "C" int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B,
@@ -481,8 +580,6 @@ extern "C" int fa_decode(const void *q, const void *k, const void *v, void *o, f
 
 namespace fa {
 namespace {
-
-bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
 // Sizes of a paged decode; the longest possible sequence page_size * max_pages
 // plays the role of Nk for the split.

@@ -44,25 +44,31 @@ namespace {
 constexpr float kRescaleLog2 = 8.0f;
 constexpr float kLn2 = 0.69314718055994530942f;
 
-template <int D>
+// F8: Q, K and V arrive as e4m3 bytes (one scale per 128-row block of Q and of K,
+// one per head of V) and P is rounded to e4m3 for the PV product; V comes
+// transposed ([d][keys]) so that both products read K-major operands.
+template <int D, bool F8 = false>
 struct FwdTile {
+    static constexpr int EB = F8 ? 1 : 2;             // bytes per element
     static constexpr int NT = (D <= 128) ? 2 : 1;     // 128-row query tiles per CTA
     static constexpr int SB = (NT == 1) ? 2 : 1;      // S slots per tile (double buffer)
     static constexpr int NS = NT * SB;                // S slots in TMEM
     static constexpr int BM = 128;
     static constexpr int ROWS = NT * BM;              // query rows per CTA
     static constexpr int BN = (D == 256) ? 64 : 128;  // keys per K/V tile
-    static constexpr int KS = (D == 64) ? 4 : 3;      // K ring stages
-    static constexpr int VS = (D == 64) ? 4 : 2;      // V ring stages
-    // Rows sit in shared memory as 128-byte swizzle chunks of 64 columns; d = 96
-    // takes two chunks, the columns past d zero-filled by the copy and never read
-    // by a product (S runs D/16 K steps, PV has N = D).
-    static constexpr int DP = (D + 63) / 64 * 64;     // row width in shared memory
-    static constexpr int NCH = DP / 64;               // 128-byte swizzle chunks per row
+    static constexpr int KS = (F8 || D == 64) ? 4 : 3;  // K ring stages
+    static constexpr int VS = (F8 || D == 64) ? 4 : 2;  // V ring stages
+    // Rows sit in shared memory as 128-byte swizzle chunks (64 bf16 or 128 e4m3
+    // columns); d = 96 takes two bf16 chunks, the columns past d zero-filled by the
+    // copy and never read by a product (S runs D/16 K steps, PV has N = D).
+    static constexpr int CW = 128 / EB;               // columns per swizzle chunk
+    static constexpr int DP = (D + CW - 1) / CW * CW; // row width in shared memory
+    static constexpr int NCH = DP / CW;               // 128-byte swizzle chunks per row
+    static constexpr int KSTEP = 32 / EB;             // K elements per MMA (32 bytes)
     static constexpr uint32_t Q_CHUNK = BM * 128;
     static constexpr uint32_t KV_CHUNK = BN * 128;
-    static constexpr uint32_t Q_BYTES = BM * DP * 2;  // one query tile
-    static constexpr uint32_t KV_BYTES = BN * DP * 2; // one of K_j, V_j
+    static constexpr uint32_t Q_BYTES = BM * DP * EB;  // one query tile
+    static constexpr uint32_t KV_BYTES = BN * DP * EB; // one of K_j, V_j (F8: V_j^T)
     // tensor memory columns: S slot u at BN u (fp32; P as bf16 over its first BN/2
     // columns), then O_t (fp32, D columns) at BN NS + D t
     static constexpr uint32_t TM_O0 = BN * NS;
@@ -82,6 +88,7 @@ struct FwdTile {
     static constexpr int THREADS = 128 * NT + 64;
 
     static_assert(D == 64 || D == 96 || D == 128 || D == 256, "head dim");
+    static_assert(!F8 || (D == 128 && BN == 128), "e4m3 path: d = 128");
     static_assert(Q_CHUNK % 1024 == 0 && KV_CHUNK % 1024 == 0, "swizzle atoms must stay aligned");
     static_assert(TM_O0 + NT * D <= TM_COLS, "tensor memory budget");
     static_assert(BN % 64 == 0, "P is packed 64 keys per tcgen05.st");
@@ -92,14 +99,21 @@ struct FwdTile {
 // k, v [T][Hkv][d], lse [H][T]; sequence b holds tokens [cu_seqlens[b],
 // cu_seqlens[b+1]).  The tensor maps are then (d, heads, T), so a box of 128 tokens
 // of one head lands in shared memory exactly like a box of the fixed layout.
-template <int D, bool CAUSAL, bool VARLEN>
-__global__ void __launch_bounds__(FwdTile<D>::THREADS, 1)
+//
+// F8: q_descale [BH][nqb] and k_descale [B*Hkv][nqb] hold one scale per 128-row
+// block, v_descale [B*Hkv] one per head (nqb = ceil(N / 128)); S_t(j) is scaled
+// by scale * q_descale(t) * k_descale(j) inside the exponent's FMA and O by
+// v_descale / l in the epilogue.
+template <int D, bool CAUSAL, bool VARLEN, bool F8>
+__global__ void __launch_bounds__(FwdTile<D, F8>::THREADS, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, __nv_bfloat16 *__restrict__ out,
                   float *__restrict__ lse, int N, int BH, int H, int group, int n_cblocks,
                   const int *__restrict__ cu_seqlens, int total_tokens, float scale_log2,
-                  int *status, unsigned long long limit_ns) {
-    using T = FwdTile<D>;
+                  const float *__restrict__ q_descale, const float *__restrict__ k_descale,
+                  const float *__restrict__ v_descale, int nqb, int *status,
+                  unsigned long long limit_ns) {
+    using T = FwdTile<D, F8>;
     constexpr int NT = T::NT;
     constexpr int KS = T::KS;
     constexpr int VS = T::VS;
@@ -238,16 +252,21 @@ __global__ void __launch_bounds__(FwdTile<D>::THREADS, 1)
                 if (w < 0) continue;
                 const Item itm = decode(w);
                 auto load_kv = [&](const CUtensorMap *map, uint32_t ring, uint32_t full, int stage,
-                                   int j) {
+                                   int j, bool is_v) {
                     mbar_arrive_expect_tx(full + 8 * stage, T::KV_BYTES);
+                    if (F8 && is_v) {  // V_j^T: D rows of BN keys, one box
+                        tma_load_3d(ring + stage * T::KV_BYTES, map, full + 8 * stage, j * T::BN, 0,
+                                    itm.kvh);
+                        return;
+                    }
                     for (int c = 0; c < T::NCH; ++c) {
                         if constexpr (VARLEN)
                             tma_load_3d(ring + stage * T::KV_BYTES + c * T::KV_CHUNK, map,
-                                        full + 8 * stage, c * 64, (itm.bh % H) / group,
+                                        full + 8 * stage, c * T::CW, (itm.bh % H) / group,
                                         itm.tok0 + j * T::BN);
                         else
                             tma_load_3d(ring + stage * T::KV_BYTES + c * T::KV_CHUNK, map,
-                                        full + 8 * stage, c * 64, j * T::BN, itm.kvh);
+                                        full + 8 * stage, c * T::CW, j * T::BN, itm.kvh);
                     }
                 };
                 for (int t = 0; ok && t < NT; ++t) {
@@ -260,10 +279,10 @@ __global__ void __launch_bounds__(FwdTile<D>::THREADS, 1)
                         const int row = itm.cb * T::ROWS + t * T::BM;
                         if constexpr (VARLEN)
                             tma_load_3d(sQ + t * T::Q_BYTES + c * T::Q_CHUNK, &tm_q,
-                                        bar_q_full + 8 * t, c * 64, itm.bh % H, itm.tok0 + row);
+                                        bar_q_full + 8 * t, c * T::CW, itm.bh % H, itm.tok0 + row);
                         else
                             tma_load_3d(sQ + t * T::Q_BYTES + c * T::Q_CHUNK, &tm_q,
-                                        bar_q_full + 8 * t, c * 64, row, itm.bh);
+                                        bar_q_full + 8 * t, c * T::CW, row, itm.bh);
                     }
                     ++q_issued[t];
                 }
@@ -273,7 +292,7 @@ __global__ void __launch_bounds__(FwdTile<D>::THREADS, 1)
                         if (gk >= KS && !(ok = mbar_wait(bar_k_empty + 8 * ks, ((gk / KS) - 1) & 1, g,
                                                          SITE_FWD_LOAD_KV_EMPTY)))
                             break;
-                        load_kv(&tm_k, sK, bar_k_full, ks, i);
+                        load_kv(&tm_k, sK, bar_k_full, ks, i, false);
                         ++k_issued;
                     }
                     if (i >= 1) {
@@ -281,7 +300,7 @@ __global__ void __launch_bounds__(FwdTile<D>::THREADS, 1)
                         if (gv >= VS && !(ok = mbar_wait(bar_v_empty + 8 * vs, ((gv / VS) - 1) & 1, g,
                                                          SITE_FWD_LOAD_KV_EMPTY)))
                             break;
-                        load_kv(&tm_v, sV, bar_v_full, vs, i - 1);
+                        load_kv(&tm_v, sV, bar_v_full, vs, i - 1, true);
                         ++v_issued;
                     }
                 }
@@ -303,29 +322,43 @@ __global__ void __launch_bounds__(FwdTile<D>::THREADS, 1)
         // ------------------------------------------------------- MMA issuer
         // The whole warp runs this loop (warp-uniform); one elected lane issues.
         {
-            constexpr uint32_t kIdescS = idesc_bf16_f32(128, T::BN, false, false);
-            constexpr uint32_t kIdescO = idesc_bf16_f32(128, D, false, true);
+            constexpr uint32_t kIdescS =
+                F8 ? idesc_e4m3_f32(128, T::BN) : idesc_bf16_f32(128, T::BN, false, false);
+            constexpr uint32_t kIdescO = F8 ? idesc_e4m3_f32(128, D) : idesc_bf16_f32(128, D, false, true);
             // S slot u = Q_t K_j^T from K stage ks: M = 128, N = BN, K = D.
             auto issue_s = [&](int t, int u, int ks_stage) {
                 const uint64_t dq = sdesc_sw128(sQ + t * T::Q_BYTES, 16, 1024);
                 const uint64_t dk = sdesc_sw128(sK + ks_stage * T::KV_BYTES, 16, 1024);
 #pragma unroll
-                for (int ks = 0; ks < D / 16; ++ks) {
-                    const uint32_t koff = (ks & 3) * 32;  // 16 bf16 = 32 bytes per K step
+                for (int ks = 0; ks < D / T::KSTEP; ++ks) {
+                    const uint32_t koff = (ks & 3) * 32;  // 32 bytes of K per step
                     const uint64_t a = desc_add(dq, (ks >> 2) * T::Q_CHUNK + koff);
                     const uint64_t b = desc_add(dk, (ks >> 2) * T::KV_CHUNK + koff);
-                    mma_ss_elect(tmem + T::BN * u, a, b, kIdescS, ks > 0 ? 1u : 0u);
+                    if constexpr (F8)
+                        mma_ss_elect_f8(tmem + T::BN * u, a, b, kIdescS, ks > 0 ? 1u : 0u);
+                    else
+                        mma_ss_elect(tmem + T::BN * u, a, b, kIdescS, ks > 0 ? 1u : 0u);
                 }
                 tc_commit_elect(bar_s_full + 8 * u);
             };
-            // O_t += P V from S slot u and V stage vs: M = 128, N = D, K = BN.
+            // O_t += P V from S slot u and V stage vs: M = 128, N = D, K = BN.  P sits
+            // in TMEM as 32-bit columns of 2 bf16 or 4 e4m3 keys: 8 columns per step.
             auto issue_pv = [&](int t, int u, int vs, bool first) {
-                const uint64_t dv = sdesc_sw128(sV + vs * T::KV_BYTES, T::KV_CHUNK, 1024);
+                if constexpr (F8) {
+                    // V_j^T is K-major: D rows of BN key bytes
+                    const uint64_t dv = sdesc_sw128(sV + vs * T::KV_BYTES, 16, 1024);
 #pragma unroll
-                for (int ks = 0; ks < T::BN / 16; ++ks) {
-                    const uint64_t b = desc_add(dv, ks * 2048);
-                    mma_ts_elect(tmem + T::TM_O0 + D * t, tmem + T::BN * u + ks * 8, b, kIdescO,
-                           (!first || ks > 0) ? 1u : 0u);
+                    for (int ks = 0; ks < T::BN / 32; ++ks)
+                        mma_ts_elect_f8(tmem + T::TM_O0 + D * t, tmem + T::BN * u + ks * 8,
+                                        desc_add(dv, ks * 32), kIdescO, (!first || ks > 0) ? 1u : 0u);
+                } else {
+                    const uint64_t dv = sdesc_sw128(sV + vs * T::KV_BYTES, T::KV_CHUNK, 1024);
+#pragma unroll
+                    for (int ks = 0; ks < T::BN / 16; ++ks) {
+                        const uint64_t b = desc_add(dv, ks * 2048);
+                        mma_ts_elect(tmem + T::TM_O0 + D * t, tmem + T::BN * u + ks * 8, b, kIdescO,
+                                     (!first || ks > 0) ? 1u : 0u);
+                    }
                 }
             };
             auto wait_k = [&](int j) {
@@ -468,11 +501,16 @@ __global__ void __launch_bounds__(FwdTile<D>::THREADS, 1)
             const int q_idx = row0 + r;
             float m_ref = -INFINITY;  // reference max, base-2 scaled units
             float l = 0.f;
+            // score -> base-2 exponent factor (F8: times the block scales of Q_t, K_j)
+            float c_q = scale_log2;
+            if constexpr (F8) c_q *= q_descale[(size_t)itm.bh * nqb + row0 / T::BM];
             for (int j = 0; j < n_it; ++j) {
                 const int gsj = sc + j;                                     // running S index
                 const int u = (T::SB == 1) ? t : (gsj & 1);                 // S slot
                 const uint32_t par = (T::SB == 1) ? (gsj & 1) : ((gsj >> 1) & 1);
                 const uint32_t t_s = tmem + lane_base + T::BN * u;
+                float c_s = c_q;
+                if constexpr (F8) c_s *= __ldg(k_descale + (size_t)itm.kvh * nqb + j);
                 ok = mbar_wait_warp(bar_s_full + 8 * u, par, g, SITE_FWD_SOFTMAX_S_FULL);
                 if (!ok) break;
                 tc_fence_after();
@@ -508,7 +546,7 @@ __global__ void __launch_bounds__(FwdTile<D>::THREADS, 1)
 #pragma unroll
                 for (int a = 1; a < NACC; ++a) mp[0] = fmaxf(mp[0], mp[a]);
                 const float mx = mp[0];
-                const float m_tile = mx * scale_log2;
+                const float m_tile = mx * c_s;
                 float alpha = 1.f;
                 const bool move = m_tile > m_ref + kRescaleLog2;
                 if (move) {
@@ -521,19 +559,30 @@ __global__ void __launch_bounds__(FwdTile<D>::THREADS, 1)
                 for (int a = 0; a < NACC; ++a) sp[a] = 0.f;
 #pragma unroll
                 for (int c = 0; c < T::BN; ++c) {
-                    s[c] = ex2(fmaf(s[c], scale_log2, neg_m));
+                    s[c] = ex2(fmaf(s[c], c_s, neg_m));
                     sp[c % NACC] += s[c];
                 }
 #pragma unroll
                 for (int a = 1; a < NACC; ++a) sp[0] += sp[a];
                 l = l * alpha + sp[0];
-                // P as bf16 pairs into the first BN/2 columns of the S slot.
-#pragma unroll
-                for (int c = 0; c < T::BN / 64; ++c) {
+                if constexpr (F8) {
+                    // P as e4m3 quadruples into the first BN/4 columns of the S slot
+                    // (P <= 2^8 with the reference max, inside e4m3's range)
                     uint32_t pk[32];
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) pk[e] = pack_bf16(s[c * 64 + 2 * e], s[c * 64 + 2 * e + 1]);
-                    tmem_st32(t_s + c * 32, pk);
+                    for (int e = 0; e < 32; ++e)
+                        pk[e] = pack_e4m3x4(s[4 * e], s[4 * e + 1], s[4 * e + 2], s[4 * e + 3]);
+                    tmem_st32(t_s, pk);
+                } else {
+                    // P as bf16 pairs into the first BN/2 columns of the S slot.
+#pragma unroll
+                    for (int c = 0; c < T::BN / 64; ++c) {
+                        uint32_t pk[32];
+#pragma unroll
+                        for (int e = 0; e < 32; ++e)
+                            pk[e] = pack_bf16(s[c * 64 + 2 * e], s[c * 64 + 2 * e + 1]);
+                        tmem_st32(t_s + c * 32, pk);
+                    }
                 }
                 if (j > 0 && __any_sync(0xffffffffu, move)) {
                     // O_t <- alpha O_t for this warp's 32 rows (alpha = 1 on rows that kept
@@ -565,7 +614,7 @@ __global__ void __launch_bounds__(FwdTile<D>::THREADS, 1)
             ok = ok && mbar_wait_warp(bar_o_full + 8 * t, oc & 1, g, SITE_FWD_EPILOGUE_O_FULL);
             if (!ok) break;
             tc_fence_after();
-            const float inv_l = 1.f / l;
+            const float inv_l = (F8 ? v_descale[itm.kvh] : 1.f) / l;
             __nv_bfloat16 *orow =
                 VARLEN ? out + ((size_t)(itm.tok0 + q_idx) * H + (itm.bh % H)) * D
                        : out + ((size_t)itm.bh * (size_t)N + (size_t)q_idx) * D;
@@ -610,10 +659,10 @@ __global__ void __launch_bounds__(FwdTile<D>::THREADS, 1)
     }
 }
 
-template <int D, bool CAUSAL, bool VARLEN>
+template <int D, bool CAUSAL, bool VARLEN, bool F8 = false>
 int launch_fwd_t(const FwdParams &p, cudaStream_t stream) {
-    using T = FwdTile<D>;
-    auto kern = fa_fwd_kernel<D, CAUSAL, VARLEN>;
+    using T = FwdTile<D, F8>;
+    auto kern = fa_fwd_kernel<D, CAUSAL, VARLEN, F8>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)T::SMEM_BYTES);
     if (e != cudaSuccess) return FA_ERR_CUDA;
@@ -625,7 +674,8 @@ int launch_fwd_t(const FwdParams &p, cudaStream_t stream) {
     const long long grid = items < p.num_sms ? items : p.num_sms;
     kern<<<(unsigned)grid, T::THREADS, T::SMEM_BYTES, stream>>>(
         p.tm_q, p.tm_k, p.tm_v, reinterpret_cast<__nv_bfloat16 *>(p.o), p.lse, p.N, p.BH, p.H,
-        p.group, n_cblocks, p.cu_seqlens, p.total_tokens, p.scale_log2, p.status, p.limit_ns);
+        p.group, n_cblocks, p.cu_seqlens, p.total_tokens, p.scale_log2, p.q_descale, p.k_descale,
+        p.v_descale, (p.N + 127) / 128, p.status, p.limit_ns);
     return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
@@ -639,6 +689,11 @@ int launch_fwd_d(const FwdParams &p, cudaStream_t stream) {
 }
 
 int launch_fwd(const FwdParams &p, cudaStream_t stream) {
+    if (p.fp8) {
+        if (p.d != 128 || p.cu_seqlens) return FA_ERR_UNSUPPORTED;
+        return p.causal ? launch_fwd_t<128, true, false, true>(p, stream)
+                        : launch_fwd_t<128, false, false, true>(p, stream);
+    }
     switch (p.d) {
         case 64: return launch_fwd_d<64>(p, stream);
         case 96: return launch_fwd_d<96>(p, stream);

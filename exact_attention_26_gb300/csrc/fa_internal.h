@@ -51,10 +51,24 @@ struct FwdParams {
     const int *cu_seqlens;         // varlen: [B+1] sequence starts (token-major layout), else null
     int total_tokens;              // varlen: T
     float scale_log2;              // scale * log2(e)
+    int fp8;                       // e4m3 inputs: tm_q/tm_k over bytes, tm_v over V^T [B*Hkv][d][Np]
+    const float *q_descale, *k_descale, *v_descale;  // fp8: [BH][nqb], [B*Hkv][nqb], [B*Hkv]
     int *status;                   // device status record (2 ints)
     unsigned long long limit_ns;
     int num_sms;
 };
+
+// e4m3 block quantiser: x bf16 [BH][N][d] -> codes [BH][N][d] (or [BH][d][Np]).
+struct QuantParams {
+    const void *x;
+    void *codes;
+    float *descale;        // [BH][n_groups]
+    float *partial;        // workspace: per 128-row chunk maxima, [BH][n_chunks]
+    const float *signs;    // incoherent processing: d signs (+-1), or null
+    int BH, N, d, block_rows, transpose, Np;
+};
+
+int launch_quant(const QuantParams &p, cudaStream_t stream);
 
 struct BwdParams {
     CUtensorMap tm_q, tm_k, tm_v, tm_do;  // 3-D maps over [BH][N][d] (q, do), [B*Hkv][N][d] (k, v)

@@ -27,7 +27,7 @@ EXPORTED = ("fa_fwd", "fa_bwd", "fa_bwd_workspace_bytes", "fa_status_string", "f
             "fa_selftest_wait_timeout", "fa_decode", "fa_decode_num_splits",
             "fa_decode_workspace_bytes", "fa_decode_paged", "fa_decode_paged_num_splits",
             "fa_decode_paged_workspace_bytes", "fa_fwd_gqa", "fa_bwd_gqa", "fa_fwd_varlen",
-            "fa_bwd_varlen")
+            "fa_bwd_varlen", "fa_quantize_fp8_workspace_bytes", "fa_quantize_fp8", "fa_fwd_fp8")
 
 _vp = ctypes.c_void_p
 _int = ctypes.c_int
@@ -73,6 +73,12 @@ def load() -> ctypes.CDLL:
         lib.fa_bwd_varlen.argtypes = [_vp] * 10 + [_int] * 7 + [ctypes.c_float, _vp, ctypes.c_size_t,
                                                                  _vp]
         lib.fa_bwd_varlen.restype = _int
+        lib.fa_quantize_fp8_workspace_bytes.argtypes = [_int] * 3
+        lib.fa_quantize_fp8_workspace_bytes.restype = ctypes.c_size_t
+        lib.fa_quantize_fp8.argtypes = [_vp] * 3 + [_int] * 4 + [_vp, _int, _vp, ctypes.c_size_t, _vp]
+        lib.fa_quantize_fp8.restype = _int
+        lib.fa_fwd_fp8.argtypes = [_vp] * 8 + [_int] * 6 + [ctypes.c_float, _vp]
+        lib.fa_fwd_fp8.restype = _int
         lib.fa_decode.argtypes = [_vp] * 5 + [_int] * 6 + [ctypes.c_float, _int, _vp,
                                                           ctypes.c_size_t, _vp]
         lib.fa_decode.restype = _int
@@ -148,6 +154,22 @@ def fa_bwd_varlen(q, k, v, o, lse, dout, dq, dk, dv, cu_seqlens, B, H, Hkv, tota
     return load().fa_bwd_varlen(q, k, v, o, lse, dout, dq, dk, dv, cu_seqlens, B, H, Hkv,
                                 total_tokens, max_seqlen, d, int(bool(causal)), scale, workspace,
                                 workspace_bytes, stream)
+
+
+def fa_quantize_fp8_workspace_bytes(BH, N, d) -> int:
+    return load().fa_quantize_fp8_workspace_bytes(BH, N, d)
+
+
+def fa_quantize_fp8(x, codes, descale, BH, N, d, block_rows, signs, transpose, workspace,
+                    workspace_bytes, stream) -> int:
+    return load().fa_quantize_fp8(x, codes, descale, BH, N, d, block_rows, signs,
+                                  int(bool(transpose)), workspace, workspace_bytes, stream)
+
+
+def fa_fwd_fp8(q8, k8, vt8, q_descale, k_descale, v_descale, o, lse, B, H, Hkv, N, d, causal,
+               scale, stream) -> int:
+    return load().fa_fwd_fp8(q8, k8, vt8, q_descale, k_descale, v_descale, o, lse, B, H, Hkv, N,
+                             d, int(bool(causal)), scale, stream)
 
 
 def fa_decode(q, k, v, o, lse, B, H, Hkv, Nq, Nk, d, scale, num_splits, workspace,
@@ -425,3 +447,64 @@ def backward_varlen(q, k, v, o, lse, do, cu_seqlens, max_seqlen, causal=False, s
     if rc != FA_OK:
         raise FaError(rc, "fa_bwd_varlen")
     return tuple(grads)
+
+
+def quantize_fp8(x, block_rows=128, signs=None, transpose=False, workspace=None, stream=None):
+    """e4m3 block quantisation of x bf16 CUDA [..., N, d] (heads flattened).
+    Returns (codes uint8 [..., N, d] or [..., d, Np], descale fp32 [..., n_blocks])."""
+    _check("x", x, torch.bfloat16)
+    if x.dim() < 2:
+        raise ValueError("x must be [..., N, d]")
+    *lead, N, d = x.shape
+    BH = int(math.prod(lead)) if lead else 1
+    Np = (N + 15) // 16 * 16
+    codes = torch.empty((*lead, d, Np) if transpose else x.shape, dtype=torch.uint8, device=x.device)
+    nb = 1 if block_rows == 0 else (N + block_rows - 1) // block_rows
+    descale = torch.empty((*lead, nb), dtype=torch.float32, device=x.device)
+    if signs is not None:
+        _check("signs", signs, torch.float32, (d,))
+    need = fa_quantize_fp8_workspace_bytes(BH, N, d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=x.device)
+    _check("workspace", workspace, torch.uint8)
+    with torch.cuda.device(x.device):
+        rc = fa_quantize_fp8(x.data_ptr(), codes.data_ptr(), descale.data_ptr(), BH, N, d,
+                             int(block_rows), None if signs is None else signs.data_ptr(),
+                             transpose, workspace.data_ptr(), workspace.numel(), _stream(x, stream))
+    if rc != FA_OK:
+        raise FaError(rc, "fa_quantize_fp8")
+    return codes, descale
+
+
+def forward_fp8(q8, k8, vt8, q_descale, k_descale, v_descale, causal=False, scale=None, out=None,
+                lse=None, stream=None):
+    """Attention on e4m3 inputs: q8 uint8 CUDA [B,H,N,d], k8 [B,Hkv,N,d], vt8 [B,Hkv,d,Np],
+    q/k descales [B,H|Hkv,ceil(N/128)], v descale [B,Hkv,1].  Returns (o bf16, lse fp32)."""
+    _check("q8", q8, torch.uint8)
+    if q8.dim() != 4:
+        raise ValueError("q8 must be [B, H, N, d]")
+    B, H, N, d = q8.shape
+    _check("k8", k8, torch.uint8)
+    if k8.dim() != 4 or k8.shape[0] != B or k8.shape[2] != N or k8.shape[3] != d or H % k8.shape[1]:
+        raise ValueError("k8 must be [B, Hkv, N, d] with Hkv dividing H")
+    Hkv = k8.shape[1]
+    Np = (N + 15) // 16 * 16
+    _check("vt8", vt8, torch.uint8, (B, Hkv, d, Np))
+    nb = (N + 127) // 128
+    _check("q_descale", q_descale, torch.float32, (B, H, nb))
+    _check("k_descale", k_descale, torch.float32, (B, Hkv, nb))
+    _check("v_descale", v_descale, torch.float32, (B, Hkv, 1))
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    if out is None:
+        out = torch.empty((B, H, N, d), dtype=torch.bfloat16, device=q8.device)
+    _check("out", out, torch.bfloat16, (B, H, N, d))
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q8.device)
+    _check("lse", lse, torch.float32, (B, H, N))
+    with torch.cuda.device(q8.device):
+        rc = fa_fwd_fp8(q8.data_ptr(), k8.data_ptr(), vt8.data_ptr(), q_descale.data_ptr(),
+                        k_descale.data_ptr(), v_descale.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                        B, H, Hkv, N, d, causal, scale, _stream(q8, stream))
+    if rc != FA_OK:
+        raise FaError(rc, "fa_fwd_fp8")
+    return out, lse

@@ -32,6 +32,12 @@ Recipes (one per workload of the measurement plan):
   k, v [T, Hkv, d] (T = sum of the lengths), i.i.d. N(0, 1) drawn in the order q,
   k, v from one CPU generator seeded with ``seed``, rounded to bf16; plus
   cu_seqlens, the int32 prefix sums [0, l0, l0 + l1, ...].
+* ``outlier_qkv``: q [B, H, N, d], k, v [B, Hkv, N, d], i.i.d. N(0, 1) drawn in the
+  order q, k, v from one generator seeded with ``seed``; with ``n_outliers`` > 0,
+  a second generator (``seed + 1``) draws that many columns by ``torch.randperm``
+  and those columns of q and k are multiplied by ``outlier_mult`` before the bf16
+  rounding (outlier channels, the case incoherent processing is for).
+* ``hadamard_signs``: d values +-1 from ``torch.randint`` (seed ``seed``), fp32.
 * ``paged_cache``: rearranges a contiguous cache k, v [B, H, Nk, d] (Nk a multiple
   of ``page_size``) into pages [num_pages, H, page_size, d]: logical page p of
   sequence b goes to physical page perm[b * Nk / page_size + p], where perm is
@@ -45,8 +51,8 @@ from __future__ import annotations
 
 import torch
 
-__all__ = ["normal_qkv", "boosted_qkv", "decode_qkv", "gqa_qkv", "varlen_qkv", "paged_cache",
-           "sample_rows", "to_f64"]
+__all__ = ["normal_qkv", "boosted_qkv", "decode_qkv", "gqa_qkv", "varlen_qkv", "outlier_qkv",
+           "hadamard_signs", "paged_cache", "sample_rows", "to_f64"]
 
 
 def _draw(gen: torch.Generator, shape, mult: float = 1.0) -> torch.Tensor:
@@ -129,6 +135,33 @@ def gqa_qkv(B: int, H: int, Hkv: int, N: int, d: int, seed: int = 0, with_do: bo
     if with_do:
         return q, k, v, _draw(gen, (B, H, N, d))
     return q, k, v
+
+
+def outlier_qkv(B: int, H: int, Hkv: int, N: int, d: int, seed: int = 0, n_outliers: int = 0,
+                outlier_mult: float = 20.0):
+    """Return (q [B,H,N,d], k, v [B,Hkv,N,d]) bf16, N(0,1) drawn q, k, v from one
+    generator; with n_outliers > 0 a second generator (seed + 1) picks that many
+    head-dimension columns, and those columns of q and k are multiplied by
+    outlier_mult (before rounding to bf16)."""
+    gen = torch.Generator(device="cpu")
+    gen.manual_seed(seed)
+    q = torch.randn((B, H, N, d), generator=gen, dtype=torch.float32)
+    k = torch.randn((B, Hkv, N, d), generator=gen, dtype=torch.float32)
+    v = torch.randn((B, Hkv, N, d), generator=gen, dtype=torch.float32)
+    if n_outliers > 0:
+        g2 = torch.Generator(device="cpu")
+        g2.manual_seed(seed + 1)
+        cols = torch.randperm(d, generator=g2)[:n_outliers]
+        q[..., cols] *= outlier_mult
+        k[..., cols] *= outlier_mult
+    return tuple(t.to(torch.bfloat16).contiguous() for t in (q, k, v))
+
+
+def hadamard_signs(d: int, seed: int = 0) -> torch.Tensor:
+    """fp32 [d] of +-1 drawn uniformly (the random signs of incoherent processing)."""
+    gen = torch.Generator(device="cpu")
+    gen.manual_seed(seed)
+    return (torch.randint(0, 2, (d,), generator=gen) * 2 - 1).to(torch.float32)
 
 
 def varlen_qkv(lens, H: int, Hkv: int, d: int, seed: int = 0):

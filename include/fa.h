@@ -144,6 +144,53 @@ int fa_bwd_noalloc(const void *q, const void *k, const void *v, const void *o,
                    int H, int N, int d, int causal, float scale, void *stream);
 
 /*
+ * e4m3 block quantisation for the low-precision forward ("FlashAttention: Move
+ * Less, Not Compute Less", section "FA1 to FA3: Optimization Moves Closer to the
+ * Hardware": FP8 with block quantisation and incoherent processing).  The pages
+ * name the technique only; this library's reading:
+ *   x           : bf16 [BH][N][d], d in {64, 128, 256}.
+ *   block_rows  : rows per scale block, 0 (one block per head) or a multiple of 128.
+ *   signs       : NULL, or fp32 [d] of +-1 (16-byte aligned, device memory): each
+ *                 row is first multiplied by diag(signs) H / sqrt(d), H the
+ *                 Sylvester-Hadamard matrix ("incoherent processing"; an orthogonal
+ *                 map, so Q K^T is unchanged when Q and K take the same signs).
+ *   codes       : uint8 e4m3 [BH][N][d], or with transpose != 0 [BH][d][Np] with
+ *                 Np = N rounded up to 16 and columns N..Np-1 zero (the value layout
+ *                 fa_fwd_fp8 reads).
+ *   descale     : fp32 [BH][n_blocks] out (n_blocks = ceil(N / block_rows), or 1).
+ * Per block, in IEEE fp32: amax = max |x|, inv = 448 / amax, code = e4m3(x * inv)
+ * rounded to nearest even with finite overflow saturated to +-448, descale =
+ * amax / 448 (an all-zero block: inv = descale = 1).  The dequantised value of a
+ * code is value(code) * descale.
+ *   workspace   : fa_quantize_fp8_workspace_bytes(BH, N, d) bytes, 16-byte aligned.
+ * Returns FA_OK or an fa_status code; nothing is launched on an error.
+ */
+size_t fa_quantize_fp8_workspace_bytes(int BH, int N, int d);
+int fa_quantize_fp8(const void *x, void *codes, float *descale, int BH, int N, int d,
+                    int block_rows, const float *signs, int transpose, void *workspace,
+                    size_t workspace_bytes, void *stream);
+
+/*
+ * Low-precision forward: attention on e4m3 inputs with fp32 accumulation.  Both
+ * products run on the tensor cores with 8-bit operands: S = Q K^T from the codes,
+ * scaled by scale * q_descale * k_descale of the two row blocks, and O += P V with P
+ * rounded to e4m3 (P <= 2^8 relative to the running reference maximum); the row
+ * sum l is taken from P before rounding, so L is that of the dequantised inputs.
+ *   q8        : e4m3 [B][H][N][d];  k8 : e4m3 [B][Hkv][N][d]  (d = 128).
+ *   vt8       : e4m3 [B][Hkv][d][Np], V transposed per head, Np = N rounded up to 16
+ *               (fa_quantize_fp8 with transpose = 1 writes it).
+ *   q_descale : fp32 [B*H][ceil(N/128)];  k_descale : fp32 [B*Hkv][ceil(N/128)]
+ *               (block_rows = 128);  v_descale : fp32 [B*Hkv] (block_rows = 0).
+ *   o, lse    : bf16 [B][H][N][d] and fp32 [B][H][N] out, as in fa_fwd.
+ * The result equals fa_fwd's definition applied to the dequantised q, k, v up to
+ * the rounding of P to e4m3 (relative 2^-4 per element, absolute 2^-10 below 2^-6).
+ * Other arguments as in fa_fwd_gqa.
+ */
+int fa_fwd_fp8(const void *q8, const void *k8, const void *vt8, const float *q_descale,
+               const float *k_descale, const float *v_descale, void *o, float *lse, int B, int H,
+               int Hkv, int N, int d, int causal, float scale, void *stream);
+
+/*
  * Forward pass over packed sequences of different lengths (variable-length
  * batches: course page "10 FlashAttention", section "8-9. Production and
  * mistakes", counts padding sequences instead of packing them among the mistakes).  Sequence

@@ -191,3 +191,35 @@ def test_varlen_backward_rejects_bad_arguments(fa, kw, code):
     assert fa.fa.fa_bwd_varlen(DUMMY, DUMMY, DUMMY, DUMMY, DUMMY, DUMMY, a["dq"], DUMMY, DUMMY, a["cu"], 2, 4,
                                a["Hkv"], a["T"], a["maxlen"], a["d"], 1, 0.1, a["ws"], a["ws_bytes"],
                                None) == code
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(x=None), 1), (dict(codes=None), 1), (dict(BH=0), 1), (dict(N=0), 1), (dict(d=96), 2),
+    (dict(block_rows=100), 1), (dict(block_rows=-128), 1), (dict(ws=None), 6), (dict(ws_bytes=8), 6),
+    (dict(x=DUMMY + 8), 3), (dict(signs=DUMMY + 4), 3), (dict(descale=DUMMY + 2), 3),
+])
+def test_quantize_fp8_rejects_bad_arguments(fa, kw, code):
+    a = dict(x=DUMMY, codes=DUMMY, descale=DUMMY, BH=2, N=300, d=128, block_rows=128, signs=None,
+             ws=DUMMY, ws_bytes=1 << 20)
+    a.update(kw)
+    assert fa.fa_quantize_fp8(a["x"], a["codes"], a["descale"], a["BH"], a["N"], a["d"], a["block_rows"],
+                              a["signs"], 0, a["ws"], a["ws_bytes"], None) == code
+
+
+def test_quantize_fp8_workspace_size(fa):
+    assert fa.fa_quantize_fp8_workspace_bytes(2, 300, 128) == 32  # 2 heads x 3 chunks x 4 B, to 16
+    assert fa.fa_quantize_fp8_workspace_bytes(1, 128, 64) == 16
+    assert fa.fa_quantize_fp8_workspace_bytes(1, 128, 96) == 0
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q8=None), 1), (dict(vd=None), 1), (dict(N=0), 1), (dict(d=64), 2), (dict(d=256), 2),
+    (dict(Hkv=3), 1), (dict(scale=0.0), 1), (dict(q8=DUMMY + 8), 3), (dict(vt8=DUMMY + 4), 3),
+    (dict(qd=DUMMY + 2), 3), (dict(lse=DUMMY + 4), 3),
+])
+def test_fwd_fp8_rejects_bad_arguments(fa, kw, code):
+    a = dict(q8=DUMMY, k8=DUMMY, vt8=DUMMY, qd=DUMMY, kd=DUMMY, vd=DUMMY, o=DUMMY, lse=DUMMY, B=1,
+             H=4, Hkv=2, N=256, d=128, scale=0.1)
+    a.update(kw)
+    assert fa.fa_fwd_fp8(a["q8"], a["k8"], a["vt8"], a["qd"], a["kd"], a["vd"], a["o"], a["lse"], a["B"],
+                         a["H"], a["Hkv"], a["N"], a["d"], 1, a["scale"], None) == code
