@@ -63,6 +63,7 @@ DEC_WORKLOADS = [
     ("B1_H32_Nq1_Nk32768_d128", 1, 32, 1, 32768, 128),
     ("B8_H32_Nq1_Nk32768_d64", 8, 32, 1, 32768, 64),
     ("B4_H16_Nq1_Nk32768_d256", 4, 16, 1, 32768, 256),
+    ("B8_H32_Nq1_Nk32768_d96", 8, 32, 1, 32768, 96),
 ]
 
 

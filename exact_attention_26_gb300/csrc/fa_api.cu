@@ -458,7 +458,7 @@ int check_decode_sizes(int B, int H, int Hkv, int Nq, int Nk, int d) {
     if ((long long)(H / Hkv) * Nq > 65535) return FA_ERR_INVALID_ARG;
     if ((long long)B * H * Nq >= (1LL << 31) || (long long)B * Hkv * Nk >= (1LL << 31))
         return FA_ERR_INVALID_ARG;
-    if (d != 64 && d != 128 && d != 256) return FA_ERR_UNSUPPORTED;
+    if (d != 64 && d != 96 && d != 128 && d != 256) return FA_ERR_UNSUPPORTED;
     return FA_OK;
 }
 

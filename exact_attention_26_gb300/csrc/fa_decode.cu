@@ -24,7 +24,11 @@ struct DecTile {
     static constexpr int STAGES = (D == 64) ? 4 : 3;
     static constexpr int NWC = 4;                       // compute warps
     static constexpr int KW = BK / NWC;                 // keys per compute warp per stage
-    static constexpr int E = D / 32;                    // head-dim elements per lane
+    // head-dim elements per lane, and the lanes that hold some (d = 96: 24 lanes of
+    // 4, so every lane's shared-memory reads stay 8-byte vectors; lanes 24-31 hold
+    // zeros and touch no memory)
+    static constexpr int E = (D == 96) ? 4 : D / 32;
+    static constexpr int LANES = D / E;
     static constexpr uint32_t TILE_BYTES = BK * D * 2;  // K (or V) rows of one stage, bf16
     static constexpr uint32_t STAGE_BYTES = 2 * TILE_BYTES;
     static constexpr uint32_t OFF_BAR = STAGES * STAGE_BYTES;
@@ -112,6 +116,7 @@ __global__ void __launch_bounds__(DecTile<D>::THREADS, 2)
     const float scale_log2 = p.scale_log2;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const bool lane_on = T::LANES == 32 || lane < T::LANES;
     // One CTA per (key/value head, key range, block of query rows).  With grouped
     // queries the rows of key/value head kvh are the Nq rows of each of the `group`
     // query heads that read it (row r: head r / Nq of the group, position r % Nq),
@@ -216,7 +221,8 @@ __global__ void __launch_bounds__(DecTile<D>::THREADS, 2)
 #pragma unroll
             for (int e = 0; e < E; ++e) {
                 acc[qi][e] = 0.f;
-                qv[qi][e] = qi < nq ? __bfloat162float(q[qrow(i0 + qi) * D + lane * E + e]) : 0.f;
+                qv[qi][e] = (qi < nq && lane_on) ? __bfloat162float(q[qrow(i0 + qi) * D + lane * E + e])
+                                                 : 0.f;
             }
         }
         const int mykey = (lane >> 2) & 7;  // key of a group of eight that this lane scores
@@ -234,7 +240,12 @@ __global__ void __launch_bounds__(DecTile<D>::THREADS, 2)
 #pragma unroll
                     for (int r = 0; r < 8; ++r) {
                         float kx[E];
-                        lds_bf16<E>(Ks + (size_t)(grp * 8 + r) * D * 2, kx);
+                        if (lane_on) {
+                            lds_bf16<E>(Ks + (size_t)(grp * 8 + r) * D * 2, kx);
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < E; ++e) kx[e] = 0.f;
+                        }
 #pragma unroll
                         for (int qi = 0; qi < QB; ++qi) {
                             float a = 0.f;
@@ -278,7 +289,12 @@ __global__ void __launch_bounds__(DecTile<D>::THREADS, 2)
                 for (int r = 0; r < KW; ++r) {
                     if (r < nvalid) {
                         float vx[E];
-                        lds_bf16<E>(Vs + (size_t)r * D * 2, vx);
+                        if (lane_on) {
+                            lds_bf16<E>(Vs + (size_t)r * D * 2, vx);
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < E; ++e) vx[e] = 0.f;
+                        }
 #pragma unroll
                         for (int qi = 0; qi < QB; ++qi) {
                             const float pr = __shfl_sync(kFull, p[qi][r / 8], (r % 8) << 2);
@@ -303,8 +319,10 @@ __global__ void __launch_bounds__(DecTile<D>::THREADS, 2)
 #pragma unroll
         for (int qi = 0; qi < QB; ++qi) {
             float *rw = red + (warp * QB + qi) * RS;
+            if (lane_on) {
 #pragma unroll
-            for (int e = 0; e < E; ++e) rw[lane * E + e] = acc[qi][e];
+                for (int e = 0; e < E; ++e) rw[lane * E + e] = acc[qi][e];
+            }
             if (lane == 0) {
                 rw[D] = m[qi];
                 rw[D + 1] = l[qi];
@@ -329,8 +347,10 @@ __global__ void __launch_bounds__(DecTile<D>::THREADS, 2)
                 const float f = (mw[w] == -INFINITY) ? 0.f : ex2(mw[w] - M);
                 const float *rw = red + (w * QB + qi) * RS;
                 L = fmaf(rw[D + 1], f, L);
+                if (lane_on) {
 #pragma unroll
-                for (int e = 0; e < E; ++e) out[e] = fmaf(rw[lane * E + e], f, out[e]);
+                    for (int e = 0; e < E; ++e) out[e] = fmaf(rw[lane * E + e], f, out[e]);
+                }
             }
             // an empty key range (a short sequence's tail ranges) contributes
             // L = -inf and O = 0 to the merge
@@ -339,17 +359,21 @@ __global__ void __launch_bounds__(DecTile<D>::THREADS, 2)
             const float l_nat = empty ? -INFINITY : (M + lg2(L)) * kLn2;  // natural-log LSE
             const size_t row = qrow(i0 + qi);
             if (S == 1) {
+                if (lane_on) {
 #pragma unroll
-                for (int e = 0; e < E; e += 2) {
-                    const uint32_t pk = pack_bf16(out[e] * inv, out[e + 1] * inv);
-                    *reinterpret_cast<uint32_t *>(o + row * D + lane * E + e) = pk;
+                    for (int e = 0; e < E; e += 2) {
+                        const uint32_t pk = pack_bf16(out[e] * inv, out[e + 1] * inv);
+                        *reinterpret_cast<uint32_t *>(o + row * D + lane * E + e) = pk;
+                    }
                 }
                 if (lane == 0) lse[row] = l_nat;
             } else {
                 const size_t prow = ((size_t)kvh * S + split) * R + i0 + qi;
-                float *po = part_o + prow * D + lane * E;
+                if (lane_on) {
+                    float *po = part_o + prow * D + lane * E;
 #pragma unroll
-                for (int e = 0; e < E; ++e) po[e] = out[e] * inv;
+                    for (int e = 0; e < E; ++e) po[e] = out[e] * inv;
+                }
                 if (lane == 0) part_l[prow] = l_nat;
             }
         }
@@ -364,10 +388,11 @@ __global__ void __launch_bounds__(128)
     fa_decode_combine_kernel(const float *__restrict__ part_o, const float *__restrict__ part_l,
                              __nv_bfloat16 *__restrict__ o, float *__restrict__ lse, long long rows,
                              int R, int S, int Nq, int H, int Hkv, int group) {
-    constexpr int E = D / 32;
+    constexpr int E = DecTile<D>::E;
     const long long row = (long long)blockIdx.x * 4 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (row >= rows) return;
+    const bool lane_on = DecTile<D>::LANES == 32 || lane < DecTile<D>::LANES;
     const long long kvh = row / R;
     const int r = (int)(row % R);
     const long long b = kvh / Hkv;
@@ -383,15 +408,19 @@ __global__ void __launch_bounds__(128)
     for (int s = 0; s < S; ++s) {
         const float w = __expf(pl[(size_t)s * R] - M);
         W += w;
-        const float *po = part_o + (((size_t)kvh * S + s) * R + r) * D + lane * E;
+        if (lane_on) {
+            const float *po = part_o + (((size_t)kvh * S + s) * R + r) * D + lane * E;
 #pragma unroll
-        for (int e = 0; e < E; ++e) out[e] = fmaf(w, po[e], out[e]);
+            for (int e = 0; e < E; ++e) out[e] = fmaf(w, po[e], out[e]);
+        }
     }
     const float inv = 1.f / W;
+    if (lane_on) {
 #pragma unroll
-    for (int e = 0; e < E; e += 2) {
-        const uint32_t pk = pack_bf16(out[e] * inv, out[e + 1] * inv);
-        *reinterpret_cast<uint32_t *>(o + orow * D + lane * E + e) = pk;
+        for (int e = 0; e < E; e += 2) {
+            const uint32_t pk = pack_bf16(out[e] * inv, out[e + 1] * inv);
+            *reinterpret_cast<uint32_t *>(o + orow * D + lane * E + e) = pk;
+        }
     }
     if (lane == 0) lse[orow] = M + __logf(W);
 }
@@ -455,6 +484,7 @@ int decode_query_block(int d, int Nq) {
 int decode_ctas_per_sm(int d, int Nq) {
     switch (d) {
         case 64: return ctas_per_sm_d<64>(Nq);
+        case 96: return ctas_per_sm_d<96>(Nq);
         case 128: return ctas_per_sm_d<128>(Nq);
         case 256: return ctas_per_sm_d<256>(Nq);
         default: return 1;
@@ -464,6 +494,7 @@ int decode_ctas_per_sm(int d, int Nq) {
 int launch_decode(const DecodeParams &p, cudaStream_t stream) {
     switch (p.d) {
         case 64: return launch_decode_d<64>(p, stream);
+        case 96: return launch_decode_d<96>(p, stream);
         case 128: return launch_decode_d<128>(p, stream);
         case 256: return launch_decode_d<256>(p, stream);
         default: return FA_ERR_UNSUPPORTED;

@@ -246,7 +246,7 @@ int fa_bwd_varlen(const void *q, const void *k, const void *v, const void *o, co
  *   lse    : fp32 [B][H][Nq] output.
  *   B, H   : >= 1; Hkv >= 1 divides H.  Nq in [1, 65535], (H/Hkv)*Nq <= 65535,
  *            Nk >= 1, B*H*Nq and B*Hkv*Nk < 2^31.
- *   d      : 64, 128 or 256.
+ *   d      : 64, 96, 128 or 256.
  *   scale  : finite and > 0.
  *   num_splits : 0 chooses S automatically (about eight CTAs per SM in total,
  *            at least four pipeline stages of keys per range); a positive value

@@ -118,7 +118,7 @@ def _dec(fa, **kw):
 @pytest.mark.parametrize("kw,code", [
     (dict(q=None), 1), (dict(k=None), 1), (dict(v=None), 1), (dict(o=None), 1), (dict(lse=None), 1),
     (dict(B=0), 1), (dict(H=0), 1), (dict(Nq=0), 1), (dict(Nq=65536), 1), (dict(Nk=0), 1),
-    (dict(B=65536, H=256, Hkv=256, Nk=256), 1), (dict(d=96), 2), (dict(d=32), 2),
+    (dict(B=65536, H=256, Hkv=256, Nk=256), 1), (dict(d=80), 2), (dict(d=32), 2),
     (dict(Hkv=0), 1), (dict(Hkv=3), 1), (dict(Hkv=4), 1), (dict(H=4096, Hkv=1, Nq=17), 1),
     (dict(scale=0.0), 1), (dict(scale=float("nan")), 1), (dict(splits=-1), 1),
     (dict(q=DUMMY + 8), 3), (dict(k=DUMMY + 2), 3), (dict(lse=DUMMY + 4), 3),
@@ -129,7 +129,7 @@ def test_decode_rejects_bad_arguments(fa, kw, code):
 
 def test_decode_split_queries_reject_bad_sizes(fa):
     assert fa.fa_decode_num_splits(0, 1, 1, 1, 100, 128, 0) == -1
-    assert fa.fa_decode_num_splits(1, 1, 1, 1, 100, 96, 0) == -2
+    assert fa.fa_decode_num_splits(1, 1, 1, 1, 100, 80, 0) == -2
     assert fa.fa_decode_num_splits(1, 1, 1, 1, 100, 128, -3) == -1
     assert fa.fa_decode_num_splits(1, 6, 4, 1, 100, 128, 0) == -1
     assert fa.fa_decode_workspace_bytes(1, 1, 1, 0, 100, 128, 0) == 0
@@ -158,7 +158,7 @@ def test_decode_paged_rejects_bad_arguments(fa, kw, code):
 
 def test_decode_paged_split_queries_reject_bad_sizes(fa):
     assert fa.fa_decode_paged_num_splits(1, 1, 1, 1, 128, 0, 4, 0) == -1
-    assert fa.fa_decode_paged_num_splits(1, 1, 1, 1, 96, 16, 4, 0) == -2
+    assert fa.fa_decode_paged_num_splits(1, 1, 1, 1, 80, 16, 4, 0) == -2
     assert fa.fa_decode_paged_workspace_bytes(1, 1, 1, 1, 128, 16, 0, 2) == 0
 
 

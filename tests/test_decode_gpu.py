@@ -43,6 +43,7 @@ SMALL = [
     (1, 2, 1, 1000, 128, 7), (1, 1, 3, 777, 64, 3), (2, 2, 8, 500, 128, 0), (1, 1, 9, 300, 128, 2),
     (1, 2, 5, 1234, 256, 0), (1, 1, 1, 4097, 256, 5), (1, 1, 20, 2000, 64, 4), (1, 1, 1, 100, 128, 50),
     (1, 1, 2, 10, 128, 3), (3, 1, 1, 64, 64, 1), (1, 3, 4, 129, 256, 2), (1, 1, 16, 65, 128, 2),
+    (1, 2, 1, 1000, 96, 0), (2, 1, 3, 777, 96, 3), (1, 1, 9, 129, 96, 1),
 ]
 
 

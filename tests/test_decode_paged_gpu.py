@@ -59,7 +59,7 @@ def _check(fa, orc, q, k, v, lens, page_size, splits, what):
 SMALL = [
     (3, 2, 1, 8, 16, 128, 0), (2, 1, 1, 5, 64, 64, 3), (4, 2, 3, 6, 16, 256, 0),
     (2, 2, 1, 30, 7, 128, 4), (1, 3, 1, 2, 256, 128, 2), (5, 1, 2, 40, 16, 64, 0),
-    (2, 2, 9, 12, 32, 128, 1), (3, 1, 1, 64, 1, 128, 0),
+    (2, 2, 9, 12, 32, 128, 1), (3, 1, 1, 64, 1, 128, 0), (2, 2, 1, 10, 16, 96, 0),
 ]
 
 
