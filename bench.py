@@ -264,7 +264,7 @@ def run_ours(args, rank, world, local_rank):
         f_ms = statistics.mean(fwd_ms)
         b_ms = statistics.mean(bwd_ms)
         if b_ms >= f_ms:
-            kern, kflops, kms = "fa_bwd (fa_bwd_pre_kernel<128> + fa_bwd_kernel_wide<128, causal>)", \
+            kern, kflops, kms = "fa_bwd (fa_bwd_pre_kernel<128> + fa_bwd_kernel<128, causal>)", \
                 bwd_flops(B, H, N, d, causal), b_ms
             traffic = recorded_traffic("fa_bwd_d128_causal_b2h16n4096")
         else:

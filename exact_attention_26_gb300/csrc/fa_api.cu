@@ -355,7 +355,7 @@ extern "C" int fa_bwd_gqa(const void *q, const void *k, const void *v, const voi
     BwdParams p{};
     const int BH = B * H;
     const int npad = (int)round_up((size_t)N, kBwdPad);
-    const int q_rows = (d >= 96) ? 64 : 128;  // query rows per backward q-block
+    const int q_rows = bwd_block_q(d);  // query rows per backward q-block
     if ((rc = make_bhnd_map(&p.tm_q, q, BH, N, d, q_rows)) != FA_OK) return rc;
     if ((rc = make_bhnd_map(&p.tm_do, dout, BH, N, d, q_rows)) != FA_OK) return rc;
     if ((rc = make_bhnd_map(&p.tm_k, k, B * Hkv, N, d, 128)) != FA_OK) return rc;
@@ -410,7 +410,7 @@ extern "C" int fa_bwd_varlen(const void *q, const void *k, const void *v, const 
     BwdParams p{};
     const int BH = B * H;
     const int npad = (int)round_up((size_t)max_seqlen, kBwdPad);
-    const int q_rows = (d >= 96) ? 64 : 128;
+    const int q_rows = bwd_block_q(d);
     if ((rc = make_thd_map(&p.tm_q, q, total_tokens, H, d, q_rows)) != FA_OK) return rc;
     if ((rc = make_thd_map(&p.tm_do, dout, total_tokens, H, d, q_rows)) != FA_OK) return rc;
     if ((rc = make_thd_map(&p.tm_k, k, total_tokens, Hkv, d, 128)) != FA_OK) return rc;

@@ -13,81 +13,35 @@
 //   dS  = P o (dP - D),   D_i = dO_i . O_i
 //   dQ  = scale dS K,     dK = scale dS^T Q
 //
-// Kernel 1 (fa_bwd_pre): D_i, L_i log2(e) (padded rows get D = 0, L = +inf so
-// their P is exactly 0), and dQ := 0.
+// Kernel 1 (fa_bwd_pre_kernel): D_i, L_i log2(e) (padded rows get D = 0, L = +inf
+// so their P is exactly 0), and dQ := 0.
 //
-// Kernel 2 (fa_bwd_kernel): one CTA per (batch*head, block of 128 keys), looping
-// over query blocks of BQ rows (BQ = 64 for d = 128, 128 for d = 64).  All
-// products are tcgen05 MMAs with fp32 accumulators in tensor memory, computed in
-// the transposed orientation so that a TMEM lane is a key:
+// Kernel 2 (fa_bwd_kernel): one CTA per (batch * key/value head, block of 128
+// keys), looping over blocks of 64 query rows.  All products are tcgen05 MMAs
+// with fp32 accumulators in tensor memory, computed in the transposed orientation
+// so that a TMEM lane is a key:
 //
 //   S^T  = K_j Q_i^T        (A = K  smem K-major,  B = Q  smem K-major)
 //   dP^T = V_j dO_i^T       (A = V,  B = dO)
 //   dV  += P^T dO_i         (A = P^T from TMEM,  B = dO smem MN-major)
 //   dK  += dS^T Q_i         (A = dS^T from TMEM, B = Q  smem MN-major)
-//   d=128: dQ_i^T = K_j^T dS^T (A = K smem MN-major, B = dS^T smem MN-major)
-//   d=64:  dQ_i   = dS K_j     (A = dS^T smem MN-major, B = K smem MN-major)
+//   dQ_i^T = K_j^T dS^T     (A = K smem MN-major, B = dS^T smem MN-major)
 //
 // dQ_i leaves tensor memory through a shared-memory staging tile and one bulk
-// asynchronous fp32 add (cp.reduce.async.bulk) into the global dQ rows, which
-// are contiguous.  At the end dK (times scale) and dV are stored once.
+// asynchronous fp32 add (cp.reduce.async.bulk) into the global dQ rows.  At the
+// end dK (times scale) and dV leave once, through shared memory and bulk copies.
 //
-// Warp roles (320 threads):
-//   warps 0-3  P^T = exp2(S^T scale log2e - L log2e), dS^T = P^T o (dP^T - D)
-//              (one key per thread), written as bf16 to TMEM and dS^T to smem;
-//              final dK/dV epilogue
-//   warps 4-7  dQ readout: TMEM -> staging smem -> bulk add into global dQ
-//   warp 8     TMA producer: K_j, V_j once; Q_i, dO_i, L_i, D_i per 2-stage slot
-//   warp 9     TMEM allocator; lane 0 issues every MMA and commit
+// Warp roles (448 threads):
+//   warps 0-7   P^T = exp2(S^T scale log2e - L log2e), dS^T = P^T o (dP^T - D)
+//               (one key per thread, two warpgroups split a block's 64 queries),
+//               written as bf16 to TMEM and dS^T to smem; final dK/dV epilogue
+//   warps 8-11  dQ readout: TMEM -> staging smem -> bulk add into global dQ
+//   warp 12     TMA producer: K_j, V_j once; Q_i, dO_i, L_i, D_i per ring stage
+//   warp 13     TMEM allocator; one elected lane issues every MMA and commit
 #include "fa_ptx.cuh"
 
 namespace fa {
 namespace {
-
-template <int D>
-struct BwdTile {
-    static constexpr int BN = 128;                      // keys per CTA
-    static constexpr int BQ = (D == 128) ? 64 : 128;    // query rows per block
-    static constexpr bool DQ_T = (D == 128);            // dQ computed transposed
-    static constexpr int NCH = D / 64;
-    static constexpr uint32_t K_CHUNK = BN * 128;       // 64 columns x 128 keys
-    static constexpr uint32_t Q_CHUNK = BQ * 128;       // 64 columns x BQ rows
-    static constexpr uint32_t KV_BYTES = BN * D * 2;
-    static constexpr uint32_t Q_BYTES = BQ * D * 2;
-    static constexpr uint32_t DS_CHUNK = BN * 128;      // 64 queries x 128 keys, bf16
-    static constexpr uint32_t DS_BYTES = BQ * BN * 2;
-    static constexpr uint32_t STAGE_BYTES = BQ * D * 4; // dQ tile, fp32
-    static constexpr uint32_t VEC_BYTES = BQ * 4;       // L or D of one q-block
-    // tensor memory columns
-    static constexpr uint32_t TM_DV = 0;
-    static constexpr uint32_t TM_DK = D;
-    static constexpr uint32_t TM_ST = 2 * D;            // S^T fp32 (BQ cols); P^T bf16 over it
-    static constexpr uint32_t TM_DPT = 2 * D + BQ;      // dP^T fp32 (BQ cols); dS^T bf16 over it
-    static constexpr uint32_t TM_DQ0 = 384;             // dQ buffers, 64 cols each
-    static constexpr uint32_t TM_DQ1 = 448;
-    static constexpr uint32_t TM_COLS = 512;
-    // shared memory layout
-    static constexpr uint32_t OFF_K = 0;
-    static constexpr uint32_t OFF_V = OFF_K + KV_BYTES;
-    static constexpr uint32_t OFF_Q = OFF_V + KV_BYTES;           // 2 stages
-    static constexpr uint32_t OFF_DO = OFF_Q + 2 * Q_BYTES;       // 2 stages
-    static constexpr uint32_t OFF_DS = OFF_DO + 2 * Q_BYTES;      // 2 buffers
-    static constexpr uint32_t OFF_STAGE = OFF_DS + 2 * DS_BYTES;  // dQ staging
-    static constexpr uint32_t OFF_L2 = OFF_STAGE + STAGE_BYTES;   // 2 stages
-    static constexpr uint32_t OFF_DELTA = OFF_L2 + 2 * VEC_BYTES; // 2 stages
-    static constexpr uint32_t OFF_BAR = OFF_DELTA + 2 * VEC_BYTES;
-    // kv_full, q_full[2], q_empty[2], s_full, ds_full, dq_full[2], dq_empty[2], done,
-    // stg_free, stg_full
-    static constexpr int NBAR = 14;
-    static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
-    static constexpr uint32_t SMEM_BYTES = OFF_MISC + 16 + 1024;
-    static constexpr int THREADS = 320;
-
-    static_assert(D == 64 || D == 128, "backward head dim");
-    static_assert(TM_DPT + BQ <= TM_DQ0, "tensor memory budget");
-    static_assert(Q_CHUNK % 1024 == 0 && DS_CHUNK % 1024 == 0, "swizzle atoms must stay aligned");
-    static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
-};
 
 // ---------------------------------------------------------------- preprocess
 
@@ -171,430 +125,9 @@ __global__ void __launch_bounds__(256)
 }
 
 // ---------------------------------------------------------------- main kernel
-
-template <int D, bool CAUSAL, bool VARLEN>
-__global__ void __launch_bounds__(320, 1)
-    fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                  const float *__restrict__ ws_lse2, const float *__restrict__ ws_delta,
-                  float *__restrict__ dq, float *__restrict__ dk, float *__restrict__ dv, int N,
-                  int Npad, int BHkv, int H, int group, const int *__restrict__ cu_seqlens,
-                  int total_tokens, float scale, float scale_log2, int *status,
-                  unsigned long long limit_ns) {
-    using T = BwdTile<D>;
-    constexpr int BQ = T::BQ;
-    extern __shared__ uint8_t smem_raw[];
-    const uint32_t raw = smem_u32(smem_raw);
-    const uint32_t base = (raw + 1023u) & ~1023u;
-    uint8_t *gbase = smem_raw + (base - raw);
-
-    const uint32_t sK = base + T::OFF_K, sV = base + T::OFF_V;
-    const uint32_t sQ = base + T::OFF_Q, sDO = base + T::OFF_DO;
-    const uint32_t sDS = base + T::OFF_DS, sStage = base + T::OFF_STAGE;
-    const uint32_t sL2 = base + T::OFF_L2, sDelta = base + T::OFF_DELTA;
-    const uint32_t bar = base + T::OFF_BAR;
-    const uint32_t bar_kv_full = bar;
-    const uint32_t bar_q_full = bar + 8;        // [2]
-    const uint32_t bar_q_empty = bar + 24;      // [2]
-    const uint32_t bar_s_full = bar + 40;
-    const uint32_t bar_ds_full = bar + 48;
-    const uint32_t bar_dq_full = bar + 56;      // [2]
-    const uint32_t bar_dq_empty = bar + 72;     // [2]
-    const uint32_t bar_done = bar + 88;
-    const uint32_t bar_stg_free = bar + 96;     // staging tile may be overwritten
-    const uint32_t bar_stg_full = bar + 104;    // staging tile written by all 128 threads
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + T::OFF_MISC);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(gbase + T::OFF_MISC + 4);
-    float *stage_f = reinterpret_cast<float *>(gbase + T::OFF_STAGE);
-    const float *l2_f = reinterpret_cast<const float *>(gbase + T::OFF_L2);
-    const float *delta_f = reinterpret_cast<const float *>(gbase + T::OFF_DELTA);
-
-    const int warp = threadIdx.x >> 5;
-    const int lane = threadIdx.x & 31;
-
-    // Causal: key block 0 has the most query blocks, so low blockIdx = key block first.
-    // Grouped-query attention: this CTA owns key/value head kvh (= b * Hkv + hk)
-    // and accumulates dK, dV over the `group` query heads that read it, walking
-    // their query blocks one head after the other.
-    const int kvh = blockIdx.x % BHkv;
-    const int jb = blockIdx.x / BHkv;
-    const int kv0 = jb * T::BN;
-    // Keys and queries of this head: N, or with packed sequences (VARLEN: token-major
-    // q, k, v, o, dO, dq, dk, dv, and N is the maximum length) the sequence's own
-    // length, checked on the device.  A key block past the sequence's end has no work.
-    const int hk = kvh % (H / group);
-    int len = N, tok0 = 0;
-    if constexpr (VARLEN) {
-        const int b = kvh / (H / group);
-        const int a = cu_seqlens[b], e = cu_seqlens[b + 1];
-        if (a < 0 || e < a || e > total_tokens || e - a > N) {
-            if (threadIdx.x == 0 && kv0 == 0 && hk == 0) {
-                atomicCAS(status + 1, 0, SITE_BWD_BAD_SEQ);
-                atomicExch(status, FA_ERR_BAD_INDEX);
-            }
-            len = 0;
-        } else {
-            len = e - a;
-            tok0 = a;
-        }
-    }
-    if (kv0 >= len) return;  // uniform across the CTA, before any barrier or TMEM use
-    const int n_qb = (len + BQ - 1) / BQ;
-    const int i_start = CAUSAL ? kv0 / BQ : 0;
-    const int n_qit = n_qb - i_start;  // query blocks per query head
-    const int n_it = group * n_qit;
-    const int bhq0 = (kvh / (H / group)) * H + (kvh % (H / group)) * group;
-    // Block it is query block qb = it % n_qit of query head bhq0 + it / n_qit; the
-    // loops below carry (qb, gq) as counters instead of dividing every block.
-
-    if (threadIdx.x == 0) {
-        mbar_init(bar_kv_full, 1);
-        for (int s = 0; s < 2; ++s) {
-            mbar_init(bar_q_full + 8 * s, 1);
-            mbar_init(bar_q_empty + 8 * s, 1);
-            mbar_init(bar_dq_full + 8 * s, 1);
-            mbar_init(bar_dq_empty + 8 * s, 128);
-        }
-        mbar_init(bar_s_full, 1);
-        mbar_init(bar_ds_full, 128);
-        mbar_init(bar_done, 1);
-        mbar_init(bar_stg_free, 1);
-        mbar_init(bar_stg_full, 128);
-        *abort_flag = 0;
-        fence_mbar_init();
-    }
-    if (warp == 9) {
-        tmem_alloc(smem_u32(tmem_slot), T::TM_COLS);
-        tmem_relinquish();
-    }
-    if (warp == 8 && lane == 0) {
-        tma_prefetch_desc(&tm_q);
-        tma_prefetch_desc(&tm_k);
-        tma_prefetch_desc(&tm_v);
-        tma_prefetch_desc(&tm_do);
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = *tmem_slot;
-    const Guard g{status, abort_flag, limit_ns};
-
-    if (warp == 8) {
-        // ------------------------------------------------------- TMA producer
-        if (lane == 0) {
-            mbar_arrive_expect_tx(bar_kv_full, 2 * T::KV_BYTES);
-            for (int c = 0; c < T::NCH; ++c) {
-                tma_load_3d(sK + c * T::K_CHUNK, &tm_k, bar_kv_full, c * 64, VARLEN ? hk : kv0,
-                            VARLEN ? tok0 + kv0 : kvh);
-                tma_load_3d(sV + c * T::K_CHUNK, &tm_v, bar_kv_full, c * 64, VARLEN ? hk : kv0,
-                            VARLEN ? tok0 + kv0 : kvh);
-            }
-            int issued = 0;
-            for (int it = 0, qb = 0, gq = 0; it < n_it; ++it, (++qb == n_qit) ? (qb = 0, ++gq) : 0) {
-                const int s = it & 1;
-                const int q0 = (i_start + qb) * BQ;
-                if (it >= 2 && !mbar_wait(bar_q_empty + 8 * s, ((it >> 1) - 1) & 1, g,
-                                          SITE_BWD_LOAD_EMPTY))
-                    break;
-                const uint32_t fb = bar_q_full + 8 * s;
-                mbar_arrive_expect_tx(fb, 2 * T::Q_BYTES + 2 * T::VEC_BYTES);
-                for (int c = 0; c < T::NCH; ++c) {
-                    tma_load_3d(sQ + s * T::Q_BYTES + c * T::Q_CHUNK, &tm_q, fb, c * 64, VARLEN ? (bhq0 + gq) % H : q0,
-                                VARLEN ? tok0 + q0 : bhq0 + gq);
-                    tma_load_3d(sDO + s * T::Q_BYTES + c * T::Q_CHUNK, &tm_do, fb, c * 64, VARLEN ? (bhq0 + gq) % H : q0,
-                                VARLEN ? tok0 + q0 : bhq0 + gq);
-                }
-                const size_t voff = (size_t)(bhq0 + gq) * Npad + q0;
-                bulk_load(sL2 + s * T::VEC_BYTES, ws_lse2 + voff, T::VEC_BYTES, fb);
-                bulk_load(sDelta + s * T::VEC_BYTES, ws_delta + voff, T::VEC_BYTES, fb);
-                ++issued;
-            }
-            if (*abort_flag) {
-                volatile int never = 0;
-                const Guard g2{status, &never, kWaitLimitNs};
-                mbar_wait(bar_kv_full, 0, g2, SITE_BWD_DRAIN);
-                for (int it = (issued > 2 ? issued - 2 : 0); it < issued; ++it)
-                    mbar_wait(bar_q_full + 8 * (it & 1), (it >> 1) & 1, g2, SITE_BWD_DRAIN);
-            }
-        }
-    } else if (warp == 9) {
-        // ------------------------------------------------------- MMA issuer
-        // The whole warp runs this loop (warp-uniform); one elected lane issues.
-        {
-            constexpr uint32_t kIdescT = idesc_bf16_f32(128, BQ, false, false);   // S^T, dP^T
-            constexpr uint32_t kIdescAcc = idesc_bf16_f32(128, D, false, true);   // dV, dK
-            constexpr uint32_t kIdescDQ = T::DQ_T ? idesc_bf16_f32(128, BQ, true, true)  // dQ^T
-                                                  : idesc_bf16_f32(128, D, true, true);  // dQ
-            bool ok = mbar_wait_warp(bar_kv_full, 0, g, SITE_BWD_MMA_KV);
-            auto issue_st_dpt = [&](int it) {
-                const int s = it & 1;
-                const uint32_t q_t = sQ + s * T::Q_BYTES, do_t = sDO + s * T::Q_BYTES;
-#pragma unroll
-                for (int ks = 0; ks < D / 16; ++ks) {
-                    const uint32_t koff = (ks & 3) * 32;
-                    const uint32_t kc = (ks >> 2);
-                    mma_ss_elect(tmem + T::TM_ST, sdesc_sw128(sK + kc * T::K_CHUNK + koff, 16, 1024),
-                           sdesc_sw128(q_t + kc * T::Q_CHUNK + koff, 16, 1024), kIdescT,
-                           ks > 0 ? 1u : 0u);
-                }
-#pragma unroll
-                for (int ks = 0; ks < D / 16; ++ks) {
-                    const uint32_t koff = (ks & 3) * 32;
-                    const uint32_t kc = (ks >> 2);
-                    mma_ss_elect(tmem + T::TM_DPT, sdesc_sw128(sV + kc * T::K_CHUNK + koff, 16, 1024),
-                           sdesc_sw128(do_t + kc * T::Q_CHUNK + koff, 16, 1024), kIdescT,
-                           ks > 0 ? 1u : 0u);
-                }
-                tc_commit_elect(bar_s_full);
-            };
-            if (ok && mbar_wait_warp(bar_q_full, 0, g, SITE_BWD_MMA_Q_FULL)) {
-                tc_fence_after();
-                issue_st_dpt(0);
-            } else {
-                ok = false;
-            }
-            for (int it = 0; ok && it < n_it; ++it) {
-                const int s = it & 1;
-                const uint32_t q_t = sQ + s * T::Q_BYTES, do_t = sDO + s * T::Q_BYTES;
-                if (!mbar_wait_warp(bar_ds_full, it & 1, g, SITE_BWD_MMA_DS_FULL)) { ok = false; break; }
-                tc_fence_after();
-                // dV += P^T dO_i ; dK += dS^T Q_i   (K = BQ queries, 16 per step)
-#pragma unroll
-                for (int ks = 0; ks < BQ / 16; ++ks)
-                    mma_ts_elect(tmem + T::TM_DV, tmem + T::TM_ST + ks * 8,
-                           sdesc_sw128(do_t + ks * 2048, T::Q_CHUNK, 1024), kIdescAcc,
-                           (it > 0 || ks > 0) ? 1u : 0u);
-#pragma unroll
-                for (int ks = 0; ks < BQ / 16; ++ks)
-                    mma_ts_elect(tmem + T::TM_DK, tmem + T::TM_DPT + ks * 8,
-                           sdesc_sw128(q_t + ks * 2048, T::Q_CHUNK, 1024), kIdescAcc,
-                           (it > 0 || ks > 0) ? 1u : 0u);
-                tc_commit_elect(bar_q_empty + 8 * s);
-                // Next block's S^T and dP^T overlap this block's dQ and the softmax of the next.
-                if (it + 1 < n_it) {
-                    if (!mbar_wait_warp(bar_q_full + 8 * ((it + 1) & 1), ((it + 1) >> 1) & 1, g,
-                                   SITE_BWD_MMA_Q_FULL)) { ok = false; break; }
-                    tc_fence_after();
-                    issue_st_dpt(it + 1);
-                }
-                // dQ of this block into TMEM buffer it&1 (K = 128 keys, 16 per step).
-                const int b = it & 1;
-                if (it >= 2 && !mbar_wait_warp(bar_dq_empty + 8 * b, ((it >> 1) - 1) & 1, g,
-                                          SITE_BWD_MMA_DQ_FREE)) { ok = false; break; }
-                tc_fence_after();
-                const uint32_t ds_t = sDS + b * T::DS_BYTES;
-                const uint32_t dq_tm = tmem + (b ? T::TM_DQ1 : T::TM_DQ0);
-#pragma unroll
-                for (int ks = 0; ks < T::BN / 16; ++ks) {
-                    if constexpr (T::DQ_T) {
-                        // dQ^T[d][q] = sum_k K[k][d] dS^T[k][q]: A = K (M = d), B = dS^T (N = q)
-                        mma_ss_elect(dq_tm, sdesc_sw128(sK + ks * 2048, T::K_CHUNK, 1024),
-                               sdesc_sw128(ds_t + ks * 2048, T::DS_CHUNK, 1024), kIdescDQ,
-                               ks > 0 ? 1u : 0u);
-                    } else {
-                        // dQ[q][d] = sum_k dS^T[k][q] K[k][d]: A = dS^T (M = q), B = K (N = d)
-                        mma_ss_elect(dq_tm, sdesc_sw128(ds_t + ks * 2048, T::DS_CHUNK, 1024),
-                               sdesc_sw128(sK + ks * 2048, T::K_CHUNK, 1024), kIdescDQ,
-                               ks > 0 ? 1u : 0u);
-                    }
-                }
-                tc_commit_elect(bar_dq_full + 8 * b);
-            }
-            tc_commit_elect(bar_done);
-            volatile int never = 0;
-            const Guard g2{status, &never, kWaitLimitNs};
-            mbar_wait_warp(bar_done, 0, g2, SITE_BWD_DRAIN);
-        }
-    } else if (warp < 4) {
-        // ------------------------------------------------------- P^T and dS^T
-        const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-        const uint32_t t_st = tmem + lane_base + T::TM_ST;
-        const uint32_t t_dpt = tmem + lane_base + T::TM_DPT;
-        const int r = threadIdx.x;       // key row within the block (TMEM lane)
-        const int key = kv0 + r;
-        bool ok = true;
-        for (int it = 0, qb = 0, gq = 0; it < n_it; ++it, (++qb == n_qit) ? (qb = 0, ++gq) : 0) {
-            const int s = it & 1;
-            const int q0 = (i_start + qb) * BQ;
-            ok = mbar_wait_warp(bar_s_full, it & 1, g, SITE_BWD_SOFTMAX_S_FULL);
-            if (!ok) break;
-            tc_fence_after();
-            const bool need_mask = (kv0 + T::BN > len) || (CAUSAL && q0 < kv0 + T::BN - 1);
-            const float *l2v = l2_f + s * BQ;
-            const float *dlv = delta_f + s * BQ;
-            uint8_t *ds_row = gbase + T::OFF_DS + (it & 1) * T::DS_BYTES + r * 128;
-#pragma unroll 1
-            for (int c = 0; c < BQ / 32; ++c) {
-                uint32_t sv[32], dpv[32];
-                tmem_ld32(t_st + c * 32, sv);
-                tmem_ld32(t_dpt + c * 32, dpv);
-                tmem_wait_ld(sv);
-                tmem_wait_ld(dpv);
-                uint32_t pk[16], dk_[16];
-#pragma unroll
-                for (int e = 0; e < 32; e += 4) {
-                    const float4 l4 = *reinterpret_cast<const float4 *>(l2v + c * 32 + e);
-                    const float4 d4 = *reinterpret_cast<const float4 *>(dlv + c * 32 + e);
-                    const float lq[4] = {l4.x, l4.y, l4.z, l4.w};
-                    const float dq_[4] = {d4.x, d4.y, d4.z, d4.w};
-                    float p[4], ds[4];
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        p[u] = ex2(fmaf(__uint_as_float(sv[e + u]), scale_log2, -lq[u]));
-                        if (need_mask) {
-                            const int q = q0 + c * 32 + e + u;
-                            if (key >= len || (CAUSAL && q < key)) p[u] = 0.f;
-                        }
-                        ds[u] = p[u] * (__uint_as_float(dpv[e + u]) - dq_[u]);
-                    }
-                    pk[e / 2] = pack_bf16(p[0], p[1]);
-                    pk[e / 2 + 1] = pack_bf16(p[2], p[3]);
-                    dk_[e / 2] = pack_bf16(ds[0], ds[1]);
-                    dk_[e / 2 + 1] = pack_bf16(ds[2], ds[3]);
-                }
-                tmem_st16(t_st + c * 16, pk);
-                tmem_st16(t_dpt + c * 16, dk_);
-                // dS^T row r, queries [32c, 32c + 32): 4 swizzled 16-byte units.
-                const int h = (c * 32) / 64;
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const int unit = ((c * 32) % 64) / 8 + u;
-                    uint4 *dst = reinterpret_cast<uint4 *>(ds_row + h * T::DS_CHUNK +
-                                                           ((unit ^ (r & 7)) * 16));
-                    *dst = make_uint4(dk_[4 * u], dk_[4 * u + 1], dk_[4 * u + 2], dk_[4 * u + 3]);
-                }
-            }
-            tmem_wait_st();
-            fence_proxy_async_smem();
-            tc_fence_before();
-            mbar_arrive(bar_ds_full);
-        }
-        // ------------------------------------------------------- dK, dV epilogue
-        ok = ok && mbar_wait_warp(bar_done, 0, g, SITE_BWD_EPILOGUE);
-        if (ok) {
-            tc_fence_after();
-            const size_t krow = VARLEN ? (size_t)(tok0 + key) * (H / group) + hk : (size_t)kvh * N + key;
-            float *dv_row = dv + krow * D;
-            float *dk_row = dk + krow * D;
-#pragma unroll 1
-            for (int c = 0; c < D / 32; ++c) {
-                uint32_t a[32], b2[32];
-                tmem_ld32(tmem + lane_base + T::TM_DV + c * 32, a);
-                tmem_ld32(tmem + lane_base + T::TM_DK + c * 32, b2);
-                tmem_wait_ld(a);
-                tmem_wait_ld(b2);
-                if (key < len) {
-#pragma unroll
-                    for (int e = 0; e < 32; e += 4) {
-                        *reinterpret_cast<float4 *>(dv_row + c * 32 + e) =
-                            make_float4(__uint_as_float(a[e]), __uint_as_float(a[e + 1]),
-                                        __uint_as_float(a[e + 2]), __uint_as_float(a[e + 3]));
-                        *reinterpret_cast<float4 *>(dk_row + c * 32 + e) = make_float4(
-                            __uint_as_float(b2[e]) * scale, __uint_as_float(b2[e + 1]) * scale,
-                            __uint_as_float(b2[e + 2]) * scale, __uint_as_float(b2[e + 3]) * scale);
-                    }
-                }
-            }
-        }
-    } else {
-        // ------------------------------------------------------- dQ readout (warps 4-7)
-        const int t = threadIdx.x - 128;  // TMEM lane: d index (d = 128) or query row (d = 64)
-        const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-        bool ok = true;
-        for (int it = 0, qb = 0, gq = 0; it < n_it; ++it, (++qb == n_qit) ? (qb = 0, ++gq) : 0) {
-            const int b = it & 1;
-            const int q0 = (i_start + qb) * BQ;
-            ok = mbar_wait_warp(bar_dq_full + 8 * b, (it >> 1) & 1, g, SITE_BWD_DQ_FULL);
-            if (!ok) break;
-            tc_fence_after();
-            const uint32_t src = tmem + lane_base + (b ? T::TM_DQ1 : T::TM_DQ0);
-            uint32_t x0[32], x1[32];
-            tmem_ld32(src, x0);
-            tmem_ld32(src + 32, x1);
-            tmem_wait_ld(x0);
-            tmem_wait_ld(x1);
-            tc_fence_before();
-            mbar_arrive(bar_dq_empty + 8 * b);
-            // The staging tile is free once the previous bulk add has read it.  All
-            // syncs here are bounded mbarrier waits, so an abort cannot strand a warp.
-            if (warp == 4) {
-                bulk_wait_group_read<0>();  // every lane's adds of the previous block
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar_stg_free);
-            }
-            ok = mbar_wait_warp(bar_stg_free, it & 1, g, SITE_BWD_DQ_FULL);
-            if (!ok) break;
-            if constexpr (T::DQ_T) {
-                // lane t = column d of dQ; the 64 columns of TMEM are the block's queries
-#pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    stage_f[e * D + t] = __uint_as_float(x0[e]) * scale;
-                    stage_f[(e + 32) * D + t] = __uint_as_float(x1[e]) * scale;
-                }
-            } else {
-                // lane t = query row; the 64 columns are d
-                float *row = stage_f + t * D;
-#pragma unroll
-                for (int e = 0; e < 32; e += 4) {
-                    *reinterpret_cast<float4 *>(row + e) =
-                        make_float4(__uint_as_float(x0[e]) * scale, __uint_as_float(x0[e + 1]) * scale,
-                                    __uint_as_float(x0[e + 2]) * scale, __uint_as_float(x0[e + 3]) * scale);
-                    *reinterpret_cast<float4 *>(row + 32 + e) =
-                        make_float4(__uint_as_float(x1[e]) * scale, __uint_as_float(x1[e + 1]) * scale,
-                                    __uint_as_float(x1[e + 2]) * scale, __uint_as_float(x1[e + 3]) * scale);
-                }
-            }
-            fence_proxy_async_smem();
-            mbar_arrive(bar_stg_full);
-            if (warp == 4) {
-                bool ok0 = true;
-                const int rows = min(BQ, len - q0);
-                if constexpr (VARLEN) {
-                    // token-major dQ: the block's rows of this head are H * D floats
-                    // apart, so each lane adds its own rows
-                    ok0 = mbar_wait_warp(bar_stg_full, it & 1, g, SITE_BWD_DQ_FULL);
-                    if (ok0) {
-                        const int hq = (bhq0 + gq) % H;
-                        for (int i = lane; i < rows; i += 32)
-                            bulk_reduce_add_f32(dq + ((size_t)(tok0 + q0 + i) * H + hq) * D,
-                                                sStage + (uint32_t)(i * D * 4), (uint32_t)(D * 4));
-                        bulk_commit_group();
-                    }
-                } else {
-                    if (lane == 0) {
-                        ok0 = mbar_wait(bar_stg_full, it & 1, g, SITE_BWD_DQ_FULL);
-                        if (ok0) {
-                            bulk_reduce_add_f32(dq + ((size_t)(bhq0 + gq) * N + q0) * D, sStage,
-                                                (uint32_t)(rows * D * 4));
-                            bulk_commit_group();
-                        }
-                    }
-                }
-                ok0 = __shfl_sync(0xffffffffu, ok0 ? 1 : 0, 0) != 0;
-                if (!ok0) {
-                    ok = false;
-                    break;
-                }
-            }
-        }
-        // Only the shared-memory reads of the last bulk add must finish before the
-        // CTA retires; its global writes complete before the kernel does.
-        if (warp == 4) bulk_wait_group_read<0>();
-    }
-
-    __syncwarp();
-    tc_fence_before();
-    __syncthreads();
-    if (warp == 9) {
-        tc_fence_after();
-        tmem_dealloc(tmem, T::TM_COLS);
-    }
-}
-
-// ---------------------------------------------------------------- d = 96, 128 kernel
 //
-// Same products as fa_bwd_kernel, scheduled so the tensor core never waits for
-// the P^T/dS^T warps.  Tensor memory (512 columns): dV [0,128), dK [128,256),
+// The products are scheduled so the tensor core never waits for the P^T/dS^T
+// warps.  Tensor memory (512 columns): dV [0,128), dK [128,256),
 // S^T [256,320), dP^T [320,384), PD [384,448) holding bf16 P^T (first 32
 // columns) and dS^T (last 32), dQ^T [448,512).  Because P^T and dS^T go to their
 // own region, the next block's S^T and dP^T can be issued as soon as the compute
@@ -607,14 +140,15 @@ __global__ void __launch_bounds__(320, 1)
 // d = 96 keeps the d = 128 layout: rows are two 64-column swizzle chunks whose
 // columns past d the copies zero-fill, S^T and dP^T run D/16 K steps, dV and dK
 // have N = D, and dQ^T keeps M = 128 (its rows past d come out zero and are not
-// read).
+// read).  d = 64 has rows of one chunk; dQ^T still has M = 128, its rows 64..127
+// read the next 64-row chunk of shared memory (the V tile) and are not read back.
 template <int D_>
-struct BwdWide {
+struct BwdTile {
     static constexpr int D = D_;
-    static constexpr int DP = 128;                      // row width in shared memory
+    static constexpr int DP = D <= 64 ? 64 : 128;       // row width in shared memory
     static constexpr int BN = 128;
     static constexpr int BQ = 64;
-    static constexpr int NCH = 2;
+    static constexpr int NCH = DP / 64;
     static constexpr int QS = 3;                        // Q/dO/L/D ring stages
     static constexpr uint32_t K_CHUNK = BN * 128;
     static constexpr uint32_t Q_CHUNK = BQ * 128;
@@ -643,19 +177,19 @@ struct BwdWide {
     static constexpr int THREADS = 448;  // compute 0-7, dQ readout 8-11, TMA 12, MMA 13
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
     static_assert(Q_CHUNK % 1024 == 0 && DS_BYTES % 1024 == 0, "swizzle atoms must stay aligned");
-    static_assert(D == 96 || D == 128, "head dim");
+    static_assert(D == 64 || D == 96 || D == 128, "head dim");
 };
 
 template <int D, bool CAUSAL, bool VARLEN>
 __global__ void __launch_bounds__(448, 1)
-    fa_bwd_kernel_wide(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+    fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                        const float *__restrict__ ws_lse2, const float *__restrict__ ws_delta,
                        float *__restrict__ dq, float *__restrict__ dk, float *__restrict__ dv, int N,
                        int Npad, int BHkv, int H, int group, const int *__restrict__ cu_seqlens,
                   int total_tokens, float scale, float scale_log2, int *status,
                        unsigned long long limit_ns) {
-    using T = BwdWide<D>;
+    using T = BwdTile<D>;
     constexpr int BQ = T::BQ, QS = T::QS;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -946,7 +480,7 @@ __global__ void __launch_bounds__(448, 1)
             // staged in shared memory at a 528-byte pitch (16-byte writes without bank
             // conflicts; the Q/dO area is free once every MMA is done) and leave with
             // one bulk copy per half-row, so global writes are 256 contiguous bytes.
-            constexpr uint32_t kPitch = 528;
+            constexpr uint32_t kPitch = T::DP * 4 + 16;  // 16-byte units shift by one per row
             static_assert(128 * kPitch <= T::OFF_DS - T::OFF_Q, "epilogue staging fits Q/dO area");
             uint8_t *stg = gbase + T::OFF_Q + r * kPitch + 256 * h;
             const uint32_t stg_s = sQ + r * kPitch + 256 * h;
@@ -969,7 +503,7 @@ __global__ void __launch_bounds__(448, 1)
                             __uint_as_float(a[e + 2]) * mul, __uint_as_float(a[e + 3]) * mul);
                 }
                 fence_proxy_async_smem();
-                if (key < len) {
+                if (key < len && (h == 0 || D > 64)) {
                     const size_t krow =
                         VARLEN ? (size_t)(tok0 + key) * (H / group) + hk : (size_t)kvh * N + key;
                     float *dst = (pass == 0 ? dv : dk) + krow * D + 64 * h;
@@ -1076,27 +610,15 @@ int launch_bwd_t(const BwdParams &p, cudaStream_t stream) {
             p.N, p.Npad, p.BH, p.H, p.cu_seqlens, p.total_tokens);
         if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
     }
-    constexpr int kBN = 128;  // keys per CTA in both kernels
-    static_assert(kBN == BwdWide<128>::BN && kBN == BwdTile<64>::BN, "key block");
-    const long long grid = (long long)((p.N + kBN - 1) / kBN) * (p.BH / p.group);
+    using W = BwdTile<D>;
+    const long long grid = (long long)((p.N + W::BN - 1) / W::BN) * (p.BH / p.group);
     if (grid > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
-    if constexpr (D >= 96) {
-        using W = BwdWide<D>;
-        auto kern = fa_bwd_kernel_wide<D, CAUSAL, VARLEN>;
+    {
+        auto kern = fa_bwd_kernel<D, CAUSAL, VARLEN>;
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)W::SMEM_BYTES) != cudaSuccess)
             return FA_ERR_CUDA;
         kern<<<(unsigned)grid, W::THREADS, W::SMEM_BYTES, stream>>>(
-            p.tm_q, p.tm_k, p.tm_v, p.tm_do, p.ws_lse2, p.ws_delta, p.dq, p.dk, p.dv, p.N, p.Npad,
-            p.BH / p.group, p.H, p.group, p.cu_seqlens, p.total_tokens, p.scale, p.scale_log2,
-            p.status, p.limit_ns);
-    } else {
-        using T = BwdTile<D>;
-        auto kern = fa_bwd_kernel<D, CAUSAL, VARLEN>;
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)T::SMEM_BYTES) != cudaSuccess)
-            return FA_ERR_CUDA;
-        kern<<<(unsigned)grid, T::THREADS, T::SMEM_BYTES, stream>>>(
             p.tm_q, p.tm_k, p.tm_v, p.tm_do, p.ws_lse2, p.ws_delta, p.dq, p.dk, p.dv, p.N, p.Npad,
             p.BH / p.group, p.H, p.group, p.cu_seqlens, p.total_tokens, p.scale, p.scale_log2,
             p.status, p.limit_ns);
@@ -1112,6 +634,8 @@ int launch_bwd_d(const BwdParams &p, cudaStream_t stream) {
 }
 
 }  // namespace
+
+int bwd_block_q(int) { return BwdTile<128>::BQ; }
 
 int launch_bwd(const BwdParams &p, cudaStream_t stream) {
     switch (p.d) {

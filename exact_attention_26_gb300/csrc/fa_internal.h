@@ -70,6 +70,10 @@ struct QuantParams {
 
 int launch_quant(const QuantParams &p, cudaStream_t stream);
 
+// Query rows per backward block of the kernel that serves head dim d (the box
+// height of the q and dO tensor maps).
+int bwd_block_q(int d);
+
 struct BwdParams {
     CUtensorMap tm_q, tm_k, tm_v, tm_do;  // 3-D maps over [BH][N][d] (q, do), [B*Hkv][N][d] (k, v)
     const void *o, *dout;                 // bf16 [BH][N][d]
