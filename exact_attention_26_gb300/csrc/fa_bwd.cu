@@ -13,8 +13,8 @@
 //   dS  = P o (dP - D),   D_i = dO_i . O_i
 //   dQ  = scale dS K,     dK = scale dS^T Q
 //
-// Kernel 1 (fa_bwd_pre_kernel): D_i, L_i log2(e) (padded rows get D = 0, L = +inf
-// so their P is exactly 0), and dQ := 0.
+// Kernel 1 (fa_bwd_pre_kernel): -D_i and -L_i log2(e), negated so the main kernel
+// adds them (padded rows get 0 and -inf, so their P is exactly 0), and dQ := 0.
 //
 // Kernel 2 (fa_bwd_kernel): one CTA per (batch * key/value head, block of 128
 // keys), looping over blocks of 64 query rows.  All products are tcgen05 MMAs
@@ -114,12 +114,12 @@ __global__ void __launch_bounds__(256)
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
             if (lane == 0) {
-                delta[r] = acc;
-                lse2[r] = lse[lse_i] * kLog2e;
+                delta[r] = -acc;
+                lse2[r] = -(lse[lse_i] * kLog2e);
             }
         } else if (lane == 0) {
             delta[r] = 0.f;
-            lse2[r] = INFINITY;
+            lse2[r] = -INFINITY;
         }
     }
 }
@@ -427,22 +427,33 @@ __global__ void __launch_bounds__(448, 1)
             const float *l2v = l2_f + s * BQ + 32 * h;
             const float *dlv = delta_f + s * BQ + 32 * h;
             uint32_t pk[16], dk_[16];
+            const uint64_t c2 = f32x2_splat(scale_log2);
 #pragma unroll
             for (int e = 0; e < 32; e += 4) {
+                // the workspace holds -L log2e and -D, so both steps are packed pair
+                // operations (the same roundings as s*c - L and dP - D)
                 const float4 l4 = *reinterpret_cast<const float4 *>(l2v + e);
                 const float4 d4 = *reinterpret_cast<const float4 *>(dlv + e);
-                const float lq[4] = {l4.x, l4.y, l4.z, l4.w};
-                const float dq_[4] = {d4.x, d4.y, d4.z, d4.w};
                 float p[4], ds[4];
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
-                    p[u] = ex2(fmaf(__uint_as_float(sv[e + u]), scale_log2, -lq[u]));
+                    p[u] = __uint_as_float(sv[e + u]);
+                    ds[u] = __uint_as_float(dpv[e + u]);
+                }
+                fma_f32x2(p[0], p[1], c2, l4.x, l4.y);
+                fma_f32x2(p[2], p[3], c2, l4.z, l4.w);
+                add_f32x2(ds[0], ds[1], d4.x, d4.y);
+                add_f32x2(ds[2], ds[3], d4.z, d4.w);
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    p[u] = ex2(p[u]);
                     if (need_mask) {
                         const int q = q0 + 32 * h + e + u;
                         if (key >= len || (CAUSAL && q < key)) p[u] = 0.f;
                     }
-                    ds[u] = p[u] * (__uint_as_float(dpv[e + u]) - dq_[u]);
                 }
+                mul_f32x2(ds[0], ds[1], p[0], p[1]);
+                mul_f32x2(ds[2], ds[3], p[2], p[3]);
                 pk[e / 2] = pack_bf16(p[0], p[1]);
                 pk[e / 2 + 1] = pack_bf16(p[2], p[3]);
                 dk_[e / 2] = pack_bf16(ds[0], ds[1]);

@@ -399,6 +399,63 @@ __device__ __forceinline__ float lg2(float x) {
     return y;
 }
 
+// Packed fp32 pairs (sm_100+): one instruction for two independent IEEE fp32
+// operations, each rounded to nearest like its scalar form.  Pairs are passed as
+// two floats; the moves in and out of the 64-bit register are free when the two
+// sit in an aligned register pair.
+__device__ __forceinline__ uint64_t f32x2_splat(float a) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %1};" : "=l"(r) : "f"(a));
+    return r;
+}
+
+// (x0, x1) <- (x0, x1) * b + c  with b, c splatted pairs.
+__device__ __forceinline__ void fma_f32x2(float &x0, float &x1, uint64_t b, uint64_t c) {
+    asm("{\n\t.reg .b64 x;\n\tmov.b64 x, {%0, %1};\n\tfma.rn.f32x2 x, x, %2, %3;\n\t"
+        "mov.b64 {%0, %1}, x;\n\t}"
+        : "+f"(x0), "+f"(x1)
+        : "l"(b), "l"(c));
+}
+
+// (x0, x1) <- (x0, x1) * b + (c0, c1)  with b a splatted pair.
+__device__ __forceinline__ void fma_f32x2(float &x0, float &x1, uint64_t b, float c0, float c1) {
+    asm("{\n\t.reg .b64 x, c;\n\tmov.b64 x, {%0, %1};\n\tmov.b64 c, {%3, %4};\n\t"
+        "fma.rn.f32x2 x, x, %2, c;\n\tmov.b64 {%0, %1}, x;\n\t}"
+        : "+f"(x0), "+f"(x1)
+        : "l"(b), "f"(c0), "f"(c1));
+}
+
+// (a0, a1) <- (a0, a1) * (x0, x1).
+__device__ __forceinline__ void mul_f32x2(float &a0, float &a1, float x0, float x1) {
+    asm("{\n\t.reg .b64 a, x;\n\tmov.b64 a, {%0, %1};\n\tmov.b64 x, {%2, %3};\n\t"
+        "mul.rn.f32x2 a, a, x;\n\tmov.b64 {%0, %1}, a;\n\t}"
+        : "+f"(a0), "+f"(a1)
+        : "f"(x0), "f"(x1));
+}
+
+// (a0, a1) <- (a0, a1) + (x0, x1).
+__device__ __forceinline__ void add_f32x2(float &a0, float &a1, float x0, float x1) {
+    asm("{\n\t.reg .b64 a, x;\n\tmov.b64 a, {%0, %1};\n\tmov.b64 x, {%2, %3};\n\t"
+        "add.rn.f32x2 a, a, x;\n\tmov.b64 {%0, %1}, a;\n\t}"
+        : "+f"(a0), "+f"(a1)
+        : "f"(x0), "f"(x1));
+}
+
+// (x0, x1) <- (x0, x1) * b  with b a splatted pair.
+__device__ __forceinline__ void mul_f32x2(float &x0, float &x1, uint64_t b) {
+    asm("{\n\t.reg .b64 x;\n\tmov.b64 x, {%0, %1};\n\tmul.rn.f32x2 x, x, %2;\n\t"
+        "mov.b64 {%0, %1}, x;\n\t}"
+        : "+f"(x0), "+f"(x1)
+        : "l"(b));
+}
+
+// max(a, b, c) in one instruction (sm_100+).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
 // Four fp32 -> four e4m3 bytes (round to nearest even, finite values beyond 448
 // saturate); a lands in bits 0-7, b in 8-15, c in 16-23, e in 24-31.
 __device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float e) {
