@@ -484,7 +484,10 @@ __global__ void __launch_bounds__(448, 1)
             mbar_arrive(bar_ds_full);
         }
         // ------------------------------------------------------- dK, dV epilogue
-        ok = ok && mbar_wait_warp(bar_done, 0, g, SITE_BWD_EPILOGUE);
+        // dK and dV are final once the last block's dV/dK products are done
+        // (pd_free); the last dQ^T product, which reads only K and dS^T, still runs
+        // while they leave through the Q/dO ring.
+        ok = ok && mbar_wait_warp(bar_pd_free, (n_it - 1) & 1, g, SITE_BWD_EPILOGUE);
         if (ok) {
             tc_fence_after();
             // Each thread owns half a key row (d columns [64h, min(64h + 64, D))).  Rows are
