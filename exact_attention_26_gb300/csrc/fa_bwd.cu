@@ -55,71 +55,99 @@ __global__ void __launch_bounds__(256)
                       const float *__restrict__ lse, float *__restrict__ delta,
                       float *__restrict__ lse2, float *__restrict__ dq, int N, int Npad, int BH,
                       int H, const int *__restrict__ cu_seqlens, int total_tokens) {
+    // A warp takes RPW consecutive rows at a time (Npad is a multiple of 128, so they
+    // share a head) and issues all their loads before any arithmetic: the kernel is
+    // bound by HBM, and one row of O and dO per warp leaves too few bytes in flight.
+    constexpr int RPW = 4;
     constexpr int PER = D / 32;  // elements per lane
+    constexpr int W = PER == 3 ? 3 : PER / 2;  // loaded words: bf16 pairs, or 3 halves at d = 96
     const int lane = threadIdx.x & 31;
     const long long warp0 = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
-    const long long rows = (long long)BH * Npad;
+    const long long groups = (long long)BH * Npad / RPW;
     constexpr float kLog2e = 1.4426950408889634074f;
-    for (long long r = warp0; r < rows; r += nwarps) {
-        const int bh = (int)(r / Npad);
-        const int i = (int)(r % Npad);
+    for (long long gidx = warp0; gidx < groups; gidx += nwarps) {
+        const long long r0 = gidx * RPW;
+        const int bh = (int)(r0 / Npad);
+        const int i0 = (int)(r0 % Npad);
         int len = N;
-        size_t row_i, lse_i;  // element offset of row i, index of its L
+        size_t row0, lse0;  // element offset of row i0, index of its L
         if constexpr (VARLEN) {
             const int b = bh / H, h = bh % H;
             const int a = cu_seqlens[b], e = cu_seqlens[b + 1];
             len = (a >= 0 && e >= a && e <= total_tokens && e - a <= N) ? e - a : 0;
-            row_i = ((size_t)(a + i) * H + h) * D;
-            lse_i = (size_t)h * total_tokens + a + i;
+            row0 = ((size_t)(a + i0) * H + h) * D;
+            lse0 = (size_t)h * total_tokens + a + i0;
         } else {
-            row_i = ((size_t)bh * N + i) * D;
-            lse_i = (size_t)bh * N + i;
+            row0 = ((size_t)bh * N + i0) * D;
+            lse0 = (size_t)bh * N + i0;
         }
-        if (i < len) {
-            float acc = 0.f;
+        const size_t rstride = VARLEN ? (size_t)H * D : (size_t)D;  // between consecutive rows
+        uint32_t ow[RPW][W], dw[RPW][W];
+        float lv[RPW];
+#pragma unroll
+        for (int k = 0; k < RPW; ++k) {
+            const bool on = i0 + k < len;
+            const size_t row = row0 + (size_t)k * rstride;
             if constexpr (PER == 3) {
-                // d = 96: lane takes columns lane, lane + 32, lane + 64 (each load of
-                // the warp reads 64 contiguous bytes)
+                // d = 96: lane takes columns lane, lane + 32, lane + 64 (each load of the
+                // warp reads 64 contiguous bytes)
 #pragma unroll
                 for (int e = 0; e < 3; ++e) {
-                    const size_t c = row_i + (size_t)(lane + 32 * e);
-                    acc = fmaf(__bfloat162float(o[c]), __bfloat162float(dout[c]), acc);
-                    dq[c] = 0.f;
+                    const size_t c = row + (size_t)(lane + 32 * e);
+                    ow[k][e] = on ? (uint32_t)__bfloat16_as_ushort(o[c]) << 16 : 0u;
+                    dw[k][e] = on ? (uint32_t)__bfloat16_as_ushort(dout[c]) << 16 : 0u;
                 }
             } else if constexpr (PER == 4) {
-                const size_t row = row_i + (size_t)lane * PER;
-                const uint2 a = *reinterpret_cast<const uint2 *>(o + row);
-                const uint2 b = *reinterpret_cast<const uint2 *>(dout + row);
-                const __nv_bfloat162 *pa = reinterpret_cast<const __nv_bfloat162 *>(&a);
-                const __nv_bfloat162 *pb = reinterpret_cast<const __nv_bfloat162 *>(&b);
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const float2 fa = __bfloat1622float2(pa[e]);
-                    const float2 fb = __bfloat1622float2(pb[e]);
-                    acc = fmaf(fa.x, fb.x, acc);
-                    acc = fmaf(fa.y, fb.y, acc);
-                }
-                *reinterpret_cast<float4 *>(dq + row) = make_float4(0.f, 0.f, 0.f, 0.f);
+                const size_t c = row + (size_t)lane * PER;
+                const uint2 a = on ? *reinterpret_cast<const uint2 *>(o + c) : make_uint2(0u, 0u);
+                const uint2 b = on ? *reinterpret_cast<const uint2 *>(dout + c) : make_uint2(0u, 0u);
+                ow[k][0] = a.x; ow[k][1] = a.y;
+                dw[k][0] = b.x; dw[k][1] = b.y;
             } else {
                 static_assert(PER == 2, "head dim 64, 96 or 128");
-                const size_t row = row_i + (size_t)lane * PER;
-                const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162 *>(o + row);
-                const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162 *>(dout + row);
-                const float2 fa = __bfloat1622float2(a);
-                const float2 fb = __bfloat1622float2(b);
-                acc = fmaf(fa.x, fb.x, fmaf(fa.y, fb.y, 0.f));
-                *reinterpret_cast<float2 *>(dq + row) = make_float2(0.f, 0.f);
+                const size_t c = row + (size_t)lane * PER;
+                ow[k][0] = on ? *reinterpret_cast<const uint32_t *>(o + c) : 0u;
+                dw[k][0] = on ? *reinterpret_cast<const uint32_t *>(dout + c) : 0u;
+            }
+            lv[k] = (on && lane == 0) ? lse[lse0 + k] : 0.f;
+        }
+#pragma unroll
+        for (int k = 0; k < RPW; ++k) {
+            const long long r = r0 + k;
+            const size_t row = row0 + (size_t)k * rstride;
+            float acc = 0.f;
+            if constexpr (PER == 3) {
+#pragma unroll
+                for (int e = 0; e < 3; ++e)
+                    acc = fmaf(__uint_as_float(ow[k][e]), __uint_as_float(dw[k][e]), acc);
+            } else {
+#pragma unroll
+                for (int e = 0; e < W; ++e) {
+                    acc = fmaf(__uint_as_float(ow[k][e] << 16), __uint_as_float(dw[k][e] << 16), acc);
+                    acc = fmaf(__uint_as_float(ow[k][e] & 0xffff0000u),
+                               __uint_as_float(dw[k][e] & 0xffff0000u), acc);
+                }
             }
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-            if (lane == 0) {
-                delta[r] = -acc;
-                lse2[r] = -(lse[lse_i] * kLog2e);
+            if (i0 + k < len) {
+                if constexpr (PER == 3) {
+#pragma unroll
+                    for (int e = 0; e < 3; ++e) dq[row + lane + 32 * e] = 0.f;
+                } else if constexpr (PER == 4) {
+                    *reinterpret_cast<float4 *>(dq + row + lane * PER) = make_float4(0.f, 0.f, 0.f, 0.f);
+                } else {
+                    *reinterpret_cast<float2 *>(dq + row + lane * PER) = make_float2(0.f, 0.f);
+                }
+                if (lane == 0) {
+                    delta[r] = -acc;
+                    lse2[r] = -(lv[k] * kLog2e);
+                }
+            } else if (lane == 0) {
+                delta[r] = 0.f;
+                lse2[r] = -INFINITY;
             }
-        } else if (lane == 0) {
-            delta[r] = 0.f;
-            lse2[r] = -INFINITY;
         }
     }
 }
@@ -614,7 +642,7 @@ template <int D, bool CAUSAL, bool VARLEN>
 int launch_bwd_t(const BwdParams &p, cudaStream_t stream) {
     {
         const long long rows = (long long)p.BH * p.Npad;
-        long long blocks = (rows * 32 + 255) / 256;
+        long long blocks = (rows / 4 * 32 + 255) / 256;  // a warp per group of four rows
         const long long cap = (long long)p.num_sms * 16;
         if (blocks > cap) blocks = cap;
         if (blocks < 1) blocks = 1;
