@@ -121,6 +121,24 @@ def recorded_traffic(kernel_key):
         return None
 
 
+# ------------------------------------------------------------------ ranks
+
+def max_over_ranks(x, world, device):
+    """The largest of every rank's value (the slowest rank sets the job's time)."""
+    if world == 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(flops_per_rank_step, world, step_ms):
+    """Whole-job throughput: every rank ran its own copy of the step (weak scaling)."""
+    return flops_per_rank_step * world / (step_ms * 1e-3) / 1e12
+
+
 # ------------------------------------------------------------------ clocks
 
 class ClockSampler:
@@ -250,13 +268,9 @@ def run_ours(args, rank, world, local_rank):
     fwd_ms = [e[0].elapsed_time(e[1]) for e in evs]
     bwd_ms = [e[1].elapsed_time(e[2]) for e in evs]
     step_ms_local = sum(fwd_ms) / len(fwd_ms) + sum(bwd_ms) / len(bwd_ms)
-    step_ms = step_ms_local
-    if world > 1:
-        t = torch.tensor([step_ms_local], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        step_ms = float(t.item())
+    step_ms = max_over_ranks(step_ms_local, world, dev)
     flops_step = fwd_flops(B, H, N, d, causal) + bwd_flops(B, H, N, d, causal)
-    value = flops_step * world / (step_ms * 1e-3) / 1e12
+    value = job_tflops(flops_step, world, step_ms)
 
     result = None
     if rank == 0:
@@ -296,12 +310,9 @@ def run_ours(args, rank, world, local_rank):
     # End-to-end through the public API with host buffers: H2D of q, k, v, dO from
     # pinned memory, forward, backward, D2H of o, lse, dq, dk, dv, every step.
     e2e = run_e2e(args, fa, torch, dev, (q_h, k_h, v_h, do_h), causal, flops_step, world)
-    if world > 1:
-        t = torch.tensor([e2e["ms"]], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e["ms"] = float(t.item())
+    e2e["ms"] = max_over_ranks(e2e["ms"], world, dev)
     if rank == 0:
-        result["e2e"] = {"value": round(flops_step * world / (e2e["ms"] * 1e-3) / 1e12, 2),
+        result["e2e"] = {"value": round(job_tflops(flops_step, world, e2e["ms"]), 2),
                          "unit": UNIT, "h2d_bytes_per_step": e2e["h2d"],
                          "d2h_bytes_per_step": e2e["d2h"], "ms_per_step": round(e2e["ms"], 5),
                          "pipelined": "HostPipeline: 2 steps in flight, H2D / kernels / D2H on "

@@ -9,3 +9,4 @@ from .fa import (FaError, backward, backward_varlen, decode, decode_paged, fa_bw
                  fa_decode_workspace_bytes, fa_device_status, fa_fwd, fa_fwd_fp8, fa_fwd_varlen,
                  fa_quantize_fp8, fa_quantize_fp8_workspace_bytes, fa_status_string, forward,
                  forward_fp8, forward_varlen, load, quantize_fp8)
+from .pipeline import HostPipeline  # noqa: F401,E402
