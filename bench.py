@@ -325,6 +325,7 @@ def run_ours(args, rank, world, local_rank):
                                                           load_peaks())
             result["decode_workloads"] = sweep_decode(fa, torch, dev, flush, load_peaks())
             result["fp8_workloads"] = sweep_fp8(fa, torch, dev, flush, load_peaks())
+            result["gqa_varlen_workloads"] = sweep_gqa_varlen(fa, torch, dev, flush, load_peaks())
         if world == 1 and not args.no_cpu_baseline:
             result["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
         else:
@@ -476,6 +477,66 @@ def sweep_decode(fa, torch, dev, flush, peaks):
                                   "peak": peaks["hbm_gbs"], "unit": "GB/s",
                                   "frac": round(gbs / peaks["hbm_gbs"], 4)}}
         del q, kc, vc, bt, o, lse, ws
+    return out
+
+
+# Grouped-query attention (query heads sharing key/value heads) and packed sequences
+# of mixed lengths, forward and backward.
+GQA_WORKLOADS = [
+    ("B2_H32_Hkv8_N4096_d128_causal", 2, 32, 8, 4096, 128, True),
+]
+# 16 packed sequences, lengths drawn uniformly from [256, 8192] (torch generator seed 0,
+# sorted), token-major, 16 query heads over 4 key/value heads, d = 128, causal.
+VARLEN_WORKLOAD = ("T_mix16_256to8192_H16_Hkv4_d128_causal", 16, 256, 8192, 16, 4, 128, True)
+
+
+def varlen_lengths(n, lo, hi, seed=0):
+    import torch
+    g = torch.Generator().manual_seed(seed)
+    return sorted(int(x) for x in torch.randint(lo, hi + 1, (n,), generator=g))
+
+
+def sweep_gqa_varlen(fa, torch, dev, flush, peaks):
+    """GQA and packed variable-length calls; FLOPs count every query head's products
+    (and, packed, each sequence's own N^2), the same convention as the fixed shapes."""
+    from exact_attention_26_gb300.inputs import gqa_qkv, varlen_qkv
+    out = {}
+    pk = peaks["bf16_tflops"]
+
+    def entry(ms_f, ms_b, ffl, bfl):
+        tf, tb = ffl / (ms_f * 1e-3) / 1e12, bfl / (ms_b * 1e-3) / 1e12
+        return {"fwd_ms": round(ms_f, 5), "fwd_tflops": round(tf, 2), "fwd_frac_of_peak": round(tf / pk, 4),
+                "bwd_ms": round(ms_b, 5), "bwd_tflops": round(tb, 2), "bwd_frac_of_peak": round(tb / pk, 4)}
+
+    for name, B, H, Hkv, N, d, causal in GQA_WORKLOADS:
+        q, k, v, do = (t.to(dev) for t in gqa_qkv(B, H, Hkv, N, d, seed=0, with_do=True))
+        o = torch.empty_like(q)
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+        g = [torch.empty(t.shape, dtype=torch.float32, device=dev) for t in (q, k, v)]
+        ws = torch.empty(fa.fa_bwd_workspace_bytes(B, H, N, d), dtype=torch.uint8, device=dev)
+        ms_f = _time_call(torch, dev, lambda: fa.forward(q, k, v, causal=causal, out=o, lse=lse), flush)
+        ms_b = _time_call(torch, dev, lambda: fa.backward(q, k, v, o, lse, do, causal=causal, dq=g[0],
+                                                          dk=g[1], dv=g[2], workspace=ws), flush)
+        out[name] = entry(ms_f, ms_b, fwd_flops(B, H, N, d, causal), bwd_flops(B, H, N, d, causal))
+        del q, k, v, do, o, lse, g, ws
+    name, n, lo, hi, H, Hkv, d, causal = VARLEN_WORKLOAD
+    lens = varlen_lengths(n, lo, hi)
+    q, k, v, cu = varlen_qkv(lens, H, Hkv, d, seed=0)
+    gen = torch.Generator().manual_seed(1)
+    do = torch.randn(q.shape, generator=gen).to(torch.bfloat16)
+    q, k, v, cu, do = (t.to(dev) for t in (q, k, v, cu, do))
+    mx = max(lens)
+    o, lse = fa.forward_varlen(q, k, v, cu, mx, causal=causal)
+    g = [torch.empty(t.shape, dtype=torch.float32, device=dev) for t in (q, k, v)]
+    ws = torch.empty(fa.fa_bwd_workspace_bytes(n, H, mx, d), dtype=torch.uint8, device=dev)
+    ms_f = _time_call(torch, dev, lambda: fa.forward_varlen(q, k, v, cu, mx, causal=causal, out=o,
+                                                            lse=lse), flush)
+    ms_b = _time_call(torch, dev, lambda: fa.backward_varlen(q, k, v, o, lse, do, cu, mx, causal=causal,
+                                                             dq=g[0], dk=g[1], dv=g[2], workspace=ws),
+                      flush)
+    ffl = sum(fwd_flops(1, H, L, d, causal) for L in lens)
+    bfl = sum(bwd_flops(1, H, L, d, causal) for L in lens)
+    out[name] = dict(entry(ms_f, ms_b, ffl, bfl), tokens=int(sum(lens)), max_seqlen=mx)
     return out
 
 

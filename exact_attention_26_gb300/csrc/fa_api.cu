@@ -94,6 +94,23 @@ int make_thd_map(CUtensorMap *map, const void *ptr, int T, int heads, int d, int
     return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
 }
 
+// 3-D map over a packed token-major fp32 [T][heads][d] tensor (the varlen dQ),
+// unswizzled: a box of d columns x 1 head x `box_rows` tokens is a row-major
+// [box_rows][d] tile in shared memory.  Used for tiled bulk adds.
+int make_thd_map_f32(CUtensorMap *map, const void *ptr, int T, int heads, int d, int box_rows) {
+    auto enc = encode_tiled();
+    if (!enc) return FA_ERR_CUDA;
+    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)heads, (cuuint64_t)T};
+    cuuint64_t strides[2] = {(cuuint64_t)d * 4, (cuuint64_t)heads * (cuuint64_t)d * 4};
+    cuuint32_t box[3] = {(cuuint32_t)d, 1, (cuuint32_t)box_rows};
+    cuuint32_t elem_strides[3] = {1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void *>(ptr), dims,
+                     strides, box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
+}
+
 // 3-D map over bytes (e4m3 codes): dims x (innermost), y, z with the given row and
 // plane pitches (multiples of 16 bytes); boxes of box_x (128: one swizzle span) by
 // box_y by 1; elements past the dims read as zeros.
@@ -415,6 +432,7 @@ extern "C" int fa_bwd_varlen(const void *q, const void *k, const void *v, const 
     if ((rc = make_thd_map(&p.tm_do, dout, total_tokens, H, d, q_rows)) != FA_OK) return rc;
     if ((rc = make_thd_map(&p.tm_k, k, total_tokens, Hkv, d, 128)) != FA_OK) return rc;
     if ((rc = make_thd_map(&p.tm_v, v, total_tokens, Hkv, d, 128)) != FA_OK) return rc;
+    if ((rc = make_thd_map_f32(&p.tm_dq, dq, total_tokens, H, d, q_rows)) != FA_OK) return rc;
     p.o = o;
     p.dout = dout;
     p.lse = lse;

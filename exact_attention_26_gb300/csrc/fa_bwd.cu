@@ -212,6 +212,7 @@ template <int D, bool CAUSAL, bool VARLEN>
 __global__ void __launch_bounds__(448, 1)
     fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                       const __grid_constant__ CUtensorMap tm_dq,
                        const float *__restrict__ ws_lse2, const float *__restrict__ ws_delta,
                        float *__restrict__ dq, float *__restrict__ dk, float *__restrict__ dv, int N,
                        int Npad, int BHkv, int H, int group, const int *__restrict__ cu_seqlens,
@@ -311,6 +312,7 @@ __global__ void __launch_bounds__(448, 1)
         tma_prefetch_desc(&tm_k);
         tma_prefetch_desc(&tm_v);
         tma_prefetch_desc(&tm_do);
+        if (VARLEN) tma_prefetch_desc(&tm_dq);
     }
     tc_fence_before();
     __syncthreads();
@@ -598,14 +600,16 @@ __global__ void __launch_bounds__(448, 1)
                 const int rows = min(BQ, len - q0);
                 if constexpr (VARLEN) {
                     // token-major dQ: the block's rows of this head are H * D floats
-                    // apart, so each lane adds its own rows
-                    ok0 = mbar_wait_warp(bar_stg_full, it & 1, g, SITE_BWD_DQ_FULL);
-                    if (ok0) {
-                        const int hq = (bhq0 + gq) % H;
-                        for (int i = lane; i < rows; i += 32)
-                            bulk_reduce_add_f32(dq + ((size_t)(tok0 + q0 + i) * H + hq) * D,
-                                                sStage + (uint32_t)(i * D * 4), (uint32_t)(D * 4));
-                        bulk_commit_group();
+                    // apart; one tiled add through the (d, heads, T) tensor map writes
+                    // all of them.  Rows of the block past the sequence's end hold exact
+                    // zeros (their P is 0), so adding them into the next sequence's rows
+                    // leaves those unchanged; rows past T are skipped by the copy.
+                    if (lane == 0) {
+                        ok0 = mbar_wait(bar_stg_full, it & 1, g, SITE_BWD_DQ_FULL);
+                        if (ok0) {
+                            tma_reduce_add_3d(&tm_dq, sStage, 0, (bhq0 + gq) % H, tok0 + q0);
+                            bulk_commit_group();
+                        }
                     }
                 } else {
                     if (lane == 0) {
@@ -661,7 +665,7 @@ int launch_bwd_t(const BwdParams &p, cudaStream_t stream) {
                                  (int)W::SMEM_BYTES) != cudaSuccess)
             return FA_ERR_CUDA;
         kern<<<(unsigned)grid, W::THREADS, W::SMEM_BYTES, stream>>>(
-            p.tm_q, p.tm_k, p.tm_v, p.tm_do, p.ws_lse2, p.ws_delta, p.dq, p.dk, p.dv, p.N, p.Npad,
+            p.tm_q, p.tm_k, p.tm_v, p.tm_do, p.tm_dq, p.ws_lse2, p.ws_delta, p.dq, p.dk, p.dv, p.N, p.Npad,
             p.BH / p.group, p.H, p.group, p.cu_seqlens, p.total_tokens, p.scale, p.scale_log2,
             p.status, p.limit_ns);
     }

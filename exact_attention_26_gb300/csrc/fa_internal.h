@@ -76,6 +76,7 @@ int bwd_block_q(int d);
 
 struct BwdParams {
     CUtensorMap tm_q, tm_k, tm_v, tm_do;  // 3-D maps over [BH][N][d] (q, do), [B*Hkv][N][d] (k, v)
+    CUtensorMap tm_dq;                    // varlen: fp32 dq (d, heads, T), box (d, 1, 64 rows)
     const void *o, *dout;                 // bf16 [BH][N][d]
     const float *lse;                     // fp32 [BH][N]
     float *dq, *dk, *dv;                  // fp32 [BH][N][d]

@@ -145,6 +145,17 @@ __device__ __forceinline__ void bulk_reduce_add_f32(void *dst, uint32_t src, uin
 }
 
 // Plain bulk copy shared -> global (async proxy); size and addresses 16-byte aligned.
+// Tiled bulk add of a shared-memory box into global memory through a tensor map
+// (fp32 elements; rows outside the tensor are skipped).  Completes in a bulk group.
+__device__ __forceinline__ void tma_reduce_add_3d(const void *tmap, uint32_t src, int x, int y,
+                                                  int z) {
+    asm volatile(
+        "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group"
+        " [%0, {%2, %3, %4}], [%1];" ::"l"(tmap),
+        "r"(src), "r"(x), "r"(y), "r"(z)
+        : "memory");
+}
+
 __device__ __forceinline__ void bulk_store(void *dst, uint32_t src, uint32_t bytes) {
     asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst),
                  "r"(src), "r"(bytes)
