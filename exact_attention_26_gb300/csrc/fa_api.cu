@@ -669,12 +669,13 @@ extern "C" const char *fa_status_string(int status) {
         case FA_OK: return "FA_OK";
         case FA_ERR_INVALID_ARG: return "FA_ERR_INVALID_ARG: invalid argument";
         case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED: head dimension not supported";
-        case FA_ERR_MISALIGNED: return "FA_ERR_MISALIGNED: pointer not 16-byte aligned";
+        case FA_ERR_MISALIGNED: return "FA_ERR_MISALIGNED: pointer not aligned (16 bytes for tensors)";
         case FA_ERR_CUDA: return "FA_ERR_CUDA: CUDA runtime or driver call failed";
         case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT: a bounded in-kernel wait ran out";
         case FA_ERR_WORKSPACE: return "FA_ERR_WORKSPACE: workspace missing or too small";
         case FA_ERR_BAD_INDEX:
-            return "FA_ERR_BAD_INDEX: a block-table entry or sequence length was out of range";
+            return "FA_ERR_BAD_INDEX: a block-table entry, sequence length or sequence offset "
+                   "was out of range";
         default: return "unknown fa_status";
     }
 }

@@ -28,8 +28,15 @@
 // Warp roles (128 NT + 64 threads):
 //   warpgroup t (t < NT)  softmax of tile t: thread r owns query row r (TMEM lane
 //                         r); rescale of O_t; epilogue O = O_t/l -> bf16, L
-//   warp 4 NT             TMEM allocator; lane 0 issues every MMA and commit
+//   warp 4 NT             TMEM allocator; one elected lane issues every MMA and
+//                         commit (the whole warp runs the loop, warp-uniform)
 //   warp 4 NT + 1         TMA producer (lane 0): Q tiles, then K_j/V_j into a ring
+//
+// CTAs are persistent (one per SM): each walks a list of work items (NT query
+// tiles of one head) longest first in snake order, with barrier phases carried
+// across items.  The e4m3 variant (F8) runs the same pipeline with 8-bit operands
+// in both products and P rounded to e4m3; packed sequences (VARLEN) read
+// token-major tensors through (d, heads, tokens) tensor maps.
 //
 // Causal tiles above the diagonal are never loaded or multiplied; the diagonal
 // and the ragged tail (keys >= N) are masked to -inf element by element, other

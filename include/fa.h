@@ -20,8 +20,10 @@
  *  - Tensors are DEVICE pointers in the caller's CUDA context, contiguous,
  *    row-major [B][H][N][d] for q, k, v, o, dout, dq, dk, dv and [B][H][N] for lse.
  *    q, k, v, o, dout hold bfloat16 values (raw 16-bit __nv_bfloat16 bits);
- *    lse, dq, dk, dv hold float32.
- *  - Every pointer must be 16-byte aligned (FA_ERR_MISALIGNED otherwise).
+ *    lse, dq, dk, dv hold float32.  Entry points with other layouts (grouped
+ *    key/value heads, packed sequences, decode caches, e4m3 codes) say so.
+ *  - Tensor pointers must be 16-byte aligned, small int32/fp32 index and scale
+ *    arrays 4-byte aligned (FA_ERR_MISALIGNED otherwise).
  *  - The caller owns every buffer.  The library allocates no device memory per
  *    call; it keeps a small per-device cache (SM count, an 8-byte device status
  *    word that lives in the library's own device data).
@@ -50,8 +52,9 @@ typedef enum {
     FA_ERR_CUDA = 4,        /* a CUDA runtime/driver call failed */
     FA_ERR_TIMEOUT = 5,     /* a bounded in-kernel wait ran out (device status) */
     FA_ERR_WORKSPACE = 6,   /* workspace missing or smaller than required */
-    FA_ERR_BAD_INDEX = 7    /* device status: a block-table entry or sequence length out
-                               of range (paged decode); that CTA wrote nothing */
+    FA_ERR_BAD_INDEX = 7    /* device status: a block-table entry, sequence length or
+                               cu_seqlens offset out of range (paged decode, packed
+                               sequences); the affected work wrote nothing */
 } fa_status;
 
 /*
