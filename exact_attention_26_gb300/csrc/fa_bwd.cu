@@ -60,6 +60,7 @@ __global__ void __launch_bounds__(256)
     // bound by HBM, and one row of O and dO per warp leaves too few bytes in flight.
     constexpr int RPW = 4;
     constexpr int PER = D / 32;  // elements per lane
+    griddep_launch_dependents();  // the main kernel may set up while this one runs
     constexpr int W = PER == 3 ? 3 : PER / 2;  // loaded words: bf16 pairs, or 3 halves at d = 96
     const int lane = threadIdx.x & 31;
     const long long warp0 = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -343,6 +344,8 @@ __global__ void __launch_bounds__(448, 1)
                 tma_load_3d(sV + c * T::K_CHUNK, &tm_v, bar_kv_full, c * 64, VARLEN ? hk : kv0,
                             VARLEN ? tok0 + kv0 : kvh);
             }
+            // the -L log2e and -D vectors come from the preprocess kernel
+            griddep_wait();
             int issued = 0;
             for (int it = 0, qb = 0, gq = 0; it < n_it; ++it, (++qb == n_qit) ? (qb = 0, ++gq) : 0) {
                 const int s = it % QS;
@@ -574,6 +577,7 @@ __global__ void __launch_bounds__(448, 1)
     } else {
         // ------------------------------------------------------- dQ readout (warps 8-11)
         const int t = threadIdx.x - 256;  // TMEM lane = column d of dQ
+        if (warp == 8) griddep_wait();    // dQ was zeroed by the preprocess kernel
         const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
         bool ok = true;
         for (int it = 0, qb = 0, gq = 0; it < n_it; ++it, (++qb == n_qit) ? (qb = 0, ++gq) : 0) {
@@ -683,11 +687,24 @@ int launch_bwd_t(const BwdParams &p, cudaStream_t stream) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)W::SMEM_BYTES) != cudaSuccess)
             return FA_ERR_CUDA;
-        kern<<<(unsigned)grid, W::THREADS, W::SMEM_BYTES, stream>>>(
-            p.tm_q, p.tm_k, p.tm_v, p.tm_do, p.tm_dq, p.ws_lse2, p.ws_delta, p.dq, p.dk, p.dv, p.N, p.Npad,
-            p.BH / p.group, p.H, p.group, head_group, p.cu_seqlens, p.total_tokens, p.scale,
-            p.scale_log2,
-            p.status, p.limit_ns);
+        // Launched as a programmatic dependent of the preprocess kernel: its CTAs set
+        // up (barriers, tensor memory, K/V loads) while the preprocess finishes, and
+        // wait for it only where they read its results.
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)grid);
+        cfg.blockDim = dim3(W::THREADS);
+        cfg.dynamicSmemBytes = W::SMEM_BYTES;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaLaunchKernelEx(&cfg, kern, p.tm_q, p.tm_k, p.tm_v, p.tm_do, p.tm_dq, p.ws_lse2,
+                               p.ws_delta, p.dq, p.dk, p.dv, p.N, p.Npad, p.BH / p.group, p.H,
+                               p.group, head_group, p.cu_seqlens, p.total_tokens, p.scale,
+                               p.scale_log2, p.status, p.limit_ns) != cudaSuccess)
+            return FA_ERR_CUDA;
     }
     return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }

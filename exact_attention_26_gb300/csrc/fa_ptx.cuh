@@ -145,6 +145,14 @@ __device__ __forceinline__ void bulk_reduce_add_f32(void *dst, uint32_t src, uin
 }
 
 // Plain bulk copy shared -> global (async proxy); size and addresses 16-byte aligned.
+// Programmatic dependent launch: the next kernel on the stream may start launching
+// once every CTA of this grid has signalled (or exited); a kernel launched that way
+// waits for the previous grid to complete, and its writes to be visible, here.
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // Tiled bulk add of a shared-memory box into global memory through a tensor map
 // (fp32 elements; rows outside the tensor are skipped).  Completes in a bulk group.
 __device__ __forceinline__ void tma_reduce_add_3d(const void *tmap, uint32_t src, int x, int y,
