@@ -101,6 +101,7 @@ template <int D, int QB, bool PAGED>
 __global__ void __launch_bounds__(DecTile<D>::THREADS, 2)
     fa_decode_split_kernel(const __grid_constant__ DecodeParams p) {
     using T = DecTile<D>;
+    griddep_launch_dependents();  // the merge kernel may launch while the ranges run
     constexpr int E = T::E, KW = T::KW, BK = T::BK, STAGES = T::STAGES;
     extern __shared__ __align__(128) uint8_t smem[];
     const uint32_t sbase = smem_u32(smem);
@@ -389,6 +390,7 @@ __global__ void __launch_bounds__(128)
                              __nv_bfloat16 *__restrict__ o, float *__restrict__ lse, long long rows,
                              int R, int S, int Nq, int H, int Hkv, int group) {
     constexpr int E = DecTile<D>::E;
+    griddep_wait();  // every key range's partial result is written
     const long long row = (long long)blockIdx.x * 4 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (row >= rows) return;
@@ -438,10 +440,21 @@ int launch_decode_t(const DecodeParams &p, cudaStream_t stream) {
     if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
     if (p.S > 1) {
         const long long rows = (long long)(p.BH / p.group) * R;
-        fa_decode_combine_kernel<D><<<(unsigned)((rows + 3) / 4), 128, 0, stream>>>(
-            p.part_o, p.part_l, reinterpret_cast<__nv_bfloat16 *>(p.o), p.lse, rows, R, p.S, p.Nq,
-            p.H, p.Hkv, p.group);
-        if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
+        // a programmatic dependent of the split kernel: launched as its last CTAs
+        // start, it waits for the whole grid before reading the partial results
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)((rows + 3) / 4));
+        cfg.blockDim = dim3(128);
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaLaunchKernelEx(&cfg, fa_decode_combine_kernel<D>, (const float *)p.part_o,
+                               (const float *)p.part_l, reinterpret_cast<__nv_bfloat16 *>(p.o),
+                               p.lse, rows, R, p.S, p.Nq, p.H, p.Hkv, p.group) != cudaSuccess)
+            return FA_ERR_CUDA;
     }
     return FA_OK;
 }
