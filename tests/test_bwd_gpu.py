@@ -129,3 +129,22 @@ def test_bwd_dk_dv_deterministic(fa):
     b = _grads(fa, q, k, v, do, True)
     assert np.array_equal(a[1], b[1]) and np.array_equal(a[2], b[2])
     assert np.allclose(a[0], b[0], atol=1e-5, rtol=0)
+
+
+def test_bwd_long_sequence_65536(fa, orc):
+    """N = 65536 (the longest sequence of the pages' table), B1 H2 d128 causal.  With a
+    causal mask the last 128 keys receive gradient only from the last 128 queries, so
+    the oracle restricted to those rows (plus 16 sampled rows for dQ) gives their dK,
+    dV exactly; dQ is checked on every row the oracle ran."""
+    from exact_attention_26_gb300.inputs import sample_rows
+    B, H, N, d = 1, 2, 65536, 128
+    q, k, v, do = normal_qkv(B, H, N, d, seed=21, with_do=True)
+    got = _grads(fa, q, k, v, do, True)
+    tail = np.arange(N - 128, N)
+    rows = np.unique(np.concatenate([sample_rows(N, 16, seed=3).numpy(), tail]))
+    rq, rk, rv = orc.bwd_rows(to_f64(q), to_f64(k), to_f64(v), to_f64(do), rows, causal=True)
+    assert_abs_close(got[0][:, :, rows], rq, GRAD_ABS, "65536 dQ rows")
+    assert_abs_close(got[1][:, :, tail], rk[:, :, tail], GRAD_ABS, "65536 dK last keys")
+    assert_abs_close(got[2][:, :, tail], rv[:, :, tail], GRAD_ABS, "65536 dV last keys")
+    dv_sum = got[2].astype(np.float64).sum(axis=2)
+    assert np.max(np.abs(dv_sum - do.double().sum(dim=2).numpy())) < 2.0

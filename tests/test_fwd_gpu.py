@@ -154,3 +154,12 @@ def test_fwd_writes_nothing_outside_outputs(fa):
     for buf in (o_buf, l_buf):
         assert torch.all(buf[:pad] == 7.0) and torch.all(buf[-pad:] == 7.0)
     assert torch.isfinite(o.float()).all() and torch.isfinite(lse).all()
+
+
+@pytest.mark.parametrize("shape", [(1, 2, 65536, 128), (1, 1, 131072, 64)], ids=["65536x128", "131072x64"])
+def test_fwd_long_sequences(fa, orc, shape):
+    """The longest sequences of the pages' table and beyond, causal, sampled rows
+    (row indices times d pass 2^23 here)."""
+    B, H, N, d = shape
+    q, k, v = normal_qkv(B, H, N, d, seed=N + d)
+    _sampled(fa, orc, q, k, v, True, 24)
