@@ -318,9 +318,21 @@ def run_ours(args, rank, world, local_rank):
                          "pipelined": "HostPipeline: 2 steps in flight, H2D / kernels / D2H on "
                                       "separate streams",
                          "serial_ms_per_step": round(e2e["serial_ms"], 5)}
+        rates = unit_rates(fa, torch, dev, clocks)
+        if rates is not None:
+            result["unit_rates"] = rates
+            pk_clk = rates.get("clock_derived_bf16_tflops")
+            if pk_clk:
+                result["roofline"]["peak_clock_derived"] = pk_clk
+                result["roofline"]["frac_clock_derived"] = round(achieved / pk_clk, 4)
+            ex2 = rates.get("ex2_per_sm_clk")
+            if ex2:
+                exps = B * H * N * N * (0.5 if causal else 1.0)  # one ex2 per score, fwd and bwd
+                floor_ms = exps / (ex2 * rates["sms"] * rates["sm_mhz"] * 1e6) * 1e3
+                result["ex2_floor_ms"] = {"fwd": round(floor_ms, 5), "bwd": round(floor_ms, 5)}
         if world == 1 and not args.no_extra:
             result["forward_workloads"] = sweep_forward(fa, torch, dev, flush, normal_qkv,
-                                                        boosted_qkv, load_peaks())
+                                                        boosted_qkv, load_peaks(), rates)
             result["backward_workloads"] = sweep_backward(fa, torch, dev, flush, normal_qkv,
                                                           load_peaks())
             result["decode_workloads"] = sweep_decode(fa, torch, dev, flush, load_peaks())
@@ -408,8 +420,31 @@ def _time_call(torch, dev, fn, flush, iters=20, warm=3):
     return statistics.median(a.elapsed_time(b) for a, b in evs)
 
 
-def sweep_forward(fa, torch, dev, flush, normal_qkv, boosted_qkv, peaks):
+def unit_rates(fa, torch, dev, clocks):
+    """The library's unit-rate probes (dense bf16 MMA and MUFU ex2 per SM clock), run
+    once outside the timed region, and the peaks they give at this GPU's SM count and
+    clocks: the clock-derived tensor peak at the maximum SM clock, the ex2 rate at the
+    median SM clock seen under load."""
+    try:
+        r = fa.probe_unit_rates(2048)
+    except Exception as exc:  # reported, never fatal: the probes are context
+        return {"error": str(exc)}
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    out = {"sms": sms, "mma_bf16_flop_per_sm_clk_n256": round(r["mma_bf16_n256_flop_per_clk"], 1),
+           "mma_bf16_flop_per_sm_clk_n64": round(r["mma_bf16_n64_flop_per_clk"], 1),
+           "ex2_per_sm_clk": round(r["ex2_per_clk"], 2),
+           "sm_max_mhz": clocks.get("sm_max_mhz"), "sm_mhz": clocks.get("sm_mhz")}
+    if out["sm_max_mhz"]:
+        out["clock_derived_bf16_tflops"] = round(
+            r["mma_bf16_n256_flop_per_clk"] * sms * out["sm_max_mhz"] * 1e6 / 1e12, 1)
+    if not out["sm_mhz"]:
+        out["ex2_per_sm_clk"] = None
+    return out
+
+
+def sweep_forward(fa, torch, dev, flush, normal_qkv, boosted_qkv, peaks, rates=None):
     out = {}
+    ex2 = (rates or {}).get("ex2_per_sm_clk")
     for name, B, H, N, d, causal, kind in FWD_WORKLOADS:
         gen = boosted_qkv if kind == "boosted" else normal_qkv
         q, k, v = (t.to(dev) for t in gen(B, H, N, d, seed=0))
@@ -420,6 +455,10 @@ def sweep_forward(fa, torch, dev, flush, normal_qkv, boosted_qkv, peaks):
         tf = fwd_flops(B, H, N, d, causal) / (ms * 1e-3) / 1e12
         out[name] = {"ms": round(ms, 5), "tflops": round(tf, 2),
                      "frac_of_peak": round(tf / peaks["bf16_tflops"], 4)}
+        if ex2:  # the exponential ceiling: one ex2 per score element
+            exps = B * H * N * N * (0.5 if causal else 1.0)
+            out[name]["ex2_floor_ms"] = round(
+                exps / (ex2 * rates["sms"] * rates["sm_mhz"] * 1e6) * 1e3, 5)
         del q, k, v, o, lse
     return out
 

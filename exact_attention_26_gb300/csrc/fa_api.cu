@@ -695,6 +695,20 @@ extern "C" int fa_device_status(void *stream) {
     return rec[0];
 }
 
+extern "C" int fa_probe_unit_rates(double *rates, int iters, void *stream) {
+    if (rates == nullptr || iters < 16 || iters > (1 << 20)) return FA_ERR_INVALID_ARG;
+    DeviceCache *dc = nullptr;
+    int rc = current_device(&dc);
+    if (rc != FA_OK) return rc;
+    rc = run_unit_probes(dc->num_sms, iters, dc->status, static_cast<cudaStream_t>(stream), rates);
+    if (rc == FA_ERR_TIMEOUT) {  // the record is this call's; clear it
+        const int zero[2] = {0, 0};
+        if (cudaMemcpy(dc->status, zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
+            return FA_ERR_CUDA;
+    }
+    return rc;
+}
+
 extern "C" int fa_selftest_wait_timeout(unsigned long long limit_ns, void *stream) {
     if (limit_ns < 1000ull || limit_ns > 5000000000ull) return FA_ERR_INVALID_ARG;
     DeviceCache *dc = nullptr;

@@ -27,7 +27,8 @@ EXPORTED = ("fa_fwd", "fa_bwd", "fa_bwd_workspace_bytes", "fa_status_string", "f
             "fa_selftest_wait_timeout", "fa_decode", "fa_decode_num_splits",
             "fa_decode_workspace_bytes", "fa_decode_paged", "fa_decode_paged_num_splits",
             "fa_decode_paged_workspace_bytes", "fa_fwd_gqa", "fa_bwd_gqa", "fa_fwd_varlen",
-            "fa_bwd_varlen", "fa_quantize_fp8_workspace_bytes", "fa_quantize_fp8", "fa_fwd_fp8")
+            "fa_bwd_varlen", "fa_quantize_fp8_workspace_bytes", "fa_quantize_fp8", "fa_fwd_fp8",
+            "fa_probe_unit_rates")
 
 _vp = ctypes.c_void_p
 _int = ctypes.c_int
@@ -131,6 +132,30 @@ def fa_selftest_wait_timeout(limit_ns: int, stream=None) -> int:
         fn.argtypes = [ctypes.c_ulonglong, _vp]
         fn.restype = _int
     return fn(limit_ns, stream)
+
+
+def fa_probe_unit_rates(rates, iters: int, stream=None) -> int:
+    """Run the unit-rate probes; `rates` is a ctypes array of 3 doubles (host)."""
+    fn = load().fa_probe_unit_rates
+    if fn.argtypes is None:
+        fn.argtypes = [ctypes.POINTER(ctypes.c_double), _int, _vp]
+        fn.restype = _int
+    return fn(rates, iters, stream)
+
+
+def probe_unit_rates(iters: int = 2048, stream=None) -> dict:
+    """Measured per-SM rates on the current device: dense bf16 MMA FLOPs per SM clock
+    at M = 128 with N = 256 and N = 64, and MUFU ex2 results per SM clock."""
+    rates = (ctypes.c_double * 3)()
+    if stream is None:
+        stream = torch.cuda.current_stream().cuda_stream
+    elif isinstance(stream, torch.cuda.Stream):
+        stream = stream.cuda_stream
+    rc = fa_probe_unit_rates(rates, int(iters), stream)
+    if rc != FA_OK:
+        raise FaError(rc, "fa_probe_unit_rates")
+    return {"mma_bf16_n256_flop_per_clk": rates[0], "mma_bf16_n64_flop_per_clk": rates[1],
+            "ex2_per_clk": rates[2]}
 
 
 def fa_fwd_gqa(q, k, v, o, lse, B, H, Hkv, N, d, causal, scale, stream) -> int:

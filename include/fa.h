@@ -327,6 +327,25 @@ size_t fa_decode_paged_workspace_bytes(int B, int H, int Hkv, int Nq, int d, int
  */
 int fa_selftest_wait_timeout(unsigned long long limit_ns, void *stream);
 
+/*
+ * Measurement utility (not on the attention path): the per-SM rates of the units
+ * the kernels are bound by, measured on the current device with one CTA per SM and
+ * clock64 stamps, `iters` iterations per probe (16 <= iters <= 2^20, else
+ * FA_ERR_INVALID_ARG; 2048 takes about a millisecond per probe).  On return
+ * (host array of 3 doubles, the median over SMs):
+ *   rates[0]  dense bf16 tcgen05.mma kind::f16, M = 128, N = 256, K = 16, fp32
+ *             accumulate: FLOPs per SM clock (the tensor core's peak shape);
+ *   rates[1]  the same at N = 64 (the shape of the backward's S^T, dP^T and dQ^T
+ *             products at d = 128);
+ *   rates[2]  MUFU ex2.approx.f32 results per SM clock (the softmax exponential).
+ * Times SM count times SM clock, rates[0] is the clock-derived tensor peak and
+ * rates[2] the exponential ceiling of the forward (one ex2 per score element).
+ * Synchronises `stream`.  Returns FA_ERR_TIMEOUT if an MMA completion wait gave up
+ * (the record is cleared), FA_ERR_UNSUPPORTED above 1024 SMs, FA_ERR_CUDA on a
+ * CUDA error.
+ */
+int fa_probe_unit_rates(double *rates, int iters, void *stream);
+
 /* Static, human-readable name of a status code (never NULL). */
 const char *fa_status_string(int status);
 

@@ -223,3 +223,11 @@ def test_fwd_fp8_rejects_bad_arguments(fa, kw, code):
     a.update(kw)
     assert fa.fa_fwd_fp8(a["q8"], a["k8"], a["vt8"], a["qd"], a["kd"], a["vd"], a["o"], a["lse"], a["B"],
                          a["H"], a["Hkv"], a["N"], a["d"], 1, a["scale"], None) == code
+
+
+def test_probe_rejects_bad_arguments_before_touching_a_device(fa):
+    import ctypes
+    rates = (ctypes.c_double * 3)()
+    assert fa.fa_probe_unit_rates(rates, 15, None) == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_probe_unit_rates(rates, (1 << 20) + 1, None) == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_probe_unit_rates(None, 2048, None) == fa.FA_ERR_INVALID_ARG
