@@ -7,6 +7,7 @@
 #include <mutex>
 
 #include "fa_internal.h"
+#include "fa_probe.h"
 #include "fa_ptx.cuh"
 
 namespace fa {

@@ -37,7 +37,6 @@ enum WaitSite : int {
     SITE_DEC_BAD_LEN = 24,
     SITE_DEC_BAD_PAGE = 25,
     SITE_SELFTEST = 30,
-    SITE_PROBE = 31,
 };
 
 // Default limit of one in-kernel wait.
@@ -115,10 +114,6 @@ struct DecodeParams {
 int launch_fwd(const FwdParams &p, cudaStream_t stream);
 int launch_bwd(const BwdParams &p, cudaStream_t stream);
 int launch_decode(const DecodeParams &p, cudaStream_t stream);
-// Unit-rate probes (fa_probe.cu): runs the N = 256 MMA, N = 64 MMA and ex2 probes
-// (one CTA per SM each), synchronises `stream` and writes the median per-SM rates
-// (FLOP, FLOP, ex2 per SM clock) to rates[3].
-int run_unit_probes(int num_sms, int iters, int *status, cudaStream_t stream, double *rates);
 int decode_block_keys(int d);          // keys per pipeline stage of the decode kernel
 int decode_query_block(int d, int Nq);  // query rows per decode CTA
 int decode_ctas_per_sm(int d, int Nq);  // resident decode CTAs per SM (occupancy query)

@@ -14,6 +14,7 @@
 #include <vector>
 
 #include "fa_internal.h"
+#include "fa_probe.h"
 #include "fa_ptx.cuh"
 
 namespace fa {
