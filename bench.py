@@ -317,7 +317,10 @@ def run_ours(args, rank, world, local_rank):
                          "d2h_bytes_per_step": e2e["d2h"], "ms_per_step": round(e2e["ms"], 5),
                          "pipelined": "HostPipeline: 2 steps in flight, H2D / kernels / D2H on "
                                       "separate streams",
-                         "serial_ms_per_step": round(e2e["serial_ms"], 5)}
+                         "serial_ms_per_step": round(e2e["serial_ms"], 5),
+                         "copy_only_ms_per_step": round(e2e["copy_ms"], 5),
+                         "copy_note": "the step's H2D + D2H bytes on the two copy streams "
+                                      "with no kernels: the host link's bound for e2e"}
         rates = unit_rates(fa, torch, dev, clocks)
         if rates is not None:
             result["unit_rates"] = rates
@@ -394,9 +397,28 @@ def run_e2e(args, fa, torch, dev, host_inputs, causal, flops_step, world):
         step()
     b.record(stream)
     b.synchronize()
+    serial_ms = a.elapsed_time(b) / n
+
+    # the copy bound: the same per-step H2D and D2H on the pipeline's two copy
+    # streams with no kernels (the host link's limit for this step's bytes)
+    sl = pipe.slots[0]
+    dev_out = [sl["o"], sl["lse"]] + sl["g"]
+    a.record(pipe.s_h2d)
+    pipe.s_d2h.wait_stream(pipe.s_h2d)
+    for _ in range(n):
+        with torch.cuda.stream(pipe.s_h2d):
+            for dst, src in zip(sl["in"], pin):
+                dst.copy_(src, non_blocking=True)
+        with torch.cuda.stream(pipe.s_d2h):
+            for dst, src in zip(outs_h, dev_out):
+                dst.copy_(src, non_blocking=True)
+    pipe.s_h2d.wait_stream(pipe.s_d2h)
+    b.record(pipe.s_h2d)
+    b.synchronize()
+    copy_ms = a.elapsed_time(b) / n
     h2d = sum(t.numel() * t.element_size() for t in pin)
     d2h = sum(t.numel() * t.element_size() for t in outs_h)
-    return {"ms": ms, "serial_ms": a.elapsed_time(b) / n, "h2d": h2d, "d2h": d2h}
+    return {"ms": ms, "serial_ms": serial_ms, "copy_ms": copy_ms, "h2d": h2d, "d2h": d2h}
 
 
 def _time_call(torch, dev, fn, flush, iters=20, warm=3):
