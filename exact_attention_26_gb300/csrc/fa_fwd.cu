@@ -48,6 +48,15 @@
 namespace fa {
 namespace {
 
+// One 32-byte global store (sm_100+), a full L2 sector per thread; dst 32-byte
+// aligned.  The epilogue writes each thread's O row with these: a warp's 16-byte
+// stores to 32 different rows leave every sector half written.
+__device__ __forceinline__ void st_global_v8(void *dst, const uint32_t *w) {
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst), "r"(w[0]),
+                 "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+                 : "memory");
+}
+
 constexpr float kRescaleLog2 = 8.0f;
 constexpr float kLn2 = 0.69314718055994530942f;
 
@@ -495,6 +504,9 @@ __global__ void __launch_bounds__(FwdTile<D, F8>::THREADS, 1)
         const int r = threadIdx.x & 127;
         const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
         const uint32_t t_o = tmem + lane_base + T::TM_O0 + D * t;
+        // O rows are D * 2 bytes apart (a multiple of 32): 32-byte stores need only a
+        // 32-byte aligned base (the boundary guarantees 16)
+        const bool out_al32 = (reinterpret_cast<uintptr_t>(out) & 31u) == 0;
         int sc = 0;  // S products of this tile consumed before the current item
         int oc = 0;  // items of this tile finished
         bool ok = true;
@@ -674,10 +686,15 @@ __global__ void __launch_bounds__(FwdTile<D, F8>::THREADS, 1)
                     pk[e] = pack_bf16(__uint_as_float(o[2 * e]) * inv_l,
                                       __uint_as_float(o[2 * e + 1]) * inv_l);
                 if (q_idx < itm.len) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
+                    if (out_al32) {  // two full 32-byte sectors per thread
+                        st_global_v8(orow + c * 32, pk);
+                        st_global_v8(orow + c * 32 + 16, pk + 8);
+                    } else {
+                        uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
 #pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        dst[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+                        for (int e = 0; e < 4; ++e)
+                            dst[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+                    }
                 }
             }
             if (q_idx < itm.len) {

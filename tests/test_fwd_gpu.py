@@ -156,6 +156,26 @@ def test_fwd_writes_nothing_outside_outputs(fa):
     assert torch.isfinite(o.float()).all() and torch.isfinite(lse).all()
 
 
+@pytest.mark.parametrize("d", [64, 96, 128, 256])
+def test_fwd_output_on_a_16_byte_boundary(fa, d):
+    """An O base that is 16- but not 32-byte aligned takes the epilogue's 16-byte
+    stores instead of its 32-byte ones: the same values, and nothing written outside
+    the output."""
+    B, H, N = 1, 2, 300
+    q, k, v = (t.to(DEV) for t in normal_qkv(B, H, N, d, seed=d))
+    ref, ref_l = fa.forward(q, k, v, causal=True)
+    n = B * H * N * d
+    buf = torch.full((n + 64,), 7.0, dtype=torch.bfloat16, device=DEV)
+    off = next(i for i in range(0, 32, 8) if (buf.data_ptr() + 2 * i) % 32 == 16)
+    o = buf[off:off + n].view(B, H, N, d)
+    assert o.data_ptr() % 32 == 16
+    _, lse = fa.forward(q, k, v, causal=True, out=o)
+    torch.cuda.synchronize()
+    assert fa.fa_device_status(None) == 0
+    assert torch.equal(o, ref) and torch.equal(lse, ref_l)
+    assert torch.all(buf[:off] == 7.0) and torch.all(buf[off + n:] == 7.0)
+
+
 @pytest.mark.parametrize("shape", [(1, 2, 65536, 128), (1, 1, 131072, 64)], ids=["65536x128", "131072x64"])
 def test_fwd_long_sequences(fa, orc, shape):
     """The longest sequences of the pages' table and beyond, causal, sampled rows
