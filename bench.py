@@ -660,9 +660,10 @@ def _workload_heads(nheads):
     return tuple(to_f64(t[:, :nheads]) for t in _INPUTS)
 
 
-def _oracle_sample(nrows, nheads=1):
+def _oracle_sample(nrows, nheads=1, nthreads=None):
     """A bounded sample of the step on the CPU: forward and backward of `nrows`
-    seeded query rows in each of the first `nheads` heads of the workload.
+    seeded query rows in each of the first `nheads` heads of the workload, on
+    `nthreads` host threads (default: every core of the affinity mask).
     Returns (seconds, flops, rows, heads)."""
     from exact_attention_26_gb300.inputs import sample_rows
     from oracle import default as oracle_default
@@ -674,8 +675,8 @@ def _oracle_sample(nrows, nheads=1):
     keys = (rows + 1) if causal else np.full(rows.shape, N)
     flops = float(nheads * ((4.0 + 10.0) * d * keys).sum())
     t0 = time.perf_counter()
-    orc.fwd_rows(q, k, v, rows, causal=causal)
-    orc.bwd_rows(q, k, v, do, rows, causal=causal)
+    orc.fwd_rows(q, k, v, rows, causal=causal, nthreads=nthreads)
+    orc.bwd_rows(q, k, v, do, rows, causal=causal, nthreads=nthreads)
     return time.perf_counter() - t0, flops, rows.size, nheads
 
 
@@ -701,11 +702,17 @@ def _sample_size(seconds):
 def cpu_baseline(target_seconds):
     rows, heads = _sample_size(target_seconds)
     secs, flops, n, h = _oracle_sample(rows, heads)
+    # the same oracle on one thread, on a sample about a quarter as long in time
+    rows1 = max(16, min(WORKLOAD["N"], int(rows * heads / max(1, _cores()) / 4)))
+    secs1, flops1, n1, _ = _oracle_sample(rows1, 1, nthreads=1)
     return {"value": round(flops / secs / 1e12, 6), "unit": UNIT, "cores": _cores(),
             "kind": "oracle",
             "sample": f"float64 oracle forward + backward of {n} seeded query rows in each of "
                       f"{h} heads of the workload ({secs:.1f} s on {_cores()} host threads; "
-                      "same FLOP convention)"}
+                      "same FLOP convention)",
+            "single_core": {"value": round(flops1 / secs1 / 1e12, 6), "unit": UNIT, "cores": 1,
+                            "sample": f"{n1} seeded query rows of one head ({secs1:.1f} s on "
+                                      "one host thread)"}}
 
 
 def run_reference(args):
