@@ -180,17 +180,6 @@ __device__ __forceinline__ void bulk_wait_group_read() {
     asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
 }
 
-// Wait until at most N committed bulk groups are still in flight (fully complete).
-template <int N>
-__device__ __forceinline__ void bulk_wait_group() {
-    asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
-}
-
-// Fire-and-forget fp32 add to global memory (no return value).
-__device__ __forceinline__ void red_add_f32(float *addr, float v) {
-    asm volatile("red.global.add.f32 [%0], %1;" ::"l"(addr), "f"(v) : "memory");
-}
-
 // Make generic-proxy writes to shared memory visible to the async proxy (TMA, MMA).
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -222,37 +211,11 @@ __device__ __forceinline__ void tc_fence_after() {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// Arrive once on `bar` when every tcgen05 operation this thread issued so far is done.
-__device__ __forceinline__ void tc_commit(uint32_t bar) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-        : "memory");
-}
-
-// D[tmem] (+)= A[smem] * B[smem]^T, kind::f16 (bf16 in, fp32 accumulate).
-__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                       uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
-// D[tmem] (+)= A[tmem] * B[smem]^T, kind::f16; A is K-major in tensor memory.
-__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                       uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
-// Warp-uniform forms: every lane of the warp executes the call with the same
-// operands and exactly one elected lane issues the instruction.  Keeping the
-// issuing code warp-uniform lets the compiler do the descriptor arithmetic on
-// the uniform datapath instead of per-lane registers, which matters because the
+// D[tmem] (+)= A * B[smem]^T, kind::f16 (bf16 in, fp32 accumulate); A from shared
+// memory (SS) or, K-major, from tensor memory (TS).  Every lane of the warp makes
+// the call with the same operands and one elected lane issues the instruction:
+// warp-uniform issuing code lets the compiler do the descriptor arithmetic on the
+// uniform datapath instead of per-lane registers, which matters because the
 // issuing warp shares its scheduler with busy softmax/compute warps.
 __device__ __forceinline__ void mma_ss_elect(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                              uint32_t idesc, uint32_t accumulate) {
@@ -296,6 +259,8 @@ __device__ __forceinline__ void mma_ts_elect_f8(uint32_t d_tmem, uint32_t a_tmem
         : "memory");
 }
 
+// Arrive once on `bar` when every tcgen05 operation the issuing thread started so
+// far is done (one elected lane of the calling warp commits).
 __device__ __forceinline__ void tc_commit_elect(uint32_t bar) {
     asm volatile(
         "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
