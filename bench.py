@@ -705,6 +705,10 @@ def _sample_size(seconds):
 
 
 def cpu_baseline(target_seconds):
+    step_flops = fwd_flops(WORKLOAD["B"], WORKLOAD["H"], WORKLOAD["N"], WORKLOAD["d"],
+                           WORKLOAD["causal"]) + bwd_flops(WORKLOAD["B"], WORKLOAD["H"],
+                                                           WORKLOAD["N"], WORKLOAD["d"],
+                                                           WORKLOAD["causal"])
     rows, heads = _sample_size(target_seconds)
     secs, flops, n, h = _oracle_sample(rows, heads)
     # the same oracle on one thread, on a sample about a quarter as long in time
@@ -717,7 +721,9 @@ def cpu_baseline(target_seconds):
                       "same FLOP convention)",
             "single_core": {"value": round(flops1 / secs1 / 1e12, 6), "unit": UNIT, "cores": 1,
                             "sample": f"{n1} seeded query rows of one head ({secs1:.1f} s on "
-                                      "one host thread)"}}
+                                      "one host thread)"},
+            # the whole step at the sampled rate (extrapolated, not run)
+            "extrapolated_full_step_s": round(step_flops / (flops / secs), 1)}
 
 
 def run_reference(args):
