@@ -29,7 +29,12 @@ def _worker(rank, world, port, out):
     try:
         local_ms = [0.8, 1.25][rank]
         step_ms = bench.max_over_ranks(local_ms, world, "cpu")
-        out[rank] = (step_ms, bench.job_tflops(1e12, world, step_ms))
+        # only rank 1 saw a thermal slowdown: both ranks must time the region again
+        clocks = [{"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": []},
+                  {"sm_mhz": 1900.0, "sm_max_mhz": 2070.0, "reasons": ["hw_thermal_slowdown"]}]
+        again = bench.max_over_ranks(1.0 if bench.clocks_rejected(clocks[rank]) else 0.0, world,
+                                     "cpu") > 0
+        out[rank] = (step_ms, bench.job_tflops(1e12, world, step_ms), again)
         dist.barrier()
     finally:
         dist.destroy_process_group()
@@ -42,9 +47,23 @@ def test_two_ranks_take_the_slowest_time():
         mp.spawn(_worker, args=(world, port, out), nprocs=world, join=True)
         res = dict(out)
     for rank in range(world):
-        step_ms, tf = res[rank]
+        step_ms, tf, again = res[rank]
         assert step_ms == 1.25
         assert tf == pytest.approx(2 * 1e12 / 1.25e-3 / 1e12)
+        assert again
+
+
+def test_clock_records_that_disqualify_a_timed_region():
+    sys.path.insert(0, ROOT)
+    import bench
+    ok = {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": []}
+    assert not bench.clocks_rejected(ok)
+    assert not bench.clocks_rejected(dict(ok, sm_mhz=1800.0, reasons=["sw_power_cap"]))
+    for why in ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown"):
+        assert bench.clocks_rejected(dict(ok, reasons=[why]))
+    assert bench.clocks_rejected(dict(ok, sm_mhz=1400.0))  # stuck low, no reason: a lock
+    assert not bench.clocks_rejected({"sm_mhz": None, "sm_max_mhz": None,
+                                      "reasons": ["nvidia-smi unavailable"]})
 
 
 def test_single_rank_passes_values_through():
