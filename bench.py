@@ -211,6 +211,35 @@ class ClockSampler:
 
 # ------------------------------------------------------------------ our arm
 
+def run_forward_only(args):
+    """`--only-forward B H N d causal [boosted]`: one forward shape, W untimed and K
+    timed calls (CUDA events, L2 flushed before each), one JSON line.  A small,
+    self-contained command for a profiler to capture a single forward launch."""
+    import torch
+
+    import exact_attention_26_gb300 as fa
+    from exact_attention_26_gb300.inputs import boosted_qkv, normal_qkv
+
+    vals = args.only_forward
+    B, H, N, d, causal = (int(x) for x in vals[:5])
+    gen = boosted_qkv if len(vals) > 5 and vals[5] == "boosted" else normal_qkv
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    fa.load()
+    q, k, v = (t.to(dev) for t in gen(B, H, N, d, seed=0))
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    ms = _time_call(torch, dev, lambda: fa.forward(q, k, v, causal=bool(causal), out=o, lse=lse),
+                    flush, iters=args.steps, warm=args.warmup)
+    status = fa.fa_device_status(None)
+    if status != 0:
+        raise RuntimeError(f"device status {fa.fa_status_string(status)}")
+    tf = fwd_flops(B, H, N, d, bool(causal)) / (ms * 1e-3) / 1e12
+    return {"only_forward": {"B": B, "H": H, "N": N, "d": d, "causal": bool(causal),
+                             "inputs": gen.__name__}, "ms": round(ms, 5), "tflops": round(tf, 2)}
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
     import torch.distributed as dist
@@ -795,6 +824,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extra", action="store_true",
                     help="skip the per-workload forward/backward sweep")
+    ap.add_argument("--only-forward", nargs="+", metavar="B H N d causal [boosted]",
+                    help="time one forward shape only (a small case for a profiler)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -802,6 +833,12 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.only_forward:
+        if len(args.only_forward) not in (5, 6):
+            ap.error("--only-forward takes B H N d causal [boosted]")
+        print(json.dumps(run_forward_only(args)), flush=True)
+        return
 
     if args.impl == "reference":
         if rank == 0:
