@@ -58,11 +58,13 @@ def test_decode_small(fa, orc, shape):
 
 
 def test_decode_split_count_is_clamped(fa):
-    """Requests beyond the number of pipeline stages shrink to one range per stage;
-    the automatic count never exceeds a quarter of the stages."""
+    """Requests beyond the number of pipeline stages shrink to one range per stage.
+    The automatic count spreads a short cache that fits one wave over one stage per
+    range (it is latency-bound), and splits a large batch only a few ways."""
     assert fa.fa_decode_num_splits(1, 1, 1, 1, 100, 128, 50) == 2
     assert fa.fa_decode_num_splits(1, 1, 1, 1, 10, 128, 3) == 1
-    assert fa.fa_decode_num_splits(1, 1, 1, 1, 64 * 40, 128, 0) <= 10
+    assert fa.fa_decode_num_splits(1, 1, 1, 1, 64 * 40, 128, 0) == 40
+    assert 1 < fa.fa_decode_num_splits(8, 32, 32, 1, 32768, 128, 0) < 16
     assert fa.fa_decode_workspace_bytes(1, 1, 1, 1, 1000, 128, 1) == 0
     assert fa.fa_decode_workspace_bytes(1, 1, 1, 1, 1000, 128, 4) > 0
 
