@@ -49,6 +49,9 @@ FWD_WORKLOADS = [
     ("B4_H8_N8192_d256_noncausal_boosted", 4, 8, 8192, 256, False, "boosted"),
     ("B2_H16_N4096_d128_causal", 2, 16, 4096, 128, True, "normal"),
     ("B4_H16_N4096_d96_causal", 4, 16, 4096, 96, True, "normal"),
+    # fewer two-tile items than SMs: the one-tile mode
+    ("B1_H8_N2048_d128_causal", 1, 8, 2048, 128, True, "normal"),
+    ("B1_H2_N16384_d128_causal", 1, 2, 16384, 128, True, "normal"),
 ]
 BWD_WORKLOADS = [
     ("B2_H16_N4096_d128_causal", 2, 16, 4096, 128, True),

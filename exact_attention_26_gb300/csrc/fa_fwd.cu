@@ -63,10 +63,13 @@ constexpr float kLn2 = 0.69314718055994530942f;
 // F8: Q, K and V arrive as e4m3 bytes (one scale per 128-row block of Q and of K,
 // one per head of V) and P is rounded to e4m3 for the PV product; V comes
 // transposed ([d][keys]) so that both products read K-major operands.
-template <int D, bool F8 = false>
+// ONE: a single 128-row tile per CTA (two S slots), for launches whose two-tile
+// items would leave SMs idle; its per-step chain is shorter, so with more CTAs in
+// flight the longest item finishes sooner.
+template <int D, bool F8 = false, bool ONE = false>
 struct FwdTile {
     static constexpr int EB = F8 ? 1 : 2;             // bytes per element
-    static constexpr int NT = (D <= 128) ? 2 : 1;     // 128-row query tiles per CTA
+    static constexpr int NT = (D <= 128 && !ONE) ? 2 : 1;  // 128-row query tiles per CTA
     static constexpr int SB = (NT == 1) ? 2 : 1;      // S slots per tile (double buffer)
     static constexpr int NS = NT * SB;                // S slots in TMEM
     static constexpr int BM = 128;
@@ -120,8 +123,8 @@ struct FwdTile {
 // block, v_descale [B*Hkv] one per head (nqb = ceil(N / 128)); S_t(j) is scaled
 // by scale * q_descale(t) * k_descale(j) inside the exponent's FMA and O by
 // v_descale / l in the epilogue.
-template <int D, bool CAUSAL, bool VARLEN, bool F8>
-__global__ void __launch_bounds__(FwdTile<D, F8>::THREADS, 1)
+template <int D, bool CAUSAL, bool VARLEN, bool F8, bool ONE>
+__global__ void __launch_bounds__(FwdTile<D, F8, ONE>::THREADS, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, __nv_bfloat16 *__restrict__ out,
                   float *__restrict__ lse, int N, int BH, int H, int group, int n_cblocks,
@@ -129,7 +132,7 @@ __global__ void __launch_bounds__(FwdTile<D, F8>::THREADS, 1)
                   const float *__restrict__ q_descale, const float *__restrict__ k_descale,
                   const float *__restrict__ v_descale, int nqb, int *status,
                   unsigned long long limit_ns) {
-    using T = FwdTile<D, F8>;
+    using T = FwdTile<D, F8, ONE>;
     constexpr int NT = T::NT;
     constexpr int KS = T::KS;
     constexpr int VS = T::VS;
@@ -716,10 +719,10 @@ __global__ void __launch_bounds__(FwdTile<D, F8>::THREADS, 1)
     }
 }
 
-template <int D, bool CAUSAL, bool VARLEN, bool F8 = false>
+template <int D, bool CAUSAL, bool VARLEN, bool F8 = false, bool ONE = false>
 int launch_fwd_t(const FwdParams &p, cudaStream_t stream) {
-    using T = FwdTile<D, F8>;
-    auto kern = fa_fwd_kernel<D, CAUSAL, VARLEN, F8>;
+    using T = FwdTile<D, F8, ONE>;
+    auto kern = fa_fwd_kernel<D, CAUSAL, VARLEN, F8, ONE>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)T::SMEM_BYTES);
     if (e != cudaSuccess) return FA_ERR_CUDA;
@@ -742,6 +745,13 @@ template <int D>
 int launch_fwd_d(const FwdParams &p, cudaStream_t stream) {
     if (p.cu_seqlens)
         return p.causal ? launch_fwd_t<D, true, true>(p, stream) : launch_fwd_t<D, false, true>(p, stream);
+    if constexpr (D <= 128) {
+        // fewer two-tile items than SMs: one tile per CTA instead
+        const long long items2 = (long long)((p.N + 255) / 256) * p.BH;
+        if (items2 < p.num_sms)
+            return p.causal ? launch_fwd_t<D, true, false, false, true>(p, stream)
+                            : launch_fwd_t<D, false, false, false, true>(p, stream);
+    }
     return p.causal ? launch_fwd_t<D, true, false>(p, stream) : launch_fwd_t<D, false, false>(p, stream);
 }
 
