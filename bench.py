@@ -55,6 +55,8 @@ FWD_WORKLOADS = [
 ]
 BWD_WORKLOADS = [
     ("B2_H16_N4096_d128_causal", 2, 16, 4096, 128, True),
+    # fewer key-block CTAs than SMs: two CTAs per key block
+    ("B1_H4_N4096_d128_causal", 1, 4, 4096, 128, True),
     ("B2_H16_N4096_d128_noncausal", 2, 16, 4096, 128, False),
     ("B8_H16_N2048_d64_causal", 8, 16, 2048, 64, True),
     ("B4_H16_N4096_d96_causal", 4, 16, 4096, 96, True),

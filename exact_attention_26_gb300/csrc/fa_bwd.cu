@@ -209,7 +209,7 @@ struct BwdTile {
     static_assert(D == 64 || D == 96 || D == 128, "head dim");
 };
 
-template <int D, bool CAUSAL, bool VARLEN>
+template <int D, bool CAUSAL, bool VARLEN, bool SPLIT>
 __global__ void __launch_bounds__(448, 1)
     fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -259,14 +259,18 @@ __global__ void __launch_bounds__(448, 1)
     // Grouped-query attention: this CTA owns key/value head kvh (= b * Hkv + hk)
     // and accumulates dK, dV over the `group` query heads that read it, walking
     // their query blocks one head after the other.
+    // SPLIT (small grids): two consecutive CTAs share a key block, each taking a
+    // contiguous half of its query blocks, and add their dK, dV into zeroed outputs.
+    const int part = SPLIT ? (int)(blockIdx.x & 1u) : 0;
+    const unsigned bid = SPLIT ? blockIdx.x >> 1 : blockIdx.x;
     int kvh, kv0;
     if (!(VARLEN || !CAUSAL) || head_group >= BHkv) {
-        kvh = blockIdx.x % BHkv;
-        kv0 = (blockIdx.x / BHkv) * T::BN;
+        kvh = bid % BHkv;
+        kv0 = (bid / BHkv) * T::BN;
     } else {
         const int n_kb = (N + T::BN - 1) / T::BN;
-        const int hgrp = (int)blockIdx.x / (head_group * n_kb);
-        const int hrem = (int)blockIdx.x % (head_group * n_kb);
+        const int hgrp = (int)bid / (head_group * n_kb);
+        const int hrem = (int)bid % (head_group * n_kb);
         const int hcnt = min(head_group, BHkv - hgrp * head_group);  // heads in this group
         kvh = hgrp * head_group + hrem % hcnt;
         kv0 = (hrem / hcnt) * T::BN;
@@ -294,7 +298,11 @@ __global__ void __launch_bounds__(448, 1)
     const int n_qb = (len + BQ - 1) / BQ;
     const int i_start = CAUSAL ? kv0 / BQ : 0;
     const int n_qit = n_qb - i_start;  // query blocks per query head
-    const int n_it = group * n_qit;
+    const int n_all = group * n_qit;
+    const int it0 = part ? n_all / 2 : 0;  // this CTA's blocks: [it0, it0 + n_it)
+    const int n_it = SPLIT ? (part ? n_all - n_all / 2 : n_all / 2) : n_all;
+    if (SPLIT && n_it == 0) return;  // uniform across the CTA, before any barrier or TMEM use
+    const int qb_first = SPLIT ? it0 % n_qit : 0, gq_first = SPLIT ? it0 / n_qit : 0;
     const int bhq0 = (kvh / (H / group)) * H + (kvh % (H / group)) * group;
     // Block it is query block qb = it % n_qit of query head bhq0 + it / n_qit; the
     // loops below carry (qb, gq) as counters instead of dividing every block.
@@ -347,7 +355,8 @@ __global__ void __launch_bounds__(448, 1)
             // the -L log2e and -D vectors come from the preprocess kernel
             griddep_wait();
             int issued = 0;
-            for (int it = 0, qb = 0, gq = 0; it < n_it; ++it, (++qb == n_qit) ? (qb = 0, ++gq) : 0) {
+            for (int it = 0, qb = qb_first, gq = gq_first; it < n_it;
+             ++it, (++qb == n_qit) ? (qb = 0, ++gq) : 0) {
                 const int s = it % QS;
                 const int q0 = (i_start + qb) * BQ;
                 if (it >= QS && !mbar_wait(bar_q_empty + 8 * s, ((it / QS) - 1) & 1, g,
@@ -456,7 +465,8 @@ __global__ void __launch_bounds__(448, 1)
         const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
         const int key = kv0 + r;
         bool ok = true;
-        for (int it = 0, qb = 0, gq = 0; it < n_it; ++it, (++qb == n_qit) ? (qb = 0, ++gq) : 0) {
+        for (int it = 0, qb = qb_first, gq = gq_first; it < n_it;
+             ++it, (++qb == n_qit) ? (qb = 0, ++gq) : 0) {
             const int s = it % QS;
             const int q0 = (i_start + qb) * BQ;
             ok = mbar_wait_warp(bar_s_full, it & 1, g, SITE_BWD_SOFTMAX_S_FULL);
@@ -567,7 +577,11 @@ __global__ void __launch_bounds__(448, 1)
                     const size_t krow =
                         VARLEN ? (size_t)(tok0 + key) * (H / group) + hk : (size_t)kvh * N + key;
                     float *dst = (pass == 0 ? dv : dk) + krow * D + 64 * h;
-                    bulk_store(dst, stg_s, h == 0 ? 256u : (uint32_t)(D - 64) * 4);
+                    const uint32_t nb = h == 0 ? 256u : (uint32_t)(D - 64) * 4;
+                    if constexpr (SPLIT)
+                        bulk_reduce_add_f32(dst, stg_s, nb);
+                    else
+                        bulk_store(dst, stg_s, nb);
                 }
                 bulk_commit_group();
             }
@@ -580,7 +594,8 @@ __global__ void __launch_bounds__(448, 1)
         if (warp == 8) griddep_wait();    // dQ was zeroed by the preprocess kernel
         const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
         bool ok = true;
-        for (int it = 0, qb = 0, gq = 0; it < n_it; ++it, (++qb == n_qit) ? (qb = 0, ++gq) : 0) {
+        for (int it = 0, qb = qb_first, gq = gq_first; it < n_it;
+             ++it, (++qb == n_qit) ? (qb = 0, ++gq) : 0) {
             const int q0 = (i_start + qb) * BQ;
             ok = mbar_wait_warp(bar_dq_full, it & 1, g, SITE_BWD_DQ_FULL);
             if (!ok) break;
@@ -661,6 +676,23 @@ __global__ void __launch_bounds__(448, 1)
 
 template <int D, bool CAUSAL, bool VARLEN>
 int launch_bwd_t(const BwdParams &p, cudaStream_t stream) {
+    using W = BwdTile<D>;
+    long long grid = (long long)((p.N + W::BN - 1) / W::BN) * (p.BH / p.group);
+    // Small grids (single sequences with few heads; fixed layout): two CTAs per key
+    // block, each over half of its query blocks, adding dK and dV into outputs
+    // zeroed here, stream-ordered ahead of the preprocess kernel (so the main kernel
+    // stays a programmatic dependent of the preprocess).  Causal: whenever the grid
+    // is under one wave, since halving the longest key blocks shortens the critical
+    // path; non-causal: only when the doubled grid still fits one wave (the CTAs are
+    // all equally long, and a second wave of halves costs as much as the whole).
+    const bool split = !VARLEN && (CAUSAL ? grid < p.num_sms : 2 * grid <= p.num_sms);
+    if (split) {
+        grid *= 2;
+        const size_t kv_bytes = (size_t)(p.BH / p.group) * p.N * D * sizeof(float);
+        if (cudaMemsetAsync(p.dk, 0, kv_bytes, stream) != cudaSuccess ||
+            cudaMemsetAsync(p.dv, 0, kv_bytes, stream) != cudaSuccess)
+            return FA_ERR_CUDA;
+    }
     {
         const long long rows = (long long)p.BH * p.Npad;
         long long blocks = (rows / 4 * 32 + 255) / 256;  // a warp per group of four rows
@@ -673,8 +705,7 @@ int launch_bwd_t(const BwdParams &p, cudaStream_t stream) {
             p.N, p.Npad, p.BH, p.H, p.cu_seqlens, p.total_tokens);
         if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
     }
-    using W = BwdTile<D>;
-    const long long grid = (long long)((p.N + W::BN - 1) / W::BN) * (p.BH / p.group);
+
     // Packed sequences and non-causal masks: groups of 8 key/value heads (measured:
     // varlen length mix 3.58 -> 2.55 ms, B8 H16 N2048 d64 non-causal +4.7%, B2 H16
     // N4096 d128 non-causal -0.5%).  Causal fixed layouts: one group, i.e. key block
@@ -682,8 +713,7 @@ int launch_bwd_t(const BwdParams &p, cudaStream_t stream) {
     // arithmetic; grouping measured -0.5% on B2 H16 N4096 d128 causal).
     const int head_group = (VARLEN || !CAUSAL) ? min(8, p.BH / p.group) : p.BH / p.group;
     if (grid > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
-    {
-        auto kern = fa_bwd_kernel<D, CAUSAL, VARLEN>;
+    auto launch = [&](auto kern) -> int {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)W::SMEM_BYTES) != cudaSuccess)
             return FA_ERR_CUDA;
@@ -705,7 +735,15 @@ int launch_bwd_t(const BwdParams &p, cudaStream_t stream) {
                                p.group, head_group, p.cu_seqlens, p.total_tokens, p.scale,
                                p.scale_log2, p.status, p.limit_ns) != cudaSuccess)
             return FA_ERR_CUDA;
-    }
+        return FA_OK;
+    };
+    int rc;
+    if constexpr (VARLEN)
+        rc = launch(fa_bwd_kernel<D, CAUSAL, true, false>);
+    else
+        rc = split ? launch(fa_bwd_kernel<D, CAUSAL, false, true>)
+                   : launch(fa_bwd_kernel<D, CAUSAL, false, false>);
+    if (rc != FA_OK) return rc;
     return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
