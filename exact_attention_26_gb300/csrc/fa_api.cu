@@ -95,20 +95,21 @@ int make_thd_map(CUtensorMap *map, const void *ptr, int T, int heads, int d, int
     return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
 }
 
-// 3-D map over a packed token-major fp32 [T][heads][d] tensor (the varlen dQ),
-// unswizzled: a box of d columns x 1 head x `box_rows` tokens is a row-major
-// [box_rows][d] tile in shared memory.  Used for tiled bulk adds.
-int make_thd_map_f32(CUtensorMap *map, const void *ptr, int T, int heads, int d, int box_rows) {
+// 3-D map over a contiguous fp32 tensor (the dQ output) for tiled bulk adds,
+// unswizzled: dims (d, n1, n2) with row pitch d and plane pitch n1 * d elements,
+// boxes of 32 columns x box1 x box2, which are row-major 128-byte rows in shared
+// memory.  Fixed layout [BH][N][d]: (d, N, BH), box (32, 32, 1); packed
+// token-major [T][heads][d]: (d, heads, T), box (32, 1, 32).
+int make_f32_map(CUtensorMap *map, const void *ptr, int d, int n1, int n2, int box1, int box2) {
     auto enc = encode_tiled();
     if (!enc) return FA_ERR_CUDA;
-    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)heads, (cuuint64_t)T};
-    cuuint64_t strides[2] = {(cuuint64_t)d * 4, (cuuint64_t)heads * (cuuint64_t)d * 4};
-    cuuint32_t box[3] = {(cuuint32_t)d, 1, (cuuint32_t)box_rows};
+    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)n1, (cuuint64_t)n2};
+    cuuint64_t strides[2] = {(cuuint64_t)d * 4, (cuuint64_t)n1 * (cuuint64_t)d * 4};
+    cuuint32_t box[3] = {32, (cuuint32_t)box1, (cuuint32_t)box2};
     cuuint32_t elem_strides[3] = {1, 1, 1};
-    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void *>(ptr), dims,
-                     strides, box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                     CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void *>(ptr), dims, strides, box,
+                     elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
 }
 
@@ -169,6 +170,48 @@ __global__ void __launch_bounds__(32) fa_wait_selftest_kernel(int *status,
 }
 
 }  // namespace
+
+namespace {
+// Kernels whose dynamic shared memory limit has been raised, per device.
+struct SmemAttr {
+    const void *kernel;
+    int device, bytes;
+};
+std::mutex g_attr_mutex;
+SmemAttr g_attr[256];
+int g_attr_count = 0;
+}  // namespace
+
+int ensure_smem_attr(const void *kernel, int bytes) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_attr_mutex);
+    for (int i = 0; i < g_attr_count; ++i)
+        if (g_attr[i].kernel == kernel && g_attr[i].device == dev && g_attr[i].bytes >= bytes)
+            return FA_OK;
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) !=
+        cudaSuccess)
+        return FA_ERR_CUDA;
+    if (g_attr_count < 256) g_attr[g_attr_count++] = {kernel, dev, bytes};
+    return FA_OK;
+}
+
+int kernel_num_regs(const void *kernel) {
+    static std::mutex m;
+    static const void *keys[64];
+    static int vals[64];
+    static int n = 0;
+    std::lock_guard<std::mutex> lock(m);
+    for (int i = 0; i < n; ++i)
+        if (keys[i] == kernel) return vals[i];
+    cudaFuncAttributes a{};
+    if (cudaFuncGetAttributes(&a, kernel) != cudaSuccess) return -1;
+    if (n < 64) {
+        keys[n] = kernel;
+        vals[n++] = a.numRegs;
+    }
+    return a.numRegs;
+}
 
 // Keys per K/V tile of the forward kernel for head dimension d.
 int fwd_block_n(int d) { return d == 256 ? 64 : 128; }
@@ -378,6 +421,7 @@ extern "C" int fa_bwd_gqa(const void *q, const void *k, const void *v, const voi
     if ((rc = make_bhnd_map(&p.tm_do, dout, BH, N, d, q_rows)) != FA_OK) return rc;
     if ((rc = make_bhnd_map(&p.tm_k, k, B * Hkv, N, d, 128)) != FA_OK) return rc;
     if ((rc = make_bhnd_map(&p.tm_v, v, B * Hkv, N, d, 128)) != FA_OK) return rc;
+    if ((rc = make_f32_map(&p.tm_dq, dq, d, N, BH, 32, 1)) != FA_OK) return rc;
     p.o = o;
     p.dout = dout;
     p.lse = lse;
@@ -433,7 +477,7 @@ extern "C" int fa_bwd_varlen(const void *q, const void *k, const void *v, const 
     if ((rc = make_thd_map(&p.tm_do, dout, total_tokens, H, d, q_rows)) != FA_OK) return rc;
     if ((rc = make_thd_map(&p.tm_k, k, total_tokens, Hkv, d, 128)) != FA_OK) return rc;
     if ((rc = make_thd_map(&p.tm_v, v, total_tokens, Hkv, d, 128)) != FA_OK) return rc;
-    if ((rc = make_thd_map_f32(&p.tm_dq, dq, total_tokens, H, d, q_rows)) != FA_OK) return rc;
+    if ((rc = make_f32_map(&p.tm_dq, dq, d, H, total_tokens, 1, 32)) != FA_OK) return rc;
     p.o = o;
     p.dout = dout;
     p.lse = lse;

@@ -17,7 +17,7 @@
 // adds them (padded rows get 0 and -inf, so their P is exactly 0), and dQ := 0.
 //
 // Kernel 2 (fa_bwd_kernel): one CTA per (batch * key/value head, block of 128
-// keys), looping over blocks of 64 query rows.  All products are tcgen05 MMAs
+// keys), looping over blocks of 128 query rows.  All products are tcgen05 MMAs
 // with fp32 accumulators in tensor memory, computed in the transposed orientation
 // so that a TMEM lane is a key:
 //
@@ -27,17 +27,17 @@
 //   dK  += dS^T Q_i         (A = dS^T from TMEM, B = Q  smem MN-major)
 //   dQ_i^T = K_j^T dS^T     (A = K smem MN-major, B = dS^T smem MN-major)
 //
-// dQ_i leaves tensor memory through a shared-memory staging tile and one bulk
-// asynchronous fp32 add (cp.reduce.async.bulk) into the global dQ rows.  At the
-// end dK (times scale) and dV leave once, through shared memory and bulk copies.
+// dQ_i leaves tensor memory into registers and goes through shared memory into
+// tiled bulk fp32 adds on the global dQ rows.  At the end dK (times scale) and dV leave once, through
+// shared memory and bulk copies.
 //
-// Warp roles (448 threads):
-//   warps 0-7   P^T = exp2(S^T scale log2e - L log2e), dS^T = P^T o (dP^T - D)
-//               (one key per thread, two warpgroups split a block's 64 queries),
-//               written as bf16 to TMEM and dS^T to smem; final dK/dV epilogue
-//   warps 8-11  dQ readout: TMEM -> staging smem -> bulk add into global dQ
-//   warp 12     TMA producer: K_j, V_j once; Q_i, dO_i, L_i, D_i per ring stage
-//   warp 13     TMEM allocator; one elected lane issues every MMA and commit
+// Warp roles (576 threads):
+//   warps 0-15  P^T = exp2(S^T scale log2e - L log2e), dS^T = P^T o (dP^T - D)
+//               (one key per thread, four warpgroups split a block's 128 queries),
+//               written as bf16 to TMEM and dS^T to smem; the dQ read-out; the
+//               final dK/dV epilogue
+//   warp 16     TMA producer: K_j, V_j once; Q_i (with L_i, D_i) and dO_i per ring stage
+//   warp 17     TMEM allocator; one elected lane issues every MMA and commit
 #include "fa_ptx.cuh"
 
 namespace fa {
@@ -155,16 +155,31 @@ __global__ void __launch_bounds__(256)
 
 // ---------------------------------------------------------------- main kernel
 //
-// The products are scheduled so the tensor core never waits for the P^T/dS^T
-// warps.  Tensor memory (512 columns): dV [0,128), dK [128,256),
-// S^T [256,320), dP^T [320,384), PD [384,448) holding bf16 P^T (first 32
-// columns) and dS^T (last 32), dQ^T [448,512).  Because P^T and dS^T go to their
-// own region, the next block's S^T and dP^T can be issued as soon as the compute
-// warps have READ the current ones (st_free), and they run on the tensor core
-// while the compute warps work; the dV/dK products of block i release PD for
-// block i+1 (pd_free).  Per block the MMA thread issues
-//   S^T(i+1), dP^T(i+1)  |  dV(i), dK(i)  |  dQ^T(i)
-// Two compute warpgroups split the 64 query columns of a block.
+// A CTA owns 128 keys (one per TMEM lane) and walks blocks of 128 query rows, so
+// every product is an M = 128, N = 128 tcgen05 MMA.  (With both operands in shared
+// memory an MMA reads (M + N) x 32 bytes per K step, and at N = 64 that operand
+// fetch, not the arithmetic, sets its time: 48 cycles instead of 32.  At N = 128
+// the fetch and the arithmetic take the same 64 cycles.)
+//
+// Tensor memory (512 columns, d = 128): dV [0,128), dK [128,256), X [256,384),
+// Y [384,512).  X holds S^T, then P^T as bf16 over its first half; Y holds dP^T,
+// then dS^T as bf16, then dQ^T.  (d = 64: dV [0,64), dK [64,128), X [128,256),
+// Y [256,384).)  Per block i the MMA thread issues
+//
+//   dP^T(i)     = V dO(i)^T   -> Y        once dQ^T(i-1) has been read out of Y
+//   dV(i)      += P^T(i) dO(i)            A = P^T in X
+//   S^T(i+1)    = K Q(i+1)^T  -> X        X is free once dV(i) has read P^T(i)
+//   dK(i)      += dS^T(i) Q(i)            A = dS^T in Y
+//   dQ^T(i)     = K^T dS^T(i) -> Y        B = dS^T from shared memory
+//
+// Warpgroups 0-1 compute dS(i) while dV(i) and S^T(i+1) run and P(i+1) while
+// dK(i), dQ^T(i) and dP^T(i+1) run.  Warpgroups 2-3 read dQ^T(i) out of Y into
+// registers (the tensor core waits only for that) and then add it into global dQ
+// through tiled bulk adds.  The adds are bound by the L2's reduction rate (about
+// 24 bytes per SM clock with every SM adding, by bulk copies or vector
+// reductions; scalar per-thread reductions reach about 19), which is why they
+// have warps of their own: their 64 KB per block then overlap the exponentials
+// and the products instead of following them.
 //
 // d = 96 keeps the d = 128 layout: rows are two 64-column swizzle chunks whose
 // columns past d the copies zero-fill, S^T and dP^T run D/16 K steps, dV and dK
@@ -175,83 +190,105 @@ template <int D_>
 struct BwdTile {
     static constexpr int D = D_;
     static constexpr int DP = D <= 64 ? 64 : 128;       // row width in shared memory
-    static constexpr int BN = 128;
-    static constexpr int BQ = 64;
+    static constexpr int BN = 128;                      // keys per CTA
+    static constexpr int BQ = 128;                      // query rows per block
     static constexpr int NCH = DP / 64;
-    static constexpr int QS = 3;                        // Q/dO/L/D ring stages
-    static constexpr uint32_t K_CHUNK = BN * 128;
+    static constexpr int QS = D <= 64 ? 4 : 2;          // Q ring stages (Q, -L log2e, -D)
+    // dO ring stages.  dO(i) serves only dP^T(i) and dV(i), issued back to back, so
+    // one stage leaves the copy of dO(i+1) the rest of the block's products.
+    static constexpr int OS = D <= 64 ? 2 : 1;
+    static constexpr uint32_t K_CHUNK = BN * 128;       // 64 columns of every key row
     static constexpr uint32_t Q_CHUNK = BQ * 128;
     static constexpr uint32_t KV_BYTES = BN * DP * 2;
     static constexpr uint32_t Q_BYTES = BQ * DP * 2;
-    static constexpr uint32_t DS_BYTES = BQ * BN * 2;   // dS^T, [128 keys][64 queries] bf16
-    static constexpr uint32_t STAGE_BYTES = BQ * D * 4; // dQ tile, fp32
+    static constexpr uint32_t DS_CHUNK = BN * 128;      // dS^T: 64 queries of every key
+    static constexpr uint32_t DS_BYTES = BN * BQ * 2;
     static constexpr uint32_t VEC_BYTES = BQ * 4;
-    static constexpr uint32_t TM_DV = 0, TM_DK = 128, TM_ST = 256, TM_DPT = 320, TM_PD = 384,
-                              TM_DQ = 448, TM_COLS = 512;
+    static constexpr uint32_t TM_DV = 0, TM_DK = DP, TM_X = 2 * DP, TM_Y = 2 * DP + 128,
+                              TM_COLS = 512;
     static constexpr uint32_t OFF_K = 0;
     static constexpr uint32_t OFF_V = OFF_K + KV_BYTES;
     static constexpr uint32_t OFF_Q = OFF_V + KV_BYTES;
     static constexpr uint32_t OFF_DO = OFF_Q + QS * Q_BYTES;
-    static constexpr uint32_t OFF_DS = OFF_DO + QS * Q_BYTES;
-    static constexpr uint32_t OFF_STAGE = OFF_DS + DS_BYTES;  // one dS^T buffer
-    static constexpr uint32_t OFF_L2 = OFF_STAGE + STAGE_BYTES;
+    static constexpr uint32_t OFF_DS = OFF_DO + OS * Q_BYTES;  // dS^T (B of dQ^T)
+    static constexpr uint32_t OFF_STG = OFF_DS + DS_BYTES;     // dQ staging, 4 KB per dQ warp
+    static constexpr uint32_t STG_BYTES = 8 * 4096;
+    static constexpr uint32_t OFF_L2 = OFF_STG + STG_BYTES;
     static constexpr uint32_t OFF_DELTA = OFF_L2 + QS * VEC_BYTES;
     static constexpr uint32_t OFF_BAR = OFF_DELTA + QS * VEC_BYTES;
-    // kv_full, q_full[QS], q_empty[QS], s_full, st_free, ds_full, pd_free, dq_full,
-    // dq_empty, stg_free, stg_full, done (dq_full also tells the compute warps that
-    // the dS^T buffer is free)
-    static constexpr int NBAR = 1 + 2 * QS + 9;
+    // kv_full, q_full[QS], q_empty[QS], o_full[OS], o_empty[OS], s_full, p_full,
+    // dp_full, ds_full, dq_full, dq_empty, done
+    static constexpr int NBAR = 1 + 2 * QS + 2 * OS + 7;
     static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
-    static constexpr uint32_t SMEM_BYTES = OFF_MISC + 16 + 1024;
-    static constexpr int THREADS = 448;  // compute 0-7, dQ readout 8-11, TMA 12, MMA 13
-    static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
-    static_assert(Q_CHUNK % 1024 == 0 && DS_BYTES % 1024 == 0, "swizzle atoms must stay aligned");
+    static constexpr uint32_t SMEM_USED = OFF_MISC + 16;
+    // The tiles need 1024-byte alignment (128-byte swizzle atoms).  At d = 128 the
+    // layout leaves no room to align the start by hand: the kernel then requires
+    // the dynamic shared memory to start aligned, and checks it.
+    static constexpr uint32_t kMaxSmem = 227 * 1024;
+    static constexpr uint32_t SMEM_BYTES =
+        SMEM_USED + 1024 <= kMaxSmem ? SMEM_USED + 1024 : SMEM_USED;
+    static constexpr int THREADS = 640;  // P/dS 0-7, dQ 8-15, TMA 16, MMA 17, 18-19 idle
+    // Registers per thread after the warpgroups rebalance (launch: 96 each, a pool
+    // of 5 x 128 x 96): P/dS warpgroups hold 64 fp32 P values per thread.
+    static constexpr int LAUNCH_REGS = 96, REG_PDS = 136, REG_DQ = 80, REG_MISC = 48;
+    static_assert(2 * REG_PDS + 2 * REG_DQ + REG_MISC <= 5 * LAUNCH_REGS, "register pool");
+    static_assert(SMEM_USED <= kMaxSmem, "shared memory budget");
+    static_assert(Q_CHUNK % 1024 == 0 && DS_CHUNK % 1024 == 0 && KV_BYTES % 1024 == 0,
+                  "swizzle atoms must stay aligned");
+    static_assert(TM_Y + 128 <= TM_COLS, "tensor memory budget");
     static_assert(D == 64 || D == 96 || D == 128, "head dim");
 };
 
 template <int D, bool CAUSAL, bool VARLEN, bool SPLIT>
-__global__ void __launch_bounds__(448, 1)
+__global__ void __launch_bounds__(640, 1)
     fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                       const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                       const __grid_constant__ CUtensorMap tm_dq,
-                       const float *__restrict__ ws_lse2, const float *__restrict__ ws_delta,
-                       float *__restrict__ dq, float *__restrict__ dk, float *__restrict__ dv, int N,
-                       int Npad, int BHkv, int H, int group, int head_group,
-                       const int *__restrict__ cu_seqlens,
+                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                  const __grid_constant__ CUtensorMap tm_dq,
+                  const float *__restrict__ ws_lse2, const float *__restrict__ ws_delta,
+                  float *__restrict__ dk, float *__restrict__ dv, int N, int Npad, int BHkv,
+                  int H, int group, int head_group, const int *__restrict__ cu_seqlens,
                   int total_tokens, float scale, float scale_log2, int *status,
-                       unsigned long long limit_ns) {
+                  unsigned long long limit_ns) {
     using T = BwdTile<D>;
-    constexpr int BQ = T::BQ, QS = T::QS;
-    extern __shared__ uint8_t smem_raw[];
-    const uint32_t raw = smem_u32(smem_raw);
+    constexpr int BQ = T::BQ, QS = T::QS, OS = T::OS;
+    extern __shared__ __align__(1024) uint8_t smem_bwd[];
+    const uint32_t raw = smem_u32(smem_bwd);
     const uint32_t base = (raw + 1023u) & ~1023u;
-    uint8_t *gbase = smem_raw + (base - raw);
+    if (base - raw + T::SMEM_USED > T::SMEM_BYTES) {
+        // uniform across the CTA, before any barrier or TMEM use
+        if (threadIdx.x == 0) {
+            atomicCAS(status + 1, 0, SITE_BWD_SMEM_ALIGN);
+            atomicExch(status, FA_ERR_UNSUPPORTED);
+        }
+        return;
+    }
+    uint8_t *gbase = smem_bwd + (base - raw);
 
     const uint32_t sK = base + T::OFF_K, sV = base + T::OFF_V;
     const uint32_t sQ = base + T::OFF_Q, sDO = base + T::OFF_DO;
-    const uint32_t sDS = base + T::OFF_DS, sStage = base + T::OFF_STAGE;
+    const uint32_t sDS = base + T::OFF_DS;
     const uint32_t sL2 = base + T::OFF_L2, sDelta = base + T::OFF_DELTA;
     const uint32_t bar = base + T::OFF_BAR;
     const uint32_t bar_kv_full = bar;
-    const uint32_t bar_q_full = bar + 8;                 // [QS]
-    const uint32_t bar_q_empty = bar_q_full + 8 * QS;     // [QS]
-    const uint32_t bar_s_full = bar_q_empty + 8 * QS;
-    const uint32_t bar_st_free = bar_s_full + 8;
-    const uint32_t bar_ds_full = bar_s_full + 16;
-    const uint32_t bar_pd_free = bar_s_full + 24;
+    const uint32_t bar_q_full = bar + 8;               // [QS]
+    const uint32_t bar_q_empty = bar_q_full + 8 * QS;  // [QS]
+    const uint32_t bar_o_full = bar_q_empty + 8 * QS;  // [OS]
+    const uint32_t bar_o_empty = bar_o_full + 8 * OS;  // [OS]
+    const uint32_t bar_s_full = bar_o_empty + 8 * OS;
+    const uint32_t bar_p_full = bar_s_full + 8;
+    const uint32_t bar_dp_full = bar_s_full + 16;
+    const uint32_t bar_ds_full = bar_s_full + 24;
     const uint32_t bar_dq_full = bar_s_full + 32;
     const uint32_t bar_dq_empty = bar_s_full + 40;
-    const uint32_t bar_stg_free = bar_s_full + 48;  // staging tile may be overwritten
-    const uint32_t bar_stg_full = bar_s_full + 56;  // staging tile written by all 128 threads
-    const uint32_t bar_done = bar_s_full + 64;
+    const uint32_t bar_done = bar_s_full + 48;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + T::OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(gbase + T::OFF_MISC + 4);
-    float *stage_f = reinterpret_cast<float *>(gbase + T::OFF_STAGE);
     const float *l2_f = reinterpret_cast<const float *>(gbase + T::OFF_L2);
     const float *delta_f = reinterpret_cast<const float *>(gbase + T::OFF_DELTA);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    constexpr int kTmaWarp = 16, kMmaWarp = 17;
 
     // CTAs walk the key/value heads in groups of head_group (whose Q/dO then stay in
     // L2 together) and, within a group, the key blocks first: with a causal mask key
@@ -313,36 +350,40 @@ __global__ void __launch_bounds__(448, 1)
             mbar_init(bar_q_full + 8 * s, 1);
             mbar_init(bar_q_empty + 8 * s, 1);
         }
+        for (int s = 0; s < OS; ++s) {
+            mbar_init(bar_o_full + 8 * s, 1);
+            mbar_init(bar_o_empty + 8 * s, 1);
+        }
         mbar_init(bar_s_full, 1);
-        mbar_init(bar_st_free, 256);
+        mbar_init(bar_p_full, 256);
+        mbar_init(bar_dp_full, 1);
         mbar_init(bar_ds_full, 256);
-        mbar_init(bar_pd_free, 1);
         mbar_init(bar_dq_full, 1);
-        mbar_init(bar_dq_empty, 128);
-        mbar_init(bar_stg_free, 1);
-        mbar_init(bar_stg_full, 128);
+        mbar_init(bar_dq_empty, 256);
         mbar_init(bar_done, 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
-    if (warp == 13) {
+    if (warp == kMmaWarp) {
         tmem_alloc(smem_u32(tmem_slot), T::TM_COLS);
         tmem_relinquish();
     }
-    if (warp == 12 && lane == 0) {
+    if (warp == kTmaWarp && lane == 0) {
         tma_prefetch_desc(&tm_q);
         tma_prefetch_desc(&tm_k);
         tma_prefetch_desc(&tm_v);
         tma_prefetch_desc(&tm_do);
-        if (VARLEN) tma_prefetch_desc(&tm_dq);
+        tma_prefetch_desc(&tm_dq);
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const Guard g{status, abort_flag, limit_ns};
-
-    if (warp == 12) {
+    // Each role rebalances its registers first thing in its own branch, so that the
+    // compiler allocates the role's code within that role's budget.
+    if (warp == kTmaWarp) {
+        setmaxnreg_dec<T::REG_MISC>();
         // ------------------------------------------------------- TMA producer
         if (lane == 0) {
             mbar_arrive_expect_tx(bar_kv_full, 2 * T::KV_BYTES);
@@ -354,211 +395,160 @@ __global__ void __launch_bounds__(448, 1)
             }
             // the -L log2e and -D vectors come from the preprocess kernel
             griddep_wait();
-            int issued = 0;
+            int issued_q = 0, issued_o = 0;
             for (int it = 0, qb = qb_first, gq = gq_first; it < n_it;
-             ++it, (++qb == n_qit) ? (qb = 0, ++gq) : 0) {
-                const int s = it % QS;
+                 ++it, (++qb == n_qit) ? (qb = 0, ++gq) : 0) {
                 const int q0 = (i_start + qb) * BQ;
-                if (it >= QS && !mbar_wait(bar_q_empty + 8 * s, ((it / QS) - 1) & 1, g,
+                const int yq = VARLEN ? (bhq0 + gq) % H : q0;
+                const int zq = VARLEN ? tok0 + q0 : bhq0 + gq;
+                // Q(it) goes first: S^T(it) is issued a block ahead of dP^T(it) and
+                // dV(it), the products of dO(it).
+                // Q(it) with its -L log2e and -D: free once dK of block it - QS is done
+                const int qs = it % QS;
+                if (it >= QS && !mbar_wait<true>(bar_q_empty + 8 * qs, ((it / QS) - 1) & 1, g,
                                            SITE_BWD_LOAD_EMPTY))
                     break;
-                const uint32_t fb = bar_q_full + 8 * s;
-                mbar_arrive_expect_tx(fb, 2 * T::Q_BYTES + 2 * T::VEC_BYTES);
-                for (int c = 0; c < T::NCH; ++c) {
-                    tma_load_3d(sQ + s * T::Q_BYTES + c * T::Q_CHUNK, &tm_q, fb, c * 64, VARLEN ? (bhq0 + gq) % H : q0,
-                                VARLEN ? tok0 + q0 : bhq0 + gq);
-                    tma_load_3d(sDO + s * T::Q_BYTES + c * T::Q_CHUNK, &tm_do, fb, c * 64, VARLEN ? (bhq0 + gq) % H : q0,
-                                VARLEN ? tok0 + q0 : bhq0 + gq);
-                }
+                const uint32_t fb = bar_q_full + 8 * qs;
+                mbar_arrive_expect_tx(fb, T::Q_BYTES + 2 * T::VEC_BYTES);
+                for (int c = 0; c < T::NCH; ++c)
+                    tma_load_3d(sQ + qs * T::Q_BYTES + c * T::Q_CHUNK, &tm_q, fb, c * 64, yq, zq);
                 const size_t voff = (size_t)(bhq0 + gq) * Npad + q0;
-                bulk_load(sL2 + s * T::VEC_BYTES, ws_lse2 + voff, T::VEC_BYTES, fb);
-                bulk_load(sDelta + s * T::VEC_BYTES, ws_delta + voff, T::VEC_BYTES, fb);
-                ++issued;
+                bulk_load(sL2 + qs * T::VEC_BYTES, ws_lse2 + voff, T::VEC_BYTES, fb);
+                bulk_load(sDelta + qs * T::VEC_BYTES, ws_delta + voff, T::VEC_BYTES, fb);
+                ++issued_q;
+                // dO(it): free once dV and dP^T of block it - OS are done
+                const int os = it % OS;
+                if (it >= OS && !mbar_wait<true>(bar_o_empty + 8 * os, ((it / OS) - 1) & 1, g,
+                                           SITE_BWD_LOAD_EMPTY))
+                    break;
+                mbar_arrive_expect_tx(bar_o_full + 8 * os, T::Q_BYTES);
+                for (int c = 0; c < T::NCH; ++c)
+                    tma_load_3d(sDO + os * T::Q_BYTES + c * T::Q_CHUNK, &tm_do, bar_o_full + 8 * os,
+                                c * 64, yq, zq);
+                ++issued_o;
             }
             if (*abort_flag) {
+                // every copy this warp started lands before the CTA exits
                 volatile int never = 0;
                 const Guard g2{status, &never, kWaitLimitNs};
-                mbar_wait(bar_kv_full, 0, g2, SITE_BWD_DRAIN);
-                for (int it = (issued > QS ? issued - QS : 0); it < issued; ++it)
-                    mbar_wait(bar_q_full + 8 * (it % QS), (it / QS) & 1, g2, SITE_BWD_DRAIN);
+                mbar_wait<true>(bar_kv_full, 0, g2, SITE_BWD_DRAIN);
+                for (int it = (issued_q > QS ? issued_q - QS : 0); it < issued_q; ++it)
+                    mbar_wait<true>(bar_q_full + 8 * (it % QS), (it / QS) & 1, g2, SITE_BWD_DRAIN);
+                for (int it = (issued_o > OS ? issued_o - OS : 0); it < issued_o; ++it)
+                    mbar_wait<true>(bar_o_full + 8 * (it % OS), (it / OS) & 1, g2, SITE_BWD_DRAIN);
             }
         }
-    } else if (warp == 13) {
+    } else if (warp == kMmaWarp) {
+        setmaxnreg_dec<T::REG_MISC>();
         // ------------------------------------------------------- MMA issuer
         // The whole warp runs this loop (warp-uniform); one elected lane issues.
-        {
-            constexpr uint32_t kIdescT = idesc_bf16_f32(128, BQ, false, false);   // S^T, dP^T
-            constexpr uint32_t kIdescAcc = idesc_bf16_f32(128, D, false, true);   // dV, dK
-            constexpr uint32_t kIdescDQ = idesc_bf16_f32(128, BQ, true, true);    // dQ^T
-            const uint64_t dK_k = sdesc_sw128(sK, 16, 1024);           // K, K-major (A of S^T)
-            const uint64_t dV_k = sdesc_sw128(sV, 16, 1024);           // V, K-major (A of dP^T)
-            const uint64_t dK_mn = sdesc_sw128(sK, T::K_CHUNK, 1024);  // K, MN-major (A of dQ^T)
-            const uint64_t dDS = sdesc_sw128(sDS, T::DS_BYTES, 1024);  // dS^T, MN-major
-            auto issue_st_dpt = [&](int it) {
-                const int s = it % QS;
-                const uint64_t dQ_k = sdesc_sw128(sQ + s * T::Q_BYTES, 16, 1024);
-                const uint64_t dDO_k = sdesc_sw128(sDO + s * T::Q_BYTES, 16, 1024);
+        constexpr uint32_t kIdescT = idesc_bf16_f32(128, BQ, false, false);   // S^T, dP^T
+        constexpr uint32_t kIdescAcc = idesc_bf16_f32(128, D, false, true);   // dV, dK
+        constexpr uint32_t kIdescDQ = idesc_bf16_f32(128, BQ, true, true);    // dQ^T
+        const uint64_t dK_k = sdesc_sw128(sK, 16, 1024);           // K, K-major (A of S^T)
+        const uint64_t dV_k = sdesc_sw128(sV, 16, 1024);           // V, K-major (A of dP^T)
+        const uint64_t dK_mn = sdesc_sw128(sK, T::K_CHUNK, 1024);  // K, MN-major (A of dQ^T)
+        const uint64_t dDS = sdesc_sw128(sDS, T::DS_CHUNK, 1024);  // dS^T, MN-major (B of dQ^T)
+        // S^T = K Q^T or dP^T = V dO^T: A (keys) and B (queries) both K-major.
+        auto issue_t = [&](uint32_t dst, uint64_t a, uint32_t b_tile) {
+            const uint64_t b = sdesc_sw128(b_tile, 16, 1024);
 #pragma unroll
-                for (int ks = 0; ks < D / 16; ++ks) {
-                    const uint32_t koff = (ks & 3) * 32, kc = ks >> 2;
-                    mma_ss_elect(tmem + T::TM_ST, desc_add(dK_k, kc * T::K_CHUNK + koff),
-                                 desc_add(dQ_k, kc * T::Q_CHUNK + koff), kIdescT, ks > 0 ? 1u : 0u);
-                }
+            for (int ks = 0; ks < D / 16; ++ks) {
+                const uint32_t koff = (ks & 3) * 32, kc = ks >> 2;
+                mma_ss_elect(tmem + dst, desc_add(a, kc * T::K_CHUNK + koff),
+                             desc_add(b, kc * T::Q_CHUNK + koff), kIdescT, ks > 0 ? 1u : 0u);
+            }
+        };
+        // dV += P^T dO or dK += dS^T Q: A (bf16, K = queries) from TMEM, where
+        // warpgroup h put queries [64h, 64h + 64) at columns 64h .. 64h + 31; B MN-major.
+        auto issue_acc = [&](uint32_t dst, uint32_t a_col, uint32_t b_tile, bool first) {
+            const uint64_t b = sdesc_sw128(b_tile, T::Q_CHUNK, 1024);
 #pragma unroll
-                for (int ks = 0; ks < D / 16; ++ks) {
-                    const uint32_t koff = (ks & 3) * 32, kc = ks >> 2;
-                    mma_ss_elect(tmem + T::TM_DPT, desc_add(dV_k, kc * T::K_CHUNK + koff),
-                                 desc_add(dDO_k, kc * T::Q_CHUNK + koff), kIdescT, ks > 0 ? 1u : 0u);
-                }
-                tc_commit_elect(bar_s_full);
-            };
-            bool ok = mbar_wait_warp(bar_kv_full, 0, g, SITE_BWD_MMA_KV) &&
-                      mbar_wait_warp(bar_q_full, 0, g, SITE_BWD_MMA_Q_FULL);
+            for (int ks = 0; ks < BQ / 16; ++ks)
+                mma_ts_elect(tmem + dst, tmem + a_col + 64 * (ks >> 2) + 8 * (ks & 3),
+                             desc_add(b, ks * 2048), kIdescAcc, (!first || ks > 0) ? 1u : 0u);
+        };
+        bool ok = mbar_wait_warp<true>(bar_kv_full, 0, g, SITE_BWD_MMA_KV) &&
+                  mbar_wait_warp<true>(bar_q_full, 0, g, SITE_BWD_MMA_Q_FULL);
+        tc_fence_after();
+        if (ok) {
+            issue_t(T::TM_X, dK_k, sQ);
+            tc_commit_elect(bar_s_full);
+        }
+        for (int it = 0; ok && it < n_it; ++it) {
+            const int qs = it % QS, os = it % OS;
+            // 1. dP^T(it) into Y once dQ^T(it - 1) has been read out of it
+            if (!(ok = mbar_wait_warp<true>(bar_o_full + 8 * os, (it / OS) & 1, g, SITE_BWD_MMA_Q_FULL)))
+                break;
+            if (it > 0 &&
+                !(ok = mbar_wait_warp<true>(bar_dq_empty, (it - 1) & 1, g, SITE_BWD_MMA_DQ_FREE)))
+                break;
             tc_fence_after();
-            if (ok) issue_st_dpt(0);
-            for (int it = 0; ok && it < n_it; ++it) {
-                const int s = it % QS;
-                // 1. S^T, dP^T of the next block, once the compute warps have read this one.
-                if (it + 1 < n_it) {
-                    ok = mbar_wait_warp(bar_st_free, it & 1, g, SITE_BWD_MMA_DS_FULL) &&
-                         mbar_wait_warp(bar_q_full + 8 * ((it + 1) % QS), ((it + 1) / QS) & 1, g,
-                                        SITE_BWD_MMA_Q_FULL);
-                    if (!ok) break;
-                    tc_fence_after();
-                    issue_st_dpt(it + 1);
-                }
-                // 2. dV += P^T dO_i, dK += dS^T Q_i (K = 64 queries, 16 per step).
-                if (!(ok = mbar_wait_warp(bar_ds_full, it & 1, g, SITE_BWD_MMA_DS_FULL))) break;
-                tc_fence_after();
-                const uint64_t dQ_mn = sdesc_sw128(sQ + s * T::Q_BYTES, T::Q_CHUNK, 1024);
-                const uint64_t dDO_mn = sdesc_sw128(sDO + s * T::Q_BYTES, T::Q_CHUNK, 1024);
-#pragma unroll
-                for (int ks = 0; ks < BQ / 16; ++ks)
-                    mma_ts_elect(tmem + T::TM_DV, tmem + T::TM_PD + ks * 8, desc_add(dDO_mn, ks * 2048),
-                                 kIdescAcc, (it > 0 || ks > 0) ? 1u : 0u);
-#pragma unroll
-                for (int ks = 0; ks < BQ / 16; ++ks)
-                    mma_ts_elect(tmem + T::TM_DK, tmem + T::TM_PD + 32 + ks * 8,
-                                 desc_add(dQ_mn, ks * 2048), kIdescAcc, (it > 0 || ks > 0) ? 1u : 0u);
-                tc_commit_elect(bar_pd_free);
-                tc_commit_elect(bar_q_empty + 8 * s);
-                // 3. dQ^T[d][q] = sum_k K[k][d] dS^T[k][q] (K = 128 keys, 16 per step).
-                if (it >= 1 &&
-                    !(ok = mbar_wait_warp(bar_dq_empty, (it - 1) & 1, g, SITE_BWD_MMA_DQ_FREE)))
+            issue_t(T::TM_Y, dV_k, sDO + os * T::Q_BYTES);
+            tc_commit_elect(bar_dp_full);
+            // 2. dV += P^T(it) dO(it); dO(it) is then done with.
+            if (!(ok = mbar_wait_warp<true>(bar_p_full, it & 1, g, SITE_BWD_MMA_DS_FULL))) break;
+            tc_fence_after();
+            issue_acc(T::TM_DV, T::TM_X, sDO + os * T::Q_BYTES, it == 0);
+            tc_commit_elect(bar_o_empty + 8 * os);
+            // 3. S^T(it + 1) into X (P^T(it) is read by dV(it), issued before)
+            if (it + 1 < n_it) {
+                const int qn = (it + 1) % QS;
+                if (!(ok = mbar_wait_warp<true>(bar_q_full + 8 * qn, ((it + 1) / QS) & 1, g,
+                                          SITE_BWD_MMA_Q_FULL)))
                     break;
                 tc_fence_after();
-#pragma unroll
-                for (int ks = 0; ks < T::BN / 16; ++ks)
-                    mma_ss_elect(tmem + T::TM_DQ, desc_add(dK_mn, ks * 2048), desc_add(dDS, ks * 2048),
-                                 kIdescDQ, ks > 0 ? 1u : 0u);
-                tc_commit_elect(bar_dq_full);
+                issue_t(T::TM_X, dK_k, sQ + qn * T::Q_BYTES);
+                tc_commit_elect(bar_s_full);
             }
-            tc_commit_elect(bar_done);
-            volatile int never = 0;
-            const Guard g2{status, &never, kWaitLimitNs};
-            mbar_wait_warp(bar_done, 0, g2, SITE_BWD_DRAIN);
+            // 4. dK += dS^T(it) Q(it); Q(it) and its vectors are then done with.
+            if (!(ok = mbar_wait_warp<true>(bar_ds_full, it & 1, g, SITE_BWD_MMA_DS_FULL))) break;
+            tc_fence_after();
+            issue_acc(T::TM_DK, T::TM_Y, sQ + qs * T::Q_BYTES, it == 0);
+            tc_commit_elect(bar_q_empty + 8 * qs);
+            // 5. dQ^T(it)[d][q] = sum_k K[k][d] dS^T[k][q] into Y (K = 128 keys, 16 per step)
+#pragma unroll
+            for (int ks = 0; ks < T::BN / 16; ++ks)
+                mma_ss_elect(tmem + T::TM_Y, desc_add(dK_mn, ks * 2048), desc_add(dDS, ks * 2048),
+                             kIdescDQ, ks > 0 ? 1u : 0u);
+            tc_commit_elect(bar_dq_full);
         }
-    } else if (warp < 8) {
-        // ------------------------------------------------------- P^T and dS^T
-        const int h = warp >> 2;          // query columns [32h, 32h + 32) of each block
-        const int r = threadIdx.x & 127;  // key row within the block (TMEM lane)
-        const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+        tc_commit_elect(bar_done);
+        volatile int never = 0;
+        const Guard g2{status, &never, kWaitLimitNs};
+        mbar_wait_warp<true>(bar_done, 0, g2, SITE_BWD_DRAIN);
+    } else if (warp >= 16) {
+        setmaxnreg_dec<T::REG_MISC>();  // warps 18-19: no role
+    } else {
+        // ------------------------------------------------------- warps 0-15
+        // Thread = key row r (TMEM lane).  Warpgroup wg: 0-1 compute P and dS of
+        // query columns [64h, 64h + 64) of every block (h = wg): P = exp2(S^T scale
+        // log2e - L log2e) into X, dS = P o (dP - D) into Y and into shared memory.
+        // 2-3 read dQ^T columns [64h, 64h + 64) (h = wg - 2) out of Y and add them
+        // into global dQ.
+        const int wg = warp >> 2;
+        const int h = wg & 1;
+        const int qt = warp & 3;          // TMEM lane quarter
+        const int r = threadIdx.x & 127;  // key row within the block
+        const uint32_t lane_base = (uint32_t)(qt * 32) << 16;
         const int key = kv0 + r;
         bool ok = true;
-        for (int it = 0, qb = qb_first, gq = gq_first; it < n_it;
-             ++it, (++qb == n_qit) ? (qb = 0, ++gq) : 0) {
-            const int s = it % QS;
-            const int q0 = (i_start + qb) * BQ;
-            ok = mbar_wait_warp(bar_s_full, it & 1, g, SITE_BWD_SOFTMAX_S_FULL);
-            if (!ok) break;
-            tc_fence_after();
-            uint32_t sv[32], dpv[32];
-            tmem_ld32(tmem + lane_base + T::TM_ST + 32 * h, sv);
-            tmem_ld32(tmem + lane_base + T::TM_DPT + 32 * h, dpv);
-            tmem_wait_ld(sv);
-            tmem_wait_ld(dpv);
-            tc_fence_before();
-            mbar_arrive(bar_st_free);  // S^T / dP^T may now be overwritten
-            const bool need_mask = (kv0 + T::BN > len) || (CAUSAL && q0 < kv0 + T::BN - 1);
-            const float *l2v = l2_f + s * BQ + 32 * h;
-            const float *dlv = delta_f + s * BQ + 32 * h;
-            uint32_t pk[16], dk_[16];
-            const uint64_t c2 = f32x2_splat(scale_log2);
-#pragma unroll
-            for (int e = 0; e < 32; e += 4) {
-                // the workspace holds -L log2e and -D, so both steps are packed pair
-                // operations (the same roundings as s*c - L and dP - D)
-                const float4 l4 = *reinterpret_cast<const float4 *>(l2v + e);
-                const float4 d4 = *reinterpret_cast<const float4 *>(dlv + e);
-                float p[4], ds[4];
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    p[u] = __uint_as_float(sv[e + u]);
-                    ds[u] = __uint_as_float(dpv[e + u]);
-                }
-                fma_f32x2(p[0], p[1], c2, l4.x, l4.y);
-                fma_f32x2(p[2], p[3], c2, l4.z, l4.w);
-                add_f32x2(ds[0], ds[1], d4.x, d4.y);
-                add_f32x2(ds[2], ds[3], d4.z, d4.w);
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    p[u] = ex2(p[u]);
-                    if (need_mask) {
-                        const int q = q0 + 32 * h + e + u;
-                        if (key >= len || (CAUSAL && q < key)) p[u] = 0.f;
-                    }
-                }
-                mul_f32x2(ds[0], ds[1], p[0], p[1]);
-                mul_f32x2(ds[2], ds[3], p[2], p[3]);
-                pk[e / 2] = pack_bf16(p[0], p[1]);
-                pk[e / 2 + 1] = pack_bf16(p[2], p[3]);
-                dk_[e / 2] = pack_bf16(ds[0], ds[1]);
-                dk_[e / 2 + 1] = pack_bf16(ds[2], ds[3]);
-            }
-            // dS^T row r, queries [32h, 32h + 32): 4 swizzled 16-byte units (MN-major).
-            // The single dS^T buffer is free once dQ^T of the previous block is done.
-            if (it > 0 && !(ok = mbar_wait_warp(bar_dq_full, (it - 1) & 1, g,
-                                                SITE_BWD_SOFTMAX_S_FULL)))
-                break;
-            uint8_t *ds_row = gbase + T::OFF_DS + r * 128;
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int unit = 4 * h + u;
-                *reinterpret_cast<uint4 *>(ds_row + ((unit ^ (r & 7)) * 16)) =
-                    make_uint4(dk_[4 * u], dk_[4 * u + 1], dk_[4 * u + 2], dk_[4 * u + 3]);
-            }
-            // PD is free once dV/dK of the previous block have read it.
-            if (it > 0 && !(ok = mbar_wait_warp(bar_pd_free, (it - 1) & 1, g,
-                                                SITE_BWD_SOFTMAX_S_FULL)))
-                break;
-            tc_fence_after();
-            tmem_st16(tmem + lane_base + T::TM_PD + 16 * h, pk);
-            tmem_st16(tmem + lane_base + T::TM_PD + 32 + 16 * h, dk_);
-            tmem_wait_st();
-            fence_proxy_async_smem();
-            tc_fence_before();
-            mbar_arrive(bar_ds_full);
-        }
         // ------------------------------------------------------- dK, dV epilogue
-        // dK and dV are final once the last block's dV/dK products are done
-        // (pd_free); the last dQ^T product, which reads only K and dS^T, still runs
-        // while they leave through the Q/dO ring.
-        ok = ok && mbar_wait_warp(bar_pd_free, (n_it - 1) & 1, g, SITE_BWD_EPILOGUE);
-        if (ok) {
-            tc_fence_after();
-            // Each thread owns half a key row (d columns [64h, min(64h + 64, D))).  Rows are
-            // staged in shared memory at a 528-byte pitch (16-byte writes without bank
-            // conflicts; the Q/dO area is free once every MMA is done) and leave with
-            // one bulk copy per half-row, so global writes are 256 contiguous bytes.
-            constexpr uint32_t kPitch = T::DP * 4 + 16;  // 16-byte units shift by one per row
-            static_assert(128 * kPitch <= T::OFF_DS - T::OFF_Q, "epilogue staging fits Q/dO area");
-            uint8_t *stg = gbase + T::OFF_Q + r * kPitch + 256 * h;
-            const uint32_t stg_s = sQ + r * kPitch + 256 * h;
-#pragma unroll 1
-            for (int pass = 0; pass < 2; ++pass) {  // 0: dV, 1: dK (times scale)
+        auto epilogue = [&]() {
+            // Every product is done: dK and dV are final.  Warpgroups 0-1 take dV, 2-3
+            // dK (times scale); each thread owns half a key row (d columns
+            // [64h, min(64h + 64, D))).  Rows are staged in shared memory at a 528-byte
+            // pitch (16-byte writes without bank conflicts; the Q/dO rings and the dS^T
+            // tile are idle once every MMA is done) and leave with one bulk copy per
+            // half-row, so global writes are 256 contiguous bytes.
+            if (ok) {
+                const int pass = wg >> 1;  // 0: dV, 1: dK
+                constexpr uint32_t kPitch = T::DP * 4 + 16;  // 16-byte units shift by one per row
+                static_assert(2 * 128 * kPitch <= T::OFF_L2 - T::OFF_Q, "epilogue staging fits");
+                const uint32_t soff = T::OFF_Q + (pass * 128 + r) * kPitch + 256 * h;
+                uint8_t *stg = gbase + soff;
                 const uint32_t tcol = (pass == 0 ? T::TM_DV : T::TM_DK) + 64 * h;
                 const float mul = pass == 0 ? 1.f : scale;
-                if (pass == 1) bulk_wait_group_read<0>();  // own staging row is reused
                 constexpr int kHalf1 = (D - 64) / 32;  // 32-column loads of the second half
 #pragma unroll
                 for (int c = 0; c < 2; ++c) {
@@ -576,99 +566,174 @@ __global__ void __launch_bounds__(448, 1)
                 if (key < len && (h == 0 || D > 64)) {
                     const size_t krow =
                         VARLEN ? (size_t)(tok0 + key) * (H / group) + hk : (size_t)kvh * N + key;
-                    float *dst = (pass == 0 ? dv : dk) + krow * D + 64 * h;
-                    const uint32_t nb = h == 0 ? 256u : (uint32_t)(D - 64) * 4;
+                    float *dstg = (pass == 0 ? dv : dk) + krow * D + 64 * h;
+                    const uint32_t nb = h == 0 ? (uint32_t)min(D, 64) * 4 : (uint32_t)(D - 64) * 4;
                     if constexpr (SPLIT)
-                        bulk_reduce_add_f32(dst, stg_s, nb);
+                        bulk_reduce_add_f32(dstg, base + soff, nb);
                     else
-                        bulk_store(dst, stg_s, nb);
+                        bulk_store(dstg, base + soff, nb);
                 }
                 bulk_commit_group();
             }
-            bulk_wait_group_read<0>();
-        }
-        tmem_wait_st();
-    } else {
-        // ------------------------------------------------------- dQ readout (warps 8-11)
-        const int t = threadIdx.x - 256;  // TMEM lane = column d of dQ
-        if (warp == 8) griddep_wait();    // dQ was zeroed by the preprocess kernel
-        const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-        bool ok = true;
-        for (int it = 0, qb = qb_first, gq = gq_first; it < n_it;
-             ++it, (++qb == n_qit) ? (qb = 0, ++gq) : 0) {
-            const int q0 = (i_start + qb) * BQ;
-            ok = mbar_wait_warp(bar_dq_full, it & 1, g, SITE_BWD_DQ_FULL);
-            if (!ok) break;
-            tc_fence_after();
-            uint32_t x0[32], x1[32];
-            tmem_ld32(tmem + lane_base + T::TM_DQ, x0);
-            tmem_ld32(tmem + lane_base + T::TM_DQ + 32, x1);
-            tmem_wait_ld(x0);
-            tmem_wait_ld(x1);
-            tc_fence_before();
-            mbar_arrive(bar_dq_empty);
-            // dQ^T column t of the block's 64 rows -> row-major fp32 staging tile ->
-            // one bulk asynchronous add into the block's contiguous global dQ rows.
-            // The tile is free once the previous bulk add has read it; every sync here
-            // is a bounded mbarrier wait, so an abort cannot strand a warp.
-            if (warp == 8) {
-                bulk_wait_group_read<0>();  // every lane's adds of the previous block
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar_stg_free);
-            }
-            ok = mbar_wait_warp(bar_stg_free, it & 1, g, SITE_BWD_DQ_FULL);
-            if (!ok) break;
-            if (t < D) {  // rows of dQ^T past d are zero padding
+        };
+        if (wg < 2) {
+            setmaxnreg_inc<T::REG_PDS>();
+            const uint64_t c2 = f32x2_splat(scale_log2);
+            float p[64];  // P of this thread's 64 queries, kept for dS
+
+            // P(it) from S^T(it) in X, in two 32-column halves.
+            auto p_stage = [&](int it, int q0) -> bool {
+                if (!mbar_wait_warp<true>(bar_s_full, it & 1, g, SITE_BWD_SOFTMAX_S_FULL)) return false;
+                tc_fence_after();
+                const bool need_mask = (kv0 + T::BN > len) || (CAUSAL && q0 < kv0 + T::BN - 1);
+                const float *l2v = l2_f + (it % QS) * BQ + 64 * h;
 #pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    stage_f[e * D + t] = __uint_as_float(x0[e]) * scale;
-                    stage_f[(e + 32) * D + t] = __uint_as_float(x1[e]) * scale;
-                }
-            }
-            fence_proxy_async_smem();
-            mbar_arrive(bar_stg_full);
-            if (warp == 8) {
-                bool ok0 = true;
-                const int rows = min(BQ, len - q0);
-                if constexpr (VARLEN) {
-                    // token-major dQ: the block's rows of this head are H * D floats
-                    // apart; one tiled add through the (d, heads, T) tensor map writes
-                    // all of them.  Rows of the block past the sequence's end hold exact
-                    // zeros (their P is 0), so adding them into the next sequence's rows
-                    // leaves those unchanged; rows past T are skipped by the copy.
-                    if (lane == 0) {
-                        ok0 = mbar_wait(bar_stg_full, it & 1, g, SITE_BWD_DQ_FULL);
-                        if (ok0) {
-                            tma_reduce_add_3d(&tm_dq, sStage, 0, (bhq0 + gq) % H, tok0 + q0);
-                            bulk_commit_group();
+                for (int c = 0; c < 2; ++c) {
+                    uint32_t sv[32];
+                    tmem_ld32(tmem + lane_base + T::TM_X + 64 * h + 32 * c, sv);
+                    tmem_wait_ld(sv);
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int e = 0; e < 32; e += 4) {
+                        // the workspace holds -L log2e, so this is one packed FMA per pair
+                        const float4 l4 = *reinterpret_cast<const float4 *>(l2v + 32 * c + e);
+                        float *pp = p + 32 * c + e;
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) pp[u] = __uint_as_float(sv[e + u]);
+                        fma_f32x2(pp[0], pp[1], c2, l4.x, l4.y);
+                        fma_f32x2(pp[2], pp[3], c2, l4.z, l4.w);
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            pp[u] = ex2(pp[u]);
+                            if (need_mask) {
+                                const int q = q0 + 64 * h + 32 * c + e + u;
+                                if (key >= len || (CAUSAL && q < key)) pp[u] = 0.f;
+                            }
                         }
+                        pk[e / 2] = pack_bf16(pp[0], pp[1]);
+                        pk[e / 2 + 1] = pack_bf16(pp[2], pp[3]);
                     }
-                } else {
-                    if (lane == 0) {
-                        ok0 = mbar_wait(bar_stg_full, it & 1, g, SITE_BWD_DQ_FULL);
-                        if (ok0) {
-                            bulk_reduce_add_f32(dq + ((size_t)(bhq0 + gq) * N + q0) * D, sStage,
-                                                (uint32_t)(rows * D * 4));
-                            bulk_commit_group();
-                        }
+                    // P of columns [32c, 32c + 32) lands on columns [16c, 16c + 16),
+                    // whose S values this thread has already read
+                    tmem_st16(tmem + lane_base + T::TM_X + 64 * h + 16 * c, pk);
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(bar_p_full);
+                return true;
+            };
+
+            // dS(it) = P o (dP - D) from dP^T(it) in Y: bf16 into Y (A of dK) and into
+            // the shared dS^T tile (B of dQ^T).
+            auto ds_stage = [&](int it) -> bool {
+                if (!mbar_wait_warp<true>(bar_dp_full, it & 1, g, SITE_BWD_SOFTMAX_S_FULL)) return false;
+                tc_fence_after();
+                const float *dlv = delta_f + (it % QS) * BQ + 64 * h;
+                uint8_t *ds_row = gbase + T::OFF_DS + h * T::DS_CHUNK + r * 128;
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    uint32_t dpv[32];
+                    tmem_ld32(tmem + lane_base + T::TM_Y + 64 * h + 32 * c, dpv);
+                    tmem_wait_ld(dpv);
+                    uint32_t dsk[16];
+#pragma unroll
+                    for (int e = 0; e < 32; e += 4) {
+                        // the workspace holds -D, so dP - D is a packed add
+                        const float4 d4 = *reinterpret_cast<const float4 *>(dlv + 32 * c + e);
+                        const float *pp = p + 32 * c + e;
+                        float ds[4];
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) ds[u] = __uint_as_float(dpv[e + u]);
+                        add_f32x2(ds[0], ds[1], d4.x, d4.y);
+                        add_f32x2(ds[2], ds[3], d4.z, d4.w);
+                        mul_f32x2(ds[0], ds[1], pp[0], pp[1]);
+                        mul_f32x2(ds[2], ds[3], pp[2], pp[3]);
+                        dsk[e / 2] = pack_bf16(ds[0], ds[1]);
+                        dsk[e / 2 + 1] = pack_bf16(ds[2], ds[3]);
+                    }
+                    tmem_st16(tmem + lane_base + T::TM_Y + 64 * h + 16 * c, dsk);
+                    // dS^T row r, queries [64h + 32c, +32): 4 swizzled 16-byte units
+                    // of the 64-query chunk h (MN-major)
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const int unit = 4 * c + u;
+                        *reinterpret_cast<uint4 *>(ds_row + ((unit ^ (r & 7)) * 16)) = make_uint4(
+                            dsk[4 * u], dsk[4 * u + 1], dsk[4 * u + 2], dsk[4 * u + 3]);
                     }
                 }
-                ok0 = __shfl_sync(0xffffffffu, ok0 ? 1 : 0, 0) != 0;
-                if (!ok0) {
-                    ok = false;
-                    break;
-                }
+                tmem_wait_st();
+                fence_proxy_async_smem();
+                tc_fence_before();
+                mbar_arrive(bar_ds_full);
+                return true;
+            };
+
+            ok = p_stage(0, (i_start + qb_first) * BQ);
+            for (int it = 0, qb = qb_first; ok && it < n_it; ++it, (++qb == n_qit) ? (qb = 0) : 0) {
+                ok = ds_stage(it);
+                if (ok && it + 1 < n_it) ok = p_stage(it + 1, (i_start + (qb + 1 == n_qit ? 0 : qb + 1)) * BQ);
             }
+            // every product is done once the last dQ^T is
+            ok = ok && mbar_wait_warp<true>(bar_dq_full, (n_it - 1) & 1, g, SITE_BWD_EPILOGUE);
+            if (ok) epilogue();
+        } else {
+            setmaxnreg_dec<T::REG_DQ>();
+            griddep_wait();  // dQ is zeroed by the preprocess kernel before any add below
+            // dQ(it): dQ^T rows [32 qt, +32) (d = 32 qt + lane) of queries [64h, 64h + 64)
+            // leave Y into registers; then, scaled, each 32-query half goes through this
+            // warp's 4 KB staging tile ([32 queries][32 columns] fp32) and one tiled
+            // bulk add into global dQ (rows past the end of the sequence are skipped
+            // by the copy, or hold exact zeros).
+            const uint32_t s_stage = base + T::OFF_STG + (warp - 8) * 4096u;
+            float *stage_f = reinterpret_cast<float *>(gbase + T::OFF_STG + (warp - 8) * 4096u);
+            auto stage_add = [&](const uint32_t(&x)[32], int row, int head) {
+                if (lane == 0) bulk_wait_group_read<0>();  // the tile's previous add has read it
+                __syncwarp();
+#pragma unroll
+                for (int e = 0; e < 32; ++e) stage_f[e * 32 + lane] = __uint_as_float(x[e]) * scale;
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    if constexpr (VARLEN)
+                        tma_reduce_add_3d(&tm_dq, s_stage, 32 * qt, head, tok0 + row);
+                    else
+                        tma_reduce_add_3d(&tm_dq, s_stage, 32 * qt, row, head);
+                    bulk_commit_group();
+                }
+            };
+            for (int it = 0, qb = qb_first, gq = gq_first; it < n_it;
+                 ++it, (++qb == n_qit) ? (qb = 0, ++gq) : 0) {
+                if (!(ok = mbar_wait_warp<true>(bar_dq_full, it & 1, g, SITE_BWD_DQ_FULL))) break;
+                tc_fence_after();
+                uint32_t x0[32], x1[32];
+                tmem_ld32(tmem + lane_base + T::TM_Y + 64 * h, x0);
+                tmem_ld32(tmem + lane_base + T::TM_Y + 64 * h + 32, x1);
+                tmem_wait_ld(x0);
+                tmem_wait_ld(x1);
+                tc_fence_before();
+                mbar_arrive(bar_dq_empty);
+                if (32 * qt >= D) continue;  // rows of dQ^T past d are padding
+                const int row0 = (i_start + qb) * BQ + 64 * h;
+                const int head = VARLEN ? (bhq0 + gq) % H : bhq0 + gq;
+                stage_add(x0, row0, head);
+                stage_add(x1, row0 + 32, head);
+            }
+            // The staging tiles' reads finish before the dK epilogue reuses the area.
+            if (lane == 0) bulk_wait_group_read<0>();
+            __syncwarp();
+            named_barrier_sync(1, 256);
+            if (ok) epilogue();
         }
-        // Only the shared-memory reads of the last bulk add must finish before the
-        // CTA retires; its global writes complete before the kernel does.
-        if (warp == 8) bulk_wait_group_read<0>();
+        // The shared-memory reads of this thread's bulk copies and adds finish before
+        // the CTA retires; their global writes complete before the kernel does.
+        bulk_wait_group_read<0>();
+        tmem_wait_st();
     }
 
     __syncwarp();
     tc_fence_before();
     __syncthreads();
-    if (warp == 13) {
+    if (warp == kMmaWarp) {
         tc_fence_after();
         tmem_dealloc(tmem, T::TM_COLS);
     }
@@ -714,9 +779,13 @@ int launch_bwd_t(const BwdParams &p, cudaStream_t stream) {
     const int head_group = (VARLEN || !CAUSAL) ? min(8, p.BH / p.group) : p.BH / p.group;
     if (grid > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
     auto launch = [&](auto kern) -> int {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)W::SMEM_BYTES) != cudaSuccess)
+        if (ensure_smem_attr(reinterpret_cast<const void *>(kern), (int)W::SMEM_BYTES) != FA_OK)
             return FA_ERR_CUDA;
+        // The warpgroups' register budgets add up to the launch allocation; a build
+        // that launches with any other count could leave a warpgroup waiting for
+        // registers forever, so it is refused here.
+        if (kernel_num_regs(reinterpret_cast<const void *>(kern)) != W::LAUNCH_REGS)
+            return FA_ERR_UNSUPPORTED;
         // Launched as a programmatic dependent of the preprocess kernel: its CTAs set
         // up (barriers, tensor memory, K/V loads) while the preprocess finishes, and
         // wait for it only where they read its results.
@@ -731,7 +800,7 @@ int launch_bwd_t(const BwdParams &p, cudaStream_t stream) {
         cfg.attrs = attr;
         cfg.numAttrs = 1;
         if (cudaLaunchKernelEx(&cfg, kern, p.tm_q, p.tm_k, p.tm_v, p.tm_do, p.tm_dq, p.ws_lse2,
-                               p.ws_delta, p.dq, p.dk, p.dv, p.N, p.Npad, p.BH / p.group, p.H,
+                               p.ws_delta, p.dk, p.dv, p.N, p.Npad, p.BH / p.group, p.H,
                                p.group, head_group, p.cu_seqlens, p.total_tokens, p.scale,
                                p.scale_log2, p.status, p.limit_ns) != cudaSuccess)
             return FA_ERR_CUDA;

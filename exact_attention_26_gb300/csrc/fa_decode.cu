@@ -12,7 +12,10 @@
 // warp and four compute warps; compute warp w takes keys [w*KW, w*KW + KW) of
 // every stage, its lanes split the head dimension, and each warp keeps its own
 // running (max, sum, output) per query row until the four are merged at the end.
+#include <atomic>
+
 #include "fa_internal.h"
+
 #include "fa_ptx.cuh"
 
 namespace fa {
@@ -431,8 +434,7 @@ template <int D, int QB, bool PAGED>
 int launch_decode_t(const DecodeParams &p, cudaStream_t stream) {
     using T = DecTile<D>;
     auto kern = fa_decode_split_kernel<D, QB, PAGED>;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)T::SMEM_BYTES) !=
-        cudaSuccess)
+    if (ensure_smem_attr(reinterpret_cast<const void *>(kern), (int)T::SMEM_BYTES) != FA_OK)
         return FA_ERR_CUDA;
     const int R = p.group * p.Nq;
     const dim3 grid((unsigned)(p.BH / p.group), (unsigned)p.S, (unsigned)((R + QB - 1) / QB));
@@ -468,16 +470,27 @@ int launch_decode_d(const DecodeParams &p, cudaStream_t stream) {
     return one ? launch_decode_t<D, 1, false>(p, stream) : launch_decode_t<D, QB, false>(p, stream);
 }
 
+// Resident CTAs per SM of the split kernel, asked of the runtime once per
+// (instantiation, device) and remembered.
 template <int D, int QB>
 int ctas_per_sm_t() {
+    static std::atomic<int> cached[kMaxCachedDevices];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+    const bool cacheable = dev >= 0 && dev < kMaxCachedDevices;
+    if (cacheable) {
+        const int c = cached[dev].load(std::memory_order_relaxed);
+        if (c > 0) return c;
+    }
     auto kern = fa_decode_split_kernel<D, QB, false>;
     int n = 0;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)DecTile<D>::SMEM_BYTES) != cudaSuccess ||
+    if (ensure_smem_attr(reinterpret_cast<const void *>(kern), (int)DecTile<D>::SMEM_BYTES) != FA_OK ||
         cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, DecTile<D>::THREADS,
                                                       DecTile<D>::SMEM_BYTES) != cudaSuccess)
         return 1;
-    return n > 0 ? n : 1;
+    n = n > 0 ? n : 1;
+    if (cacheable) cached[dev].store(n, std::memory_order_relaxed);
+    return n;
 }
 
 template <int D>

@@ -723,9 +723,8 @@ template <int D, bool CAUSAL, bool VARLEN, bool F8 = false, bool ONE = false>
 int launch_fwd_t(const FwdParams &p, cudaStream_t stream) {
     using T = FwdTile<D, F8, ONE>;
     auto kern = fa_fwd_kernel<D, CAUSAL, VARLEN, F8, ONE>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)T::SMEM_BYTES);
-    if (e != cudaSuccess) return FA_ERR_CUDA;
+    if (ensure_smem_attr(reinterpret_cast<const void *>(kern), (int)T::SMEM_BYTES) != FA_OK)
+        return FA_ERR_CUDA;
     // varlen: N is the longest sequence the caller allows
     const int n_cblocks = (p.N + T::ROWS - 1) / T::ROWS;
     const long long items = (long long)n_cblocks * p.BH;

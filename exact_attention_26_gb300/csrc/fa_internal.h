@@ -31,6 +31,7 @@ enum WaitSite : int {
     SITE_BWD_EPILOGUE = 18,
     SITE_BWD_DRAIN = 19,
     SITE_BWD_BAD_SEQ = 20,
+    SITE_BWD_SMEM_ALIGN = 26,
     SITE_DEC_FULL = 21,
     SITE_DEC_EMPTY = 22,
     SITE_DEC_DRAIN = 23,
@@ -76,7 +77,8 @@ int bwd_block_q(int d);
 
 struct BwdParams {
     CUtensorMap tm_q, tm_k, tm_v, tm_do;  // 3-D maps over [BH][N][d] (q, do), [B*Hkv][N][d] (k, v)
-    CUtensorMap tm_dq;                    // varlen: fp32 dq (d, heads, T), box (d, 1, 64 rows)
+    CUtensorMap tm_dq;                    // fp32 dq: (d, N, BH) box (32, 32, 1), or packed
+                                          // (d, heads, T) box (32, 1, 32); tiled bulk adds
     const void *o, *dout;                 // bf16 [BH][N][d]
     const float *lse;                     // fp32 [BH][N]
     float *dq, *dk, *dv;                  // fp32 [BH][N][d]
@@ -110,6 +112,17 @@ struct DecodeParams {
     int *status;
     unsigned long long limit_ns;
 };
+
+// Devices the per-device caches of the host code cover (ordinals 0..63).
+constexpr int kMaxCachedDevices = 64;
+
+// Raise a kernel's dynamic shared memory limit to `bytes` once per (kernel,
+// device): the attribute stays with the function in the device's context, so
+// later launches skip the driver call.  FA_OK or FA_ERR_CUDA.
+int ensure_smem_attr(const void *kernel, int bytes);
+
+// Registers per thread a kernel is launched with (cached per kernel), or -1.
+int kernel_num_regs(const void *kernel);
 
 int launch_fwd(const FwdParams &p, cudaStream_t stream);
 int launch_bwd(const BwdParams &p, cudaStream_t stream);

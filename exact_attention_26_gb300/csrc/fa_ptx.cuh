@@ -79,8 +79,8 @@ struct Guard {
     unsigned long long limit_ns;
 };
 
-__device__ __noinline__ inline bool mbar_wait_slow(uint32_t bar, uint32_t parity, const Guard &g,
-                                                   int site) {
+__device__ __forceinline__ bool mbar_wait_slow_body(uint32_t bar, uint32_t parity, const Guard &g,
+                                                    int site) {
     const uint64_t t0 = global_timer_ns();
     for (;;) {
         if (mbar_try_wait_sleep(bar, parity, 100000u)) return true;
@@ -94,19 +94,32 @@ __device__ __noinline__ inline bool mbar_wait_slow(uint32_t bar, uint32_t parity
     }
 }
 
+__device__ __noinline__ inline bool mbar_wait_slow(uint32_t bar, uint32_t parity, const Guard &g,
+                                                   int site) {
+    return mbar_wait_slow_body(bar, parity, g, site);
+}
+
 // Wait until the phase with the given parity of barrier `bar` has completed.
 // Returns false (after recording FA_ERR_TIMEOUT, or because another role of this
-// CTA already gave up) instead of spinning forever.
+// CTA already gave up) instead of spinning forever.  The slow path is a called
+// function, except with kInline: a kernel whose warpgroups rebalance registers
+// (setmaxnreg) cannot share one compiled function across their different
+// register budgets, so it inlines the slow path at every wait.
+template <bool kInline = false>
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const Guard &g, int site) {
     if (mbar_try_wait(bar, parity)) return true;
-    return mbar_wait_slow(bar, parity, g, site);
+    if constexpr (kInline)
+        return mbar_wait_slow_body(bar, parity, g, site);
+    else
+        return mbar_wait_slow(bar, parity, g, site);
 }
 
 // The same for all 32 lanes of a warp; the result is warp-uniform, so code after
 // it may issue warp-collective (.sync.aligned) instructions.
+template <bool kInline = false>
 __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, const Guard &g,
                                                int site) {
-    bool ok = mbar_wait(bar, parity, g, site);
+    bool ok = mbar_wait<kInline>(bar, parity, g, site);
     return __all_sync(0xffffffffu, ok);
 }
 
@@ -366,6 +379,25 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t *r) {
 
 __device__ __forceinline__ void tmem_wait_st() {
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// Barrier `id` (1-15; 0 is __syncthreads) over the first `count` threads that
+// reach it, a multiple of 32.
+__device__ __forceinline__ void named_barrier_sync(int id, int count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// Warpgroup register reallocation: every warp of a warpgroup makes the same call.
+// dec returns registers to the CTA's pool; inc waits until the pool can supply
+// them, so the targets of all warpgroups must add up to no more than the
+// registers the CTA was launched with.
+template <int N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
 }
 
 // ------------------------------------------------------------------ numerics
