@@ -15,6 +15,13 @@ is bracketed by a barrier and a synchronize, and the slowest rank's time counts.
 
 --impl reference times the float64 CPU oracle on the host cores instead (a
 bounded row sample of the same workload per step).
+
+The line ends with `targets`: the five configurations the parity and throughput
+target is stated on (C1-C5), each with TFLOPS, its fraction of the measured bf16
+GEMM peak and of the clock-derived tensor peak, and the max-abs error of a seeded
+sample against the float64 oracle (checked in the cpu_baseline leg, the one leg
+that runs the oracle), plus whether the forward at N = 16384, d = 128 reaches 60%
+of the measured peak.
 """
 from __future__ import annotations
 
@@ -245,6 +252,47 @@ def run_forward_only(args):
                              "inputs": gen.__name__}, "ms": round(ms, 5), "tflops": round(tf, 2)}
 
 
+def run_backward_only(args):
+    """`--only-backward B H N d causal`: one backward shape (fa_bwd on the output of one
+    forward), W untimed and K timed calls (CUDA events, L2 flushed before each), one
+    JSON line.  A small, self-contained command for a profiler to capture the
+    backward's launches."""
+    import torch
+
+    import exact_attention_26_gb300 as fa
+    from exact_attention_26_gb300.inputs import normal_qkv
+
+    B, H, N, d, causal = (int(x) for x in args.only_backward)
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    fa.load()
+    q, k, v, do = (t.to(dev) for t in normal_qkv(B, H, N, d, seed=0, with_do=True))
+    o, lse = fa.forward(q, k, v, causal=bool(causal))
+    g = [torch.empty(q.shape, dtype=torch.float32, device=dev) for _ in range(3)]
+    ws = torch.empty(fa.fa_bwd_workspace_bytes(B, H, N, d), dtype=torch.uint8, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    ms = _time_call(torch, dev, lambda: fa.backward(q, k, v, o, lse, do, causal=bool(causal),
+                                                    dq=g[0], dk=g[1], dv=g[2], workspace=ws),
+                    flush, iters=args.steps, warm=args.warmup)
+    status = fa.fa_device_status(None)
+    if status != 0:
+        raise RuntimeError(f"device status {fa.fa_status_string(status)}")
+    tf = bwd_flops(B, H, N, d, bool(causal)) / (ms * 1e-3) / 1e12
+    return {"only_backward": {"B": B, "H": H, "N": N, "d": d, "causal": bool(causal)},
+            "ms": round(ms, 5), "tflops": round(tf, 2)}
+
+
+def run_config():
+    """The workload's description, the same for both arms of the benchmark."""
+    B, H, N, d, causal = (WORKLOAD[k] for k in ("B", "H", "N", "d", "causal"))
+    return {"workload": WORKLOAD_NAME, "B": B, "H": H, "N": N, "d": d, "causal": causal,
+            "scale": 1.0 / math.sqrt(d),
+            "inputs": "bf16(N(0,1)) q,k,v,dO from one torch CPU generator, seed 0",
+            "l2": f"flushed between steps ({L2_FLUSH_BYTES >> 20} MiB write, outside "
+                  "the per-step CUDA events)",
+            "per_rank": "each rank runs its own copy (independent batches)"}
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
     import torch.distributed as dist
@@ -349,12 +397,7 @@ def run_ours(args, rank, world, local_rank):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_ms, 5),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic",
-            "config": {"workload": WORKLOAD_NAME, "B": B, "H": H, "N": N, "d": d,
-                       "causal": causal, "scale": 1.0 / math.sqrt(d),
-                       "inputs": "bf16(N(0,1)) q,k,v,dO from one torch CPU generator, seed 0",
-                       "l2": f"flushed between steps ({L2_FLUSH_BYTES >> 20} MiB write, outside "
-                             "the per-step CUDA events)",
-                       "per_rank": "each rank runs its own copy (independent batches)"},
+            "config": run_config(),
             "fwd_ms": round(f_ms, 5), "bwd_ms": round(b_ms, 5),
             "fwd_tflops": round(fwd_flops(B, H, N, d, causal) / (f_ms * 1e-3) / 1e12, 2),
             "bwd_tflops": round(bwd_flops(B, H, N, d, causal) / (b_ms * 1e-3) / 1e12, 2),
@@ -407,11 +450,123 @@ def run_ours(args, rank, world, local_rank):
             result["decode_workloads"] = sweep_decode(fa, torch, dev, flush, load_peaks())
             result["fp8_workloads"] = sweep_fp8(fa, torch, dev, flush, load_peaks())
             result["gqa_varlen_workloads"] = sweep_gqa_varlen(fa, torch, dev, flush, load_peaks())
+        targets, jobs = None, []
+        if world == 1 and not args.no_targets:
+            targets, jobs = sweep_targets(fa, torch, dev, flush, load_peaks(), rates,
+                                          (f_ms, b_ms), (q_h, k_h, v_h, do_h),
+                                          (o, lse, dq, dk, dv))
         if world == 1 and not args.no_cpu_baseline:
             result["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
+            if targets is not None:
+                parity_sample(targets, jobs)
         else:
             result["cpu_baseline"] = None
+        if targets is not None:
+            result["targets"] = targets  # last key: the shortest record of the line keeps it
     return result
+
+
+# The configurations the target is stated on: (name, B, H, N, d, masks, inputs).
+TARGET_CONFIGS = [
+    ("C1_B1H1N128d64", 1, 1, 128, 64, (False, True), "normal"),
+    ("C2_B8H16N2048d64", 8, 16, 2048, 64, (False, True), "normal"),
+    ("C3_B1H16N16384d128", 1, 16, 16384, 128, (True,), "normal"),
+    ("C4_B4H8N8192d256", 4, 8, 8192, 256, (False,), "boosted"),
+]
+TARGET_ROWS, TARGET_HEADS = 64, 2   # the oracle's seeded sample per configuration
+FWD_TARGET = 0.60                   # forward fraction of the bf16 peak at N >= 8192, d = 128
+
+
+def sweep_targets(fa, torch, dev, flush, peaks, rates, step_ms, step_inputs, step_outputs):
+    """The target configurations C1-C5: forward (and, C5, backward) TFLOPS, their
+    fraction of the measured bf16 GEMM peak and of the clock-derived peak, and the GPU
+    results of a seeded sample of rows and heads for the oracle to check in the
+    cpu_baseline leg (C5 reuses the timed step's inputs and outputs)."""
+    from exact_attention_26_gb300.inputs import boosted_qkv, normal_qkv, sample_rows
+    pk = peaks["bf16_tflops"]
+    pk_clk = (rates or {}).get("clock_derived_bf16_tflops")
+
+    def perf(flops, ms):
+        tf = flops / (ms * 1e-3) / 1e12
+        e = {"tflops": round(tf, 1), "frac": round(tf / pk, 3)}
+        if pk_clk:
+            e["frac_clk"] = round(tf / pk_clk, 3)
+        return e
+
+    out, jobs = {}, []
+    for name, B, H, N, d, masks, kind in TARGET_CONFIGS:
+        gen = boosted_qkv if kind == "boosted" else normal_qkv
+        qh, kh, vh = gen(B, H, N, d, seed=0)
+        q, k, v = (t.to(dev) for t in (qh, kh, vh))
+        o = torch.empty_like(q)
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+        rows = sample_rows(N, TARGET_ROWS, seed=2)
+        nh = min(TARGET_HEADS, B * H)
+        entry = {}
+        for causal in masks:
+            ms = _time_call(torch, dev, lambda: fa.forward(q, k, v, causal=causal, out=o, lse=lse),
+                            flush)
+            e = perf(fwd_flops(B, H, N, d, causal), ms)
+            torch.cuda.synchronize(dev)
+            jobs.append({"entry": e, "gen": kind, "shape": (B, H, N, d), "causal": causal,
+                         "rows": rows, "heads": nh,
+                         "o": o.reshape(B * H, N, d)[:nh, rows].float().cpu(),
+                         "lse": lse.reshape(B * H, N)[:nh, rows].cpu()})
+            entry["causal" if causal else "noncausal"] = e
+        out[name] = entry if len(masks) > 1 else entry[next(iter(entry))]
+        del q, k, v, o, lse
+    B, H, N, d, causal = (WORKLOAD[k] for k in ("B", "H", "N", "d", "causal"))
+    o, lse, dq, dk, dv = step_outputs
+    rows = sample_rows(N, TARGET_ROWS, seed=2)
+    c5 = {"fwd": perf(fwd_flops(B, H, N, d, causal), step_ms[0]),
+          "bwd": perf(bwd_flops(B, H, N, d, causal), step_ms[1])}
+    jobs.append({"entry": c5, "gen": "step", "shape": (B, H, N, d), "causal": causal,
+                 "rows": rows, "heads": 1, "inputs": step_inputs,
+                 "o": o.reshape(B * H, N, d)[:1, rows].float().cpu(),
+                 "lse": lse.reshape(B * H, N)[:1, rows].cpu(),
+                 "grads": [t.reshape(B * H, N, d)[0].cpu() for t in (dq, dk, dv)]})
+    out["C5_B2H16N4096d128_causal"] = c5
+    c3 = out["C3_B1H16N16384d128"]["frac"]
+    out["fwd_N16384_d128"] = {"frac": c3, "target": FWD_TARGET, "met": bool(c3 >= FWD_TARGET)}
+    return out, jobs
+
+
+def parity_sample(targets, jobs):
+    """The oracle on each target's seeded sample (the rows and heads whose GPU results
+    sweep_targets kept): max-abs error of O, L and, for the timed step, of dQ, dK, dV
+    over its first head, and whether each is within the parity tolerance."""
+    from exact_attention_26_gb300.inputs import boosted_qkv, normal_qkv, to_f64
+    from oracle import default as oracle_default
+
+    orc = oracle_default()
+    ok = True
+    for job in jobs:
+        B, H, N, d = job["shape"]
+        nh, rows = job["heads"], job["rows"].numpy()
+        if job["gen"] == "step":
+            q, k, v, do = job["inputs"]
+        else:
+            gen = boosted_qkv if job["gen"] == "boosted" else normal_qkv
+            q, k, v = gen(B, H, N, d, seed=0)
+        sel = [to_f64(t.reshape(1, B * H, N, d)[:, :nh]) for t in (q, k, v)]
+        ro, rl = orc.fwd_rows(*sel, rows, causal=job["causal"])
+        go, gl = job["o"].numpy()[None], job["lse"].numpy()[None]
+        err_o = float(np.max(np.abs(go - ro)))
+        err_l = float(np.max(np.abs(gl - rl)))
+        ok &= bool(np.all(np.abs(go - ro) <= np.maximum(1e-2, 2.0 ** -7 * np.abs(ro))))
+        ok &= err_l <= 1e-3
+        errs = [err_o, err_l]
+        if "grads" in job:
+            dsel = to_f64(do.reshape(1, B * H, N, d)[:, :1])
+            ref = orc.bwd(*[x[:, :1] for x in sel], dsel, causal=job["causal"])
+            for g, r in zip(job["grads"], ref):
+                e = float(np.max(np.abs(g.numpy() - r[0, 0])))
+                errs.append(e)
+                ok &= e <= 2e-2
+        job["entry"]["err"] = [float(f"{e:.2e}") for e in errs]
+    targets["parity"] = {"ok": bool(ok), "err": "max-abs [O, L] (+ [dQ, dK, dV] of head 0 "
+                         "for C5) vs the float64 oracle", "tol": "O max(1e-2, 2^-7|O|), "
+                         "L 1e-3, grads 2e-2"}
 
 
 def run_e2e(args, fa, torch, dev, host_inputs, causal, flops_step, world):
@@ -569,23 +724,39 @@ def sweep_backward(fa, torch, dev, flush, normal_qkv, peaks):
     return out
 
 
+def read_rate_gbs(torch, dev, x, flush):
+    """HBM read rate of a reduction over `x` (a tensor far larger than L2): the
+    ceiling of a kernel whose traffic is reads, which a copy (half reads, half
+    writes) understates."""
+    ms = _time_call(torch, dev, lambda: torch.sum(x, dtype=torch.float32), flush, iters=10)
+    return x.numel() * x.element_size() / (ms * 1e-3) / 1e9
+
+
 def sweep_decode(fa, torch, dev, flush, peaks):
-    """Decode calls (automatic key-range split) against the measured HBM copy rate."""
+    """Decode calls (automatic key-range split) against the measured HBM read rate (a
+    decode's traffic is almost all reads of the cache); the copy rate is kept beside it."""
     from exact_attention_26_gb300.inputs import decode_qkv
     out = {}
+    read_peak = None
     for name, B, H, Nq, Nk, d in DEC_WORKLOADS:
         q, k, v = decode_qkv(B, H, Nq, Nk, d, seed=0, device=dev)
         o = torch.empty_like(q)
         lse = torch.empty((B, H, Nq), dtype=torch.float32, device=dev)
         need = fa.fa_decode_workspace_bytes(B, H, H, Nq, Nk, d, 0)
         ws = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+        if read_peak is None:
+            read_peak = read_rate_gbs(torch, dev, k, flush)
+            out["read_peak"] = {"GB/s": round(read_peak, 1),
+                                "how": "torch.sum over the first cache (4.3 GB bf16), L2 flushed",
+                                "copy_GB/s": peaks["hbm_gbs"]}
         ms = _time_call(torch, dev, lambda: fa.decode(q, k, v, out=o, lse=lse, workspace=ws), flush)
         gbs = decode_bytes(B, H, Nq, Nk, d) / (ms * 1e-3) / 1e9
         out[name] = {"ms": round(ms, 5), "GB/s": round(gbs, 1),
                      "splits": fa.fa_decode_num_splits(B, H, H, Nq, Nk, d, 0),
                      "roofline": {"bound": "hbm", "achieved": round(gbs, 1),
-                                  "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                                  "frac": round(gbs / peaks["hbm_gbs"], 4)}}
+                                  "peak": round(read_peak, 1), "unit": "GB/s",
+                                  "frac": round(gbs / read_peak, 4),
+                                  "frac_of_copy_rate": round(gbs / peaks["hbm_gbs"], 4)}}
         del q, k, v, o, lse, ws
     from exact_attention_26_gb300.inputs import paged_cache
     for name, B, H, Nq, Nk, d, ps in PAGED_WORKLOADS:
@@ -602,8 +773,9 @@ def sweep_decode(fa, torch, dev, flush, peaks):
         gbs = decode_bytes(B, H, Nq, Nk, d) / (ms * 1e-3) / 1e9
         out[name] = {"ms": round(ms, 5), "GB/s": round(gbs, 1),
                      "roofline": {"bound": "hbm", "achieved": round(gbs, 1),
-                                  "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                                  "frac": round(gbs / peaks["hbm_gbs"], 4)}}
+                                  "peak": round(read_peak, 1), "unit": "GB/s",
+                                  "frac": round(gbs / read_peak, 4),
+                                  "frac_of_copy_rate": round(gbs / peaks["hbm_gbs"], 4)}}
         del q, kc, vc, bt, o, lse, ws
     return out
 
@@ -809,8 +981,7 @@ def run_reference(args):
         "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(secs * 1e3 / args.steps, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": WORKLOAD_NAME, **WORKLOAD,
-                   "inputs": "bf16(N(0,1)) q,k,v,dO from one torch CPU generator, seed 0"},
+        "config": run_config(),
         "impl": "reference",
         "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": _cores(),
                          "kind": "oracle", "sample": sample},
@@ -829,8 +1000,12 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extra", action="store_true",
                     help="skip the per-workload forward/backward sweep")
+    ap.add_argument("--no-targets", action="store_true",
+                    help="skip the C1-C5 target configurations and their oracle sample")
     ap.add_argument("--only-forward", nargs="+", metavar="B H N d causal [boosted]",
                     help="time one forward shape only (a small case for a profiler)")
+    ap.add_argument("--only-backward", nargs=5, metavar=("B", "H", "N", "d", "causal"),
+                    help="time one backward shape only (a small case for a profiler)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -843,6 +1018,10 @@ def main():
         if len(args.only_forward) not in (5, 6):
             ap.error("--only-forward takes B H N d causal [boosted]")
         print(json.dumps(run_forward_only(args)), flush=True)
+        return
+
+    if args.only_backward:
+        print(json.dumps(run_backward_only(args)), flush=True)
         return
 
     if args.impl == "reference":

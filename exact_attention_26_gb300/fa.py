@@ -238,9 +238,14 @@ def fa_device_status(stream=None) -> int:
 
 # ------------------------------------------------------------ tensor wrappers
 
-def _check(name, t, dtype, shape=None):
+def _check(name, t, dtype, shape=None, dev=None):
+    """Argument checks before any launch: a contiguous CUDA tensor of `dtype` (and
+    `shape`) on device `dev`, the first tensor's device: the kernels dereference every
+    pointer on that one GPU."""
     if not isinstance(t, torch.Tensor) or t.device.type != "cuda":
         raise ValueError(f"{name} must be a CUDA tensor")
+    if dev is not None and t.device != dev:
+        raise ValueError(f"{name} is on {t.device}, the call's first tensor on {dev}")
     if t.dtype != dtype:
         raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
     if not t.is_contiguous():
@@ -258,10 +263,10 @@ def _stream(t, stream):
 def _kv_heads(q, k, v):
     """Key/value head count of k, v [B, Hkv, N, d] next to q [B, H, N, d] (Hkv divides H)."""
     B, H, N, d = q.shape
-    _check("k", k, torch.bfloat16)
+    _check("k", k, torch.bfloat16, dev=q.device)
     if k.dim() != 4 or k.shape[0] != B or k.shape[2] != N or k.shape[3] != d or H % k.shape[1]:
         raise ValueError("k must be [B, Hkv, N, d] with Hkv dividing q's H")
-    _check("v", v, torch.bfloat16, k.shape)
+    _check("v", v, torch.bfloat16, k.shape, dev=q.device)
     return k.shape[1]
 
 
@@ -276,10 +281,10 @@ def forward(q, k, v, causal=False, scale=None, out=None, lse=None, stream=None):
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
     if out is None:
         out = torch.empty_like(q)
-    _check("out", out, torch.bfloat16, q.shape)
+    _check("out", out, torch.bfloat16, q.shape, dev=q.device)
     if lse is None:
         lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
-    _check("lse", lse, torch.float32, (B, H, N))
+    _check("lse", lse, torch.float32, (B, H, N), dev=q.device)
     with torch.cuda.device(q.device):
         rc = fa_fwd_gqa(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
                         B, H, Hkv, N, d, causal, scale, _stream(q, stream))
@@ -299,19 +304,19 @@ def backward(q, k, v, o, lse, do, causal=False, scale=None, dq=None, dk=None, dv
     B, H, N, d = q.shape
     Hkv = _kv_heads(q, k, v)
     for name, t in (("o", o), ("do", do)):
-        _check(name, t, torch.bfloat16, q.shape)
-    _check("lse", lse, torch.float32, (B, H, N))
+        _check(name, t, torch.bfloat16, q.shape, dev=q.device)
+    _check("lse", lse, torch.float32, (B, H, N), dev=q.device)
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
     grads = []
     for name, t, shape in (("dq", dq, q.shape), ("dk", dk, k.shape), ("dv", dv, k.shape)):
         if t is None:
             t = torch.empty(shape, dtype=torch.float32, device=q.device)
-        _check(name, t, torch.float32, shape)
+        _check(name, t, torch.float32, shape, dev=q.device)
         grads.append(t)
     need = fa_bwd_workspace_bytes(B, H, N, d)
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
-    _check("workspace", workspace, torch.uint8)
+    _check("workspace", workspace, torch.uint8, dev=q.device)
     with torch.cuda.device(q.device):
         rc = fa_bwd_gqa(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
                         do.data_ptr(), grads[0].data_ptr(), grads[1].data_ptr(),
@@ -330,24 +335,24 @@ def decode(q, k, v, scale=None, num_splits=0, out=None, lse=None, workspace=None
     if q.dim() != 4:
         raise ValueError("q must be [B, H, Nq, d]")
     B, H, Nq, d = q.shape
-    _check("k", k, torch.bfloat16)
+    _check("k", k, torch.bfloat16, dev=q.device)
     if k.dim() != 4 or k.shape[0] != B or k.shape[3] != d or H % k.shape[1]:
         raise ValueError("k must be [B, Hkv, Nk, d] with q's B and d, Hkv dividing H")
     Hkv, Nk = k.shape[1], k.shape[2]
-    _check("v", v, torch.bfloat16, k.shape)
+    _check("v", v, torch.bfloat16, k.shape, dev=q.device)
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
     if out is None:
         out = torch.empty_like(q)
-    _check("out", out, torch.bfloat16, q.shape)
+    _check("out", out, torch.bfloat16, q.shape, dev=q.device)
     if lse is None:
         lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
-    _check("lse", lse, torch.float32, (B, H, Nq))
+    _check("lse", lse, torch.float32, (B, H, Nq), dev=q.device)
     with torch.cuda.device(q.device):
         need = fa_decode_workspace_bytes(B, H, Hkv, Nq, Nk, d, num_splits)
         if workspace is None and need > 0:
             workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
         if workspace is not None:
-            _check("workspace", workspace, torch.uint8)
+            _check("workspace", workspace, torch.uint8, dev=q.device)
         ws_ptr = workspace.data_ptr() if workspace is not None else None
         ws_len = workspace.numel() if workspace is not None else 0
         rc = fa_decode(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
@@ -366,29 +371,29 @@ def decode_paged(q, k_cache, v_cache, block_table, seq_lens, scale=None, num_spl
     if q.dim() != 4:
         raise ValueError("q must be [B, H, Nq, d]")
     B, H, Nq, d = q.shape
-    _check("k_cache", k_cache, torch.bfloat16)
+    _check("k_cache", k_cache, torch.bfloat16, dev=q.device)
     if k_cache.dim() != 4 or H % k_cache.shape[1] or k_cache.shape[3] != d:
         raise ValueError("k_cache must be [num_pages, Hkv, page_size, d], Hkv dividing H")
     num_pages, Hkv, page_size, _ = k_cache.shape
-    _check("v_cache", v_cache, torch.bfloat16, k_cache.shape)
-    _check("block_table", block_table, torch.int32)
+    _check("v_cache", v_cache, torch.bfloat16, k_cache.shape, dev=q.device)
+    _check("block_table", block_table, torch.int32, dev=q.device)
     if block_table.dim() != 2 or block_table.shape[0] != B:
         raise ValueError("block_table must be [B, max_pages]")
     max_pages = block_table.shape[1]
-    _check("seq_lens", seq_lens, torch.int32, (B,))
+    _check("seq_lens", seq_lens, torch.int32, (B,), dev=q.device)
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
     if out is None:
         out = torch.empty_like(q)
-    _check("out", out, torch.bfloat16, q.shape)
+    _check("out", out, torch.bfloat16, q.shape, dev=q.device)
     if lse is None:
         lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
-    _check("lse", lse, torch.float32, (B, H, Nq))
+    _check("lse", lse, torch.float32, (B, H, Nq), dev=q.device)
     with torch.cuda.device(q.device):
         need = fa_decode_paged_workspace_bytes(B, H, Hkv, Nq, d, page_size, max_pages, num_splits)
         if workspace is None and need > 0:
             workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
         if workspace is not None:
-            _check("workspace", workspace, torch.uint8)
+            _check("workspace", workspace, torch.uint8, dev=q.device)
         ws_ptr = workspace.data_ptr() if workspace is not None else None
         ws_len = workspace.numel() if workspace is not None else 0
         rc = fa_decode_paged(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
@@ -409,22 +414,22 @@ def forward_varlen(q, k, v, cu_seqlens, max_seqlen, causal=False, scale=None, ou
     if q.dim() != 3:
         raise ValueError("q must be [T, H, d]")
     T, H, d = q.shape
-    _check("k", k, torch.bfloat16)
+    _check("k", k, torch.bfloat16, dev=q.device)
     if k.dim() != 3 or k.shape[0] != T or k.shape[2] != d or H % k.shape[1]:
         raise ValueError("k must be [T, Hkv, d] with Hkv dividing H")
     Hkv = k.shape[1]
-    _check("v", v, torch.bfloat16, k.shape)
-    _check("cu_seqlens", cu_seqlens, torch.int32)
+    _check("v", v, torch.bfloat16, k.shape, dev=q.device)
+    _check("cu_seqlens", cu_seqlens, torch.int32, dev=q.device)
     if cu_seqlens.dim() != 1 or cu_seqlens.numel() < 2:
         raise ValueError("cu_seqlens must be [B + 1]")
     B = cu_seqlens.numel() - 1
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
     if out is None:
         out = torch.empty_like(q)
-    _check("out", out, torch.bfloat16, q.shape)
+    _check("out", out, torch.bfloat16, q.shape, dev=q.device)
     if lse is None:
         lse = torch.empty((H, T), dtype=torch.float32, device=q.device)
-    _check("lse", lse, torch.float32, (H, T))
+    _check("lse", lse, torch.float32, (H, T), dev=q.device)
     with torch.cuda.device(q.device):
         rc = fa_fwd_varlen(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
                            cu_seqlens.data_ptr(), B, H, Hkv, T, int(max_seqlen), d, causal, scale,
@@ -442,27 +447,27 @@ def backward_varlen(q, k, v, o, lse, do, cu_seqlens, max_seqlen, causal=False, s
     if q.dim() != 3:
         raise ValueError("q must be [T, H, d]")
     T, H, d = q.shape
-    _check("k", k, torch.bfloat16)
+    _check("k", k, torch.bfloat16, dev=q.device)
     if k.dim() != 3 or k.shape[0] != T or k.shape[2] != d or H % k.shape[1]:
         raise ValueError("k must be [T, Hkv, d] with Hkv dividing H")
     Hkv = k.shape[1]
-    _check("v", v, torch.bfloat16, k.shape)
+    _check("v", v, torch.bfloat16, k.shape, dev=q.device)
     for name, t in (("o", o), ("do", do)):
-        _check(name, t, torch.bfloat16, q.shape)
-    _check("lse", lse, torch.float32, (H, T))
-    _check("cu_seqlens", cu_seqlens, torch.int32)
+        _check(name, t, torch.bfloat16, q.shape, dev=q.device)
+    _check("lse", lse, torch.float32, (H, T), dev=q.device)
+    _check("cu_seqlens", cu_seqlens, torch.int32, dev=q.device)
     B = cu_seqlens.numel() - 1
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
     grads = []
     for name, t, shape in (("dq", dq, q.shape), ("dk", dk, k.shape), ("dv", dv, k.shape)):
         if t is None:
             t = torch.zeros(shape, dtype=torch.float32, device=q.device)
-        _check(name, t, torch.float32, shape)
+        _check(name, t, torch.float32, shape, dev=q.device)
         grads.append(t)
     need = fa_bwd_workspace_bytes(B, H, int(max_seqlen), d)
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
-    _check("workspace", workspace, torch.uint8)
+    _check("workspace", workspace, torch.uint8, dev=q.device)
     with torch.cuda.device(q.device):
         rc = fa_bwd_varlen(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
                            do.data_ptr(), grads[0].data_ptr(), grads[1].data_ptr(),
@@ -487,11 +492,11 @@ def quantize_fp8(x, block_rows=128, signs=None, transpose=False, workspace=None,
     nb = 1 if block_rows == 0 else (N + block_rows - 1) // block_rows
     descale = torch.empty((*lead, nb), dtype=torch.float32, device=x.device)
     if signs is not None:
-        _check("signs", signs, torch.float32, (d,))
+        _check("signs", signs, torch.float32, (d,), dev=x.device)
     need = fa_quantize_fp8_workspace_bytes(BH, N, d)
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=x.device)
-    _check("workspace", workspace, torch.uint8)
+    _check("workspace", workspace, torch.uint8, dev=x.device)
     with torch.cuda.device(x.device):
         rc = fa_quantize_fp8(x.data_ptr(), codes.data_ptr(), descale.data_ptr(), BH, N, d,
                              int(block_rows), None if signs is None else signs.data_ptr(),
@@ -509,23 +514,23 @@ def forward_fp8(q8, k8, vt8, q_descale, k_descale, v_descale, causal=False, scal
     if q8.dim() != 4:
         raise ValueError("q8 must be [B, H, N, d]")
     B, H, N, d = q8.shape
-    _check("k8", k8, torch.uint8)
+    _check("k8", k8, torch.uint8, dev=q8.device)
     if k8.dim() != 4 or k8.shape[0] != B or k8.shape[2] != N or k8.shape[3] != d or H % k8.shape[1]:
         raise ValueError("k8 must be [B, Hkv, N, d] with Hkv dividing H")
     Hkv = k8.shape[1]
     Np = (N + 15) // 16 * 16
-    _check("vt8", vt8, torch.uint8, (B, Hkv, d, Np))
+    _check("vt8", vt8, torch.uint8, (B, Hkv, d, Np), dev=q8.device)
     nb = (N + 127) // 128
-    _check("q_descale", q_descale, torch.float32, (B, H, nb))
-    _check("k_descale", k_descale, torch.float32, (B, Hkv, nb))
-    _check("v_descale", v_descale, torch.float32, (B, Hkv, 1))
+    _check("q_descale", q_descale, torch.float32, (B, H, nb), dev=q8.device)
+    _check("k_descale", k_descale, torch.float32, (B, Hkv, nb), dev=q8.device)
+    _check("v_descale", v_descale, torch.float32, (B, Hkv, 1), dev=q8.device)
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
     if out is None:
         out = torch.empty((B, H, N, d), dtype=torch.bfloat16, device=q8.device)
-    _check("out", out, torch.bfloat16, (B, H, N, d))
+    _check("out", out, torch.bfloat16, (B, H, N, d), dev=q8.device)
     if lse is None:
         lse = torch.empty((B, H, N), dtype=torch.float32, device=q8.device)
-    _check("lse", lse, torch.float32, (B, H, N))
+    _check("lse", lse, torch.float32, (B, H, N), dev=q8.device)
     with torch.cuda.device(q8.device):
         rc = fa_fwd_fp8(q8.data_ptr(), k8.data_ptr(), vt8.data_ptr(), q_descale.data_ptr(),
                         k_descale.data_ptr(), v_descale.data_ptr(), out.data_ptr(), lse.data_ptr(),

@@ -29,7 +29,7 @@ def _run(*args):
 
 def test_bench_line_keeps_the_contract():
     steps = 6
-    r = _run("--steps", str(steps), "--warmup", "3", "--no-extra", "--no-cpu-baseline")
+    r = _run("--steps", str(steps), "--warmup", "3", "--no-extra", "--cpu-seconds", "1")
     for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
                 "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
                 "roofline", "e2e", "gpu_launches", "clocks"):
@@ -52,9 +52,27 @@ def test_bench_line_keeps_the_contract():
     assert e2e["d2h_bytes_per_step"] == B * H * N * (d * 2 + 4 + 3 * d * 4)
     assert r["gpu_launches"] == 3 * steps
     assert r["clocks"]["sm_mhz"] is None or r["clocks"]["sm_mhz"] > 0
+    # the line ends with the target configurations, checked against the oracle
+    assert list(r)[-1] == "targets"
+    t = r["targets"]
+    for name in ("C1_B1H1N128d64", "C2_B8H16N2048d64", "C3_B1H16N16384d128", "C4_B4H8N8192d256",
+                 "C5_B2H16N4096d128_causal"):
+        assert name in t, name
+    assert t["parity"]["ok"] is True
+    c5 = t["C5_B2H16N4096d128_causal"]
+    assert len(c5["err"]) == 5 and max(c5["err"][2:]) <= 2e-2
+    assert c5["bwd"]["tflops"] == pytest.approx(r["bwd_tflops"], rel=2e-3)
+    assert t["fwd_N16384_d128"]["frac"] == t["C3_B1H16N16384d128"]["frac"]
+    assert r["cpu_baseline"]["cores"] >= 1
 
 
 def test_single_forward_mode():
     r = _run("--only-forward", "1", "2", "1000", "128", "1", "--steps", "3", "--warmup", "3")
     assert r["only_forward"]["N"] == 1000 and r["only_forward"]["causal"] is True
+    assert r["ms"] > 0 and r["tflops"] > 0
+
+
+def test_single_backward_mode():
+    r = _run("--only-backward", "1", "2", "1000", "64", "1", "--steps", "3", "--warmup", "3")
+    assert r["only_backward"]["N"] == 1000 and r["only_backward"]["d"] == 64
     assert r["ms"] > 0 and r["tflops"] > 0

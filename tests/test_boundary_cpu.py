@@ -107,6 +107,38 @@ def test_python_wrapper_rejects_cpu_tensors(fa):
         fa.forward(q, q, q)
 
 
+def _on(t, index):
+    """A CPU tensor that reports CUDA device `index`: enough for the wrappers'
+    argument checks, which all run before anything is allocated or launched."""
+    import torch
+
+    class OnDevice(torch.Tensor):
+        @property
+        def device(self):
+            return self._reported
+
+    s = t.as_subclass(OnDevice)
+    s._reported = torch.device("cuda", index)
+    return s
+
+
+def test_python_wrapper_rejects_tensors_on_another_device(fa):
+    import torch
+    x = lambda i, shape=(1, 2, 8, 64), dt=torch.bfloat16: _on(torch.zeros(shape, dtype=dt), i)
+    q = x(0)
+    with pytest.raises(ValueError, match="k is on cuda:1"):
+        fa.forward(q, x(1), x(0), out=x(0), lse=x(0, (1, 2, 8), torch.float32))
+    with pytest.raises(ValueError, match="lse is on cuda:1"):
+        fa.forward(q, x(0), x(0), out=x(0), lse=x(1, (1, 2, 8), torch.float32))
+    lse0 = x(0, (1, 2, 8), torch.float32)
+    with pytest.raises(ValueError, match="do is on cuda:1"):
+        fa.backward(q, x(0), x(0), x(0), lse0, x(1))
+    with pytest.raises(ValueError, match="dq is on cuda:1"):
+        fa.backward(q, x(0), x(0), x(0), lse0, x(0), dq=x(1, dt=torch.float32))
+    with pytest.raises(ValueError, match="v is on cuda:1"):
+        fa.decode(x(0, (1, 2, 1, 64)), x(0), x(1))
+
+
 def _dec(fa, **kw):
     a = dict(q=DUMMY, k=DUMMY, v=DUMMY, o=DUMMY, lse=DUMMY, B=1, H=2, Hkv=2, Nq=1, Nk=1000, d=128,
              scale=0.1, splits=0, ws=None, ws_bytes=0, stream=None)
