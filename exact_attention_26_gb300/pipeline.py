@@ -49,7 +49,11 @@ class HostPipeline:
         self.n = 0
 
     def step(self, host_in, host_out):
-        """Issue one step: host_in = (q, k, v, dO), host_out = (o, lse, dq, dk, dv)."""
+        """Issue one step: host_in = (q, k, v, dO), host_out = (o, lse, dq, dk, dv).
+
+        Returns (h2d, d2h) events.  The copies run asynchronously: do not overwrite
+        the pinned host_in tensors until `h2d` has completed (their bytes are still
+        being read), and read host_out only once `d2h` has completed."""
         sl = self.slots[self.n % self.depth]
         self.n += 1
         if sl["used"]:
@@ -75,7 +79,7 @@ class HostPipeline:
             for dst, src in zip(host_out, [sl["o"], sl["lse"]] + sl["g"]):
                 dst.copy_(src, non_blocking=True)
             sl["d2h"].record(self.s_d2h)
-        return sl["d2h"]
+        return sl["h2d"], sl["d2h"]
 
     def synchronize(self):
         for s in (self.s_h2d, self.s_run, self.s_d2h):

@@ -135,7 +135,10 @@ int fa_bwd_gqa(const void *q, const void *k, const void *v, const void *o, const
  *     FA_ERR_WORKSPACE before anything is launched.
  *   - The first call on each device looks up the array's device address
  *     (cudaGetSymbolAddress) while that device is current; make that first call
- *     before any stream capture.
+ *     before any stream capture.  The address is cached per device ordinal for the
+ *     life of the process: do not reset the device (cudaDeviceReset) or otherwise
+ *     tear down its primary context between calls, which would leave the cached
+ *     address pointing at memory that no longer exists.
  *   - Every call shares the one array; its contents on entry do not matter (each
  *     call rewrites what it reads).  Calls that overlap on the GPU (different
  *     streams, no ordering between them) race on it and give wrong results.

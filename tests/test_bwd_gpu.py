@@ -4,7 +4,7 @@ import pytest
 import torch
 
 from exact_attention_26_gb300.inputs import normal_qkv, to_f64
-from gpu_common import GRAD_ABS, assert_abs_close, load_fa
+from gpu_common import grad_bounds, GRAD_ABS, assert_abs_close, load_fa
 from oracle import Oracle
 
 pytestmark = pytest.mark.gpu
@@ -95,21 +95,33 @@ def test_bwd_b2_h8_n2048_d96(fa, orc, causal):
 
 @pytest.mark.parametrize("scale", [1.5, 0.02])
 def test_bwd_extreme_scales(fa, orc, scale):
-    """Far from 1/sqrt(d) the gradients scale with `scale` and P/dS are rounded to
-    bf16 (relative precision 2^-9), so the bound here is relative to the largest
-    reference gradient: 2e-2 * max(1, max|ref| / 2), i.e. 1% of the largest
-    gradient once gradients exceed 2.  The main error terms are D_i = dO_i . O_i
-    taken from the bf16-rounded O and the bf16 rounding of dS."""
+    """Far from 1/sqrt(d) the gradients grow with `scale` and the kernel's bf16
+    roundings (of P and dS for the products, of O inside D_i) are relative, so a fixed
+    absolute bound does not apply.  Each element is held to the bound derived from
+    those roundings (gpu_common.grad_bounds: six standard deviations of independent
+    round-to-nearest errors, plus fp32 accumulation).  At the usual 1/sqrt(d) the
+    derived bound is tighter than the stated 2e-2: everywhere without a mask, and for
+    at least 99.5% of elements with one (the first causal rows, whose P sits on few
+    keys, get a wider bound)."""
     q, k, v, do = normal_qkv(1, 2, 400, 128, seed=11, with_do=True)
+    qf, kf, vf, dof = (to_f64(t).reshape(2, 400, 128) for t in (q, k, v, do))
     for causal in (False, True):
         got = _grads(fa, q, k, v, do, causal, scale=scale)
         ref = orc.bwd(to_f64(q), to_f64(k), to_f64(v), to_f64(do), causal=causal, scale=scale)
-        for name, g, r in zip(("dQ", "dK", "dV"), got, ref):
-            mag = float(np.max(np.abs(r)))
-            err = float(np.max(np.abs(g - r)))
-            print(f"scale={scale} causal={causal} {name}: max|ref| {mag:.3g} max-abs err {err:.3g}")
+        bounds = grad_bounds(qf, kf, vf, dof, causal, scale)
+        for name, g, r, b in zip(("dQ", "dK", "dV"), got, ref, bounds):
+            g, r = g.reshape(b.shape), r.reshape(b.shape)
+            err = np.abs(g - r)
+            worst = np.unravel_index(np.argmax(err / b), err.shape)
+            print(f"scale={scale} causal={causal} {name}: max|ref| {np.abs(r).max():.3g} "
+                  f"max-abs err {err.max():.3g}, worst err/bound {err[worst] / b[worst]:.3f}")
             assert np.all(np.isfinite(g))
-            assert err <= GRAD_ABS * max(1.0, mag / 2.0), (name, err, mag)
+            assert np.all(err <= b), (name, worst, float(err[worst]), float(b[worst]))
+    # at the usual scale the derived bound is tighter than the stated tolerance
+    for causal in (False, True):
+        for b in grad_bounds(qf, kf, vf, dof, causal, 1.0 / np.sqrt(128)):
+            tight = float(np.percentile(b, 99.5)) if causal else float(b.max())
+            assert tight < GRAD_ABS
 
 
 def test_bwd_workspace_contents_do_not_matter(fa):
