@@ -724,14 +724,6 @@ def sweep_backward(fa, torch, dev, flush, normal_qkv, peaks):
     return out
 
 
-def read_rate_gbs(torch, dev, x, flush):
-    """HBM read rate of a reduction over `x` (a tensor far larger than L2): the
-    ceiling of a kernel whose traffic is reads, which a copy (half reads, half
-    writes) understates."""
-    ms = _time_call(torch, dev, lambda: torch.sum(x, dtype=torch.float32), flush, iters=10)
-    return x.numel() * x.element_size() / (ms * 1e-3) / 1e9
-
-
 def sweep_decode(fa, torch, dev, flush, peaks):
     """Decode calls (automatic key-range split) against the measured HBM read rate (a
     decode's traffic is almost all reads of the cache); the copy rate is kept beside it."""
@@ -745,9 +737,10 @@ def sweep_decode(fa, torch, dev, flush, peaks):
         need = fa.fa_decode_workspace_bytes(B, H, H, Nq, Nk, d, 0)
         ws = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
         if read_peak is None:
-            read_peak = read_rate_gbs(torch, dev, k, flush)
+            read_peak = fa.probe_read_bandwidth(k, iters=5)
             out["read_peak"] = {"GB/s": round(read_peak, 1),
-                                "how": "torch.sum over the first cache (4.3 GB bf16), L2 flushed",
+                                "how": "fa_probe_read_bandwidth: 16-byte non-allocating loads "
+                                       "over the first cache's K (2.1 GB), 5 passes",
                                 "copy_GB/s": peaks["hbm_gbs"]}
         ms = _time_call(torch, dev, lambda: fa.decode(q, k, v, out=o, lse=lse, workspace=ws), flush)
         gbs = decode_bytes(B, H, Nq, Nk, d) / (ms * 1e-3) / 1e9

@@ -745,6 +745,17 @@ extern "C" int fa_device_status(void *stream) {
     return rec[0];
 }
 
+extern "C" int fa_probe_read_bandwidth(const void *buf, size_t bytes, int iters, void *stream,
+                                       double *gbs) {
+    if (!buf || !gbs || !aligned16(buf) || bytes < ((size_t)1 << 20) || (bytes & 15) ||
+        iters < 1 || iters > 1000)
+        return FA_ERR_INVALID_ARG;
+    DeviceCache *dc = nullptr;
+    int rc = current_device(&dc);
+    if (rc != FA_OK) return rc;
+    return run_read_probe(dc->num_sms, buf, bytes, iters, static_cast<cudaStream_t>(stream), gbs);
+}
+
 extern "C" int fa_probe_unit_rates(double *rates, int iters, void *stream) {
     if (rates == nullptr || iters < 16 || iters > (1 << 20)) return FA_ERR_INVALID_ARG;
     DeviceCache *dc = nullptr;

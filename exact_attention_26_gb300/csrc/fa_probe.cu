@@ -106,6 +106,26 @@ __global__ void __launch_bounds__(1024, 1)
     if (threadIdx.x == 0) cycles[blockIdx.x] = (unsigned long long)(t1 - t0);
 }
 
+// Streaming read: each thread XORs 16-byte words of the buffer into a register,
+// L1 not allocated; nothing is written unless the XOR equals a value it never
+// takes in practice (that keeps the loads live).
+__global__ void __launch_bounds__(512)
+    fa_probe_read_kernel(const uint4 *__restrict__ p, size_t n16, unsigned *sink) {
+    uint4 acc = make_uint4(0u, 0u, 0u, 0u);
+    const size_t stride = (size_t)gridDim.x * blockDim.x;
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += stride) {
+        uint4 w;
+        asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(w.x), "=r"(w.y), "=r"(w.z), "=r"(w.w)
+                     : "l"(p + i));
+        acc.x ^= w.x;
+        acc.y ^= w.y;
+        acc.z ^= w.z;
+        acc.w ^= w.w;
+    }
+    if ((acc.x ^ acc.y ^ acc.z ^ acc.w) == 0x9e3779b9u) sink[0] = acc.x;
+}
+
 }  // namespace
 
 // Per-CTA clock64 intervals of the three probes, module globals (the library
@@ -113,6 +133,36 @@ __global__ void __launch_bounds__(1024, 1)
 constexpr int kProbeMaxSms = 1024;
 __device__ unsigned long long g_probe_cycles[3 * kProbeMaxSms];
 __device__ float g_probe_sink[1];
+
+__device__ unsigned g_probe_read_sink[1];
+
+int run_read_probe(int num_sms, const void *buf, size_t bytes, int iters, cudaStream_t stream,
+                   double *gbs) {
+    void *sink = nullptr;
+    if (cudaGetSymbolAddress(&sink, g_probe_read_sink) != cudaSuccess) return FA_ERR_CUDA;
+    const uint4 *p = static_cast<const uint4 *>(buf);
+    const size_t n16 = bytes / 16;
+    const unsigned grid = (unsigned)num_sms * 4;
+    fa_probe_read_kernel<<<grid, 512, 0, stream>>>(p, n16, static_cast<unsigned *>(sink));
+    cudaEvent_t a = nullptr, b = nullptr;
+    if (cudaEventCreate(&a) != cudaSuccess || cudaEventCreate(&b) != cudaSuccess) {
+        if (a) cudaEventDestroy(a);
+        return FA_ERR_CUDA;
+    }
+    int rc = FA_OK;
+    float ms = 0.f;
+    if (cudaEventRecord(a, stream) != cudaSuccess) rc = FA_ERR_CUDA;
+    for (int i = 0; rc == FA_OK && i < iters; ++i)
+        fa_probe_read_kernel<<<grid, 512, 0, stream>>>(p, n16, static_cast<unsigned *>(sink));
+    if (rc == FA_OK && (cudaGetLastError() != cudaSuccess || cudaEventRecord(b, stream) != cudaSuccess ||
+                        cudaEventSynchronize(b) != cudaSuccess ||
+                        cudaEventElapsedTime(&ms, a, b) != cudaSuccess || ms <= 0.f))
+        rc = FA_ERR_CUDA;
+    cudaEventDestroy(a);
+    cudaEventDestroy(b);
+    if (rc == FA_OK) *gbs = (double)n16 * 16.0 * iters / (ms * 1e-3) / 1e9;
+    return rc;
+}
 
 int run_unit_probes(int num_sms, int iters, int *status, cudaStream_t stream, double *rates) {
     if (num_sms < 1 || num_sms > kProbeMaxSms) return FA_ERR_UNSUPPORTED;

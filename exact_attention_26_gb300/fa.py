@@ -28,7 +28,7 @@ EXPORTED = ("fa_fwd", "fa_bwd", "fa_bwd_workspace_bytes", "fa_status_string", "f
             "fa_decode_workspace_bytes", "fa_decode_paged", "fa_decode_paged_num_splits",
             "fa_decode_paged_workspace_bytes", "fa_fwd_gqa", "fa_bwd_gqa", "fa_fwd_varlen",
             "fa_bwd_varlen", "fa_quantize_fp8_workspace_bytes", "fa_quantize_fp8", "fa_fwd_fp8",
-            "fa_probe_unit_rates")
+            "fa_probe_unit_rates", "fa_probe_read_bandwidth")
 
 _vp = ctypes.c_void_p
 _int = ctypes.c_int
@@ -141,6 +141,28 @@ def fa_probe_unit_rates(rates, iters: int, stream=None) -> int:
         fn.argtypes = [ctypes.POINTER(ctypes.c_double), _int, _vp]
         fn.restype = _int
     return fn(rates, iters, stream)
+
+
+def fa_probe_read_bandwidth(buf, nbytes: int, iters: int, stream, gbs) -> int:
+    """Time streaming reads of nbytes at device pointer buf; `gbs` a ctypes double."""
+    fn = load().fa_probe_read_bandwidth
+    if fn.argtypes is None:
+        fn.argtypes = [_vp, ctypes.c_size_t, _int, _vp, ctypes.POINTER(ctypes.c_double)]
+        fn.restype = _int
+    return fn(buf, nbytes, iters, stream, ctypes.byref(gbs))
+
+
+def probe_read_bandwidth(t, iters: int = 5) -> float:
+    """HBM read rate (GB/s) measured by reading the CUDA tensor `t` (contiguous, far
+    larger than L2; its first multiple of 16 bytes is read, nothing is written)."""
+    _check("t", t, t.dtype)
+    nbytes = t.numel() * t.element_size() // 16 * 16
+    gbs = ctypes.c_double(0.0)
+    with torch.cuda.device(t.device):
+        rc = fa_probe_read_bandwidth(t.data_ptr(), nbytes, int(iters), _stream(t, None), gbs)
+    if rc != FA_OK:
+        raise FaError(rc, "fa_probe_read_bandwidth")
+    return gbs.value
 
 
 def probe_unit_rates(iters: int = 2048, stream=None) -> dict:

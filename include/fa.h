@@ -349,6 +349,19 @@ int fa_selftest_wait_timeout(unsigned long long limit_ns, void *stream);
  */
 int fa_probe_unit_rates(double *rates, int iters, void *stream);
 
+/*
+ * Measurement utility (not on the attention path): the HBM read rate, the ceiling
+ * of a kernel whose traffic is reads (the decode kernels read the cache once and
+ * write almost nothing, which a copy rate, half reads and half writes, does not
+ * describe).  Reads the `bytes` at device pointer `buf` (16-byte aligned, a multiple
+ * of 16 bytes, at least 1 MiB; choose far more than the L2) with 16-byte loads that
+ * do not allocate in L1, once untimed and then `iters` times (1..1000) between CUDA
+ * events on `stream`, and writes the rate in GB/s (10^9 bytes per second) to *gbs.
+ * Synchronises `stream`.  FA_ERR_INVALID_ARG on a bad argument, FA_ERR_CUDA on a
+ * CUDA error.  The buffer's contents do not matter and are not changed.
+ */
+int fa_probe_read_bandwidth(const void *buf, size_t bytes, int iters, void *stream, double *gbs);
+
 /* Static, human-readable name of a status code (never NULL). */
 const char *fa_status_string(int status);
 

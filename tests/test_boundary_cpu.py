@@ -257,6 +257,18 @@ def test_fwd_fp8_rejects_bad_arguments(fa, kw, code):
                          a["H"], a["Hkv"], a["N"], a["d"], 1, a["scale"], None) == code
 
 
+def test_read_probe_rejects_bad_arguments_before_touching_a_device(fa):
+    import ctypes
+    g = ctypes.c_double(0.0)
+    ok_ptr, mib = 0x100000, 1 << 20
+    assert fa.fa_probe_read_bandwidth(None, mib, 1, None, g) == 1
+    assert fa.fa_probe_read_bandwidth(ok_ptr + 8, mib, 1, None, g) == 1   # not 16-byte aligned
+    assert fa.fa_probe_read_bandwidth(ok_ptr, mib - 16, 1, None, g) == 1  # under 1 MiB
+    assert fa.fa_probe_read_bandwidth(ok_ptr, mib + 8, 1, None, g) == 1   # not a multiple of 16
+    assert fa.fa_probe_read_bandwidth(ok_ptr, mib, 0, None, g) == 1
+    assert fa.fa_probe_read_bandwidth(ok_ptr, mib, 1001, None, g) == 1
+
+
 def test_probe_rejects_bad_arguments_before_touching_a_device(fa):
     import ctypes
     rates = (ctypes.c_double * 3)()

@@ -46,3 +46,21 @@ def test_unit_rates_reject_bad_arguments():
     rates = (ctypes.c_double * 3)()
     assert fa.fa_probe_unit_rates(rates, 8, None) == fa.FA_ERR_INVALID_ARG
     assert fa.fa_probe_unit_rates(None, 2048, None) == fa.FA_ERR_INVALID_ARG
+
+
+def test_read_bandwidth_probe():
+    """The HBM read rate over a 2 GiB buffer (16x the L2): a plausible GB300 figure,
+    and no slower than a device-to-device copy moves its read half."""
+    fa = load_fa()
+    x = torch.zeros(1 << 30, dtype=torch.bfloat16, device="cuda:0")
+    gbs = fa.probe_read_bandwidth(x, iters=3)
+    y = torch.empty_like(x)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    y.copy_(x)
+    a.record()
+    y.copy_(x)
+    b.record()
+    b.synchronize()
+    copy_read_gbs = x.numel() * 2 / (a.elapsed_time(b) * 1e-3) / 1e9
+    assert 1000.0 < gbs < 12000.0, gbs
+    assert gbs > copy_read_gbs, (gbs, copy_read_gbs)
