@@ -59,6 +59,8 @@ FWD_WORKLOADS = [
     # fewer two-tile items than SMs: the one-tile mode
     ("B1_H8_N2048_d128_causal", 1, 8, 2048, 128, True, "normal"),
     ("B1_H2_N16384_d128_causal", 1, 2, 16384, 128, True, "normal"),
+    # one head: the key ranges are cut over CTAs and merged
+    ("B1_H1_N16384_d128_causal", 1, 1, 16384, 128, True, "normal"),
 ]
 BWD_WORKLOADS = [
     ("B2_H16_N4096_d128_causal", 2, 16, 4096, 128, True),

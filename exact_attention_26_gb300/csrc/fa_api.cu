@@ -230,6 +230,87 @@ int gqa_group(int H, int Hkv) {
 }  // namespace
 }  // namespace fa
 
+namespace fa {
+namespace {
+// Chunk (K/V tiles; 0: no cut), chunks of the longest key range and workspace bytes
+// of a forward with cut key ranges, for the current device.
+struct FwdSplit {
+    int chunk, s_max;
+    size_t bytes, l_offset;
+};
+int fwd_split_plan(int B, int H, int N, int d, int causal, int kv_chunk_keys, FwdSplit *out) {
+    DeviceCache *dc = nullptr;
+    const int rc = current_device(&dc);
+    if (rc != FA_OK) return rc;
+    const int bn = fwd_block_n(d);
+    const int forced = kv_chunk_keys > 0 ? (kv_chunk_keys + bn - 1) / bn : 0;
+    FwdSplit s{};
+    s.chunk = fwd_split_chunk(d, B * H, N, causal, dc->num_sms, forced);
+    if (s.chunk > 0) {
+        const int n_kv = (N + bn - 1) / bn;
+        s.s_max = (n_kv + s.chunk - 1) / s.chunk;
+        const size_t rows = (size_t)B * H * N * s.s_max;
+        s.l_offset = round_up(rows * d * sizeof(float), 256);
+        s.bytes = s.l_offset + round_up(rows * sizeof(float), 256);
+    }
+    *out = s;
+    return FA_OK;
+}
+}  // namespace
+}  // namespace fa
+
+extern "C" size_t fa_fwd_workspace_bytes(int B, int H, int N, int d, int causal, int kv_chunk) {
+    if (check_sizes(B, H, N, d, true) != FA_OK || kv_chunk < 0) return 0;
+    FwdSplit s{};
+    if (fwd_split_plan(B, H, N, d, causal, kv_chunk, &s) != FA_OK) return 0;
+    return s.bytes;
+}
+
+extern "C" int fa_fwd_ws(const void *q, const void *k, const void *v, void *o, float *lse, int B,
+                         int H, int Hkv, int N, int d, int causal, float scale, int kv_chunk,
+                         void *workspace, size_t workspace_bytes, void *stream) {
+    if (!q || !k || !v || !o || !lse || kv_chunk < 0) return FA_ERR_INVALID_ARG;
+    int rc = check_sizes(B, H, N, d, true);
+    if (rc != FA_OK) return rc;
+    const int group = gqa_group(H, Hkv);
+    if (group == 0) return FA_ERR_INVALID_ARG;
+    if ((rc = check_scale(scale)) != FA_OK) return rc;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+        return FA_ERR_MISALIGNED;
+    FwdSplit sp{};
+    if ((rc = fwd_split_plan(B, H, N, d, causal, kv_chunk, &sp)) != FA_OK) return rc;
+    if (sp.chunk > 0) {
+        if (!workspace || workspace_bytes < sp.bytes) return FA_ERR_WORKSPACE;
+        if (reinterpret_cast<uintptr_t>(workspace) & 255u) return FA_ERR_MISALIGNED;
+    }
+    DeviceCache *dc = nullptr;
+    if ((rc = current_device(&dc)) != FA_OK) return rc;
+    FwdParams p{};
+    const int BH = B * H;
+    if ((rc = make_bhnd_map(&p.tm_q, q, BH, N, d, 128)) != FA_OK) return rc;
+    if ((rc = make_bhnd_map(&p.tm_k, k, B * Hkv, N, d, fwd_block_n(d))) != FA_OK) return rc;
+    if ((rc = make_bhnd_map(&p.tm_v, v, B * Hkv, N, d, fwd_block_n(d))) != FA_OK) return rc;
+    p.o = o;
+    p.lse = lse;
+    p.N = N;
+    p.BH = BH;
+    p.H = H;
+    p.group = group;
+    p.d = d;
+    p.causal = causal ? 1 : 0;
+    p.scale_log2 = scale * kLog2e;
+    p.kv_chunk = sp.chunk;
+    if (sp.chunk > 0) {
+        p.ws_o = static_cast<float *>(workspace);
+        p.ws_l = reinterpret_cast<float *>(static_cast<char *>(workspace) + sp.l_offset);
+        p.s_max = sp.s_max;
+    }
+    p.status = dc->status;
+    p.limit_ns = kWaitLimitNs;
+    p.num_sms = dc->num_sms;
+    return launch_fwd(p, static_cast<cudaStream_t>(stream));
+}
+
 extern "C" int fa_fwd_gqa(const void *q, const void *k, const void *v, void *o, float *lse, int B,
                           int H, int Hkv, int N, int d, int causal, float scale, void *stream) {
     if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;

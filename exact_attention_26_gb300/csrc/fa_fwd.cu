@@ -43,6 +43,11 @@
 // tiles take no mask work ("The causal masking freebie").  A tile whose first row
 // is past N is skipped; rows past N inside a tile compute on zero-filled Q rows
 // and are not stored.
+#include <algorithm>
+#include <array>
+#include <mutex>
+#include <vector>
+
 #include "fa_ptx.cuh"
 
 namespace fa {
@@ -123,14 +128,24 @@ struct FwdTile {
 // block, v_descale [B*Hkv] one per head (nqb = ceil(N / 128)); S_t(j) is scaled
 // by scale * q_descale(t) * k_descale(j) inside the exponent's FMA and O by
 // v_descale / l in the epilogue.
-template <int D, bool CAUSAL, bool VARLEN, bool F8, bool ONE>
+//
+// SPLIT (one query tile per CTA, fixed layout, bf16): the key range of every row
+// block is cut into chunks of `chunk` K/V tiles ("FlashAttention-2: ...", section
+// "FA2 change #2: Parallelize over sequence length": a single long sequence must
+// still fill the GPU; the merge rule is the one of the course page "10
+// FlashAttention", section "The decode variant: FlashDecoding").  A work item is
+// then one chunk; a row block with one chunk writes O and L as usual, the others
+// write their normalised partial O_s (fp32, ws_o [BH][N][s_max][D]) and
+// L_s = m_s + ln l_s (ws_l [BH][N][s_max]), which fa_fwd_merge_kernel combines.
+template <int D, bool CAUSAL, bool VARLEN, bool F8, bool ONE, bool SPLIT>
 __global__ void __launch_bounds__(FwdTile<D, F8, ONE>::THREADS, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, __nv_bfloat16 *__restrict__ out,
                   float *__restrict__ lse, int N, int BH, int H, int group, int n_cblocks,
                   const int *__restrict__ cu_seqlens, int total_tokens, float scale_log2,
                   const float *__restrict__ q_descale, const float *__restrict__ k_descale,
-                  const float *__restrict__ v_descale, int nqb, int *status,
+                  const float *__restrict__ v_descale, int nqb, int chunk,
+                  float *__restrict__ ws_o, float *__restrict__ ws_l, int s_max, int *status,
                   unsigned long long limit_ns) {
     using T = FwdTile<D, F8, ONE>;
     constexpr int NT = T::NT;
@@ -168,7 +183,27 @@ __global__ void __launch_bounds__(FwdTile<D, F8, ONE>::THREADS, 1)
     // odd ones (G = gridDim.x), which visits every item once and evens out the
     // longest-first sizes.  Every role walks the same sequence; barrier phases are
     // running counts carried from one item to the next.
-    const int n_items = n_cblocks * BH;
+    static_assert(!SPLIT || (T::NT == 1 && !VARLEN && !F8), "split key ranges: one tile, bf16");
+    const int n_kv_all = (N + T::BN - 1) / T::BN;  // fixed layout (SPLIT)
+    const int ratio = T::ROWS / T::BN;               // K/V tiles per row block on the diagonal
+    // SPLIT: chunks of the row blocks [0, c] together (c < n_cblocks - 1, whose key
+    // ranges are not cut by N): sum over y = 1..c+1 of ceil(y ratio / chunk), chunk a
+    // multiple of ratio.
+    auto chunks_upto = [&](int c) -> int {
+        const int cc = chunk / ratio, n = c + 1, q = n / cc, rr = n % cc;
+        return cc * q * (q + 1) / 2 + (q + 1) * rr;
+    };
+    auto n_kv_of = [&](int cb) -> int {
+        return CAUSAL ? min(n_kv_all, ((cb + 1) * T::ROWS + T::BN - 1) / T::BN) : n_kv_all;
+    };
+    int per_bh = n_cblocks;  // work items per (batch, head)
+    int last_chunks = 1;     // SPLIT: chunks of the last row block
+    if constexpr (SPLIT) {
+        last_chunks = (n_kv_of(n_cblocks - 1) + chunk - 1) / chunk;
+        per_bh = CAUSAL ? (n_cblocks > 1 ? chunks_upto(n_cblocks - 2) : 0) + last_chunks
+                        : n_cblocks * last_chunks;
+    }
+    const int n_items = per_bh * BH;
     const int G = (int)gridDim.x;
     const int n_rounds = (n_items + G - 1) / G;
     auto item_of = [&](int rnd) -> int {
@@ -178,6 +213,8 @@ __global__ void __launch_bounds__(FwdTile<D, F8, ONE>::THREADS, 1)
     struct Item {
         int bh, kvh, cb, n_kv[NT], n_max;
         int len, tok0;  // rows of this head's sequence; its first token (packed layout)
+        int kv_lo;      // first K/V tile of the item's key range
+        int s, ns;      // SPLIT: chunk index, chunks of this row block
     };
     auto decode = [&](int w) {
         Item it;
@@ -187,6 +224,39 @@ __global__ void __launch_bounds__(FwdTile<D, F8, ONE>::THREADS, 1)
         it.cb = CAUSAL ? (n_cblocks - 1 - w / BH) : (w / BH);
         it.len = N;
         it.tok0 = 0;
+        it.kv_lo = 0;
+        it.s = 0;
+        it.ns = 1;
+        if constexpr (SPLIT) {
+            // items run row block by row block, the longest (last) first, chunks in
+            // key order within a row block
+            int r = w / BH;
+            if (!CAUSAL) {
+                it.cb = r / last_chunks;
+                it.s = r % last_chunks;
+                it.ns = last_chunks;
+            } else if (r < last_chunks) {
+                it.cb = n_cblocks - 1;
+                it.s = r;
+                it.ns = last_chunks;
+            } else {
+                // row blocks n_cblocks - 2 down to 0: row block c's chunks follow the
+                // total - chunks_upto(c) chunks of the row blocks above it, so the item
+                // lies in the smallest c whose count above is at most r (bisection)
+                r -= last_chunks;
+                const int total = chunks_upto(n_cblocks - 2);
+                int lo = 0, hi = n_cblocks - 2;
+                while (lo < hi) {
+                    const int mid = (lo + hi) >> 1;
+                    if (total - chunks_upto(mid) <= r) hi = mid; else lo = mid + 1;
+                }
+                it.cb = lo;
+                const int before = total - chunks_upto(lo);
+                it.s = r - before;
+                it.ns = (n_kv_of(lo) + chunk - 1) / chunk;
+            }
+            it.kv_lo = it.s * chunk;
+        }
         if constexpr (VARLEN) {
             // cu_seqlens lives on the device, so it is checked here: a sequence that is
             // not inside [0, total_tokens) or is longer than the launch's maximum is
@@ -204,7 +274,7 @@ __global__ void __launch_bounds__(FwdTile<D, F8, ONE>::THREADS, 1)
                 it.tok0 = a;
             }
         }
-        const int n_kv_all = (it.len + T::BN - 1) / T::BN;
+        const int n_kv_seq = (it.len + T::BN - 1) / T::BN;
         it.n_max = 0;
 #pragma unroll
         for (int t = 0; t < NT; ++t) {  // K/V tiles query tile t visits (0: past the end)
@@ -212,7 +282,8 @@ __global__ void __launch_bounds__(FwdTile<D, F8, ONE>::THREADS, 1)
             if (row0 >= it.len)
                 it.n_kv[t] = 0;
             else
-                it.n_kv[t] = CAUSAL ? min(n_kv_all, (row0 + T::BM + T::BN - 1) / T::BN) : n_kv_all;
+                it.n_kv[t] = CAUSAL ? min(n_kv_seq, (row0 + T::BM + T::BN - 1) / T::BN) : n_kv_seq;
+            if constexpr (SPLIT) it.n_kv[t] = max(0, min(it.n_kv[t] - it.kv_lo, chunk));
             it.n_max = max(it.n_max, it.n_kv[t]);
         }
         return it;
@@ -311,7 +382,7 @@ __global__ void __launch_bounds__(FwdTile<D, F8, ONE>::THREADS, 1)
                         if (gk >= KS && !(ok = mbar_wait(bar_k_empty + 8 * ks, ((gk / KS) - 1) & 1, g,
                                                          SITE_FWD_LOAD_KV_EMPTY)))
                             break;
-                        load_kv(&tm_k, sK, bar_k_full, ks, i, false);
+                        load_kv(&tm_k, sK, bar_k_full, ks, itm.kv_lo + i, false);
                         ++k_issued;
                     }
                     if (i >= 1) {
@@ -319,7 +390,7 @@ __global__ void __launch_bounds__(FwdTile<D, F8, ONE>::THREADS, 1)
                         if (gv >= VS && !(ok = mbar_wait(bar_v_empty + 8 * vs, ((gv / VS) - 1) & 1, g,
                                                          SITE_FWD_LOAD_KV_EMPTY)))
                             break;
-                        load_kv(&tm_v, sV, bar_v_full, vs, i - 1, true);
+                        load_kv(&tm_v, sV, bar_v_full, vs, itm.kv_lo + i - 1, true);
                         ++v_issued;
                     }
                 }
@@ -532,7 +603,7 @@ __global__ void __launch_bounds__(FwdTile<D, F8, ONE>::THREADS, 1)
                 const uint32_t par = (T::SB == 1) ? (gsj & 1) : ((gsj >> 1) & 1);
                 const uint32_t t_s = tmem + lane_base + T::BN * u;
                 float c_s = c_q;
-                if constexpr (F8) c_s *= __ldg(k_descale + (size_t)itm.kvh * nqb + j);
+                if constexpr (F8) c_s *= __ldg(k_descale + (size_t)itm.kvh * nqb + itm.kv_lo + j);
                 ok = mbar_wait_warp(bar_s_full + 8 * u, par, g, SITE_FWD_SOFTMAX_S_FULL);
                 if (!ok) break;
                 tc_fence_after();
@@ -547,7 +618,7 @@ __global__ void __launch_bounds__(FwdTile<D, F8, ONE>::THREADS, 1)
 #pragma unroll
                     for (int e = 0; e < 32; ++e) s[c * 32 + e] = __uint_as_float(sr[c][e]);
 
-                const int kv0 = j * T::BN;
+                const int kv0 = (itm.kv_lo + j) * T::BN;
                 const int len = itm.len;
                 const bool need_mask = (kv0 + T::BN > len) || (CAUSAL && kv0 + T::BN - 1 > row0);
                 if (need_mask) {
@@ -673,6 +744,31 @@ __global__ void __launch_bounds__(FwdTile<D, F8, ONE>::THREADS, 1)
             __nv_bfloat16 *orow =
                 VARLEN ? out + ((size_t)(itm.tok0 + q_idx) * H + (itm.bh % H)) * D
                        : out + ((size_t)itm.bh * (size_t)N + (size_t)q_idx) * D;
+            if (SPLIT && itm.ns > 1) {
+                // one chunk of a cut key range: the normalised partial O_s in fp32 and
+                // its L_s, for the merge kernel
+                const size_t prow = ((size_t)itm.bh * (size_t)N + (size_t)q_idx) * s_max + itm.s;
+                float *prow_o = ws_o + prow * D;
+#pragma unroll 1
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t o[32];
+                    tmem_ld32(t_o + c * 32, o);
+                    tmem_wait_ld(o);
+                    if (c == D / 32 - 1) {
+                        tc_fence_before();
+                        mbar_arrive(bar_o_free + 8 * t);
+                    }
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * inv_l);
+                    if (q_idx < itm.len) {
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) st_global_v8(prow_o + c * 32 + 8 * e, o + 8 * e);
+                    }
+                }
+                if (q_idx < itm.len) ws_l[prow] = (m_ref + lg2(l)) * kLn2;
+                ++oc;
+                continue;
+            }
 #pragma unroll 1
             for (int c = 0; c < D / 32; ++c) {
                 uint32_t o[32];
@@ -719,23 +815,169 @@ __global__ void __launch_bounds__(FwdTile<D, F8, ONE>::THREADS, 1)
     }
 }
 
-template <int D, bool CAUSAL, bool VARLEN, bool F8 = false, bool ONE = false>
+// Merge of the cut key ranges: one warp per query row whose row block was cut
+// (rows of uncut row blocks were written by the attention kernel), lanes over the
+// head dimension.  With L = ln sum_s e^{L_s}: O = sum_s e^{L_s - L} O_s, the
+// online-softmax combination of the course page "10 FlashAttention", section "The
+// decode variant: FlashDecoding".
+template <int D>
+__global__ void __launch_bounds__(256)
+    fa_fwd_merge_kernel(const float *__restrict__ ws_o, const float *__restrict__ ws_l,
+                        __nv_bfloat16 *__restrict__ out, float *__restrict__ lse, int N, int BH,
+                        int causal, int rows_per_block, int n_kv_all, int keys_per_tile, int chunk,
+                        int s_max) {
+    griddep_wait();  // the partials come from the attention kernel
+    constexpr int PER = D / 32;
+    const int lane = threadIdx.x & 31;
+    const long long row = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    if (row >= (long long)BH * N) return;
+    const int q = (int)(row % N);
+    const int cb = q / rows_per_block;
+    const int n_kv = causal ? min(n_kv_all, ((cb + 1) * rows_per_block + keys_per_tile - 1) /
+                                                keys_per_tile)
+                            : n_kv_all;
+    const int ns = (n_kv + chunk - 1) / chunk;
+    if (ns <= 1) return;
+    const float *pl = ws_l + (size_t)row * s_max;
+    float m = -INFINITY;
+    for (int s = 0; s < ns; ++s) m = fmaxf(m, pl[s]);
+    float acc[PER];
+#pragma unroll
+    for (int e = 0; e < PER; ++e) acc[e] = 0.f;
+    float wsum = 0.f;
+    for (int s = 0; s < ns; ++s) {
+        const float w = __expf(pl[s] - m);
+        wsum += w;
+        const float *po = ws_o + ((size_t)row * s_max + s) * D;
+#pragma unroll
+        for (int e = 0; e < PER; ++e) acc[e] = fmaf(w, po[lane + 32 * e], acc[e]);
+    }
+    const float inv = 1.f / wsum;
+#pragma unroll
+    for (int e = 0; e < PER; ++e)
+        out[(size_t)row * D + lane + 32 * e] = __float2bfloat16_rn(acc[e] * inv);
+    if (lane == 0) lse[row] = m + __logf(wsum);
+}
+
+// Predicted time, in K/V-tile steps, of a one-tile launch whose row blocks are cut
+// into chunks of `chunk` tiles (0: uncut): the persistent snake schedule of the
+// kernel over min(items, SMs) CTAs, each item costing its tiles plus a fixed
+// kItemCost (Q load, pipeline fill, epilogue), and a cut launch kMergeCost more for
+// the merge kernel.  The constants come from fitting measured launches on this GPU
+// (B1 H1 and H2 N16384, B1 H1 N32768 causal, B1 H1 N8192 non-causal, d = 128 and
+// 256, chunks of 8, 16, 32 tiles and uncut): a tile step is ~0.86 us, an item's
+// fixed cost ~6 steps.
+constexpr double kItemCost = 6.0, kMergeCost = 5.0;
+
+double fwd_split_cost(long long BH, long long n_cb, long long ratio, long long n_kv_all,
+                      bool causal, long long chunk, int num_sms) {
+    std::vector<long long> len;  // item lengths in the kernel's order (row block major)
+    for (long long i = 0; i < n_cb; ++i) {
+        const long long cb = causal ? n_cb - 1 - i : i;
+        const long long nk = causal ? std::min(n_kv_all, (cb + 1) * ratio) : n_kv_all;
+        const long long c = chunk > 0 ? chunk : nk;
+        for (long long s = 0; s * c < nk; ++s)
+            for (long long h = 0; h < BH; ++h) len.push_back(std::min(c, nk - s * c));
+    }
+    const long long n = (long long)len.size();
+    const long long G = std::min<long long>(n, num_sms);
+    std::vector<double> load((size_t)G, 0.0);
+    for (long long r = 0; r * G < n; ++r)
+        for (long long c = 0; c < G; ++c) {
+            const long long idx = r * G + ((r & 1) ? G - 1 - c : c);
+            if (idx < n) load[(size_t)c] += (double)len[(size_t)idx] + kItemCost;
+        }
+    double worst = 0.0;
+    for (double x : load) worst = std::max(worst, x);
+    return worst + (chunk > 0 ? kMergeCost : 0.0);
+}
+
+// Key-range chunk (in K/V tiles, a multiple of the row block's tiles on the
+// diagonal) for a one-tile launch of B*H heads: 0 (no cut) unless the cost model
+// above predicts a cut at least 5% faster; decisions are remembered per shape.
+template <int D>
+int fwd_split_chunk_t(int BH, int N, int causal, int num_sms, int forced) {
+    using T = FwdTile<D, false, true>;
+    const int ratio = T::ROWS / T::BN;
+    if (forced > 0) return (forced + ratio - 1) / ratio * ratio;
+    const long long n_cb = (N + T::ROWS - 1) / T::ROWS;
+    const long long n_kv_all = (N + T::BN - 1) / T::BN;
+    if (n_cb * BH >= num_sms) return 0;  // the row blocks alone fill the GPU
+    static std::mutex m;
+    static std::vector<std::array<int, 5>> memo;  // BH, N, causal, num_sms, chunk
+    {
+        std::lock_guard<std::mutex> lock(m);
+        for (const auto &e : memo)
+            if (e[0] == BH && e[1] == N && e[2] == causal && e[3] == num_sms) return e[4];
+    }
+    const long long longest = causal ? std::min(n_kv_all, n_cb * ratio) : n_kv_all;
+    const double uncut = fwd_split_cost(BH, n_cb, ratio, n_kv_all, causal, 0, num_sms);
+    double best = uncut * 0.95;
+    int chunk = 0;
+    for (long long c : {16, 24, 32, 48, 64, 96, 128, 192, 256, 384, 512}) {
+        const long long ct = c * ratio;
+        if (ct >= longest) break;
+        const double cost = fwd_split_cost(BH, n_cb, ratio, n_kv_all, causal, ct, num_sms);
+        if (cost < best) {
+            best = cost;
+            chunk = (int)ct;
+        }
+    }
+    std::lock_guard<std::mutex> lock(m);
+    if (memo.size() >= 256) memo.erase(memo.begin());
+    memo.push_back({BH, N, causal, num_sms, chunk});
+    return chunk;
+}
+
+template <int D, bool CAUSAL, bool VARLEN, bool F8 = false, bool ONE = false, bool SPLIT = false>
 int launch_fwd_t(const FwdParams &p, cudaStream_t stream) {
     using T = FwdTile<D, F8, ONE>;
-    auto kern = fa_fwd_kernel<D, CAUSAL, VARLEN, F8, ONE>;
+    auto kern = fa_fwd_kernel<D, CAUSAL, VARLEN, F8, ONE, SPLIT>;
     if (ensure_smem_attr(reinterpret_cast<const void *>(kern), (int)T::SMEM_BYTES) != FA_OK)
         return FA_ERR_CUDA;
     // varlen: N is the longest sequence the caller allows
     const int n_cblocks = (p.N + T::ROWS - 1) / T::ROWS;
-    const long long items = (long long)n_cblocks * p.BH;
+    long long items = (long long)n_cblocks * p.BH;
+    const int n_kv_all = (p.N + T::BN - 1) / T::BN;
+    if (SPLIT) {
+        const int ratio = T::ROWS / T::BN;
+        long long per = 0;
+        for (long long cb = 0; cb < n_cblocks; ++cb) {
+            const long long nk = CAUSAL ? std::min<long long>(n_kv_all, (cb + 1) * ratio) : n_kv_all;
+            per += (nk + p.kv_chunk - 1) / p.kv_chunk;
+        }
+        items = per * p.BH;
+    }
     if (items > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
     // Persistent: one CTA per SM (the shared-memory footprint allows no more).
     const long long grid = items < p.num_sms ? items : p.num_sms;
+    if (grid < 1) return FA_OK;
     kern<<<(unsigned)grid, T::THREADS, T::SMEM_BYTES, stream>>>(
         p.tm_q, p.tm_k, p.tm_v, reinterpret_cast<__nv_bfloat16 *>(p.o), p.lse, p.N, p.BH, p.H,
         p.group, n_cblocks, p.cu_seqlens, p.total_tokens, p.scale_log2, p.q_descale, p.k_descale,
-        p.v_descale, (p.N + 127) / 128, p.status, p.limit_ns);
-    return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+        p.v_descale, (p.N + 127) / 128, p.kv_chunk, p.ws_o, p.ws_l, p.s_max, p.status,
+        p.limit_ns);
+    if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
+    if (SPLIT) {
+        const long long rows = (long long)p.BH * p.N;
+        const long long blocks = (rows * 32 + 255) / 256;
+        if (blocks > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)blocks);
+        cfg.blockDim = dim3(256);
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaLaunchKernelEx(&cfg, fa_fwd_merge_kernel<D>, (const float *)p.ws_o,
+                               (const float *)p.ws_l, reinterpret_cast<__nv_bfloat16 *>(p.o), p.lse,
+                               p.N, p.BH, p.causal, T::ROWS, n_kv_all, T::BN, p.kv_chunk,
+                               p.s_max) != cudaSuccess)
+            return FA_ERR_CUDA;
+    }
+    return FA_OK;
 }
 
 }  // namespace
@@ -744,6 +986,10 @@ template <int D>
 int launch_fwd_d(const FwdParams &p, cudaStream_t stream) {
     if (p.cu_seqlens)
         return p.causal ? launch_fwd_t<D, true, true>(p, stream) : launch_fwd_t<D, false, true>(p, stream);
+    if (p.kv_chunk > 0) {  // cut key ranges (one tile per CTA); the caller sized the workspace
+        return p.causal ? launch_fwd_t<D, true, false, false, (D <= 128), true>(p, stream)
+                        : launch_fwd_t<D, false, false, false, (D <= 128), true>(p, stream);
+    }
     if constexpr (D <= 128) {
         // fewer two-tile items than SMs: one tile per CTA instead
         const long long items2 = (long long)((p.N + 255) / 256) * p.BH;
@@ -752,6 +998,16 @@ int launch_fwd_d(const FwdParams &p, cudaStream_t stream) {
                             : launch_fwd_t<D, false, false, false, true>(p, stream);
     }
     return p.causal ? launch_fwd_t<D, true, false>(p, stream) : launch_fwd_t<D, false, false>(p, stream);
+}
+
+int fwd_split_chunk(int d, int BH, int N, int causal, int num_sms, int forced) {
+    switch (d) {
+        case 64: return fwd_split_chunk_t<64>(BH, N, causal, num_sms, forced);
+        case 96: return fwd_split_chunk_t<96>(BH, N, causal, num_sms, forced);
+        case 128: return fwd_split_chunk_t<128>(BH, N, causal, num_sms, forced);
+        case 256: return fwd_split_chunk_t<256>(BH, N, causal, num_sms, forced);
+        default: return 0;
+    }
 }
 
 int launch_fwd(const FwdParams &p, cudaStream_t stream) {

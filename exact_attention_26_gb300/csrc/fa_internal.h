@@ -54,10 +54,18 @@ struct FwdParams {
     float scale_log2;              // scale * log2(e)
     int fp8;                       // e4m3 inputs: tm_q/tm_k over bytes, tm_v over V^T [B*Hkv][d][Np]
     const float *q_descale, *k_descale, *v_descale;  // fp8: [BH][nqb], [B*Hkv][nqb], [B*Hkv]
+    int kv_chunk;                  // > 0: key ranges cut into chunks of this many K/V tiles
+    float *ws_o, *ws_l;            // kv_chunk > 0: partial O [BH][N][s_max][d], L [BH][N][s_max]
+    int s_max;                     // chunks of the longest key range
     int *status;                   // device status record (2 ints)
     unsigned long long limit_ns;
     int num_sms;
 };
+
+// Key-range chunk in K/V tiles of the one-tile forward for B*H heads of N rows
+// (0: no cut); `forced` > 0 asks for that many tiles (rounded up to the tiles of a
+// row block on the diagonal).
+int fwd_split_chunk(int d, int BH, int N, int causal, int num_sms, int forced);
 
 // e4m3 block quantiser: x bf16 [BH][N][d] -> codes [BH][N][d] (or [BH][d][Np]).
 struct QuantParams {

@@ -28,7 +28,7 @@ EXPORTED = ("fa_fwd", "fa_bwd", "fa_bwd_workspace_bytes", "fa_status_string", "f
             "fa_decode_workspace_bytes", "fa_decode_paged", "fa_decode_paged_num_splits",
             "fa_decode_paged_workspace_bytes", "fa_fwd_gqa", "fa_bwd_gqa", "fa_fwd_varlen",
             "fa_bwd_varlen", "fa_quantize_fp8_workspace_bytes", "fa_quantize_fp8", "fa_fwd_fp8",
-            "fa_probe_unit_rates", "fa_probe_read_bandwidth")
+            "fa_probe_unit_rates", "fa_probe_read_bandwidth", "fa_fwd_ws", "fa_fwd_workspace_bytes")
 
 _vp = ctypes.c_void_p
 _int = ctypes.c_int
@@ -180,6 +180,24 @@ def probe_unit_rates(iters: int = 2048, stream=None) -> dict:
             "ex2_per_clk": rates[2]}
 
 
+def fa_fwd_workspace_bytes(B, H, N, d, causal, kv_chunk=0) -> int:
+    fn = load().fa_fwd_workspace_bytes
+    if fn.argtypes is None:
+        fn.argtypes = [_int] * 6
+        fn.restype = ctypes.c_size_t
+    return fn(B, H, N, d, int(bool(causal)), kv_chunk)
+
+
+def fa_fwd_ws(q, k, v, o, lse, B, H, Hkv, N, d, causal, scale, kv_chunk, workspace,
+              workspace_bytes, stream) -> int:
+    fn = load().fa_fwd_ws
+    if fn.argtypes is None:
+        fn.argtypes = [_vp] * 5 + [_int] * 6 + [ctypes.c_float, _int, _vp, ctypes.c_size_t, _vp]
+        fn.restype = _int
+    return fn(q, k, v, o, lse, B, H, Hkv, N, d, int(bool(causal)), scale, kv_chunk, workspace,
+              workspace_bytes, stream)
+
+
 def fa_fwd_gqa(q, k, v, o, lse, B, H, Hkv, N, d, causal, scale, stream) -> int:
     return load().fa_fwd_gqa(q, k, v, o, lse, B, H, Hkv, N, d, int(bool(causal)), scale, stream)
 
@@ -292,9 +310,15 @@ def _kv_heads(q, k, v):
     return k.shape[1]
 
 
-def forward(q, k, v, causal=False, scale=None, out=None, lse=None, stream=None):
+def forward(q, k, v, causal=False, scale=None, out=None, lse=None, stream=None, kv_chunk=0,
+            workspace=None):
     """O, L = attention(q, k, v); q bf16 CUDA [B,H,N,d], k/v [B,Hkv,N,d] (Hkv = H, or
-    fewer heads shared by groups of query heads).  Returns (o, lse)."""
+    fewer heads shared by groups of query heads).  Returns (o, lse).
+
+    When few long heads would leave SMs idle, the key ranges are cut over several
+    CTAs and merged (fa_fwd_ws): kv_chunk = 0 lets the library decide, > 0 asks for
+    chunks of about that many keys; the workspace that needs is allocated here
+    unless given."""
     _check("q", q, torch.bfloat16)
     if q.dim() != 4:
         raise ValueError("q must be [B, H, N, d]")
@@ -308,10 +332,21 @@ def forward(q, k, v, causal=False, scale=None, out=None, lse=None, stream=None):
         lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
     _check("lse", lse, torch.float32, (B, H, N), dev=q.device)
     with torch.cuda.device(q.device):
-        rc = fa_fwd_gqa(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
-                        B, H, Hkv, N, d, causal, scale, _stream(q, stream))
+        need = fa_fwd_workspace_bytes(B, H, N, d, causal, int(kv_chunk))
+        if need == 0:
+            rc = fa_fwd_gqa(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                            lse.data_ptr(), B, H, Hkv, N, d, causal, scale, _stream(q, stream))
+            where = "fa_fwd_gqa"
+        else:
+            if workspace is None:
+                workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+            _check("workspace", workspace, torch.uint8, dev=q.device)
+            rc = fa_fwd_ws(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                           lse.data_ptr(), B, H, Hkv, N, d, causal, scale, int(kv_chunk),
+                           workspace.data_ptr(), workspace.numel(), _stream(q, stream))
+            where = "fa_fwd_ws"
     if rc != FA_OK:
-        raise FaError(rc, "fa_fwd_gqa")
+        raise FaError(rc, where)
     return out, lse
 
 

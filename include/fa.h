@@ -121,6 +121,34 @@ int fa_bwd_gqa(const void *q, const void *k, const void *v, const void *o, const
                void *stream);
 
 /*
+ * Forward pass with the key range of each query row block cut over several CTAs
+ * ("FlashAttention-2: ...", section "FA2 change #2: Parallelize over sequence
+ * length": a batch-1 call with few heads must still fill the GPU).  Each chunk
+ * yields a normalised partial O_s and its L_s = m_s + ln l_s, and the chunks of a
+ * row are merged as L = ln sum_s e^(L_s), O = sum_s e^(L_s - L) O_s (the combination
+ * of the course page "10 FlashAttention", section "The decode variant:
+ * FlashDecoding").  Same definition, layouts, results and errors as fa_fwd_gqa.
+ *   kv_chunk    : 0 lets the library choose: it cuts key ranges only when one
+ *                 query tile per CTA would leave SMs idle or wait on the longest
+ *                 rows (few heads, long causal sequences), into chunks of about
+ *                 twice the launch's work per SM; > 0 asks for chunks of about
+ *                 kv_chunk keys (rounded up to the keys of a 128-row block's
+ *                 diagonal: 128, or 64 at d = 256, times one).  < 0:
+ *                 FA_ERR_INVALID_ARG.
+ *   workspace   : device buffer of at least fa_fwd_workspace_bytes(B, H, N, d,
+ *                 causal, kv_chunk) bytes, 256-byte aligned (FA_ERR_MISALIGNED),
+ *                 owned by the caller, contents on entry irrelevant; may be NULL
+ *                 when that size is 0 (no cut: the call is fa_fwd_gqa).  Too
+ *                 small or missing: FA_ERR_WORKSPACE before anything is launched.
+ *                 Calls that share a workspace must not overlap.
+ * The choice and the size depend on the current device's SM count.
+ */
+size_t fa_fwd_workspace_bytes(int B, int H, int N, int d, int causal, int kv_chunk);
+int fa_fwd_ws(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H,
+              int Hkv, int N, int d, int causal, float scale, int kv_chunk, void *workspace,
+              size_t workspace_bytes, void *stream);
+
+/*
  * Backward pass that allocates nothing, for callers that cannot allocate device
  * memory or pass a workspace: a host that reserves all device memory up front in
  * its own pool and forbids side allocations, or a latency-critical loop where a

@@ -257,6 +257,19 @@ def test_fwd_fp8_rejects_bad_arguments(fa, kw, code):
                          a["H"], a["Hkv"], a["N"], a["d"], 1, a["scale"], None) == code
 
 
+def test_fwd_ws_rejects_bad_arguments_before_touching_a_device(fa):
+    a = [DUMMY] * 5
+    ok = (1, 2, 2, 1000, 128, 1, 0.088)
+    assert fa.fa_fwd_ws(*a, *ok, -1, None, 0, None) == 1                   # negative chunk
+    assert fa.fa_fwd_ws(None, *a[1:], *ok, 0, None, 0, None) == 1          # null q
+    assert fa.fa_fwd_ws(*a, 1, 2, 2, 1000, 80, 1, 0.088, 0, None, 0, None) == 2  # head dim
+    assert fa.fa_fwd_ws(*a, 1, 2, 3, 1000, 128, 1, 0.088, 0, None, 0, None) == 1  # Hkv
+    assert fa.fa_fwd_ws(*a, 1, 2, 2, 1000, 128, 1, 0.0, 0, None, 0, None) == 1    # scale
+    assert fa.fa_fwd_ws(DUMMY + 8, *a[1:], *ok, 0, None, 0, None) == 3     # misaligned q
+    assert fa.fa_fwd_workspace_bytes(1, 2, 1000, 80, 1, 0) == 0
+    assert fa.fa_fwd_workspace_bytes(1, 2, 1000, 128, 1, -5) == 0
+
+
 def test_read_probe_rejects_bad_arguments_before_touching_a_device(fa):
     import ctypes
     g = ctypes.c_double(0.0)
