@@ -25,12 +25,20 @@
 // other tile's products (the ping-pong of the course page "10 FlashAttention",
 // section 6, mapped onto one MMA-issuing thread and two softmax warpgroups).
 //
-// Warp roles (128 NT + 64 threads):
-//   warpgroup t (t < NT)  softmax of tile t: thread r owns query row r (TMEM lane
-//                         r); rescale of O_t; epilogue O = O_t/l -> bf16, L
-//   warp 4 NT             TMEM allocator; one elected lane issues every MMA and
+// Warp roles (NH softmax warpgroups per tile: 2 with two tiles at d <= 96, else 1):
+//   warpgroup w < NT NH   softmax of tile t = w / NH over keys [h CB, h CB + CB) of
+//                         each S row (h = w % NH, CB = BN / NH): thread r owns query
+//                         row r (TMEM lane r); the two halves of a row trade their
+//                         maxima once per K/V tile and their sums once per item
+//                         through shared memory, so both take the same reference
+//                         max; rescale of O_t and the epilogue O = O_t/l -> bf16, L
+//                         split over the halves by 32-column chunks
+//   warp 4 NT NH          TMEM allocator; one elected lane issues every MMA and
 //                         commit (the whole warp runs the loop, warp-uniform)
-//   warp 4 NT + 1         TMA producer (lane 0): Q tiles, then K_j/V_j into a ring
+//   warp 4 NT NH + 1      TMA producer (lane 0): Q tiles, then K_j/V_j into a ring
+// Halving the row per thread halves the serial chain of each tile's softmax (load
+// S, max, exponentials, pack P), the part of the per-tile step that the tensor core
+// waits on; the exponential unit's throughput is unchanged.
 //
 // CTAs are persistent (one per SM): each walks a list of work items (NT query
 // tiles of one head) longest first in snake order, with barrier phases carried
@@ -93,8 +101,9 @@ struct FwdTile {
     static constexpr uint32_t KV_CHUNK = BN * 128;
     static constexpr uint32_t Q_BYTES = BM * DP * EB;  // one query tile
     static constexpr uint32_t KV_BYTES = BN * DP * EB; // one of K_j, V_j (F8: V_j^T)
-    // tensor memory columns: S slot u at BN u (fp32; P as bf16 over its first BN/2
-    // columns), then O_t (fp32, D columns) at BN NS + D t
+    // tensor memory columns: S slot u at BN u (fp32; the P of the keys of softmax
+    // half h as bf16 pairs or e4m3 quadruples from column h CB of the slot on), then
+    // O_t (fp32, D columns) at BN NS + D t
     static constexpr uint32_t TM_O0 = BN * NS;
     static constexpr uint32_t TM_COLS = 512;
     // shared memory layout (offsets from a 1024-byte aligned base)
@@ -104,19 +113,46 @@ struct FwdTile {
     static constexpr uint32_t OFF_BAR = OFF_V + VS * KV_BYTES;
     // q_full[NT], q_empty[NT], k_full[KS], k_empty[KS], v_full[VS], v_empty[VS],
     // s_full[NS], p_full[NT], o_full[NT], o_free[NT], pv_done, mma_done
-    static constexpr int NBAR = 2 * NT + 2 * KS + 2 * VS + NS + 3 * NT + 2;
+    // With two tiles and d <= 96 (bf16) each tile's softmax runs on NH = 2
+    // warpgroups, one per half of the BN keys of an S row (CB columns each); the
+    // halves trade their row maxima and row sums through a shared-memory exchange
+    // guarded by bar_x[t].  (At d = 128 and in e4m3, whose tensor work per step is
+    // larger, the split measured 2% and 6% slower: the MMA warp then shares its
+    // scheduler with four busy softmax warps instead of two and issues late.)
+    static constexpr int NH = (NT == 2 && D <= 96 && !F8) ? 2 : 1;  // softmax warpgroups per tile
+    static constexpr int CB = BN / NH;                // S columns per softmax thread
+    static constexpr int NWG = NT * NH;               // softmax warpgroups
+    // ... s_full[NS], p_full[NT], o_full[NT], o_free[NT], pv_done, mma_done, x[NT]
+    static constexpr int NBAR = 2 * NT + 2 * KS + 2 * VS + NS + 3 * NT + 2 + NT;
     static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
-    static constexpr uint32_t SMEM_BYTES = OFF_MISC + 16 + 1024;
-    static constexpr int WARP_MMA = 4 * NT;
-    static constexpr int WARP_LOAD = 4 * NT + 1;
-    static constexpr int THREADS = 128 * NT + 64;
+    static constexpr uint32_t OFF_XCH = OFF_MISC + 16;  // fp32 [NT][NH][BM] (NH = 2)
+    static constexpr uint32_t SMEM_USED = OFF_XCH + (NH > 1 ? NT * NH * BM * 4 : 0);
+    // The tiles need 1024-byte alignment (128-byte swizzle atoms).  Where the layout
+    // leaves no room to align the start by hand (d = 96 with two tiles) the
+    // kernel requires the dynamic shared memory to start aligned, and checks it.
+    static constexpr uint32_t kMaxSmem = 227 * 1024;
+    static constexpr uint32_t SMEM_BYTES =
+        SMEM_USED + 1024 <= kMaxSmem ? SMEM_USED + 1024 : SMEM_USED;
+    static constexpr int WARP_MMA = 4 * NWG;
+    static constexpr int WARP_LOAD = 4 * NWG + 1;
+    // Two tiles (RB): a last warpgroup holds the MMA and TMA warps (and two idle
+    // ones), and the warpgroups rebalance registers from the launch's even split
+    // (registers are granted per four warps, so a 10-warp CTA would get no more per
+    // thread than a 12-warp one): softmax threads hold CB fp32 scores and the P
+    // they pack, the MMA and TMA warps little.
+    static constexpr bool RB = (NT == 2);
+    static constexpr int THREADS = 128 * NWG + (RB ? 128 : 64);
+    static constexpr int LAUNCH_REGS = NH > 1 ? 96 : 168;
+    static constexpr int REG_SOFTMAX = NH > 1 ? 112 : 224, REG_MISC = NH > 1 ? 32 : 56;
+    static_assert(!RB || NWG * REG_SOFTMAX + REG_MISC <= (NWG + 1) * LAUNCH_REGS, "register pool");
 
     static_assert(D == 64 || D == 96 || D == 128 || D == 256, "head dim");
     static_assert(!F8 || (D == 128 && BN == 128), "e4m3 path: d = 128");
     static_assert(Q_CHUNK % 1024 == 0 && KV_CHUNK % 1024 == 0, "swizzle atoms must stay aligned");
     static_assert(TM_O0 + NT * D <= TM_COLS, "tensor memory budget");
     static_assert(BN % 64 == 0, "P is packed 64 keys per tcgen05.st");
-    static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+    static_assert(SMEM_USED <= kMaxSmem, "shared memory budget");
+    static_assert(CB % 32 == 0 && (NH == 1 || CB == 64), "S columns per thread");
 };
 
 // VARLEN: packed sequences of different lengths, token-major: q, o [T][H][d],
@@ -151,9 +187,20 @@ __global__ void __launch_bounds__(FwdTile<D, F8, ONE>::THREADS, 1)
     constexpr int NT = T::NT;
     constexpr int KS = T::KS;
     constexpr int VS = T::VS;
+    // warpgroups with different register budgets cannot share a called function:
+    // the waits' slow path is inlined where they rebalance
+    constexpr bool kIn = T::RB;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
+    if (base - raw + T::SMEM_USED > T::SMEM_BYTES) {
+        // uniform across the CTA, before any barrier or TMEM use
+        if (threadIdx.x == 0) {
+            atomicCAS(status + 1, 0, SITE_FWD_SMEM_ALIGN);
+            atomicExch(status, FA_ERR_UNSUPPORTED);
+        }
+        return;
+    }
     uint8_t *gbase = smem_raw + (base - raw);
 
     const uint32_t sQ = base + T::OFF_Q;
@@ -171,6 +218,7 @@ __global__ void __launch_bounds__(FwdTile<D, F8, ONE>::THREADS, 1)
     const uint32_t bar_o_free = bar_o_full + 8 * NT;     // [NT]
     const uint32_t bar_pv_done = bar_o_free + 8 * NT;    // one tile, two S slots only
     const uint32_t bar_mma_done = bar_pv_done + 8;
+    const uint32_t bar_x = bar_mma_done + 8;             // [NT] softmax half exchange
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + T::OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(gbase + T::OFF_MISC + 4);
 
@@ -293,9 +341,10 @@ __global__ void __launch_bounds__(FwdTile<D, F8, ONE>::THREADS, 1)
         for (int t = 0; t < NT; ++t) {
             mbar_init(bar_q_full + 8 * t, 1);
             mbar_init(bar_q_empty + 8 * t, 1);
-            mbar_init(bar_p_full + 8 * t, 128);
+            mbar_init(bar_p_full + 8 * t, 128 * T::NH);
             mbar_init(bar_o_full + 8 * t, 1);
-            mbar_init(bar_o_free + 8 * t, 128);
+            mbar_init(bar_o_free + 8 * t, 128 * T::NH);
+            mbar_init(bar_x + 8 * t, 4 * T::NH);  // one arrival per softmax warp of the tile
         }
         for (int u = 0; u < T::NS; ++u) mbar_init(bar_s_full + 8 * u, 1);
         for (int s = 0; s < KS; ++s) {
@@ -327,6 +376,7 @@ __global__ void __launch_bounds__(FwdTile<D, F8, ONE>::THREADS, 1)
     const Guard g{status, abort_flag, limit_ns};
 
     if (warp == T::WARP_LOAD) {
+        if constexpr (T::RB) setmaxnreg_dec<T::REG_MISC>();
         // ------------------------------------------------------- TMA producer
         // Per item: Q tiles (each once the previous item's last S MMA on that tile
         // has read it), then K_i ahead of V_{i-1}, since S needs K one step before
@@ -361,7 +411,7 @@ __global__ void __launch_bounds__(FwdTile<D, F8, ONE>::THREADS, 1)
                 };
                 for (int t = 0; ok && t < NT; ++t) {
                     if (itm.n_kv[t] == 0) continue;
-                    if (q_issued[t] > 0 && !(ok = mbar_wait(bar_q_empty + 8 * t, (q_issued[t] - 1) & 1,
+                    if (q_issued[t] > 0 && !(ok = mbar_wait<kIn>(bar_q_empty + 8 * t, (q_issued[t] - 1) & 1,
                                                             g, SITE_FWD_LOAD_KV_EMPTY)))
                         break;
                     mbar_arrive_expect_tx(bar_q_full + 8 * t, T::Q_BYTES);
@@ -379,7 +429,7 @@ __global__ void __launch_bounds__(FwdTile<D, F8, ONE>::THREADS, 1)
                 for (int i = 0; ok && i <= itm.n_max; ++i) {
                     if (i < itm.n_max) {
                         const int gk = k_issued, ks = gk % KS;
-                        if (gk >= KS && !(ok = mbar_wait(bar_k_empty + 8 * ks, ((gk / KS) - 1) & 1, g,
+                        if (gk >= KS && !(ok = mbar_wait<kIn>(bar_k_empty + 8 * ks, ((gk / KS) - 1) & 1, g,
                                                          SITE_FWD_LOAD_KV_EMPTY)))
                             break;
                         load_kv(&tm_k, sK, bar_k_full, ks, itm.kv_lo + i, false);
@@ -387,7 +437,7 @@ __global__ void __launch_bounds__(FwdTile<D, F8, ONE>::THREADS, 1)
                     }
                     if (i >= 1) {
                         const int gv = v_issued, vs = gv % VS;
-                        if (gv >= VS && !(ok = mbar_wait(bar_v_empty + 8 * vs, ((gv / VS) - 1) & 1, g,
+                        if (gv >= VS && !(ok = mbar_wait<kIn>(bar_v_empty + 8 * vs, ((gv / VS) - 1) & 1, g,
                                                          SITE_FWD_LOAD_KV_EMPTY)))
                             break;
                         load_kv(&tm_v, sV, bar_v_full, vs, itm.kv_lo + i - 1, true);
@@ -401,14 +451,15 @@ __global__ void __launch_bounds__(FwdTile<D, F8, ONE>::THREADS, 1)
                 const Guard g2{status, &never, kWaitLimitNs};
                 for (int t = 0; t < NT; ++t)
                     if (q_issued[t] > 0)
-                        mbar_wait(bar_q_full + 8 * t, (q_issued[t] - 1) & 1, g2, SITE_FWD_DRAIN);
+                        mbar_wait<kIn>(bar_q_full + 8 * t, (q_issued[t] - 1) & 1, g2, SITE_FWD_DRAIN);
                 for (int j = (k_issued > KS ? k_issued - KS : 0); j < k_issued; ++j)
-                    mbar_wait(bar_k_full + 8 * (j % KS), (j / KS) & 1, g2, SITE_FWD_DRAIN);
+                    mbar_wait<kIn>(bar_k_full + 8 * (j % KS), (j / KS) & 1, g2, SITE_FWD_DRAIN);
                 for (int j = (v_issued > VS ? v_issued - VS : 0); j < v_issued; ++j)
-                    mbar_wait(bar_v_full + 8 * (j % VS), (j / VS) & 1, g2, SITE_FWD_DRAIN);
+                    mbar_wait<kIn>(bar_v_full + 8 * (j % VS), (j / VS) & 1, g2, SITE_FWD_DRAIN);
             }
         }
     } else if (warp == T::WARP_MMA) {
+        if constexpr (T::RB) setmaxnreg_dec<T::REG_MISC>();
         // ------------------------------------------------------- MMA issuer
         // The whole warp runs this loop (warp-uniform); one elected lane issues.
         {
@@ -432,33 +483,38 @@ __global__ void __launch_bounds__(FwdTile<D, F8, ONE>::THREADS, 1)
                 tc_commit_elect(bar_s_full + 8 * u);
             };
             // O_t += P V from S slot u and V stage vs: M = 128, N = D, K = BN.  P sits
-            // in TMEM as 32-bit columns of 2 bf16 or 4 e4m3 keys: 8 columns per step.
+            // in TMEM as 32-bit columns of 2 bf16 or 4 e4m3 keys: 8 columns per step,
+            // the keys of softmax half h from column h CB of the slot on.
+            auto p_col = [&](int ks, int steps) -> uint32_t {
+                const int per_half = steps / T::NH;
+                return (uint32_t)((ks / per_half) * T::CB + (ks % per_half) * 8);
+            };
             auto issue_pv = [&](int t, int u, int vs, bool first) {
                 if constexpr (F8) {
                     // V_j^T is K-major: D rows of BN key bytes
                     const uint64_t dv = sdesc_sw128(sV + vs * T::KV_BYTES, 16, 1024);
 #pragma unroll
                     for (int ks = 0; ks < T::BN / 32; ++ks)
-                        mma_ts_elect_f8(tmem + T::TM_O0 + D * t, tmem + T::BN * u + ks * 8,
+                        mma_ts_elect_f8(tmem + T::TM_O0 + D * t, tmem + T::BN * u + p_col(ks, T::BN / 32),
                                         desc_add(dv, ks * 32), kIdescO, (!first || ks > 0) ? 1u : 0u);
                 } else {
                     const uint64_t dv = sdesc_sw128(sV + vs * T::KV_BYTES, T::KV_CHUNK, 1024);
 #pragma unroll
                     for (int ks = 0; ks < T::BN / 16; ++ks) {
                         const uint64_t b = desc_add(dv, ks * 2048);
-                        mma_ts_elect(tmem + T::TM_O0 + D * t, tmem + T::BN * u + ks * 8, b, kIdescO,
-                                     (!first || ks > 0) ? 1u : 0u);
+                        mma_ts_elect(tmem + T::TM_O0 + D * t, tmem + T::BN * u + p_col(ks, T::BN / 16), b,
+                                     kIdescO, (!first || ks > 0) ? 1u : 0u);
                     }
                 }
             };
             auto wait_k = [&](int j) {
-                const bool r = mbar_wait_warp(bar_k_full + 8 * (j % KS), (j / KS) & 1, g,
+                const bool r = mbar_wait_warp<kIn>(bar_k_full + 8 * (j % KS), (j / KS) & 1, g,
                                          SITE_FWD_MMA_KV_FULL);
                 tc_fence_after();
                 return r;
             };
             auto wait_v = [&](int j) {
-                const bool r = mbar_wait_warp(bar_v_full + 8 * (j % VS), (j / VS) & 1, g,
+                const bool r = mbar_wait_warp<kIn>(bar_v_full + 8 * (j % VS), (j / VS) & 1, g,
                                          SITE_FWD_MMA_KV_FULL);
                 tc_fence_after();
                 return r;
@@ -479,7 +535,7 @@ __global__ void __launch_bounds__(FwdTile<D, F8, ONE>::THREADS, 1)
                     ok = wait_k(kc);
                     for (int t = 0; ok && t < NT; ++t) {
                         if (itm.n_kv[t] == 0) continue;
-                        ok = mbar_wait_warp(bar_q_full + 8 * t, qc[t] & 1, g, SITE_FWD_MMA_Q);
+                        ok = mbar_wait_warp<kIn>(bar_q_full + 8 * t, qc[t] & 1, g, SITE_FWD_MMA_Q);
                         ++qc[t];
                         tc_fence_after();
                         if (!ok) break;
@@ -498,12 +554,12 @@ __global__ void __launch_bounds__(FwdTile<D, F8, ONE>::THREADS, 1)
 #pragma unroll
                         for (int t = 0; t < NT; ++t) {
                             if (!ok || j >= itm.n_kv[t]) continue;
-                            ok = mbar_wait_warp(bar_p_full + 8 * t, pc[t] & 1, g, SITE_FWD_MMA_P_FULL);
+                            ok = mbar_wait_warp<kIn>(bar_p_full + 8 * t, pc[t] & 1, g, SITE_FWD_MMA_P_FULL);
                             ++pc[t];
                             // The first PV of an item overwrites O_t: the previous item's
                             // epilogue must have read it.
                             if (ok && j == 0 && oc[t] > 0)
-                                ok = mbar_wait_warp(bar_o_free + 8 * t, (oc[t] - 1) & 1, g,
+                                ok = mbar_wait_warp<kIn>(bar_o_free + 8 * t, (oc[t] - 1) & 1, g,
                                                     SITE_FWD_MMA_P_FULL);
                             tc_fence_after();
                             if (ok && !v_ready) ok = v_ready = wait_v(vc + j);
@@ -526,7 +582,7 @@ __global__ void __launch_bounds__(FwdTile<D, F8, ONE>::THREADS, 1)
                     // One tile, two S slots: S(j+2) is issued right after PV(j) frees its
                     // slot, so the tensor core computes it while the softmax works on S(j+1).
                     const int n = itm.n_kv[0];
-                    ok = mbar_wait_warp(bar_q_full, qc[0] & 1, g, SITE_FWD_MMA_Q);
+                    ok = mbar_wait_warp<kIn>(bar_q_full, qc[0] & 1, g, SITE_FWD_MMA_Q);
                     ++qc[0];
                     ok = ok && wait_k(kc);
                     if (ok) {
@@ -540,10 +596,10 @@ __global__ void __launch_bounds__(FwdTile<D, F8, ONE>::THREADS, 1)
                         if (n == 2) tc_commit_elect(bar_q_empty);
                     }
                     for (int j = 0; ok && j < n; ++j) {
-                        ok = mbar_wait_warp(bar_p_full, pc[0] & 1, g, SITE_FWD_MMA_P_FULL);
+                        ok = mbar_wait_warp<kIn>(bar_p_full, pc[0] & 1, g, SITE_FWD_MMA_P_FULL);
                         ++pc[0];
                         if (ok && j == 0 && oc[0] > 0)
-                            ok = mbar_wait_warp(bar_o_free, (oc[0] - 1) & 1, g, SITE_FWD_MMA_P_FULL);
+                            ok = mbar_wait_warp<kIn>(bar_o_free, (oc[0] - 1) & 1, g, SITE_FWD_MMA_P_FULL);
                         tc_fence_after();
                         if (ok) ok = wait_v(vc + j);
                         if (!ok) break;
@@ -570,17 +626,55 @@ __global__ void __launch_bounds__(FwdTile<D, F8, ONE>::THREADS, 1)
             tc_commit_elect(bar_mma_done);
             volatile int never = 0;
             const Guard g2{status, &never, kWaitLimitNs};
-            mbar_wait_warp(bar_mma_done, 0, g2, SITE_FWD_DRAIN);
+            mbar_wait_warp<kIn>(bar_mma_done, 0, g2, SITE_FWD_DRAIN);
         }
+    } else if (warp > T::WARP_LOAD) {
+        if constexpr (T::RB) setmaxnreg_dec<T::REG_MISC>();  // warps with no role
     } else {
+        if constexpr (T::RB) setmaxnreg_inc<T::REG_SOFTMAX>();
         // ------------------------------------------------------- softmax warpgroups
-        const int t = warp >> 2;  // query tile of this warpgroup
+        // Warpgroup wg serves tile t = wg / NH and the CB keys [hc CB, hc CB + CB) of
+        // every S row (hc = wg % NH); thread r owns TMEM lane r, query row r of the tile.
+        const int wg = warp >> 2;
+        const int t = wg / T::NH;
+        const int hc = wg % T::NH;
         const int r = threadIdx.x & 127;
         const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
         const uint32_t t_o = tmem + lane_base + T::TM_O0 + D * t;
         // O rows are D * 2 bytes apart (a multiple of 32): 32-byte stores need only a
         // 32-byte aligned base (the boundary guarantees 16)
         const bool out_al32 = (reinterpret_cast<uintptr_t>(out) & 31u) == 0;
+        // Half exchange (NH = 2): each thread publishes one value per phase of bar_x[t]
+        // (its half's row maximum per K/V tile; its partial row sum, then a "read"
+        // mark, per item) and reads the other half's.  Both halves run the same
+        // sequence of phases.  A slot is rewritten only after the other half has read
+        // it: within an item the next maximum follows S(j+1), which the MMA issues
+        // only after both halves' P(j); across items the "read" phase guards it.
+        // Each half writes its P over its own S columns, so the halves share no
+        // tensor memory within a step.
+        float *x_mine = reinterpret_cast<float *>(gbase + T::OFF_XCH) + (t * T::NH + hc) * T::BM + r;
+        const float *x_other =
+            reinterpret_cast<const float *>(gbase + T::OFF_XCH) + (t * T::NH + (T::NH - 1 - hc)) * T::BM + r;
+        uint32_t xph = 0;      // phases of bar_x[t] this thread has taken part in
+        bool x_guard = false;  // the last phase was a "read" mark not yet waited for
+        auto x_arrive = [&]() {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_x + 8 * t);
+            ++xph;
+        };
+        auto x_wait_last = [&]() {
+            return mbar_wait_warp<kIn>(bar_x + 8 * t, (xph - 1) & 1, g, SITE_FWD_SOFTMAX_S_FULL);
+        };
+        // publish v, wait for the other half's value of the same phase
+        auto x_trade = [&](float v, float &other) -> bool {
+            if (x_guard && !x_wait_last()) return false;
+            x_guard = false;
+            *x_mine = v;
+            x_arrive();
+            if (!x_wait_last()) return false;
+            other = *x_other;
+            return true;
+        };
         int sc = 0;  // S products of this tile consumed before the current item
         int oc = 0;  // items of this tile finished
         bool ok = true;
@@ -593,7 +687,10 @@ __global__ void __launch_bounds__(FwdTile<D, F8, ONE>::THREADS, 1)
             const int row0 = itm.cb * T::ROWS + t * T::BM;
             const int q_idx = row0 + r;
             float m_ref = -INFINITY;  // reference max, base-2 scaled units
-            float l = 0.f;
+            // Row sum in parts over keys [0, 64) and [64, 128) of each K/V tile, added
+            // at the end: every layout (one thread or two halves per row) then rounds
+            // the same way.  l: this thread's first part; l_hi: its second (CB = 128).
+            float l = 0.f, l_hi = 0.f;
             // score -> base-2 exponent factor (F8: times the block scales of Q_t, K_j)
             float c_q = scale_log2;
             if constexpr (F8) c_q *= q_descale[(size_t)itm.bh * nqb + row0 / T::BM];
@@ -604,59 +701,58 @@ __global__ void __launch_bounds__(FwdTile<D, F8, ONE>::THREADS, 1)
                 const uint32_t t_s = tmem + lane_base + T::BN * u;
                 float c_s = c_q;
                 if constexpr (F8) c_s *= __ldg(k_descale + (size_t)itm.kvh * nqb + itm.kv_lo + j);
-                ok = mbar_wait_warp(bar_s_full + 8 * u, par, g, SITE_FWD_SOFTMAX_S_FULL);
+                ok = mbar_wait_warp<kIn>(bar_s_full + 8 * u, par, g, SITE_FWD_SOFTMAX_S_FULL);
                 if (!ok) break;
                 tc_fence_after();
-                uint32_t sr[T::BN / 32][32];
+                constexpr int CB = T::CB;
+                uint32_t sr[CB / 32][32];
 #pragma unroll
-                for (int c = 0; c < T::BN / 32; ++c) tmem_ld32(t_s + c * 32, sr[c]);
+                for (int c = 0; c < CB / 32; ++c) tmem_ld32(t_s + hc * CB + c * 32, sr[c]);
 #pragma unroll
-                for (int c = 0; c < T::BN / 32; ++c) tmem_wait_ld(sr[c]);
-                float s[T::BN];
+                for (int c = 0; c < CB / 32; ++c) tmem_wait_ld(sr[c]);
+                float s[CB];
 #pragma unroll
-                for (int c = 0; c < T::BN / 32; ++c)
+                for (int c = 0; c < CB / 32; ++c)
 #pragma unroll
                     for (int e = 0; e < 32; ++e) s[c * 32 + e] = __uint_as_float(sr[c][e]);
 
-                const int kv0 = (itm.kv_lo + j) * T::BN;
+                const int kv0 = (itm.kv_lo + j) * T::BN;  // first key of the tile
                 const int len = itm.len;
                 const bool need_mask = (kv0 + T::BN > len) || (CAUSAL && kv0 + T::BN - 1 > row0);
                 if (need_mask) {
                     const int lim = CAUSAL ? min(len, q_idx + 1) : len;  // keys [0, lim) are visible
+                    const int k0 = kv0 + hc * CB;
 #pragma unroll
-                    for (int c = 0; c < T::BN; ++c)
-                        if (kv0 + c >= lim) s[c] = -INFINITY;
+                    for (int c = 0; c < CB; ++c)
+                        if (k0 + c >= lim) s[c] = -INFINITY;
                 }
                 // Row max and row sum as two independent partial chains: one thread
-                // owns the row, and a single chain of BN dependent operations would be
-                // BN latencies long.  Three-input max and packed fp32-pair FMA/add
-                // halve the instruction count (the issue slots of the softmax warps
-                // are the scarce resource); the sums keep the even/odd split, so the
-                // rounding is that of two scalar chains.
+                // owns CB columns of the row, and a single chain of CB dependent
+                // operations would be CB latencies long.  Three-input max and packed
+                // fp32-pair FMA/add halve the instruction count (the issue slots of the
+                // softmax warps are the scarce resource); the sums keep the even/odd
+                // split per 64 keys, so the rounding is that of two scalar chains.
                 // (d = 256, whose 64-key tiles leave the softmax less to do than the
                 // tensor core, measured 1.4% faster with the scalar forms.)
+                // Measured and not kept: exponentials against the previous reference
+                // max with this tile's max found in the same pass (the pass repeated
+                // from S in TMEM when the max moves): the pass grew by what the
+                // separate max took, since the exponential pass is throughput-bound.
                 constexpr bool kPacked = D != 256;
-                float mp0, mp1;
-                if constexpr (kPacked) {
-                    mp0 = fmax3(s[0], s[1], s[2]);
-                    mp1 = fmax3(s[3], s[4], s[5]);
+                float mp0 = -INFINITY, mp1 = -INFINITY;
+                static_assert(CB % 4 == 0, "max chains take four columns per step");
 #pragma unroll
-                    for (int c = 6; c + 3 < T::BN; c += 4) {
-                        mp0 = fmax3(mp0, s[c], s[c + 1]);
-                        mp1 = fmax3(mp1, s[c + 2], s[c + 3]);
-                    }
-                    static_assert(T::BN % 4 == 0, "tail of the max chains");
-                    mp0 = fmax3(mp0, s[T::BN - 2], s[T::BN - 1]);
-                } else {
-                    mp0 = s[0];
-                    mp1 = s[1];
-#pragma unroll
-                    for (int c = 2; c < T::BN; c += 2) {
-                        mp0 = fmaxf(mp0, s[c]);
-                        mp1 = fmaxf(mp1, s[c + 1]);
-                    }
+                for (int c = 0; c < CB; c += 4) {
+                    mp0 = fmax3(mp0, s[c], s[c + 1]);
+                    mp1 = fmax3(mp1, s[c + 2], s[c + 3]);
                 }
-                const float mx = fmaxf(mp0, mp1);
+                float mx = fmaxf(mp0, mp1);
+                if constexpr (T::NH > 1) {
+                    // the row maximum over both halves; both then take the same steps
+                    float mo;
+                    if (!(ok = x_trade(mx, mo))) break;
+                    mx = fmaxf(mx, mo);
+                }
                 const float m_tile = mx * c_s;
                 float alpha = 1.f;
                 const bool move = m_tile > m_ref + kRescaleLog2;
@@ -664,20 +760,23 @@ __global__ void __launch_bounds__(FwdTile<D, F8, ONE>::THREADS, 1)
                     alpha = ex2(m_ref - m_tile);
                     m_ref = m_tile;
                 }
-                float sp0 = 0.f, sp1 = 0.f;
+                float sp0 = 0.f, sp1 = 0.f, sq0 = 0.f, sq1 = 0.f;
                 if constexpr (kPacked) {
                     const uint64_t c2 = f32x2_splat(c_s), nm2 = f32x2_splat(-m_ref);
 #pragma unroll
-                    for (int c = 0; c < T::BN; c += 2) {
+                    for (int c = 0; c < CB; c += 2) {
                         fma_f32x2(s[c], s[c + 1], c2, nm2);
                         s[c] = ex2(s[c]);
                         s[c + 1] = ex2(s[c + 1]);
-                        add_f32x2(sp0, sp1, s[c], s[c + 1]);
+                        if (c < 64)
+                            add_f32x2(sp0, sp1, s[c], s[c + 1]);
+                        else
+                            add_f32x2(sq0, sq1, s[c], s[c + 1]);
                     }
                 } else {
                     const float neg_m = -m_ref;
 #pragma unroll
-                    for (int c = 0; c < T::BN; c += 2) {
+                    for (int c = 0; c < CB; c += 2) {
                         s[c] = ex2(fmaf(s[c], c_s, neg_m));
                         s[c + 1] = ex2(fmaf(s[c + 1], c_s, neg_m));
                         sp0 += s[c];
@@ -685,38 +784,43 @@ __global__ void __launch_bounds__(FwdTile<D, F8, ONE>::THREADS, 1)
                     }
                 }
                 l = l * alpha + (sp0 + sp1);
+                if constexpr (CB > 64) l_hi = l_hi * alpha + (sq0 + sq1);
+                // P over the first columns of this thread's own CB S columns (keys in
+                // order): e4m3 quadruples (P <= 2^8 with the reference max, inside
+                // e4m3's range) or bf16 pairs
                 if constexpr (F8) {
-                    // P as e4m3 quadruples into the first BN/4 columns of the S slot
-                    // (P <= 2^8 with the reference max, inside e4m3's range)
-                    uint32_t pk[32];
+                    uint32_t pk[CB / 4];
 #pragma unroll
-                    for (int e = 0; e < 32; ++e)
+                    for (int e = 0; e < CB / 4; ++e)
                         pk[e] = pack_e4m3x4(s[4 * e], s[4 * e + 1], s[4 * e + 2], s[4 * e + 3]);
-                    tmem_st32(t_s, pk);
+                    if constexpr (CB / 4 == 32)
+                        tmem_st32(t_s + hc * CB, pk);
+                    else
+                        tmem_st16(t_s + hc * CB, pk);
                 } else {
-                    // P as bf16 pairs into the first BN/2 columns of the S slot.
 #pragma unroll
-                    for (int c = 0; c < T::BN / 64; ++c) {
+                    for (int c = 0; c < CB / 64; ++c) {
                         uint32_t pk[32];
 #pragma unroll
                         for (int e = 0; e < 32; ++e)
                             pk[e] = pack_bf16(s[c * 64 + 2 * e], s[c * 64 + 2 * e + 1]);
-                        tmem_st32(t_s + c * 32, pk);
+                        tmem_st32(t_s + hc * CB + c * 32, pk);
                     }
                 }
                 if (j > 0 && __any_sync(0xffffffffu, move)) {
                     // O_t <- alpha O_t for this warp's 32 rows (alpha = 1 on rows that kept
-                    // m), after P is stored so the S registers are free.  PV(j-1) must be
-                    // complete: with one slot per tile S(j) was issued after it; with two
-                    // slots it is awaited here.  PV(j) waits for the arrive below.
-                    if (T::SB == 2 && !mbar_wait_warp(bar_pv_done, (gsj - 1) & 1, g,
+                    // m), after P is stored so the S registers are free; the halves take
+                    // alternate 32-column chunks.  PV(j-1) must be complete: with one
+                    // slot per tile S(j) was issued after it; with two slots it is
+                    // awaited here.  PV(j) waits for the arrive below.
+                    if (T::SB == 2 && !mbar_wait_warp<kIn>(bar_pv_done, (gsj - 1) & 1, g,
                                                       SITE_FWD_SOFTMAX_S_FULL)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
 #pragma unroll 1
-                    for (int c = 0; c < D / 32; ++c) {
+                    for (int c = hc; c < D / 32; c += T::NH) {
                         uint32_t o[32];
                         tmem_ld32(t_o + c * 32, o);
                         tmem_wait_ld(o);
@@ -735,11 +839,23 @@ __global__ void __launch_bounds__(FwdTile<D, F8, ONE>::THREADS, 1)
                 tc_fence_before();
                 mbar_arrive(bar_p_full + 8 * t);
             }
+            if (!ok) break;
             sc += n_it;
             // --------------------------------------------------- epilogue of this item
-            ok = ok && mbar_wait_warp(bar_o_full + 8 * t, oc & 1, g, SITE_FWD_EPILOGUE_O_FULL);
+            ok = mbar_wait_warp<kIn>(bar_o_full + 8 * t, oc & 1, g, SITE_FWD_EPILOGUE_O_FULL);
             if (!ok) break;
             tc_fence_after();
+            if constexpr (T::NH > 1) {
+                // the whole row sum (the same sum, in the same order, in both halves),
+                // then mark the other half's slot as read
+                float lo;
+                if (!(ok = x_trade(l, lo))) break;
+                l = (hc == 0) ? l + lo : lo + l;
+                x_arrive();
+                x_guard = true;
+            } else if constexpr (T::CB > 64) {
+                l = l + l_hi;
+            }
             const float inv_l = (F8 ? v_descale[itm.kvh] : 1.f) / l;
             __nv_bfloat16 *orow =
                 VARLEN ? out + ((size_t)(itm.tok0 + q_idx) * H + (itm.bh % H)) * D
@@ -750,11 +866,11 @@ __global__ void __launch_bounds__(FwdTile<D, F8, ONE>::THREADS, 1)
                 const size_t prow = ((size_t)itm.bh * (size_t)N + (size_t)q_idx) * s_max + itm.s;
                 float *prow_o = ws_o + prow * D;
 #pragma unroll 1
-                for (int c = 0; c < D / 32; ++c) {
+                for (int c = hc; c < D / 32; c += T::NH) {
                     uint32_t o[32];
                     tmem_ld32(t_o + c * 32, o);
                     tmem_wait_ld(o);
-                    if (c == D / 32 - 1) {
+                    if (c + T::NH >= D / 32) {
                         tc_fence_before();
                         mbar_arrive(bar_o_free + 8 * t);
                     }
@@ -765,16 +881,16 @@ __global__ void __launch_bounds__(FwdTile<D, F8, ONE>::THREADS, 1)
                         for (int e = 0; e < 4; ++e) st_global_v8(prow_o + c * 32 + 8 * e, o + 8 * e);
                     }
                 }
-                if (q_idx < itm.len) ws_l[prow] = (m_ref + lg2(l)) * kLn2;
+                if (hc == 0 && q_idx < itm.len) ws_l[prow] = (m_ref + lg2(l)) * kLn2;
                 ++oc;
                 continue;
             }
 #pragma unroll 1
-            for (int c = 0; c < D / 32; ++c) {
+            for (int c = hc; c < D / 32; c += T::NH) {
                 uint32_t o[32];
                 tmem_ld32(t_o + c * 32, o);
                 tmem_wait_ld(o);
-                if (c == D / 32 - 1) {
+                if (c + T::NH >= D / 32) {
                     // O_t has been read: the next item's first PV may overwrite it.
                     tc_fence_before();
                     mbar_arrive(bar_o_free + 8 * t);
@@ -796,7 +912,7 @@ __global__ void __launch_bounds__(FwdTile<D, F8, ONE>::THREADS, 1)
                     }
                 }
             }
-            if (q_idx < itm.len) {
+            if (hc == 0 && q_idx < itm.len) {
                 const size_t li = VARLEN ? (size_t)(itm.bh % H) * total_tokens + itm.tok0 + q_idx
                                          : (size_t)itm.bh * (size_t)N + q_idx;
                 lse[li] = (m_ref + lg2(l)) * kLn2;
@@ -935,6 +1051,9 @@ int launch_fwd_t(const FwdParams &p, cudaStream_t stream) {
     auto kern = fa_fwd_kernel<D, CAUSAL, VARLEN, F8, ONE, SPLIT>;
     if (ensure_smem_attr(reinterpret_cast<const void *>(kern), (int)T::SMEM_BYTES) != FA_OK)
         return FA_ERR_CUDA;
+    // the warpgroups' register targets add up to the launch's pool only at this count
+    if (T::RB && kernel_num_regs(reinterpret_cast<const void *>(kern)) != T::LAUNCH_REGS)
+        return FA_ERR_UNSUPPORTED;
     // varlen: N is the longest sequence the caller allows
     const int n_cblocks = (p.N + T::ROWS - 1) / T::ROWS;
     long long items = (long long)n_cblocks * p.BH;

@@ -32,6 +32,7 @@ enum WaitSite : int {
     SITE_BWD_DRAIN = 19,
     SITE_BWD_BAD_SEQ = 20,
     SITE_BWD_SMEM_ALIGN = 26,
+    SITE_FWD_SMEM_ALIGN = 27,
     SITE_DEC_FULL = 21,
     SITE_DEC_EMPTY = 22,
     SITE_DEC_DRAIN = 23,
