@@ -213,7 +213,7 @@ int kernel_num_regs(const void *kernel) {
     return a.numRegs;
 }
 
-// Keys per K/V tile of the forward kernel for head dimension d.
+// Keys per K/V tile of the one-tile forward kernel (the one that cuts key ranges).
 int fwd_block_n(int d) { return d == 256 ? 64 : 128; }
 
 }  // namespace fa
@@ -288,8 +288,8 @@ extern "C" int fa_fwd_ws(const void *q, const void *k, const void *v, void *o, f
     FwdParams p{};
     const int BH = B * H;
     if ((rc = make_bhnd_map(&p.tm_q, q, BH, N, d, 128)) != FA_OK) return rc;
-    if ((rc = make_bhnd_map(&p.tm_k, k, B * Hkv, N, d, fwd_block_n(d))) != FA_OK) return rc;
-    if ((rc = make_bhnd_map(&p.tm_v, v, B * Hkv, N, d, fwd_block_n(d))) != FA_OK) return rc;
+    if ((rc = make_bhnd_map(&p.tm_k, k, B * Hkv, N, d, fwd_kv_box_rows(d))) != FA_OK) return rc;
+    if ((rc = make_bhnd_map(&p.tm_v, v, B * Hkv, N, d, fwd_kv_box_rows(d))) != FA_OK) return rc;
     p.o = o;
     p.lse = lse;
     p.N = N;
@@ -327,8 +327,8 @@ extern "C" int fa_fwd_gqa(const void *q, const void *k, const void *v, void *o, 
     FwdParams p{};
     const int BH = B * H;
     if ((rc = make_bhnd_map(&p.tm_q, q, BH, N, d, 128)) != FA_OK) return rc;
-    if ((rc = make_bhnd_map(&p.tm_k, k, B * Hkv, N, d, fwd_block_n(d))) != FA_OK) return rc;
-    if ((rc = make_bhnd_map(&p.tm_v, v, B * Hkv, N, d, fwd_block_n(d))) != FA_OK) return rc;
+    if ((rc = make_bhnd_map(&p.tm_k, k, B * Hkv, N, d, fwd_kv_box_rows(d))) != FA_OK) return rc;
+    if ((rc = make_bhnd_map(&p.tm_v, v, B * Hkv, N, d, fwd_kv_box_rows(d))) != FA_OK) return rc;
     p.o = o;
     p.lse = lse;
     p.N = N;
@@ -449,8 +449,8 @@ extern "C" int fa_fwd_varlen(const void *q, const void *k, const void *v, void *
     if ((rc = current_device(&dc)) != FA_OK) return rc;
     FwdParams p{};
     if ((rc = make_thd_map(&p.tm_q, q, total_tokens, H, d, 128)) != FA_OK) return rc;
-    if ((rc = make_thd_map(&p.tm_k, k, total_tokens, Hkv, d, fwd_block_n(d))) != FA_OK) return rc;
-    if ((rc = make_thd_map(&p.tm_v, v, total_tokens, Hkv, d, fwd_block_n(d))) != FA_OK) return rc;
+    if ((rc = make_thd_map(&p.tm_k, k, total_tokens, Hkv, d, fwd_kv_box_rows(d))) != FA_OK) return rc;
+    if ((rc = make_thd_map(&p.tm_v, v, total_tokens, Hkv, d, fwd_kv_box_rows(d))) != FA_OK) return rc;
     p.o = o;
     p.lse = lse;
     p.N = max_seqlen;

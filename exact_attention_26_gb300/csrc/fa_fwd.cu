@@ -83,11 +83,17 @@ template <int D, bool F8 = false, bool ONE = false>
 struct FwdTile {
     static constexpr int EB = F8 ? 1 : 2;             // bytes per element
     static constexpr int NT = (D <= 128 && !ONE) ? 2 : 1;  // 128-row query tiles per CTA
-    static constexpr int SB = (NT == 1) ? 2 : 1;      // S slots per tile (double buffer)
+    // keys per K/V tile: 64 at d = 256 (tensor memory).  (Two tiles at d = 64 with
+    // 64-key tiles, which leaves room for two S slots per tile so that each tile's
+    // next S is computed while its softmax runs, measured 4% slower non-causal and
+    // 2% faster causal: both tiles' softmaxes then run in step and contend for the
+    // exponential unit.)
+    static constexpr int BN = (D == 256) ? 64 : 128;
+    static constexpr int SB = (NT == 1) ? 2 : 1;      // S slots per tile
     static constexpr int NS = NT * SB;                // S slots in TMEM
     static constexpr int BM = 128;
     static constexpr int ROWS = NT * BM;              // query rows per CTA
-    static constexpr int BN = (D == 256) ? 64 : 128;  // keys per K/V tile
+    static constexpr int KV_BOX = fwd_kv_box_rows(D); // rows per K/V TMA box
     static constexpr int KS = (F8 || D == 64) ? 4 : 3;  // K ring stages
     static constexpr int VS = (F8 || D == 64) ? 4 : 2;  // V ring stages
     // Rows sit in shared memory as 128-byte swizzle chunks (64 bf16 or 128 e4m3
@@ -111,8 +117,6 @@ struct FwdTile {
     static constexpr uint32_t OFF_K = OFF_Q + NT * Q_BYTES;
     static constexpr uint32_t OFF_V = OFF_K + KS * KV_BYTES;
     static constexpr uint32_t OFF_BAR = OFF_V + VS * KV_BYTES;
-    // q_full[NT], q_empty[NT], k_full[KS], k_empty[KS], v_full[VS], v_empty[VS],
-    // s_full[NS], p_full[NT], o_full[NT], o_free[NT], pv_done, mma_done
     // With two tiles and d <= 96 (bf16) each tile's softmax runs on NH = 2
     // warpgroups, one per half of the BN keys of an S row (CB columns each); the
     // halves trade their row maxima and row sums through a shared-memory exchange
@@ -122,11 +126,16 @@ struct FwdTile {
     static constexpr int NH = (NT == 2 && D <= 96 && !F8) ? 2 : 1;  // softmax warpgroups per tile
     static constexpr int CB = BN / NH;                // S columns per softmax thread
     static constexpr int NWG = NT * NH;               // softmax warpgroups
-    // ... s_full[NS], p_full[NT], o_full[NT], o_free[NT], pv_done, mma_done, x[NT]
-    static constexpr int NBAR = 2 * NT + 2 * KS + 2 * VS + NS + 3 * NT + 2 + NT;
+    // q_full[NT], q_empty[NT], k_full[KS], k_empty[KS], v_full[VS], v_empty[VS],
+    // s_full[NS], p_full[NS], o_full[NT], o_free[NT], pv_done[NT], mma_done, x[NT]
+    static constexpr int NBAR = 2 * NT + 2 * KS + 2 * VS + 2 * NS + 4 * NT + 1;
     static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
-    static constexpr uint32_t OFF_XCH = OFF_MISC + 16;  // fp32 [NT][NH][BM] (NH = 2)
-    static constexpr uint32_t SMEM_USED = OFF_XCH + (NH > 1 ? NT * NH * BM * 4 : 0);
+    // half exchange: fp32 [XB][NT][NH][BM]; two buffers, alternating by phase, where
+    // the S slots are double-buffered (a half may then run a step ahead) and room
+    // allows
+    static constexpr int XB = (NH > 1 && SB == 2) ? 2 : 1;
+    static constexpr uint32_t OFF_XCH = OFF_MISC + 16;
+    static constexpr uint32_t SMEM_USED = OFF_XCH + (NH > 1 ? XB * NT * NH * BM * 4 : 0);
     // The tiles need 1024-byte alignment (128-byte swizzle atoms).  Where the layout
     // leaves no room to align the start by hand (d = 96 with two tiles) the
     // kernel requires the dynamic shared memory to start aligned, and checks it.
@@ -143,16 +152,17 @@ struct FwdTile {
     static constexpr bool RB = (NT == 2);
     static constexpr int THREADS = 128 * NWG + (RB ? 128 : 64);
     static constexpr int LAUNCH_REGS = NH > 1 ? 96 : 168;
-    static constexpr int REG_SOFTMAX = NH > 1 ? 112 : 224, REG_MISC = NH > 1 ? 32 : 56;
+    static constexpr int REG_SOFTMAX = NH == 1 ? 224 : CB == 32 ? 104 : 112;
+    static constexpr int REG_MISC = NH == 1 ? 56 : CB == 32 ? 64 : 32;
     static_assert(!RB || NWG * REG_SOFTMAX + REG_MISC <= (NWG + 1) * LAUNCH_REGS, "register pool");
 
     static_assert(D == 64 || D == 96 || D == 128 || D == 256, "head dim");
     static_assert(!F8 || (D == 128 && BN == 128), "e4m3 path: d = 128");
     static_assert(Q_CHUNK % 1024 == 0 && KV_CHUNK % 1024 == 0, "swizzle atoms must stay aligned");
     static_assert(TM_O0 + NT * D <= TM_COLS, "tensor memory budget");
-    static_assert(BN % 64 == 0, "P is packed 64 keys per tcgen05.st");
+    static_assert(BN % 64 == 0, "K/V tiles of whole 64-key groups");
     static_assert(SMEM_USED <= kMaxSmem, "shared memory budget");
-    static_assert(CB % 32 == 0 && (NH == 1 || CB == 64), "S columns per thread");
+    static_assert(CB == 32 || CB == 64 || CB == 128, "S columns per thread");
 };
 
 // VARLEN: packed sequences of different lengths, token-major: q, o [T][H][d],
@@ -213,11 +223,11 @@ __global__ void __launch_bounds__(FwdTile<D, F8, ONE>::THREADS, 1)
     const uint32_t bar_v_full = bar_k_empty + 8 * KS;    // [VS]
     const uint32_t bar_v_empty = bar_v_full + 8 * VS;    // [VS]
     const uint32_t bar_s_full = bar_v_empty + 8 * VS;    // [NS]
-    const uint32_t bar_p_full = bar_s_full + 8 * T::NS;  // [NT]
-    const uint32_t bar_o_full = bar_p_full + 8 * NT;     // [NT]
+    const uint32_t bar_p_full = bar_s_full + 8 * T::NS;  // [NS], per S slot like s_full
+    const uint32_t bar_o_full = bar_p_full + 8 * T::NS;  // [NT]
     const uint32_t bar_o_free = bar_o_full + 8 * NT;     // [NT]
-    const uint32_t bar_pv_done = bar_o_free + 8 * NT;    // one tile, two S slots only
-    const uint32_t bar_mma_done = bar_pv_done + 8;
+    const uint32_t bar_pv_done = bar_o_free + 8 * NT;    // [NT] two S slots per tile only
+    const uint32_t bar_mma_done = bar_pv_done + 8 * NT;
     const uint32_t bar_x = bar_mma_done + 8;             // [NT] softmax half exchange
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + T::OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(gbase + T::OFF_MISC + 4);
@@ -341,12 +351,18 @@ __global__ void __launch_bounds__(FwdTile<D, F8, ONE>::THREADS, 1)
         for (int t = 0; t < NT; ++t) {
             mbar_init(bar_q_full + 8 * t, 1);
             mbar_init(bar_q_empty + 8 * t, 1);
-            mbar_init(bar_p_full + 8 * t, 128 * T::NH);
             mbar_init(bar_o_full + 8 * t, 1);
             mbar_init(bar_o_free + 8 * t, 128 * T::NH);
             mbar_init(bar_x + 8 * t, 4 * T::NH);  // one arrival per softmax warp of the tile
         }
-        for (int u = 0; u < T::NS; ++u) mbar_init(bar_s_full + 8 * u, 1);
+        for (int u = 0; u < T::NS; ++u) {
+            mbar_init(bar_s_full + 8 * u, 1);
+            // P of a slot: one arrival per softmax thread of the slot's tile.  Per slot,
+            // not per tile: with two slots a tile's softmax may finish P(j) and P(j+1)
+            // before the MMA warp looks for P(j), and one barrier would then be two
+            // phases ahead of its waiter, which a parity wait cannot tell apart.
+            mbar_init(bar_p_full + 8 * u, 128 * T::NH);
+        }
         for (int s = 0; s < KS; ++s) {
             mbar_init(bar_k_full + 8 * s, 1);
             mbar_init(bar_k_empty + 8 * s, 1);
@@ -355,7 +371,7 @@ __global__ void __launch_bounds__(FwdTile<D, F8, ONE>::THREADS, 1)
             mbar_init(bar_v_full + 8 * s, 1);
             mbar_init(bar_v_empty + 8 * s, 1);
         }
-        mbar_init(bar_pv_done, 1);
+        for (int t = 0; t < NT; ++t) mbar_init(bar_pv_done + 8 * t, 1);
         mbar_init(bar_mma_done, 1);
         *abort_flag = 0;
         fence_mbar_init();
@@ -399,15 +415,16 @@ __global__ void __launch_bounds__(FwdTile<D, F8, ONE>::THREADS, 1)
                                     itm.kvh);
                         return;
                     }
-                    for (int c = 0; c < T::NCH; ++c) {
-                        if constexpr (VARLEN)
-                            tma_load_3d(ring + stage * T::KV_BYTES + c * T::KV_CHUNK, map,
-                                        full + 8 * stage, c * T::CW, (itm.bh % H) / group,
-                                        itm.tok0 + j * T::BN);
-                        else
-                            tma_load_3d(ring + stage * T::KV_BYTES + c * T::KV_CHUNK, map,
-                                        full + 8 * stage, c * T::CW, j * T::BN, itm.kvh);
-                    }
+                    static_assert(T::BN % T::KV_BOX == 0, "K/V tile of whole boxes");
+                    for (int c = 0; c < T::NCH; ++c)
+                        for (int rr = 0; rr < T::BN; rr += T::KV_BOX) {
+                            const uint32_t dst = ring + stage * T::KV_BYTES + c * T::KV_CHUNK + rr * 128;
+                            if constexpr (VARLEN)
+                                tma_load_3d(dst, map, full + 8 * stage, c * T::CW, (itm.bh % H) / group,
+                                            itm.tok0 + j * T::BN + rr);
+                            else
+                                tma_load_3d(dst, map, full + 8 * stage, c * T::CW, j * T::BN + rr, itm.kvh);
+                        }
                 };
                 for (int t = 0; ok && t < NT; ++t) {
                     if (itm.n_kv[t] == 0) continue;
@@ -523,8 +540,9 @@ __global__ void __launch_bounds__(FwdTile<D, F8, ONE>::THREADS, 1)
             int kc = 0, vc = 0;  // K/V tiles consumed before the current item (running)
             int qc[NT], pc[NT], oc[NT];  // per tile: Q loads, P arrivals, items finished
 #pragma unroll
-            for (int t = 0; t < NT; ++t) qc[t] = pc[t] = oc[t] = 0;
-            int gs = 0;          // S products issued before the current item (two-slot case)
+            int gs[NT];  // per tile: S products issued before the current item (two slots)
+#pragma unroll
+            for (int t = 0; t < NT; ++t) qc[t] = pc[t] = oc[t] = gs[t] = 0;
             for (int rnd = 0; ok && rnd < n_rounds; ++rnd) {
                 const int w = item_of(rnd);
                 if (w < 0) continue;
@@ -579,45 +597,66 @@ __global__ void __launch_bounds__(FwdTile<D, F8, ONE>::THREADS, 1)
                         }
                     }
                 } else {
-                    // One tile, two S slots: S(j+2) is issued right after PV(j) frees its
-                    // slot, so the tensor core computes it while the softmax works on S(j+1).
-                    const int n = itm.n_kv[0];
-                    ok = mbar_wait_warp<kIn>(bar_q_full, qc[0] & 1, g, SITE_FWD_MMA_Q);
-                    ++qc[0];
-                    ok = ok && wait_k(kc);
-                    if (ok) {
-                        issue_s(0, gs & 1, kc % KS);
-                        tc_commit_elect(bar_k_empty + 8 * (kc % KS));
-                        if (n == 1) tc_commit_elect(bar_q_empty);
+                    // Two S slots per tile (the g-th S of tile t in slot 2t + (g & 1)):
+                    // S_t(j+2) is issued right after PV_t(j) frees its slot, so the tensor
+                    // core computes it while the softmax works on S_t(j+1).  Per K/V step
+                    // the tiles' products interleave: PV_0(j), S_0(j+2), PV_1(j), S_1(j+2).
+                    auto slot = [&](int t, int gi) { return 2 * t + (gi & 1); };
+                    for (int jj = 0; ok && jj < 2 && jj < itm.n_max; ++jj) {
+                        if (!(ok = wait_k(kc + jj))) break;
+                        for (int t = 0; ok && t < NT; ++t) {
+                            if (jj >= itm.n_kv[t]) continue;
+                            if (jj == 0) {
+                                ok = mbar_wait_warp<kIn>(bar_q_full + 8 * t, qc[t] & 1, g, SITE_FWD_MMA_Q);
+                                ++qc[t];
+                                tc_fence_after();
+                                if (!ok) break;
+                            }
+                            issue_s(t, slot(t, gs[t] + jj), (kc + jj) % KS);
+                            if (jj + 1 == itm.n_kv[t]) tc_commit_elect(bar_q_empty + 8 * t);
+                        }
+                        if (ok) tc_commit_elect(bar_k_empty + 8 * ((kc + jj) % KS));
                     }
-                    if (ok && n > 1 && (ok = wait_k(kc + 1))) {
-                        issue_s(0, (gs + 1) & 1, (kc + 1) % KS);
-                        tc_commit_elect(bar_k_empty + 8 * ((kc + 1) % KS));
-                        if (n == 2) tc_commit_elect(bar_q_empty);
-                    }
-                    for (int j = 0; ok && j < n; ++j) {
-                        ok = mbar_wait_warp<kIn>(bar_p_full, pc[0] & 1, g, SITE_FWD_MMA_P_FULL);
-                        ++pc[0];
-                        if (ok && j == 0 && oc[0] > 0)
-                            ok = mbar_wait_warp<kIn>(bar_o_free, (oc[0] - 1) & 1, g, SITE_FWD_MMA_P_FULL);
-                        tc_fence_after();
-                        if (ok) ok = wait_v(vc + j);
-                        if (!ok) break;
-                        issue_pv(0, (gs + j) & 1, (vc + j) % VS, j == 0);
-                        tc_commit_elect(bar_v_empty + 8 * ((vc + j) % VS));
-                        tc_commit_elect(bar_pv_done);
-                        if (j + 2 < n) {
-                            if (!(ok = wait_k(kc + j + 2))) break;
-                            issue_s(0, (gs + j) & 1, (kc + j + 2) % KS);
-                            tc_commit_elect(bar_k_empty + 8 * ((kc + j + 2) % KS));
-                            if (j + 3 == n) tc_commit_elect(bar_q_empty);
+                    for (int j = 0; ok && j < itm.n_max; ++j) {
+                        int last_pv = 0, last_s = -1;
+#pragma unroll
+                        for (int t = 0; t < NT; ++t) {
+                            if (j < itm.n_kv[t]) last_pv = t;
+                            if (j + 2 < itm.n_kv[t]) last_s = t;
+                        }
+                        bool v_ready = false, k_ready = false;
+#pragma unroll
+                        for (int t = 0; t < NT; ++t) {
+                            if (!ok || j >= itm.n_kv[t]) continue;
+                            const int gi = gs[t] + j;
+                            ok = mbar_wait_warp<kIn>(bar_p_full + 8 * slot(t, gi), (gi >> 1) & 1, g,
+                                                     SITE_FWD_MMA_P_FULL);
+                            // The first PV of an item overwrites O_t: the previous item's
+                            // epilogue must have read it.
+                            if (ok && j == 0 && oc[t] > 0)
+                                ok = mbar_wait_warp<kIn>(bar_o_free + 8 * t, (oc[t] - 1) & 1, g,
+                                                         SITE_FWD_MMA_P_FULL);
+                            tc_fence_after();
+                            if (ok && !v_ready) ok = v_ready = wait_v(vc + j);
+                            if (!ok) break;
+                            issue_pv(t, slot(t, gi), (vc + j) % VS, j == 0);
+                            tc_commit_elect(bar_pv_done + 8 * t);
+                            if (t == last_pv) tc_commit_elect(bar_v_empty + 8 * ((vc + j) % VS));
+                            if (j + 2 < itm.n_kv[t]) {
+                                if (!k_ready) ok = k_ready = wait_k(kc + j + 2);
+                                if (!ok) break;
+                                issue_s(t, slot(t, gs[t] + j), (kc + j + 2) % KS);
+                                if (j + 3 == itm.n_kv[t]) tc_commit_elect(bar_q_empty + 8 * t);
+                                if (t == last_s) tc_commit_elect(bar_k_empty + 8 * ((kc + j + 2) % KS));
+                            }
+                            if (j + 1 == itm.n_kv[t]) {
+                                tc_commit_elect(bar_o_full + 8 * t);  // O_t is final once this fires
+                                ++oc[t];
+                            }
                         }
                     }
-                    if (ok) {
-                        tc_commit_elect(bar_o_full);
-                        ++oc[0];
-                    }
-                    gs += n;
+#pragma unroll
+                    for (int t = 0; t < NT; ++t) gs[t] += itm.n_kv[t];
                 }
                 kc += itm.n_max;
                 vc += itm.n_max;
@@ -645,18 +684,19 @@ __global__ void __launch_bounds__(FwdTile<D, F8, ONE>::THREADS, 1)
         // 32-byte aligned base (the boundary guarantees 16)
         const bool out_al32 = (reinterpret_cast<uintptr_t>(out) & 31u) == 0;
         // Half exchange (NH = 2): each thread publishes one value per phase of bar_x[t]
-        // (its half's row maximum per K/V tile; its partial row sum, then a "read"
-        // mark, per item) and reads the other half's.  Both halves run the same
-        // sequence of phases.  A slot is rewritten only after the other half has read
-        // it: within an item the next maximum follows S(j+1), which the MMA issues
-        // only after both halves' P(j); across items the "read" phase guards it.
-        // Each half writes its P over its own S columns, so the halves share no
-        // tensor memory within a step.
-        float *x_mine = reinterpret_cast<float *>(gbase + T::OFF_XCH) + (t * T::NH + hc) * T::BM + r;
-        const float *x_other =
-            reinterpret_cast<const float *>(gbase + T::OFF_XCH) + (t * T::NH + (T::NH - 1 - hc)) * T::BM + r;
+        // (its half's row maximum per K/V tile, its partial row sum per item) and reads
+        // the other half's; both halves run the same sequence of phases.  A slot is
+        // rewritten only after the other half has read it.  With two buffers (XB = 2,
+        // alternating by phase) that holds by itself: a buffer is rewritten two phases
+        // later, which the writer reaches only after the reader's next arrival.  With
+        // one buffer (one S slot per tile) it holds within an item because the next
+        // maximum follows S(j+1), which the MMA issues only after both halves' P(j);
+        // across items a "read" phase after the row sums guards it.  Each half writes
+        // its P over its own S columns, so the halves share no tensor memory.
+        float *x_base = reinterpret_cast<float *>(gbase + T::OFF_XCH);
+        auto x_slot = [&](int b, int h) { return x_base + ((b * NT + t) * T::NH + h) * T::BM + r; };
         uint32_t xph = 0;      // phases of bar_x[t] this thread has taken part in
-        bool x_guard = false;  // the last phase was a "read" mark not yet waited for
+        bool x_guard = false;  // one buffer: the last phase was a "read" mark not yet waited for
         auto x_arrive = [&]() {
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_x + 8 * t);
@@ -667,12 +707,13 @@ __global__ void __launch_bounds__(FwdTile<D, F8, ONE>::THREADS, 1)
         };
         // publish v, wait for the other half's value of the same phase
         auto x_trade = [&](float v, float &other) -> bool {
-            if (x_guard && !x_wait_last()) return false;
+            if (T::XB == 1 && x_guard && !x_wait_last()) return false;
             x_guard = false;
-            *x_mine = v;
+            const int b = (T::XB == 2) ? (int)(xph & 1) : 0;
+            *x_slot(b, hc) = v;
             x_arrive();
             if (!x_wait_last()) return false;
-            other = *x_other;
+            other = *x_slot(b, T::NH - 1 - hc);
             return true;
         };
         int sc = 0;  // S products of this tile consumed before the current item
@@ -696,7 +737,7 @@ __global__ void __launch_bounds__(FwdTile<D, F8, ONE>::THREADS, 1)
             if constexpr (F8) c_q *= q_descale[(size_t)itm.bh * nqb + row0 / T::BM];
             for (int j = 0; j < n_it; ++j) {
                 const int gsj = sc + j;                                     // running S index
-                const int u = (T::SB == 1) ? t : (gsj & 1);                 // S slot
+                const int u = (T::SB == 1) ? t : (2 * t + (gsj & 1));       // S slot
                 const uint32_t par = (T::SB == 1) ? (gsj & 1) : ((gsj >> 1) & 1);
                 const uint32_t t_s = tmem + lane_base + T::BN * u;
                 float c_s = c_q;
@@ -797,7 +838,7 @@ __global__ void __launch_bounds__(FwdTile<D, F8, ONE>::THREADS, 1)
                         tmem_st32(t_s + hc * CB, pk);
                     else
                         tmem_st16(t_s + hc * CB, pk);
-                } else {
+                } else if constexpr (CB >= 64) {
 #pragma unroll
                     for (int c = 0; c < CB / 64; ++c) {
                         uint32_t pk[32];
@@ -806,6 +847,12 @@ __global__ void __launch_bounds__(FwdTile<D, F8, ONE>::THREADS, 1)
                             pk[e] = pack_bf16(s[c * 64 + 2 * e], s[c * 64 + 2 * e + 1]);
                         tmem_st32(t_s + hc * CB + c * 32, pk);
                     }
+                } else {
+                    uint32_t pk[CB / 2];
+#pragma unroll
+                    for (int e = 0; e < CB / 2; ++e) pk[e] = pack_bf16(s[2 * e], s[2 * e + 1]);
+                    static_assert(CB / 2 == 16, "P words per thread");
+                    tmem_st16(t_s + hc * CB, pk);
                 }
                 if (j > 0 && __any_sync(0xffffffffu, move)) {
                     // O_t <- alpha O_t for this warp's 32 rows (alpha = 1 on rows that kept
@@ -813,7 +860,7 @@ __global__ void __launch_bounds__(FwdTile<D, F8, ONE>::THREADS, 1)
                     // alternate 32-column chunks.  PV(j-1) must be complete: with one
                     // slot per tile S(j) was issued after it; with two slots it is
                     // awaited here.  PV(j) waits for the arrive below.
-                    if (T::SB == 2 && !mbar_wait_warp<kIn>(bar_pv_done, (gsj - 1) & 1, g,
+                    if (T::SB == 2 && !mbar_wait_warp<kIn>(bar_pv_done + 8 * t, (gsj - 1) & 1, g,
                                                       SITE_FWD_SOFTMAX_S_FULL)) {
                         ok = false;
                         break;
@@ -837,7 +884,7 @@ __global__ void __launch_bounds__(FwdTile<D, F8, ONE>::THREADS, 1)
                 }
                 tmem_wait_st();
                 tc_fence_before();
-                mbar_arrive(bar_p_full + 8 * t);
+                mbar_arrive(bar_p_full + 8 * u);
             }
             if (!ok) break;
             sc += n_it;
@@ -851,8 +898,10 @@ __global__ void __launch_bounds__(FwdTile<D, F8, ONE>::THREADS, 1)
                 float lo;
                 if (!(ok = x_trade(l, lo))) break;
                 l = (hc == 0) ? l + lo : lo + l;
-                x_arrive();
-                x_guard = true;
+                if constexpr (T::XB == 1) {
+                    x_arrive();
+                    x_guard = true;
+                }
             } else if constexpr (T::CB > 64) {
                 l = l + l_hi;
             }

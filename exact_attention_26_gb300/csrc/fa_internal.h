@@ -67,6 +67,9 @@ struct FwdParams {
 // (0: no cut); `forced` > 0 asks for that many tiles (rounded up to the tiles of a
 // row block on the diagonal).
 int fwd_split_chunk(int d, int BH, int N, int causal, int num_sms, int forced);
+// Rows per TMA box of the forward's K and V tensor maps (the kernel loads a K/V
+// tile of BN keys as BN / box boxes).
+constexpr int fwd_kv_box_rows(int d) { return d == 256 ? 64 : 128; }
 
 // e4m3 block quantiser: x bf16 [BH][N][d] -> codes [BH][N][d] (or [BH][d][Np]).
 struct QuantParams {
