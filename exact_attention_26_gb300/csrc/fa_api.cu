@@ -613,11 +613,11 @@ int check_decode_sizes(int B, int H, int Hkv, int Nq, int Nk, int d) {
 // times (four stages of fill and merge per CTA), and each range keeps at least
 // eight stages so the ring has something to overlap.  BHkv key/value heads, R
 // query rows per key/value head.
-void decode_split(long long BHkv, int R, int Nk, int d, int requested, int num_sms, int *S,
-                  int *keys_per_split) {
-    const long long bk = decode_block_keys(d);
+void decode_split(long long BHkv, int R, int Nk, int d, bool paged, int requested, int num_sms,
+                  int *S, int *keys_per_split) {
+    const long long bk = decode_block_keys(d, R, paged);
     const long long tiles = (Nk + bk - 1) / bk;
-    const long long qb = decode_query_block(d, R);
+    const long long qb = decode_query_block(d, R, paged);
     const long long base = BHkv * ((R + qb - 1) / qb);
     long long s = 1;
     if (requested > 0) {
@@ -628,7 +628,8 @@ void decode_split(long long BHkv, int R, int Nk, int d, int requested, int num_s
         // minimised over every split down to one stage per CTA.  Short caches are
         // latency-bound, so they split finely (B1 H8 Nk1024 d128: 16 ranges, 7.6 us,
         // against 14.0 us with at least 8 stages per range).
-        const long long slots = (long long)(num_sms > 0 ? num_sms : 1) * decode_ctas_per_sm(d, R);
+        const long long slots =
+            (long long)(num_sms > 0 ? num_sms : 1) * decode_ctas_per_sm(d, R, paged);
         long long cap = tiles;
         if (cap < 1) cap = 1;
         if (cap > 1024) cap = 1024;
@@ -663,7 +664,7 @@ int decode_launch(DecodeParams &p, int B, int num_splits, void *workspace, size_
     int rc = current_device(&dc);
     if (rc != FA_OK) return rc;
     const int R = p.group * p.Nq;
-    decode_split((long long)B * p.Hkv, R, p.Nk, p.d, num_splits, dc->num_sms, &p.S,
+    decode_split((long long)B * p.Hkv, R, p.Nk, p.d, p.paged != 0, num_splits, dc->num_sms, &p.S,
                  &p.keys_per_split);
     const long long rows = (long long)B * p.H * p.Nq;
     const size_t need = decode_ws_bytes(rows, p.S, p.d);
@@ -675,23 +676,42 @@ int decode_launch(DecodeParams &p, int B, int num_splits, void *workspace, size_
                                              round_up((size_t)rows * p.S * p.d * sizeof(float), 256));
     }
     p.BH = B * p.H;
+    if (decode_uses_mma(p.d, R, p.paged != 0)) {
+        // tensor-core kernel: q as one [B*H*Nq][d] matrix in boxes of 128 rows, the
+        // cache in 64-key boxes
+        if ((rc = make_bhnd_map(&p.tm_q, p.q, 1, (int)rows, p.d, 128)) != FA_OK) return rc;
+        if ((rc = make_bhnd_map(&p.tm_k, p.k, B * p.Hkv, p.Nk, p.d, 64)) != FA_OK) return rc;
+        if ((rc = make_bhnd_map(&p.tm_v, p.v, B * p.Hkv, p.Nk, p.d, 64)) != FA_OK) return rc;
+    }
     p.status = dc->status;
     p.limit_ns = kWaitLimitNs;
     return launch_decode(p, static_cast<cudaStream_t>(stream));
 }
 
-}  // namespace
-}  // namespace fa
-
-extern "C" int fa_decode_num_splits(int B, int H, int Hkv, int Nq, int Nk, int d, int num_splits) {
+// Key ranges a decode launch uses, or -(error code).
+int decode_num_splits(int B, int H, int Hkv, int Nq, int Nk, int d, int num_splits, bool paged) {
     int rc = check_decode_sizes(B, H, Hkv, Nq, Nk, d);
     if (rc != FA_OK) return -rc;
     if (num_splits < 0) return -FA_ERR_INVALID_ARG;
     DeviceCache *dc = nullptr;
     if ((rc = current_device(&dc)) != FA_OK) return -rc;
     int S = 1, per = 0;
-    decode_split((long long)B * Hkv, (H / Hkv) * Nq, Nk, d, num_splits, dc->num_sms, &S, &per);
+    decode_split((long long)B * Hkv, (H / Hkv) * Nq, Nk, d, paged, num_splits, dc->num_sms, &S,
+                 &per);
     return S;
+}
+
+}  // namespace
+}  // namespace fa
+
+extern "C" int fa_decode_num_splits(int B, int H, int Hkv, int Nq, int Nk, int d, int num_splits) {
+    return decode_num_splits(B, H, Hkv, Nq, Nk, d, num_splits, false);
+}
+
+extern "C" int fa_decode_uses_tensor_cores(int H, int Hkv, int Nq, int d, int paged) {
+    const int rc = check_decode_sizes(1, H, Hkv, Nq, 1, d);
+    if (rc != FA_OK) return -rc;
+    return decode_uses_mma(d, (H / Hkv) * Nq, paged != 0) ? 1 : 0;
 }
 
 extern "C" size_t fa_decode_workspace_bytes(int B, int H, int Hkv, int Nq, int Nk, int d,
@@ -747,7 +767,7 @@ extern "C" int fa_decode_paged_num_splits(int B, int H, int Hkv, int Nq, int d, 
                                           int max_pages_per_seq, int num_splits) {
     int rc = check_paged_sizes(B, H, Hkv, Nq, d, page_size, max_pages_per_seq, 1);
     if (rc != FA_OK) return -rc;
-    return fa_decode_num_splits(B, H, Hkv, Nq, page_size * max_pages_per_seq, d, num_splits);
+    return decode_num_splits(B, H, Hkv, Nq, page_size * max_pages_per_seq, d, num_splits, true);
 }
 
 extern "C" size_t fa_decode_paged_workspace_bytes(int B, int H, int Hkv, int Nq, int d,

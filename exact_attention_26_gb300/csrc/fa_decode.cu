@@ -46,6 +46,9 @@ constexpr int dec_qblock() { return D == 256 ? 4 : 8; }
 
 constexpr unsigned kFull = 0xffffffffu;
 constexpr float kLn2 = 0.69314718055994530942f;
+// The tensor-core kernel's reference max moves only when a tile's max passes it by
+// more than 2^8 (as in the forward): a stale reference cancels exactly in O/l and L.
+constexpr float kRescaleLog2Dec = 8.0f;
 
 // Eight per-lane partial dot products (one per key of a group) -> the full
 // 32-lane sum of key ((lane >> 2) & 7) in every lane, with 9 shuffles instead of
@@ -430,16 +433,11 @@ __global__ void __launch_bounds__(128)
     if (lane == 0) lse[orow] = M + __logf(W);
 }
 
-template <int D, int QB, bool PAGED>
-int launch_decode_t(const DecodeParams &p, cudaStream_t stream) {
-    using T = DecTile<D>;
-    auto kern = fa_decode_split_kernel<D, QB, PAGED>;
-    if (ensure_smem_attr(reinterpret_cast<const void *>(kern), (int)T::SMEM_BYTES) != FA_OK)
-        return FA_ERR_CUDA;
+// The merge of the key ranges (S > 1), a programmatic dependent of the kernel that
+// wrote the partial results.
+template <int D>
+int launch_decode_combine(const DecodeParams &p, cudaStream_t stream) {
     const int R = p.group * p.Nq;
-    const dim3 grid((unsigned)(p.BH / p.group), (unsigned)p.S, (unsigned)((R + QB - 1) / QB));
-    kern<<<grid, T::THREADS, T::SMEM_BYTES, stream>>>(p);
-    if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
     if (p.S > 1) {
         const long long rows = (long long)(p.BH / p.group) * R;
         // a programmatic dependent of the split kernel: launched as its last CTAs
@@ -461,9 +459,380 @@ int launch_decode_t(const DecodeParams &p, cudaStream_t stream) {
     return FA_OK;
 }
 
+template <int D, int QB, bool PAGED>
+int launch_decode_t(const DecodeParams &p, cudaStream_t stream) {
+    using T = DecTile<D>;
+    auto kern = fa_decode_split_kernel<D, QB, PAGED>;
+    if (ensure_smem_attr(reinterpret_cast<const void *>(kern), (int)T::SMEM_BYTES) != FA_OK)
+        return FA_ERR_CUDA;
+    const int R = p.group * p.Nq;
+    const dim3 grid((unsigned)(p.BH / p.group), (unsigned)p.S, (unsigned)((R + QB - 1) / QB));
+    kern<<<grid, T::THREADS, T::SMEM_BYTES, stream>>>(p);
+    if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
+    return launch_decode_combine<D>(p, stream);
+}
+
+// ---------------------------------------------------------------------------
+// Tensor-core decode, for R = (H / Hkv) Nq >= kDecMmaMinRows query rows per
+// key/value head (a few new tokens per sequence, or grouped queries).  With
+// several rows the score and output products are small matrix products, and on
+// CUDA cores their multiply-adds (2 R d per key), not the cache stream, bound the
+// kernel.  Here they run as tcgen05 products with M = 128: the CTA's rows of one
+// key/value head (up to 128; the rest of the 128 are padding whose results are
+// dropped) against 64-key tiles of K and V that TMA streams through a ring.  Per
+// tile j:
+//   S(j) = Q K_j^T    (A and B from shared memory, N = 64, K = d) into one of two
+//                     S slots
+//   softmax of the CTA's rows (thread r owns row r: the forward's online softmax
+//   with its lazy reference max), P(j) as bf16 over S(j)
+//   O += P(j) V_j     (A = P from tensor memory, N = d, K = 64)
+// S(j+2) is issued right after PV(j) frees its slot, so the next S is ready while
+// the softmax works.  Warps 0-3: softmax (warp w rows 32w..32w+31; warps without
+// rows idle); warp 4: TMEM allocation and MMA issue (one elected lane); warp 5:
+// TMA producer.  The key range split and the merge of the ranges are the CUDA-core
+// kernel's (same partial-result layout).
+template <int D>
+struct DecMmaTile {
+    static constexpr int BM = 128;                   // query rows per CTA (the MMA's M)
+    static constexpr int BK = 64;                    // keys per stage
+    static constexpr int DP = (D + 63) / 64 * 64;    // row width in shared memory
+    static constexpr int NCH = DP / 64;              // 128-byte swizzle chunks per row
+    static constexpr int STAGES = (DP == 64) ? 8 : 5;
+    static constexpr uint32_t Q_CHUNK = BM * 128;
+    static constexpr uint32_t KV_CHUNK = BK * 128;
+    static constexpr uint32_t Q_BYTES = BM * DP * 2;
+    static constexpr uint32_t KV_BYTES = BK * DP * 2;      // one of K_j, V_j
+    static constexpr uint32_t STAGE_BYTES = 2 * KV_BYTES;  // K_j, then V_j
+    static constexpr uint32_t OFF_Q = 0;
+    static constexpr uint32_t OFF_KV = Q_BYTES;
+    static constexpr uint32_t OFF_BAR = OFF_KV + STAGES * STAGE_BYTES;
+    // q_full, full[STAGES], empty[STAGES], s_full[2], p_full[2], pv_done, o_full, mma_done
+    static constexpr int NBAR = 1 + 2 * STAGES + 2 + 2 + 3;
+    static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
+    static constexpr uint32_t SMEM_BYTES = OFF_MISC + 16 + 1024;  // + alignment slack
+    static constexpr uint32_t TM_O = 2 * BK;  // S slots at columns 0 and BK, then O (d columns)
+    static constexpr uint32_t TM_COLS = 256;
+    static constexpr int THREADS = 192;
+    static_assert(TM_O + D <= TM_COLS, "tensor memory budget");
+    static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+    static_assert(Q_CHUNK % 1024 == 0 && KV_CHUNK % 1024 == 0 && KV_BYTES % 1024 == 0,
+                  "swizzle atoms must stay aligned");
+};
+
+constexpr int kDecMmaMinRows = 4;
+
+template <int D>
+__global__ void __launch_bounds__(DecMmaTile<D>::THREADS, 1)
+    fa_decode_mma_kernel(const __grid_constant__ DecodeParams p) {
+    using T = DecMmaTile<D>;
+    griddep_launch_dependents();  // the merge kernel may launch while the ranges run
+    constexpr int BK = T::BK, STAGES = T::STAGES;
+    extern __shared__ uint8_t dec_smem_raw[];
+    const uint32_t raw = smem_u32(dec_smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *gbase = dec_smem_raw + (base - raw);
+    const uint32_t sQ = base + T::OFF_Q, sKV = base + T::OFF_KV;
+    const uint32_t bar_q = base + T::OFF_BAR;
+    const uint32_t bar_full = bar_q + 8;                  // [STAGES]
+    const uint32_t bar_empty = bar_full + 8 * STAGES;     // [STAGES]
+    const uint32_t bar_s = bar_empty + 8 * STAGES;        // [2]
+    const uint32_t bar_p = bar_s + 16;                    // [2]
+    const uint32_t bar_pv = bar_p + 16, bar_o = bar_pv + 8, bar_done = bar_o + 8;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + T::OFF_MISC);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(gbase + T::OFF_MISC + 4);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    // One CTA per (key/value head, key range, block of 128 of its R rows).  The R
+    // rows of key/value head kvh are consecutive in q, o and lse: the Nq rows of
+    // each of its `group` query heads in turn.
+    const int kvh = blockIdx.x, split = blockIdx.y;
+    const int R = p.group * p.Nq;
+    const int r0 = blockIdx.z * T::BM;
+    const int nrows = min(T::BM, R - r0);
+    const int b = kvh / p.Hkv;
+    const long long row_base =
+        ((long long)b * p.H + (long long)(kvh % p.Hkv) * p.group) * p.Nq + r0;
+    const int k0 = split * p.keys_per_split;
+    const int k1 = min(p.Nk, k0 + p.keys_per_split);
+    const int n_tiles = k1 > k0 ? (k1 - k0 + BK - 1) / BK : 0;  // 0: an empty range
+    const int n_sw = (nrows + 31) / 32;                           // softmax warps with rows
+
+    if (threadIdx.x == 0) {
+        mbar_init(bar_q, 1);
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(bar_full + 8 * s, 1);
+            mbar_init(bar_empty + 8 * s, 1);
+        }
+        for (int u = 0; u < 2; ++u) {
+            mbar_init(bar_s + 8 * u, 1);
+            mbar_init(bar_p + 8 * u, 32 * n_sw);  // per S slot, one arrival per softmax thread
+        }
+        mbar_init(bar_pv, 1);
+        mbar_init(bar_o, 1);
+        mbar_init(bar_done, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 4) {
+        tmem_alloc(smem_u32(tmem_slot), T::TM_COLS);
+        tmem_relinquish();
+    }
+    if (warp == 5 && lane == 0) {
+        tma_prefetch_desc(&p.tm_q);
+        tma_prefetch_desc(&p.tm_k);
+        tma_prefetch_desc(&p.tm_v);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const Guard g{p.status, abort_flag, p.limit_ns};
+
+    if (warp == 5) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0 && n_tiles > 0) {
+            int issued = 0;
+            // the CTA's 128 rows of q: rows past this head's R belong to other heads
+            // (or read as zeros past the tensor) and are computed and dropped
+            mbar_arrive_expect_tx(bar_q, T::Q_BYTES);
+            for (int c = 0; c < T::NCH; ++c)
+                tma_load_3d(sQ + c * T::Q_CHUNK, &p.tm_q, bar_q, c * 64, (int)row_base, 0);
+            for (int t = 0; t < n_tiles; ++t) {
+                const int st = t % STAGES;
+                if (t >= STAGES &&
+                    !mbar_wait(bar_empty + 8 * st, ((t / STAGES) - 1) & 1, g, SITE_DEC_EMPTY))
+                    break;
+                const uint32_t dst = sKV + st * T::STAGE_BYTES;
+                const uint32_t fb = bar_full + 8 * st;
+                const int key = k0 + t * BK;  // keys past Nk read as zeros and are masked
+                mbar_arrive_expect_tx(fb, T::STAGE_BYTES);
+                for (int c = 0; c < T::NCH; ++c) {
+                    tma_load_3d(dst + c * T::KV_CHUNK, &p.tm_k, fb, c * 64, key, kvh);
+                    tma_load_3d(dst + T::KV_BYTES + c * T::KV_CHUNK, &p.tm_v, fb, c * 64, key, kvh);
+                }
+                ++issued;
+            }
+            if (*abort_flag) {
+                // let every copy still in flight land before the CTA exits
+                volatile int never = 0;
+                const Guard g2{p.status, &never, kWaitLimitNs};
+                mbar_wait(bar_q, 0, g2, SITE_DEC_DRAIN);
+                for (int t = (issued > STAGES ? issued - STAGES : 0); t < issued; ++t)
+                    mbar_wait(bar_full + 8 * (t % STAGES), (t / STAGES) & 1, g2, SITE_DEC_DRAIN);
+            }
+        }
+    } else if (warp == 4) {
+        // ------------------------------------------------------------ MMA issuer
+        // The whole warp runs this loop (warp-uniform); one elected lane issues.
+        constexpr uint32_t kIdescS = idesc_bf16_f32(128, BK, false, false);
+        constexpr uint32_t kIdescO = idesc_bf16_f32(128, D, false, true);
+        auto issue_s = [&](int u, int st) {  // S slot u = Q K^T from stage st
+            const uint64_t dq = sdesc_sw128(sQ, 16, 1024);
+            const uint64_t dk = sdesc_sw128(sKV + st * T::STAGE_BYTES, 16, 1024);
+#pragma unroll
+            for (int ks = 0; ks < D / 16; ++ks) {
+                const uint32_t koff = (ks & 3) * 32;
+                mma_ss_elect(tmem + BK * u, desc_add(dq, (ks >> 2) * T::Q_CHUNK + koff),
+                             desc_add(dk, (ks >> 2) * T::KV_CHUNK + koff), kIdescS, ks > 0 ? 1u : 0u);
+            }
+            tc_commit_elect(bar_s + 8 * u);
+        };
+        auto issue_pv = [&](int u, int st, bool first) {  // O += P(slot u) V(stage st)
+            const uint64_t dv = sdesc_sw128(sKV + st * T::STAGE_BYTES + T::KV_BYTES, T::KV_CHUNK, 1024);
+#pragma unroll
+            for (int ks = 0; ks < BK / 16; ++ks)
+                mma_ts_elect(tmem + T::TM_O, tmem + BK * u + ks * 8, desc_add(dv, ks * 2048), kIdescO,
+                             (!first || ks > 0) ? 1u : 0u);
+        };
+        auto wait_full = [&](int t) {
+            const bool r = mbar_wait_warp(bar_full + 8 * (t % STAGES), (t / STAGES) & 1, g, SITE_DEC_FULL);
+            tc_fence_after();
+            return r;
+        };
+        bool ok = n_tiles > 0;
+        if (ok) {
+            ok = mbar_wait_warp(bar_q, 0, g, SITE_DEC_MMA);
+            tc_fence_after();
+        }
+        for (int t = 0; ok && t < 2 && t < n_tiles; ++t)
+            if ((ok = wait_full(t))) issue_s(t & 1, t % STAGES);
+        for (int j = 0; ok && j < n_tiles; ++j) {
+            ok = mbar_wait_warp(bar_p + 8 * (j & 1), (j >> 1) & 1, g, SITE_DEC_MMA);
+            tc_fence_after();
+            if (!ok) break;
+            issue_pv(j & 1, j % STAGES, j == 0);
+            tc_commit_elect(bar_pv);
+            tc_commit_elect(bar_empty + 8 * (j % STAGES));  // S(j) and PV(j) have read the stage
+            if (j + 2 < n_tiles) {
+                if (!(ok = wait_full(j + 2))) break;
+                issue_s(j & 1, (j + 2) % STAGES);
+            }
+        }
+        if (ok && n_tiles > 0) tc_commit_elect(bar_o);
+        // fires once every MMA issued above has completed (normal or aborted run)
+        tc_commit_elect(bar_done);
+        volatile int never = 0;
+        const Guard g2{p.status, &never, kWaitLimitNs};
+        mbar_wait_warp(bar_done, 0, g2, SITE_DEC_DRAIN);
+    } else if (warp < n_sw) {
+        // ------------------------------------------------------------ softmax
+        const int r = warp * 32 + lane;  // row of this CTA (TMEM lane r)
+        const bool valid = r < nrows;
+        const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+        const uint32_t t_o = tmem + lane_base + T::TM_O;
+        const float c_s = p.scale_log2;
+        float m_ref = -INFINITY, l = 0.f;
+        bool ok = true;
+        for (int j = 0; j < n_tiles; ++j) {
+            const int u = j & 1;
+            const uint32_t t_s = tmem + lane_base + BK * u;
+            if (!(ok = mbar_wait_warp(bar_s + 8 * u, (j >> 1) & 1, g, SITE_DEC_MMA))) break;
+            tc_fence_after();
+            uint32_t sr[2][32];
+            tmem_ld32(t_s, sr[0]);
+            tmem_ld32(t_s + 32, sr[1]);
+            tmem_wait_ld(sr[0]);
+            tmem_wait_ld(sr[1]);
+            float s[BK];
+#pragma unroll
+            for (int c = 0; c < 2; ++c)
+#pragma unroll
+                for (int e = 0; e < 32; ++e) s[c * 32 + e] = __uint_as_float(sr[c][e]);
+            const int key0 = k0 + j * BK;
+            if (key0 + BK > k1) {  // the range's last tile: keys from k1 on are not this CTA's
+#pragma unroll
+                for (int c = 0; c < BK; ++c)
+                    if (key0 + c >= k1) s[c] = -INFINITY;
+            }
+            float mp0 = -INFINITY, mp1 = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < BK; c += 4) {
+                mp0 = fmax3(mp0, s[c], s[c + 1]);
+                mp1 = fmax3(mp1, s[c + 2], s[c + 3]);
+            }
+            const float m_tile = fmaxf(mp0, mp1) * c_s;  // finite: tile j has a key of the range
+            float alpha = 1.f;
+            const bool move = m_tile > m_ref + kRescaleLog2Dec;
+            if (move) {
+                alpha = ex2(m_ref - m_tile);
+                m_ref = m_tile;
+            }
+            float sp0 = 0.f, sp1 = 0.f;
+            const uint64_t c2 = f32x2_splat(c_s), nm2 = f32x2_splat(-m_ref);
+#pragma unroll
+            for (int c = 0; c < BK; c += 2) {
+                fma_f32x2(s[c], s[c + 1], c2, nm2);
+                s[c] = ex2(s[c]);
+                s[c + 1] = ex2(s[c + 1]);
+                add_f32x2(sp0, sp1, s[c], s[c + 1]);
+            }
+            l = l * alpha + (sp0 + sp1);
+            uint32_t pk[32];
+#pragma unroll
+            for (int e = 0; e < 32; ++e) pk[e] = pack_bf16(s[2 * e], s[2 * e + 1]);
+            tmem_st32(t_s, pk);
+            if (j > 0 && __any_sync(0xffffffffu, move)) {
+                // O <- alpha O once PV(j-1) is complete (PV(j) waits for the arrive below)
+                if (!(ok = mbar_wait_warp(bar_pv, (j - 1) & 1, g, SITE_DEC_MMA))) break;
+                tc_fence_after();
+#pragma unroll 1
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t o[32];
+                    tmem_ld32(t_o + c * 32, o);
+                    tmem_wait_ld(o);
+                    const uint64_t a2 = f32x2_splat(alpha);
+#pragma unroll
+                    for (int e = 0; e < 32; e += 2) {
+                        float x0 = __uint_as_float(o[e]), x1 = __uint_as_float(o[e + 1]);
+                        mul_f32x2(x0, x1, a2);
+                        o[e] = __float_as_uint(x0);
+                        o[e + 1] = __float_as_uint(x1);
+                    }
+                    tmem_st32(t_o + c * 32, o);
+                }
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(bar_p + 8 * u);
+        }
+        if (ok && n_tiles > 0) ok = mbar_wait_warp(bar_o, 0, g, SITE_DEC_MMA);
+        tc_fence_after();
+        if (ok && !*abort_flag) {
+            // an empty key range contributes L = -inf and O = 0 to the merge
+            const bool empty = n_tiles == 0;
+            const float inv = empty ? 0.f : 1.f / l;
+            const float l_nat = empty ? -INFINITY : (m_ref + lg2(l)) * kLn2;
+            const long long row = row_base + r;
+            const long long prow = ((long long)kvh * p.S + split) * R + r0 + r;
+#pragma unroll 1
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t o[32];
+                if (!empty) {
+                    tmem_ld32(t_o + c * 32, o);
+                    tmem_wait_ld(o);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) o[e] = 0u;
+                }
+                if (!valid) continue;
+                if (p.S == 1) {
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e)
+                        pk[e] = pack_bf16(__uint_as_float(o[2 * e]) * inv, __uint_as_float(o[2 * e + 1]) * inv);
+                    uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(p.o) +
+                                                           (size_t)row * D + c * 32);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        dst[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+                } else {
+                    uint4 *dst = reinterpret_cast<uint4 *>(p.part_o + (size_t)prow * D + c * 32);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        dst[e] = make_uint4(__float_as_uint(__uint_as_float(o[4 * e]) * inv),
+                                            __float_as_uint(__uint_as_float(o[4 * e + 1]) * inv),
+                                            __float_as_uint(__uint_as_float(o[4 * e + 2]) * inv),
+                                            __float_as_uint(__uint_as_float(o[4 * e + 3]) * inv));
+                }
+            }
+            if (valid) {
+                if (p.S == 1)
+                    p.lse[row] = l_nat;
+                else
+                    p.part_l[prow] = l_nat;
+            }
+        }
+        tmem_wait_st();  // an aborted step may leave a store in flight
+    }
+
+    __syncwarp();
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 4) {
+        tc_fence_after();
+        tmem_dealloc(tmem, T::TM_COLS);
+    }
+}
+
+template <int D>
+int launch_decode_mma(const DecodeParams &p, cudaStream_t stream) {
+    using T = DecMmaTile<D>;
+    auto kern = fa_decode_mma_kernel<D>;
+    if (ensure_smem_attr(reinterpret_cast<const void *>(kern), (int)T::SMEM_BYTES) != FA_OK)
+        return FA_ERR_CUDA;
+    const int R = p.group * p.Nq;
+    const dim3 grid((unsigned)(p.BH / p.group), (unsigned)p.S, (unsigned)((R + T::BM - 1) / T::BM));
+    kern<<<grid, T::THREADS, T::SMEM_BYTES, stream>>>(p);
+    if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
+    return launch_decode_combine<D>(p, stream);
+}
+
 template <int D>
 int launch_decode_d(const DecodeParams &p, cudaStream_t stream) {
     constexpr int QB = dec_qblock<D>();
+    if constexpr (D <= 128) {
+        if (decode_uses_mma(D, p.group * p.Nq, p.paged != 0)) return launch_decode_mma<D>(p, stream);
+    }
     const bool one = p.group * p.Nq == 1;  // one query row per key/value head
     if (p.paged)
         return one ? launch_decode_t<D, 1, true>(p, stream) : launch_decode_t<D, QB, true>(p, stream);
@@ -500,19 +869,30 @@ int ctas_per_sm_d(int Nq) {
 
 }  // namespace
 
-int decode_block_keys(int d) { return d == 256 ? DecTile<256>::BK : DecTile<128>::BK; }
+// Several query rows per key/value head, contiguous cache, d <= 128: the tensor-core
+// kernel.  (Paged caches and d = 256 stay on the CUDA-core kernel.)
+bool decode_uses_mma(int d, int R, bool paged) {
+    return !paged && d <= 128 && R >= kDecMmaMinRows;
+}
 
-int decode_query_block(int d, int Nq) {
-    if (Nq == 1) return 1;
+int decode_block_keys(int d, int R, bool paged) {
+    if (decode_uses_mma(d, R, paged)) return DecMmaTile<128>::BK;
+    return d == 256 ? DecTile<256>::BK : DecTile<128>::BK;
+}
+
+int decode_query_block(int d, int R, bool paged) {
+    if (decode_uses_mma(d, R, paged)) return DecMmaTile<128>::BM;
+    if (R == 1) return 1;
     return d == 256 ? dec_qblock<256>() : dec_qblock<128>();
 }
 
-int decode_ctas_per_sm(int d, int Nq) {
+int decode_ctas_per_sm(int d, int R, bool paged) {
+    if (decode_uses_mma(d, R, paged)) return 1;  // ~190 KB of shared memory per CTA
     switch (d) {
-        case 64: return ctas_per_sm_d<64>(Nq);
-        case 96: return ctas_per_sm_d<96>(Nq);
-        case 128: return ctas_per_sm_d<128>(Nq);
-        case 256: return ctas_per_sm_d<256>(Nq);
+        case 64: return ctas_per_sm_d<64>(R);
+        case 96: return ctas_per_sm_d<96>(R);
+        case 128: return ctas_per_sm_d<128>(R);
+        case 256: return ctas_per_sm_d<256>(R);
         default: return 1;
     }
 }

@@ -38,6 +38,7 @@ enum WaitSite : int {
     SITE_DEC_DRAIN = 23,
     SITE_DEC_BAD_LEN = 24,
     SITE_DEC_BAD_PAGE = 25,
+    SITE_DEC_MMA = 28,
     SITE_SELFTEST = 30,
 };
 
@@ -109,6 +110,9 @@ struct BwdParams {
 constexpr int kBwdPad = 128;
 
 struct DecodeParams {
+    // tensor-core path only: q as [1][BH*Nq][d] (boxes of 128 rows), k and v as
+    // [B*Hkv][Nk][d] (boxes of 64 keys)
+    CUtensorMap tm_q, tm_k, tm_v;
     const void *q;            // bf16 [BH][Nq][d]
     const void *k, *v;        // bf16 [B*Hkv][Nk][d], or paged [num_pages][Hkv][page_size][d]
     void *o;                  // bf16 [BH][Nq][d]
@@ -139,8 +143,11 @@ int kernel_num_regs(const void *kernel);
 int launch_fwd(const FwdParams &p, cudaStream_t stream);
 int launch_bwd(const BwdParams &p, cudaStream_t stream);
 int launch_decode(const DecodeParams &p, cudaStream_t stream);
-int decode_block_keys(int d);          // keys per pipeline stage of the decode kernel
-int decode_query_block(int d, int Nq);  // query rows per decode CTA
-int decode_ctas_per_sm(int d, int Nq);  // resident decode CTAs per SM (occupancy query)
+// Decode with R = (H / Hkv) * Nq query rows per key/value head: whether the
+// tensor-core kernel serves it, and the launch shape of the kernel that does.
+bool decode_uses_mma(int d, int R, bool paged);
+int decode_block_keys(int d, int R, bool paged);   // keys per pipeline stage
+int decode_query_block(int d, int R, bool paged);  // query rows per decode CTA
+int decode_ctas_per_sm(int d, int R, bool paged);  // resident decode CTAs per SM
 
 }  // namespace fa

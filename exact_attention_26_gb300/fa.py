@@ -25,6 +25,7 @@ FA_ERR_BAD_INDEX = 7
 
 EXPORTED = ("fa_fwd", "fa_bwd", "fa_bwd_workspace_bytes", "fa_status_string", "fa_device_status",
             "fa_selftest_wait_timeout", "fa_decode", "fa_decode_num_splits",
+            "fa_decode_uses_tensor_cores",
             "fa_decode_workspace_bytes", "fa_decode_paged", "fa_decode_paged_num_splits",
             "fa_decode_paged_workspace_bytes", "fa_fwd_gqa", "fa_bwd_gqa", "fa_fwd_varlen",
             "fa_bwd_varlen", "fa_quantize_fp8_workspace_bytes", "fa_quantize_fp8", "fa_fwd_fp8",
@@ -85,6 +86,8 @@ def load() -> ctypes.CDLL:
         lib.fa_decode.restype = _int
         lib.fa_decode_num_splits.argtypes = [_int] * 7
         lib.fa_decode_num_splits.restype = _int
+        lib.fa_decode_uses_tensor_cores.argtypes = [_int] * 5
+        lib.fa_decode_uses_tensor_cores.restype = _int
         lib.fa_decode_workspace_bytes.argtypes = [_int] * 7
         lib.fa_decode_workspace_bytes.restype = ctypes.c_size_t
         lib.fa_decode_paged.argtypes = [_vp] * 7 + [_int] * 8 + [ctypes.c_float, _int, _vp,
@@ -245,6 +248,10 @@ def fa_decode(q, k, v, o, lse, B, H, Hkv, Nq, Nk, d, scale, num_splits, workspac
 
 def fa_decode_num_splits(B, H, Hkv, Nq, Nk, d, num_splits=0) -> int:
     return load().fa_decode_num_splits(B, H, Hkv, Nq, Nk, d, num_splits)
+
+
+def fa_decode_uses_tensor_cores(H, Hkv, Nq, d, paged=0) -> int:
+    return load().fa_decode_uses_tensor_cores(H, Hkv, Nq, d, int(paged))
 
 
 def fa_decode_workspace_bytes(B, H, Hkv, Nq, Nk, d, num_splits=0) -> int:

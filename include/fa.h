@@ -273,7 +273,10 @@ int fa_bwd_varlen(const void *q, const void *k, const void *v, const void *o, co
  * merges them: L = ln sum_s exp(L_s), O = sum_s exp(L_s - L) O_s.  The result is
  * the same as with one range up to rounding.  With grouped queries (Hkv < H, see
  * fa_fwd_gqa) the H / Hkv query heads of a key/value head are handled by the same
- * CTAs, so the cache is read once for all of them.
+ * CTAs, so the cache is read once for all of them.  With R = (H / Hkv) * Nq >= 4
+ * query rows per key/value head and d <= 128 the products run on the tensor cores
+ * (tcgen05, the CTA's rows as M = 128 against 64-key tiles); otherwise on CUDA
+ * cores (see fa_decode_uses_tensor_cores).
  *   q      : bf16 [B][H][Nq][d] (the new tokens' queries).
  *   k, v   : bf16 [B][Hkv][Nk][d] (the key/value cache, contiguous per head).
  *   o      : bf16 [B][H][Nq][d] output, rounded to nearest even.
@@ -301,6 +304,13 @@ int fa_decode(const void *q, const void *k, const void *v, void *o, float *lse, 
  * error.  Needs the device's SM count when num_splits is 0.
  */
 int fa_decode_num_splits(int B, int H, int Hkv, int Nq, int Nk, int d, int num_splits);
+
+/*
+ * 1 if fa_decode (paged = 0) or fa_decode_paged (paged = 1) runs these sizes on
+ * the tensor-core kernel, 0 if on the CUDA-core kernel, minus an fa_status code
+ * for invalid sizes.  (Paged caches always use the CUDA-core kernel.)
+ */
+int fa_decode_uses_tensor_cores(int H, int Hkv, int Nq, int d, int paged);
 
 /*
  * Workspace bytes fa_decode needs: 0 when S = 1, else room for the S partial

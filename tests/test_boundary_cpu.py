@@ -159,6 +159,19 @@ def test_decode_rejects_bad_arguments(fa, kw, code):
     assert _dec(fa, **kw) == code
 
 
+def test_decode_kernel_choice(fa):
+    """Several rows per key/value head with d <= 128 and a contiguous cache: the
+    tensor-core kernel; one row, d = 256 or a paged cache: the CUDA-core one."""
+    assert fa.fa_decode_uses_tensor_cores(32, 32, 4, 128, 0) == 1
+    assert fa.fa_decode_uses_tensor_cores(32, 8, 1, 64, 0) == 1
+    assert fa.fa_decode_uses_tensor_cores(32, 32, 3, 128, 0) == 0
+    assert fa.fa_decode_uses_tensor_cores(32, 32, 1, 128, 0) == 0
+    assert fa.fa_decode_uses_tensor_cores(32, 32, 4, 256, 0) == 0
+    assert fa.fa_decode_uses_tensor_cores(32, 32, 4, 128, 1) == 0
+    assert fa.fa_decode_uses_tensor_cores(6, 4, 1, 128, 0) == -1
+    assert fa.fa_decode_uses_tensor_cores(4, 4, 1, 80, 0) == -2
+
+
 def test_decode_split_queries_reject_bad_sizes(fa):
     assert fa.fa_decode_num_splits(0, 1, 1, 1, 100, 128, 0) == -1
     assert fa.fa_decode_num_splits(1, 1, 1, 1, 100, 80, 0) == -2
