@@ -678,10 +678,11 @@ int decode_launch(DecodeParams &p, int B, int num_splits, void *workspace, size_
     p.BH = B * p.H;
     if (decode_uses_mma(p.d, R, p.paged != 0)) {
         // tensor-core kernel: q as one [B*H*Nq][d] matrix in boxes of 128 rows, the
-        // cache in 64-key boxes
+        // cache in boxes of one pipeline stage of keys
         if ((rc = make_bhnd_map(&p.tm_q, p.q, 1, (int)rows, p.d, 128)) != FA_OK) return rc;
-        if ((rc = make_bhnd_map(&p.tm_k, p.k, B * p.Hkv, p.Nk, p.d, 64)) != FA_OK) return rc;
-        if ((rc = make_bhnd_map(&p.tm_v, p.v, B * p.Hkv, p.Nk, p.d, 64)) != FA_OK) return rc;
+        const int bk = decode_block_keys(p.d, R, false);
+        if ((rc = make_bhnd_map(&p.tm_k, p.k, B * p.Hkv, p.Nk, p.d, bk)) != FA_OK) return rc;
+        if ((rc = make_bhnd_map(&p.tm_v, p.v, B * p.Hkv, p.Nk, p.d, bk)) != FA_OK) return rc;
     }
     p.status = dc->status;
     p.limit_ns = kWaitLimitNs;

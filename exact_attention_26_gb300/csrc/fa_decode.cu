@@ -473,19 +473,19 @@ int launch_decode_t(const DecodeParams &p, cudaStream_t stream) {
 }
 
 // ---------------------------------------------------------------------------
-// Tensor-core decode, for R = (H / Hkv) Nq >= kDecMmaMinRows query rows per
+// Tensor-core decode, for R = (H / Hkv) Nq >= 2 query rows per
 // key/value head (a few new tokens per sequence, or grouped queries).  With
 // several rows the score and output products are small matrix products, and on
 // CUDA cores their multiply-adds (2 R d per key), not the cache stream, bound the
 // kernel.  Here they run as tcgen05 products with M = 128: the CTA's rows of one
 // key/value head (up to 128; the rest of the 128 are padding whose results are
-// dropped) against 64-key tiles of K and V that TMA streams through a ring.  Per
-// tile j:
-//   S(j) = Q K_j^T    (A and B from shared memory, N = 64, K = d) into one of two
+// dropped) against tiles of BK keys of K and V (64, or 128 at d = 64: a stage of
+// at least 16 KB each) that TMA streams through a ring.  Per tile j:
+//   S(j) = Q K_j^T    (A and B from shared memory, N = BK, K = d) into one of two
 //                     S slots
 //   softmax of the CTA's rows (thread r owns row r: the forward's online softmax
 //   with its lazy reference max), P(j) as bf16 over S(j)
-//   O += P(j) V_j     (A = P from tensor memory, N = d, K = 64)
+//   O += P(j) V_j     (A = P from tensor memory, N = d, K = BK)
 // S(j+2) is issued right after PV(j) frees its slot, so the next S is ready while
 // the softmax works.  Warps 0-3: softmax (warp w rows 32w..32w+31; warps without
 // rows idle); warp 4: TMEM allocation and MMA issue (one elected lane); warp 5:
@@ -494,10 +494,10 @@ int launch_decode_t(const DecodeParams &p, cudaStream_t stream) {
 template <int D>
 struct DecMmaTile {
     static constexpr int BM = 128;                   // query rows per CTA (the MMA's M)
-    static constexpr int BK = 64;                    // keys per stage
     static constexpr int DP = (D + 63) / 64 * 64;    // row width in shared memory
+    static constexpr int BK = (DP == 64) ? 128 : 64; // keys per stage (a stage of 16 KB or more)
     static constexpr int NCH = DP / 64;              // 128-byte swizzle chunks per row
-    static constexpr int STAGES = (DP == 64) ? 8 : 5;
+    static constexpr int STAGES = 5;
     static constexpr uint32_t Q_CHUNK = BM * 128;
     static constexpr uint32_t KV_CHUNK = BK * 128;
     static constexpr uint32_t Q_BYTES = BM * DP * 2;
@@ -511,7 +511,7 @@ struct DecMmaTile {
     static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr uint32_t SMEM_BYTES = OFF_MISC + 16 + 1024;  // + alignment slack
     static constexpr uint32_t TM_O = 2 * BK;  // S slots at columns 0 and BK, then O (d columns)
-    static constexpr uint32_t TM_COLS = 256;
+    static constexpr uint32_t TM_COLS = (TM_O + D <= 256) ? 256 : 512;
     static constexpr int THREADS = 192;
     static_assert(TM_O + D <= TM_COLS, "tensor memory budget");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
@@ -519,7 +519,7 @@ struct DecMmaTile {
                   "swizzle atoms must stay aligned");
 };
 
-constexpr int kDecMmaMinRows = 4;
+constexpr int kDecMmaMinRows = 2;
 
 template <int D>
 __global__ void __launch_bounds__(DecMmaTile<D>::THREADS, 1)
@@ -688,14 +688,14 @@ __global__ void __launch_bounds__(DecMmaTile<D>::THREADS, 1)
             const uint32_t t_s = tmem + lane_base + BK * u;
             if (!(ok = mbar_wait_warp(bar_s + 8 * u, (j >> 1) & 1, g, SITE_DEC_MMA))) break;
             tc_fence_after();
-            uint32_t sr[2][32];
-            tmem_ld32(t_s, sr[0]);
-            tmem_ld32(t_s + 32, sr[1]);
-            tmem_wait_ld(sr[0]);
-            tmem_wait_ld(sr[1]);
+            uint32_t sr[BK / 32][32];
+#pragma unroll
+            for (int c = 0; c < BK / 32; ++c) tmem_ld32(t_s + c * 32, sr[c]);
+#pragma unroll
+            for (int c = 0; c < BK / 32; ++c) tmem_wait_ld(sr[c]);
             float s[BK];
 #pragma unroll
-            for (int c = 0; c < 2; ++c)
+            for (int c = 0; c < BK / 32; ++c)
 #pragma unroll
                 for (int e = 0; e < 32; ++e) s[c * 32 + e] = __uint_as_float(sr[c][e]);
             const int key0 = k0 + j * BK;
@@ -727,10 +727,13 @@ __global__ void __launch_bounds__(DecMmaTile<D>::THREADS, 1)
                 add_f32x2(sp0, sp1, s[c], s[c + 1]);
             }
             l = l * alpha + (sp0 + sp1);
-            uint32_t pk[32];
 #pragma unroll
-            for (int e = 0; e < 32; ++e) pk[e] = pack_bf16(s[2 * e], s[2 * e + 1]);
-            tmem_st32(t_s, pk);
+            for (int c = 0; c < BK / 64; ++c) {  // P as bf16 pairs over the slot's first BK/2 columns
+                uint32_t pk[32];
+#pragma unroll
+                for (int e = 0; e < 32; ++e) pk[e] = pack_bf16(s[64 * c + 2 * e], s[64 * c + 2 * e + 1]);
+                tmem_st32(t_s + c * 32, pk);
+            }
             if (j > 0 && __any_sync(0xffffffffu, move)) {
                 // O <- alpha O once PV(j-1) is complete (PV(j) waits for the arrive below)
                 if (!(ok = mbar_wait_warp(bar_pv, (j - 1) & 1, g, SITE_DEC_MMA))) break;
@@ -876,7 +879,7 @@ bool decode_uses_mma(int d, int R, bool paged) {
 }
 
 int decode_block_keys(int d, int R, bool paged) {
-    if (decode_uses_mma(d, R, paged)) return DecMmaTile<128>::BK;
+    if (decode_uses_mma(d, R, paged)) return d == 64 ? DecMmaTile<64>::BK : DecMmaTile<128>::BK;
     return d == 256 ? DecTile<256>::BK : DecTile<128>::BK;
 }
 

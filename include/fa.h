@@ -273,10 +273,10 @@ int fa_bwd_varlen(const void *q, const void *k, const void *v, const void *o, co
  * merges them: L = ln sum_s exp(L_s), O = sum_s exp(L_s - L) O_s.  The result is
  * the same as with one range up to rounding.  With grouped queries (Hkv < H, see
  * fa_fwd_gqa) the H / Hkv query heads of a key/value head are handled by the same
- * CTAs, so the cache is read once for all of them.  With R = (H / Hkv) * Nq >= 4
+ * CTAs, so the cache is read once for all of them.  With R = (H / Hkv) * Nq >= 2
  * query rows per key/value head and d <= 128 the products run on the tensor cores
- * (tcgen05, the CTA's rows as M = 128 against 64-key tiles); otherwise on CUDA
- * cores (see fa_decode_uses_tensor_cores).
+ * (tcgen05, the CTA's rows as M = 128 against tiles of 64 or 128 keys); otherwise
+ * on CUDA cores (see fa_decode_uses_tensor_cores).
  *   q      : bf16 [B][H][Nq][d] (the new tokens' queries).
  *   k, v   : bf16 [B][Hkv][Nk][d] (the key/value cache, contiguous per head).
  *   o      : bf16 [B][H][Nq][d] output, rounded to nearest even.

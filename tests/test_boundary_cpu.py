@@ -164,7 +164,7 @@ def test_decode_kernel_choice(fa):
     tensor-core kernel; one row, d = 256 or a paged cache: the CUDA-core one."""
     assert fa.fa_decode_uses_tensor_cores(32, 32, 4, 128, 0) == 1
     assert fa.fa_decode_uses_tensor_cores(32, 8, 1, 64, 0) == 1
-    assert fa.fa_decode_uses_tensor_cores(32, 32, 3, 128, 0) == 0
+    assert fa.fa_decode_uses_tensor_cores(32, 32, 2, 96, 0) == 1
     assert fa.fa_decode_uses_tensor_cores(32, 32, 1, 128, 0) == 0
     assert fa.fa_decode_uses_tensor_cores(32, 32, 4, 256, 0) == 0
     assert fa.fa_decode_uses_tensor_cores(32, 32, 4, 128, 1) == 0

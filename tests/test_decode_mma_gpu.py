@@ -1,8 +1,9 @@
 """Tensor-core decode (several query rows per key/value head) against the float64
 oracle, through the C ABI.
 
-R = (H / Hkv) * Nq >= 4 rows per key/value head and d <= 128 run on the tcgen05
-kernel: the CTA's rows as M = 128 against 64-key tiles of the cache, two S slots,
+R = (H / Hkv) * Nq >= 2 rows per key/value head and d <= 128 run on the tcgen05
+kernel: the CTA's rows as M = 128 against 64-key tiles of the cache (128 at
+d = 64), two S slots,
 the forward's online softmax per row.  Cases: Nq in {2, 4, 8, 16}, grouped
 queries, more than 128 rows (several row blocks), ragged key counts and ranges,
 every head dimension it serves, and the B=8 H=32 Nq=4 Nk=32768 d=128 workload.
@@ -50,15 +51,17 @@ def _check(fa, orc, B, H, Hkv, Nq, Nk, d, splits, seed, what):
 @pytest.mark.parametrize("Nq", [2, 4, 8, 16])
 @pytest.mark.parametrize("splits", [0, 1, 3])
 def test_decode_rows(fa, orc, Nq, splits):
-    """Nq rows per head (multi-head: R = Nq); Nq = 2 stays on the CUDA-core kernel."""
+    """Nq rows per head (multi-head: R = Nq)."""
     B, H, Nk, d = 2, 4, 3001, 128
-    assert fa.fa_decode_uses_tensor_cores(H, H, Nq, d, 0) == (1 if Nq >= 4 else 0)
+    assert fa.fa_decode_uses_tensor_cores(H, H, Nq, d, 0) == 1
     _check(fa, orc, B, H, H, Nq, Nk, d, splits, Nq * 10 + splits, f"Nq={Nq} splits={splits}")
 
 
 # (B, H, Hkv, Nq, Nk, d, splits)
 SHAPES = [
     (1, 8, 2, 1, 1000, 128, 0),     # grouped queries, one new token: R = 4
+    (2, 4, 2, 1, 999, 64, 3),       # R = 2, d = 64 (128-key tiles)
+    (1, 2, 2, 3, 129, 64, 0),       # d = 64, a ragged second tile
     (2, 32, 4, 2, 777, 64, 0),      # R = 16, d = 64
     (1, 16, 1, 16, 700, 64, 2),     # R = 256: two row blocks of 128
     (1, 8, 1, 16, 513, 128, 0),     # R = 128 exactly
