@@ -71,13 +71,17 @@ BWD_WORKLOADS = [
     ("B4_H16_N4096_d96_causal", 4, 16, 4096, 96, True),
 ]
 
-# Split-KV decode (one query row per sequence against a long cache): bound by HBM.
+# Split-KV decode against a long cache: bound by HBM.  One query row per sequence
+# (CUDA-core kernel), and several rows per key/value head (four new tokens, or four
+# query heads sharing a key/value head: tensor-core kernel).  (name, B, H, Hkv, Nq, Nk, d)
 DEC_WORKLOADS = [
-    ("B8_H32_Nq1_Nk32768_d128", 8, 32, 1, 32768, 128),
-    ("B1_H32_Nq1_Nk32768_d128", 1, 32, 1, 32768, 128),
-    ("B8_H32_Nq1_Nk32768_d64", 8, 32, 1, 32768, 64),
-    ("B4_H16_Nq1_Nk32768_d256", 4, 16, 1, 32768, 256),
-    ("B8_H32_Nq1_Nk32768_d96", 8, 32, 1, 32768, 96),
+    ("B8_H32_Nq1_Nk32768_d128", 8, 32, 32, 1, 32768, 128),
+    ("B1_H32_Nq1_Nk32768_d128", 1, 32, 32, 1, 32768, 128),
+    ("B8_H32_Nq1_Nk32768_d64", 8, 32, 32, 1, 32768, 64),
+    ("B4_H16_Nq1_Nk32768_d256", 4, 16, 16, 1, 32768, 256),
+    ("B8_H32_Nq1_Nk32768_d96", 8, 32, 32, 1, 32768, 96),
+    ("B8_H32_Nq4_Nk32768_d128", 8, 32, 32, 4, 32768, 128),
+    ("B8_H32_Hkv8_Nq1_Nk32768_d128", 8, 32, 8, 1, 32768, 128),
 ]
 
 
@@ -88,10 +92,11 @@ PAGED_WORKLOADS = [
 ]
 
 
-def decode_bytes(B, H, Nq, Nk, d):
-    """Algorithmic HBM bytes of one decode call: read K, V (bf16) and q, write o
-    (bf16) and L (fp32); the partial results stay in L2."""
-    return 2 * B * H * Nk * d * 2 + 2 * B * H * Nq * d * 2 + B * H * Nq * 4
+def decode_bytes(B, H, Nq, Nk, d, Hkv=None):
+    """Algorithmic HBM bytes of one decode call: read K, V (bf16, Hkv heads) and q,
+    write o (bf16) and L (fp32); the partial results stay in L2."""
+    Hkv = H if Hkv is None else Hkv
+    return 2 * B * Hkv * Nk * d * 2 + 2 * B * H * Nq * d * 2 + B * H * Nq * 4
 
 
 def fwd_flops(B, H, N, d, causal):
@@ -732,11 +737,13 @@ def sweep_decode(fa, torch, dev, flush, peaks):
     from exact_attention_26_gb300.inputs import decode_qkv
     out = {}
     read_peak = None
-    for name, B, H, Nq, Nk, d in DEC_WORKLOADS:
-        q, k, v = decode_qkv(B, H, Nq, Nk, d, seed=0, device=dev)
+    for name, B, H, Hkv, Nq, Nk, d in DEC_WORKLOADS:
+        _, k, v = decode_qkv(B, Hkv, 1, Nk, d, seed=0, device=dev)
+        gq = torch.Generator(device=dev).manual_seed(1)
+        q = torch.randn((B, H, Nq, d), generator=gq, device=dev).to(torch.bfloat16)
         o = torch.empty_like(q)
         lse = torch.empty((B, H, Nq), dtype=torch.float32, device=dev)
-        need = fa.fa_decode_workspace_bytes(B, H, H, Nq, Nk, d, 0)
+        need = fa.fa_decode_workspace_bytes(B, H, Hkv, Nq, Nk, d, 0)
         ws = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
         if read_peak is None:
             read_peak = fa.probe_read_bandwidth(k, iters=5)
@@ -745,9 +752,11 @@ def sweep_decode(fa, torch, dev, flush, peaks):
                                        "over the first cache's K (2.1 GB), 5 passes",
                                 "copy_GB/s": peaks["hbm_gbs"]}
         ms = _time_call(torch, dev, lambda: fa.decode(q, k, v, out=o, lse=lse, workspace=ws), flush)
-        gbs = decode_bytes(B, H, Nq, Nk, d) / (ms * 1e-3) / 1e9
+        gbs = decode_bytes(B, H, Nq, Nk, d, Hkv) / (ms * 1e-3) / 1e9
         out[name] = {"ms": round(ms, 5), "GB/s": round(gbs, 1),
-                     "splits": fa.fa_decode_num_splits(B, H, H, Nq, Nk, d, 0),
+                     "splits": fa.fa_decode_num_splits(B, H, Hkv, Nq, Nk, d, 0),
+                     "kernel": ("tcgen05" if fa.fa_decode_uses_tensor_cores(H, Hkv, Nq, d, 0) == 1
+                                else "cuda-core"),
                      "roofline": {"bound": "hbm", "achieved": round(gbs, 1),
                                   "peak": round(read_peak, 1), "unit": "GB/s",
                                   "frac": round(gbs / read_peak, 4),

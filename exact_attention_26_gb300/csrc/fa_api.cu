@@ -61,38 +61,82 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_tiled() {
     return fn;
 }
 
+// A 3-D tiled map (unit element strides, no interleave, 256-byte L2 promotion, zero
+// fill past the bounds).  A map is a pure function of its arguments, so the last
+// few encodings are kept and reused: calls that repeat a tensor and shape (every
+// step of a training loop, every decode step) skip the driver call.  Keys hold the
+// address, so a freed and reallocated tensor at the same address with the same
+// shape gets the identical map.
+int encode_3d(CUtensorMap *map, CUtensorMapDataType dtype, const void *ptr, const cuuint64_t (&dims)[3],
+              const cuuint64_t (&strides)[2], const cuuint32_t (&box)[3], CUtensorMapSwizzle swizzle) {
+    struct Entry {
+        const void *ptr;
+        int dtype, swizzle;
+        cuuint64_t dims[3], strides[2];
+        cuuint32_t box[3];
+        CUtensorMap map;
+    };
+    constexpr int kEntries = 32;
+    static Entry cache[kEntries];
+    static int used = 0, next = 0;
+    static std::mutex m;
+    auto same = [&](const Entry &e) {
+        return e.ptr == ptr && e.dtype == (int)dtype && e.swizzle == (int)swizzle &&
+               e.dims[0] == dims[0] && e.dims[1] == dims[1] && e.dims[2] == dims[2] &&
+               e.strides[0] == strides[0] && e.strides[1] == strides[1] && e.box[0] == box[0] &&
+               e.box[1] == box[1] && e.box[2] == box[2];
+    };
+    {
+        std::lock_guard<std::mutex> lock(m);
+        for (int i = 0; i < used; ++i)
+            if (same(cache[i])) {
+                *map = cache[i].map;
+                return FA_OK;
+            }
+    }
+    auto enc = encode_tiled();
+    if (!enc) return FA_ERR_CUDA;
+    cuuint64_t d3[3] = {dims[0], dims[1], dims[2]};
+    cuuint64_t s2[2] = {strides[0], strides[1]};
+    cuuint32_t b3[3] = {box[0], box[1], box[2]};
+    cuuint32_t elem_strides[3] = {1, 1, 1};
+    CUresult r = enc(map, dtype, 3, const_cast<void *>(ptr), d3, s2, b3, elem_strides,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return FA_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(m);
+    Entry &e = cache[next];
+    e.ptr = ptr;
+    e.dtype = (int)dtype;
+    e.swizzle = (int)swizzle;
+    for (int i = 0; i < 3; ++i) e.dims[i] = dims[i], e.box[i] = box[i];
+    for (int i = 0; i < 2; ++i) e.strides[i] = strides[i];
+    e.map = *map;
+    next = (next + 1) % kEntries;
+    if (used < kEntries) ++used;
+    return FA_OK;
+}
+
 // 3-D map over a contiguous bf16 [BH][N][d] tensor: x = column within the head
 // dimension, y = row, z = (batch, head).  Boxes are 64 columns (128 bytes, one
 // swizzle span) by `box_rows` rows; rows past N read as zeros.
 int make_bhnd_map(CUtensorMap *map, const void *ptr, int BH, int N, int d, int box_rows) {
-    auto enc = encode_tiled();
-    if (!enc) return FA_ERR_CUDA;
-    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
-    cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)N * (cuuint64_t)d * 2};
-    cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
-    cuuint32_t elem_strides[3] = {1, 1, 1};
-    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims,
-                     strides, box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
+    const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
+    const cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)N * (cuuint64_t)d * 2};
+    const cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
+    return encode_3d(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, ptr, dims, strides, box,
+                     CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 // 3-D map over a packed token-major bf16 [T][heads][d] tensor: x = column, y = head,
 // z = token.  A box of 64 columns x 1 head x `box_rows` tokens lands in shared
 // memory as [box_rows][64], like a box of make_bhnd_map; tokens past T read as zeros.
 int make_thd_map(CUtensorMap *map, const void *ptr, int T, int heads, int d, int box_rows) {
-    auto enc = encode_tiled();
-    if (!enc) return FA_ERR_CUDA;
-    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)heads, (cuuint64_t)T};
-    cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)heads * (cuuint64_t)d * 2};
-    cuuint32_t box[3] = {64, 1, (cuuint32_t)box_rows};
-    cuuint32_t elem_strides[3] = {1, 1, 1};
-    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims,
-                     strides, box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
+    const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)heads, (cuuint64_t)T};
+    const cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)heads * (cuuint64_t)d * 2};
+    const cuuint32_t box[3] = {64, 1, (cuuint32_t)box_rows};
+    return encode_3d(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, ptr, dims, strides, box,
+                     CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 // 3-D map over a contiguous fp32 tensor (the dQ output) for tiled bulk adds,
@@ -101,16 +145,11 @@ int make_thd_map(CUtensorMap *map, const void *ptr, int T, int heads, int d, int
 // memory.  Fixed layout [BH][N][d]: (d, N, BH), box (32, 32, 1); packed
 // token-major [T][heads][d]: (d, heads, T), box (32, 1, 32).
 int make_f32_map(CUtensorMap *map, const void *ptr, int d, int n1, int n2, int box1, int box2) {
-    auto enc = encode_tiled();
-    if (!enc) return FA_ERR_CUDA;
-    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)n1, (cuuint64_t)n2};
-    cuuint64_t strides[2] = {(cuuint64_t)d * 4, (cuuint64_t)n1 * (cuuint64_t)d * 4};
-    cuuint32_t box[3] = {32, (cuuint32_t)box1, (cuuint32_t)box2};
-    cuuint32_t elem_strides[3] = {1, 1, 1};
-    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void *>(ptr), dims, strides, box,
-                     elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
+    const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)n1, (cuuint64_t)n2};
+    const cuuint64_t strides[2] = {(cuuint64_t)d * 4, (cuuint64_t)n1 * (cuuint64_t)d * 4};
+    const cuuint32_t box[3] = {32, (cuuint32_t)box1, (cuuint32_t)box2};
+    return encode_3d(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, ptr, dims, strides, box,
+                     CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
 // 3-D map over bytes (e4m3 codes): dims x (innermost), y, z with the given row and
@@ -118,16 +157,11 @@ int make_f32_map(CUtensorMap *map, const void *ptr, int d, int n1, int n2, int b
 // box_y by 1; elements past the dims read as zeros.
 int make_u8_map(CUtensorMap *map, const void *ptr, uint64_t nx, uint64_t ny, uint64_t nz,
                 uint64_t pitch_y, uint64_t pitch_z, uint32_t box_x, uint32_t box_y) {
-    auto enc = encode_tiled();
-    if (!enc) return FA_ERR_CUDA;
-    cuuint64_t dims[3] = {(cuuint64_t)nx, (cuuint64_t)ny, (cuuint64_t)nz};
-    cuuint64_t strides[2] = {(cuuint64_t)pitch_y, (cuuint64_t)pitch_z};
-    cuuint32_t box[3] = {box_x, box_y, 1};
-    cuuint32_t elem_strides[3] = {1, 1, 1};
-    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(ptr), dims, strides,
-                     box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
+    const cuuint64_t dims[3] = {(cuuint64_t)nx, (cuuint64_t)ny, (cuuint64_t)nz};
+    const cuuint64_t strides[2] = {(cuuint64_t)pitch_y, (cuuint64_t)pitch_z};
+    const cuuint32_t box[3] = {box_x, box_y, 1};
+    return encode_3d(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, ptr, dims, strides, box,
+                     CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -613,8 +647,8 @@ int check_decode_sizes(int B, int H, int Hkv, int Nq, int Nk, int d) {
 // times (four stages of fill and merge per CTA), and each range keeps at least
 // eight stages so the ring has something to overlap.  BHkv key/value heads, R
 // query rows per key/value head.
-void decode_split(long long BHkv, int R, int Nk, int d, bool paged, int requested, int num_sms,
-                  int *S, int *keys_per_split) {
+void decode_split_uncached(long long BHkv, int R, int Nk, int d, bool paged, int requested,
+                           int num_sms, int *S, int *keys_per_split) {
     const long long bk = decode_block_keys(d, R, paged);
     const long long tiles = (Nk + bk - 1) / bk;
     const long long qb = decode_query_block(d, R, paged);
@@ -649,6 +683,36 @@ void decode_split(long long BHkv, int R, int Nk, int d, bool paged, int requeste
     const long long per = ((tiles + s - 1) / s) * bk;
     *keys_per_split = (int)per;
     *S = (int)((Nk + per - 1) / per);
+}
+
+// The same, remembered for the last shapes asked (a decode loop repeats one shape).
+void decode_split(long long BHkv, int R, int Nk, int d, bool paged, int requested, int num_sms,
+                  int *S, int *keys_per_split) {
+    struct Entry {
+        long long BHkv;
+        int R, Nk, d, paged, requested, num_sms, S, per;
+    };
+    constexpr int kEntries = 16;
+    static Entry cache[kEntries];
+    static int used = 0, next = 0;
+    static std::mutex m;
+    {
+        std::lock_guard<std::mutex> lock(m);
+        for (int i = 0; i < used; ++i) {
+            const Entry &e = cache[i];
+            if (e.BHkv == BHkv && e.R == R && e.Nk == Nk && e.d == d && e.paged == (int)paged &&
+                e.requested == requested && e.num_sms == num_sms) {
+                *S = e.S;
+                *keys_per_split = e.per;
+                return;
+            }
+        }
+    }
+    decode_split_uncached(BHkv, R, Nk, d, paged, requested, num_sms, S, keys_per_split);
+    std::lock_guard<std::mutex> lock(m);
+    cache[next] = Entry{BHkv, R, Nk, d, (int)paged, requested, num_sms, *S, *keys_per_split};
+    next = (next + 1) % kEntries;
+    if (used < kEntries) ++used;
 }
 
 size_t decode_ws_bytes(long long rows, int S, int d) {  // rows = B * H * Nq

@@ -6,6 +6,7 @@ There is no CPU path; a missing library or a non-CUDA tensor raises.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import math
 import os
@@ -287,33 +288,65 @@ def fa_device_status(stream=None) -> int:
 
 def _check(name, t, dtype, shape=None, dev=None):
     """Argument checks before any launch: a contiguous CUDA tensor of `dtype` (and
-    `shape`) on device `dev`, the first tensor's device: the kernels dereference every
-    pointer on that one GPU."""
-    if not isinstance(t, torch.Tensor) or t.device.type != "cuda":
+    `shape`) on device `dev` (a torch.device or an ordinal), the first tensor's device:
+    the kernels dereference every pointer on that one GPU."""
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor")
-    if dev is not None and t.device != dev:
+    if dev is not None and t.get_device() != (dev if isinstance(dev, int) else dev.index):
         raise ValueError(f"{name} is on {t.device}, the call's first tensor on {dev}")
-    if t.dtype != dtype:
+    if t.dtype is not dtype:
         raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
-    if shape is not None and tuple(t.shape) != tuple(shape):
+    if shape is not None and t.shape != shape:
         raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+
+
+# The current stream's handle: torch's raw getter where it has one (a plain integer,
+# no Stream object is built), else the public call.
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
 
 
 def _stream(t, stream):
     if stream is None:
+        if _raw_stream is not None:
+            return _raw_stream(t.get_device())
         return torch.cuda.current_stream(t.device).cuda_stream
     return stream.cuda_stream if isinstance(stream, torch.cuda.Stream) else int(stream)
+
+
+_SAME_DEVICE = contextlib.nullcontext()
+
+
+def _device(index: int):
+    """The device context for a call on GPU `index`: a no-op when it is already
+    current (the common case), else torch.cuda.device(index)."""
+    return _SAME_DEVICE if torch.cuda.current_device() == index else torch.cuda.device(index)
+
+
+_SIZE_MEMO: dict = {}
+
+
+def _memo(fn, *args):
+    """fn(*args) for the workspace-size queries, remembered per argument tuple and
+    current device (the answers depend only on them and the device's SM count)."""
+    key = (fn, torch.cuda.current_device(), args)
+    r = _SIZE_MEMO.get(key)
+    if r is None:
+        if len(_SIZE_MEMO) > 4096:
+            _SIZE_MEMO.clear()
+        r = _SIZE_MEMO[key] = fn(*args)
+    return r
 
 
 def _kv_heads(q, k, v):
     """Key/value head count of k, v [B, Hkv, N, d] next to q [B, H, N, d] (Hkv divides H)."""
     B, H, N, d = q.shape
-    _check("k", k, torch.bfloat16, dev=q.device)
+    di = q.get_device()
+    _check("k", k, torch.bfloat16, dev=di)
     if k.dim() != 4 or k.shape[0] != B or k.shape[2] != N or k.shape[3] != d or H % k.shape[1]:
         raise ValueError("k must be [B, Hkv, N, d] with Hkv dividing q's H")
-    _check("v", v, torch.bfloat16, k.shape, dev=q.device)
+    _check("v", v, torch.bfloat16, k.shape, dev=di)
     return k.shape[1]
 
 
@@ -330,16 +363,17 @@ def forward(q, k, v, causal=False, scale=None, out=None, lse=None, stream=None, 
     if q.dim() != 4:
         raise ValueError("q must be [B, H, N, d]")
     B, H, N, d = q.shape
+    di = q.get_device()
     Hkv = _kv_heads(q, k, v)
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
     if out is None:
         out = torch.empty_like(q)
-    _check("out", out, torch.bfloat16, q.shape, dev=q.device)
+    _check("out", out, torch.bfloat16, q.shape, dev=di)
     if lse is None:
         lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
-    _check("lse", lse, torch.float32, (B, H, N), dev=q.device)
-    with torch.cuda.device(q.device):
-        need = fa_fwd_workspace_bytes(B, H, N, d, causal, int(kv_chunk))
+    _check("lse", lse, torch.float32, (B, H, N), dev=di)
+    with _device(di):
+        need = _memo(fa_fwd_workspace_bytes, B, H, N, d, causal, int(kv_chunk))
         if need == 0:
             rc = fa_fwd_gqa(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
                             lse.data_ptr(), B, H, Hkv, N, d, causal, scale, _stream(q, stream))
@@ -399,24 +433,25 @@ def decode(q, k, v, scale=None, num_splits=0, out=None, lse=None, workspace=None
     if q.dim() != 4:
         raise ValueError("q must be [B, H, Nq, d]")
     B, H, Nq, d = q.shape
-    _check("k", k, torch.bfloat16, dev=q.device)
+    di = q.get_device()
+    _check("k", k, torch.bfloat16, dev=di)
     if k.dim() != 4 or k.shape[0] != B or k.shape[3] != d or H % k.shape[1]:
         raise ValueError("k must be [B, Hkv, Nk, d] with q's B and d, Hkv dividing H")
     Hkv, Nk = k.shape[1], k.shape[2]
-    _check("v", v, torch.bfloat16, k.shape, dev=q.device)
+    _check("v", v, torch.bfloat16, k.shape, dev=di)
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
     if out is None:
         out = torch.empty_like(q)
-    _check("out", out, torch.bfloat16, q.shape, dev=q.device)
+    _check("out", out, torch.bfloat16, q.shape, dev=di)
     if lse is None:
         lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
-    _check("lse", lse, torch.float32, (B, H, Nq), dev=q.device)
-    with torch.cuda.device(q.device):
-        need = fa_decode_workspace_bytes(B, H, Hkv, Nq, Nk, d, num_splits)
+    _check("lse", lse, torch.float32, (B, H, Nq), dev=di)
+    with _device(di):
+        need = _memo(fa_decode_workspace_bytes, B, H, Hkv, Nq, Nk, d, num_splits)
         if workspace is None and need > 0:
             workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
         if workspace is not None:
-            _check("workspace", workspace, torch.uint8, dev=q.device)
+            _check("workspace", workspace, torch.uint8, dev=di)
         ws_ptr = workspace.data_ptr() if workspace is not None else None
         ws_len = workspace.numel() if workspace is not None else 0
         rc = fa_decode(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),

@@ -117,6 +117,13 @@ def _on(t, index):
         def device(self):
             return self._reported
 
+        @property
+        def is_cuda(self):
+            return True
+
+        def get_device(self):
+            return self._reported.index
+
     s = t.as_subclass(OnDevice)
     s._reported = torch.device("cuda", index)
     return s
