@@ -289,6 +289,39 @@ def run_backward_only(args):
             "ms": round(ms, 5), "tflops": round(tf, 2)}
 
 
+def run_decode_only(args):
+    """`--only-decode B H Hkv Nq Nk d`: one decode shape (automatic key ranges), W
+    untimed and K timed calls (CUDA events, L2 flushed before each), one JSON line.  A
+    small, self-contained command for a profiler to capture the decode's launches."""
+    import torch
+
+    import exact_attention_26_gb300 as fa
+    from exact_attention_26_gb300.inputs import decode_qkv
+
+    B, H, Hkv, Nq, Nk, d = (int(x) for x in args.only_decode)
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    fa.load()
+    _, k, v = decode_qkv(B, Hkv, 1, Nk, d, seed=0, device=dev)
+    q = torch.randn((B, H, Nq, d), generator=torch.Generator(device=dev).manual_seed(1),
+                    device=dev).to(torch.bfloat16)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, Nq), dtype=torch.float32, device=dev)
+    ws = torch.empty(max(16, fa.fa_decode_workspace_bytes(B, H, Hkv, Nq, Nk, d, 0)),
+                     dtype=torch.uint8, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    ms = _time_call(torch, dev, lambda: fa.decode(q, k, v, out=o, lse=lse, workspace=ws), flush,
+                    iters=args.steps, warm=args.warmup)
+    status = fa.fa_device_status(None)
+    if status != 0:
+        raise RuntimeError(f"device status {fa.fa_status_string(status)}")
+    gbs = decode_bytes(B, H, Nq, Nk, d, Hkv) / (ms * 1e-3) / 1e9
+    return {"only_decode": {"B": B, "H": H, "Hkv": Hkv, "Nq": Nq, "Nk": Nk, "d": d},
+            "kernel": "tcgen05" if fa.fa_decode_uses_tensor_cores(H, Hkv, Nq, d, 0) == 1 else "cuda-core",
+            "splits": fa.fa_decode_num_splits(B, H, Hkv, Nq, Nk, d, 0),
+            "ms": round(ms, 5), "GB/s": round(gbs, 1)}
+
+
 def run_config():
     """The workload's description, the same for both arms of the benchmark."""
     B, H, N, d, causal = (WORKLOAD[k] for k in ("B", "H", "N", "d", "causal"))
@@ -1010,6 +1043,8 @@ def main():
                     help="time one forward shape only (a small case for a profiler)")
     ap.add_argument("--only-backward", nargs=5, metavar=("B", "H", "N", "d", "causal"),
                     help="time one backward shape only (a small case for a profiler)")
+    ap.add_argument("--only-decode", nargs=6, metavar=("B", "H", "Hkv", "Nq", "Nk", "d"),
+                    help="time one decode shape only (a small case for a profiler)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -1026,6 +1061,9 @@ def main():
 
     if args.only_backward:
         print(json.dumps(run_backward_only(args)), flush=True)
+        return
+    if args.only_decode:
+        print(json.dumps(run_decode_only(args)), flush=True)
         return
 
     if args.impl == "reference":

@@ -76,3 +76,9 @@ def test_single_backward_mode():
     r = _run("--only-backward", "1", "2", "1000", "64", "1", "--steps", "3", "--warmup", "3")
     assert r["only_backward"]["N"] == 1000 and r["only_backward"]["d"] == 64
     assert r["ms"] > 0 and r["tflops"] > 0
+
+
+def test_single_decode_mode():
+    r = _run("--only-decode", "1", "8", "2", "1", "3000", "128", "--steps", "3", "--warmup", "3")
+    assert r["only_decode"]["Hkv"] == 2 and r["kernel"] == "tcgen05"
+    assert r["ms"] > 0 and r["GB/s"] > 0 and r["splits"] >= 1
