@@ -36,7 +36,7 @@
 //               (one key per thread, four warpgroups split a block's 128 queries),
 //               written as bf16 to TMEM and dS^T to smem; the dQ read-out; the
 //               final dK/dV epilogue
-//   warp 16     TMA producer: K_j, V_j once; Q_i (with L_i, D_i) and dO_i per ring stage
+//   warp 16     TMA producer: K_j; Q_i (with L_i, D_i) and dO_i per ring stage; V_j after Q_0
 //   warp 17     TMEM allocator; one elected lane issues every MMA and commit
 #include "fa_ptx.cuh"
 
@@ -216,9 +216,9 @@ struct BwdTile {
     static constexpr uint32_t OFF_L2 = OFF_STG + STG_BYTES;
     static constexpr uint32_t OFF_DELTA = OFF_L2 + QS * VEC_BYTES;
     static constexpr uint32_t OFF_BAR = OFF_DELTA + QS * VEC_BYTES;
-    // kv_full, q_full[QS], q_empty[QS], o_full[OS], o_empty[OS], s_full, p_full,
-    // dp_full, ds_full, dq_full, dq_empty, done
-    static constexpr int NBAR = 1 + 2 * QS + 2 * OS + 7;
+    // k_full, q_full[QS], q_empty[QS], o_full[OS], o_empty[OS], s_full, p_full,
+    // dp_full, ds_full, dq_full, dq_empty, done, v_full
+    static constexpr int NBAR = 1 + 2 * QS + 2 * OS + 8;
     static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr uint32_t SMEM_USED = OFF_MISC + 16;
     // The tiles need 1024-byte alignment (128-byte swizzle atoms).  At d = 128 the
@@ -269,7 +269,7 @@ __global__ void __launch_bounds__(640, 1)
     const uint32_t sDS = base + T::OFF_DS;
     const uint32_t sL2 = base + T::OFF_L2, sDelta = base + T::OFF_DELTA;
     const uint32_t bar = base + T::OFF_BAR;
-    const uint32_t bar_kv_full = bar;
+    const uint32_t bar_k_full = bar;
     const uint32_t bar_q_full = bar + 8;               // [QS]
     const uint32_t bar_q_empty = bar_q_full + 8 * QS;  // [QS]
     const uint32_t bar_o_full = bar_q_empty + 8 * QS;  // [OS]
@@ -281,6 +281,7 @@ __global__ void __launch_bounds__(640, 1)
     const uint32_t bar_dq_full = bar_s_full + 32;
     const uint32_t bar_dq_empty = bar_s_full + 40;
     const uint32_t bar_done = bar_s_full + 48;
+    const uint32_t bar_v_full = bar_s_full + 56;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + T::OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(gbase + T::OFF_MISC + 4);
     const float *l2_f = reinterpret_cast<const float *>(gbase + T::OFF_L2);
@@ -345,7 +346,8 @@ __global__ void __launch_bounds__(640, 1)
     // loops below carry (qb, gq) as counters instead of dividing every block.
 
     if (threadIdx.x == 0) {
-        mbar_init(bar_kv_full, 1);
+        mbar_init(bar_k_full, 1);
+        mbar_init(bar_v_full, 1);
         for (int s = 0; s < QS; ++s) {
             mbar_init(bar_q_full + 8 * s, 1);
             mbar_init(bar_q_empty + 8 * s, 1);
@@ -386,16 +388,16 @@ __global__ void __launch_bounds__(640, 1)
         setmaxnreg_dec<T::REG_MISC>();
         // ------------------------------------------------------- TMA producer
         if (lane == 0) {
-            mbar_arrive_expect_tx(bar_kv_full, 2 * T::KV_BYTES);
-            for (int c = 0; c < T::NCH; ++c) {
-                tma_load_3d(sK + c * T::K_CHUNK, &tm_k, bar_kv_full, c * 64, VARLEN ? hk : kv0,
+            // K, then Q(0), then V: S^T(0) needs K and Q(0), and V is first read by
+            // dP^T(0) after it, so the CTA's first product waits for two tiles, not three.
+            mbar_arrive_expect_tx(bar_k_full, T::KV_BYTES);
+            for (int c = 0; c < T::NCH; ++c)
+                tma_load_3d(sK + c * T::K_CHUNK, &tm_k, bar_k_full, c * 64, VARLEN ? hk : kv0,
                             VARLEN ? tok0 + kv0 : kvh);
-                tma_load_3d(sV + c * T::K_CHUNK, &tm_v, bar_kv_full, c * 64, VARLEN ? hk : kv0,
-                            VARLEN ? tok0 + kv0 : kvh);
-            }
             // the -L log2e and -D vectors come from the preprocess kernel
             griddep_wait();
             int issued_q = 0, issued_o = 0;
+            bool v_issued = false;
             for (int it = 0, qb = qb_first, gq = gq_first; it < n_it;
                  ++it, (++qb == n_qit) ? (qb = 0, ++gq) : 0) {
                 const int q0 = (i_start + qb) * BQ;
@@ -416,6 +418,13 @@ __global__ void __launch_bounds__(640, 1)
                 bulk_load(sL2 + qs * T::VEC_BYTES, ws_lse2 + voff, T::VEC_BYTES, fb);
                 bulk_load(sDelta + qs * T::VEC_BYTES, ws_delta + voff, T::VEC_BYTES, fb);
                 ++issued_q;
+                if (!v_issued) {
+                    mbar_arrive_expect_tx(bar_v_full, T::KV_BYTES);
+                    for (int c = 0; c < T::NCH; ++c)
+                        tma_load_3d(sV + c * T::K_CHUNK, &tm_v, bar_v_full, c * 64, VARLEN ? hk : kv0,
+                                    VARLEN ? tok0 + kv0 : kvh);
+                    v_issued = true;
+                }
                 // dO(it): free once dV and dP^T of block it - OS are done
                 const int os = it % OS;
                 if (it >= OS && !mbar_wait<true>(bar_o_empty + 8 * os, ((it / OS) - 1) & 1, g,
@@ -431,7 +440,8 @@ __global__ void __launch_bounds__(640, 1)
                 // every copy this warp started lands before the CTA exits
                 volatile int never = 0;
                 const Guard g2{status, &never, kWaitLimitNs};
-                mbar_wait<true>(bar_kv_full, 0, g2, SITE_BWD_DRAIN);
+                mbar_wait<true>(bar_k_full, 0, g2, SITE_BWD_DRAIN);
+                if (v_issued) mbar_wait<true>(bar_v_full, 0, g2, SITE_BWD_DRAIN);
                 for (int it = (issued_q > QS ? issued_q - QS : 0); it < issued_q; ++it)
                     mbar_wait<true>(bar_q_full + 8 * (it % QS), (it / QS) & 1, g2, SITE_BWD_DRAIN);
                 for (int it = (issued_o > OS ? issued_o - OS : 0); it < issued_o; ++it)
@@ -468,7 +478,7 @@ __global__ void __launch_bounds__(640, 1)
                 mma_ts_elect(tmem + dst, tmem + a_col + 64 * (ks >> 2) + 8 * (ks & 3),
                              desc_add(b, ks * 2048), kIdescAcc, (!first || ks > 0) ? 1u : 0u);
         };
-        bool ok = mbar_wait_warp<true>(bar_kv_full, 0, g, SITE_BWD_MMA_KV) &&
+        bool ok = mbar_wait_warp<true>(bar_k_full, 0, g, SITE_BWD_MMA_KV) &&
                   mbar_wait_warp<true>(bar_q_full, 0, g, SITE_BWD_MMA_Q_FULL);
         tc_fence_after();
         if (ok) {
@@ -478,6 +488,7 @@ __global__ void __launch_bounds__(640, 1)
         for (int it = 0; ok && it < n_it; ++it) {
             const int qs = it % QS, os = it % OS;
             // 1. dP^T(it) into Y once dQ^T(it - 1) has been read out of it
+            if (it == 0 && !(ok = mbar_wait_warp<true>(bar_v_full, 0, g, SITE_BWD_MMA_KV))) break;
             if (!(ok = mbar_wait_warp<true>(bar_o_full + 8 * os, (it / OS) & 1, g, SITE_BWD_MMA_Q_FULL)))
                 break;
             if (it > 0 &&
