@@ -505,8 +505,8 @@ extern "C" int fa_fwd_varlen(const void *q, const void *k, const void *v, void *
 extern "C" size_t fa_bwd_workspace_bytes(int B, int H, int N, int d) {
     if (check_sizes(B, H, N, d, false) != FA_OK) return 0;
     const size_t npad = round_up((size_t)N, kBwdPad);
-    // delta[BH][Npad] and lse2[BH][Npad], fp32 each
-    return 2 * (size_t)B * (size_t)H * npad * sizeof(float);
+    // delta[BH][Npad] and lse2[BH][Npad], fp32 each, and the work-item counter
+    return 2 * (size_t)B * (size_t)H * npad * sizeof(float) + kBwdCounterBytes;
 }
 
 extern "C" int fa_bwd_gqa(const void *q, const void *k, const void *v, const void *o,
@@ -545,6 +545,7 @@ extern "C" int fa_bwd_gqa(const void *q, const void *k, const void *v, const voi
     p.dv = dv;
     p.ws_delta = static_cast<float *>(workspace);
     p.ws_lse2 = p.ws_delta + (size_t)BH * (size_t)npad;
+    p.ws_counter = reinterpret_cast<int *>(p.ws_lse2 + (size_t)BH * (size_t)npad);
     p.N = N;
     p.Npad = npad;
     p.BH = BH;
@@ -601,6 +602,7 @@ extern "C" int fa_bwd_varlen(const void *q, const void *k, const void *v, const 
     p.dv = dv;
     p.ws_delta = static_cast<float *>(workspace);
     p.ws_lse2 = p.ws_delta + (size_t)BH * (size_t)npad;
+    p.ws_counter = reinterpret_cast<int *>(p.ws_lse2 + (size_t)BH * (size_t)npad);
     p.N = max_seqlen;
     p.Npad = npad;
     p.BH = BH;

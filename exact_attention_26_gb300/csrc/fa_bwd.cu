@@ -38,6 +38,8 @@
 //               final dK/dV epilogue
 //   warp 16     TMA producer: K_j; Q_i (with L_i, D_i) and dO_i per ring stage; V_j after Q_0
 //   warp 17     TMEM allocator; one elected lane issues every MMA and commit
+#include <algorithm>
+
 #include "fa_ptx.cuh"
 
 namespace fa {
@@ -54,13 +56,15 @@ __global__ void __launch_bounds__(256)
     fa_bwd_pre_kernel(const __nv_bfloat16 *__restrict__ o, const __nv_bfloat16 *__restrict__ dout,
                       const float *__restrict__ lse, float *__restrict__ delta,
                       float *__restrict__ lse2, float *__restrict__ dq, int N, int Npad, int BH,
-                      int H, const int *__restrict__ cu_seqlens, int total_tokens) {
+                      int H, const int *__restrict__ cu_seqlens, int total_tokens,
+                      int *__restrict__ item_counter) {
     // A warp takes RPW consecutive rows at a time (Npad is a multiple of 128, so they
     // share a head) and issues all their loads before any arithmetic: the kernel is
     // bound by HBM, and one row of O and dO per warp leaves too few bytes in flight.
     constexpr int RPW = 4;
     constexpr int PER = D / 32;  // elements per lane
     griddep_launch_dependents();  // the main kernel may set up while this one runs
+    if (blockIdx.x == 0 && threadIdx.x == 0) *item_counter = 0;  // the main kernel's items
     constexpr int W = PER == 3 ? 3 : PER / 2;  // loaded words: bf16 pairs, or 3 halves at d = 96
     const int lane = threadIdx.x & 31;
     const long long warp0 = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -217,9 +221,10 @@ struct BwdTile {
     static constexpr uint32_t OFF_DELTA = OFF_L2 + QS * VEC_BYTES;
     static constexpr uint32_t OFF_BAR = OFF_DELTA + QS * VEC_BYTES;
     // k_full, q_full[QS], q_empty[QS], o_full[OS], o_empty[OS], s_full, p_full,
-    // dp_full, ds_full, dq_full, dq_empty, done, v_full
-    static constexpr int NBAR = 1 + 2 * QS + 2 * OS + 8;
-    static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
+    // dp_full, ds_full, dq_full, dq_empty, done, v_full, kv_empty, dv_free, dk_free,
+    // stg_free, dq_sync, item[2]
+    static constexpr int NBAR = 1 + 2 * QS + 2 * OS + 15;
+    static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;  // TMEM base, abort flag, item[2]
     static constexpr uint32_t SMEM_USED = OFF_MISC + 16;
     // The tiles need 1024-byte alignment (128-byte swizzle atoms).  At d = 128 the
     // layout leaves no room to align the start by hand: the kernel then requires
@@ -229,9 +234,13 @@ struct BwdTile {
         SMEM_USED + 1024 <= kMaxSmem ? SMEM_USED + 1024 : SMEM_USED;
     static constexpr int THREADS = 640;  // P/dS 0-7, dQ 8-15, TMA 16, MMA 17, 18-19 idle
     // Registers per thread after the warpgroups rebalance (launch: 96 each, a pool
-    // of 5 x 128 x 96): P/dS warpgroups hold 64 fp32 P values per thread.
-    static constexpr int LAUNCH_REGS = 96, REG_PDS = 136, REG_DQ = 80, REG_MISC = 48;
+    // of 5 x 128 x 96): P/dS warpgroups hold 64 fp32 P values per thread.  Chosen by
+    // timing (B8 H16 N2048 d64 causal 0.290 ms vs 0.295 at 136 / 80; B4 H16 N4096
+    // d96 causal 0.569 ms vs 0.581 at 144 / 72).
+    static constexpr int LAUNCH_REGS = 96, REG_PDS = D == 96 ? 136 : 144, REG_DQ = D == 96 ? 80 : 72,
+                         REG_MISC = 48;
     static_assert(2 * REG_PDS + 2 * REG_DQ + REG_MISC <= 5 * LAUNCH_REGS, "register pool");
+    static_assert(REG_PDS % 8 == 0 && REG_DQ % 8 == 0 && REG_MISC % 8 == 0, "register targets");
     static_assert(SMEM_USED <= kMaxSmem, "shared memory budget");
     static_assert(Q_CHUNK % 1024 == 0 && DS_CHUNK % 1024 == 0 && KV_BYTES % 1024 == 0,
                   "swizzle atoms must stay aligned");
@@ -248,7 +257,7 @@ __global__ void __launch_bounds__(640, 1)
                   float *__restrict__ dk, float *__restrict__ dv, int N, int Npad, int BHkv,
                   int H, int group, int head_group, const int *__restrict__ cu_seqlens,
                   int total_tokens, float scale, float scale_log2, int *status,
-                  unsigned long long limit_ns) {
+                  unsigned long long limit_ns, int *__restrict__ item_counter) {
     using T = BwdTile<D>;
     constexpr int BQ = T::BQ, QS = T::QS, OS = T::OS;
     extern __shared__ __align__(1024) uint8_t smem_bwd[];
@@ -282,8 +291,15 @@ __global__ void __launch_bounds__(640, 1)
     const uint32_t bar_dq_empty = bar_s_full + 40;
     const uint32_t bar_done = bar_s_full + 48;
     const uint32_t bar_v_full = bar_s_full + 56;
+    const uint32_t bar_kv_empty = bar_s_full + 64;  // an item's last products are done
+    const uint32_t bar_dv_free = bar_s_full + 72;   // the epilogue has read dV from TMEM
+    const uint32_t bar_dk_free = bar_s_full + 80;   // ... dK
+    const uint32_t bar_stg_free = bar_s_full + 88;  // the epilogue's copies have read the staging
+    const uint32_t bar_dq_sync = bar_s_full + 96;   // the dQ warps' adds have read their tiles
+    const uint32_t bar_item = bar_s_full + 104;     // [2] the next item is published
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + T::OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(gbase + T::OFF_MISC + 4);
+    volatile int *item_slot = reinterpret_cast<volatile int *>(gbase + T::OFF_MISC + 8);  // [2]
     const float *l2_f = reinterpret_cast<const float *>(gbase + T::OFF_L2);
     const float *delta_f = reinterpret_cast<const float *>(gbase + T::OFF_DELTA);
 
@@ -299,55 +315,85 @@ __global__ void __launch_bounds__(640, 1)
     // their query blocks one head after the other.
     // SPLIT (small grids): two consecutive CTAs share a key block, each taking a
     // contiguous half of its query blocks, and add their dK, dV into zeroed outputs.
+    // Work items: key blocks of key/value heads, numbered as the grid used to be.
+    // CTAs walk the key/value heads in groups of head_group (whose Q/dO then stay in
+    // L2 together) and, within a group, the key blocks first: with a causal mask key
+    // block 0 has the most query blocks, so a low item number is a long item.
+    // Without SPLIT the CTAs are persistent (one per SM): CTA c starts with item c and
+    // then takes the next unclaimed item from a counter in global memory (zeroed by
+    // the preprocess kernel), so the CTAs finish together as if the hardware had
+    // scheduled one CTA per item, and the next item's K/V loads and first products
+    // overlap the previous item's dK/dV epilogue instead of a CTA's launch and setup.
+    // The TMA warp claims the items and publishes each in a two-entry ring that every
+    // role reads; all barrier phases are running counts across the items.
+    // SPLIT (small grids): one item per CTA; two consecutive CTAs share a key block,
+    // each taking a contiguous half of its query blocks, and add their dK, dV into
+    // zeroed outputs.
     const int part = SPLIT ? (int)(blockIdx.x & 1u) : 0;
-    const unsigned bid = SPLIT ? blockIdx.x >> 1 : blockIdx.x;
-    int kvh, kv0;
-    if (!(VARLEN || !CAUSAL) || head_group >= BHkv) {
-        kvh = bid % BHkv;
-        kv0 = (bid / BHkv) * T::BN;
-    } else {
-        const int n_kb = (N + T::BN - 1) / T::BN;
-        const int hgrp = (int)bid / (head_group * n_kb);
-        const int hrem = (int)bid % (head_group * n_kb);
-        const int hcnt = min(head_group, BHkv - hgrp * head_group);  // heads in this group
-        kvh = hgrp * head_group + hrem % hcnt;
-        kv0 = (hrem / hcnt) * T::BN;
-    }
-    // Keys and queries of this head: N, or with packed sequences (VARLEN: token-major
-    // q, k, v, o, dO, dq, dk, dv, and N is the maximum length) the sequence's own
-    // length, checked on the device.  A key block past the sequence's end has no work.
-    const int hk = kvh % (H / group);
-    int len = N, tok0 = 0;
-    if constexpr (VARLEN) {
-        const int b = kvh / (H / group);
-        const int a = cu_seqlens[b], e = cu_seqlens[b + 1];
-        if (a < 0 || e < a || e > total_tokens || e - a > N) {
-            if (threadIdx.x == 0 && kv0 == 0 && hk == 0) {
-                atomicCAS(status + 1, 0, SITE_BWD_BAD_SEQ);
-                atomicExch(status, FA_ERR_BAD_INDEX);
-            }
-            len = 0;
+    const int n_kb = (N + T::BN - 1) / T::BN;
+    const int n_items = SPLIT ? 1 : n_kb * BHkv;
+    struct Item {
+        int kvh, kv0, hk, len, tok0;
+        int n_it;             // query blocks of this item (0: no work)
+        int i_start, n_qit;   // first query block; query blocks per query head
+        int qb_first, gq_first, bhq0;
+    };
+    auto decode_item = [&](int bid) -> Item {
+        Item it;
+        if (!(VARLEN || !CAUSAL) || head_group >= BHkv) {
+            it.kvh = bid % BHkv;
+            it.kv0 = (bid / BHkv) * T::BN;
         } else {
-            len = e - a;
-            tok0 = a;
+            const int hgrp = bid / (head_group * n_kb);
+            const int hrem = bid % (head_group * n_kb);
+            const int hcnt = min(head_group, BHkv - hgrp * head_group);  // heads in this group
+            it.kvh = hgrp * head_group + hrem % hcnt;
+            it.kv0 = (hrem / hcnt) * T::BN;
         }
+        // Keys and queries of this head: N, or with packed sequences (VARLEN: token-
+        // major q, k, v, o, dO, dq, dk, dv, and N is the maximum length) the
+        // sequence's own length, checked on the device.  A key block past the
+        // sequence's end has no work.
+        it.hk = it.kvh % (H / group);
+        it.len = N;
+        it.tok0 = 0;
+        if constexpr (VARLEN) {
+            const int b = it.kvh / (H / group);
+            const int a = cu_seqlens[b], e = cu_seqlens[b + 1];
+            if (a < 0 || e < a || e > total_tokens || e - a > N) {
+                // reported once, by the TMA thread that claims the sequence's first item
+                if (threadIdx.x == kTmaWarp * 32 && it.kv0 == 0 && it.hk == 0) {
+                    atomicCAS(status + 1, 0, SITE_BWD_BAD_SEQ);
+                    atomicExch(status, FA_ERR_BAD_INDEX);
+                }
+                it.len = 0;
+            } else {
+                it.len = e - a;
+                it.tok0 = a;
+            }
+        }
+        const int n_qb = (it.len + BQ - 1) / BQ;
+        it.i_start = CAUSAL ? it.kv0 / BQ : 0;
+        it.n_qit = n_qb - it.i_start;
+        const int n_all = it.kv0 < it.len ? group * it.n_qit : 0;
+        const int it0 = part ? n_all / 2 : 0;  // this CTA's blocks: [it0, it0 + n_it)
+        it.n_it = SPLIT ? (part ? n_all - n_all / 2 : n_all / 2) : n_all;
+        it.qb_first = (SPLIT && it.n_qit > 0) ? it0 % it.n_qit : 0;
+        it.gq_first = (SPLIT && it.n_qit > 0) ? it0 / it.n_qit : 0;
+        it.bhq0 = (it.kvh / (H / group)) * H + (it.kvh % (H / group)) * group;
+        // Block i of the item is query block qb = i % n_qit of query head
+        // bhq0 + i / n_qit; the loops below carry (qb, gq) as counters.
+        return it;
+    };
+    if constexpr (SPLIT) {
+        // uniform across the CTA, before any barrier or TMEM use
+        if (decode_item((int)(blockIdx.x >> 1)).n_it == 0) return;
     }
-    if (kv0 >= len) return;  // uniform across the CTA, before any barrier or TMEM use
-    const int n_qb = (len + BQ - 1) / BQ;
-    const int i_start = CAUSAL ? kv0 / BQ : 0;
-    const int n_qit = n_qb - i_start;  // query blocks per query head
-    const int n_all = group * n_qit;
-    const int it0 = part ? n_all / 2 : 0;  // this CTA's blocks: [it0, it0 + n_it)
-    const int n_it = SPLIT ? (part ? n_all - n_all / 2 : n_all / 2) : n_all;
-    if (SPLIT && n_it == 0) return;  // uniform across the CTA, before any barrier or TMEM use
-    const int qb_first = SPLIT ? it0 % n_qit : 0, gq_first = SPLIT ? it0 / n_qit : 0;
-    const int bhq0 = (kvh / (H / group)) * H + (kvh % (H / group)) * group;
-    // Block it is query block qb = it % n_qit of query head bhq0 + it / n_qit; the
-    // loops below carry (qb, gq) as counters instead of dividing every block.
 
     if (threadIdx.x == 0) {
         mbar_init(bar_k_full, 1);
         mbar_init(bar_v_full, 1);
+        mbar_init(bar_kv_empty, 1);
         for (int s = 0; s < QS; ++s) {
             mbar_init(bar_q_full + 8 * s, 1);
             mbar_init(bar_q_empty + 8 * s, 1);
@@ -363,6 +409,12 @@ __global__ void __launch_bounds__(640, 1)
         mbar_init(bar_dq_full, 1);
         mbar_init(bar_dq_empty, 256);
         mbar_init(bar_done, 1);
+        mbar_init(bar_dv_free, 256);
+        mbar_init(bar_dk_free, 256);
+        mbar_init(bar_stg_free, 512);
+        mbar_init(bar_dq_sync, 256);
+        mbar_init(bar_item, 1);
+        mbar_init(bar_item + 8, 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -382,70 +434,112 @@ __global__ void __launch_bounds__(640, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const Guard g{status, abort_flag, limit_ns};
+    // Item ri of this CTA (a running count): its number, or -1 after the last.  The
+    // entry of ri - 2 is free when the TMA warp overwrites it: every role has begun
+    // item ri - 1 by then (the TMA warp waited for the end of ri - 2's products and
+    // epilogue before loading ri - 1).
+    auto next_item = [&](int ri, int &w) -> bool {
+        if (!mbar_wait_warp<true>(bar_item + 8 * (ri & 1), (ri >> 1) & 1, g, SITE_BWD_ITEM)) return false;
+        w = item_slot[ri & 1];
+        return true;
+    };
     // Each role rebalances its registers first thing in its own branch, so that the
     // compiler allocates the role's code within that role's budget.
     if (warp == kTmaWarp) {
         setmaxnreg_dec<T::REG_MISC>();
         // ------------------------------------------------------- TMA producer
         if (lane == 0) {
-            // K, then Q(0), then V: S^T(0) needs K and Q(0), and V is first read by
-            // dP^T(0) after it, so the CTA's first product waits for two tiles, not three.
-            mbar_arrive_expect_tx(bar_k_full, T::KV_BYTES);
-            for (int c = 0; c < T::NCH; ++c)
-                tma_load_3d(sK + c * T::K_CHUNK, &tm_k, bar_k_full, c * 64, VARLEN ? hk : kv0,
-                            VARLEN ? tok0 + kv0 : kvh);
-            // the -L log2e and -D vectors come from the preprocess kernel
-            griddep_wait();
-            int issued_q = 0, issued_o = 0;
-            bool v_issued = false;
-            for (int it = 0, qb = qb_first, gq = gq_first; it < n_it;
-                 ++it, (++qb == n_qit) ? (qb = 0, ++gq) : 0) {
-                const int q0 = (i_start + qb) * BQ;
-                const int yq = VARLEN ? (bhq0 + gq) % H : q0;
-                const int zq = VARLEN ? tok0 + q0 : bhq0 + gq;
-                // Q(it) goes first: S^T(it) is issued a block ahead of dP^T(it) and
-                // dV(it), the products of dO(it).
-                // Q(it) with its -L log2e and -D: free once dK of block it - QS is done
-                const int qs = it % QS;
-                if (it >= QS && !mbar_wait<true>(bar_q_empty + 8 * qs, ((it / QS) - 1) & 1, g,
-                                           SITE_BWD_LOAD_EMPTY))
-                    break;
-                const uint32_t fb = bar_q_full + 8 * qs;
-                mbar_arrive_expect_tx(fb, T::Q_BYTES + 2 * T::VEC_BYTES);
-                for (int c = 0; c < T::NCH; ++c)
-                    tma_load_3d(sQ + qs * T::Q_BYTES + c * T::Q_CHUNK, &tm_q, fb, c * 64, yq, zq);
-                const size_t voff = (size_t)(bhq0 + gq) * Npad + q0;
-                bulk_load(sL2 + qs * T::VEC_BYTES, ws_lse2 + voff, T::VEC_BYTES, fb);
-                bulk_load(sDelta + qs * T::VEC_BYTES, ws_delta + voff, T::VEC_BYTES, fb);
-                ++issued_q;
-                if (!v_issued) {
-                    mbar_arrive_expect_tx(bar_v_full, T::KV_BYTES);
-                    for (int c = 0; c < T::NCH; ++c)
-                        tma_load_3d(sV + c * T::K_CHUNK, &tm_v, bar_v_full, c * 64, VARLEN ? hk : kv0,
-                                    VARLEN ? tok0 + kv0 : kvh);
-                    v_issued = true;
+            int issued_q = 0, issued_o = 0;  // running over the CTA's items
+            int n_k = 0, n_v = 0;            // items whose K, V were issued
+            bool ok = true;
+            // The CTA's next item with work (-1: none left).
+            auto claim = [&](int ri) -> int {
+                if constexpr (SPLIT) return ri == 0 ? (int)(blockIdx.x >> 1) : -1;
+                int w = ri == 0 ? (int)blockIdx.x : -1;
+                for (;;) {
+                    if (w < 0) {
+                        griddep_wait();  // the counter is zeroed by the preprocess kernel
+                        w = (int)gridDim.x + atomicAdd(item_counter, 1);
+                    }
+                    if (w >= n_items) return -1;
+                    if (decode_item(w).n_it > 0) return w;
+                    w = -1;
                 }
-                // dO(it): free once dV and dP^T of block it - OS are done
-                const int os = it % OS;
-                if (it >= OS && !mbar_wait<true>(bar_o_empty + 8 * os, ((it / OS) - 1) & 1, g,
-                                           SITE_BWD_LOAD_EMPTY))
+            };
+            for (int ri = 0; ok; ) {
+                const int w = claim(ri);
+                item_slot[ri & 1] = w;
+                mbar_arrive(bar_item + 8 * (ri & 1));
+                if (w < 0) break;
+                const Item itm = decode_item(w);
+                // K, then Q(0), then V: S^T(0) needs K and Q(0), and V is first read by
+                // dP^T(0) after it, so an item's first product waits for two tiles.  K and V
+                // of the previous item are free once its last dQ^T is done.
+                if (ri > 0 && !(ok = mbar_wait<true>(bar_kv_empty, (ri - 1) & 1, g, SITE_BWD_LOAD_EMPTY)))
                     break;
-                mbar_arrive_expect_tx(bar_o_full + 8 * os, T::Q_BYTES);
+                mbar_arrive_expect_tx(bar_k_full, T::KV_BYTES);
                 for (int c = 0; c < T::NCH; ++c)
-                    tma_load_3d(sDO + os * T::Q_BYTES + c * T::Q_CHUNK, &tm_do, bar_o_full + 8 * os,
-                                c * 64, yq, zq);
-                ++issued_o;
+                    tma_load_3d(sK + c * T::K_CHUNK, &tm_k, bar_k_full, c * 64, VARLEN ? itm.hk : itm.kv0,
+                                VARLEN ? itm.tok0 + itm.kv0 : itm.kvh);
+                ++n_k;
+                // the -L log2e and -D vectors come from the preprocess kernel
+                if (ri == 0) griddep_wait();
+                // The Q/dO rings, the dS^T tile and the dQ staging tiles held the previous
+                // item's dK/dV staging until its epilogue's copies read it.
+                if (ri > 0 && !(ok = mbar_wait<true>(bar_stg_free, (ri - 1) & 1, g, SITE_BWD_LOAD_EMPTY)))
+                    break;
+                bool v_issued = false;
+                for (int i = 0, qb = itm.qb_first, gq = itm.gq_first; i < itm.n_it;
+                     ++i, (++qb == itm.n_qit) ? (qb = 0, ++gq) : 0) {
+                    const int q0 = (itm.i_start + qb) * BQ;
+                    const int yq = VARLEN ? (itm.bhq0 + gq) % H : q0;
+                    const int zq = VARLEN ? itm.tok0 + q0 : itm.bhq0 + gq;
+                    // Q(i) goes first: S^T(i) is issued a block ahead of dP^T(i) and dV(i),
+                    // the products of dO(i).
+                    // Q(i) with its -L log2e and -D: free once dK of the block QS before is done
+                    const int gi = issued_q, qs = gi % QS;
+                    if (gi >= QS && !(ok = mbar_wait<true>(bar_q_empty + 8 * qs, ((gi / QS) - 1) & 1, g,
+                                                          SITE_BWD_LOAD_EMPTY)))
+                        break;
+                    const uint32_t fb = bar_q_full + 8 * qs;
+                    mbar_arrive_expect_tx(fb, T::Q_BYTES + 2 * T::VEC_BYTES);
+                    for (int c = 0; c < T::NCH; ++c)
+                        tma_load_3d(sQ + qs * T::Q_BYTES + c * T::Q_CHUNK, &tm_q, fb, c * 64, yq, zq);
+                    const size_t voff = (size_t)(itm.bhq0 + gq) * Npad + q0;
+                    bulk_load(sL2 + qs * T::VEC_BYTES, ws_lse2 + voff, T::VEC_BYTES, fb);
+                    bulk_load(sDelta + qs * T::VEC_BYTES, ws_delta + voff, T::VEC_BYTES, fb);
+                    ++issued_q;
+                    if (!v_issued) {
+                        mbar_arrive_expect_tx(bar_v_full, T::KV_BYTES);
+                        for (int c = 0; c < T::NCH; ++c)
+                            tma_load_3d(sV + c * T::K_CHUNK, &tm_v, bar_v_full, c * 64,
+                                        VARLEN ? itm.hk : itm.kv0, VARLEN ? itm.tok0 + itm.kv0 : itm.kvh);
+                        v_issued = true;
+                        ++n_v;
+                    }
+                    // dO(i): free once dV and dP^T of the block OS before are done
+                    const int go = issued_o, os = go % OS;
+                    if (go >= OS && !(ok = mbar_wait<true>(bar_o_empty + 8 * os, ((go / OS) - 1) & 1, g,
+                                                          SITE_BWD_LOAD_EMPTY)))
+                        break;
+                    mbar_arrive_expect_tx(bar_o_full + 8 * os, T::Q_BYTES);
+                    for (int c = 0; c < T::NCH; ++c)
+                        tma_load_3d(sDO + os * T::Q_BYTES + c * T::Q_CHUNK, &tm_do, bar_o_full + 8 * os,
+                                    c * 64, yq, zq);
+                    ++issued_o;
+                }
+                ++ri;
             }
             if (*abort_flag) {
                 // every copy this warp started lands before the CTA exits
                 volatile int never = 0;
                 const Guard g2{status, &never, kWaitLimitNs};
-                mbar_wait<true>(bar_k_full, 0, g2, SITE_BWD_DRAIN);
-                if (v_issued) mbar_wait<true>(bar_v_full, 0, g2, SITE_BWD_DRAIN);
-                for (int it = (issued_q > QS ? issued_q - QS : 0); it < issued_q; ++it)
-                    mbar_wait<true>(bar_q_full + 8 * (it % QS), (it / QS) & 1, g2, SITE_BWD_DRAIN);
-                for (int it = (issued_o > OS ? issued_o - OS : 0); it < issued_o; ++it)
-                    mbar_wait<true>(bar_o_full + 8 * (it % OS), (it / OS) & 1, g2, SITE_BWD_DRAIN);
+                if (n_k > 0) mbar_wait<true>(bar_k_full, (n_k - 1) & 1, g2, SITE_BWD_DRAIN);
+                if (n_v > 0) mbar_wait<true>(bar_v_full, (n_v - 1) & 1, g2, SITE_BWD_DRAIN);
+                for (int i = (issued_q > QS ? issued_q - QS : 0); i < issued_q; ++i)
+                    mbar_wait<true>(bar_q_full + 8 * (i % QS), (i / QS) & 1, g2, SITE_BWD_DRAIN);
+                for (int i = (issued_o > OS ? issued_o - OS : 0); i < issued_o; ++i)
+                    mbar_wait<true>(bar_o_full + 8 * (i % OS), (i / OS) & 1, g2, SITE_BWD_DRAIN);
             }
         }
     } else if (warp == kMmaWarp) {
@@ -478,51 +572,70 @@ __global__ void __launch_bounds__(640, 1)
                 mma_ts_elect(tmem + dst, tmem + a_col + 64 * (ks >> 2) + 8 * (ks & 3),
                              desc_add(b, ks * 2048), kIdescAcc, (!first || ks > 0) ? 1u : 0u);
         };
-        bool ok = mbar_wait_warp<true>(bar_k_full, 0, g, SITE_BWD_MMA_KV) &&
-                  mbar_wait_warp<true>(bar_q_full, 0, g, SITE_BWD_MMA_Q_FULL);
-        tc_fence_after();
-        if (ok) {
-            issue_t(T::TM_X, dK_k, sQ);
+        bool ok = true;
+        int gb = 0;  // blocks of the CTA's earlier items
+        for (int ri = 0; ok;) {
+            int w = -1;
+            if (!(ok = next_item(ri, w)) || w < 0) break;
+            const Item itm = decode_item(w);
+            const int n_it = itm.n_it;
+            ok = mbar_wait_warp<true>(bar_k_full, ri & 1, g, SITE_BWD_MMA_KV) &&
+                 mbar_wait_warp<true>(bar_q_full + 8 * (gb % QS), (gb / QS) & 1, g, SITE_BWD_MMA_Q_FULL);
+            tc_fence_after();
+            if (!ok) break;
+            issue_t(T::TM_X, dK_k, sQ + (gb % QS) * T::Q_BYTES);
             tc_commit_elect(bar_s_full);
-        }
-        for (int it = 0; ok && it < n_it; ++it) {
-            const int qs = it % QS, os = it % OS;
-            // 1. dP^T(it) into Y once dQ^T(it - 1) has been read out of it
-            if (it == 0 && !(ok = mbar_wait_warp<true>(bar_v_full, 0, g, SITE_BWD_MMA_KV))) break;
-            if (!(ok = mbar_wait_warp<true>(bar_o_full + 8 * os, (it / OS) & 1, g, SITE_BWD_MMA_Q_FULL)))
-                break;
-            if (it > 0 &&
-                !(ok = mbar_wait_warp<true>(bar_dq_empty, (it - 1) & 1, g, SITE_BWD_MMA_DQ_FREE)))
-                break;
-            tc_fence_after();
-            issue_t(T::TM_Y, dV_k, sDO + os * T::Q_BYTES);
-            tc_commit_elect(bar_dp_full);
-            // 2. dV += P^T(it) dO(it); dO(it) is then done with.
-            if (!(ok = mbar_wait_warp<true>(bar_p_full, it & 1, g, SITE_BWD_MMA_DS_FULL))) break;
-            tc_fence_after();
-            issue_acc(T::TM_DV, T::TM_X, sDO + os * T::Q_BYTES, it == 0);
-            tc_commit_elect(bar_o_empty + 8 * os);
-            // 3. S^T(it + 1) into X (P^T(it) is read by dV(it), issued before)
-            if (it + 1 < n_it) {
-                const int qn = (it + 1) % QS;
-                if (!(ok = mbar_wait_warp<true>(bar_q_full + 8 * qn, ((it + 1) / QS) & 1, g,
-                                          SITE_BWD_MMA_Q_FULL)))
+            for (int i = 0; ok && i < n_it; ++i) {
+                const int it = gb + i;  // the block's running index
+                const int qs = it % QS, os = it % OS;
+                // 1. dP^T(it) into Y once dQ^T(it - 1) has been read out of it
+                if (i == 0 && !(ok = mbar_wait_warp<true>(bar_v_full, ri & 1, g, SITE_BWD_MMA_KV))) break;
+                if (!(ok = mbar_wait_warp<true>(bar_o_full + 8 * os, (it / OS) & 1, g, SITE_BWD_MMA_Q_FULL)))
+                    break;
+                if (it > 0 &&
+                    !(ok = mbar_wait_warp<true>(bar_dq_empty, (it - 1) & 1, g, SITE_BWD_MMA_DQ_FREE)))
                     break;
                 tc_fence_after();
-                issue_t(T::TM_X, dK_k, sQ + qn * T::Q_BYTES);
-                tc_commit_elect(bar_s_full);
-            }
-            // 4. dK += dS^T(it) Q(it); Q(it) and its vectors are then done with.
-            if (!(ok = mbar_wait_warp<true>(bar_ds_full, it & 1, g, SITE_BWD_MMA_DS_FULL))) break;
-            tc_fence_after();
-            issue_acc(T::TM_DK, T::TM_Y, sQ + qs * T::Q_BYTES, it == 0);
-            tc_commit_elect(bar_q_empty + 8 * qs);
-            // 5. dQ^T(it)[d][q] = sum_k K[k][d] dS^T[k][q] into Y (K = 128 keys, 16 per step)
+                issue_t(T::TM_Y, dV_k, sDO + os * T::Q_BYTES);
+                tc_commit_elect(bar_dp_full);
+                // 2. dV += P^T(it) dO(it); dO(it) is then done with.  The item's first dV
+                //    overwrites the accumulator once the previous item's epilogue read it.
+                if (!(ok = mbar_wait_warp<true>(bar_p_full, it & 1, g, SITE_BWD_MMA_DS_FULL))) break;
+                if (i == 0 && ri > 0 &&
+                    !(ok = mbar_wait_warp<true>(bar_dv_free, (ri - 1) & 1, g, SITE_BWD_MMA_DS_FULL)))
+                    break;
+                tc_fence_after();
+                issue_acc(T::TM_DV, T::TM_X, sDO + os * T::Q_BYTES, i == 0);
+                tc_commit_elect(bar_o_empty + 8 * os);
+                // 3. S^T(it + 1) into X (P^T(it) is read by dV(it), issued before)
+                if (i + 1 < n_it) {
+                    const int qn = (it + 1) % QS;
+                    if (!(ok = mbar_wait_warp<true>(bar_q_full + 8 * qn, ((it + 1) / QS) & 1, g,
+                                                    SITE_BWD_MMA_Q_FULL)))
+                        break;
+                    tc_fence_after();
+                    issue_t(T::TM_X, dK_k, sQ + qn * T::Q_BYTES);
+                    tc_commit_elect(bar_s_full);
+                }
+                // 4. dK += dS^T(it) Q(it); Q(it) and its vectors are then done with.
+                if (!(ok = mbar_wait_warp<true>(bar_ds_full, it & 1, g, SITE_BWD_MMA_DS_FULL))) break;
+                if (i == 0 && ri > 0 &&
+                    !(ok = mbar_wait_warp<true>(bar_dk_free, (ri - 1) & 1, g, SITE_BWD_MMA_DS_FULL)))
+                    break;
+                tc_fence_after();
+                issue_acc(T::TM_DK, T::TM_Y, sQ + qs * T::Q_BYTES, i == 0);
+                tc_commit_elect(bar_q_empty + 8 * qs);
+                // 5. dQ^T(it)[d][q] = sum_k K[k][d] dS^T[k][q] into Y (K = 128 keys, 16 per step)
 #pragma unroll
-            for (int ks = 0; ks < T::BN / 16; ++ks)
-                mma_ss_elect(tmem + T::TM_Y, desc_add(dK_mn, ks * 2048), desc_add(dDS, ks * 2048),
-                             kIdescDQ, ks > 0 ? 1u : 0u);
-            tc_commit_elect(bar_dq_full);
+                for (int ks = 0; ks < T::BN / 16; ++ks)
+                    mma_ss_elect(tmem + T::TM_Y, desc_add(dK_mn, ks * 2048), desc_add(dDS, ks * 2048),
+                                 kIdescDQ, ks > 0 ? 1u : 0u);
+                tc_commit_elect(bar_dq_full);
+            }
+            // K and V are free for the next item once this item's products are done
+            if (ok) tc_commit_elect(bar_kv_empty);
+            gb += n_it;
+            ++ri;
         }
         tc_commit_elect(bar_done);
         volatile int never = 0;
@@ -536,61 +649,67 @@ __global__ void __launch_bounds__(640, 1)
         // query columns [64h, 64h + 64) of every block (h = wg): P = exp2(S^T scale
         // log2e - L log2e) into X, dS = P o (dP - D) into Y and into shared memory.
         // 2-3 read dQ^T columns [64h, 64h + 64) (h = wg - 2) out of Y and add them
-        // into global dQ.
+        // into global dQ.  At the end of an item, 0-1 write dV and 2-3 dK.
         const int wg = warp >> 2;
         const int h = wg & 1;
         const int qt = warp & 3;          // TMEM lane quarter
         const int r = threadIdx.x & 127;  // key row within the block
         const uint32_t lane_base = (uint32_t)(qt * 32) << 16;
-        const int key = kv0 + r;
         bool ok = true;
         // ------------------------------------------------------- dK, dV epilogue
-        auto epilogue = [&]() {
-            // Every product is done: dK and dV are final.  Warpgroups 0-1 take dV, 2-3
-            // dK (times scale); each thread owns half a key row (d columns
+        auto epilogue = [&](const Item &itm) {
+            // Every product of the item is done: dK and dV are final.  Warpgroups 0-1
+            // take dV, 2-3 dK (times scale); each thread owns half a key row (d columns
             // [64h, min(64h + 64, D))).  Rows are staged in shared memory at a 528-byte
-            // pitch (16-byte writes without bank conflicts; the Q/dO rings and the dS^T
-            // tile are idle once every MMA is done) and leave with one bulk copy per
-            // half-row, so global writes are 256 contiguous bytes.
-            if (ok) {
-                const int pass = wg >> 1;  // 0: dV, 1: dK
-                constexpr uint32_t kPitch = T::DP * 4 + 16;  // 16-byte units shift by one per row
-                static_assert(2 * 128 * kPitch <= T::OFF_L2 - T::OFF_Q, "epilogue staging fits");
-                const uint32_t soff = T::OFF_Q + (pass * 128 + r) * kPitch + 256 * h;
-                uint8_t *stg = gbase + soff;
-                const uint32_t tcol = (pass == 0 ? T::TM_DV : T::TM_DK) + 64 * h;
-                const float mul = pass == 0 ? 1.f : scale;
-                constexpr int kHalf1 = (D - 64) / 32;  // 32-column loads of the second half
+            // pitch (16-byte writes without bank conflicts; the Q/dO rings, the dS^T tile
+            // and the dQ staging tiles are idle once every product of the item is done;
+            // the next item's loads into them wait on stg_free) and leave with one bulk
+            // copy per half-row, so global writes are 256 contiguous bytes.  The
+            // accumulator is free for the next item's first product once it is read.
+            const int pass = wg >> 1;  // 0: dV, 1: dK
+            constexpr uint32_t kPitch = T::DP * 4 + 16;  // 16-byte units shift by one per row
+            static_assert(2 * 128 * kPitch <= T::OFF_L2 - T::OFF_Q, "epilogue staging fits");
+            const uint32_t soff = T::OFF_Q + (pass * 128 + r) * kPitch + 256 * h;
+            uint8_t *stg = gbase + soff;
+            const uint32_t tcol = (pass == 0 ? T::TM_DV : T::TM_DK) + 64 * h;
+            const float mul = pass == 0 ? 1.f : scale;
+            constexpr int kHalf1 = (D - 64) / 32;  // 32-column loads of the second half
 #pragma unroll
-                for (int c = 0; c < 2; ++c) {
-                    if (h == 1 && c >= kHalf1) break;
-                    uint32_t a[32];
-                    tmem_ld32(tmem + lane_base + tcol + 32 * c, a);
-                    tmem_wait_ld(a);
+            for (int c = 0; c < 2; ++c) {
+                if (h == 1 && c >= kHalf1) break;
+                uint32_t a[32];
+                tmem_ld32(tmem + lane_base + tcol + 32 * c, a);
+                tmem_wait_ld(a);
 #pragma unroll
-                    for (int e = 0; e < 32; e += 4)
-                        *reinterpret_cast<float4 *>(stg + (32 * c + e) * 4) = make_float4(
-                            __uint_as_float(a[e]) * mul, __uint_as_float(a[e + 1]) * mul,
-                            __uint_as_float(a[e + 2]) * mul, __uint_as_float(a[e + 3]) * mul);
-                }
-                fence_proxy_async_smem();
-                if (key < len && (h == 0 || D > 64)) {
-                    const size_t krow =
-                        VARLEN ? (size_t)(tok0 + key) * (H / group) + hk : (size_t)kvh * N + key;
-                    float *dstg = (pass == 0 ? dv : dk) + krow * D + 64 * h;
-                    const uint32_t nb = h == 0 ? (uint32_t)min(D, 64) * 4 : (uint32_t)(D - 64) * 4;
-                    if constexpr (SPLIT)
-                        bulk_reduce_add_f32(dstg, base + soff, nb);
-                    else
-                        bulk_store(dstg, base + soff, nb);
-                }
-                bulk_commit_group();
+                for (int e = 0; e < 32; e += 4)
+                    *reinterpret_cast<float4 *>(stg + (32 * c + e) * 4) = make_float4(
+                        __uint_as_float(a[e]) * mul, __uint_as_float(a[e + 1]) * mul,
+                        __uint_as_float(a[e + 2]) * mul, __uint_as_float(a[e + 3]) * mul);
             }
+            tc_fence_before();
+            mbar_arrive(pass == 0 ? bar_dv_free : bar_dk_free);
+            fence_proxy_async_smem();
+            const int key = itm.kv0 + r;
+            if (key < itm.len && (h == 0 || D > 64)) {
+                const size_t krow = VARLEN ? (size_t)(itm.tok0 + key) * (H / group) + itm.hk
+                                           : (size_t)itm.kvh * N + key;
+                float *dstg = (pass == 0 ? dv : dk) + krow * D + 64 * h;
+                const uint32_t nb = h == 0 ? (uint32_t)min(D, 64) * 4 : (uint32_t)(D - 64) * 4;
+                if constexpr (SPLIT)
+                    bulk_reduce_add_f32(dstg, base + soff, nb);
+                else
+                    bulk_store(dstg, base + soff, nb);
+            }
+            bulk_commit_group();
+            // the staging area is free for the next item once every copy has read it
+            bulk_wait_group_read<0>();
+            mbar_arrive(bar_stg_free);
         };
         if (wg < 2) {
             setmaxnreg_inc<T::REG_PDS>();
             const uint64_t c2 = f32x2_splat(scale_log2);
             float p[64];  // P of this thread's 64 queries, kept for dS
+            int key = 0, len = 0, kv0 = 0;  // of the current item
 
             // P(it) from S^T(it) in X, in two 32-column halves.
             auto p_stage = [&](int it, int q0) -> bool {
@@ -679,14 +798,29 @@ __global__ void __launch_bounds__(640, 1)
                 return true;
             };
 
-            ok = p_stage(0, (i_start + qb_first) * BQ);
-            for (int it = 0, qb = qb_first; ok && it < n_it; ++it, (++qb == n_qit) ? (qb = 0) : 0) {
-                ok = ds_stage(it);
-                if (ok && it + 1 < n_it) ok = p_stage(it + 1, (i_start + (qb + 1 == n_qit ? 0 : qb + 1)) * BQ);
+
+            int gb = 0;  // blocks of the CTA's earlier items
+            for (int ri = 0; ok; ++ri) {
+                int w = -1;
+                if (!(ok = next_item(ri, w)) || w < 0) break;
+                const Item itm = decode_item(w);
+                const int n_it = itm.n_it;
+                kv0 = itm.kv0;
+                len = itm.len;
+                key = kv0 + r;
+                ok = p_stage(gb, (itm.i_start + itm.qb_first) * BQ);
+                for (int i = 0, qb = itm.qb_first; ok && i < n_it; ++i, (++qb == itm.n_qit) ? (qb = 0) : 0) {
+                    ok = ds_stage(gb + i);
+                    if (ok && i + 1 < n_it)
+                        ok = p_stage(gb + i + 1, (itm.i_start + (qb + 1 == itm.n_qit ? 0 : qb + 1)) * BQ);
+                }
+                // every product of the item is done once its last dQ^T is
+                ok = ok && mbar_wait_warp<true>(bar_dq_full, (gb + n_it - 1) & 1, g, SITE_BWD_EPILOGUE);
+                if (!ok) break;
+                tc_fence_after();
+                epilogue(itm);
+                gb += n_it;
             }
-            // every product is done once the last dQ^T is
-            ok = ok && mbar_wait_warp<true>(bar_dq_full, (n_it - 1) & 1, g, SITE_BWD_EPILOGUE);
-            if (ok) epilogue();
         } else {
             setmaxnreg_dec<T::REG_DQ>();
             griddep_wait();  // dQ is zeroed by the preprocess kernel before any add below
@@ -697,6 +831,7 @@ __global__ void __launch_bounds__(640, 1)
             // by the copy, or hold exact zeros).
             const uint32_t s_stage = base + T::OFF_STG + (warp - 8) * 4096u;
             float *stage_f = reinterpret_cast<float *>(gbase + T::OFF_STG + (warp - 8) * 4096u);
+            int tok0 = 0;  // of the current item
             auto stage_add = [&](const uint32_t(&x)[32], int row, int head) {
                 if (lane == 0) bulk_wait_group_read<0>();  // the tile's previous add has read it
                 __syncwarp();
@@ -712,28 +847,45 @@ __global__ void __launch_bounds__(640, 1)
                     bulk_commit_group();
                 }
             };
-            for (int it = 0, qb = qb_first, gq = gq_first; it < n_it;
-                 ++it, (++qb == n_qit) ? (qb = 0, ++gq) : 0) {
-                if (!(ok = mbar_wait_warp<true>(bar_dq_full, it & 1, g, SITE_BWD_DQ_FULL))) break;
-                tc_fence_after();
-                uint32_t x0[32], x1[32];
-                tmem_ld32(tmem + lane_base + T::TM_Y + 64 * h, x0);
-                tmem_ld32(tmem + lane_base + T::TM_Y + 64 * h + 32, x1);
-                tmem_wait_ld(x0);
-                tmem_wait_ld(x1);
-                tc_fence_before();
-                mbar_arrive(bar_dq_empty);
-                if (32 * qt >= D) continue;  // rows of dQ^T past d are padding
-                const int row0 = (i_start + qb) * BQ + 64 * h;
-                const int head = VARLEN ? (bhq0 + gq) % H : bhq0 + gq;
-                stage_add(x0, row0, head);
-                stage_add(x1, row0 + 32, head);
+            int gb = 0, ri = 0;  // blocks and items of the CTA's earlier items
+            for (; ok;) {
+                int w = -1;
+                if (!(ok = next_item(ri, w)) || w < 0) break;
+                const Item itm = decode_item(w);
+                const int n_it = itm.n_it;
+                tok0 = itm.tok0;
+                // the staging tiles held part of the previous item's dK/dV staging
+                if (ri > 0 && !(ok = mbar_wait_warp<true>(bar_stg_free, (ri - 1) & 1, g, SITE_BWD_DQ_FULL)))
+                    break;
+                for (int i = 0, qb = itm.qb_first, gq = itm.gq_first; i < n_it;
+                     ++i, (++qb == itm.n_qit) ? (qb = 0, ++gq) : 0) {
+                    const int it = gb + i;
+                    if (!(ok = mbar_wait_warp<true>(bar_dq_full, it & 1, g, SITE_BWD_DQ_FULL))) break;
+                    tc_fence_after();
+                    uint32_t x0[32], x1[32];
+                    tmem_ld32(tmem + lane_base + T::TM_Y + 64 * h, x0);
+                    tmem_ld32(tmem + lane_base + T::TM_Y + 64 * h + 32, x1);
+                    tmem_wait_ld(x0);
+                    tmem_wait_ld(x1);
+                    tc_fence_before();
+                    mbar_arrive(bar_dq_empty);
+                    if (32 * qt >= D) continue;  // rows of dQ^T past d are padding
+                    const int row0 = (itm.i_start + qb) * BQ + 64 * h;
+                    const int head = VARLEN ? (itm.bhq0 + gq) % H : itm.bhq0 + gq;
+                    stage_add(x0, row0, head);
+                    stage_add(x1, row0 + 32, head);
+                }
+                // The staging tiles' reads finish before the dK epilogue reuses the area:
+                // every dQ thread arrives once its warp's adds have read their tile, and
+                // waits for the other 255 (a bounded wait, like every other).
+                if (lane == 0) bulk_wait_group_read<0>();
+                __syncwarp();
+                mbar_arrive(bar_dq_sync);
+                if (!(ok = ok && mbar_wait_warp<true>(bar_dq_sync, ri & 1, g, SITE_BWD_DQ_FULL))) break;
+                epilogue(itm);
+                gb += n_it;
+                ++ri;
             }
-            // The staging tiles' reads finish before the dK epilogue reuses the area.
-            if (lane == 0) bulk_wait_group_read<0>();
-            __syncwarp();
-            named_barrier_sync(1, 256);
-            if (ok) epilogue();
         }
         // The shared-memory reads of this thread's bulk copies and adds finish before
         // the CTA retires; their global writes complete before the kernel does.
@@ -778,7 +930,7 @@ int launch_bwd_t(const BwdParams &p, cudaStream_t stream) {
         fa_bwd_pre_kernel<D, VARLEN><<<(unsigned)blocks, 256, 0, stream>>>(
             reinterpret_cast<const __nv_bfloat16 *>(p.o),
             reinterpret_cast<const __nv_bfloat16 *>(p.dout), p.lse, p.ws_delta, p.ws_lse2, p.dq,
-            p.N, p.Npad, p.BH, p.H, p.cu_seqlens, p.total_tokens);
+            p.N, p.Npad, p.BH, p.H, p.cu_seqlens, p.total_tokens, p.ws_counter);
         if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
     }
 
@@ -801,7 +953,8 @@ int launch_bwd_t(const BwdParams &p, cudaStream_t stream) {
         // up (barriers, tensor memory, K/V loads) while the preprocess finishes, and
         // wait for it only where they read its results.
         cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3((unsigned)grid);
+        // Persistent CTAs (one per SM) over the items, or one CTA per half item (split).
+        cfg.gridDim = dim3((unsigned)(split ? grid : std::min<long long>(grid, p.num_sms)));
         cfg.blockDim = dim3(W::THREADS);
         cfg.dynamicSmemBytes = W::SMEM_BYTES;
         cfg.stream = stream;
@@ -813,7 +966,7 @@ int launch_bwd_t(const BwdParams &p, cudaStream_t stream) {
         if (cudaLaunchKernelEx(&cfg, kern, p.tm_q, p.tm_k, p.tm_v, p.tm_do, p.tm_dq, p.ws_lse2,
                                p.ws_delta, p.dk, p.dv, p.N, p.Npad, p.BH / p.group, p.H,
                                p.group, head_group, p.cu_seqlens, p.total_tokens, p.scale,
-                               p.scale_log2, p.status, p.limit_ns) != cudaSuccess)
+                               p.scale_log2, p.status, p.limit_ns, p.ws_counter) != cudaSuccess)
             return FA_ERR_CUDA;
         return FA_OK;
     };

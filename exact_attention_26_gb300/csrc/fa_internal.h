@@ -39,6 +39,7 @@ enum WaitSite : int {
     SITE_DEC_BAD_LEN = 24,
     SITE_DEC_BAD_PAGE = 25,
     SITE_DEC_MMA = 28,
+    SITE_BWD_ITEM = 29,
     SITE_SELFTEST = 30,
 };
 
@@ -96,6 +97,7 @@ struct BwdParams {
     const float *lse;                     // fp32 [BH][N]
     float *dq, *dk, *dv;                  // fp32 [BH][N][d]
     float *ws_delta, *ws_lse2;            // workspace, [BH][Npad] each
+    int *ws_counter;                      // workspace: the main kernel's next unclaimed item
     int N, Npad, BH, d, causal;
     int H, group;                         // query heads per batch; query heads per k/v head
     const int *cu_seqlens;                // varlen: [B+1] sequence starts (token-major), else null
@@ -108,6 +110,8 @@ struct BwdParams {
 
 // Query rows per backward q-block and the padding unit of the workspace vectors.
 constexpr int kBwdPad = 128;
+// Bytes at the end of the backward workspace for the work-item counter.
+constexpr size_t kBwdCounterBytes = 16;
 
 struct DecodeParams {
     // tensor-core path only: q as [1][BH*Nq][d] (boxes of 128 rows), k and v as

@@ -76,7 +76,8 @@ int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int
 
 /*
  * Bytes of caller-provided device workspace fa_bwd needs for these sizes (the
- * per-row D_i = dO_i . O_i and the base-2 copy of L, padded per head).
+ * per-row D_i = dO_i . O_i and the base-2 copy of L, padded per head, and a
+ * 16-byte counter the kernels use to hand out their work).
  * Returns 0 for invalid sizes.
  */
 size_t fa_bwd_workspace_bytes(int B, int H, int N, int d);

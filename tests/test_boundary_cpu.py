@@ -92,12 +92,12 @@ def test_bwd_rejects_bad_arguments(fa, kw, code):
 
 
 def test_workspace_size(fa):
-    # delta and base-2 lse, fp32, rows padded to 128 per head
-    assert fa.fa_bwd_workspace_bytes(2, 16, 4096, 128) == 2 * 32 * 4096 * 4
-    assert fa.fa_bwd_workspace_bytes(1, 1, 129, 64) == 2 * 256 * 4
+    # delta and base-2 lse, fp32, rows padded to 128 per head, and a 16-byte work counter
+    assert fa.fa_bwd_workspace_bytes(2, 16, 4096, 128) == 2 * 32 * 4096 * 4 + 16
+    assert fa.fa_bwd_workspace_bytes(1, 1, 129, 64) == 2 * 256 * 4 + 16
     assert fa.fa_bwd_workspace_bytes(1, 1, 0, 64) == 0
     assert fa.fa_bwd_workspace_bytes(1, 1, 128, 256) == 0
-    assert fa.fa_bwd_workspace_bytes(1, 2, 100, 96) == 2 * 2 * 128 * 4
+    assert fa.fa_bwd_workspace_bytes(1, 2, 100, 96) == 2 * 2 * 128 * 4 + 16
 
 
 def test_python_wrapper_rejects_cpu_tensors(fa):
