@@ -14,10 +14,13 @@
 //   dQ  = scale dS K,     dK = scale dS^T Q
 //
 // Kernel 1 (fa_bwd_pre_kernel): -D_i and -L_i log2(e), negated so the main kernel
-// adds them (padded rows get 0 and -inf, so their P is exactly 0), and dQ := 0.
+// adds them (padded rows get 0 and -inf, so their P is exactly 0), dQ := 0, and
+// the main kernel's work counter := 0.
 //
-// Kernel 2 (fa_bwd_kernel): one CTA per (batch * key/value head, block of 128
-// keys), looping over blocks of 128 query rows.  All products are tcgen05 MMAs
+// Kernel 2 (fa_bwd_kernel): persistent CTAs (one per SM) over work items, an item
+// being (batch * key/value head, block of 128 keys), each looping over blocks of
+// 128 query rows; small grids instead give each item to two CTAs, one per half of
+// its query blocks.  All products are tcgen05 MMAs
 // with fp32 accumulators in tensor memory, computed in the transposed orientation
 // so that a TMEM lane is a key:
 //
@@ -31,13 +34,15 @@
 // tiled bulk fp32 adds on the global dQ rows.  At the end dK (times scale) and dV leave once, through
 // shared memory and bulk copies.
 //
-// Warp roles (576 threads):
-//   warps 0-15  P^T = exp2(S^T scale log2e - L log2e), dS^T = P^T o (dP^T - D)
-//               (one key per thread, four warpgroups split a block's 128 queries),
-//               written as bf16 to TMEM and dS^T to smem; the dQ read-out; the
-//               final dK/dV epilogue
-//   warp 16     TMA producer: K_j; Q_i (with L_i, D_i) and dO_i per ring stage; V_j after Q_0
+// Warp roles (640 threads):
+//   warps 0-7   P^T = exp2(S^T scale log2e - L log2e), dS^T = P^T o (dP^T - D)
+//               (one key per thread, two warpgroups split a block's 128 queries),
+//               written as bf16 to TMEM and dS^T to smem; the dV epilogue
+//   warps 8-15  the dQ read-out and adds; the dK epilogue
+//   warp 16     TMA producer: claims the items; K_j, Q_0, V_j, then Q_i (with L_i,
+//               D_i) and dO_i per ring stage
 //   warp 17     TMEM allocator; one elected lane issues every MMA and commit
+//   warps 18-19 idle (the register pool is allocated per warpgroup)
 #include <algorithm>
 
 #include "fa_ptx.cuh"
