@@ -31,8 +31,8 @@
 //   dQ_i^T = K_j^T dS^T     (A = K smem MN-major, B = dS^T smem MN-major)
 //
 // dQ_i leaves tensor memory into registers and goes through shared memory into
-// tiled bulk fp32 adds on the global dQ rows.  At the end dK (times scale) and dV leave once, through
-// shared memory and bulk copies.
+// tiled bulk fp32 adds on the global dQ rows.  At the end of an item dK (times
+// scale) and dV leave once, turned around in shared memory into whole-line stores.
 //
 // Warp roles (640 threads):
 //   warps 0-7   P^T = exp2(S^T scale log2e - L log2e), dS^T = P^T o (dP^T - D)
@@ -227,8 +227,8 @@ struct BwdTile {
     static constexpr uint32_t OFF_BAR = OFF_DELTA + QS * VEC_BYTES;
     // k_full, q_full[QS], q_empty[QS], o_full[OS], o_empty[OS], s_full, p_full,
     // dp_full, ds_full, dq_full, dq_empty, done, v_full, kv_empty, dv_free, dk_free,
-    // stg_free, dq_sync, item[2]
-    static constexpr int NBAR = 1 + 2 * QS + 2 * OS + 15;
+    // item[2]
+    static constexpr int NBAR = 1 + 2 * QS + 2 * OS + 13;
     static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;  // TMEM base, abort flag, item[2]
     static constexpr uint32_t SMEM_USED = OFF_MISC + 16;
     // The tiles need 1024-byte alignment (128-byte swizzle atoms).  At d = 128 the
@@ -299,9 +299,7 @@ __global__ void __launch_bounds__(640, 1)
     const uint32_t bar_kv_empty = bar_s_full + 64;  // an item's last products are done
     const uint32_t bar_dv_free = bar_s_full + 72;   // the epilogue has read dV from TMEM
     const uint32_t bar_dk_free = bar_s_full + 80;   // ... dK
-    const uint32_t bar_stg_free = bar_s_full + 88;  // the epilogue's copies have read the staging
-    const uint32_t bar_dq_sync = bar_s_full + 96;   // the dQ warps' adds have read their tiles
-    const uint32_t bar_item = bar_s_full + 104;     // [2] the next item is published
+    const uint32_t bar_item = bar_s_full + 88;      // [2] the next item is published
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + T::OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(gbase + T::OFF_MISC + 4);
     volatile int *item_slot = reinterpret_cast<volatile int *>(gbase + T::OFF_MISC + 8);  // [2]
@@ -416,8 +414,6 @@ __global__ void __launch_bounds__(640, 1)
         mbar_init(bar_done, 1);
         mbar_init(bar_dv_free, 256);
         mbar_init(bar_dk_free, 256);
-        mbar_init(bar_stg_free, 512);
-        mbar_init(bar_dq_sync, 256);
         mbar_init(bar_item, 1);
         mbar_init(bar_item + 8, 1);
         *abort_flag = 0;
@@ -489,10 +485,6 @@ __global__ void __launch_bounds__(640, 1)
                 ++n_k;
                 // the -L log2e and -D vectors come from the preprocess kernel
                 if (ri == 0) griddep_wait();
-                // The Q/dO rings, the dS^T tile and the dQ staging tiles held the previous
-                // item's dK/dV staging until its epilogue's copies read it.
-                if (ri > 0 && !(ok = mbar_wait<true>(bar_stg_free, (ri - 1) & 1, g, SITE_BWD_LOAD_EMPTY)))
-                    break;
                 bool v_issued = false;
                 for (int i = 0, qb = itm.qb_first, gq = itm.gq_first; i < itm.n_it;
                      ++i, (++qb == itm.n_qit) ? (qb = 0, ++gq) : 0) {
@@ -665,50 +657,61 @@ __global__ void __launch_bounds__(640, 1)
         auto epilogue = [&](const Item &itm) {
             // Every product of the item is done: dK and dV are final.  Warpgroups 0-1
             // take dV, 2-3 dK (times scale); each thread owns half a key row (d columns
-            // [64h, min(64h + 64, D))).  Rows are staged in shared memory at a 528-byte
-            // pitch (16-byte writes without bank conflicts; the Q/dO rings, the dS^T tile
-            // and the dQ staging tiles are idle once every product of the item is done;
-            // the next item's loads into them wait on stg_free) and leave with one bulk
-            // copy per half-row, so global writes are 256 contiguous bytes.  The
-            // accumulator is free for the next item's first product once it is read.
+            // [64h, min(64h + 64, D))).  A warp turns each 32-key by 32-column tile
+            // around in a 4 KB buffer of its own (128-byte swizzle: 16-byte unit j of
+            // row x at unit j ^ (x & 7), so both the row-wise writes and the transposed
+            // reads are free of bank conflicts) and stores it with plain 16-byte stores,
+            // eight lanes to a 128-byte row segment, so every store instruction writes
+            // four whole lines.  The buffers are the warp's own quarter of its half of
+            // the dS^T tile (P/dS warps: the item's last dQ^T is done, and the same warps
+            // write the next item's dS^T) or its own dQ staging tile (dQ warps, after
+            // their adds have read it): nothing waits on the epilogue but its own warp,
+            // and the stores stay out of the bulk-copy queue the dQ adds keep busy.
+            // The accumulator is free for the next item's first product once it is read.
             const int pass = wg >> 1;  // 0: dV, 1: dK
-            constexpr uint32_t kPitch = T::DP * 4 + 16;  // 16-byte units shift by one per row
-            static_assert(2 * 128 * kPitch <= T::OFF_L2 - T::OFF_Q, "epilogue staging fits");
-            const uint32_t soff = T::OFF_Q + (pass * 128 + r) * kPitch + 256 * h;
-            uint8_t *stg = gbase + soff;
             const uint32_t tcol = (pass == 0 ? T::TM_DV : T::TM_DK) + 64 * h;
             const float mul = pass == 0 ? 1.f : scale;
-            constexpr int kHalf1 = (D - 64) / 32;  // 32-column loads of the second half
+            constexpr int kHalf1 = (D - 64) / 32;  // 32-column groups of the second half
+            const int ncol = h == 0 ? 2 : kHalf1;
+            uint8_t *wbuf = gbase + (pass == 0 ? T::OFF_DS + h * T::DS_CHUNK + qt * 4096u
+                                               : T::OFF_STG + (warp - 8) * 4096u);
+            const int tr = lane >> 3, tu = lane & 7;  // transposed: row 4k + tr, unit tu
+            float *out = pass == 0 ? dv : dk;
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
-                if (h == 1 && c >= kHalf1) break;
+                if (c >= ncol) break;
                 uint32_t a[32];
                 tmem_ld32(tmem + lane_base + tcol + 32 * c, a);
                 tmem_wait_ld(a);
 #pragma unroll
-                for (int e = 0; e < 32; e += 4)
-                    *reinterpret_cast<float4 *>(stg + (32 * c + e) * 4) = make_float4(
-                        __uint_as_float(a[e]) * mul, __uint_as_float(a[e + 1]) * mul,
-                        __uint_as_float(a[e + 2]) * mul, __uint_as_float(a[e + 3]) * mul);
+                for (int j = 0; j < 8; ++j)
+                    *reinterpret_cast<float4 *>(wbuf + lane * 128 + ((j ^ (lane & 7)) << 4)) = make_float4(
+                        __uint_as_float(a[4 * j]) * mul, __uint_as_float(a[4 * j + 1]) * mul,
+                        __uint_as_float(a[4 * j + 2]) * mul, __uint_as_float(a[4 * j + 3]) * mul);
+                __syncwarp();
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const int x = 4 * k + tr;  // row of the tile
+                    const float4 v = *reinterpret_cast<const float4 *>(wbuf + x * 128 + ((tu ^ (x & 7)) << 4));
+                    const int key = itm.kv0 + 32 * qt + x;
+                    if (key < itm.len) {
+                        const size_t krow = VARLEN ? (size_t)(itm.tok0 + key) * (H / group) + itm.hk
+                                                   : (size_t)itm.kvh * N + key;
+                        float *dst = out + krow * D + 64 * h + 32 * c + 4 * tu;
+                        if constexpr (SPLIT) {
+                            atomicAdd(dst, v.x);
+                            atomicAdd(dst + 1, v.y);
+                            atomicAdd(dst + 2, v.z);
+                            atomicAdd(dst + 3, v.w);
+                        } else {
+                            *reinterpret_cast<float4 *>(dst) = v;
+                        }
+                    }
+                }
+                __syncwarp();  // the buffer's reads are done before the next tile's writes
             }
             tc_fence_before();
             mbar_arrive(pass == 0 ? bar_dv_free : bar_dk_free);
-            fence_proxy_async_smem();
-            const int key = itm.kv0 + r;
-            if (key < itm.len && (h == 0 || D > 64)) {
-                const size_t krow = VARLEN ? (size_t)(itm.tok0 + key) * (H / group) + itm.hk
-                                           : (size_t)itm.kvh * N + key;
-                float *dstg = (pass == 0 ? dv : dk) + krow * D + 64 * h;
-                const uint32_t nb = h == 0 ? (uint32_t)min(D, 64) * 4 : (uint32_t)(D - 64) * 4;
-                if constexpr (SPLIT)
-                    bulk_reduce_add_f32(dstg, base + soff, nb);
-                else
-                    bulk_store(dstg, base + soff, nb);
-            }
-            bulk_commit_group();
-            // the staging area is free for the next item once every copy has read it
-            bulk_wait_group_read<0>();
-            mbar_arrive(bar_stg_free);
         };
         if (wg < 2) {
             setmaxnreg_inc<T::REG_PDS>();
@@ -859,14 +862,20 @@ __global__ void __launch_bounds__(640, 1)
                 const Item itm = decode_item(w);
                 const int n_it = itm.n_it;
                 tok0 = itm.tok0;
-                // the staging tiles held part of the previous item's dK/dV staging
-                if (ri > 0 && !(ok = mbar_wait_warp<true>(bar_stg_free, (ri - 1) & 1, g, SITE_BWD_DQ_FULL)))
-                    break;
                 for (int i = 0, qb = itm.qb_first, gq = itm.gq_first; i < n_it;
                      ++i, (++qb == itm.n_qit) ? (qb = 0, ++gq) : 0) {
                     const int it = gb + i;
                     if (!(ok = mbar_wait_warp<true>(bar_dq_full, it & 1, g, SITE_BWD_DQ_FULL))) break;
                     tc_fence_after();
+                    if (i == n_it - 1) {
+                        // Every product of the item is done: dK leaves first (through the
+                        // warp's staging tile, once its last add has read it), so the next
+                        // item's first dK product need not wait for these dQ adds; the MMA
+                        // warp's next dP^T waits for Y below instead, which is sooner.
+                        if (lane == 0) bulk_wait_group_read<0>();
+                        __syncwarp();
+                        epilogue(itm);
+                    }
                     uint32_t x0[32], x1[32];
                     tmem_ld32(tmem + lane_base + T::TM_Y + 64 * h, x0);
                     tmem_ld32(tmem + lane_base + T::TM_Y + 64 * h + 32, x1);
@@ -880,14 +889,7 @@ __global__ void __launch_bounds__(640, 1)
                     stage_add(x0, row0, head);
                     stage_add(x1, row0 + 32, head);
                 }
-                // The staging tiles' reads finish before the dK epilogue reuses the area:
-                // every dQ thread arrives once its warp's adds have read their tile, and
-                // waits for the other 255 (a bounded wait, like every other).
-                if (lane == 0) bulk_wait_group_read<0>();
-                __syncwarp();
-                mbar_arrive(bar_dq_sync);
-                if (!(ok = ok && mbar_wait_warp<true>(bar_dq_sync, ri & 1, g, SITE_BWD_DQ_FULL))) break;
-                epilogue(itm);
+                if (!ok) break;
                 gb += n_it;
                 ++ri;
             }
