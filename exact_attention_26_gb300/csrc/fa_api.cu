@@ -270,6 +270,7 @@ namespace {
 // of a forward with cut key ranges, for the current device.
 struct FwdSplit {
     int chunk, s_max;
+    const FwdSegPlan *seg;  // the balanced plan, when the library chose one
     size_t bytes, l_offset;
 };
 int fwd_split_plan(int B, int H, int N, int d, int causal, int kv_chunk_keys, FwdSplit *out) {
@@ -279,10 +280,12 @@ int fwd_split_plan(int B, int H, int N, int d, int causal, int kv_chunk_keys, Fw
     const int bn = fwd_block_n(d);
     const int forced = kv_chunk_keys > 0 ? (kv_chunk_keys + bn - 1) / bn : 0;
     FwdSplit s{};
-    s.chunk = fwd_split_chunk(d, B * H, N, causal, dc->num_sms, forced);
-    if (s.chunk > 0) {
+    // automatic: a balanced plan first, else even chunks or no cut
+    s.seg = forced > 0 ? nullptr : fwd_seg_plan(d, B * H, N, causal, dc->num_sms);
+    s.chunk = s.seg ? 0 : fwd_split_chunk(d, B * H, N, causal, dc->num_sms, forced);
+    if (s.chunk > 0 || s.seg) {
         const int n_kv = (N + bn - 1) / bn;
-        s.s_max = (n_kv + s.chunk - 1) / s.chunk;
+        s.s_max = s.seg ? s.seg->s_max : (n_kv + s.chunk - 1) / s.chunk;
         const size_t rows = (size_t)B * H * N * s.s_max;
         s.l_offset = round_up(rows * d * sizeof(float), 256);
         s.bytes = s.l_offset + round_up(rows * sizeof(float), 256);
@@ -292,6 +295,27 @@ int fwd_split_plan(int B, int H, int N, int d, int causal, int kv_chunk_keys, Fw
 }
 }  // namespace
 }  // namespace fa
+
+extern "C" int fa_fwd_split_segments(int B, int H, int N, int d, int causal, int num_sms,
+                                     int *out, int cap) {
+    if (check_sizes(B, H, N, d, true) != FA_OK || num_sms < 1 || cap < 0 || (cap > 0 && !out))
+        return FA_ERR_INVALID_ARG;
+    const FwdSegPlan *plan = fwd_seg_plan(d, B * H, N, causal ? 1 : 0, num_sms);
+    if (!plan) return 0;
+    for (int c = 0; c < plan->tab.n_cta; ++c)
+        for (int i = plan->tab.start[c]; i < plan->tab.start[c + 1] && i < cap; ++i) {
+            const uint32_t w0 = plan->tab.seg[i][0], w1 = plan->tab.seg[i][1];
+            int *e = out + 7 * i;
+            e[0] = (int)(w0 & 0xffffu);
+            e[1] = (int)(w0 >> 16);
+            e[2] = (int)(w1 & 0xfffu);
+            e[3] = (int)((w1 >> 12) & 0xfffu);
+            e[4] = (int)((w1 >> 24) & 0xfu);
+            e[5] = (int)(w1 >> 28);
+            e[6] = c;
+        }
+    return plan->n_seg;
+}
 
 extern "C" size_t fa_fwd_workspace_bytes(int B, int H, int N, int d, int causal, int kv_chunk) {
     if (check_sizes(B, H, N, d, true) != FA_OK || kv_chunk < 0) return 0;
@@ -313,7 +337,7 @@ extern "C" int fa_fwd_ws(const void *q, const void *k, const void *v, void *o, f
         return FA_ERR_MISALIGNED;
     FwdSplit sp{};
     if ((rc = fwd_split_plan(B, H, N, d, causal, kv_chunk, &sp)) != FA_OK) return rc;
-    if (sp.chunk > 0) {
+    if (sp.chunk > 0 || sp.seg) {
         if (!workspace || workspace_bytes < sp.bytes) return FA_ERR_WORKSPACE;
         if (reinterpret_cast<uintptr_t>(workspace) & 255u) return FA_ERR_MISALIGNED;
     }
@@ -334,7 +358,8 @@ extern "C" int fa_fwd_ws(const void *q, const void *k, const void *v, void *o, f
     p.causal = causal ? 1 : 0;
     p.scale_log2 = scale * kLog2e;
     p.kv_chunk = sp.chunk;
-    if (sp.chunk > 0) {
+    p.seg = sp.seg;
+    if (sp.chunk > 0 || sp.seg) {
         p.ws_o = static_cast<float *>(workspace);
         p.ws_l = reinterpret_cast<float *>(static_cast<char *>(workspace) + sp.l_offset);
         p.s_max = sp.s_max;

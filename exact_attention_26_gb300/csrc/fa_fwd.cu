@@ -53,6 +53,8 @@
 // and are not stored.
 #include <algorithm>
 #include <array>
+#include <memory>
+#include <type_traits>
 #include <mutex>
 #include <vector>
 
@@ -183,6 +185,14 @@ struct FwdTile {
 // then one chunk; a row block with one chunk writes O and L as usual, the others
 // write their normalised partial O_s (fp32, ws_o [BH][N][s_max][D]) and
 // L_s = m_s + ln l_s (ws_l [BH][N][s_max]), which fa_fwd_merge_kernel combines.
+// Kernel argument carrying the balanced plan (n_cta = 0: none); launches that
+// cannot cut key ranges take a one-int stand-in.
+struct SegNone {
+    int n_cta;
+};
+template <bool SPLIT>
+using SegArg = typename std::conditional<SPLIT, FwdSegTable, SegNone>::type;
+
 template <int D, bool CAUSAL, bool VARLEN, bool F8, bool ONE, bool SPLIT>
 __global__ void __launch_bounds__(FwdTile<D, F8, ONE>::THREADS, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -192,7 +202,7 @@ __global__ void __launch_bounds__(FwdTile<D, F8, ONE>::THREADS, 1)
                   const float *__restrict__ q_descale, const float *__restrict__ k_descale,
                   const float *__restrict__ v_descale, int nqb, int chunk,
                   float *__restrict__ ws_o, float *__restrict__ ws_l, int s_max, int *status,
-                  unsigned long long limit_ns) {
+                  unsigned long long limit_ns, const __grid_constant__ SegArg<SPLIT> tab) {
     using T = FwdTile<D, F8, ONE>;
     constexpr int NT = T::NT;
     constexpr int KS = T::KS;
@@ -254,17 +264,30 @@ __global__ void __launch_bounds__(FwdTile<D, F8, ONE>::THREADS, 1)
     auto n_kv_of = [&](int cb) -> int {
         return CAUSAL ? min(n_kv_all, ((cb + 1) * T::ROWS + T::BN - 1) / T::BN) : n_kv_all;
     };
+    // balanced plan (SPLIT, tab.n_cta > 0): CTA c runs the table's segments
+    // [start[c], start[c + 1]) in order instead of the snake over even chunks
+    const bool use_tab = SPLIT && tab.n_cta > 0;
     int per_bh = n_cblocks;  // work items per (batch, head)
     int last_chunks = 1;     // SPLIT: chunks of the last row block
     if constexpr (SPLIT) {
-        last_chunks = (n_kv_of(n_cblocks - 1) + chunk - 1) / chunk;
-        per_bh = CAUSAL ? (n_cblocks > 1 ? chunks_upto(n_cblocks - 2) : 0) + last_chunks
-                        : n_cblocks * last_chunks;
+        if (!use_tab) {
+            last_chunks = (n_kv_of(n_cblocks - 1) + chunk - 1) / chunk;
+            per_bh = CAUSAL ? (n_cblocks > 1 ? chunks_upto(n_cblocks - 2) : 0) + last_chunks
+                            : n_cblocks * last_chunks;
+        }
     }
     const int n_items = per_bh * BH;
     const int G = (int)gridDim.x;
-    const int n_rounds = (n_items + G - 1) / G;
+    int n_rounds = (n_items + G - 1) / G;
+    if constexpr (SPLIT)
+        if (use_tab) n_rounds = tab.max_per_cta;
     auto item_of = [&](int rnd) -> int {
+        if constexpr (SPLIT) {
+            if (use_tab) {
+                const int idx = (int)tab.start[blockIdx.x] + rnd;
+                return idx < (int)tab.start[blockIdx.x + 1] ? idx : -1;
+            }
+        }
         const int idx = rnd * G + ((rnd & 1) ? (G - 1 - (int)blockIdx.x) : (int)blockIdx.x);
         return idx < n_items ? idx : -1;
     };
@@ -273,6 +296,7 @@ __global__ void __launch_bounds__(FwdTile<D, F8, ONE>::THREADS, 1)
         int len, tok0;  // rows of this head's sequence; its first token (packed layout)
         int kv_lo;      // first K/V tile of the item's key range
         int s, ns;      // SPLIT: chunk index, chunks of this row block
+        int n_seg;      // SPLIT: K/V tiles of the item's key range (at most)
     };
     auto decode = [&](int w) {
         Item it;
@@ -285,7 +309,18 @@ __global__ void __launch_bounds__(FwdTile<D, F8, ONE>::THREADS, 1)
         it.kv_lo = 0;
         it.s = 0;
         it.ns = 1;
+        it.n_seg = chunk;
         if constexpr (SPLIT) {
+          if (use_tab) {
+            const uint32_t w0 = tab.seg[w][0], w1 = tab.seg[w][1];
+            it.bh = (int)(w0 & 0xffffu);
+            it.cb = (int)(w0 >> 16);
+            it.kvh = (it.bh / H) * (H / group) + (it.bh % H) / group;
+            it.kv_lo = (int)(w1 & 0xfffu);
+            it.n_seg = (int)((w1 >> 12) & 0xfffu);
+            it.s = (int)((w1 >> 24) & 0xfu);
+            it.ns = (int)(w1 >> 28);
+          } else {
             // items run row block by row block, the longest (last) first, chunks in
             // key order within a row block
             int r = w / BH;
@@ -314,6 +349,7 @@ __global__ void __launch_bounds__(FwdTile<D, F8, ONE>::THREADS, 1)
                 it.ns = (n_kv_of(lo) + chunk - 1) / chunk;
             }
             it.kv_lo = it.s * chunk;
+          }
         }
         if constexpr (VARLEN) {
             // cu_seqlens lives on the device, so it is checked here: a sequence that is
@@ -341,7 +377,7 @@ __global__ void __launch_bounds__(FwdTile<D, F8, ONE>::THREADS, 1)
                 it.n_kv[t] = 0;
             else
                 it.n_kv[t] = CAUSAL ? min(n_kv_seq, (row0 + T::BM + T::BN - 1) / T::BN) : n_kv_seq;
-            if constexpr (SPLIT) it.n_kv[t] = max(0, min(it.n_kv[t] - it.kv_lo, chunk));
+            if constexpr (SPLIT) it.n_kv[t] = max(0, min(it.n_kv[t] - it.kv_lo, it.n_seg));
             it.n_max = max(it.n_max, it.n_kv[t]);
         }
         return it;
@@ -990,7 +1026,7 @@ __global__ void __launch_bounds__(256)
     fa_fwd_merge_kernel(const float *__restrict__ ws_o, const float *__restrict__ ws_l,
                         __nv_bfloat16 *__restrict__ out, float *__restrict__ lse, int N, int BH,
                         int causal, int rows_per_block, int n_kv_all, int keys_per_tile, int chunk,
-                        int s_max) {
+                        int s_max, const __grid_constant__ FwdMergeNs mns, int n_cb_tab) {
     griddep_wait();  // the partials come from the attention kernel
     constexpr int PER = D / 32;
     const int lane = threadIdx.x & 31;
@@ -1001,7 +1037,8 @@ __global__ void __launch_bounds__(256)
     const int n_kv = causal ? min(n_kv_all, ((cb + 1) * rows_per_block + keys_per_tile - 1) /
                                                 keys_per_tile)
                             : n_kv_all;
-    const int ns = (n_kv + chunk - 1) / chunk;
+    // balanced plan (n_cb_tab > 0): the row block's segment count from its table
+    const int ns = n_cb_tab > 0 ? (int)mns.ns[(row / N) * n_cb_tab + cb] : (n_kv + chunk - 1) / chunk;
     if (ns <= 1) return;
     const float *pl = ws_l + (size_t)row * s_max;
     float m = -INFINITY;
@@ -1094,6 +1131,140 @@ int fwd_split_chunk_t(int BH, int N, int causal, int num_sms, int forced) {
     return chunk;
 }
 
+// Balanced plan: the row blocks of all heads, longest first, laid end to end and
+// cut into segments so that each CTA's run of consecutive segments stays within
+// `cap` steps (its tiles plus kItemCost per segment); no piece shorter than
+// `min_seg` tiles is cut off a row block unless the CTA is otherwise empty.  Fills
+// `out` (when given) and returns the CTAs used, or 0 when more than G CTAs, kSegMax
+// segments or kSegMaxParts segments of one row block would be needed.
+struct SegRow {
+    int bh, cb;
+    long long nk;
+};
+int seg_fill(const std::vector<SegRow> &rows, int n_cb, long long cap, long long min_seg, int G,
+             FwdSegPlan *out) {
+    const long long ic = (long long)kItemCost;
+    int cta = 0, n = 0, s_max = 0;
+    long long load = 0, worst = 0;
+    if (out) out->tab.start[0] = 0;
+    for (const SegRow &row : rows) {
+        long long rem = row.nk, kv = 0;
+        int parts = 0;
+        const int first = n;
+        while (rem > 0) {
+            const long long avail = cap - load - ic;
+            long long take;
+            if (rem <= avail) {
+                take = rem;
+            } else {
+                take = rem - avail < min_seg ? rem - min_seg : avail;
+                if (take < min_seg) take = load == 0 ? std::min(rem, std::max(avail, 1LL)) : 0;
+            }
+            if (take > 0) {
+                if (n >= kSegMax || parts >= kSegMaxParts) return 0;
+                if (out) {
+                    out->tab.seg[n][0] = (uint32_t)row.bh | ((uint32_t)row.cb << 16);
+                    out->tab.seg[n][1] = (uint32_t)kv | ((uint32_t)take << 12) | ((uint32_t)parts << 24);
+                }
+                ++n;
+                ++parts;
+                kv += take;
+                rem -= take;
+                load += take + ic;
+                worst = std::max(worst, load);
+            }
+            if (rem > 0) {  // the CTA is full: the rest of the row block goes to the next
+                if (++cta >= G) return 0;
+                if (out) out->tab.start[cta] = (uint16_t)n;
+                load = 0;
+            }
+        }
+        if (out) {
+            for (int i = first; i < n; ++i) out->tab.seg[i][1] |= (uint32_t)parts << 28;
+            out->mns.ns[row.bh * n_cb + row.cb] = (uint8_t)parts;
+        }
+        s_max = std::max(s_max, parts);
+    }
+    const int used = load > 0 ? cta + 1 : cta;
+    if (out) {
+        out->tab.n_cta = used;
+        out->tab.start[used] = (uint16_t)n;
+        int busiest = 0;
+        for (int c = 0; c < used; ++c) busiest = std::max(busiest, out->tab.start[c + 1] - out->tab.start[c]);
+        out->tab.max_per_cta = busiest;
+        out->n_seg = n;
+        out->s_max = s_max;
+        out->cost = (double)worst + kMergeCost;
+    }
+    return used;
+}
+
+template <int D>
+const FwdSegPlan *fwd_seg_plan_t(int BH, int N, int causal, int num_sms) {
+    using T = FwdTile<D, false, true>;
+    const long long ratio = T::ROWS / T::BN;
+    const long long n_cb = (N + T::ROWS - 1) / T::ROWS;
+    const long long n_kv_all = (N + T::BN - 1) / T::BN;
+    const int G = std::min(num_sms, kSegMaxCta);
+    if (n_cb * BH >= num_sms || n_cb * BH > kSegMaxRows || n_kv_all >= 4096 || n_cb > 65535 ||
+        BH > 65535)
+        return nullptr;
+    struct Memo {
+        int BH, N, causal, num_sms;
+        std::unique_ptr<FwdSegPlan> plan;
+    };
+    static std::mutex m;
+    static std::vector<Memo> memo;
+    {
+        std::lock_guard<std::mutex> lock(m);
+        for (const Memo &e : memo)
+            if (e.BH == BH && e.N == N && e.causal == causal && e.num_sms == num_sms) return e.plan.get();
+    }
+    std::vector<SegRow> rows;
+    long long total = 0, longest = 0;
+    for (long long i = 0; i < n_cb; ++i) {
+        const long long cb = causal ? n_cb - 1 - i : i;
+        const long long nk = causal ? std::min(n_kv_all, (cb + 1) * ratio) : n_kv_all;
+        for (int h = 0; h < BH; ++h) rows.push_back({h, (int)cb, nk});
+        total += BH * (nk + (long long)kItemCost);
+        longest = std::max(longest, nk);
+    }
+    // Smallest cap the greedy fill meets with at most G CTAs (bisection); pieces of
+    // at least eight row blocks' worth of diagonal tiles.  Only launches of at least
+    // eight tiles per CTA: the cost model was fitted on long launches.
+    const long long min_seg = 8 * ratio;
+    if (total - BH * n_cb * (long long)kItemCost < 8LL * G) {
+        std::lock_guard<std::mutex> lock(m);
+        memo.push_back({BH, N, causal, num_sms, nullptr});
+        return nullptr;
+    }
+    long long lo = std::max<long long>((total + G - 1) / G, (long long)kItemCost + 2 * min_seg);
+    long long hi = lo + longest + (long long)kItemCost + 2 * min_seg;
+    std::unique_ptr<FwdSegPlan> plan;
+    if (seg_fill(rows, (int)n_cb, hi, min_seg, G, nullptr) > 0) {
+        while (lo < hi) {
+            const long long mid = (lo + hi) / 2;
+            if (seg_fill(rows, (int)n_cb, mid, min_seg, G, nullptr) > 0) hi = mid; else lo = mid + 1;
+        }
+        plan.reset(new FwdSegPlan{});
+        seg_fill(rows, (int)n_cb, lo, min_seg, G, plan.get());
+        // kept only when predicted 5% faster than no cut and faster than even chunks
+        const double uncut = fwd_split_cost(BH, n_cb, ratio, n_kv_all, causal, 0, num_sms);
+        double even = uncut;
+        for (long long c : {16, 24, 32, 48, 64, 96, 128, 192, 256, 384, 512}) {
+            const long long ct = c * ratio;
+            if (ct >= longest) break;
+            even = std::min(even, fwd_split_cost(BH, n_cb, ratio, n_kv_all, causal, ct, num_sms));
+        }
+        if (!(plan->cost < 0.95 * uncut && plan->cost < even) || plan->s_max < 2) plan.reset();
+    }
+    // plans are kept for the life of the process (a few KB per shape), so the
+    // pointers handed out stay valid
+    std::lock_guard<std::mutex> lock(m);
+    memo.push_back({BH, N, causal, num_sms, std::move(plan)});
+    return memo.back().plan.get();
+}
+
 template <int D, bool CAUSAL, bool VARLEN, bool F8 = false, bool ONE = false, bool SPLIT = false>
 int launch_fwd_t(const FwdParams &p, cudaStream_t stream) {
     using T = FwdTile<D, F8, ONE>;
@@ -1107,7 +1278,9 @@ int launch_fwd_t(const FwdParams &p, cudaStream_t stream) {
     const int n_cblocks = (p.N + T::ROWS - 1) / T::ROWS;
     long long items = (long long)n_cblocks * p.BH;
     const int n_kv_all = (p.N + T::BN - 1) / T::BN;
-    if (SPLIT) {
+    if (SPLIT && p.seg) {
+        items = p.seg->tab.n_cta;  // the plan's CTAs, each with its run of segments
+    } else if (SPLIT) {
         const int ratio = T::ROWS / T::BN;
         long long per = 0;
         for (long long cb = 0; cb < n_cblocks; ++cb) {
@@ -1120,11 +1293,14 @@ int launch_fwd_t(const FwdParams &p, cudaStream_t stream) {
     // Persistent: one CTA per SM (the shared-memory footprint allows no more).
     const long long grid = items < p.num_sms ? items : p.num_sms;
     if (grid < 1) return FA_OK;
+    SegArg<SPLIT> tab{};
+    if constexpr (SPLIT)
+        if (p.seg) tab = p.seg->tab;
     kern<<<(unsigned)grid, T::THREADS, T::SMEM_BYTES, stream>>>(
         p.tm_q, p.tm_k, p.tm_v, reinterpret_cast<__nv_bfloat16 *>(p.o), p.lse, p.N, p.BH, p.H,
         p.group, n_cblocks, p.cu_seqlens, p.total_tokens, p.scale_log2, p.q_descale, p.k_descale,
         p.v_descale, (p.N + 127) / 128, p.kv_chunk, p.ws_o, p.ws_l, p.s_max, p.status,
-        p.limit_ns);
+        p.limit_ns, tab);
     if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
     if (SPLIT) {
         const long long rows = (long long)p.BH * p.N;
@@ -1139,10 +1315,12 @@ int launch_fwd_t(const FwdParams &p, cudaStream_t stream) {
         attr[0].val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
+        FwdMergeNs mns{};
+        if (p.seg) mns = p.seg->mns;
         if (cudaLaunchKernelEx(&cfg, fa_fwd_merge_kernel<D>, (const float *)p.ws_o,
                                (const float *)p.ws_l, reinterpret_cast<__nv_bfloat16 *>(p.o), p.lse,
                                p.N, p.BH, p.causal, T::ROWS, n_kv_all, T::BN, p.kv_chunk,
-                               p.s_max) != cudaSuccess)
+                               p.s_max, mns, p.seg ? n_cblocks : 0) != cudaSuccess)
             return FA_ERR_CUDA;
     }
     return FA_OK;
@@ -1154,7 +1332,7 @@ template <int D>
 int launch_fwd_d(const FwdParams &p, cudaStream_t stream) {
     if (p.cu_seqlens)
         return p.causal ? launch_fwd_t<D, true, true>(p, stream) : launch_fwd_t<D, false, true>(p, stream);
-    if (p.kv_chunk > 0) {  // cut key ranges (one tile per CTA); the caller sized the workspace
+    if (p.kv_chunk > 0 || p.seg) {  // cut key ranges (one tile per CTA); the caller sized the workspace
         return p.causal ? launch_fwd_t<D, true, false, false, (D <= 128), true>(p, stream)
                         : launch_fwd_t<D, false, false, false, (D <= 128), true>(p, stream);
     }
@@ -1166,6 +1344,16 @@ int launch_fwd_d(const FwdParams &p, cudaStream_t stream) {
                             : launch_fwd_t<D, false, false, false, true>(p, stream);
     }
     return p.causal ? launch_fwd_t<D, true, false>(p, stream) : launch_fwd_t<D, false, false>(p, stream);
+}
+
+const FwdSegPlan *fwd_seg_plan(int d, int BH, int N, int causal, int num_sms) {
+    switch (d) {
+        case 64: return fwd_seg_plan_t<64>(BH, N, causal, num_sms);
+        case 96: return fwd_seg_plan_t<96>(BH, N, causal, num_sms);
+        case 128: return fwd_seg_plan_t<128>(BH, N, causal, num_sms);
+        case 256: return fwd_seg_plan_t<256>(BH, N, causal, num_sms);
+        default: return nullptr;
+    }
 }
 
 int fwd_split_chunk(int d, int BH, int N, int causal, int num_sms, int forced) {

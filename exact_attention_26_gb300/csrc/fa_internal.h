@@ -46,6 +46,8 @@ enum WaitSite : int {
 // Default limit of one in-kernel wait.
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 
+struct FwdSegPlan;
+
 struct FwdParams {
     CUtensorMap tm_q, tm_k, tm_v;  // 3-D maps over [BH][N][d] (q) and [B*Hkv][N][d] (k, v) bf16
     void *o;                       // bf16 [BH][N][d]
@@ -58,6 +60,7 @@ struct FwdParams {
     int fp8;                       // e4m3 inputs: tm_q/tm_k over bytes, tm_v over V^T [B*Hkv][d][Np]
     const float *q_descale, *k_descale, *v_descale;  // fp8: [BH][nqb], [B*Hkv][nqb], [B*Hkv]
     int kv_chunk;                  // > 0: key ranges cut into chunks of this many K/V tiles
+    const FwdSegPlan *seg;         // non-null: key ranges cut by this balanced plan
     float *ws_o, *ws_l;            // kv_chunk > 0: partial O [BH][N][s_max][d], L [BH][N][s_max]
     int s_max;                     // chunks of the longest key range
     int *status;                   // device status record (2 ints)
@@ -69,6 +72,31 @@ struct FwdParams {
 // (0: no cut); `forced` > 0 asks for that many tiles (rounded up to the tiles of a
 // row block on the diagonal).
 int fwd_split_chunk(int d, int BH, int N, int causal, int num_sms, int forced);
+
+// Balanced cut of the one-tile forward's key ranges: the row blocks, longest first,
+// are laid end to end and cut into segments (a row block's K/V tiles
+// [kv_lo, kv_lo + n)) so that every CTA's run of consecutive segments costs about
+// the same (its tiles plus a fixed cost per segment); the kernel reads its run from
+// the table and the merge kernel the segment count of each row block.
+constexpr int kSegMaxCta = 256, kSegMax = 640, kSegMaxRows = 256, kSegMaxParts = 15;
+struct FwdSegTable {
+    int n_cta, max_per_cta;           // CTAs of the launch; segments of the busiest
+    uint16_t start[kSegMaxCta + 1];   // CTA c runs segments [start[c], start[c + 1])
+    uint32_t seg[kSegMax][2];         // bh | cb << 16;  kv_lo | n << 12 | s << 24 | ns << 28
+};
+struct FwdMergeNs {
+    uint8_t ns[kSegMaxRows];          // segments of row block bh * n_cb + cb
+};
+struct FwdSegPlan {
+    FwdSegTable tab;
+    FwdMergeNs mns;
+    int n_seg, s_max;                 // segments; most segments of one row block
+    double cost;                      // predicted K/V-tile steps, merge included
+};
+// The balanced plan for B*H heads of N rows, or null when the library does not cut
+// this way (the cut is not predicted 5% faster than no cut and faster than even
+// chunks).  Plans are remembered per shape; the pointer stays valid.
+const FwdSegPlan *fwd_seg_plan(int d, int BH, int N, int causal, int num_sms);
 // Rows per TMA box of the forward's K and V tensor maps (the kernel loads a K/V
 // tile of BN keys as BN / box boxes).
 constexpr int fwd_kv_box_rows(int d) { return d == 256 ? 64 : 128; }

@@ -30,7 +30,8 @@ EXPORTED = ("fa_fwd", "fa_bwd", "fa_bwd_workspace_bytes", "fa_status_string", "f
             "fa_decode_workspace_bytes", "fa_decode_paged", "fa_decode_paged_num_splits",
             "fa_decode_paged_workspace_bytes", "fa_fwd_gqa", "fa_bwd_gqa", "fa_fwd_varlen",
             "fa_bwd_varlen", "fa_quantize_fp8_workspace_bytes", "fa_quantize_fp8", "fa_fwd_fp8",
-            "fa_probe_unit_rates", "fa_probe_read_bandwidth", "fa_fwd_ws", "fa_fwd_workspace_bytes")
+            "fa_probe_unit_rates", "fa_probe_read_bandwidth", "fa_fwd_ws", "fa_fwd_workspace_bytes",
+            "fa_fwd_split_segments")
 
 _vp = ctypes.c_void_p
 _int = ctypes.c_int
@@ -190,6 +191,29 @@ def fa_fwd_workspace_bytes(B, H, N, d, causal, kv_chunk=0) -> int:
         fn.argtypes = [_int] * 6
         fn.restype = ctypes.c_size_t
     return fn(B, H, N, d, int(bool(causal)), kv_chunk)
+
+
+def fa_fwd_split_segments(B, H, N, d, causal, num_sms, out=None, cap=0) -> int:
+    """Raw call: fills `out` (ctypes int array of 7 * cap) and returns the count."""
+    fn = load().fa_fwd_split_segments
+    if fn.argtypes is None:
+        fn.argtypes = [_int] * 6 + [_vp, _int]
+        fn.restype = _int
+    return fn(B, H, N, d, int(bool(causal)), num_sms, out, cap)
+
+
+def fwd_split_segments(B, H, N, d, causal, num_sms):
+    """The balanced cut of fa_fwd_ws (kv_chunk = 0) for num_sms SMs, as a list of
+    (head, row block, first K/V tile, K/V tiles, part, parts, CTA) tuples ([]: no
+    such cut).  Host only."""
+    n = fa_fwd_split_segments(B, H, N, d, causal, num_sms)
+    if n < 0:
+        raise FaError(n, "fa_fwd_split_segments")
+    if n == 0:
+        return []
+    buf = (ctypes.c_int * (7 * n))()
+    fa_fwd_split_segments(B, H, N, d, causal, num_sms, ctypes.cast(buf, _vp), n)
+    return [tuple(buf[7 * i:7 * i + 7]) for i in range(n)]
 
 
 def fa_fwd_ws(q, k, v, o, lse, B, H, Hkv, N, d, causal, scale, kv_chunk, workspace,

@@ -145,6 +145,25 @@ int fa_bwd_gqa(const void *q, const void *k, const void *v, const void *o, const
  * The choice and the size depend on the current device's SM count.
  */
 size_t fa_fwd_workspace_bytes(int B, int H, int N, int d, int causal, int kv_chunk);
+
+/*
+ * The balanced cut fa_fwd_ws makes with kv_chunk = 0 on a device of num_sms SMs, for
+ * inspection (host only: nothing is launched and no device is needed).  The row
+ * blocks of 128 query rows of all B*H heads, longest first, are laid end to end and
+ * cut into segments so that every CTA's run of consecutive segments costs about the
+ * same, counting a segment's K/V tiles plus a fixed cost of six tile steps (its Q
+ * load, pipeline fill and epilogue); no row block is cut into more than 15 parts.
+ * The library uses this cut when its cost model predicts it at least 5% faster than
+ * no cut and faster than even chunks, and otherwise cuts evenly or not at all.
+ *   out : int[cap][7] host buffer, filled with the first cap segments in CTA order:
+ *         head (b * H + h), row block, first K/V tile, K/V tiles, part s within the
+ *         row block (in key order), parts of the row block, CTA.  May be NULL when
+ *         cap = 0.
+ * Returns the number of segments (0: the library does not cut this shape this way),
+ * or FA_ERR_INVALID_ARG for invalid sizes, num_sms < 1, cap < 0 or a NULL out with
+ * cap > 0.
+ */
+int fa_fwd_split_segments(int B, int H, int N, int d, int causal, int num_sms, int *out, int cap);
 int fa_fwd_ws(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H,
               int Hkv, int N, int d, int causal, float scale, int kv_chunk, void *workspace,
               size_t workspace_bytes, void *stream);

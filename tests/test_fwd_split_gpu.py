@@ -73,6 +73,31 @@ def test_single_head_long_causal_workload(fa, orc):
     assert_abs_close(lse.cpu().numpy()[:, :, rows], rl, L_ABS, "B1H1N16384 sample L")
 
 
+# shapes the library cuts with its balanced plan (kv_chunk = 0): every head
+# dimension, both masks, one and two heads, ragged N
+AUTO = [(1, 2, 6000, 128, True), (1, 1, 8192, 64, True), (1, 2, 3000, 256, False),
+        (1, 1, 8192, 96, False)]
+
+
+@pytest.mark.parametrize("case", AUTO, ids=lambda c: "x".join(map(str, c)))
+def test_balanced_cut_matches_the_oracle(fa, orc, case):
+    B, H, N, d, causal = case
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    segs = fa.fwd_split_segments(B, H, N, d, causal, sms)
+    assert segs and max(s[5] for s in segs) >= 2, "the library cuts this shape"
+    q, k, v = normal_qkv(B, H, N, d, seed=N + d)
+    o, lse = fa.forward(q.to(DEV), k.to(DEV), v.to(DEV), causal=causal)
+    torch.cuda.synchronize()
+    assert fa.fa_device_status(None) == 0
+    # rows of every cut row block's first and last 128, plus seeded ones
+    cut = sorted({s[1] for s in segs if s[5] >= 2})
+    rows = np.unique(np.concatenate([sample_rows(N, 128, seed=3).numpy(),
+                                     [cut[0] * 128, min(N, cut[-1] * 128 + 128) - 1, N - 1]]))
+    ro, rl = orc.fwd_rows(to_f64(q), to_f64(k), to_f64(v), rows, causal=causal)
+    assert_o_close(o.float().cpu().numpy()[:, :, rows], ro, f"{case}")
+    assert_abs_close(lse.cpu().numpy()[:, :, rows], rl, L_ABS, f"{case} L")
+
+
 def test_cut_and_uncut_agree(fa):
     """The same inputs through fa_fwd and through cut key ranges: O within the bf16
     rounding of either, L within fp32 rounding of the merge."""
