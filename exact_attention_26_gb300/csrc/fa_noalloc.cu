@@ -19,7 +19,7 @@
 namespace fa {
 namespace {
 
-constexpr size_t kScratchBytes = FA_NOALLOC_SCRATCH_BYTES;  // 8 MiB
+constexpr size_t kScratchBytes = FA_NOALLOC_SCRATCH_BYTES;  // 8 MiB + 256 bytes
 
 static __device__ __align__(256) unsigned char g_bwd_scratch[kScratchBytes];
 

@@ -192,7 +192,8 @@ int fa_fwd_ws(const void *q, const void *k, const void *v, void *o, float *lse, 
  *     streams, no ordering between them) race on it and give wrong results.
  * Calls no cudaMalloc, cudaFree or other allocating routine.
  */
-#define FA_NOALLOC_SCRATCH_BYTES ((size_t)8 << 20)
+/* 8 MiB for 1,048,576 rows of the two fp32 vectors, plus room for the work counter */
+#define FA_NOALLOC_SCRATCH_BYTES (((size_t)8 << 20) + 256)
 int fa_bwd_noalloc(const void *q, const void *k, const void *v, const void *o,
                    const float *lse, const void *dout, float *dq, float *dk, float *dv, int B,
                    int H, int N, int d, int causal, float scale, void *stream);

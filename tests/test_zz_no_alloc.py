@@ -41,6 +41,9 @@ def test_noalloc_rejects_sizes_beyond_its_scratch():
     # B*H*roundup(N,128) = 8 * 16 * 16384 = 2,097,152 rows > 1,048,576
     rc = lib.fa_bwd_noalloc(*([ptr] * 9), 8, 16, 16384, 128, 1, 0.088, None)
     assert rc == FA_ERR_WORKSPACE
+    # one 128-row block past the limit
+    rc = lib.fa_bwd_noalloc(*([ptr] * 9), 1, 1, 1048576 + 128, 128, 1, 0.088, None)
+    assert rc == FA_ERR_WORKSPACE
 
 
 @pytest.mark.gpu
