@@ -173,13 +173,16 @@ __global__ void __launch_bounds__(256)
 // Tensor memory (512 columns, d = 128): dV [0,128), dK [128,256), X [256,384),
 // Y [384,512).  X holds S^T, then P^T as bf16 over its first half; Y holds dP^T,
 // then dS^T as bf16, then dQ^T.  (d = 64: dV [0,64), dK [64,128), X [128,256),
-// Y [256,384).)  Per block i the MMA thread issues
+// Y [256,384), and dQ^T in Z [384,512) of its own.)  Per block i the MMA thread
+// issues
 //
 //   dP^T(i)     = V dO(i)^T   -> Y        once dQ^T(i-1) has been read out of Y
+//                                         (d = 64: without waiting)
 //   dV(i)      += P^T(i) dO(i)            A = P^T in X
 //   S^T(i+1)    = K Q(i+1)^T  -> X        X is free once dV(i) has read P^T(i)
 //   dK(i)      += dS^T(i) Q(i)            A = dS^T in Y
-//   dQ^T(i)     = K^T dS^T(i) -> Y        B = dS^T from shared memory
+//   dQ^T(i)     = K^T dS^T(i) -> Y        B = dS^T from shared memory (d = 64: -> Z,
+//                                         once dQ^T(i-1) has been read out of it)
 //
 // Warpgroups 0-1 compute dS(i) while dV(i) and S^T(i+1) run and P(i+1) while
 // dK(i), dQ^T(i) and dP^T(i+1) run.  Warpgroups 2-3 read dQ^T(i) out of Y into
@@ -215,6 +218,11 @@ struct BwdTile {
     static constexpr uint32_t VEC_BYTES = BQ * 4;
     static constexpr uint32_t TM_DV = 0, TM_DK = DP, TM_X = 2 * DP, TM_Y = 2 * DP + 128,
                               TM_COLS = 512;
+    // d = 64 leaves 128 columns spare: dQ^T gets its own (Z), so the next block's
+    // dP^T need not wait for the dQ warps to read dQ^T out of Y; the next dQ^T waits
+    // instead, a block later.  Wider heads share Y.
+    static constexpr bool SEPQ = DP == 64;
+    static constexpr uint32_t TM_QT = SEPQ ? TM_Y + 128 : TM_Y;
     static constexpr uint32_t OFF_K = 0;
     static constexpr uint32_t OFF_V = OFF_K + KV_BYTES;
     static constexpr uint32_t OFF_Q = OFF_V + KV_BYTES;
@@ -249,7 +257,7 @@ struct BwdTile {
     static_assert(SMEM_USED <= kMaxSmem, "shared memory budget");
     static_assert(Q_CHUNK % 1024 == 0 && DS_CHUNK % 1024 == 0 && KV_BYTES % 1024 == 0,
                   "swizzle atoms must stay aligned");
-    static_assert(TM_Y + 128 <= TM_COLS, "tensor memory budget");
+    static_assert(TM_Y + 128 <= TM_COLS && TM_QT + 128 <= TM_COLS, "tensor memory budget");
     static_assert(D == 64 || D == 96 || D == 128, "head dim");
 };
 
@@ -585,11 +593,11 @@ __global__ void __launch_bounds__(640, 1)
             for (int i = 0; ok && i < n_it; ++i) {
                 const int it = gb + i;  // the block's running index
                 const int qs = it % QS, os = it % OS;
-                // 1. dP^T(it) into Y once dQ^T(it - 1) has been read out of it
+                // 1. dP^T(it) into Y once dQ^T(it - 1) has been read out of it (shared Y)
                 if (i == 0 && !(ok = mbar_wait_warp<true>(bar_v_full, ri & 1, g, SITE_BWD_MMA_KV))) break;
                 if (!(ok = mbar_wait_warp<true>(bar_o_full + 8 * os, (it / OS) & 1, g, SITE_BWD_MMA_Q_FULL)))
                     break;
-                if (it > 0 &&
+                if (!T::SEPQ && it > 0 &&
                     !(ok = mbar_wait_warp<true>(bar_dq_empty, (it - 1) & 1, g, SITE_BWD_MMA_DQ_FREE)))
                     break;
                 tc_fence_after();
@@ -622,10 +630,18 @@ __global__ void __launch_bounds__(640, 1)
                 tc_fence_after();
                 issue_acc(T::TM_DK, T::TM_Y, sQ + qs * T::Q_BYTES, i == 0);
                 tc_commit_elect(bar_q_empty + 8 * qs);
-                // 5. dQ^T(it)[d][q] = sum_k K[k][d] dS^T[k][q] into Y (K = 128 keys, 16 per step)
+                // 5. dQ^T(it)[d][q] = sum_k K[k][d] dS^T[k][q] into Y, or Z once dQ^T(it - 1)
+                //    has been read out of it (K = 128 keys, 16 per step).  The next dP^T is
+                //    issued after it, so the tensor pipe, in order, has read the dS^T tile
+                //    before the P/dS warps (waiting for that dP^T) overwrite it.
+                if (T::SEPQ && it > 0) {
+                    if (!(ok = mbar_wait_warp<true>(bar_dq_empty, (it - 1) & 1, g, SITE_BWD_MMA_DQ_FREE)))
+                        break;
+                    tc_fence_after();
+                }
 #pragma unroll
                 for (int ks = 0; ks < T::BN / 16; ++ks)
-                    mma_ss_elect(tmem + T::TM_Y, desc_add(dK_mn, ks * 2048), desc_add(dDS, ks * 2048),
+                    mma_ss_elect(tmem + T::TM_QT, desc_add(dK_mn, ks * 2048), desc_add(dDS, ks * 2048),
                                  kIdescDQ, ks > 0 ? 1u : 0u);
                 tc_commit_elect(bar_dq_full);
             }
@@ -877,8 +893,8 @@ __global__ void __launch_bounds__(640, 1)
                         epilogue(itm);
                     }
                     uint32_t x0[32], x1[32];
-                    tmem_ld32(tmem + lane_base + T::TM_Y + 64 * h, x0);
-                    tmem_ld32(tmem + lane_base + T::TM_Y + 64 * h + 32, x1);
+                    tmem_ld32(tmem + lane_base + T::TM_QT + 64 * h, x0);
+                    tmem_ld32(tmem + lane_base + T::TM_QT + 64 * h + 32, x1);
                     tmem_wait_ld(x0);
                     tmem_wait_ld(x1);
                     tc_fence_before();
