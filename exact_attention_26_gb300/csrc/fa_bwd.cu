@@ -62,7 +62,8 @@ __global__ void __launch_bounds__(256)
                       const float *__restrict__ lse, float *__restrict__ delta,
                       float *__restrict__ lse2, float *__restrict__ dq, int N, int Npad, int BH,
                       int H, const int *__restrict__ cu_seqlens, int total_tokens,
-                      int *__restrict__ item_counter) {
+                      int *__restrict__ item_counter, float *__restrict__ zero_k,
+                      float *__restrict__ zero_v, long long kv_elems) {
     // A warp takes RPW consecutive rows at a time (Npad is a multiple of 128, so they
     // share a head) and issues all their loads before any arithmetic: the kernel is
     // bound by HBM, and one row of O and dO per warp leaves too few bytes in flight.
@@ -70,6 +71,12 @@ __global__ void __launch_bounds__(256)
     constexpr int PER = D / 32;  // elements per lane
     griddep_launch_dependents();  // the main kernel may set up while this one runs
     if (blockIdx.x == 0 && threadIdx.x == 0) *item_counter = 0;  // the main kernel's items
+    // split key blocks: dK and dV := 0 (both parts of a key block add into them)
+    for (long long e = ((long long)blockIdx.x * blockDim.x + threadIdx.x) * 4; e < kv_elems;
+         e += (long long)gridDim.x * blockDim.x * 4) {
+        *reinterpret_cast<float4 *>(zero_k + e) = make_float4(0.f, 0.f, 0.f, 0.f);
+        *reinterpret_cast<float4 *>(zero_v + e) = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
     constexpr int W = PER == 3 ? 3 : PER / 2;  // loaded words: bf16 pairs, or 3 halves at d = 96
     const int lane = threadIdx.x & 31;
     const long long warp0 = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -842,6 +849,8 @@ __global__ void __launch_bounds__(640, 1)
                 ok = ok && mbar_wait_warp<true>(bar_dq_full, (gb + n_it - 1) & 1, g, SITE_BWD_EPILOGUE);
                 if (!ok) break;
                 tc_fence_after();
+                // split: dV adds into the zeros the preprocess kernel wrote
+                if constexpr (SPLIT) griddep_wait();
                 epilogue(itm);
                 gb += n_it;
             }
@@ -930,20 +939,17 @@ int launch_bwd_t(const BwdParams &p, cudaStream_t stream) {
     using W = BwdTile<D>;
     long long grid = (long long)((p.N + W::BN - 1) / W::BN) * (p.BH / p.group);
     // Small grids (single sequences with few heads; fixed layout): two CTAs per key
-    // block, each over half of its query blocks, adding dK and dV into outputs
-    // zeroed here, stream-ordered ahead of the preprocess kernel (so the main kernel
-    // stays a programmatic dependent of the preprocess).  Causal: whenever the grid
+    // block, each over half of its query blocks, adding dK and dV into outputs the
+    // preprocess kernel zeroes (the main kernel waits for it before its first add).
+    // Zeroing there instead of two memsets ahead of it saves two launches on these
+    // latency-bound shapes.  Causal: whenever the grid
     // is under one wave, since halving the longest key blocks shortens the critical
     // path; non-causal: only when the doubled grid still fits one wave (the CTAs are
     // all equally long, and a second wave of halves costs as much as the whole).
     const bool split = !VARLEN && (CAUSAL ? grid < p.num_sms : 2 * grid <= p.num_sms);
-    if (split) {
-        grid *= 2;
-        const size_t kv_bytes = (size_t)(p.BH / p.group) * p.N * D * sizeof(float);
-        if (cudaMemsetAsync(p.dk, 0, kv_bytes, stream) != cudaSuccess ||
-            cudaMemsetAsync(p.dv, 0, kv_bytes, stream) != cudaSuccess)
-            return FA_ERR_CUDA;
-    }
+    // split: the preprocess kernel zeroes dK and dV (elements, a multiple of 4)
+    const long long kv_elems = split ? (long long)(p.BH / p.group) * p.N * D : 0;
+    if (split) grid *= 2;
     {
         const long long rows = (long long)p.BH * p.Npad;
         long long blocks = (rows / 4 * 32 + 255) / 256;  // a warp per group of four rows
@@ -953,7 +959,8 @@ int launch_bwd_t(const BwdParams &p, cudaStream_t stream) {
         fa_bwd_pre_kernel<D, VARLEN><<<(unsigned)blocks, 256, 0, stream>>>(
             reinterpret_cast<const __nv_bfloat16 *>(p.o),
             reinterpret_cast<const __nv_bfloat16 *>(p.dout), p.lse, p.ws_delta, p.ws_lse2, p.dq,
-            p.N, p.Npad, p.BH, p.H, p.cu_seqlens, p.total_tokens, p.ws_counter);
+            p.N, p.Npad, p.BH, p.H, p.cu_seqlens, p.total_tokens, p.ws_counter, p.dk, p.dv,
+            kv_elems);
         if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
     }
 
