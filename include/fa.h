@@ -131,11 +131,12 @@ int fa_bwd_gqa(const void *q, const void *k, const void *v, const void *o, const
  * FlashDecoding").  Same definition, layouts, results and errors as fa_fwd_gqa.
  *   kv_chunk    : 0 lets the library choose: it cuts key ranges only when one
  *                 query tile per CTA would leave SMs idle or wait on the longest
- *                 rows (few heads, long causal sequences), into chunks of about
- *                 twice the launch's work per SM; > 0 asks for chunks of about
- *                 kv_chunk keys (rounded up to the keys of a 128-row block's
- *                 diagonal: 128, or 64 at d = 256, times one).  < 0:
- *                 FA_ERR_INVALID_ARG.
+ *                 rows (few heads, long sequences), preferably by the balanced
+ *                 plan fa_fwd_split_segments reports (segments of uneven length
+ *                 that give every CTA about the same work), else into even
+ *                 chunks; > 0 asks for even chunks of about kv_chunk keys
+ *                 (rounded up to the keys of a 128-row block's diagonal: 128, or
+ *                 64 at d = 256, times one).  < 0: FA_ERR_INVALID_ARG.
  *   workspace   : device buffer of at least fa_fwd_workspace_bytes(B, H, N, d,
  *                 causal, kv_chunk) bytes, 256-byte aligned (FA_ERR_MISALIGNED),
  *                 owned by the caller, contents on entry irrelevant; may be NULL
