@@ -242,8 +242,8 @@ struct BwdTile {
     static constexpr uint32_t OFF_BAR = OFF_DELTA + QS * VEC_BYTES;
     // k_full, q_full[QS], q_empty[QS], o_full[OS], o_empty[OS], s_full, p_full,
     // dp_full, ds_full, dq_full, dq_empty, done, v_full, kv_empty, dv_free, dk_free,
-    // item[2]
-    static constexpr int NBAR = 1 + 2 * QS + 2 * OS + 13;
+    // item[2], item_read[2]
+    static constexpr int NBAR = 1 + 2 * QS + 2 * OS + 15;
     static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;  // TMEM base, abort flag, item[2]
     static constexpr uint32_t SMEM_USED = OFF_MISC + 16;
     // The tiles need 1024-byte alignment (128-byte swizzle atoms).  At d = 128 the
@@ -315,6 +315,7 @@ __global__ void __launch_bounds__(640, 1)
     const uint32_t bar_dv_free = bar_s_full + 72;   // the epilogue has read dV from TMEM
     const uint32_t bar_dk_free = bar_s_full + 80;   // ... dK
     const uint32_t bar_item = bar_s_full + 88;      // [2] the next item is published
+    const uint32_t bar_item_read = bar_s_full + 104; // [2] every reading warp has read it
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + T::OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(gbase + T::OFF_MISC + 4);
     volatile int *item_slot = reinterpret_cast<volatile int *>(gbase + T::OFF_MISC + 8);  // [2]
@@ -431,6 +432,9 @@ __global__ void __launch_bounds__(640, 1)
         mbar_init(bar_dk_free, 256);
         mbar_init(bar_item, 1);
         mbar_init(bar_item + 8, 1);
+        // readers: the MMA warp, the 8 P/dS warps and the 8 dQ warps, one arrival each
+        mbar_init(bar_item_read, 17);
+        mbar_init(bar_item_read + 8, 17);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -450,13 +454,15 @@ __global__ void __launch_bounds__(640, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const Guard g{status, abort_flag, limit_ns};
-    // Item ri of this CTA (a running count): its number, or -1 after the last.  The
-    // entry of ri - 2 is free when the TMA warp overwrites it: every role has begun
-    // item ri - 1 by then (the TMA warp waited for the end of ri - 2's products and
-    // epilogue before loading ri - 1).
+    // Item ri of this CTA (a running count): its number, or -1 after the last.  Each
+    // reading warp marks the entry read (item_read), and the TMA warp rewrites the
+    // entry of ri - 2 with ri only after all 17 have: no other chain orders the dQ
+    // warps' read of an item with one block before the TMA warp runs two items on.
     auto next_item = [&](int ri, int &w) -> bool {
         if (!mbar_wait_warp<true>(bar_item + 8 * (ri & 1), (ri >> 1) & 1, g, SITE_BWD_ITEM)) return false;
         w = item_slot[ri & 1];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_item_read + 8 * (ri & 1));
         return true;
     };
     // Each role rebalances its registers first thing in its own branch, so that the
@@ -484,6 +490,10 @@ __global__ void __launch_bounds__(640, 1)
             };
             for (int ri = 0; ok; ) {
                 const int w = claim(ri);
+                // the entry's previous item (ri - 2) has been read by every role
+                if (ri >= 2 && !(ok = mbar_wait<true>(bar_item_read + 8 * (ri & 1), ((ri - 2) >> 1) & 1, g,
+                                                      SITE_BWD_ITEM)))
+                    break;
                 item_slot[ri & 1] = w;
                 mbar_arrive(bar_item + 8 * (ri & 1));
                 if (w < 0) break;
