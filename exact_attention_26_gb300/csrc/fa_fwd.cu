@@ -1152,61 +1152,89 @@ int fwd_split_chunk_t(int BH, int N, int causal, int num_sms, int forced) {
     return chunk;
 }
 
-// Balanced plan: the row blocks of all heads, longest first, laid end to end and
-// cut into segments so that each CTA's run of consecutive segments stays within
-// `cap` steps (its tiles plus kItemCost per segment); no piece shorter than
-// `min_seg` tiles is cut off a row block unless the CTA is otherwise empty.  Fills
-// `out` (when given) and returns the CTAs used, or 0 when more than G CTAs, kSegMax
-// segments or kSegMaxParts segments of one row block would be needed.
+// Balanced plan within a cap of `cap` steps per CTA (a segment costs its tiles plus
+// kItemCost).  First the row blocks too long for one CTA's budget, longest first,
+// are laid end to end from CTA 0 and cut where a CTA is full; no piece shorter than
+// `min_seg` tiles is cut off unless the CTA is otherwise empty.  Then every other
+// row block goes whole, longest first, to the CTA with the least room that still
+// holds it, so only the long row blocks leave partials to merge.  Fills `out` (when
+// given) and returns the CTAs used, or 0 when more than G CTAs, kSegMax segments or
+// kSegMaxParts parts of one row block would be needed.
 struct SegRow {
     int bh, cb;
     long long nk;
 };
+
 int seg_fill(const std::vector<SegRow> &rows, int n_cb, long long cap, long long min_seg, int G,
              FwdSegPlan *out) {
     const long long ic = (long long)kItemCost;
-    int cta = 0, n = 0, s_max = 0;
-    long long load = 0, worst = 0;
-    if (out) out->tab.start[0] = 0;
-    for (const SegRow &row : rows) {
-        long long rem = row.nk, kv = 0;
+    struct Piece {
+        int row, part;
+        long long kv, n;
+    };
+    std::vector<std::vector<Piece>> per((size_t)G);
+    std::vector<long long> load((size_t)G, 0);
+    std::vector<int> parts_of(rows.size(), 1);
+    int n = 0, cta = 0;
+    for (size_t r = 0; r < rows.size(); ++r) {  // long row blocks, cut
+        if (rows[r].nk + ic <= cap) continue;
+        long long rem = rows[r].nk, kv = 0;
         int parts = 0;
-        const int first = n;
         while (rem > 0) {
-            const long long avail = cap - load - ic;
+            if (cta >= G) return 0;
+            const long long avail = cap - load[cta] - ic;
             long long take;
             if (rem <= avail) {
                 take = rem;
             } else {
                 take = rem - avail < min_seg ? rem - min_seg : avail;
-                if (take < min_seg) take = load == 0 ? std::min(rem, std::max(avail, 1LL)) : 0;
+                if (take < min_seg) take = load[cta] == 0 ? std::min(rem, std::max(avail, 1LL)) : 0;
             }
             if (take > 0) {
                 if (n >= kSegMax || parts >= kSegMaxParts) return 0;
-                if (out) {
-                    out->tab.seg[n][0] = (uint32_t)row.bh | ((uint32_t)row.cb << 16);
-                    out->tab.seg[n][1] = (uint32_t)kv | ((uint32_t)take << 12) | ((uint32_t)parts << 24);
-                }
+                per[cta].push_back({(int)r, parts, kv, take});
                 ++n;
                 ++parts;
                 kv += take;
                 rem -= take;
-                load += take + ic;
-                worst = std::max(worst, load);
+                load[cta] += take + ic;
             }
-            if (rem > 0) {  // the CTA is full: the rest of the row block goes to the next
-                if (++cta >= G) return 0;
-                if (out) out->tab.start[cta] = (uint16_t)n;
-                load = 0;
-            }
+            if (rem > 0) ++cta;  // the CTA is full: the rest goes to the next
         }
-        if (out) {
-            for (int i = first; i < n; ++i) out->tab.seg[i][1] |= (uint32_t)parts << 28;
-            out->mns.ns[row.bh * n_cb + row.cb] = (uint8_t)parts;
-        }
-        s_max = std::max(s_max, parts);
+        parts_of[r] = parts;
     }
-    const int used = load > 0 ? cta + 1 : cta;
+    for (size_t r = 0; r < rows.size(); ++r) {  // the others, whole, best fit
+        const long long need = rows[r].nk + ic;
+        if (need > cap) continue;
+        int best = -1;
+        for (int c = 0; c < G; ++c)
+            if (cap - load[c] >= need && (best < 0 || load[c] > load[best])) best = c;
+        if (best < 0 || n >= kSegMax) return 0;
+        per[best].push_back({(int)r, 0, 0, rows[r].nk});
+        ++n;
+        load[best] += need;
+    }
+    int used = 0, s_max = 1, k = 0;
+    long long worst = 0;
+    for (int c = 0; c < G; ++c) {
+        if (per[c].empty()) continue;
+        if (out) {
+            out->tab.start[used] = (uint16_t)k;
+            for (const Piece &pc : per[c]) {
+                const SegRow &row = rows[pc.row];
+                out->tab.seg[k][0] = (uint32_t)row.bh | ((uint32_t)row.cb << 16);
+                out->tab.seg[k][1] = (uint32_t)pc.kv | ((uint32_t)pc.n << 12) | ((uint32_t)pc.part << 24) |
+                                     ((uint32_t)parts_of[pc.row] << 28);
+                ++k;
+            }
+        }
+        worst = std::max(worst, load[c]);
+        ++used;
+    }
+    for (size_t r = 0; r < rows.size(); ++r) {
+        s_max = std::max(s_max, parts_of[r]);
+        if (out) out->mns.ns[rows[r].bh * n_cb + rows[r].cb] = (uint8_t)parts_of[r];
+    }
     if (out) {
         out->tab.n_cta = used;
         out->tab.start[used] = (uint16_t)n;
