@@ -149,11 +149,12 @@ size_t fa_fwd_workspace_bytes(int B, int H, int N, int d, int causal, int kv_chu
 
 /*
  * The balanced cut fa_fwd_ws makes with kv_chunk = 0 on a device of num_sms SMs, for
- * inspection (host only: nothing is launched and no device is needed).  The row
- * blocks of 128 query rows of all B*H heads, longest first, are laid end to end and
- * cut into segments so that every CTA's run of consecutive segments costs about the
- * same, counting a segment's K/V tiles plus a fixed cost of six tile steps (its Q
- * load, pipeline fill and epilogue); no row block is cut into more than 15 parts.
+ * inspection (host only: nothing is launched and no device is needed).  Every CTA
+ * gets about the same work, counting a segment's K/V tiles plus a fixed cost of six
+ * tile steps (its Q load, pipeline fill and epilogue): the row blocks of 128 query
+ * rows longer than that budget (all B*H heads, longest first) are laid end to end
+ * and cut where a CTA is full, into at most 15 parts; the other row blocks go whole
+ * to the fullest CTA that still holds them.
  * The library uses this cut when its cost model predicts it at least 5% faster than
  * no cut and faster than even chunks, and otherwise cuts evenly or not at all.
  *   out : int[cap][7] host buffer, filled with the first cap segments in CTA order:
